@@ -1,0 +1,173 @@
+"""Per-vector TurboQuant_mse (values) and TurboQuant_prod (keys), and packing.
+
+TurboQuant_mse ([Reconstruction] §5 Steps 1-5):
+  1. norm separation: n = ||x||, u = x / n; n stored as float32 (§8 storage
+     formula: "Norm: 1 float32");
+  2. rotation: y = Pi u;
+  4./5. each coordinate is mapped to the index of its Lloyd-Max bucket; the
+     reconstruction is x_hat = n Pi^T c[idx].
+  Zero guard ([Reconstruction] §11 item 2, §13 reference logic): if
+  n < 1e-7 the record is a zero code with norm 0.
+  "RMS-scaled" (reading): the decision variable is z = sqrt(d) * y, compared
+  against the float32 boundaries of the RMS-scaled codebook; ties go up,
+  idx_j = #{i : z_j >= t_i}.
+
+TurboQuant_prod for keys ([Reconstruction] §6 "The Residual and
+Bit-Splitting", "The 1-Bit QJL Transform", "The Asymmetric Unbiased
+Estimator"): a (b-1)-bit MSE code, the residual r, its norm gamma = ||r||
+stored as float32, and the sign sketch sign(S r) with S d x d i.i.d. N(0,1).
+Reading: the residual is taken in the rotated basis, r = y - y_hat with
+y_hat = c[idx] / sqrt(d); <q, r_original> = <Pi q, r> for orthogonal Pi, and
+S Pi^T is again an i.i.d. Gaussian matrix, so the estimator's law is the one
+stated on the page.  sign(0) = +1.  For a zero vector gamma = 0 and all sign
+bits are +1.
+
+Packing (reading; [README] §How It Works packs nibbles, [Design study]
+§Packed format asks for a bit-packed code stream): sign-magnitude bit planes.
+Per vector and b-bit code: plane 0 holds the sign side (bit = 1 iff
+idx >= 2^(b-1)); planes 1..b-1 hold the magnitude m (LSB first), where
+m = idx - 2^(b-1) on the non-negative side and m = 2^(b-1) - 1 - idx on the
+negative side.  Coordinate j sits at bit (j mod 32) of 32-bit word j // 32.
+The QJL sketch is one plane, bit = 1 iff (S r)_j >= 0.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import transforms as T
+from .codebook import Codebook
+
+ZERO_NORM = 1e-7
+
+
+def qjl_constant(d: int) -> float:
+    """sqrt(pi/2) / d: the QJL estimator constant for m = d sketch rows."""
+    return math.sqrt(math.pi / 2.0) / d
+
+
+def bucketize(z: np.ndarray, boundaries: np.ndarray) -> np.ndarray:
+    """idx = #{i : z >= t_i} in float64 against the float32 boundaries."""
+    t = np.asarray(boundaries, dtype=np.float32).astype(np.float64)
+    return (z[..., None] >= t).sum(axis=-1).astype(np.int64)
+
+
+def boundary_margin(z: np.ndarray, boundaries: np.ndarray) -> np.ndarray:
+    t = np.asarray(boundaries, dtype=np.float32).astype(np.float64)
+    return np.min(np.abs(z[..., None] - t), axis=-1)
+
+
+def quantize_mse(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook) -> dict:
+    """TurboQuant_mse of the rows of x ([N, d]); everything in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    n = np.sqrt(np.sum(x * x, axis=-1))
+    zero = n < ZERO_NORM
+    u = np.where(zero[:, None], 0.0, x / np.where(zero, 1.0, n)[:, None])
+    y = T.rotate(kind, rot, u)
+    z = math.sqrt(d) * y
+    idx = bucketize(z, cb.boundaries)
+    yhat = np.asarray(cb.centroids, dtype=np.float32).astype(np.float64)[idx] / math.sqrt(d)
+    norm32 = np.where(zero, 0.0, n).astype(np.float32)
+    return {"norm": norm32, "norm_f64": np.where(zero, 0.0, n), "idx": idx, "y": y, "z": z,
+            "yhat": yhat, "zero": zero, "margin": boundary_margin(z, cb.boundaries)}
+
+
+def quantize_prod(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, S: np.ndarray) -> dict:
+    """TurboQuant_prod of the rows of x: MSE code + residual norm + QJL signs."""
+    rec = quantize_mse(x, kind, rot, cb)
+    r = rec["y"] - rec["yhat"]
+    gamma = np.sqrt(np.sum(r * r, axis=-1))
+    Sr = sketch(r, S)
+    signs = Sr >= 0.0
+    zero = rec["zero"]
+    gamma = np.where(zero, 0.0, gamma)
+    signs[zero] = True
+    rec.update({"r": r, "rnorm": gamma.astype(np.float32), "rnorm_f64": gamma, "signs": signs,
+                "Sr": Sr, "sign_margin": np.where(zero[:, None], np.inf, np.abs(Sr))})
+    return rec
+
+
+# ----------------------------------------------------------------------------- packing
+
+def code_planes(idx: np.ndarray, bits: int) -> np.ndarray:
+    """Sign-magnitude planes as 0/1 arrays: [..., bits, d]."""
+    half = 1 << (bits - 1)
+    pos = idx >= half
+    mag = np.where(pos, idx - half, half - 1 - idx)
+    planes = [pos.astype(np.uint8)]
+    for k in range(bits - 1):
+        planes.append(((mag >> k) & 1).astype(np.uint8))
+    return np.stack(planes, axis=-2)
+
+
+def planes_to_idx(planes: np.ndarray) -> np.ndarray:
+    bits = planes.shape[-2]
+    half = 1 << (bits - 1)
+    mag = np.zeros(planes.shape[:-2] + planes.shape[-1:], dtype=np.int64)
+    for k in range(bits - 1):
+        mag |= planes[..., k + 1, :].astype(np.int64) << k
+    pos = planes[..., 0, :].astype(bool)
+    return np.where(pos, half + mag, half - 1 - mag)
+
+
+def pack_bits(b: np.ndarray) -> np.ndarray:
+    """0/1 array [..., d] -> uint32 words [..., d // 32], coordinate j at bit j % 32."""
+    d = b.shape[-1]
+    if d % 32:
+        raise ValueError("d must be a multiple of 32")
+    w = b.reshape(b.shape[:-1] + (d // 32, 32)).astype(np.uint64)
+    return (w << np.arange(32, dtype=np.uint64)).sum(axis=-1).astype(np.uint32)
+
+
+def unpack_bits(w: np.ndarray, d: int) -> np.ndarray:
+    w = np.asarray(w, dtype=np.uint64)[..., None]
+    b = (w >> np.arange(32, dtype=np.uint64)) & np.uint64(1)
+    return b.reshape(w.shape[:-2] + (d,)).astype(np.uint8)
+
+
+def pack_codes(idx: np.ndarray, bits: int) -> np.ndarray:
+    """[N, d] code indices -> uint32 [N, bits, d // 32]."""
+    return pack_bits(code_planes(idx, bits))
+
+
+def unpack_codes(words: np.ndarray, bits: int, d: int) -> np.ndarray:
+    return planes_to_idx(unpack_bits(words, d))
+
+
+# ----------------------------------------------------------------------------- reconstruction
+
+def dequantize_mse(norm: np.ndarray, idx: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook) -> np.ndarray:
+    """x_hat = n Pi^T c[idx] / sqrt(d)  ([Reconstruction] §5 Step 5)."""
+    d = idx.shape[-1]
+    yhat = np.asarray(cb.centroids, dtype=np.float32).astype(np.float64)[idx] / math.sqrt(d)
+    return np.asarray(norm, dtype=np.float64)[:, None] * T.rotate_inverse(kind, rot, yhat)
+
+
+def dequantize_prod(norm, rnorm, idx, signs, kind, rot, cb, S) -> np.ndarray:
+    """Explicit key the estimator is an inner product with:
+    k_hat = n Pi^T (y_hat + sqrt(pi/2)/d * gamma * S^T (2 s - 1))."""
+    d = idx.shape[-1]
+    yhat = np.asarray(cb.centroids, dtype=np.float32).astype(np.float64)[idx] / math.sqrt(d)
+    pm = np.where(np.asarray(signs, dtype=bool), 1.0, -1.0)
+    corr = pm @ np.asarray(S, dtype=np.float32).astype(np.float64)
+    ytil = yhat + qjl_constant(d) * np.asarray(rnorm, dtype=np.float64)[:, None] * corr
+    return np.asarray(norm, dtype=np.float64)[:, None] * T.rotate_inverse(kind, rot, ytil)
+
+
+def sketch(v: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """S v for v [..., d] and S [..., d, d] (broadcast), float64."""
+    S = np.asarray(S)
+    S = S.astype(np.float64) if S.dtype != np.float64 else S
+    return np.matmul(S, np.asarray(v, dtype=np.float64)[..., None])[..., 0]
+
+
+def qjl_estimate(q: np.ndarray, r_norm, signs: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """Residual inner-product estimate sqrt(pi/2)/d * ||r|| * <S q, sign(S r)>
+    ([Reconstruction] §6 "The Asymmetric Unbiased Estimator"); broadcasts
+    over leading axes of S / signs."""
+    d = q.shape[-1]
+    pm = np.where(np.asarray(signs, dtype=bool), 1.0, -1.0)
+    return qjl_constant(d) * np.asarray(r_norm, dtype=np.float64) * np.sum(sketch(q, S) * pm, axis=-1)
