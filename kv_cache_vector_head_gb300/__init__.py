@@ -1,0 +1,133 @@
+"""TurboQuant KV-cache hot path for NVIDIA GB300 (sm_103a).
+
+Python side of the C ABI in ``include/tq.h``: ``_lib`` marshals arguments to
+libtq.so; the classes below only allocate device memory (PyTorch) and fill
+the ctypes structures.  Every step of quantization, paging and decode runs in
+libtq's CUDA kernels; if libtq.so is missing, importing the binding's functions
+raises.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import _lib
+from ._lib import (PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
+                   Cache, LayerParams, TQError, append_page, build_codebook, build_transform, check_device_error,
+                   decode_attention, decode_workspace_size, quantize_keys, quantize_values, subblock_bytes)
+
+__all__ = [
+    "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
+    "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
+    "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
+    "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL",
+]
+
+
+def n_compressed(T: int, window: int) -> int:
+    """Compressed tokens at length T: 16 * floor(max(0, T - W) / 16)."""
+    return PAGE_SIZE * (max(0, T - window) // PAGE_SIZE)
+
+
+class TQLayer:
+    """Codebooks, per-head transforms (device) and the tq_layer_params of one layer."""
+
+    def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
+                 window: int = 0, key_qjl: bool = True, seed: int = 0, layer: int = 0, device="cuda"):
+        import torch
+
+        self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
+        self.key_bits, self.value_bits, self.kind, self.window = key_bits, value_bits, kind, window
+        self.key_qjl, self.seed, self.layer = bool(key_qjl), seed, layer
+        self.k_cb = build_codebook(d, key_bits)
+        self.v_cb = build_codebook(d, value_bits)
+        kr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_KEY_ROT) for h in range(n_kv_heads)])
+        vr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_VALUE_ROT) for h in range(n_kv_heads)])
+        self.k_rot_host, self.v_rot_host = kr, vr
+        self.k_rot = torch.from_numpy(kr).to(device)
+        self.v_rot = torch.from_numpy(vr).to(device)
+        if key_qjl:
+            s = np.stack([build_transform(kind, d, seed, layer, h, ROLE_QJL) for h in range(n_kv_heads)])
+            self.qjl_s_host = s
+            self.qjl_s = torch.from_numpy(s).to(device)
+        else:
+            self.qjl_s_host, self.qjl_s = None, None
+        p = LayerParams()
+        p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = d, n_kv_heads, n_q_heads, PAGE_SIZE, window
+        p.key_bits, p.key_qjl, p.value_bits, p.kind = key_bits, int(key_qjl), value_bits, kind
+        p.k_rot, p.v_rot = self.k_rot.data_ptr(), self.v_rot.data_ptr()
+        p.qjl_s = self.qjl_s.data_ptr() if key_qjl else None
+        for name, (c, t, _) in (("k", self.k_cb), ("v", self.v_cb)):
+            getattr(p, f"{name}_centroids")[: len(c)] = [float(x) for x in c]
+            getattr(p, f"{name}_bounds")[: len(t)] = [float(x) for x in t]
+        self.params = p
+        self.sub_bytes = subblock_bytes(p)
+
+
+class PagedCache:
+    """Device buffers of one layer's paged cache and its tq_cache descriptor.
+
+    Pages are handed out contiguously: sequence b owns pages
+    [b * max_pages_per_seq, (b + 1) * max_pages_per_seq).
+    """
+
+    def __init__(self, layer: TQLayer, batch: int, max_ctx: int, device="cuda", pool_pages: int | None = None):
+        import torch
+
+        self.layer, self.batch = layer, batch
+        self.max_pages = max(1, math.ceil(max_ctx / PAGE_SIZE))
+        n_pages = pool_pages if pool_pages is not None else batch * self.max_pages
+        self.pool = torch.zeros(n_pages * layer.n_kv_heads * layer.sub_bytes, dtype=torch.uint8, device=device)
+        bt = torch.arange(batch * self.max_pages, dtype=torch.int32, device=device).reshape(batch, self.max_pages)
+        self.block_table = bt % n_pages
+        self.seq_len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.n_compressed = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.ring = layer.window + PAGE_SIZE if layer.window > 0 else 0
+        if self.ring:
+            shape = (batch, layer.n_kv_heads, self.ring, layer.d)
+            self.win_k = torch.zeros(shape, dtype=torch.float16, device=device)
+            self.win_v = torch.zeros(shape, dtype=torch.float16, device=device)
+        else:
+            self.win_k = self.win_v = None
+        c = Cache()
+        c.page_pool, c.n_pages = self.pool.data_ptr(), n_pages
+        c.block_table, c.max_pages_per_seq = self.block_table.data_ptr(), self.max_pages
+        c.seq_len, c.n_compressed = self.seq_len.data_ptr(), self.n_compressed.data_ptr()
+        c.win_k = self.win_k.data_ptr() if self.win_k is not None else None
+        c.win_v = self.win_v.data_ptr() if self.win_v is not None else None
+        c.batch = batch
+        self.cache = c
+        self.n_pages = n_pages
+
+    def slot_mapping(self, T: int):
+        """Pool slots (page * 16 + slot) of token positions 0..T-1 of every sequence, [batch * T]."""
+        import torch
+
+        pos = torch.arange(T, device=self.block_table.device)
+        pages = self.block_table[:, pos // PAGE_SIZE].to(torch.int64)
+        return (pages * PAGE_SIZE + (pos % PAGE_SIZE)[None, :]).reshape(-1)
+
+    def prefill(self, k, v, stream=None) -> None:
+        """Fill every sequence with T tokens: k, v [batch, T, Hkv, d].
+
+        Tokens 0..n_c-1 are quantized straight into their pages (direct
+        slots); the remaining T - n_c (< W + 16) go through decode-step
+        appends into the float16 window, exactly as live decoding would.
+        """
+        B, T = k.shape[0], k.shape[1]
+        nc = n_compressed(T, self.layer.window)
+        self.seq_len.fill_(nc)
+        self.n_compressed.fill_(nc)
+        if nc:
+            slots = self.slot_mapping(nc)
+            kk = k[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.d).contiguous()
+            vv = v[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.d).contiguous()
+            append_page(self.layer.params, self.cache, kk, vv, B * nc, slots, stream)
+        for t in range(nc, T):
+            append_page(self.layer.params, self.cache, k[:, t].contiguous(), v[:, t].contiguous(), B, None, stream)
+
+    def append(self, k, v, stream=None) -> None:
+        """One decode step: k, v [batch, Hkv, d]."""
+        append_page(self.layer.params, self.cache, k, v, self.batch, None, stream)

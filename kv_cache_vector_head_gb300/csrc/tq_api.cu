@@ -1,0 +1,230 @@
+// C ABI entry points of libtq: argument checks on the host, then launches.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "tq_internal.h"
+#include "tq_launch.h"
+
+namespace tq {
+
+static thread_local char g_msg[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+void clear_error() { g_msg[0] = '\0'; }
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int num_sms() {
+  static int cached = -1;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached < 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached = n;
+    else
+      cached = 148;
+  }
+  return cached;
+}
+
+// Checks the layer parameters and fills the kernel-side copy.
+static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_device_ptrs) {
+  if (!p) return fail(TQ_ERR_INVALID_ARG, "null tq_layer_params");
+  if (p->d != 128 && p->d != 256) return fail(TQ_ERR_UNSUPPORTED, "d must be 128 or 256");
+  if (p->n_kv_heads < 1 || p->n_q_heads < p->n_kv_heads || p->n_q_heads % p->n_kv_heads)
+    return fail(TQ_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (p->n_q_heads / p->n_kv_heads > TQ_MAX_GQA) return fail(TQ_ERR_UNSUPPORTED, "n_q_heads / n_kv_heads must be <= 8");
+  if (p->page_size != TQ_PAGE_SIZE) return fail(TQ_ERR_UNSUPPORTED, "page_size must be 16");
+  if (p->window < 0) return fail(TQ_ERR_INVALID_ARG, "window must be >= 0");
+  if (p->key_bits < 1 || p->key_bits > TQ_MAX_BITS || p->value_bits < 1 || p->value_bits > TQ_MAX_BITS)
+    return fail(TQ_ERR_UNSUPPORTED, "key_bits and value_bits must be 1..4");
+  if (p->key_qjl != 0 && p->key_qjl != 1) return fail(TQ_ERR_INVALID_ARG, "key_qjl must be 0 or 1");
+  if (p->kind != TQ_DENSE && p->kind != TQ_FWHT) return fail(TQ_ERR_INVALID_ARG, "bad transform kind");
+  if (need_device_ptrs) {
+    if (!p->k_rot || !p->v_rot) return fail(TQ_ERR_INVALID_ARG, "null k_rot / v_rot");
+    if (p->key_qjl && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
+    if (!aligned(p->k_rot, 16) || !aligned(p->v_rot, 16) || (p->qjl_s && !aligned(p->qjl_s, 16)))
+      return fail(TQ_ERR_INVALID_ARG, "transforms must be 16-byte aligned");
+  }
+  K->d = p->d;
+  K->hkv = p->n_kv_heads;
+  K->hq = p->n_q_heads;
+  K->G = p->n_q_heads / p->n_kv_heads;
+  K->window = p->window;
+  K->kb = p->key_bits;
+  K->kqjl = p->key_qjl;
+  K->vb = p->value_bits;
+  K->kind = p->kind;
+  K->k_rot = p->k_rot;
+  K->v_rot = p->v_rot;
+  K->qjl_s = p->qjl_s;
+  for (int i = 0; i < 16; ++i) {
+    K->kc[i] = p->k_centroids[i];
+    K->kt[i] = p->k_bounds[i];
+    K->vc[i] = p->v_centroids[i];
+    K->vt[i] = p->v_bounds[i];
+  }
+  const int d = p->d, w = d / 32, P = TQ_PAGE_SIZE;
+  int o = 0;
+  K->off_knorm = o; o += 4 * P;
+  K->off_krnorm = o; o += p->key_qjl ? 4 * P : 0;
+  K->off_kcodes = o; o += 4 * p->key_bits * P * w;
+  K->off_ksigns = o; o += p->key_qjl ? 4 * P * w : 0;
+  K->off_vnorm = o; o += 4 * P;
+  K->off_vcodes = o; o += 2 * p->value_bits * d;
+  K->sub_bytes = o;
+  return TQ_OK;
+}
+
+static tq_status check_dtype(tq_dtype dt) {
+  if (dt != TQ_F32 && dt != TQ_BF16 && dt != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
+  return TQ_OK;
+}
+
+static tq_status cuda_status(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return TQ_ERR_CUDA;
+  }
+  return ok();
+}
+
+static tq_status make_cache(const tq_cache* c, const KParams& K, KCache* C, bool need_window) {
+  if (!c) return fail(TQ_ERR_INVALID_ARG, "null tq_cache");
+  if (!c->page_pool || !aligned(c->page_pool, 16)) return fail(TQ_ERR_INVALID_ARG, "page_pool null or not 16-byte aligned");
+  if (c->n_pages < 1 || c->batch < 1 || c->max_pages_per_seq < 1)
+    return fail(TQ_ERR_INVALID_ARG, "n_pages, batch and max_pages_per_seq must be >= 1");
+  if (!c->block_table || !c->seq_len || !c->n_compressed) return fail(TQ_ERR_INVALID_ARG, "null block_table / counters");
+  if (need_window && K.window > 0 && (!c->win_k || !c->win_v))
+    return fail(TQ_ERR_INVALID_ARG, "window > 0 needs win_k and win_v");
+  C->pool = reinterpret_cast<unsigned char*>(c->page_pool);
+  C->n_pages = c->n_pages;
+  C->block_table = c->block_table;
+  C->max_pages = c->max_pages_per_seq;
+  C->seq_len = c->seq_len;
+  C->n_compressed = c->n_compressed;
+  C->win_k = reinterpret_cast<__half*>(c->win_k);
+  C->win_v = reinterpret_cast<__half*>(c->win_v);
+  C->batch = c->batch;
+  C->ring = K.window > 0 ? K.window + TQ_PAGE_SIZE : 0;
+  return TQ_OK;
+}
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" const char* tq_last_error(void) { return g_msg; }
+
+extern "C" size_t tq_subblock_bytes(const tq_layer_params* p) {
+  KParams K;
+  if (make_params(p, &K, false) != TQ_OK) return 0;
+  clear_error();
+  return (size_t)K.sub_bytes;
+}
+
+extern "C" tq_status tq_quantize_keys(const tq_layer_params* p, const void* k, tq_dtype dtype, int64_t n_vec,
+                                      uint32_t* code_planes, uint32_t* sign_planes, float* norms, float* rnorms,
+                                      tq_stream_t stream) {
+  KParams K;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if (n_vec < 0) return fail(TQ_ERR_INVALID_ARG, "n_vec < 0");
+  if (n_vec == 0) return ok();
+  if (!k || !code_planes || !norms) return fail(TQ_ERR_INVALID_ARG, "null input or output");
+  if (K.kqjl && (!sign_planes || !rnorms)) return fail(TQ_ERR_INVALID_ARG, "key_qjl needs sign_planes and rnorms");
+  if (!aligned(k, 16)) return fail(TQ_ERR_INVALID_ARG, "k must be 16-byte aligned");
+  return cuda_status(launch_quantize_flat(K, k, dtype, n_vec, true, code_planes, sign_planes, norms, rnorms,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     "tq_quantize_keys");
+}
+
+extern "C" tq_status tq_quantize_values(const tq_layer_params* p, const void* v, tq_dtype dtype, int64_t n_vec,
+                                        uint32_t* code_planes, float* norms, tq_stream_t stream) {
+  KParams K;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if (n_vec < 0) return fail(TQ_ERR_INVALID_ARG, "n_vec < 0");
+  if (n_vec == 0) return ok();
+  if (!v || !code_planes || !norms) return fail(TQ_ERR_INVALID_ARG, "null input or output");
+  if (!aligned(v, 16)) return fail(TQ_ERR_INVALID_ARG, "v must be 16-byte aligned");
+  return cuda_status(launch_quantize_flat(K, v, dtype, n_vec, false, code_planes, nullptr, norms, nullptr,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     "tq_quantize_values");
+}
+
+extern "C" tq_status tq_append_page(const tq_layer_params* p, tq_cache* cache, const void* k, const void* v,
+                                    tq_dtype dtype, int64_t n_tok, const int64_t* slot_mapping, tq_stream_t stream) {
+  KParams K;
+  KCache C;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if ((s = make_cache(cache, K, &C, slot_mapping == nullptr)) != TQ_OK) return s;
+  if (n_tok < 0) return fail(TQ_ERR_INVALID_ARG, "n_tok < 0");
+  if (n_tok == 0) return ok();
+  if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return fail(TQ_ERR_INVALID_ARG, "k / v null or not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (slot_mapping == nullptr) {
+    if (n_tok != cache->batch) return fail(TQ_ERR_INVALID_ARG, "decode-step append needs n_tok == batch");
+    return cuda_status(launch_append_step(K, C, k, v, dtype, st), "tq_append_page");
+  }
+  return cuda_status(launch_append_direct(K, C, k, v, dtype, n_tok, reinterpret_cast<const long long*>(slot_mapping), st),
+                     "tq_append_page");
+}
+
+extern "C" size_t tq_decode_workspace_size(const tq_layer_params* p, int batch, int max_ctx, int n_splits) {
+  KParams K;
+  if (make_params(p, &K, false) != TQ_OK || batch < 1 || max_ctx < 0 || n_splits < 0) return 0;
+  clear_error();
+  return decode_ws_layout(K, batch, max_ctx, n_splits, num_sms()).total;
+}
+
+extern "C" tq_status tq_decode_attention(const tq_layer_params* p, const tq_cache* cache, const void* q, tq_dtype dtype,
+                                         float scale, float* out, float* lse, float* scores, void* workspace,
+                                         size_t workspace_bytes, int max_ctx, int n_splits, tq_stream_t stream) {
+  KParams K;
+  KCache C;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if ((s = make_cache(cache, K, &C, true)) != TQ_OK) return s;
+  if (!q || !out || !workspace) return fail(TQ_ERR_INVALID_ARG, "null q / out / workspace");
+  if (!aligned(workspace, 256)) return fail(TQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (max_ctx < 0 || n_splits < 0) return fail(TQ_ERR_INVALID_ARG, "max_ctx and n_splits must be >= 0");
+  if (!(scale == scale)) return fail(TQ_ERR_INVALID_ARG, "scale is NaN");
+  const WsLayout L = decode_ws_layout(K, cache->batch, max_ctx, n_splits, num_sms());
+  if (workspace_bytes < L.total) {
+    set_error("workspace too small: %zu < %zu", workspace_bytes, L.total);
+    return TQ_ERR_CAPACITY;
+  }
+  return cuda_status(launch_decode(K, C, q, dtype, scale, out, lse, scores, workspace, L, max_ctx,
+                                   reinterpret_cast<cudaStream_t>(stream)),
+                     "tq_decode_attention");
+}
+
+extern "C" tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_out) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e, "tq_check_device_error: stream");
+  unsigned a = 0, b = 0;
+  if ((e = read_clear_quant_error(&a)) != cudaSuccess) return cuda_status(e, "tq_check_device_error");
+  if ((e = read_clear_decode_error(&b)) != cudaSuccess) return cuda_status(e, "tq_check_device_error");
+  if (bits_out) *bits_out = a | b;
+  if (a | b) {
+    set_error("device error word 0x%x", a | b);
+    return TQ_ERR_DEVICE_CHECK;
+  }
+  return ok();
+}

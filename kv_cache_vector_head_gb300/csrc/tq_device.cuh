@@ -1,0 +1,90 @@
+// Device-side definitions shared by the kernels of libtq (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kPage = 16;      // tokens per page
+constexpr int kTile = 16;      // vectors per quantize tile
+constexpr float kZeroNorm = 1e-7f;
+
+// Kernel-side copy of tq_layer_params plus the derived page layout.
+struct KParams {
+  int d, hkv, hq, G, window, kb, kqjl, vb, kind;
+  const float* k_rot;
+  const float* v_rot;
+  const float* qjl_s;
+  float kc[16], kt[16], vc[16], vt[16];
+  int sub_bytes;                       // bytes of one (page, head) sub-block
+  int off_knorm, off_krnorm, off_kcodes, off_ksigns, off_vnorm, off_vcodes;
+};
+
+// Cache descriptor as seen by the kernels.
+struct KCache {
+  unsigned char* pool;
+  long long n_pages;
+  const int32_t* block_table;
+  int max_pages;
+  int32_t* seq_len;
+  int32_t* n_compressed;
+  __half* win_k;
+  __half* win_v;
+  int batch;
+  int ring;                            // window + 16 (0 without window)
+};
+
+__device__ __forceinline__ float load_elem(const void* p, int dtype, long long i) {
+  if (dtype == TQ_F32) return __ldg(reinterpret_cast<const float*>(p) + i);
+  if (dtype == TQ_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  return __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Code index of z: #{i : z >= t_i} over the 2^bits - 1 boundaries.
+__device__ __forceinline__ int bucketize(float z, const float* t, int bits) {
+  const int nb = (1 << bits) - 1;
+  int idx = 0;
+#pragma unroll
+  for (int i = 0; i < 15; ++i) idx += (i < nb && z >= t[i]) ? 1 : 0;
+  return idx;
+}
+
+// Sign-magnitude plane bit p of code idx.
+__device__ __forceinline__ unsigned plane_bit(int idx, int bits, int p) {
+  const int half = 1 << (bits - 1);
+  const bool pos = idx >= half;
+  if (p == 0) return pos ? 1u : 0u;
+  const int m = pos ? idx - half : half - 1 - idx;
+  return (unsigned)((m >> (p - 1)) & 1);
+}
+
+// Centroid of a code given its sign bit and magnitude m.
+__device__ __forceinline__ float centroid_sm(const float* c, int bits, unsigned pos, int m) {
+  const int half = 1 << (bits - 1);
+  return pos ? c[half + m] : c[half - 1 - m];
+}
+
+}  // namespace tq

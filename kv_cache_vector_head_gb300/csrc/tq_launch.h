@@ -1,0 +1,33 @@
+// Host-side launchers of libtq's kernels (defined in the .cu files).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
+                                 uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st);
+cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                 long long n_tok, const long long* slots, cudaStream_t st);
+cudaError_t launch_append_step(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                               cudaStream_t st);
+
+// Decode workspace layout (byte offsets; every region 256-byte aligned).
+struct WsLayout {
+  size_t qrot, qsk, ml, acc, total;
+  int n_comp_splits;   // compressed-page splits; one extra split holds the window
+  int pages_per_split;
+};
+WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits, int num_sms);
+
+cudaError_t launch_decode(const KParams& P, const KCache& C, const void* q, int dtype, float scale, float* out,
+                          float* lse, float* scores, void* ws, const WsLayout& L, int max_ctx, cudaStream_t st);
+
+cudaError_t read_clear_quant_error(unsigned* bits);
+cudaError_t read_clear_decode_error(unsigned* bits);
+
+}  // namespace tq

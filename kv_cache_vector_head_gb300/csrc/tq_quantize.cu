@@ -1,0 +1,476 @@
+// TurboQuant key / value quantization and paged append (sm_103a).
+//
+// [Reconstruction] §5 Steps 1-5 (norm separation, rotation, Lloyd-Max code)
+// and §6 (residual, QJL sign sketch); [Design study] §CPU and WASM kernel
+// design ("Append-time key kernel": sign flips + FWHT, quantize, pack, store
+// norm and the residual sign stream), §Packed format, §Append cost.
+//
+// One CTA owns a tile of up to 16 vectors of ONE kv head (so the per-head
+// rotation and QJL matrix are shared by the tile) and blockDim == d threads:
+//   1. norms in double, one warp per vector;
+//   2. rotation: FWHT as a register/shuffle butterfly, one warp per vector
+//      (coordinate e*32 + lane lives in register e of that lane), or the dense
+//      rotation as a tile product, thread j computing coordinate j of every
+//      vector of the tile;
+//   3. bucketize z = sqrt(d) * (Pi x) / n against the float32 boundaries and
+//      pack sign-magnitude planes with warp ballots (warp w owns word w);
+//   4. keys: residual (in z units) z - C[idx], its norm, and the QJL sketch
+//      S (z - C[idx]) as a second tile product; signs packed by ballot.
+#include <cuda_runtime.h>
+
+#include "tq_device.cuh"
+#include "tq_launch.h"
+#include "tq_tile.cuh"
+
+namespace tq {
+
+__device__ unsigned int g_quant_err = 0;
+
+// Quantize the tile held in s.x (nv vectors, rows >= nv are ignored).
+// is_key selects the key codebook/transform and the QJL stage.
+// slot_of[v] (when non-null) gives the page slot of vector v for the
+// coordinate-major value masks.
+template <int D>
+__device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head, bool is_key,
+                              const int* slot_of) {
+  constexpr int E = D / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bits = is_key ? P.kb : P.vb;
+  const float sqrt_d = sqrtf((float)D);
+  if (tid < 16) {
+    s.cb[tid] = is_key ? P.kc[tid] : P.vc[tid];
+    s.tb[tid] = is_key ? P.kt[tid] : P.vt[tid];
+  }
+  // 1. norms (double accumulation)
+  for (int v = warp; v < nv; v += D / 32) {
+    double acc = 0.0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const double xv = s.x[v][e * 32 + lane];
+      acc += xv * xv;
+    }
+    acc = warp_sum_d(acc);
+    if (lane == 0) {
+      const double n = sqrt(acc);
+      const bool zero = n < (double)kZeroNorm;
+      s.zero[v] = zero;
+      s.norm[v] = zero ? 0.f : (float)n;
+      s.inv[v] = zero ? 0.f : (P.kind == TQ_FWHT ? (float)(1.0 / n) : (float)((double)sqrt_d / n));
+    }
+  }
+  __syncthreads();
+  // 2. rotation to z = sqrt(d) * Pi x / n
+  const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (P.kind == TQ_FWHT ? D : D * D);
+  rotate_tile<D>(s, nv, P.kind, rot);
+  // 3. codes, planes, residual
+  const int j = tid;
+  unsigned vm[TQ_MAX_BITS] = {0u, 0u, 0u, 0u};
+  for (int v = 0; v < nv; ++v) {
+    const float z = s.x[v][j];
+    const int idx = bucketize(z, s.tb, bits);
+#pragma unroll
+    for (int p = 0; p < TQ_MAX_BITS; ++p) {
+      if (p < bits) {
+        const unsigned b = plane_bit(idx, bits, p);
+        const unsigned w = __ballot_sync(0xffffffffu, b);
+        if (lane == 0) s.codes[v][p][warp] = w;
+        if (slot_of && slot_of[v] >= 0) vm[p] |= b << slot_of[v];
+      }
+    }
+    if (is_key) s.r[v][j] = z - s.cb[idx];
+  }
+  if (!is_key && slot_of) {
+#pragma unroll
+    for (int p = 0; p < TQ_MAX_BITS; ++p) s.vmask[p][j] = vm[p];
+  }
+  __syncthreads();
+  if (!is_key) return;
+  // 4. residual norm gamma = ||z - C|| / sqrt(d)
+  for (int v = warp; v < nv; v += D / 32) {
+    double acc = 0.0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const double rv = s.r[v][e * 32 + lane];
+      acc += rv * rv;
+    }
+    acc = warp_sum_d(acc);
+    if (lane == 0) s.gam[v] = s.zero[v] ? 0.f : (float)(sqrt(acc) / (double)sqrt_d);
+  }
+  if (!P.kqjl) {
+    __syncthreads();
+    return;
+  }
+  // 5. QJL signs of S r (r in z units; the sign is scale free)
+  const float4* row = reinterpret_cast<const float4*>(P.qjl_s + (size_t)head * D * D + (size_t)j * D);
+  float acc[kTile];
+#pragma unroll
+  for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
+#pragma unroll 2
+  for (int i4 = 0; i4 < D / 4; ++i4) {
+    const float4 p = __ldg(row + i4);
+#pragma unroll
+    for (int v = 0; v < kTile; ++v) {
+      if (v < nv) {
+        const float4 rv = *reinterpret_cast<const float4*>(&s.r[v][i4 * 4]);
+        acc[v] = fmaf(p.x, rv.x, acc[v]);
+        acc[v] = fmaf(p.y, rv.y, acc[v]);
+        acc[v] = fmaf(p.z, rv.z, acc[v]);
+        acc[v] = fmaf(p.w, rv.w, acc[v]);
+      }
+    }
+  }
+  for (int v = 0; v < nv; ++v) {
+    const unsigned b = (s.zero[v] || acc[v] >= 0.f) ? 1u : 0u;
+    const unsigned w = __ballot_sync(0xffffffffu, b);
+    if (lane == 0) s.signs[v][warp] = w;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ flat quantize
+
+template <int D>
+__global__ void __launch_bounds__(D) quantize_flat_kernel(const __grid_constant__ KParams P, const void* x,
+                                                          int dtype, long long n_vec, int is_key,
+                                                          uint32_t* codes, uint32_t* signs, float* norms,
+                                                          float* rnorms) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
+  constexpr int E = D / 32;
+  const int head = blockIdx.y;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const int bits = is_key ? P.kb : P.vb;
+  for (long long t0 = (long long)blockIdx.x * kTile; t0 < n_tok; t0 += (long long)gridDim.x * kTile) {
+    int nv = 0;
+    // tile = tokens t0..t0+15 of this head; vector n = t * hkv + head
+    for (int v = 0; v < kTile; ++v) {
+      const long long n = (t0 + v) * P.hkv + head;
+      if (t0 + v < n_tok && n < n_vec) nv = v + 1;
+    }
+    for (int v = 0; v < nv; ++v) {
+      const long long n = (t0 + v) * P.hkv + head;
+      s.x[v][threadIdx.x] = load_elem(x, dtype, n * D + threadIdx.x);
+    }
+    __syncthreads();
+    quantize_tile<D>(P, s, nv, head, is_key != 0, nullptr);
+    // stores: record words are contiguous per vector
+    const int words = bits * E;
+    for (int i = threadIdx.x; i < nv * words; i += D) {
+      const int v = i / words, k = i % words;
+      const long long n = (t0 + v) * P.hkv + head;
+      codes[n * words + k] = s.codes[v][k / E][k % E];
+    }
+    if (is_key && P.kqjl) {
+      for (int i = threadIdx.x; i < nv * E; i += D) {
+        const int v = i / E, k = i % E;
+        const long long n = (t0 + v) * P.hkv + head;
+        signs[n * E + k] = s.signs[v][k];
+      }
+    }
+    if (threadIdx.x < nv) {
+      const long long n = (t0 + threadIdx.x) * P.hkv + head;
+      norms[n] = s.norm[threadIdx.x];
+      if (is_key && P.kqjl) rnorms[n] = s.gam[threadIdx.x];
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ page stores
+
+__device__ __forceinline__ unsigned char* subblock(const KParams& P, const KCache& C, long long page, int head) {
+  return C.pool + ((size_t)page * P.hkv + head) * (size_t)P.sub_bytes;
+}
+
+// Store the key part of vector v at (page, slot).
+template <int D>
+__device__ void store_key_slot(const KParams& P, const TileSmem<D>& s, unsigned char* sb, int v, int slot) {
+  constexpr int E = D / 32;
+  uint32_t* kc = reinterpret_cast<uint32_t*>(sb + P.off_kcodes);
+  for (int i = threadIdx.x; i < P.kb * E; i += D) {
+    const int p = i / E, w = i % E;
+    kc[(p * kPage + slot) * E + w] = s.codes[v][p][w];
+  }
+  if (P.kqjl) {
+    uint32_t* ks = reinterpret_cast<uint32_t*>(sb + P.off_ksigns);
+    for (int w = threadIdx.x; w < E; w += D) ks[slot * E + w] = s.signs[v][w];
+  }
+  if (threadIdx.x == 0) {
+    reinterpret_cast<float*>(sb + P.off_knorm)[slot] = s.norm[v];
+    if (P.kqjl) reinterpret_cast<float*>(sb + P.off_krnorm)[slot] = s.gam[v];
+  }
+}
+
+// Value planes of the tile into one sub-block: mask = slots written by this
+// tile (bits of s.vmask outside mask are zero).  full == true writes whole
+// words; otherwise read-modify-write with atomics (other slots may be written
+// concurrently by other CTAs).
+template <int D>
+__device__ void store_value_planes(const KParams& P, const TileSmem<D>& s, unsigned char* sb, unsigned mask,
+                                   bool full) {
+  const int j = threadIdx.x;
+  uint16_t* vc16 = reinterpret_cast<uint16_t*>(sb + P.off_vcodes);
+  for (int p = 0; p < P.vb; ++p) {
+    const unsigned bits = s.vmask[p][j] & mask;
+    if (full) {
+      vc16[p * D + j] = (uint16_t)bits;
+    } else {
+      unsigned int* w32 = reinterpret_cast<unsigned int*>(vc16 + p * D + (j & ~1));
+      const int sh = (j & 1) * 16;
+      atomicAnd(w32, ~(mask << sh));
+      atomicOr(w32, bits << sh);
+    }
+  }
+}
+
+// Value planes of one vector v into slot `slot` of a sub-block (atomic
+// read-modify-write: other slots of the page may be written concurrently).
+template <int D>
+__device__ void store_value_slot(const KParams& P, const TileSmem<D>& s, unsigned char* sb, int v, int slot) {
+  const int j = threadIdx.x;
+  uint16_t* vc16 = reinterpret_cast<uint16_t*>(sb + P.off_vcodes);
+  for (int p = 0; p < P.vb; ++p) {
+    const unsigned bit = (s.codes[v][p][j >> 5] >> (j & 31)) & 1u;
+    unsigned int* w32 = reinterpret_cast<unsigned int*>(vc16 + p * D + (j & ~1));
+    const int sh = (j & 1) * 16 + slot;
+    atomicAnd(w32, ~(1u << sh));
+    atomicOr(w32, bit << sh);
+  }
+}
+
+// ------------------------------------------------------------------ append: direct slots
+
+template <int D>
+__global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant__ KParams P,
+                                                          const __grid_constant__ KCache C, const void* k,
+                                                          const void* v, int dtype, long long n_tok,
+                                                          const long long* slot_mapping) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
+  __shared__ int slot_of[kTile];
+  __shared__ long long page_of[kTile];
+  __shared__ int same_page;
+  const int head = blockIdx.y;
+  const bool is_key = blockIdx.z == 0;
+  const void* x = is_key ? k : v;
+  for (long long t0 = (long long)blockIdx.x * kTile; t0 < n_tok; t0 += (long long)gridDim.x * kTile) {
+    const int nv = (int)min((long long)kTile, n_tok - t0);
+    if (threadIdx.x < kTile) {
+      long long pg = -1;
+      int sl = 0;
+      if (threadIdx.x < nv) {
+        const long long sm = slot_mapping[t0 + threadIdx.x];
+        if (sm >= 0) {
+          pg = sm / kPage;
+          sl = (int)(sm % kPage);
+          if (pg >= C.n_pages) {
+            atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+            pg = -1;
+          }
+        }
+      }
+      page_of[threadIdx.x] = pg;
+      slot_of[threadIdx.x] = pg >= 0 ? sl : -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long first = -1;
+      int same = 1;
+      for (int i = 0; i < nv; ++i) {
+        if (page_of[i] < 0) continue;
+        if (first < 0) first = page_of[i];
+        else if (page_of[i] != first) same = 0;
+      }
+      same_page = same;
+    }
+    for (int i = 0; i < nv; ++i) {
+      const long long n = (t0 + i) * P.hkv + head;
+      s.x[i][threadIdx.x] = page_of[i] >= 0 ? load_elem(x, dtype, n * D + threadIdx.x) : 0.f;
+    }
+    __syncthreads();
+    quantize_tile<D>(P, s, nv, head, is_key, slot_of);
+    if (is_key) {
+      for (int i = 0; i < nv; ++i)
+        if (page_of[i] >= 0) store_key_slot<D>(P, s, subblock(P, C, page_of[i], head), i, slot_of[i]);
+    } else {
+      if (same_page) {
+        unsigned mask = 0;
+        long long pg = -1;
+        for (int i = 0; i < nv; ++i)
+          if (page_of[i] >= 0) {
+            mask |= 1u << slot_of[i];
+            pg = page_of[i];
+          }
+        if (pg >= 0) {
+          unsigned char* sb = subblock(P, C, pg, head);
+          store_value_planes<D>(P, s, sb, mask, mask == 0xFFFFu);
+        }
+      } else {
+        for (int i = 0; i < nv; ++i)
+          if (page_of[i] >= 0) store_value_slot<D>(P, s, subblock(P, C, page_of[i], head), i, slot_of[i]);
+      }
+      if (threadIdx.x < nv && page_of[threadIdx.x] >= 0)
+        reinterpret_cast<float*>(subblock(P, C, page_of[threadIdx.x], head) + P.off_vnorm)[slot_of[threadIdx.x]] =
+            s.norm[threadIdx.x];
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ append: decode step
+
+// grid (batch, hkv, 2): blockIdx.z = 0 keys, 1 values.  Reads the counters;
+// append_counters_kernel advances them afterwards (stream order).
+template <int D>
+__global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ KParams P,
+                                                        const __grid_constant__ KCache C, const void* k,
+                                                        const void* v, int dtype) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
+  __shared__ int slot_of[kTile];
+  const int b = blockIdx.x, head = blockIdx.y;
+  const bool is_key = blockIdx.z == 0;
+  const void* x = is_key ? k : v;
+  const int T = C.seq_len[b];
+  const int nc = C.n_compressed[b];
+  const long long src = ((long long)b * P.hkv + head) * D;
+  if (P.window > 0) {
+    __half* ring = (is_key ? C.win_k : C.win_v) + (((size_t)b * P.hkv + head) * C.ring) * D;
+    if (T - nc < 0 || T - nc >= P.window + kPage) {
+      if (threadIdx.x == 0) atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
+      return;
+    }
+    ring[(size_t)(T % C.ring) * D + threadIdx.x] = __float2half_rn(load_elem(x, dtype, src + threadIdx.x));
+    if (T + 1 - nc != P.window + kPage) return;
+    // flush the oldest 16 window tokens into page nc / 16
+    const int pidx = nc / kPage;
+    long long page = -1;
+    if (pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
+    if (page < 0 || page >= C.n_pages) {
+      if (threadIdx.x == 0) atomicOr(&g_quant_err, pidx < C.max_pages ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
+      return;
+    }
+    for (int i = 0; i < kPage; ++i)
+      s.x[i][threadIdx.x] = __half2float(ring[(size_t)((nc + i) % C.ring) * D + threadIdx.x]);
+    if (threadIdx.x < kTile) slot_of[threadIdx.x] = threadIdx.x;
+    __syncthreads();
+    quantize_tile<D>(P, s, kPage, head, is_key, slot_of);
+    unsigned char* sb = subblock(P, C, page, head);
+    if (is_key) {
+      for (int i = 0; i < kPage; ++i) store_key_slot<D>(P, s, sb, i, i);
+    } else {
+      store_value_planes<D>(P, s, sb, 0xFFFFu, true);
+      if (threadIdx.x < kPage) reinterpret_cast<float*>(sb + P.off_vnorm)[threadIdx.x] = s.norm[threadIdx.x];
+    }
+  } else {
+    const int pidx = T / kPage, slot = T % kPage;
+    long long page = -1;
+    if (pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
+    if (page < 0 || page >= C.n_pages) {
+      if (threadIdx.x == 0) atomicOr(&g_quant_err, pidx < C.max_pages ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
+      return;
+    }
+    s.x[0][threadIdx.x] = load_elem(x, dtype, src + threadIdx.x);
+    if (threadIdx.x == 0) slot_of[0] = slot;
+    __syncthreads();
+    quantize_tile<D>(P, s, 1, head, is_key, slot_of);
+    unsigned char* sb = subblock(P, C, page, head);
+    if (is_key) {
+      store_key_slot<D>(P, s, sb, 0, slot);
+    } else {
+      store_value_slot<D>(P, s, sb, 0, slot);
+      if (threadIdx.x == 0) reinterpret_cast<float*>(sb + P.off_vnorm)[slot] = s.norm[0];
+    }
+  }
+}
+
+__global__ void append_counters_kernel(const __grid_constant__ KCache C, int window) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= C.batch) return;
+  const int T = C.seq_len[b];
+  int nc = C.n_compressed[b];
+  if (window > 0) {
+    if (T - nc < 0 || T - nc >= window + kPage) return;  // flagged by the step kernel
+    if (T + 1 - nc == window + kPage) nc += kPage;
+  } else {
+    if (T / kPage >= C.max_pages) return;
+    nc = T + 1;
+  }
+  C.seq_len[b] = T + 1;
+  C.n_compressed[b] = nc;
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <int D>
+static size_t tile_smem() {
+  return sizeof(TileSmem<D>);
+}
+
+template <int D>
+static cudaError_t launch_quantize_flat_d(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
+                                          uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
+                                          cudaStream_t st) {
+  const size_t sm = tile_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(quantize_flat_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  long long tiles = (n_tok + kTile - 1) / kTile;
+  const int gx = (int)std::min<long long>(tiles, 65535);
+  dim3 grid(gx, P.hkv);
+  quantize_flat_kernel<D><<<grid, D, sm, st>>>(P, x, dtype, n_vec, is_key ? 1 : 0, codes, signs, norms, rnorms);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
+                                 uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
+  if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
+  return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
+}
+
+template <int D>
+static cudaError_t launch_append_direct_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                          long long n_tok, const long long* slots, cudaStream_t st) {
+  const size_t sm = tile_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(append_direct_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (n_tok + kTile - 1) / kTile;
+  dim3 grid((int)std::min<long long>(tiles, 65535), P.hkv, 2);
+  append_direct_kernel<D><<<grid, D, sm, st>>>(P, C, k, v, dtype, n_tok, slots);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                 long long n_tok, const long long* slots, cudaStream_t st) {
+  if (P.d == 128) return launch_append_direct_d<128>(P, C, k, v, dtype, n_tok, slots, st);
+  return launch_append_direct_d<256>(P, C, k, v, dtype, n_tok, slots, st);
+}
+
+template <int D>
+static cudaError_t launch_append_step_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                        cudaStream_t st) {
+  const size_t sm = tile_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(append_step_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  dim3 grid(C.batch, P.hkv, 2);
+  append_step_kernel<D><<<grid, D, sm, st>>>(P, C, k, v, dtype);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  append_counters_kernel<<<(C.batch + 127) / 128, 128, 0, st>>>(C, P.window);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_step(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                               cudaStream_t st) {
+  if (P.d == 128) return launch_append_step_d<128>(P, C, k, v, dtype, st);
+  return launch_append_step_d<256>(P, C, k, v, dtype, st);
+}
+
+cudaError_t read_clear_quant_error(unsigned* bits) {
+  unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_quant_err, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_quant_err, &zero, sizeof(unsigned));
+}
+
+}  // namespace tq

@@ -1,0 +1,287 @@
+"""GPU-vs-oracle parity of the CUDA path, through the C ABI.
+
+Every case draws seeded synthetic inputs with the workload recipes of
+synthetic_kv (reduced batch / context so the oracle finishes in seconds),
+runs libtq on cuda:0 and compares element by element with the oracle's own
+quantization and attention, under the tolerances in tests/parity.py.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import synthetic_kv as SK
+import parity as PY
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    from kv_cache_vector_head_gb300 import build
+
+    build.build()
+    import kv_cache_vector_head_gb300 as tq
+
+    return tq
+
+
+def _layer(tq, w, layer=0):
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
+                   key_qjl=w.key_qjl, seed=w.seed, layer=layer)
+    O = PY.OracleLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
+                       qjl=w.key_qjl, seed=w.seed, layer=layer)
+    return L, O
+
+
+CASES = [
+    ("tiny", dict(ctx=200)),
+    ("qwen", dict(batch=1, ctx=61)),
+    ("llama", dict(batch=1, ctx=53)),
+    ("long", dict(ctx=37)),
+    ("bulk", dict(ctx=70)),
+    ("tiny", dict(ctx=50, kind=SK.FWHT, key_bits=1, value_bits=1)),
+    ("qwen", dict(batch=1, ctx=40, kind=SK.DENSE, key_bits=4, value_bits=3, key_qjl=False)),
+]
+
+
+@pytest.mark.parametrize("name,over", CASES)
+def test_quantize_flat_parity(tq, name, over):
+    w = SK.workload(name, **over)
+    kv = SK.keys_values(w)
+    L, O = _layer(tq, w)
+    dt = w.dtype
+    K = kv["K"].reshape(-1, w.d)
+    V = kv["V"].reshape(-1, w.d)
+    n_vec = K.shape[0] - 1  # ragged: the last token is missing its last head
+    kt = SK.to_torch(K, dt).cuda()
+    vt = SK.to_torch(V, dt).cuda()
+    E = w.d // 32
+    codes = torch.zeros(n_vec, w.key_bits * E, dtype=torch.int32, device="cuda")
+    signs = torch.zeros(n_vec, E, dtype=torch.int32, device="cuda") if w.key_qjl else None
+    norms = torch.zeros(n_vec, device="cuda")
+    rn = torch.zeros(n_vec, device="cuda") if w.key_qjl else None
+    tq.quantize_keys(L.params, kt, n_vec, codes, signs, norms, rn)
+    vcodes = torch.zeros(n_vec, w.value_bits * E, dtype=torch.int32, device="cuda")
+    vnorms = torch.zeros(n_vec, device="cuda")
+    tq.quantize_values(L.params, vt, n_vec, vcodes, vnorms)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    heads = np.arange(n_vec) % w.n_kv_heads
+    stats = {}
+    for h in range(w.n_kv_heads):
+        sel = heads == h
+        ok = O.keys(K[:n_vec][sel], h)
+        g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d)
+        g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d) if w.key_qjl else None
+        g_r = rn.cpu().numpy()[sel] if w.key_qjl else None
+        PY.compare_records(ok, g_idx, norms.cpu().numpy()[sel], g_s, g_r, True, stats)
+        ov = O.values(V[:n_vec][sel], h)
+        g_vidx = PY.unpack_flat_codes(vcodes.cpu().numpy().view(np.uint32)[sel], w.value_bits, w.d)
+        PY.compare_records(ov, g_vidx, vnorms.cpu().numpy()[sel], is_key=False, stats=stats)
+    assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
+
+
+def test_quantize_zero_and_tiny_vectors(tq):
+    w = SK.workload("qwen", batch=1, ctx=4)
+    L, O = _layer(tq, w)
+    x = np.zeros((4 * w.n_kv_heads, w.d))
+    x[1, 5] = 5e-8        # below the 1e-7 guard -> zero record
+    x[2, :] = 1e-3        # small but regular
+    x[3, 7] = 1.0         # basis vector
+    xt = torch.from_numpy(x.astype(np.float32)).cuda()
+    E = w.d // 32
+    n = x.shape[0]
+    codes = torch.zeros(n, w.key_bits * E, dtype=torch.int32, device="cuda")
+    signs = torch.zeros(n, E, dtype=torch.int32, device="cuda")
+    norms = torch.zeros(n, device="cuda")
+    rn = torch.zeros(n, device="cuda")
+    tq.quantize_keys(L.params, xt, n, codes, signs, norms, rn)
+    torch.cuda.synchronize()
+    heads = np.arange(n) % w.n_kv_heads
+    for h in range(w.n_kv_heads):
+        sel = heads == h
+        ok = O.keys(x[sel], h)
+        g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d)
+        g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d)
+        PY.compare_records(ok, g_idx, norms.cpu().numpy()[sel], g_s, rn.cpu().numpy()[sel], True, exact=True)
+    zero_rows = [0, 1]
+    for r in zero_rows:
+        assert norms[r].item() == 0.0 and rn[r].item() == 0.0
+        assert np.all(signs[r].cpu().numpy().view(np.uint32) == 0xFFFFFFFF)
+
+
+def _paged_roundtrip(tq, w, T0, steps, seed_layer=0):
+    """Prefill T0 tokens, run `steps` decode-step appends; return everything."""
+    kv = SK.keys_values(w, layer=seed_layer, ctx=T0 + steps)
+    L, O = _layer(tq, w, layer=seed_layer)
+    B, H, d = w.batch, w.n_kv_heads, w.d
+    pc = tq.PagedCache(L, B, T0 + steps)
+    kt = SK.to_torch(kv["K"], w.dtype).cuda()
+    vt = SK.to_torch(kv["V"], w.dtype).cuda()
+    pc.prefill(kt[:, :T0], vt[:, :T0])
+    for t in range(T0, T0 + steps):
+        pc.append(kt[:, t].contiguous(), vt[:, t].contiguous())
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    return kv, L, O, pc
+
+
+def _oracle_cache(w, O, kv, T, nc0):
+    """Oracle records per (b, head) of compressed tokens [0, n_c(T)) and the window.
+    Tokens < nc0 were quantized from the input; later pages from float16."""
+    nc = 16 * (max(0, T - w.window) // 16) if w.window > 0 else T
+    out = []
+    for b in range(w.batch):
+        recs_k, recs_v = [], []
+        for h in range(w.n_kv_heads):
+            K = kv["K"][b, :nc, h].copy()
+            V = kv["V"][b, :nc, h].copy()
+            K[nc0:] = K[nc0:].astype(np.float16).astype(np.float64)
+            V[nc0:] = V[nc0:].astype(np.float16).astype(np.float64)
+            recs_k.append(O.keys(K, h))
+            recs_v.append(O.values(V, h))
+        win_k = kv["K"][b, nc:T].transpose(1, 0, 2).astype(np.float16)
+        win_v = kv["V"][b, nc:T].transpose(1, 0, 2).astype(np.float16)
+        out.append((recs_k, recs_v, win_k, win_v, nc))
+    return out
+
+
+PAGED = [
+    ("qwen", dict(batch=2, window=20), 75, 40),   # window with flushes
+    ("tiny", dict(), 37, 30),                      # no window: partial pages, fp32 inputs
+    ("llama", dict(batch=2), 33, 18),
+    ("qwen", dict(batch=1, window=128), 150, 20),
+]
+
+
+@pytest.mark.parametrize("name,over,T0,steps", PAGED)
+def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
+    w = SK.workload(name, **over)
+    kv, L, O, pc = _paged_roundtrip(tq, w, T0, steps)
+    T = T0 + steps
+    nc0 = 16 * (max(0, T0 - w.window) // 16)
+    exp_nc = 16 * (max(0, T - w.window) // 16) if w.window > 0 else T
+    assert pc.seq_len.cpu().tolist() == [T] * w.batch
+    assert pc.n_compressed.cpu().tolist() == [exp_nc] * w.batch
+    ref = _oracle_cache(w, O, kv, T, nc0 if w.window > 0 else T)
+    pool = pc.pool.cpu().numpy()
+    bt = pc.block_table.cpu().numpy()
+    stats = {}
+    q = kv["q"]
+    qt = SK.to_torch(q, w.dtype).cuda()
+    scale = 1.0 / math.sqrt(w.d)
+    ws = torch.empty(tq.decode_workspace_size(L.params, w.batch, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.batch, w.n_q_heads, w.d, device="cuda")
+    lse = torch.zeros(w.batch, w.n_q_heads, device="cuda")
+    scores = torch.full((w.batch, w.n_q_heads, T), float("nan"), device="cuda")
+    tq.decode_attention(L.params, pc.cache, qt, scale, out, lse, scores, ws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    for b in range(w.batch):
+        recs_k, recs_v, win_k, win_v, nc = ref[b]
+        npg = (nc + 15) // 16
+        for h in range(w.n_kv_heads):
+            pages = [PY.read_pool(pool, O, int(bt[b, p]), h) for p in range(npg)]
+            cat = {k: np.concatenate([pg[k] for pg in pages])[:nc] for k in pages[0]} if npg else None
+            if nc:
+                PY.compare_records(recs_k[h], cat["kidx"], cat["knorm"], cat.get("ksigns"), cat.get("krnorm"),
+                                   True, stats)
+                PY.compare_records(recs_v[h], cat["vidx"], cat["vnorm"], is_key=False, stats=stats)
+            if w.window > 0 and T - nc > 0:
+                ring = pc.win_k[b, h].cpu().numpy()
+                slots = [p % pc.ring for p in range(nc, T)]
+                assert np.array_equal(ring[slots], win_k[h])
+                assert np.array_equal(pc.win_v[b, h].cpu().numpy()[slots], win_v[h])
+        comp = PY.stack_comp(recs_k, recs_v) if nc else None
+        r = PY.decode_reference(O, q[b], comp, win_k if T > nc else None, win_v if T > nc else None, scale)
+        g_sc = scores[b].cpu().numpy()
+        ex_tok = np.zeros(T, dtype=bool)
+        if nc:
+            for h in range(w.n_kv_heads):
+                ex_tok[:nc] |= PY.exempt_mask(recs_k[h], True).any(axis=1)
+        sc_err = np.abs(g_sc - r["scores"])[:, ~ex_tok]
+        assert np.isfinite(g_sc).all()
+        assert sc_err.max() < PY.SCORE_ATOL, sc_err.max()
+        assert np.abs(out[b].cpu().numpy() - r["out"]).max() < PY.OUT_ATOL
+        assert np.abs(lse[b].cpu().numpy() - r["lse"]).max() < PY.SCORE_ATOL
+
+
+def test_decode_split_invariance_and_determinism(tq):
+    w = SK.workload("qwen", batch=2, window=16)
+    kv, L, O, pc = _paged_roundtrip(tq, w, 300, 5)
+    T = 305
+    qt = SK.to_torch(kv["q"], w.dtype).cuda()
+    outs = []
+    for ns in (1, 3, 0, 0):
+        ws = torch.empty(tq.decode_workspace_size(L.params, w.batch, T, ns), dtype=torch.uint8, device="cuda")
+        out = torch.zeros(w.batch, w.n_q_heads, w.d, device="cuda")
+        tq.decode_attention(L.params, pc.cache, qt, 1 / math.sqrt(w.d), out, None, None, ws, T, ns)
+        outs.append(out.cpu().numpy())
+    assert np.abs(outs[0] - outs[1]).max() < 1e-5
+    assert np.abs(outs[0] - outs[2]).max() < 1e-5
+    assert np.array_equal(outs[2], outs[3])  # same launch configuration: bit-identical
+
+
+def test_empty_sequence_and_device_error(tq):
+    w = SK.workload("tiny")
+    L, O = _layer(tq, w)
+    pc = tq.PagedCache(L, 2, 64)
+    q = torch.randn(2, w.n_q_heads, w.d, device="cuda")
+    ws = torch.empty(tq.decode_workspace_size(L.params, 2, 64), dtype=torch.uint8, device="cuda")
+    out = torch.full((2, w.n_q_heads, w.d), 7.0, device="cuda")
+    lse = torch.zeros(2, w.n_q_heads, device="cuda")
+    tq.decode_attention(L.params, pc.cache, q, 0.1, out, lse, None, ws, 64)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isinf(lse))
+    assert tq.check_device_error() == 0
+    # a sequence longer than max_ctx is flagged on the device, not trapped
+    pc.seq_len.fill_(100)
+    pc.n_compressed.fill_(100)
+    tq.decode_attention(L.params, pc.cache, q, 0.1, out, lse, None, ws, 64)
+    bits = tq.check_device_error()
+    assert bits & 0x2
+    # a block-table entry outside the pool is flagged
+    pc.seq_len.fill_(32)
+    pc.n_compressed.fill_(32)
+    pc.block_table[0, 1] = 10 ** 6
+    tq.decode_attention(L.params, pc.cache, q, 0.1, out, lse, None, ws, 64)
+    bits = tq.check_device_error()
+    assert bits & 0x1
+    assert tq.check_device_error() == 0  # cleared
+
+
+def test_direct_slot_append_with_skips(tq):
+    w = SK.workload("llama", batch=1, ctx=40)
+    kv = SK.keys_values(w, ctx=40)
+    L, O = _layer(tq, w)
+    pc = tq.PagedCache(L, 1, 64, pool_pages=8)
+    kt = SK.to_torch(kv["K"][0], w.dtype).cuda()
+    vt = SK.to_torch(kv["V"][0], w.dtype).cuda()
+    # scattered slots across pages 5, 2, 7; token 3 skipped (-1)
+    rng = np.random.default_rng(0)
+    slots = rng.permutation(8 * 16)[:40].astype(np.int64)
+    slots[3] = -1
+    st = torch.from_numpy(slots).cuda()
+    tq.append_page(L.params, pc.cache, kt, vt, 40, st)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    pool = pc.pool.cpu().numpy()
+    for h in range(w.n_kv_heads):
+        ok = O.keys(kv["K"][0, :, h], h)
+        ov = O.values(kv["V"][0, :, h], h)
+        for t, s in enumerate(slots):
+            if s < 0:
+                continue
+            pg = PY.read_pool(pool, O, int(s // 16), h)
+            sl = int(s % 16)
+            sub = {k: v[t: t + 1] for k, v in ok.items() if isinstance(v, np.ndarray) and v.shape[:1] == (40,)}
+            PY.compare_records(sub, pg["kidx"][sl: sl + 1], pg["knorm"][sl: sl + 1], pg["ksigns"][sl: sl + 1],
+                               pg["krnorm"][sl: sl + 1], True)
+            subv = {k: v[t: t + 1] for k, v in ov.items() if isinstance(v, np.ndarray) and v.shape[:1] == (40,)}
+            PY.compare_records(subv, pg["vidx"][sl: sl + 1], pg["vnorm"][sl: sl + 1], is_key=False)

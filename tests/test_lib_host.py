@@ -1,0 +1,104 @@
+"""libtq on the host (no GPU needed): exports, host setup functions and
+argument checks.
+
+The library's codebook (Lloyd-Max with an integration-by-parts recurrence for
+the cell masses) and transforms (its own SplitMix64, Box-Muller and
+Householder QR) are written independently of the oracle; here they are
+compared with the oracle's.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import codebook as OCB
+from oracle import transforms as OT
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kv_cache_vector_head_gb300 import build
+
+    build.build()
+    from kv_cache_vector_head_gb300 import _lib
+
+    return _lib
+
+
+def test_exports_every_declared_symbol(L):
+    hdr = open(os.path.join(ROOT, "include", "tq.h")).read()
+    declared = set(re.findall(r"^\S[^\n(]*?\b(tq_\w+)\(", hdr, flags=re.M))
+    assert {"tq_build_codebook", "tq_decode_attention", "tq_append_page"} <= declared
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(L.EXPORTED)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_codebook_matches_oracle(L, d, bits):
+    c, t, mse = L.build_codebook(d, bits)
+    ref = OCB.lloyd_max(d, bits)
+    ulp = np.abs(c.view(np.int32) - ref.centroids.view(np.int32))
+    assert ulp.max() <= 1
+    np.testing.assert_allclose(c, ref.centroids, rtol=2e-7, atol=0)
+    assert np.array_equal(t, ((c[:-1] + c[1:]) * np.float32(0.5)).astype(np.float32))
+    assert abs(mse - ref.mse_unit) < 1e-10
+
+
+@pytest.mark.parametrize("d", [32, 128, 256])
+def test_transforms_match_oracle(L, d):
+    for layer, head in [(0, 0), (3, 1), (31, 7)]:
+        s = L.build_transform(L.TQ_FWHT, d, 0, layer, head, L.ROLE_KEY_ROT)
+        assert np.array_equal(s, OT.build_transform(OT.FWHT, d, 0, layer, head, 0))
+        S = L.build_transform(L.TQ_FWHT, d, 5, layer, head, L.ROLE_QJL)
+        So = OT.build_transform(OT.FWHT, d, 5, layer, head, 2).ravel()
+        assert np.abs(S.view(np.int32) - So.view(np.int32)).max() <= 1
+        P = L.build_transform(L.TQ_DENSE, d, 0, layer, head, L.ROLE_VALUE_ROT)
+        Po = OT.build_transform(OT.DENSE, d, 0, layer, head, 1).ravel()
+        assert np.max(np.abs(P - Po)) <= 2e-7
+
+
+def test_argument_checks_return_status_without_gpu(L):
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size = 96, 2, 4, 16
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 2, 2, 1, L.TQ_FWHT
+    lib = L.lib()
+    st = lib.tq_quantize_keys(ctypes.byref(p), None, 0, 10, None, None, None, None, None)
+    assert st == L.TQ_ERR_UNSUPPORTED and b"d must be" in lib.tq_last_error()
+    p.d = 128
+    st = lib.tq_quantize_keys(ctypes.byref(p), None, 0, 10, None, None, None, None, None)
+    assert st == L.TQ_ERR_INVALID_ARG  # null transforms
+    p.page_size = 32
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.page_size = 16
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * 92
+    p.n_q_heads = 20
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0  # G = 10 > 8
+    p.n_q_heads = 4
+    p.key_bits = 5
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.key_bits = 3
+    p.value_bits = 4
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * 140
+    assert lib.tq_build_codebook(2, 2, None, None, None) == L.TQ_ERR_INVALID_ARG
+    assert lib.tq_build_transform(L.TQ_FWHT, 96, 0, 0, 0, 0, None) == L.TQ_ERR_INVALID_ARG
+    out = np.zeros(96, np.float32)
+    assert lib.tq_build_transform(L.TQ_FWHT, 96, 0, 0, 0, 0,
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))) == L.TQ_ERR_UNSUPPORTED
+
+
+def test_subblock_layout_matches_oracle(L):
+    from oracle import paging as PG
+
+    for d, kb, qjl, vb in [(128, 2, 1, 2), (256, 2, 1, 2), (128, 3, 1, 4), (256, 4, 0, 1)]:
+        p = L.LayerParams()
+        p.d, p.n_kv_heads, p.n_q_heads, p.page_size = d, 2, 4, 16
+        p.key_bits, p.value_bits, p.key_qjl, p.kind = kb, vb, qjl, L.TQ_FWHT
+        assert L.subblock_bytes(p) == PG.subblock_layout(d, kb, bool(qjl), vb)["bytes"]
