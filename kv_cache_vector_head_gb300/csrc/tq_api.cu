@@ -74,6 +74,20 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
     K->vc[i] = p->v_centroids[i];
     K->vt[i] = p->v_bounds[i];
   }
+  // Walsh coefficients a_S = 2^-(b-1) sum_m c(m) (-1)^popcount(m & S), c(m) = C[half + m]
+  auto walsh = [](const float* c, int bits, float* a) {
+    const int half = 1 << (bits - 1);
+    for (int S = 0; S < 8; ++S) {
+      double acc = 0;
+      if (S < half)
+        for (int m = 0; m < half; ++m) acc += (double)c[half + m] * ((__builtin_popcount(m & S) & 1) ? -1.0 : 1.0);
+      a[S] = S < half ? (float)(acc / half) : 0.f;
+    }
+  };
+  walsh(p->k_centroids, p->key_bits, K->akw);
+  walsh(p->v_centroids, p->value_bits, K->avw);
+  K->kp = 1 << (p->key_bits - 1);
+  K->vp = 1 << (p->value_bits - 1);
   const int d = p->d, w = d / 32, P = TQ_PAGE_SIZE;
   int o = 0;
   K->off_knorm = o; o += 4 * P;

@@ -21,6 +21,10 @@ struct KParams {
   const float* v_rot;
   const float* qjl_s;
   float kc[16], kt[16], vc[16], vt[16];
+  // Walsh-plane coefficients: a code (sign s, magnitude bits m) has centroid
+  // s * sum_S a_S * prod_{i in S} (1 - 2 m_i); plane S has bit s ^ parity(m & S).
+  float akw[8], avw[8];
+  int kp, vp;                          // 2^(bits-1) planes
   int sub_bytes;                       // bytes of one (page, head) sub-block
   int off_knorm, off_krnorm, off_kcodes, off_ksigns, off_vnorm, off_vcodes;
 };

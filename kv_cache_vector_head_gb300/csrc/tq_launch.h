@@ -18,7 +18,8 @@ cudaError_t launch_append_step(const KParams& P, const KCache& C, const void* k,
 
 // Decode workspace layout (byte offsets; every region 256-byte aligned).
 struct WsLayout {
-  size_t qrot, qsk, ml, acc, total;
+  size_t afrag, ml, acc, total;
+  size_t afrag_bytes_per_head;  // per (sequence, kv head)
   int n_comp_splits;   // compressed-page splits; one extra split holds the window
   int pages_per_split;
 };
