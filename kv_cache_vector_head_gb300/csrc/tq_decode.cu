@@ -27,16 +27,17 @@
 // ~2^-22 relative query rounding instead of f16's 2^-11.
 //
 // Launches per call:
-//   decode_prologue_kernel  grid (Hq, batch): q' = Pi q, q'' = S q' and this
-//                           head's rows of the query fragments (mma order).
-//   decode_window_kernel    grid (Hkv, batch): the float16 window, unrotated
-//                           basis, CUDA cores (at most W + 15 tokens).
-//   decode_mma_kernel       grid (splits, Hkv, batch): split-K over the page
+//   decode_prologue_kernel  grid (Hkv, ceil(batch G / 16)): q' = Pi q,
+//                           q'' = S q' as tile products and the query rows
+//                           of the score operands in mma fragment order.
+//   decode_mma_kernel       grid (splits + 1, Hkv, batch): split-K over the page
 //                           list.  Pages stream into shared memory with 1-D
-//                           TMA bulk copies (cp.async.bulk + mbarrier, three
-//                           stages of 4 pages); warp w scores page w of each
-//                           4-page chunk, then all warps accumulate values for
-//                           their quarter of the coordinates.
+//                           TMA bulk copies (cp.async.bulk + mbarrier, two or
+//                           three stages of 8 pages); warp w scores page w of
+//                           each 8-page chunk, then every warp accumulates
+//                           values for its eighth of the coordinates.  The
+//                           last split scans the float16 window (unrotated
+//                           basis, CUDA cores) concurrently.
 //   decode_combine_kernel   grid (Hq, batch): merges the partials in a fixed
 //                           order, applies Pi_v^T once, adds the window part.
 #include <math.h>
@@ -51,10 +52,10 @@ namespace tq {
 
 __device__ unsigned int g_decode_err = 0;
 
-constexpr int kMmaThreads = 128;
-constexpr int kChunkPages = 4;
+constexpr int kMmaThreads = 256;
+constexpr int kMmaPages = kMmaThreads / 32;  // pages per chunk: one per warp in the key phase
 constexpr int kStages = 3;
-constexpr int kWinThreads = 128;
+constexpr int kCombThreads = 256;
 constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -67,7 +68,7 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
   int S = n_splits;
   if (S <= 0) {
     const int units = std::max(1, batch * P.hkv);
-    S = (3 * num_sms + units - 1) / units;
+    S = (4 * num_sms + units - 1) / units;  // two waves of two CTAs per SM
     S = std::max(1, std::min(S, (max_pages + 7) / 8));
   }
   S = std::min(S, max_pages);
@@ -101,8 +102,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, uint32_t
 }
 
 // f16 pair (+-1, +-1) from bits i and i + 16 of nw = ~plane_word (bit set -> -1).
+// The shift is an integer multiply so that it issues on the FMA pipe; only
+// the mask-and-merge (one LOP3) uses the integer ALU pipe.
 __device__ __forceinline__ uint32_t pm1_pair(uint32_t nw, int i) {
-  return ((nw << (15 - i)) & 0x80008000u) | 0x3C003C00u;
+  uint32_t x;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(nw), "r"(1u << (15 - i)));
+  return (x & 0x80008000u) | 0x3C003C00u;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
@@ -175,105 +180,106 @@ __device__ __forceinline__ void warp_fwht(float (&a)[E], int lane) {
 
 // ------------------------------------------------------------------ prologue
 
-// One CTA per (query head h, sequence): q' = Pi_g q and q'' = S_g q' (g the
-// kv head of h), then this head's rows of the query operand of the score
-// products, in mma.m16n8k16 A-fragment order:
+// One CTA per (kv head g, tile of 16 query vectors of that head across the
+// batch): q' = Pi_g q and q'' = S_g q' as tile products (each row of Pi_g and
+// S_g is read once per tile), then every vector's rows of the query operand
+// of the score products, in mma.m16n8k16 A-fragment order:
 //   frag[plane][kk][lane] = 4 x f16x2, rows h_local (hi limb) and h_local + 8
 //   (lo limb), k-pair (2t, 2t+1) <-> bits (i0, i0+16) and (2t+8, 2t+9) <->
 //   (i0+1, i0+17) of plane word w = t * (d/128) + kk / 8, i0 = 2 (kk mod 8),
 //   t = lane mod 4.  Rows of absent heads (h_local >= G) are zero.
 template <int D>
 __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constant__ KParams P, const void* q,
-                                                            int dtype, unsigned char* ws, WsLayout L) {
-  constexpr int KS = D / 16, WPL = D / 128, E = D / 32;
-  __shared__ float qr[D], qs[D];
-  const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x, lane = j & 31, warp = j >> 5;
-  const int G = P.G, g = hq / G, hl = hq % G;
-  const size_t qoff = ((size_t)b * P.hq + hq) * D;
-  if (P.kind == TQ_FWHT) {
-    if (warp == 0) {
-      const float* sg = P.k_rot + (size_t)g * D;
-      float a[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e)
-        a[e] = load_elem(q, dtype, (long long)(qoff + e * 32 + lane)) * __ldg(sg + e * 32 + lane);
-      warp_fwht<E>(a, lane);
-      const float sc = rsqrtf((float)D);
-#pragma unroll
-      for (int e = 0; e < E; ++e) qr[e * 32 + lane] = a[e] * sc;
-    }
-  } else {
-    qs[j] = load_elem(q, dtype, (long long)(qoff + j));
-    __syncthreads();
-    const float4* row = reinterpret_cast<const float4*>(P.k_rot + (size_t)g * D * D + (size_t)j * D);
-    float acc = 0.f;
-#pragma unroll 8
-    for (int i4 = 0; i4 < D / 4; ++i4) {
-      const float4 p = __ldg(row + i4);
-      acc = fmaf(p.x, qs[4 * i4], fmaf(p.y, qs[4 * i4 + 1], fmaf(p.z, qs[4 * i4 + 2], fmaf(p.w, qs[4 * i4 + 3], acc))));
-    }
-    qr[j] = acc;
+                                                            int dtype, unsigned char* ws, WsLayout L, int batch) {
+  constexpr int KS = D / 16, WPL = D / 128;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
+  const int g = blockIdx.x, j = threadIdx.x;
+  const int G = P.G;
+  const int n0 = blockIdx.y * kTile;
+  const int nv = min(kTile, batch * G - n0);
+  for (int v = 0; v < nv; ++v) {
+    const int n = n0 + v, b = n / G, hl = n % G;
+    s.x[v][j] = load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * D + j));
   }
+  if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
+  rotate_tile<D>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
   if (P.kqjl) {
     const float4* row = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)j * D);
-    float acc = 0.f;
+    float acc[kTile];
+#pragma unroll
+    for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
 #pragma unroll 8
     for (int i4 = 0; i4 < D / 4; ++i4) {
       const float4 p = __ldg(row + i4);
-      acc = fmaf(p.x, qr[4 * i4], fmaf(p.y, qr[4 * i4 + 1], fmaf(p.z, qr[4 * i4 + 2], fmaf(p.w, qr[4 * i4 + 3], acc))));
+#pragma unroll
+      for (int v = 0; v < kTile; ++v) {
+        if (v < nv) {
+          const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][i4 * 4]);
+          acc[v] = fmaf(p.x, xv.x, fmaf(p.y, xv.y, fmaf(p.z, xv.z, fmaf(p.w, xv.w, acc[v]))));
+        }
+      }
     }
-    __syncthreads();
-    qs[j] = acc;
+#pragma unroll
+    for (int v = 0; v < kTile; ++v)
+      if (v < nv) s.r[v][j] = acc[v];
   }
   __syncthreads();
   const int nplanes = P.kp + (P.kqjl ? 1 : 0);
-  uint32_t* frag = reinterpret_cast<uint32_t*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
-  // this head's entries: lanes with lane / 4 == hl; head 0 also zeroes the rows of absent heads
-  const int nrow = (hl == 0) ? (8 - G + 1) : 1;
-  const int total = nplanes * KS * 4 * 4 * nrow;
-  for (int idx = j; idx < total; idx += D) {
-    const int r = idx & 3, t4 = (idx >> 2) & 3, rest = idx >> 4;
-    const int rowsel = rest % nrow, kk = (rest / nrow) % KS, pl = (rest / nrow) / KS;
-    const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
-    const int lanei = g8 * 4 + t4;
-    uint32_t val = 0;
-    if (rowsel == 0) {
-      const int w = t4 * WPL + kk / 8, i0 = 2 * (kk % 8) + ((r >= 2) ? 1 : 0);
-      const int ca = 32 * w + i0, cb = ca + 16;
-      float va, vb;
-      if (pl < P.kp) {
-        va = P.akw[pl] * qr[ca];
-        vb = P.akw[pl] * qr[cb];
-      } else {
-        va = qs[ca];
-        vb = qs[cb];
+  for (int v = 0; v < nv; ++v) {
+    const int n = n0 + v, b = n / G, hl = n % G;
+    uint32_t* frag = reinterpret_cast<uint32_t*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
+    // this head's entries (lanes with lane / 4 == hl); head 0 also zeroes the rows of absent heads
+    const int nrow = (hl == 0) ? (8 - G + 1) : 1;
+    const int total = nplanes * KS * 4 * 4 * nrow;
+    for (int idx = j; idx < total; idx += D) {
+      const int r = idx & 3, t4 = (idx >> 2) & 3, rest = idx >> 4;
+      const int rowsel = rest % nrow, kk = (rest / nrow) % KS, pl = (rest / nrow) / KS;
+      const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
+      uint32_t val = 0;
+      if (rowsel == 0) {
+        const int w = t4 * WPL + kk / 8, i0 = 2 * (kk % 8) + ((r >= 2) ? 1 : 0);
+        const int ca = 32 * w + i0, cb = ca + 16;
+        float va, vb;
+        if (pl < P.kp) {
+          va = P.akw[pl] * s.x[v][ca];
+          vb = P.akw[pl] * s.x[v][cb];
+        } else {
+          va = s.r[v][ca];
+          vb = s.r[v][cb];
+        }
+        __half ha, la, hb, lb;
+        split_f16(va, ha, la);
+        split_f16(vb, hb, lb);
+        val = (r & 1) ? pack_h2(la, lb) : pack_h2(ha, hb);
       }
-      __half ha, la, hb, lb;
-      split_f16(va, ha, la);
-      split_f16(vb, hb, lb);
-      val = (r & 1) ? pack_h2(la, lb) : pack_h2(ha, hb);
+      frag[((pl * KS + kk) * 32 + g8 * 4 + t4) * 4 + r] = val;
     }
-    frag[((pl * KS + kk) * 32 + lanei) * 4 + r] = val;
   }
 }
 
 // ------------------------------------------------------------------ window (CUDA cores)
 
-// One CTA per (kv head, sequence): scores of every window token for the G
-// heads (one warp per token), one softmax per head over the window, then the
-// weighted sum of the float16 values (thread per coordinate).
+// The float16 window of one (kv head, sequence), run by the last split of the
+// decode grid (concurrently with the page splits): chunks of 16 tokens are
+// staged in shared memory with 16-byte loads; scores for the G heads (one
+// warp per token, unrotated basis), an online softmax per head, and the
+// weighted sum of the values (thread per coordinate).
 template <int D>
-__global__ void __launch_bounds__(kWinThreads) decode_window_kernel(const __grid_constant__ KParams P,
-                                                                    const __grid_constant__ KCache C,
-                                                                    const void* q, int dtype, float scale,
-                                                                    float* scores, unsigned char* ws, WsLayout L,
-                                                                    int max_ctx) {
-  constexpr int E = D / 32, CPT = D / kWinThreads;
-  extern __shared__ __align__(16) float wsc[];  // [ring][TQ_MAX_GQA] scores, then weights
-  __shared__ float qs[TQ_MAX_GQA][D];
-  __shared__ float mx_s[TQ_MAX_GQA], sum_s[TQ_MAX_GQA];
-  const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ void window_split(const KParams& P, const KCache& C, const void* q, int dtype, float scale,
+                             float* scores, unsigned char* ws, const WsLayout& L, int max_ctx, int g, int b,
+                             unsigned char* smem) {
+  constexpr int E = D / 32, NT = kMmaThreads;
+  constexpr int NG = NT / D, TG = kPage / NG;  // value phase: token groups
+  __half* kst = reinterpret_cast<__half*>(smem);                     // [16][D]
+  __half* vst = kst + kPage * D;                                     // [16][D]
+  float* qs = reinterpret_cast<float*>(vst + kPage * D);             // [G][D]
+  float* sc = qs + TQ_MAX_GQA * D;                                   // [16][8]
+  float* st_m = sc + kPage * TQ_MAX_GQA;                             // [8] running max
+  float* st_l = st_m + TQ_MAX_GQA;                                   // [8] running sum
+  float* st_a = st_l + TQ_MAX_GQA;                                   // [8] rescale
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.G;
   const int st = L.n_comp_splits + 1;
   const size_t head0 = (size_t)b * P.hq + (size_t)g * G;
@@ -288,95 +294,138 @@ __global__ void __launch_bounds__(kWinThreads) decode_window_kernel(const __grid
     if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
     nw = C.ring == 0 ? 0 : min(nw, C.ring);
   }
-  for (int i = tid; i < G * D; i += kWinThreads) qs[i / D][i % D] = load_elem(q, dtype, (long long)(head0 * D + i));
-  __syncthreads();
+  for (int i = tid; i < G * D; i += NT) qs[i] = load_elem(q, dtype, (long long)(head0 * D + i));
+  if (tid < TQ_MAX_GQA) {
+    st_m[tid] = -INFINITY;
+    st_l[tid] = 0.f;
+  }
+  const int cj = tid % D, tg = tid / D;
+  float acc[TQ_MAX_GQA];
+#pragma unroll
+  for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] = 0.f;
   const size_t ring0 = ((size_t)b * P.hkv + g) * (size_t)C.ring;
-  for (int t = warp; t < nw; t += kWinThreads / 32) {
-    const __half* kr = C.win_k + (ring0 + (size_t)((nc + t) % C.ring)) * D;
-    float kv[E];
+  for (int c0 = 0; c0 < nw; c0 += kPage) {
+    __syncthreads();
+    constexpr int V16 = D / 8;  // 16-byte vectors per row
+    for (int i = tid; i < 2 * kPage * V16; i += NT) {
+      const int which = i / (kPage * V16), t = (i / V16) % kPage, v8 = i % V16;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (c0 + t < nw) {
+        const __half* src = (which ? C.win_v : C.win_k) + (ring0 + (size_t)((nc + c0 + t) % C.ring)) * D;
+        val = reinterpret_cast<const uint4*>(src)[v8];
+      }
+      reinterpret_cast<uint4*>(which ? vst : kst)[t * V16 + v8] = val;
+    }
+    __syncthreads();
+    for (int t = warp; t < kPage; t += NT / 32) {
+      const bool live = c0 + t < nw;
+      float kv[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) kv[e] = __half2float(kr[e * 32 + lane]);
-    for (int h = 0; h < G; ++h) {
-      float a = 0.f;
+      for (int e = 0; e < E; ++e) kv[e] = __half2float(kst[t * D + e * 32 + lane]);
+      for (int h = 0; h < G; ++h) {
+        float a = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) a = fmaf(qs[h][e * 32 + lane], kv[e], a);
-      a = warp_sum_f(a);
+        for (int e = 0; e < E; ++e) a = fmaf(qs[h * D + e * 32 + lane], kv[e], a);
+        a = warp_sum_f(a);
+        if (lane == 0) {
+          sc[t * TQ_MAX_GQA + h] = live ? scale * a : -INFINITY;
+          if (scores && live) scores[(head0 + h) * (size_t)max_ctx + nc + c0 + t] = scale * a;
+        }
+      }
+    }
+    __syncthreads();
+    if (warp < G && lane < kPage) {  // warp h updates head h over the 16 tokens
+      const int h = warp;
+      const float l = sc[lane * TQ_MAX_GQA + h];
+      float mx = l;
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0x0000ffffu, mx, o));
+      const float mnew = fmaxf(st_m[h], mx);
+      const float e = (l == -INFINITY) ? 0.f : expf(l - mnew);
+      float sm = e;
+      for (int o = 8; o > 0; o >>= 1) sm += __shfl_xor_sync(0x0000ffffu, sm, o);
+      sc[lane * TQ_MAX_GQA + h] = e;
+      __syncwarp(0x0000ffffu);
       if (lane == 0) {
-        wsc[t * TQ_MAX_GQA + h] = scale * a;
-        if (scores) scores[(head0 + h) * (size_t)max_ctx + nc + t] = scale * a;
+        const float a = (mnew == -INFINITY) ? 1.f : expf(st_m[h] - mnew);
+        st_a[h] = a;
+        st_l[h] = st_l[h] * a + sm;
+        if (mnew != -INFINITY) st_m[h] = mnew;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < TQ_MAX_GQA; ++h) {
+      if (h < G) {
+        float a = acc[h] * st_a[h];
+#pragma unroll
+        for (int tt = 0; tt < TG; ++tt) {
+          const int t = tg * TG + tt;
+          a = fmaf(sc[t * TQ_MAX_GQA + h], __half2float(vst[t * D + cj]), a);
+        }
+        acc[h] = a;
       }
     }
   }
   __syncthreads();
-  // per-head max and sum: warp h handles head h, lanes stride the tokens
-  for (int h = warp; h < G; h += kWinThreads / 32) {
-    float m = -INFINITY;
-    for (int t = lane; t < nw; t += 32) m = fmaxf(m, wsc[t * TQ_MAX_GQA + h]);
-    m = warp_max_f(m);
-    float sm = 0.f;
-    for (int t = lane; t < nw; t += 32) {
-      const float e = expf(wsc[t * TQ_MAX_GQA + h] - m);
-      wsc[t * TQ_MAX_GQA + h] = e;
-      sm += e;
-    }
-    sm = warp_sum_f(sm);
-    if (lane == 0) {
-      mx_s[h] = m;
-      sum_s[h] = sm;
-    }
-  }
+  // reduce token groups through the (now free) staging buffer
+  float* red = reinterpret_cast<float*>(smem);  // [NT][8]
+#pragma unroll
+  for (int h = 0; h < TQ_MAX_GQA; ++h) red[tid * TQ_MAX_GQA + h] = acc[h];
   __syncthreads();
-  float acc[TQ_MAX_GQA][CPT];
-#pragma unroll
-  for (int h = 0; h < TQ_MAX_GQA; ++h)
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) acc[h][c] = 0.f;
-  for (int t = 0; t < nw; ++t) {
-    const __half* vr = C.win_v + (ring0 + (size_t)((nc + t) % C.ring)) * D;
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const float vv = __half2float(vr[tid + c * kWinThreads]);
-#pragma unroll
-      for (int h = 0; h < TQ_MAX_GQA; ++h)
-        if (h < G) acc[h][c] = fmaf(wsc[t * TQ_MAX_GQA + h], vv, acc[h][c]);
-    }
-  }
   float* ml = reinterpret_cast<float*>(ws + L.ml);
   float* accw = reinterpret_cast<float*>(ws + L.acc);
-  for (int h = 0; h < G; ++h)
+  if (tid < D) {
+    for (int h = 0; h < G; ++h) {
+      float v = 0.f;
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) accw[((head0 + h) * st + (st - 1)) * D + tid + c * kWinThreads] = acc[h][c];
-  if (tid < G) {
-    ml[((head0 + tid) * st + (st - 1)) * 2 + 0] = nw > 0 ? mx_s[tid] : -INFINITY;
-    ml[((head0 + tid) * st + (st - 1)) * 2 + 1] = nw > 0 ? sum_s[tid] : 0.f;
+      for (int gr = 0; gr < NG; ++gr) v += red[(gr * D + tid) * TQ_MAX_GQA + h];
+      accw[((head0 + h) * st + (st - 1)) * D + tid] = v;
+    }
   }
+  if (tid < G) {
+    ml[((head0 + tid) * st + (st - 1)) * 2 + 0] = st_m[tid];
+    ml[((head0 + tid) * st + (st - 1)) * 2 + 1] = st_l[tid];
+  }
+}
+
+// Shared memory the window split needs (staging, query, scores, state, reduction).
+static size_t window_smem_bytes(int d) {
+  const size_t stage = 2 * (size_t)kPage * d * sizeof(__half) + (size_t)TQ_MAX_GQA * d * sizeof(float) +
+                       (size_t)(kPage + 3) * TQ_MAX_GQA * sizeof(float);
+  const size_t red = (size_t)kMmaThreads * TQ_MAX_GQA * sizeof(float);
+  return std::max(stage, red);
 }
 
 // ------------------------------------------------------------------ compressed pages (tensor cores)
 
+constexpr int kPidCache = 1024;  // block-table entries of a split staged in shared memory
+
 struct MmaShared {
   uint64_t full[kStages];
-  int pvalid[kStages][kChunkPages];
-  float wsm[kChunkPages * kPage][TQ_MAX_GQA];  // weights of the chunk's 64 tokens
-  float redm[kChunkPages][TQ_MAX_GQA];
-  float reds[kChunkPages][TQ_MAX_GQA];
-  float mrun[TQ_MAX_GQA], lrun[TQ_MAX_GQA], alpha[TQ_MAX_GQA];
+  uint4 wf[kMmaPages / 2][2][32];     // softmax weights in mma A-fragment order, per page pair
+  float redm[kMmaPages][TQ_MAX_GQA];  // per-warp chunk maxima
+  float lsum[kMmaPages][TQ_MAX_GQA];  // per-warp softmax denominators
+  float mfin[TQ_MAX_GQA];
   uint32_t vlut[16];  // values with b >= 3: raw sign-magnitude bits -> (hi, lo) f16 of the centroid
-  int abort;
 };
 
 template <int D, bool VLUT>
 __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_constant__ KParams P,
-                                                                 const __grid_constant__ KCache C, float scale,
-                                                                 float* scores, unsigned char* ws, WsLayout L,
-                                                                 int max_ctx) {
+                                                                 const __grid_constant__ KCache C, const void* q,
+                                                                 int dtype, float scale, float* scores,
+                                                                 unsigned char* ws, WsLayout L, int max_ctx,
+                                                                 int nst) {
   constexpr int E = D / 32, WPL = D / 128, KS = D / 16;
-  constexpr int CPW = D / 4;         // value coordinates per warp
-  constexpr int CB = CPW / 8;        // n-tiles per value plane per warp
-  constexpr int VPL = 2;             // value planes held (Walsh b <= 2, or LUT hi / lo)
+  constexpr int NW = kMmaThreads / 32;  // warps = pages per chunk
+  constexpr int CPW = D / NW;           // value coordinates per warp
+  constexpr int CB = CPW / 8;           // n-tiles per value plane per warp
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ MmaShared sh;
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  if (s == L.n_comp_splits) {  // the float16 window runs as the last split
+    window_split<D>(P, C, q, dtype, scale, scores, ws, L, max_ctx, g, b, dyn);
+    return;
+  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, t4 = lane & 3;
   const int G = P.G;
   const int st = L.n_comp_splits + 1;
@@ -385,9 +434,10 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   const float kappa = sqrtf(1.57079632679489662f) / (float)D;
   const int sub = P.sub_bytes;
 
-  // shared memory: query fragments, then the page stages
-  uint4* afr = reinterpret_cast<uint4*>(dyn);                        // [nkp][KS][32]
-  unsigned char* stage0 = dyn + L.afrag_bytes_per_head;              // [kStages][4][sub]
+  // shared memory: query fragments | page stages | page ids of this split
+  uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
+  unsigned char* stage0 = dyn + L.afrag_bytes_per_head;                        // [nst][NW][sub]
+  long long* pids = reinterpret_cast<long long*>(stage0 + (size_t)nst * NW * sub);  // [<= kPidCache]
 
   int T = C.seq_len[b], nc = C.n_compressed[b];
   if (T < 0 || T > max_ctx || nc < 0 || nc > T) {
@@ -402,18 +452,22 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   }
   const int p0 = s * L.pages_per_split;
   const int p1 = min(p0 + L.pages_per_split, np);
-  const int nchunks = p1 > p0 ? (p1 - p0 + kChunkPages - 1) / kChunkPages : 0;
+  const int npg = max(0, p1 - p0);
+  const int nchunks = (npg + NW - 1) / NW;
+  const int ncache = min(npg, kPidCache);
 
   {
     const uint4* src = reinterpret_cast<const uint4*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
     for (int i = tid; i < (int)(L.afrag_bytes_per_head / 16); i += kMmaThreads) afr[i] = src[i];
   }
-  if (tid < TQ_MAX_GQA) {
-    sh.mrun[tid] = -INFINITY;
-    sh.lrun[tid] = 0.f;
-    sh.alpha[tid] = 1.f;
+  for (int i = tid; i < ncache; i += kMmaThreads) {
+    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    if (pid < 0 || pid >= C.n_pages) {
+      atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
+      pid = -1;
+    }
+    pids[i] = pid;
   }
-  for (int i = tid; i < kChunkPages * kPage * TQ_MAX_GQA; i += kMmaThreads) (&sh.wsm[0][0])[i] = 0.f;
   if (VLUT && tid < 16) {
     const int vb = P.vb, half = 1 << (vb - 1);
     uint32_t e = 0;
@@ -427,118 +481,119 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
     sh.vlut[tid] = e;
   }
   if (tid == 0) {
-    sh.abort = 0;
     for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // producer (thread 0): chunk k = pages p0 + 4k .. into stage k % kStages
-  auto issue = [&](int k) {
-    const int stg = k % kStages;
-    unsigned char* dst = stage0 + (size_t)stg * kChunkPages * sub;
-    uint32_t bytes = 0;
-    long long pids[kChunkPages];
-#pragma unroll
-    for (int i = 0; i < kChunkPages; ++i) {
-      const int p = p0 + k * kChunkPages + i;
-      long long pid = -1;
-      if (p < p1) {
-        pid = C.block_table[(size_t)b * C.max_pages + p];
-        if (pid < 0 || pid >= C.n_pages) {
-          atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
-          pid = -1;
-        }
-      }
-      pids[i] = pid;
-      sh.pvalid[stg][i] = pid >= 0;
-      if (pid >= 0) bytes += (uint32_t)sub;
+  auto page_id = [&](int i) -> long long {  // i = page index within the split
+    if (i >= npg) return -1;
+    if (i < ncache) return pids[i];
+    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    if (pid < 0 || pid >= C.n_pages) {
+      atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
+      pid = -1;
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(&sh.full[stg], bytes);
-#pragma unroll
-    for (int i = 0; i < kChunkPages; ++i)
-      if (pids[i] >= 0)
-        bulk_g2s(dst + (size_t)i * sub, C.pool + ((size_t)pids[i] * P.hkv + g) * (size_t)sub, (uint32_t)sub,
-                 &sh.full[stg]);
+    return pid;
   };
-  if (tid == 0)
-    for (int k = 0; k < kStages - 1 && k < nchunks; ++k) issue(k);
+  // producer (warp 0, lane i < NW handles page i): chunk k = split pages
+  // NW k .. NW k + NW - 1 into stage k % nst
+  auto issue = [&](int k) {
+    const int stg = k % nst;
+    const long long pid = lane < NW ? page_id(k * NW + lane) : -1;
+    const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub);
+    }
+    __syncwarp();
+    if (pid >= 0)
+      bulk_g2s(stage0 + ((size_t)stg * NW + lane) * sub, C.pool + ((size_t)pid * P.hkv + g) * (size_t)sub,
+               (uint32_t)sub, &sh.full[stg]);
+  };
+  if (warp == 0)
+    for (int k = 0; k < nst - 1 && k < nchunks; ++k) issue(k);
 
-  float accv[VPL][CB][4];
+  float accv[2][CB][4];
 #pragma unroll
-  for (int p = 0; p < VPL; ++p)
+  for (int p = 0; p < 2; ++p)
 #pragma unroll
     for (int c = 0; c < CB; ++c)
 #pragma unroll
       for (int r = 0; r < 4; ++r) accv[p][c][r] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;  // softmax state of head g8 (identical across warps for m)
+  bool timed_out = false;
 
   for (int k = 0; k < nchunks; ++k) {
-    __syncthreads();  // chunk k-1 fully consumed: its stage and sh.wsm may be rewritten
-    if (tid == 0 && k + kStages - 1 < nchunks) issue(k + kStages - 1);
-    const int stg = k % kStages;
-    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / kStages) & 1))) {
-      atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
-      sh.abort = 1;
+    __syncthreads();  // chunk k-1 fully consumed: its stage and sh.wf may be rewritten
+    if (warp == 0 && k + nst - 1 < nchunks) issue(k + nst - 1);
+    const int stg = k % nst;
+    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) {
+      if (!timed_out) atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
+      timed_out = true;
     }
-    __syncthreads();
-    if (sh.abort) break;
-    unsigned char* stbase = stage0 + (size_t)stg * kChunkPages * sub;
+    unsigned char* stbase = stage0 + (size_t)stg * NW * sub;
 
     // ---------------- key phase: warp w scores page w of the chunk
-    const int pg = p0 + k * kChunkPages + warp;
-    const bool pvalid = pg < p1 && sh.pvalid[stg][warp];
-    unsigned char* pb = stbase + (size_t)warp * sub;
+    const int pi = k * NW + warp;
+    const bool pvalid = pi < npg && page_id(pi) >= 0;
+    const int pg = p0 + pi;
+    const unsigned char* pb = stbase + (size_t)warp * sub;
     float sc[2][2];
     {
-      float accm[2][4], accq[2][4];
+      float accm[2][2][4], accq[2][2][4];  // [kk parity][n-tile][frag]
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) accm[nt][r] = accq[nt][r] = 0.f;
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) accm[x][nt][r] = accq[x][nt][r] = 0.f;
       if (pvalid) {
         const uint32_t* kc = reinterpret_cast<const uint32_t*>(pb + P.off_kcodes);
-        const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
-        // plane words of token 8 nt + g8, words t4 * WPL + jw; inverted (bit set -> -1)
-        uint32_t nwp[2][8][WPL];
-        uint32_t nwq[2][WPL];
+        // raw words of token 8 nt + g8, words t4 * WPL + jw
+        uint32_t rs[2][WPL], rm[3][2][WPL];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int tk = 8 * nt + g8;
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int jw = 0; jw < WPL; ++jw) {
-            const int w = t4 * WPL + jw;
-            const uint32_t sgn = kc[(0 * kPage + tk) * E + w];
-            uint32_t mag[3] = {0u, 0u, 0u};
-            for (int pl = 1; pl < P.kb; ++pl) mag[pl - 1] = kc[(pl * kPage + tk) * E + w];
+            const int tk = 8 * nt + g8, w = t4 * WPL + jw;
+            rs[nt][jw] = kc[tk * E + w];
 #pragma unroll
-            for (int S = 0; S < 8; ++S) {
-              uint32_t wd = sgn;
-              if (S & 1) wd ^= mag[0];
-              if (S & 2) wd ^= mag[1];
-              if (S & 4) wd ^= mag[2];
-              nwp[nt][S][jw] = S < P.kp ? ~wd : 0u;
-            }
-            nwq[nt][jw] = P.kqjl ? ~ks[tk * E + w] : 0u;
+            for (int m = 0; m < 3; ++m) rm[m][nt][jw] = (m + 1 < P.kb) ? kc[((m + 1) * kPage + tk) * E + w] : 0u;
           }
-        }
+        for (int S = 0; S < P.kp; ++S) {
+          uint32_t nw[2][WPL];
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const int jw = kk / 8, i0 = 2 * (kk % 8);
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int S = 0; S < 8; ++S) {
-            if (S < P.kp) {
-              const uint4 a = afr[(S * KS + kk) * 32 + lane];
+            for (int jw = 0; jw < WPL; ++jw)
+              nw[nt][jw] = ~(rs[nt][jw] ^ ((S & 1) ? rm[0][nt][jw] : 0u) ^ ((S & 2) ? rm[1][nt][jw] : 0u) ^
+                             ((S & 4) ? rm[2][nt][jw] : 0u));
+          const uint4* ap = afr + (size_t)S * KS * 32 + lane;
 #pragma unroll
-              for (int nt = 0; nt < 2; ++nt)
-                mma16816(accm[nt], a, pm1_pair(nwp[nt][S][jw], i0), pm1_pair(nwp[nt][S][jw], i0 + 1));
-            }
-          }
-          if (P.kqjl) {
-            const uint4 a = afr[(P.kp * KS + kk) * 32 + lane];
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint4 a = ap[kk * 32];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accq[nt], a, pm1_pair(nwq[nt][jw], i0), pm1_pair(nwq[nt][jw], i0 + 1));
+              mma16816(accm[kk & 1][nt], a, pm1_pair(nw[nt][kk / 8], 2 * (kk % 8)),
+                       pm1_pair(nw[nt][kk / 8], 2 * (kk % 8) + 1));
+          }
+        }
+        if (P.kqjl) {
+          const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
+          uint32_t nq[2][WPL];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int jw = 0; jw < WPL; ++jw) nq[nt][jw] = ~ks[(8 * nt + g8) * E + t4 * WPL + jw];
+          const uint4* ap = afr + (size_t)P.kp * KS * 32 + lane;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint4 a = ap[kk * 32];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              mma16816(accq[kk & 1][nt], a, pm1_pair(nq[nt][kk / 8], 2 * (kk % 8)),
+                       pm1_pair(nq[nt][kk / 8], 2 * (kk % 8) + 1));
           }
         }
       }
@@ -554,8 +609,8 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
           const bool live = pvalid && g8 < G && tok < nc;
           float l = -INFINITY;
           if (live) {
-            const float mse = accm[nt][e] + accm[nt][e + 2];
-            const float qj = accq[nt][e] + accq[nt][e + 2];
+            const float mse = accm[0][nt][e] + accm[0][nt][e + 2] + accm[1][nt][e] + accm[1][nt][e + 2];
+            const float qj = accq[0][nt][e] + accq[0][nt][e + 2] + accq[1][nt][e] + accq[1][nt][e + 2];
             const float gm = P.kqjl ? krn[t] : 0.f;
             l = scale * knorm[t] * (mse * inv_sqrt_d + kappa * gm * qj);
             if (scores) scores[(head0 + g8) * (size_t)max_ctx + tok] = l;
@@ -569,20 +624,22 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
       if (t4 == 0) sh.redm[warp][g8] = mx;
     }
     __syncthreads();
-    if (tid < G) {
-      float cm = sh.redm[0][tid];
-#pragma unroll
-      for (int w = 1; w < kChunkPages; ++w) cm = fmaxf(cm, sh.redm[w][tid]);
-      const float mold = sh.mrun[tid];
-      const float mnew = fmaxf(mold, cm);
-      sh.alpha[tid] = mnew == -INFINITY ? 1.f : expf(mold - mnew);
-      sh.mrun[tid] = mnew;
-    }
-    __syncthreads();
+    // ---------------- online softmax: every lane tracks the state of head g8
+    float alpha = 1.f;
     {
-      // weights of this warp's page: exp(l - m) * ||v|| / sqrt(d)
+      float cm = sh.redm[0][g8];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) cm = fmaxf(cm, sh.redm[w][g8]);
+      const float mnew = fmaxf(m_run, cm);
+      if (mnew != -INFINITY) {
+        alpha = expf(m_run - mnew);
+        m_run = mnew;
+      }
+      // weights of this warp's page, written in A-fragment order of its page pair:
+      // token t = 8 nt + 2 t4 + e -> k-step nt, lane (g8, t4), component 2 e (hi) / 2 e + 1 (lo),
+      // half = page parity within the pair
       const float* vnorm = reinterpret_cast<const float*>(pb + P.off_vnorm);
-      const float m = g8 < G ? sh.mrun[g8] : 0.f;
+      uint16_t* wfh = reinterpret_cast<uint16_t*>(&sh.wf[warp >> 1][0][0]);
       float ls = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -591,106 +648,98 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
           const int t = 8 * nt + 2 * t4 + e;
           float wgt = 0.f;
           if (sc[nt][e] != -INFINITY) {
-            const float ex = expf(sc[nt][e] - m);
+            const float ex = expf(sc[nt][e] - m_run);
             ls += ex;
             wgt = ex * vnorm[t] * inv_sqrt_d;
           }
-          if (g8 < G) sh.wsm[warp * kPage + t][g8] = wgt;
+          __half hi, lo;
+          split_f16(wgt, hi, lo);
+          uint16_t* dst = wfh + ((nt * 32 + lane) * 4 + 2 * e) * 2 + (warp & 1);
+          dst[0] = __half_as_ushort(hi);
+          dst[2] = __half_as_ushort(lo);
         }
-      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-      if (t4 == 0) sh.reds[warp][g8] = ls;
-    }
-    __syncthreads();
-    if (tid < G) {
-      float sum = 0.f;
+      l_run = l_run * alpha + ls;
 #pragma unroll
-      for (int w = 0; w < kChunkPages; ++w) sum += sh.reds[w][tid];
-      sh.lrun[tid] = sh.lrun[tid] * sh.alpha[tid] + sum;
-    }
-    // ---------------- value phase: warp w owns coordinates [w*CPW, (w+1)*CPW)
-    {
-      const float al = g8 < G ? sh.alpha[g8] : 1.f;
-#pragma unroll
-      for (int p = 0; p < VPL; ++p)
+      for (int p = 0; p < 2; ++p)
 #pragma unroll
         for (int c = 0; c < CB; ++c)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) accv[p][c][r] *= al;
-#pragma unroll
-      for (int jg = 0; jg < kChunkPages / 2; ++jg) {
-        const unsigned char* pa = stbase + (size_t)(2 * jg) * sub;
-        const unsigned char* pbb = stbase + (size_t)(2 * jg + 1) * sub;
-        const uint16_t* va = reinterpret_cast<const uint16_t*>(pa + P.off_vcodes);
-        const uint16_t* vbp = reinterpret_cast<const uint16_t*>(pbb + P.off_vcodes);
-        // weights fragment for the two k-steps of this page pair: rows h (hi) / h + 8 (lo),
-        // k-pair (2t, 2t+1) <-> token i of page A / page B with i = 8 ks + 2 t (+1 for k + 8)
-        uint4 wf[2];
-#pragma unroll
-        for (int ksx = 0; ksx < 2; ++ksx) {
-          const int i0 = 8 * ksx + 2 * t4, i1 = i0 + 1;
-          const float wA0 = sh.wsm[(2 * jg) * kPage + i0][g8], wB0 = sh.wsm[(2 * jg + 1) * kPage + i0][g8];
-          const float wA1 = sh.wsm[(2 * jg) * kPage + i1][g8], wB1 = sh.wsm[(2 * jg + 1) * kPage + i1][g8];
-          __half hA0, lA0, hB0, lB0, hA1, lA1, hB1, lB1;
-          split_f16(wA0, hA0, lA0);
-          split_f16(wB0, hB0, lB0);
-          split_f16(wA1, hA1, lA1);
-          split_f16(wB1, hB1, lB1);
-          wf[ksx].x = pack_h2(hA0, hB0);
-          wf[ksx].y = pack_h2(lA0, lB0);
-          wf[ksx].z = pack_h2(hA1, hB1);
-          wf[ksx].w = pack_h2(lA1, lB1);
-        }
+          for (int r = 0; r < 4; ++r) accv[p][c][r] *= alpha;
+    }
+    __syncthreads();
+    // ---------------- value phase: warp w owns coordinates [w*CPW, (w+1)*CPW)
+#pragma unroll 1
+    for (int jg = 0; jg < NW / 2; ++jg) {
+      const uint16_t* va = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg) * sub + P.off_vcodes);
+      const uint16_t* vbp = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg + 1) * sub + P.off_vcodes);
+      const uint4 wf0 = sh.wf[jg][0][lane], wf1 = sh.wf[jg][1][lane];
+      if (!VLUT) {
+        uint32_t n0[CB], n1[CB];
 #pragma unroll
         for (int cbk = 0; cbk < CB; ++cbk) {
           const int c = warp * CPW + cbk * 8 + g8;
-          if (!VLUT) {
-            const uint32_t u0 = (uint32_t)va[c] | ((uint32_t)vbp[c] << 16);
-            uint32_t u1 = u0;
-            if (P.vb == 2) u1 = u0 ^ ((uint32_t)va[D + c] | ((uint32_t)vbp[D + c] << 16));
-            const uint32_t n0 = ~u0, n1 = ~u1;
+          const uint32_t u0 = (uint32_t)va[c] | ((uint32_t)vbp[c] << 16);
+          n0[cbk] = ~u0;
+          n1[cbk] = P.vb == 2 ? ~(u0 ^ ((uint32_t)va[D + c] | ((uint32_t)vbp[D + c] << 16))) : 0u;
+        }
 #pragma unroll
-            for (int ksx = 0; ksx < 2; ++ksx) {
-              const int i0 = 8 * ksx + 2 * t4;
-              mma16816(accv[0][cbk], wf[ksx], pm1_pair(n0, i0), pm1_pair(n0, i0 + 1));
-              if (P.vb == 2) mma16816(accv[1][cbk], wf[ksx], pm1_pair(n1, i0), pm1_pair(n1, i0 + 1));
+        for (int ksx = 0; ksx < 2; ++ksx) {
+          const uint4 wfk = ksx ? wf1 : wf0;
+          const int i0 = 8 * ksx + 2 * t4;
+#pragma unroll
+          for (int cbk = 0; cbk < CB; ++cbk)
+            mma16816(accv[0][cbk], wfk, pm1_pair(n0[cbk], i0), pm1_pair(n0[cbk], i0 + 1));
+          if (P.vb == 2) {
+#pragma unroll
+            for (int cbk = 0; cbk < CB; ++cbk)
+              mma16816(accv[1][cbk], wfk, pm1_pair(n1[cbk], i0), pm1_pair(n1[cbk], i0 + 1));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int cbk = 0; cbk < CB; ++cbk) {
+          const int c = warp * CPW + cbk * 8 + g8;
+          uint32_t u[TQ_MAX_BITS];
+#pragma unroll
+          for (int p = 0; p < TQ_MAX_BITS; ++p)
+            u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
+#pragma unroll
+          for (int ksx = 0; ksx < 2; ++ksx) {
+            const int i0 = 8 * ksx + 2 * t4;
+            uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
+#pragma unroll
+            for (int p = 0; p < TQ_MAX_BITS; ++p) {
+              rA0 |= ((u[p] >> i0) & 1u) << p;
+              rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
+              rA1 |= ((u[p] >> (i0 + 1)) & 1u) << p;
+              rB1 |= ((u[p] >> (i0 + 17)) & 1u) << p;
             }
-          } else {
-            uint32_t u[TQ_MAX_BITS];
-#pragma unroll
-            for (int p = 0; p < TQ_MAX_BITS; ++p)
-              u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
-#pragma unroll
-            for (int ksx = 0; ksx < 2; ++ksx) {
-              const int i0 = 8 * ksx + 2 * t4;
-              uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
-#pragma unroll
-              for (int p = 0; p < TQ_MAX_BITS; ++p) {
-                rA0 |= ((u[p] >> i0) & 1u) << p;
-                rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
-                rA1 |= ((u[p] >> (i0 + 1)) & 1u) << p;
-                rB1 |= ((u[p] >> (i0 + 17)) & 1u) << p;
-              }
-              const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
-              // hi halves -> plane 0, lo halves -> plane 1; pair = (token of page A, token of page B)
-              mma16816(accv[0][cbk], wf[ksx], __byte_perm(eA0, eB0, 0x5410), __byte_perm(eA1, eB1, 0x5410));
-              mma16816(accv[1][cbk], wf[ksx], __byte_perm(eA0, eB0, 0x7632), __byte_perm(eA1, eB1, 0x7632));
-            }
+            const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
+            const uint4 wfk = ksx ? wf1 : wf0;
+            // hi halves -> plane 0, lo halves -> plane 1; pair = (token of page A, token of page B)
+            mma16816(accv[0][cbk], wfk, __byte_perm(eA0, eB0, 0x5410), __byte_perm(eA1, eB1, 0x5410));
+            mma16816(accv[1][cbk], wfk, __byte_perm(eA0, eB0, 0x7632), __byte_perm(eA1, eB1, 0x7632));
           }
         }
       }
     }
   }
-  __syncthreads();
-  if (sh.abort) {
+  if (timed_out) {
     // a bounded wait ran out: give the copies still in flight a second bounded
     // chance to land before the CTA's shared memory is released
-    for (int k = 0; k < nchunks; ++k) (void)mbar_wait_bounded(&sh.full[k % kStages], (uint32_t)((k / kStages) & 1));
+    for (int k = 0; k < nchunks; ++k) (void)mbar_wait_bounded(&sh.full[k % nst], (uint32_t)((k / nst) & 1));
   }
-  // partials: acc_rot[h][c] = sum over planes of coefficient x (hi-limb row + lo-limb row)
+  // ---- partials
+  float ls = l_run;
+  ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+  ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+  if (t4 == 0) sh.lsum[warp][g8] = ls;
+  if (warp == 0 && t4 == 0) sh.mfin[g8] = m_run;
+  __syncthreads();
   float* ml = reinterpret_cast<float*>(ws + L.ml);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
   if (g8 < G) {
+    // acc_rot[h][c] = sum over planes of coefficient x (hi-limb row + lo-limb row)
     const float c0 = VLUT ? 1.f : P.avw[0];
     const float c1 = VLUT ? 1.f : (P.vb == 2 ? P.avw[1] : 0.f);
 #pragma unroll
@@ -704,46 +753,51 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
     }
   }
   if (tid < G) {
-    ml[((head0 + tid) * st + s) * 2 + 0] = sh.mrun[tid];
-    ml[((head0 + tid) * st + s) * 2 + 1] = sh.lrun[tid];
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) l += sh.lsum[w][tid];
+    ml[((head0 + tid) * st + s) * 2 + 0] = sh.mfin[tid];
+    ml[((head0 + tid) * st + s) * 2 + 1] = l;
   }
 }
 
 // ------------------------------------------------------------------ combine
 
 // One CTA per (query head, sequence): the split weights exp(m_s - M) are
-// computed once into shared memory, then thread j sums the partials of
-// coordinate j over the splits (coalesced across threads) and the rotated
-// sum gets Pi_v^T once.
+// computed once into shared memory; the partial accumulators are summed by
+// SG groups of threads (each group takes every SG-th split, float4 per
+// thread, coalesced), the groups are reduced in shared memory, and the
+// rotated sum gets Pi_v^T once.
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant__ KParams P,
-                                                           const unsigned char* ws, WsLayout L, float* out,
-                                                           float* lse) {
-  constexpr int E = D / 32;
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __grid_constant__ KParams P,
+                                                                      const unsigned char* ws, WsLayout L,
+                                                                      float* out, float* lse) {
+  constexpr int E = D / 32, TPR = D / 4, SG = kCombThreads / TPR;
   extern __shared__ __align__(16) float fsplit[];  // [st] split weights
+  __shared__ __align__(16) float part[SG][D];
   __shared__ float y[D];
-  __shared__ float red[D / 32];
+  __shared__ float red[kCombThreads / 32];
   __shared__ float Msh, Lsh;
-  const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.G, g = hq / G;
   const int st = L.n_comp_splits + 1;
   const size_t head = (size_t)b * P.hq + hq;
   const float* ml = reinterpret_cast<const float*>(ws + L.ml) + head * st * 2;
   const float* acc = reinterpret_cast<const float*>(ws + L.acc) + head * st * D;
   float m = -INFINITY;
-  for (int k = j; k < st; k += D) m = fmaxf(m, ml[2 * k]);
+  for (int k = tid; k < st; k += kCombThreads) m = fmaxf(m, ml[2 * k]);
   m = warp_max_f(m);
   if (lane == 0) red[warp] = m;
   __syncthreads();
-  if (j == 0) {
+  if (tid == 0) {
     float M = red[0];
-    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+    for (int w = 1; w < kCombThreads / 32; ++w) M = fmaxf(M, red[w]);
     Msh = M;
   }
   __syncthreads();
   const float M = Msh;
   float lsum = 0.f;
-  for (int k = j; k < st; k += D) {
+  for (int k = tid; k < st; k += kCombThreads) {
     const float mk = ml[2 * k];
     const float f = (M == -INFINITY || mk == -INFINITY) ? 0.f : expf(mk - M);
     fsplit[k] = f;
@@ -753,19 +807,35 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant
   __syncthreads();
   if (lane == 0) red[warp] = lsum;
   __syncthreads();
-  if (j == 0) {
+  if (tid == 0) {
     float s2 = 0.f;
-    for (int w = 0; w < D / 32; ++w) s2 += red[w];
+    for (int w = 0; w < kCombThreads / 32; ++w) s2 += red[w];
     Lsh = s2;
   }
-  float rot = 0.f;
+  // compressed splits 0 .. st-2: group sg sums splits sg, sg + SG, ...
+  {
+    const int sg = tid / TPR, c4 = tid % TPR;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int k = 0; k < st - 1; ++k) rot = fmaf(fsplit[k], acc[(size_t)k * D + j], rot);
-  const float win = fsplit[st - 1] * acc[(size_t)(st - 1) * D + j];
-  y[j] = rot;
+    for (int k = sg; k < st - 1; k += SG) {
+      const float f = fsplit[k];
+      const float4 v = reinterpret_cast<const float4*>(acc + (size_t)k * D)[c4];
+      a.x = fmaf(f, v.x, a.x);
+      a.y = fmaf(f, v.y, a.y);
+      a.z = fmaf(f, v.z, a.z);
+      a.w = fmaf(f, v.w, a.w);
+    }
+    reinterpret_cast<float4*>(part[sg])[c4] = a;
+  }
+  __syncthreads();
+  for (int j = tid; j < D; j += kCombThreads) {
+    float r = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < SG; ++sg) r += part[sg][j];
+    y[j] = r;
+  }
   __syncthreads();
   const float* vrot = P.v_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D);
-  float o;
   if (P.kind == TQ_FWHT) {
     // Pi^T y = sigma * (H y) / sqrt(d)
     if (warp == 0) {
@@ -779,30 +849,45 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant
       for (int e = 0; e < E; ++e) y[e * 32 + lane] = a[e] * sc * __ldg(vrot + e * 32 + lane);
     }
     __syncthreads();
-    o = y[j];
   } else {
-    float a = 0.f;
+    float o = 0.f;
+    if (tid < D) {
 #pragma unroll 8
-    for (int jj = 0; jj < D; ++jj) a = fmaf(__ldg(vrot + (size_t)jj * D + j), y[jj], a);  // column j of Pi_v
-    o = a;
+      for (int jj = 0; jj < D; ++jj) o = fmaf(__ldg(vrot + (size_t)jj * D + tid), y[jj], o);  // column of Pi_v
+    }
+    __syncthreads();
+    if (tid < D) y[tid] = o;
+    __syncthreads();
   }
   const float Lsum = Lsh;
   const bool empty = M == -INFINITY || Lsum <= 0.f;
-  out[head * D + j] = empty ? 0.f : (o + win) / Lsum;
-  if (lse && j == 0) lse[head] = empty ? -INFINITY : M + logf(Lsum);
+  const float fw = fsplit[st - 1];
+  for (int j = tid; j < D; j += kCombThreads) {
+    const float win = fw * acc[(size_t)(st - 1) * D + j];
+    out[head * D + j] = empty ? 0.f : (y[j] + win) / Lsum;
+  }
+  if (lse && tid == 0) lse[head] = empty ? -INFINITY : M + logf(Lsum);
 }
 
 // ------------------------------------------------------------------ launcher
 
 template <int D, bool VLUT>
-static cudaError_t launch_mma(const KParams& P, const KCache& C, float scale, float* scores, unsigned char* ws,
-                              const WsLayout& L, int max_ctx, cudaStream_t st) {
-  const size_t dyn = L.afrag_bytes_per_head + (size_t)kStages * kChunkPages * P.sub_bytes;
+static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, int dtype, float scale,
+                              float* scores, unsigned char* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
+  const size_t pid_bytes = (size_t)std::min(L.pages_per_split, kPidCache) * sizeof(long long);
+  const size_t stage_bytes = (size_t)kMmaPages * P.sub_bytes;
+  int nst = kStages;
+  size_t dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
+  if (dyn > 110 * 1024) {  // keep two CTAs per SM where the pages are large
+    nst = 2;
+    dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
+  }
+  dyn = std::max(dyn, window_smem_bytes(D));
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dyn);
   if (e != cudaSuccess) return e;
-  dim3 grid(L.n_comp_splits, P.hkv, C.batch);
-  decode_mma_kernel<D, VLUT><<<grid, kMmaThreads, dyn, st>>>(P, C, scale, scores, ws, L, max_ctx);
+  dim3 grid(L.n_comp_splits + 1, P.hkv, C.batch);
+  decode_mma_kernel<D, VLUT><<<grid, kMmaThreads, dyn, st>>>(P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
   return cudaGetLastError();
 }
 
@@ -811,27 +896,21 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
                                    float* out, float* lse, float* scores, void* ws, const WsLayout& L, int max_ctx,
                                    cudaStream_t st) {
   unsigned char* w = reinterpret_cast<unsigned char*>(ws);
-  cudaError_t e;
-  const dim3 gh(P.hq, C.batch);
-  decode_prologue_kernel<D><<<gh, D, 0, st>>>(P, q, dtype, w, L);
+  const size_t tsm = sizeof(TileSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsm);
+  if (e != cudaSuccess) return e;
+  const dim3 gp(P.hkv, (C.batch * P.G + kTile - 1) / kTile);
+  decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, C.batch);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t wdyn = (size_t)std::max(1, C.ring) * TQ_MAX_GQA * sizeof(float);
-  if (wdyn > 48 * 1024) {
-    e = cudaFuncSetAttribute(decode_window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wdyn);
-    if (e != cudaSuccess) return e;
-  }
-  decode_window_kernel<D><<<dim3(P.hkv, C.batch), kWinThreads, wdyn, st>>>(P, C, q, dtype, scale, scores, w, L,
-                                                                           max_ctx);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = P.vb >= 3 ? launch_mma<D, true>(P, C, scale, scores, w, L, max_ctx, st)
-                : launch_mma<D, false>(P, C, scale, scores, w, L, max_ctx, st);
+  e = P.vb >= 3 ? launch_mma<D, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+                : launch_mma<D, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
   if (e != cudaSuccess) return e;
   const size_t cdyn = (size_t)(L.n_comp_splits + 1) * sizeof(float);
   if (cdyn > 48 * 1024) {
     e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cdyn);
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<D><<<gh, D, cdyn, st>>>(P, w, L, out, lse);
+  decode_combine_kernel<D><<<dim3(P.hq, C.batch), kCombThreads, cdyn, st>>>(P, w, L, out, lse);
   return cudaGetLastError();
 }
 

@@ -61,7 +61,7 @@ __device__ void rotate_tile(TileSmem<D>& s, int nv, int kind, const float* rot) 
 #pragma unroll
     for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
     const float4* row = reinterpret_cast<const float4*>(rot + (size_t)j * D);
-#pragma unroll 2
+#pragma unroll 8
     for (int i4 = 0; i4 < D / 4; ++i4) {
       const float4 p = __ldg(row + i4);
 #pragma unroll
