@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the TurboQuant KV-cache hot path on GB300.
+
+Workload (Qwen-like full-attention layer): bf16 inputs, d = 256, 4 KV / 24 q
+heads, batch 8, 32768-token context, keys 3 bits (2-bit Lloyd-Max code + 1-bit
+QJL sketch), values 2 bits, FWHT rotation, 16-token pages, float16 window of
+the last 128 tokens.  One step = the whole hot path of one decode step of one
+layer: append one token per sequence (quantize K and V into the window ring,
+flushing a page of 16 quantized tokens when due) and decode attention over the
+compressed pages plus the window.  Steps rotate over several resident layer
+caches so the working set (~770 MB) is far above the 129 MB L2.
+
+Metric: algorithmic bytes of the step (compressed records of every cached
+token, the float16 window, the new K/V, q and the output) per second, as GB/s
+and as a fraction of the measured HBM bandwidth; plus bulk quantize
+token-heads/s as a secondary line item.
+
+  python bench.py [--gpus N --steps K --warmup W]          GPU path (libtq)
+  python bench.py --impl reference [...]                   the CPU oracle
+Under torchrun every rank runs its own replica (independent sequences, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention compressed-KV GB/s & % HBM roofline; quantize tokens·heads/s"
+WORKLOAD = ("qwen-like full-attention layer: bf16, d=256, 4 KV / 24 q heads, batch 8, 32768 ctx, "
+            "keys 3b (2b Lloyd-Max + 1b QJL), values 2b, FWHT, page 16, fp16 window 128")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--layers", type=int, default=4, help="resident layer caches rotated over")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def record_bytes(d, kb, qjl, vb):
+    return 8 + (kb + 1) * d // 8 if qjl else 4 + kb * d // 8, 4 + vb * d // 8
+
+
+def decode_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True):
+    """Algorithmic bytes one decode call reads and writes for sequences of length T:
+    compressed records, the float16 window K and V, q (bf16) and the output (fp32)."""
+    kr, vr = record_bytes(d, kb, qjl, vb)
+    nc = 16 * (max(0, T - W) // 16)
+    return B * Hkv * (nc * (kr + vr) + (T - nc) * d * 2 * 2) + B * Hq * d * (2 + 4)
+
+
+def step_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True):
+    """Algorithmic bytes of one step for sequences of length T (after the append)."""
+    kr, vr = record_bytes(d, kb, qjl, vb)
+    nc = 16 * (max(0, T - W) // 16)
+    nw = T - nc
+    per_head = nc * (kr + vr) + nw * d * 2 * 2           # compressed records + fp16 window K,V
+    append = B * Hkv * d * (2 * 2 + 2 * 2)                # new K,V in (bf16) + ring writes (fp16)
+    return B * Hkv * per_head + append + B * Hq * d * (2 + 4)   # + q in (bf16) + out (fp32)
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region (skipped if unavailable)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = max(mx, float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def profiled_traffic():
+    """DRAM bytes per decode call from the committed ncu summary, or None when
+    the decode source changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "decode_qwen_ncu.md")
+    src = os.path.join(ROOT, "kv_cache_vector_head_gb300", "csrc", "tq_decode.cu")
+    try:
+        fields = dict(ln.split(":", 1) for ln in open(path) if ln.startswith(("traffic_bytes_per_call:", "source_sha256:")))
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if fields.get("source_sha256", "").strip() != digest:
+            return None
+        return int(fields["traffic_bytes_per_call"].strip())
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def max_over_ranks(x: float) -> float:
+    """The largest value of x over all ranks (identity without torch.distributed)."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample_setup():
+    """One sequence, one KV head (its 6 query heads) of the workload, quantized
+    by the oracle; the step is one append + decode over it."""
+    import numpy as np
+
+    import synthetic_kv as SK
+    from oracle import codebook as OCB
+    from oracle import codec as OC
+    from oracle import transforms as OT
+
+    w = SK.workload("qwen")
+    kv = SK.keys_values(w, seqs=[0])
+    G = w.n_q_heads // w.n_kv_heads
+    T, W, d = w.ctx, w.window, w.d
+    nc = 16 * (max(0, T - W) // 16)
+    kcb, vcb = OCB.lloyd_max(d, w.key_bits), OCB.lloyd_max(d, w.value_bits)
+    prm = {"kind": w.kind, "k_cb": kcb, "v_cb": vcb, "key_qjl": True,
+           "k_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 0)], "v_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 1)],
+           "qjl_s": [OT.build_transform(w.kind, d, 0, 0, 0, 2)]}
+    K, V = kv["K"][0, :, 0], kv["V"][0, :, 0]
+    kr = OC.quantize_prod(K[:nc], w.kind, prm["k_rot"][0], kcb, prm["qjl_s"][0])
+    vr = OC.quantize_mse(V[:nc], w.kind, prm["v_rot"][0], vcb)
+    comp = {"knorm": kr["norm"][None], "krnorm": kr["rnorm"][None], "kidx": kr["idx"][None],
+            "ksigns": kr["signs"][None], "vnorm": vr["norm"][None], "vidx": vr["idx"][None]}
+    win_k = K[nc:].astype(np.float16)[None]
+    win_v = V[nc:].astype(np.float16)[None]
+    q = kv["q"][0, :G]
+    kr_b, vr_b = record_bytes(d, w.key_bits, True, w.value_bits)
+    nbytes = nc * (kr_b + vr_b) + (T - nc) * d * 4 + d * (2 * 2 + 2 * 2) + G * d * 6
+    return {"prm": prm, "comp": comp, "win_k": win_k, "win_v": win_v, "q": q, "d": d, "bytes": nbytes,
+            "new_k": K[-1:], "new_v": V[-1:], "kind": w.kind, "T": T, "nc": nc}
+
+
+def oracle_step(S):
+    from oracle import attention as OA
+    from oracle import codec as OC
+
+    # append: the new token enters the float16 window (no page flush due at this length)
+    import numpy as np
+
+    nk = S["new_k"].astype(np.float16)[None]
+    nv = S["new_v"].astype(np.float16)[None]
+    wk = np.concatenate([S["win_k"][:, 1:], nk], axis=1)
+    wv = np.concatenate([S["win_v"][:, 1:], nv], axis=1)
+    OC.qjl_constant(S["d"])
+    return OA.decode_one(S["q"], S["comp"], wk, wv, S["prm"], 1.0 / math.sqrt(S["d"]))
+
+
+def run_cpu_sample(steps=3, warmup=1):
+    S = oracle_sample_setup()
+    for _ in range(warmup):
+        oracle_step(S)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(S)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"1 sequence x 1 KV head (6 q heads) of the workload, T={S['T']}, "
+                       f"{S['bytes'] / 1e6:.1f} MB per step, {steps} steps, 1 thread"),
+            "s_per_step": dt}
+
+
+def cpu_baseline_subprocess():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample"], capture_output=True, text=True,
+                       env=env, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    S = oracle_sample_setup()
+    for _ in range(args.warmup):
+        oracle_step(S)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(S)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    value = S["bytes"] / dt / 1e9
+    sample = (f"each step: 1 sequence x 1 KV head (6 q heads) of the workload, T={S['T']}, "
+              f"{S['bytes'] / 1e6:.1f} MB algorithmic bytes")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "1 sequence x 1 KV head per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU path
+
+def bench_quantize(tq, torch, n=1 << 20):
+    """Bulk quantize (d = 128, keys 3b + QJL, values 4b) of n token-heads: keys and values."""
+    out = {}
+    x = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
+    y = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
+    for name, kind in (("fwht", tq.TQ_FWHT), ("dense", tq.TQ_DENSE)):
+        L = tq.TQLayer(128, 8, 8, 3, 4, kind)
+        codes = torch.empty(n, 12, dtype=torch.int32, device="cuda")
+        signs = torch.empty(n, 4, dtype=torch.int32, device="cuda")
+        nk = torch.empty(n, device="cuda")
+        rk = torch.empty(n, device="cuda")
+        vcodes = torch.empty(n, 16, dtype=torch.int32, device="cuda")
+        nv = torch.empty(n, device="cuda")
+
+        def run():
+            tq.quantize_keys(L.params, x, n, codes, signs, nk, rk)
+            tq.quantize_values(L.params, y, n, vcodes, nv)
+
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        for _ in range(3):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 3
+        nbytes = n * (2 * 128 * 2 + 140)  # bf16 K, V in; 140 B of records out per token-head
+        out[name] = {"token_heads_per_s": n / (ms * 1e-3), "ms": ms, "GB_per_s": nbytes / ms / 1e6}
+    return out
+
+
+def run_gpu(args):
+    import torch
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from kv_cache_vector_head_gb300 import build
+
+    build.build()
+    import kv_cache_vector_head_gb300 as tq
+    import synthetic_kv as SK
+
+    w = SK.workload("qwen", seed=1000 * rank)
+    B, Hkv, Hq, d, T0, W = w.batch, w.n_kv_heads, w.n_q_heads, w.d, w.ctx, w.window
+    total_steps = args.warmup + 2 * args.steps
+    per_layer = (total_steps + args.layers - 1) // args.layers + 1
+    max_ctx = T0 + per_layer + 16
+    layers, caches, qs, news = [], [], [], []
+    for l in range(args.layers):
+        L = tq.TQLayer(d, Hkv, Hq, w.key_bits, w.value_bits, w.kind, window=W, seed=w.seed, layer=l)
+        pc = tq.PagedCache(L, B, max_ctx)
+        K, V, q = SK.keys_values_torch(w, layer=l, ctx=T0 + per_layer)
+        pc.prefill(K[:, :T0], V[:, :T0])
+        news.append((K[:, T0:].transpose(0, 1).contiguous(), V[:, T0:].transpose(0, 1).contiguous()))
+        del K, V
+        layers.append(L)
+        caches.append(pc)
+        qs.append(q.contiguous())
+    torch.cuda.synchronize()
+    if tq.check_device_error():
+        raise RuntimeError("device error after prefill")
+    wsz = tq.decode_workspace_size(layers[0].params, B, max_ctx)
+    work = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+    out = torch.empty(B, Hq, d, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    T = [T0] * args.layers
+    used = [0] * args.layers
+
+    def step(i, k=None, v=None, q=None, dec_ev=None):
+        l = i % args.layers
+        j = used[l]
+        used[l] += 1
+        kk = news[l][0][j] if k is None else k
+        vv = news[l][1][j] if v is None else v
+        caches[l].append(kk, vv)
+        T[l] += 1
+        if dec_ev is not None:
+            dec_ev[0].record()
+        tq.decode_attention(layers[l].params, caches[l].cache, qs[l] if q is None else q, scale, out, None, None,
+                            work, max_ctx)
+        if dec_ev is not None:
+            dec_ev[1].record()
+        return step_bytes(T[l], W, B, Hkv, Hq, d, w.key_bits, w.value_bits)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    torch.cuda.nvtx.range_push("timed")
+    t0.record()
+    total_bytes = 0
+    for i in range(args.steps):
+        total_bytes += step(args.warmup + i, dec_ev=ev[i])
+    t1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if tq.check_device_error():
+        raise RuntimeError("device error during the timed steps")
+    ms = max_over_ranks(ms)
+    # end to end through the public API with host buffers: H2D of the step's K, V, q
+    # from pinned memory and D2H of the output, inside the timed region
+    npool = 16  # pinned host copies of step inputs, used cyclically
+    hk = [news[i % args.layers][0][i // args.layers].cpu().pin_memory() for i in range(npool)]
+    hv = [news[i % args.layers][1][i // args.layers].cpu().pin_memory() for i in range(npool)]
+    hq = [qs[i % args.layers].cpu().pin_memory() for i in range(npool)]
+    hout = torch.empty(B, Hq, d).pin_memory()
+    dk, dv, dq = torch.empty_like(news[0][0][0]), torch.empty_like(news[0][1][0]), torch.empty_like(qs[0])
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record()
+    e2e_bytes = 0
+    for i in range(args.steps):
+        dk.copy_(hk[i % npool], non_blocking=True)
+        dv.copy_(hv[i % npool], non_blocking=True)
+        dq.copy_(hq[i % npool], non_blocking=True)
+        e2e_bytes += step(args.warmup + args.steps + i, dk, dv, dq)
+        hout.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e2e_ms)
+    quant = bench_quantize(tq, torch)
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
+    peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
+    value = total_bytes * ws / (ms * 1e-3) / 1e9
+    # roofline of the decode call (prologue + tensor-core split-K kernel + combine),
+    # algorithmic bytes of its reads and writes per launch over its measured duration
+    dec_bytes = decode_bytes(T0 + 1 + args.warmup // args.layers, W, B, Hkv, Hq, d, w.key_bits, w.value_bits)
+    dec_avg = statistics.mean(dec_ms)
+    achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch Philox on the device)",
+        "config": {"workload": WORKLOAD, "batch": B, "ctx": T0, "kv_heads": Hkv, "q_heads": Hq, "d": d,
+                   "key_bits": w.key_bits + 1, "value_bits": w.value_bits, "window": W, "page": 16,
+                   "layer_caches": args.layers, "l2": f"inputs larger than L2: {args.layers} rotating layer caches "
+                   f"of {step_bytes(T0, W, B, Hkv, Hq, d, w.key_bits, w.value_bits) / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{ws}"},
+        "hbm_fraction": value / ws / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "tq_decode_attention (prologue + split-K tensor-core + combine)",
+                     "peak_source": peak_src},
+        "quantize": {"metric": "bulk quantize token-heads/s (d=128, keys 3b+QJL, values 4b, 2^20 token-heads)",
+                     "fwht": quant["fwht"], "dense": quant["dense"]},
+        "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
+                "d2h_bytes_per_step": int(hout.numel() * 4)},
+        "gpu_launches": args.steps * 5,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess()
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.cpu_sample:
+        print(json.dumps(run_cpu_sample()))
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

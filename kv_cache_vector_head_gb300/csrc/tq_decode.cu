@@ -56,6 +56,7 @@ constexpr int kMmaThreads = 256;
 constexpr int kMmaPages = kMmaThreads / 32;  // pages per chunk: one per warp in the key phase
 constexpr int kStages = 3;
 constexpr int kCombThreads = 256;
+constexpr int kPrologueTile = 4;  // query vectors per prologue CTA (more CTAs, shorter walks)
 constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -180,7 +181,7 @@ __device__ __forceinline__ void warp_fwht(float (&a)[E], int lane) {
 
 // ------------------------------------------------------------------ prologue
 
-// One CTA per (kv head g, tile of 16 query vectors of that head across the
+// One CTA per (kv head g, tile of 4 query vectors of that head across the
 // batch): q' = Pi_g q and q'' = S_g q' as tile products (each row of Pi_g and
 // S_g is read once per tile), then every vector's rows of the query operand
 // of the score products, in mma.m16n8k16 A-fragment order:
@@ -196,8 +197,8 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
   const int g = blockIdx.x, j = threadIdx.x;
   const int G = P.G;
-  const int n0 = blockIdx.y * kTile;
-  const int nv = min(kTile, batch * G - n0);
+  const int n0 = blockIdx.y * kPrologueTile;
+  const int nv = min(kPrologueTile, batch * G - n0);
   for (int v = 0; v < nv; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
     s.x[v][j] = load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * D + j));
@@ -899,7 +900,7 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   const size_t tsm = sizeof(TileSmem<D>);
   cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsm);
   if (e != cudaSuccess) return e;
-  const dim3 gp(P.hkv, (C.batch * P.G + kTile - 1) / kTile);
+  const dim3 gp(P.hkv, (C.batch * P.G + kPrologueTile - 1) / kPrologueTile);
   decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, C.batch);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = P.vb >= 3 ? launch_mma<D, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)

@@ -198,3 +198,42 @@ def to_torch(x: np.ndarray, dtype: str):
 
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     return {"f32": t, "bf16": t.to(torch.bfloat16), "f16": t.to(torch.float16)}[dtype]
+
+
+def keys_values_torch(w: Workload, layer: int = 0, ctx: int | None = None, device="cuda", seed: int | None = None):
+    """The same recipe drawn on the device with torch's seeded generator (for
+    full-size benchmark caches, where the host generator is too slow).  The
+    values differ from keys_values() (different generator), the distribution
+    does not.  Returns K, V [B, T, Hkv, d] and q [B, Hq, d] in the workload dtype."""
+    import torch
+
+    T = w.ctx if ctx is None else ctx
+    g = torch.Generator(device=device)
+    g.manual_seed(stream_start(w.seed if seed is None else seed, 0xB0, layer) & ((1 << 63) - 1))
+    B, H, Hq, d = w.batch, w.n_kv_heads, w.n_q_heads, w.d
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
+    K = torch.randn(B, T, H, d, generator=g, device=device, dtype=torch.float32)
+    V = torch.randn(B, T, H, d, generator=g, device=device, dtype=torch.float32)
+    q = torch.randn(B, 1, Hq, d, generator=g, device=device, dtype=torch.float32)
+    if w.key_scale in ("pre_rope_exp", "lognormal"):
+        K *= torch.exp(torch.randn(H, d, generator=g, device=device))[None, None]
+    if w.value_scale == "lognormal":
+        V *= torch.exp(torch.randn(H, d, generator=g, device=device))[None, None]
+    if w.rope:
+        half = d // 2
+        inv = 1e4 ** (-torch.arange(half, device=device, dtype=torch.float64) * 2.0 / d)
+
+        def rot(x, pos):
+            ang = (pos[:, None].double() * inv[None, :]).float()
+            c, s = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+            x1, x2 = x[..., :half], x[..., half:]
+            return torch.cat([x1 * c - x2 * s, x1 * s + x2 * c], dim=-1)
+
+        for b in range(B):
+            K[b] = rot(K[b], torch.arange(T, device=device))
+        q = rot(q, torch.tensor([T], device=device))
+    if w.key_scale == "outliers":
+        for h in range(H):
+            idx = torch.randperm(d, generator=g, device=device)[:4]
+            K[:, :, h, idx] *= 20.0
+    return K.to(dt), V.to(dt), q[:, 0].to(dt)

@@ -1,0 +1,51 @@
+"""Host-side logic of bench.py: byte accounting and the cross-rank reduction
+(two gloo ranks on the CPU; the GPU bench runs one replica per rank)."""
+
+import os
+import socket
+
+import pytest
+
+import bench
+from oracle import paging as PG
+
+
+def test_byte_accounting_matches_record_formulas():
+    d, kb, vb = 256, 2, 2
+    kr, vr = bench.record_bytes(d, kb, True, vb)
+    assert kr + vr == PG.record_bytes(d, kb, True, vb) == 172
+    B, Hkv, Hq, W = 8, 4, 24, 128
+    T = 32768
+    nc = PG.n_compressed(T, W)
+    exp = B * Hkv * (nc * 172 + (T - nc) * d * 4) + B * Hq * d * 6
+    assert bench.decode_bytes(T, W, B, Hkv, Hq, d, kb, vb) == exp
+    assert bench.step_bytes(T, W, B, Hkv, Hq, d, kb, vb) == exp + B * Hkv * d * 8
+    assert abs(exp / 1e6 - 183.8) < 0.5
+
+
+def _worker(rank, port, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    q.put((rank, bench.max_over_ranks(10.0 + rank)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    import torch.multiprocessing as mp
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ps = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 11.0), (1, 11.0)]
+    assert bench.max_over_ranks(3.5) == 3.5  # single process: identity
