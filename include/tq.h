@@ -235,6 +235,30 @@ tq_status tq_decode_attention(const tq_layer_params* p, const tq_cache* cache, c
                               void* workspace, size_t workspace_bytes, int max_ctx, int n_splits,
                               tq_stream_t stream);
 
+/*
+ * tq_decode_attention_static -- tq_decode_attention without a workspace
+ * argument, for callers that cannot allocate device memory (for example a
+ * host runtime whose memory is all pre-planned, or code running where
+ * cudaMalloc is forbidden or would stall).  The pages this library follows
+ * have no counterpart to it; it is a convenience of this library.
+ * The scratch lives in a fixed array inside the library, TQ_STATIC_SCRATCH_BYTES
+ * large, which every GPU that loads the library keeps for the life of the
+ * process.  Same arguments, results and errors as tq_decode_attention; a
+ * configuration whose workspace (tq_decode_workspace_size) exceeds the array
+ * returns TQ_ERR_CAPACITY and launches nothing.  Nothing is allocated.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race and corrupt each other's
+ *     scratch.  Serialise them on one stream.  The array keeps the last call's
+ *     contents; decode writes every scratch byte it reads, so nothing needs
+ *     clearing between calls.
+ */
+#define TQ_STATIC_SCRATCH_BYTES (16u << 20)
+tq_status tq_decode_attention_static(const tq_layer_params* p, const tq_cache* cache, const void* q,
+                                     tq_dtype dtype, float scale, float* out, float* lse, float* scores,
+                                     int max_ctx, int n_splits, tq_stream_t stream);
+
 /* Synchronises the stream, reads and clears the device error word.
  * Returns TQ_ERR_DEVICE_CHECK if any bit was set (bits in *bits_out, nullable). */
 tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_out);

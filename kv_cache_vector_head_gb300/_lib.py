@@ -25,7 +25,9 @@ PAGE_SIZE = 16
 EXPORTED = [
     "tq_build_codebook", "tq_build_transform", "tq_quantize_keys", "tq_quantize_values", "tq_subblock_bytes",
     "tq_append_page", "tq_decode_workspace_size", "tq_decode_attention", "tq_check_device_error", "tq_last_error",
+    "tq_decode_attention_static",
 ]
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class TQError(RuntimeError):
@@ -75,6 +77,8 @@ def lib():
         L.tq_decode_workspace_size.restype = c_size_t
         L.tq_decode_attention.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_int, c_float, c_void_p,
                                           c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_int, c_void_p]
+        L.tq_decode_attention_static.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_int, c_float,
+                                                 c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]
         L.tq_check_device_error.argtypes = [c_void_p, POINTER(c_uint32)]
         L.tq_last_error.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -161,6 +165,13 @@ def decode_attention(p: LayerParams, cache: Cache, q, scale: float, out, lse, sc
     _check(lib().tq_decode_attention(ctypes.byref(p), ctypes.byref(cache), _ptr(q), dtype_code(q), scale, _ptr(out),
                                      _ptr(lse), _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      max_ctx, n_splits, _stream(stream)))
+
+
+def decode_attention_static(p: LayerParams, cache: Cache, q, scale: float, out, lse, scores, max_ctx: int,
+                            n_splits: int = 0, stream=None) -> None:
+    """tq_decode_attention with the library's own static scratch (no workspace)."""
+    _check(lib().tq_decode_attention_static(ctypes.byref(p), ctypes.byref(cache), _ptr(q), dtype_code(q), scale,
+                                            _ptr(out), _ptr(lse), _ptr(scores), max_ctx, n_splits, _stream(stream)))
 
 
 def check_device_error(stream=None) -> int:

@@ -242,3 +242,49 @@ extern "C" tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_ou
   }
   return ok();
 }
+
+// ------------------------------------------------------------------ decode without a workspace argument
+
+namespace tq {
+namespace {
+// Scratch for tq_decode_attention_static.  In host code this symbol is only a
+// stand-in: its device address comes from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) unsigned char g_static_scratch[TQ_STATIC_SCRATCH_BYTES];
+std::mutex g_static_mu;
+void* g_static_ptr[256] = {};
+}  // namespace
+}  // namespace tq
+
+extern "C" tq_status tq_decode_attention_static(const tq_layer_params* p, const tq_cache* cache, const void* q,
+                                                tq_dtype dtype, float scale, float* out, float* lse, float* scores,
+                                                int max_ctx, int n_splits, tq_stream_t stream) {
+  KParams K;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if (!cache || cache->batch < 1 || max_ctx < 0 || n_splits < 0)
+    return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention_static: bad cache, max_ctx or n_splits");
+  const size_t need = decode_ws_layout(K, cache->batch, max_ctx, n_splits, num_sms()).total;
+  if (need > (size_t)TQ_STATIC_SCRATCH_BYTES) {
+    set_error("tq_decode_attention_static: this configuration needs %zu bytes of scratch, more than the %u-byte "
+              "static array; use tq_decode_attention with a workspace", need, (unsigned)TQ_STATIC_SCRATCH_BYTES);
+    return TQ_ERR_CAPACITY;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "tq_decode_attention_static: cudaGetDevice");
+  if (dev < 0 || dev >= 256) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention_static: device index >= 256");
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_static_ptr[dev], g_static_scratch);
+      if (e != cudaSuccess) {
+        g_static_ptr[dev] = nullptr;
+        return cuda_status(e, "tq_decode_attention_static: cudaGetSymbolAddress");
+      }
+    }
+    ptr = g_static_ptr[dev];
+  }
+  return tq_decode_attention(p, cache, q, dtype, scale, out, lse, scores, ptr, (size_t)TQ_STATIC_SCRATCH_BYTES,
+                             max_ctx, n_splits, stream);
+}
