@@ -102,13 +102,18 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, uint32_t
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-// f16 pair (+-1, +-1) from bits i and i + 16 of nw = ~plane_word (bit set -> -1).
-// The shift is an integer multiply so that it issues on the FMA pipe; only
-// the mask-and-merge (one LOP3) uses the integer ALU pipe.
-__device__ __forceinline__ uint32_t pm1_pair(uint32_t nw, int i) {
-  uint32_t x;
-  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(nw), "r"(1u << (15 - i)));
-  return (x & 0x80008000u) | 0x3C003C00u;
+// f16 pair (+-1, +-1) from bits i and i + 16 of nw = ~plane_word (bit set -> -1):
+// ((nw << (15 - i)) & 0x80008000) | 0x3C003C00.  The shift is an integer
+// multiply (FMA pipe); the mask-and-merge is one LOP3 whose two constants come
+// in registers (mask = 0x80008000, one = 0x3C003C00).
+__device__ __forceinline__ uint32_t pm1_mul(uint32_t nw, uint32_t mult, uint32_t mask, uint32_t one) {
+  uint32_t x, r;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(nw), "r"(mult));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(one));
+  return r;
+}
+__device__ __forceinline__ uint32_t pm1_pair(uint32_t nw, int i, uint32_t mask, uint32_t one) {
+  return pm1_mul(nw, 1u << (15 - i), mask, one);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
@@ -434,6 +439,10 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   const float inv_sqrt_d = rsqrtf((float)D);
   const float kappa = sqrtf(1.57079632679489662f) / (float)D;
   const int sub = P.sub_bytes;
+  const uint32_t pmM = P.pm_mask, pmO = P.pm_one;
+  // value-phase shift multipliers of this lane: bits 2t, 2t+1, 8+2t, 9+2t -> bit 15
+  const uint32_t vm0 = 1u << (15 - 2 * t4), vm1 = 1u << (14 - 2 * t4), vm2 = 1u << (7 - 2 * t4),
+                 vm3 = 1u << (6 - 2 * t4);
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -576,8 +585,8 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
             const uint4 a = ap[kk * 32];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accm[kk & 1][nt], a, pm1_pair(nw[nt][kk / 8], 2 * (kk % 8)),
-                       pm1_pair(nw[nt][kk / 8], 2 * (kk % 8) + 1));
+              mma16816(accm[kk & 1][nt], a, pm1_pair(nw[nt][kk / 8], 2 * (kk % 8), pmM, pmO),
+                       pm1_pair(nw[nt][kk / 8], 2 * (kk % 8) + 1, pmM, pmO));
           }
         }
         if (P.kqjl) {
@@ -593,8 +602,8 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
             const uint4 a = ap[kk * 32];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accq[kk & 1][nt], a, pm1_pair(nq[nt][kk / 8], 2 * (kk % 8)),
-                       pm1_pair(nq[nt][kk / 8], 2 * (kk % 8) + 1));
+              mma16816(accq[kk & 1][nt], a, pm1_pair(nq[nt][kk / 8], 2 * (kk % 8), pmM, pmO),
+                       pm1_pair(nq[nt][kk / 8], 2 * (kk % 8) + 1, pmM, pmO));
           }
         }
       }
@@ -660,12 +669,14 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
           dst[2] = __half_as_ushort(lo);
         }
       l_run = l_run * alpha + ls;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-      for (int p = 0; p < 2; ++p)
+        for (int p = 0; p < 2; ++p)
 #pragma unroll
-        for (int c = 0; c < CB; ++c)
+          for (int c = 0; c < CB; ++c)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) accv[p][c][r] *= alpha;
+            for (int r = 0; r < 4; ++r) accv[p][c][r] *= alpha;
+      }
     }
     __syncthreads();
     // ---------------- value phase: warp w owns coordinates [w*CPW, (w+1)*CPW)
@@ -686,14 +697,14 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
 #pragma unroll
         for (int ksx = 0; ksx < 2; ++ksx) {
           const uint4 wfk = ksx ? wf1 : wf0;
-          const int i0 = 8 * ksx + 2 * t4;
+          const uint32_t ma = ksx ? vm2 : vm0, mb = ksx ? vm3 : vm1;
 #pragma unroll
           for (int cbk = 0; cbk < CB; ++cbk)
-            mma16816(accv[0][cbk], wfk, pm1_pair(n0[cbk], i0), pm1_pair(n0[cbk], i0 + 1));
+            mma16816(accv[0][cbk], wfk, pm1_mul(n0[cbk], ma, pmM, pmO), pm1_mul(n0[cbk], mb, pmM, pmO));
           if (P.vb == 2) {
 #pragma unroll
             for (int cbk = 0; cbk < CB; ++cbk)
-              mma16816(accv[1][cbk], wfk, pm1_pair(n1[cbk], i0), pm1_pair(n1[cbk], i0 + 1));
+              mma16816(accv[1][cbk], wfk, pm1_mul(n1[cbk], ma, pmM, pmO), pm1_mul(n1[cbk], mb, pmM, pmO));
           }
         }
       } else {
