@@ -21,6 +21,7 @@
 #include "tq_device.cuh"
 #include "tq_launch.h"
 #include "tq_tile.cuh"
+#include "tq_quantize_mma.cuh"
 
 namespace tq {
 
@@ -422,8 +423,55 @@ static cudaError_t launch_quantize_flat_d(const KParams& P, const void* x, int d
   return cudaGetLastError();
 }
 
+// Codebook tables with c[half + m] = -c[half - 1 - m], a zero middle boundary,
+// antisymmetric and strictly increasing boundaries (tq_build_codebook's tables).
+static bool antisymmetric(const float* c, const float* t, int bits) {
+  const int half = 1 << (bits - 1);
+  if (t[half - 1] != 0.f) return false;
+  for (int m = 0; m < half; ++m)
+    if (c[half + m] != -c[half - 1 - m]) return false;
+  for (int k = 1; k < half; ++k)
+    if (t[half - 1 + k] != -t[half - 1 - k]) return false;
+  for (int k = half - 1; k + 1 < 2 * half - 1; ++k)
+    if (!(t[k] < t[k + 1])) return false;
+  return true;
+}
+
+template <bool QJL, bool DENSE>
+static cudaError_t launch_quantize_warp(const KParams& P, const void* x, long long n_vec, bool is_key,
+                                        uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
+                                        cudaStream_t st) {
+  constexpr int warps = wq::warps_for(DENSE);
+  auto kern = wq::quantize_warp_kernel<QJL, DENSE>;
+  const size_t sm = wq::smem_bytes(QJL, DENSE);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  int occ = 0, dev = 0, sms = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * warps, sm)) != cudaSuccess) return e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 15) / 16;
+  if (n_tiles == 0) return cudaSuccess;
+  long long gx = std::max(1LL, (long long)std::max(occ, 1) * sms / P.hkv);
+  gx = std::min(gx, (n_tiles + warps - 1) / warps);
+  dim3 grid((int)std::min(gx, 65535LL), P.hkv);
+  kern<<<grid, 32 * warps, sm, st>>>(P, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, is_key ? 1 : 0, codes,
+                                      signs, norms, rnorms);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
+  const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
+  if (P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && ((uintptr_t)codes & 15) == 0) {
+    const bool qjl = is_key && P.kqjl;
+    if (P.kind == TQ_FWHT)
+      return qjl ? launch_quantize_warp<true, false>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+                 : launch_quantize_warp<false, false>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    return qjl ? launch_quantize_warp<true, true>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+               : launch_quantize_warp<false, true>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+  }
   if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
   return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
 }

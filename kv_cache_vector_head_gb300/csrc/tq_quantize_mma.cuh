@@ -1,0 +1,503 @@
+// Bulk quantize of d = 128 bf16 vectors with the products on tensor cores.
+//
+// [Reconstruction] §5 Steps 1-5 and §6; [Design study] §CPU and WASM kernel
+// design ("Append-time key kernel") and §Packed format.  Same results as
+// quantize_tile (every decision on fp32 values of the same accuracy), laid
+// out for mma.m16n8k16:
+//
+//   * one warp owns a tile of 16 vectors (the M rows of the MMAs) of one kv
+//     head and keeps it in registers from the load to the stores;
+//   * coordinates are permuted inside each 16-wide k-block so that one
+//     16-byte load per lane yields two A fragments; the same permutation
+//     makes every lane hold 4 consecutive coordinates per block of the
+//     outputs, so a lane owns one byte of every packed 32-bit word;
+//   * FWHT: H_128 = H_8 (x) H_16 over a split of the 7 index bits; the
+//     H_16 factor (with the sign flips folded in) is one bf16 MMA per
+//     k-block (+-1 and bf16 inputs are exact, accumulation in fp32), the
+//     H_8 factor a register butterfly across the 8 accumulator blocks;
+//   * dense Pi: bf16 inputs against Pi split in three bf16 limbs (24
+//     significant bits), fragments staged once per CTA in shared memory;
+//   * QJL: S r as one f16 MMA (r and S rounded to f16).  Every entry whose
+//     magnitude is below a certified bound of that rounding,
+//     2^-10 (1 + eps) ||r|| ||S_c||, is recomputed in fp32 by the warp, so
+//     every sign is the sign of an fp32 product;
+//   * norms in fp32 with balanced summation trees of depth 7 (relative
+//     error at most 7 u before the square root halves it), scales taken as
+//     sqrt(d / s) and sqrt(s_r / d) (d a power of two).
+//
+// Requirements checked by the launcher: d = 128, bf16 input, 16-byte aligned
+// input and code arrays, codebook tables antisymmetric (c[half+m] =
+// -c[half-1-m], middle boundary 0), which lets the code be taken as a sign
+// and a magnitude found by binary search over the positive boundaries.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <limits.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace wq {
+
+constexpr int D = 128;
+constexpr int KB = D / 16;     // k-blocks
+constexpr int RS = D + 4;      // row stride (floats) of the per-warp residual buffer
+
+// Permuted coordinates.  Logical index L in [0, 16) of k-block kk sits at
+// blk_base(kk) + free_off(L): bits 2, 5, 6 of the coordinate come from the
+// block, bits 0, 1, 3, 4 from L.
+__host__ __device__ constexpr int blk_base(int kk) { return 32 * (kk >> 1) + 4 * (kk & 1); }
+__host__ __device__ constexpr int free_off(int L) { return 8 * ((L >> 1) & 3) + 2 * (L >> 3) + (L & 1); }
+// output coordinate of column n in rotation tile nt (tiles 2a', 2a'+1 form block a')
+__host__ __device__ constexpr int rot_out(int nt, int n) {
+  return blk_base(nt >> 1) + 8 * (n >> 1) + 2 * (nt & 1) + (n & 1);
+}
+// sketch coordinate of column n in tile nt: tiles 4w..4w+3 cover word w
+__host__ __device__ constexpr int sk_out(int nt, int n) {
+  return 32 * (nt >> 2) + 8 * (n >> 1) + 2 * (nt & 3) + (n & 1);
+}
+
+struct Shared {
+  int tpi[8];                  // positive boundaries as int bits, ascending (INT_MAX pads)
+  float cpos[8];               // positive centroids
+  float snorm[D];              // ||S_c|| (rounded up)
+  uint2 hfrag[KB][2][32];      // FWHT H_16 * sigma fragments (bf16)
+};
+constexpr size_t kSfragBytes = (size_t)16 * KB * 32 * sizeof(uint2);     // S (f16)
+constexpr size_t kPfragBytes = (size_t)3 * 16 * KB * 32 * sizeof(uint2);  // Pi limbs (bf16)
+__host__ __device__ constexpr size_t rbuf_bytes(int warps) { return (size_t)warps * 16 * RS * sizeof(float); }
+
+// FWHT: 6 warps, two CTAs per SM, next tile staged in shared memory by
+// cp.async; dense: 8 warps, one CTA per SM (the Pi limbs fill shared memory),
+// next tile prefetched into registers.
+__host__ __device__ constexpr int warps_for(bool dense) { return dense ? 8 : 6; }
+__host__ __device__ constexpr size_t stage_bytes(bool dense) {
+  return dense ? 0 : (size_t)warps_for(dense) * 8 * 32 * sizeof(uint4);
+}
+
+__host__ __device__ constexpr size_t smem_bytes(bool qjl, bool dense) {
+  return sizeof(Shared) + (qjl ? kSfragBytes + rbuf_bytes(warps_for(dense)) : 0) + (dense ? kPfragBytes : 0) +
+         stage_bytes(dense);
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint2 b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint2 b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ uint32_t f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Byte transpose across the 4 lanes t of a quad: byte k of v on lane t is
+// element (t, k); the result's byte s on lane t is element (s, t).
+__device__ __forceinline__ uint32_t quad_transpose(uint32_t v, int t) {
+  const uint32_t p = __shfl_xor_sync(0xffffffffu, v, 1);
+  const uint32_t a = (t & 1) ? p : v;
+  const uint32_t b = (t & 1) ? v : p;
+  const uint32_t k0 = t & 1;
+  const uint32_t u = __byte_perm(a, b, k0 | ((4 + k0) << 4) | ((k0 + 2) << 8) | ((6 + k0) << 12));
+  const uint32_t o = __shfl_xor_sync(0xffffffffu, u, 2);
+  return (t < 2) ? __byte_perm(u, o, 0x5410) : __byte_perm(o, u, 0x7632);
+}
+
+// B fragment of an m16n8k16 product: lane (g, t), register j, half e holds
+// k-row 2t + e + 8j of column g.  elem(L, n) returns the 16-bit pattern.
+template <class F>
+__device__ __forceinline__ uint2 make_frag(int lane, F&& elem) {
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t r[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) r[j] = elem(2 * t + 8 * j, g) | (elem(2 * t + 1 + 8 * j, g) << 16);
+  return make_uint2(r[0], r[1]);
+}
+
+// QJL: keys with the sketch; DENSE: dense rotation (else FWHT).  grid (x, Hkv).
+template <bool QJL, bool DENSE>
+__global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
+    quantize_warp_kernel(const __grid_constant__ KParams P, const __nv_bfloat16* __restrict__ x, long long n_vec,
+                         int is_key, uint32_t* __restrict__ codes, uint32_t* __restrict__ signs,
+                         float* __restrict__ norms, float* __restrict__ rnorms) {
+  constexpr int WARPS = warps_for(DENSE);
+  constexpr int NT = 32 * WARPS;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  unsigned char* dyn = smem_raw + sizeof(Shared);
+  uint2* sfrag = reinterpret_cast<uint2*>(dyn);                   // [16][KB][32]
+  float* rbuf = reinterpret_cast<float*>(dyn + kSfragBytes);      // [WARPS][16][RS]
+  uint2* pfrag = reinterpret_cast<uint2*>(dyn + (QJL ? kSfragBytes + rbuf_bytes(WARPS) : 0));  // [3][16][KB][32]
+  uint4* stage = reinterpret_cast<uint4*>(dyn + (QJL ? kSfragBytes + rbuf_bytes(WARPS) : 0));    // [WARPS][8][32]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  const int head = blockIdx.y;
+  const int bits = is_key ? P.kb : P.vb;
+  const int half = 1 << (bits - 1), levels = bits - 1;
+  const float* ctab = is_key ? P.kc : P.vc;
+  const float* ttab = is_key ? P.kt : P.vt;
+  const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
+  const float* S = QJL ? P.qjl_s + (size_t)head * D * D : nullptr;
+
+  // ---- per-CTA constants
+  if (tid < 8) {
+    sh.tpi[tid] = tid < half - 1 ? __float_as_int(ttab[half + tid]) : INT_MAX;
+    sh.cpos[tid] = tid < half ? ctab[half + tid] : 0.f;
+  }
+  if (!DENSE) {
+    for (int i = tid; i < KB * 2 * 32; i += NT) {
+      const int ln = i & 31, nt = (i >> 5) & 1, kk = i >> 6;
+      sh.hfrag[kk][nt][ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
+        const int in = blk_base(kk) + free_off(L);
+        const int out = 8 * (n >> 1) + 2 * nt + (n & 1);
+        const bool neg = (__ldg(rot + in) < 0.f) != (bool)(__popc(free_off(L) & out) & 1);
+        return neg ? 0xBF80u : 0x3F80u;
+      });
+    }
+  } else {
+    for (int i = tid; i < 16 * KB * 32; i += NT) {
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
+      const uint2 frag[3] = {
+          make_frag(ln, [&](int L, int n) -> uint32_t {
+            return bf16_bits(__ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L)));
+          }),
+          make_frag(ln, [&](int L, int n) -> uint32_t {
+            const float a = __ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L));
+            const float l0 = __bfloat162float(__float2bfloat16_rn(a));
+            return bf16_bits(a - l0);
+          }),
+          make_frag(ln, [&](int L, int n) -> uint32_t {
+            const float a = __ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L));
+            const float l0 = __bfloat162float(__float2bfloat16_rn(a));
+            const float l1 = __bfloat162float(__float2bfloat16_rn(a - l0));
+            return bf16_bits((a - l0) - l1);
+          })};
+#pragma unroll
+      for (int l = 0; l < 3; ++l) pfrag[((l * 16 + nt) * KB + kk) * 32 + ln] = frag[l];
+    }
+  }
+  if (QJL) {
+    for (int i = tid; i < 16 * KB * 32; i += NT) {
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
+      sfrag[(nt * KB + kk) * 32 + ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
+        return f16_bits(__ldg(S + (size_t)sk_out(nt, n) * D + blk_base(kk) + free_off(L)));
+      });
+    }
+    for (int c = warp; c < D; c += WARPS) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(S + (size_t)c * D) + lane);
+      float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      s2 = warp_sum_f(s2);
+      if (lane == 0) sh.snorm[c] = sqrtf(s2) * 1.0001f;
+    }
+  }
+  __syncthreads();
+
+  // ---- tiles of 16 tokens of this head
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 15) / 16;
+  const long long stride = (long long)gridDim.x * WARPS;
+  float* rb = rbuf + (size_t)warp * 16 * RS;
+  // |f16 product - fp32 product| <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||)
+  // (k2 covers f16 subnormals and the fp32 accumulation)
+  const float k1 = 1.05f / 1024.f, k2 = 4e-7f;
+
+  auto row_index = [&](long long mt, int R, long long& n) -> bool {
+    const long long tok = mt * 16 + g + 8 * R;
+    n = tok * P.hkv + head;
+    return tok < n_tok && n < n_vec;
+  };
+  // next tile: registers (dense) or this lane's own slots of the staging area
+  uint4 nxt[2][4];  // dense only
+  uint4* stg = stage + (size_t)warp * 8 * 32 + lane;  // slot k at stg[32 k]
+  auto load = [&](long long mt) {
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      long long n;
+      const bool ok = row_index(mt, R, n);
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * D) + t;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if constexpr (DENSE) nxt[R][m] = ok ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
+        else cp_async16(stg + 32 * (4 * R + m), src + 4 * m, ok ? 16 : 0);
+      }
+    }
+    if (!DENSE) cp_async_commit();
+  };
+  long long mt = (long long)blockIdx.x * WARPS + warp;
+  if (mt < n_tiles) load(mt);
+  for (; mt < n_tiles; mt += stride) {
+    uint4 X[2][4];
+    if (!DENSE) cp_async_wait_all();
+#pragma unroll
+    for (int R = 0; R < 2; ++R)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if constexpr (DENSE) X[R][m] = nxt[R][m];
+        else X[R][m] = stg[32 * (4 * R + m)];
+      }
+    if (mt + stride < n_tiles) load(mt + stride);
+
+    // norms of rows g (R = 0) and g + 8 (R = 1): squares of bf16 values are
+    // exact in fp32; a balanced tree of depth 7 sums them
+    float inv[2], nrm[2];
+    bool zero[2];
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      float part[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t w[4] = {X[R][m].x, X[R][m].y, X[R][m].z, X[R][m].w};
+        float q2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+          q2[k] = lo * lo + hi * hi;
+        }
+        part[m] = (q2[0] + q2[1]) + (q2[2] + q2[3]);
+      }
+      float s2 = (part[0] + part[1]) + (part[2] + part[3]);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+      const float n = sqrtf(s2);
+      zero[R] = n < kZeroNorm;
+      nrm[R] = zero[R] ? 0.f : n;
+      // z = sqrt(d) Pi x / n (dense) or H (sigma x) / n (FWHT): one division
+      // and one square root of the exact sum's fp32 value
+      inv[R] = zero[R] ? 0.f : sqrtf((DENSE ? (float)D : 1.0f) / s2);
+    }
+
+    // FWHT: acc[a][h][r] = row g + 8 (r >> 1), coordinate blk_base(a) + 8t + 2h + (r & 1)
+    float acc[KB][2][4];  // unused by the dense path
+    if constexpr (!DENSE) {
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) {
+        const uint4& u0 = X[0][kk >> 1];
+        const uint4& u1 = X[1][kk >> 1];
+        const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
+        const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[kk][h][r] = 0.f;
+          mma_bf16(acc[kk][h], a0, a1, a2, a3, sh.hfrag[kk][h][lane]);
+        }
+      }
+      // H_8 across the blocks
+#pragma unroll
+      for (int s = 1; s < KB; s <<= 1)
+#pragma unroll
+        for (int a = 0; a < KB; ++a)
+          if ((a & s) == 0)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const float p = acc[a][h][r], q = acc[a + s][h][r];
+                acc[a][h][r] = p + q;
+                acc[a + s][h][r] = p - q;
+              }
+    }
+
+    // codes: byte p of W[R][m] is plane p of this lane's byte of word m
+    uint32_t W[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+    uint32_t rA[KB][4];  // residual (f16) as A fragments of the sketch product
+    float rsum[2][4];    // ||r||^2 partial sums, combined as a balanced tree
+#pragma unroll
+    for (int a = 0; a < KB; ++a) {
+      float zr[2][4];  // [h][r]: pre-scale rotation outputs of block a
+      if constexpr (DENSE) {
+        // tiles 2a, 2a+1; leading limb split over even / odd k-blocks, small
+        // limbs in their own accumulators, summed in fp32 at the end
+        float c[4][2][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) c[i][h][r] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+          const uint4& u0 = X[0][kk >> 1];
+          const uint4& u1 = X[1][kk >> 1];
+          const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
+          const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int nt = 2 * a + h;
+            mma_bf16(c[kk & 1][h], a0, a1, a2, a3, pfrag[((0 * 16 + nt) * KB + kk) * 32 + lane]);
+            mma_bf16(c[2][h], a0, a1, a2, a3, pfrag[((1 * 16 + nt) * KB + kk) * 32 + lane]);
+            mma_bf16(c[3][h], a0, a1, a2, a3, pfrag[((2 * 16 + nt) * KB + kk) * 32 + lane]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) zr[h][r] = (c[0][h][r] + c[1][h][r]) + (c[2][h][r] + c[3][h][r]);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) zr[h][r] = acc[a][h][r];
+      }
+      float rv[2][4];  // [R][2h + e]
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int R = r >> 1, e = r & 1;
+          const float z = __fmaf_rn(zr[h][r], inv[R], 0.f);  // +0 for zero rows
+          const uint32_t zb = __float_as_uint(z);
+          const uint32_t neg = zb >> 31;
+          const int ai = (int)(zb & 0x7fffffffu) - (int)neg;  // for z < 0: |z| > t <=> ai >= bits(t)
+          int mag = 0;
+#pragma unroll
+          for (int l = 2; l >= 0; --l) {
+            if (l < levels) {
+              const int probe = mag + (1 << l);
+              mag = ai >= sh.tpi[probe - 1] ? probe : mag;
+            }
+          }
+          const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
+          const int pos = 4 * (a & 1) + 2 * h + e;
+          W[R][a >> 1] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
+          if (QJL) {
+            const float c = __uint_as_float(__float_as_uint(sh.cpos[mag]) ^ (neg << 31));
+            const float res = z - c;
+            rv[R][2 * h + e] = res;
+          }
+        }
+      if (QJL) {
+        // block sum (depth 2), then pairs of blocks, quads, all eight
+#pragma unroll
+        for (int R = 0; R < 2; ++R) {
+          const float b = (rv[R][0] * rv[R][0] + rv[R][1] * rv[R][1]) + (rv[R][2] * rv[R][2] + rv[R][3] * rv[R][3]);
+          if ((a & 1) == 0) rsum[R][a >> 1] = b;
+          else rsum[R][a >> 1] += b;
+          if ((a & 3) == 3) rsum[R][a >> 1 & 2] += rsum[R][(a >> 1 & 2) + 1];
+        }
+        const int c0 = blk_base(a) + 8 * t;
+#pragma unroll
+        for (int R = 0; R < 2; ++R)
+          *reinterpret_cast<float4*>(rb + (g + 8 * R) * RS + c0) = make_float4(rv[R][0], rv[R][1], rv[R][2], rv[R][3]);
+        rA[a][0] = pack_f16(rv[0][0], rv[0][1]);
+        rA[a][1] = pack_f16(rv[1][0], rv[1][1]);
+        rA[a][2] = pack_f16(rv[0][2], rv[0][3]);
+        rA[a][3] = pack_f16(rv[1][2], rv[1][3]);
+      }
+    }
+
+    long long nrow[2];
+    bool okrow[2];
+#pragma unroll
+    for (int R = 0; R < 2; ++R) okrow[R] = row_index(mt, R, nrow[R]);
+
+    // packed code words: lane t gets plane t of words 0..3
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      uint4 cw;
+      cw.x = quad_transpose(W[R][0], t);
+      cw.y = quad_transpose(W[R][1], t);
+      cw.z = quad_transpose(W[R][2], t);
+      cw.w = quad_transpose(W[R][3], t);
+      if (okrow[R] && t < bits) reinterpret_cast<uint4*>(codes + (size_t)nrow[R] * bits * 4)[t] = cw;
+      if (okrow[R] && t == 0) norms[nrow[R]] = nrm[R];
+    }
+
+    if (QJL) {
+      float rn[2], gam[2], bA[2], bB[2];
+#pragma unroll
+      for (int R = 0; R < 2; ++R) {
+        float s2 = rsum[R][0] + rsum[R][2];
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+        gam[R] = sqrtf(s2 * (1.0f / D));  // exact scaling by a power of two
+        rn[R] = sqrtf(s2);
+        bA[R] = fmaf(k1, rn[R], k2);
+        bB[R] = k2 * rn[R];
+      }
+      __syncwarp();  // residual rows visible to the whole warp
+      uint32_t SB[2] = {0u, 0u};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float sacc[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) sacc[q][r] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], sfrag[((4 * w + q) * KB + kk) * 32 + lane]);
+        const float4 sn0 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t]);
+        const float4 sn1 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t + 4]);
+        const float sn[8] = {sn0.x, sn0.y, sn0.z, sn0.w, sn1.x, sn1.y, sn1.z, sn1.w};
+        uint32_t sb = 0, pend = 0;  // bit 8R + 2q + e
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int R = r >> 1, e = r & 1, bit = 8 * R + 2 * q + e;
+            const float v = sacc[q][r];
+            sb |= (uint32_t)(v >= 0.f || zero[R]) << bit;
+            pend |= (uint32_t)(!zero[R] && fabsf(v) < fmaf(sn[2 * q + e], bA[R], bB[R] + k2)) << bit;
+          }
+        // fp32 recomputation of the uncertain entries, one per pass of the warp
+        while (true) {
+          const unsigned ball = __ballot_sync(0xffffffffu, pend != 0);
+          if (ball == 0) break;
+          const int src = __ffs(ball) - 1;
+          const int bit = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
+          const int row = (src >> 2) + 8 * (bit >> 3);
+          const int c = 32 * w + 8 * (src & 3) + (bit & 7);
+          const float4 rr = *reinterpret_cast<const float4*>(rb + row * RS + 4 * lane);
+          const float4 ss = __ldg(reinterpret_cast<const float4*>(S + (size_t)c * D) + lane);
+          float dsum = rr.x * ss.x;
+          dsum = fmaf(rr.y, ss.y, dsum);
+          dsum = fmaf(rr.z, ss.z, dsum);
+          dsum = fmaf(rr.w, ss.w, dsum);
+          dsum = warp_sum_f(dsum);
+          if (lane == src) {
+            sb = (sb & ~(1u << bit)) | ((uint32_t)(dsum >= 0.f) << bit);
+            pend &= ~(1u << bit);
+          }
+        }
+        SB[0] |= (sb & 0xffu) << (8 * w);
+        SB[1] |= ((sb >> 8) & 0xffu) << (8 * w);
+      }
+#pragma unroll
+      for (int R = 0; R < 2; ++R) {
+        const uint32_t word = quad_transpose(SB[R], t);
+        if (okrow[R]) signs[(size_t)nrow[R] * 4 + t] = word;
+        if (okrow[R] && t == 0) rnorms[nrow[R]] = zero[R] ? 0.f : gam[R];
+      }
+      __syncwarp();  // the residual buffer is rewritten by the next tile
+    }
+  }
+}
+
+}  // namespace wq
+}  // namespace tq

@@ -95,7 +95,8 @@ def compare_records(ora, g_idx, g_norm, g_signs=None, g_rnorm=None, is_key=True,
         stats["exempt"] = stats.get("exempt", 0) + n_exempt_codes
         stats["codes"] = stats.get("codes", 0) + total
         stats["flipped"] = stats.get("flipped", 0) + int(diff.sum())
-    assert n_exempt_codes <= max(3, EXEMPT_FRACTION * total), (n_exempt_codes, total)
+    if stats is None:  # callers that pass stats check the fraction over the whole call
+        assert n_exempt_codes <= max(3, EXEMPT_FRACTION * total), (n_exempt_codes, total)
     return {"exempt": n_exempt_codes, "flipped": int(diff.sum()), "total": total}
 
 

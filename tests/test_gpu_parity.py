@@ -47,6 +47,14 @@ CASES = [
     ("bulk", dict(ctx=70)),
     ("tiny", dict(ctx=50, kind=SK.FWHT, key_bits=1, value_bits=1)),
     ("qwen", dict(batch=1, ctx=40, kind=SK.DENSE, key_bits=4, value_bits=3, key_qjl=False)),
+    # d = 128 bf16: the tensor-core bulk path (several tiles per warp, ragged tail)
+    ("bulk", dict(ctx=300, kind=SK.FWHT)),
+    ("bulk", dict(ctx=4100)),
+    ("llama", dict(batch=2, ctx=45, kind=SK.FWHT, key_bits=2, value_bits=1)),
+    ("bulk", dict(ctx=400, key_bits=4, value_bits=2)),
+    ("bulk", dict(ctx=5000, kind=SK.FWHT, key_bits=4, value_bits=3)),
+    ("bulk", dict(ctx=20, kind=SK.FWHT, key_bits=1, key_qjl=False, value_bits=4)),
+    ("bulk", dict(ctx=21, key_bits=2, key_qjl=False, value_bits=1)),
 ]
 
 
@@ -113,6 +121,51 @@ def test_quantize_zero_and_tiny_vectors(tq):
     zero_rows = [0, 1]
     for r in zero_rows:
         assert norms[r].item() == 0.0 and rn[r].item() == 0.0
+        assert np.all(signs[r].cpu().numpy().view(np.uint32) == 0xFFFFFFFF)
+
+
+@pytest.mark.parametrize("kind", [SK.FWHT, SK.DENSE])
+def test_quantize_zero_and_tiny_vectors_bf16(tq, kind):
+    """The same crafted rows through the d = 128 bf16 path (rows rounded to
+    bf16 first, so both sides see the same inputs).  A constant row puts many
+    FWHT coordinates exactly on the z = 0 boundary, where the fp64 oracle
+    lands at +-1e-17: those are compared under the boundary exemption, the
+    zero rows exactly."""
+    w = SK.workload("bulk", ctx=4, kind=kind)
+    L, O = _layer(tq, w)
+    x = np.zeros((4 * w.n_kv_heads + 3, w.d))
+    x[1, 5] = 5e-8
+    x[2, :] = 1e-3
+    x[3, 7] = 1.0
+    x[4 * w.n_kv_heads + 1, :] = -2.0
+    xt = SK.to_torch(x, "bf16").cuda()
+    x = xt.float().cpu().numpy().astype(np.float64)
+    E = w.d // 32
+    n = x.shape[0]
+    codes = torch.zeros(n, w.key_bits * E, dtype=torch.int32, device="cuda")
+    signs = torch.zeros(n, E, dtype=torch.int32, device="cuda")
+    norms = torch.zeros(n, device="cuda")
+    rn = torch.zeros(n, device="cuda")
+    tq.quantize_keys(L.params, xt, n, codes, signs, norms, rn)
+    vcodes = torch.zeros(n, w.value_bits * E, dtype=torch.int32, device="cuda")
+    vnorms = torch.zeros(n, device="cuda")
+    tq.quantize_values(L.params, xt, n, vcodes, vnorms)
+    torch.cuda.synchronize()
+    heads = np.arange(n) % w.n_kv_heads
+    stats = {}
+    for h in range(w.n_kv_heads):
+        sel = heads == h
+        ok = O.keys(x[sel], h)
+        g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d)
+        g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d)
+        PY.compare_records(ok, g_idx, norms.cpu().numpy()[sel], g_s, rn.cpu().numpy()[sel], True, stats)
+        ov = O.values(x[sel], h)
+        g_v = PY.unpack_flat_codes(vcodes.cpu().numpy().view(np.uint32)[sel], w.value_bits, w.d)
+        PY.compare_records(ov, g_v, vnorms.cpu().numpy()[sel], is_key=False, stats=stats)
+        zr = np.where(np.all(x[sel] == 0, axis=1) | (np.linalg.norm(x[sel], axis=1) < 1e-7))[0]
+        assert np.array_equal(g_idx[zr], ok["idx"][zr]) and np.array_equal(g_v[zr], ov["idx"][zr])
+    for r in (0, 1):
+        assert norms[r].item() == 0.0 and rn[r].item() == 0.0 and vnorms[r].item() == 0.0
         assert np.all(signs[r].cpu().numpy().view(np.uint32) == 0xFFFFFFFF)
 
 
@@ -198,6 +251,8 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
                 slots = [p % pc.ring for p in range(nc, T)]
                 assert np.array_equal(ring[slots], win_k[h])
                 assert np.array_equal(pc.win_v[b, h].cpu().numpy()[slots], win_v[h])
+        if stats:
+            assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
         comp = PY.stack_comp(recs_k, recs_v) if nc else None
         r = PY.decode_reference(O, q[b], comp, win_k if T > nc else None, win_v if T > nc else None, scale)
         g_sc = scores[b].cpu().numpy()
