@@ -437,12 +437,12 @@ static bool antisymmetric(const float* c, const float* t, int bits) {
   return true;
 }
 
-template <bool QJL, bool DENSE>
+template <int BITS, bool QJL, bool DENSE>
 static cudaError_t launch_quantize_warp(const KParams& P, const void* x, long long n_vec, bool is_key,
                                         uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
                                         cudaStream_t st) {
-  constexpr int warps = wq::warps_for(DENSE);
-  auto kern = wq::quantize_warp_kernel<QJL, DENSE>;
+  constexpr int warps = wq::warps_for(QJL, DENSE);
+  auto kern = wq::quantize_warp_kernel<BITS, QJL, DENSE>;
   const size_t sm = wq::smem_bytes(QJL, DENSE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
@@ -461,16 +461,29 @@ static cudaError_t launch_quantize_warp(const KParams& P, const void* x, long lo
   return cudaGetLastError();
 }
 
+template <bool QJL, bool DENSE>
+static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const void* x, long long n_vec,
+                                             bool is_key, uint32_t* codes, uint32_t* signs, float* norms,
+                                             float* rnorms, cudaStream_t st) {
+  switch (bits) {
+    case 1: return launch_quantize_warp<1, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 2: return launch_quantize_warp<2, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 3: return launch_quantize_warp<3, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    default: return launch_quantize_warp<4, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+  }
+}
+
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
-  if (P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && ((uintptr_t)codes & 15) == 0) {
+  if (P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0) {
     const bool qjl = is_key && P.kqjl;
+    const int bits = is_key ? P.kb : P.vb;
     if (P.kind == TQ_FWHT)
-      return qjl ? launch_quantize_warp<true, false>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-                 : launch_quantize_warp<false, false>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    return qjl ? launch_quantize_warp<true, true>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-               : launch_quantize_warp<false, true>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+      return qjl ? launch_quantize_warp_bits<true, false>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+                 : launch_quantize_warp_bits<false, false>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    return qjl ? launch_quantize_warp_bits<true, true>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+               : launch_quantize_warp_bits<false, true>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
   }
   if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
   return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);

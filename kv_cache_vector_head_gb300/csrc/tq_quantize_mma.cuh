@@ -6,29 +6,32 @@
 // out for mma.m16n8k16:
 //
 //   * one warp owns a tile of 16 vectors (the M rows of the MMAs) of one kv
-//     head and keeps it in registers from the load to the stores;
-//   * coordinates are permuted inside each 16-wide k-block so that one
-//     16-byte load per lane yields two A fragments; the same permutation
-//     makes every lane hold 4 consecutive coordinates per block of the
-//     outputs, so a lane owns one byte of every packed 32-bit word;
+//     head; coordinates are permuted inside each 16-wide k-block so that one
+//     16-byte load per lane yields two A fragments, and so that every lane
+//     holds 4 consecutive coordinates per block of the outputs: a lane owns
+//     one byte of every packed 32-bit word (a byte transpose across the quad
+//     assembles the words);
 //   * FWHT: H_128 = H_8 (x) H_16 over a split of the 7 index bits; the
 //     H_16 factor (with the sign flips folded in) is one bf16 MMA per
 //     k-block (+-1 and bf16 inputs are exact, accumulation in fp32), the
 //     H_8 factor a register butterfly across the 8 accumulator blocks;
 //   * dense Pi: bf16 inputs against Pi split in three bf16 limbs (24
 //     significant bits), fragments staged once per CTA in shared memory;
-//   * QJL: S r as one f16 MMA (r and S rounded to f16).  Every entry whose
-//     magnitude is below a certified bound of that rounding,
-//     2^-10 (1 + eps) ||r|| ||S_c||, is recomputed in fp32 by the warp, so
-//     every sign is the sign of an fp32 product;
-//   * norms in fp32 with balanced summation trees of depth 7 (relative
-//     error at most 7 u before the square root halves it), scales taken as
+//   * codes: sign and magnitude, the magnitude by binary search over the
+//     positive boundaries held in registers (bit width a template
+//     parameter); planes packed four at a time with one multiply;
+//   * QJL: S r as three f16 MMAs over hi / lo limbs of r and S (hi*hi +
+//     hi*lo + lo*hi).  Every entry whose magnitude is below a certified
+//     bound of the limb and accumulation errors (6e-5 ||r|| ||S_c||, a few
+//     per thousand vectors) is recomputed in fp32 by the warp from the
+//     limbs, so every sign is that of the fp32 product up to 2^-21 relative;
+//   * norms in fp32 with balanced summation trees (relative error at most
+//     about 8 u before the square root halves it), scales taken as
 //     sqrt(d / s) and sqrt(s_r / d) (d a power of two).
 //
 // Requirements checked by the launcher: d = 128, bf16 input, 16-byte aligned
-// input and code arrays, codebook tables antisymmetric (c[half+m] =
-// -c[half-1-m], middle boundary 0), which lets the code be taken as a sign
-// and a magnitude found by binary search over the positive boundaries.
+// input, codebook tables antisymmetric (c[half+m] = -c[half-1-m], middle
+// boundary 0, increasing boundaries).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,7 +45,6 @@ namespace wq {
 
 constexpr int D = 128;
 constexpr int KB = D / 16;     // k-blocks
-constexpr int RS = D + 4;      // row stride (floats) of the per-warp residual buffer
 
 // Permuted coordinates.  Logical index L in [0, 16) of k-block kk sits at
 // blk_base(kk) + free_off(L): bits 2, 5, 6 of the coordinate come from the
@@ -59,26 +61,31 @@ __host__ __device__ constexpr int sk_out(int nt, int n) {
 }
 
 struct Shared {
-  int tpi[8];                  // positive boundaries as int bits, ascending (INT_MAX pads)
-  float cpos[8];               // positive centroids
   float snorm[D];              // ||S_c|| (rounded up)
   uint2 hfrag[KB][2][32];      // FWHT H_16 * sigma fragments (bf16)
 };
-constexpr size_t kSfragBytes = (size_t)16 * KB * 32 * sizeof(uint2);     // S (f16)
+constexpr size_t kSfragBytes = (size_t)2 * 16 * KB * 32 * sizeof(uint2);  // S as f16 hi and lo limbs
 constexpr size_t kPfragBytes = (size_t)3 * 16 * KB * 32 * sizeof(uint2);  // Pi limbs (bf16)
-__host__ __device__ constexpr size_t rbuf_bytes(int warps) { return (size_t)warps * 16 * RS * sizeof(float); }
+// Per-warp block buffer: [2][KB][32] uint4.  FWHT: the rotated tile (R = 0
+// rows in half 0, R = 1 rows in half 1); keys: then the residual's f16 hi
+// and lo limbs in A-fragment order, written over the same slots.
+constexpr size_t kBlkBytes = (size_t)2 * KB * 32 * sizeof(uint4);
 
-// FWHT: 6 warps, two CTAs per SM, next tile staged in shared memory by
-// cp.async; dense: 8 warps, one CTA per SM (the Pi limbs fill shared memory),
-// next tile prefetched into registers.
-__host__ __device__ constexpr int warps_for(bool dense) { return dense ? 8 : 6; }
-__host__ __device__ constexpr size_t stage_bytes(bool dense) {
-  return dense ? 0 : (size_t)warps_for(dense) * 8 * 32 * sizeof(uint4);
+// FWHT: 12 warps, next tile staged in shared memory by cp.async; dense: the
+// Pi limbs fill most of shared memory (7 warps with the sketch, 8 and two
+// CTAs per SM without), next tile prefetched into registers.
+__host__ __device__ constexpr int warps_for(bool qjl, bool dense) { return dense ? (qjl ? 7 : 8) : 12; }
+__host__ __device__ constexpr int ctas_for(bool qjl, bool dense) { return dense && !qjl ? 2 : 1; }
+__host__ __device__ constexpr size_t blk_bytes(bool qjl, bool dense) {
+  return (qjl || !dense) ? (size_t)warps_for(qjl, dense) * kBlkBytes : 0;
+}
+__host__ __device__ constexpr size_t stage_bytes(bool qjl, bool dense) {
+  return dense ? 0 : (size_t)warps_for(qjl, dense) * 8 * 32 * sizeof(uint4);
 }
 
 __host__ __device__ constexpr size_t smem_bytes(bool qjl, bool dense) {
-  return sizeof(Shared) + (qjl ? kSfragBytes + rbuf_bytes(warps_for(dense)) : 0) + (dense ? kPfragBytes : 0) +
-         stage_bytes(dense);
+  return sizeof(Shared) + (qjl ? kSfragBytes : 0) + (dense ? kPfragBytes : 0) + blk_bytes(qjl, dense) +
+         stage_bytes(qjl, dense);
 }
 
 // 16-byte global -> shared copy; src_bytes = 0 fills zeros.
@@ -137,37 +144,77 @@ __device__ __forceinline__ uint2 make_frag(int lane, F&& elem) {
   return make_uint2(r[0], r[1]);
 }
 
+// Positive half of an antisymmetric codebook: boundaries (as int bits,
+// ascending) and centroids.
+template <int BITS>
+struct Book {
+  int tp[BITS > 1 ? (1 << (BITS - 1)) - 1 : 1];
+  float cp[1 << (BITS - 1)];
+};
+
+// Number of positive boundaries t with ai >= bits(t) (binary search).
+template <int BITS>
+__device__ __forceinline__ int magnitude(int ai, const Book<BITS>& b) {
+  if constexpr (BITS == 1) {
+    return 0;
+  } else if constexpr (BITS == 2) {
+    return ai >= b.tp[0] ? 1 : 0;
+  } else if constexpr (BITS == 3) {
+    const int m1 = ai >= b.tp[1] ? 2 : 0;
+    return m1 + (ai >= (m1 ? b.tp[2] : b.tp[0]) ? 1 : 0);
+  } else {
+    const int m2 = ai >= b.tp[3] ? 4 : 0;
+    const int m1 = ai >= (m2 ? b.tp[5] : b.tp[1]) ? 2 : 0;
+    const int th = m2 ? (m1 ? b.tp[6] : b.tp[4]) : (m1 ? b.tp[2] : b.tp[0]);
+    return m2 + m1 + (ai >= th ? 1 : 0);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ float centroid_pos(int mag, const Book<BITS>& b) {
+  float c = b.cp[0];
+#pragma unroll
+  for (int i = 1; i < (1 << (BITS - 1)); ++i) c = mag == i ? b.cp[i] : c;
+  return c;
+}
+
+__device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
+__device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
 // QJL: keys with the sketch; DENSE: dense rotation (else FWHT).  grid (x, Hkv).
-template <bool QJL, bool DENSE>
-__global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
+template <int BITS, bool QJL, bool DENSE>
+__global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENSE))
     quantize_warp_kernel(const __grid_constant__ KParams P, const __nv_bfloat16* __restrict__ x, long long n_vec,
                          int is_key, uint32_t* __restrict__ codes, uint32_t* __restrict__ signs,
                          float* __restrict__ norms, float* __restrict__ rnorms) {
-  constexpr int WARPS = warps_for(DENSE);
+  constexpr int WARPS = warps_for(QJL, DENSE);
   constexpr int NT = 32 * WARPS;
+  constexpr int HALF = 1 << (BITS - 1);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned char* dyn = smem_raw + sizeof(Shared);
-  uint2* sfrag = reinterpret_cast<uint2*>(dyn);                   // [16][KB][32]
-  float* rbuf = reinterpret_cast<float*>(dyn + kSfragBytes);      // [WARPS][16][RS]
-  uint2* pfrag = reinterpret_cast<uint2*>(dyn + (QJL ? kSfragBytes + rbuf_bytes(WARPS) : 0));  // [3][16][KB][32]
-  uint4* stage = reinterpret_cast<uint4*>(dyn + (QJL ? kSfragBytes + rbuf_bytes(WARPS) : 0));    // [WARPS][8][32]
+  uint2* sfrag = reinterpret_cast<uint2*>(dyn);  // [2 limbs][16][KB][32]
+  dyn += QJL ? kSfragBytes : 0;
+  uint2* pfrag = reinterpret_cast<uint2*>(dyn);  // [3][16][KB][32]
+  dyn += DENSE ? kPfragBytes : 0;
+  uint4* blk = reinterpret_cast<uint4*>(dyn);    // [WARPS][2][KB][32]
+  dyn += blk_bytes(QJL, DENSE);
+  uint4* stage = reinterpret_cast<uint4*>(dyn);  // [WARPS][8][32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int head = blockIdx.y;
-  const int bits = is_key ? P.kb : P.vb;
-  const int half = 1 << (bits - 1), levels = bits - 1;
   const float* ctab = is_key ? P.kc : P.vc;
   const float* ttab = is_key ? P.kt : P.vt;
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
   const float* S = QJL ? P.qjl_s + (size_t)head * D * D : nullptr;
+  Book<BITS> bk;
+#pragma unroll
+  for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(ttab[HALF + k]);
+#pragma unroll
+  for (int m = 0; m < HALF; ++m) bk.cp[m] = ctab[HALF + m];
 
   // ---- per-CTA constants
-  if (tid < 8) {
-    sh.tpi[tid] = tid < half - 1 ? __float_as_int(ttab[half + tid]) : INT_MAX;
-    sh.cpos[tid] = tid < half ? ctab[half + tid] : 0.f;
-  }
-  if (!DENSE) {
+  if constexpr (!DENSE) {
     for (int i = tid; i < KB * 2 * 32; i += NT) {
       const int ln = i & 31, nt = (i >> 5) & 1, kk = i >> 6;
       sh.hfrag[kk][nt][ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
@@ -199,11 +246,15 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
       for (int l = 0; l < 3; ++l) pfrag[((l * 16 + nt) * KB + kk) * 32 + ln] = frag[l];
     }
   }
-  if (QJL) {
+  if constexpr (QJL) {
     for (int i = tid; i < 16 * KB * 32; i += NT) {
       const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
       sfrag[(nt * KB + kk) * 32 + ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
         return f16_bits(__ldg(S + (size_t)sk_out(nt, n) * D + blk_base(kk) + free_off(L)));
+      });
+      sfrag[((16 + nt) * KB + kk) * 32 + ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
+        const float v = __ldg(S + (size_t)sk_out(nt, n) * D + blk_base(kk) + free_off(L));
+        return f16_bits(v - __half2float(__float2half_rn(v)));
       });
     }
     for (int c = warp; c < D; c += WARPS) {
@@ -219,10 +270,14 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
   const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
   const long long n_tiles = (n_tok + 15) / 16;
   const long long stride = (long long)gridDim.x * WARPS;
-  float* rb = rbuf + (size_t)warp * 16 * RS;
-  // |f16 product - fp32 product| <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||)
-  // (k2 covers f16 subnormals and the fp32 accumulation)
-  const float k1 = 1.05f / 1024.f, k2 = 4e-7f;
+  uint4* wb = blk + (size_t)warp * 2 * KB * 32;  // this warp's block buffer: wb[(half * KB + a) * 32 + lane]
+  // |three-limb f16 product - exact product of the fp32 values|
+  //   <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||):
+  // k1 covers the dropped lo*lo term and the limb roundings (3 * 2^-22) and
+  // the fp32 accumulation over 24 chained MMAs even if every MMA truncated
+  // each of its 17 addends by one unit in the last place (24 * 17 * 2^-23);
+  // k2 covers f16 subnormal limbs (2^-25 per element, times sqrt(d))
+  const float k1 = 6e-5f, k2 = 4e-7f;
 
   auto row_index = [&](long long mt, int R, long long& n) -> bool {
     const long long tok = mt * 16 + g + 8 * R;
@@ -244,13 +299,13 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
         else cp_async16(stg + 32 * (4 * R + m), src + 4 * m, ok ? 16 : 0);
       }
     }
-    if (!DENSE) cp_async_commit();
+    if constexpr (!DENSE) cp_async_commit();
   };
   long long mt = (long long)blockIdx.x * WARPS + warp;
   if (mt < n_tiles) load(mt);
   for (; mt < n_tiles; mt += stride) {
     uint4 X[2][4];
-    if (!DENSE) cp_async_wait_all();
+    if constexpr (!DENSE) cp_async_wait_all();
 #pragma unroll
     for (int R = 0; R < 2; ++R)
 #pragma unroll
@@ -259,6 +314,11 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
         else X[R][m] = stg[32 * (4 * R + m)];
       }
     if (mt + stride < n_tiles) load(mt + stride);
+
+    long long nrow[2];
+    bool okrow[2];
+#pragma unroll
+    for (int R = 0; R < 2; ++R) okrow[R] = row_index(mt, R, nrow[R]);
 
     // norms of rows g (R = 0) and g + 8 (R = 1): squares of bf16 values are
     // exact in fp32; a balanced tree of depth 7 sums them
@@ -285,13 +345,15 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
       zero[R] = n < kZeroNorm;
       nrm[R] = zero[R] ? 0.f : n;
       // z = sqrt(d) Pi x / n (dense) or H (sigma x) / n (FWHT): one division
-      // and one square root of the exact sum's fp32 value
+      // and one square root of the sum's fp32 value
       inv[R] = zero[R] ? 0.f : sqrtf((DENSE ? (float)D : 1.0f) / s2);
+      if (okrow[R] && t == 0) norms[nrow[R]] = nrm[R];
     }
 
-    // FWHT: acc[a][h][r] = row g + 8 (r >> 1), coordinate blk_base(a) + 8t + 2h + (r & 1)
-    float acc[KB][2][4];  // unused by the dense path
     if constexpr (!DENSE) {
+      // FWHT: H_16 factor per k-block on tensor cores, H_8 across the blocks,
+      // then the rotated tile into the block buffer
+      float acc[KB][2][4];
 #pragma unroll
       for (int kk = 0; kk < KB; ++kk) {
         const uint4& u0 = X[0][kk >> 1];
@@ -305,7 +367,6 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
           mma_bf16(acc[kk][h], a0, a1, a2, a3, sh.hfrag[kk][h][lane]);
         }
       }
-      // H_8 across the blocks
 #pragma unroll
       for (int s = 1; s < KB; s <<= 1)
 #pragma unroll
@@ -319,128 +380,127 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
                 acc[a][h][r] = p + q;
                 acc[a + s][h][r] = p - q;
               }
+#pragma unroll
+      for (int a = 0; a < KB; ++a) {
+        wb[(0 * KB + a) * 32 + lane] = make_uint4(__float_as_uint(acc[a][0][0]), __float_as_uint(acc[a][0][1]),
+                                                  __float_as_uint(acc[a][1][0]), __float_as_uint(acc[a][1][1]));
+        wb[(1 * KB + a) * 32 + lane] = make_uint4(__float_as_uint(acc[a][0][2]), __float_as_uint(acc[a][0][3]),
+                                                  __float_as_uint(acc[a][1][2]), __float_as_uint(acc[a][1][3]));
+      }
     }
 
-    // codes: byte p of W[R][m] is plane p of this lane's byte of word m
-    uint32_t W[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
-    uint32_t rA[KB][4];  // residual (f16) as A fragments of the sketch product
-    float rsum[2][4];    // ||r||^2 partial sums, combined as a balanced tree
+    // codes, two blocks (one packed word) per pass
+    float rs[2] = {0.f, 0.f};  // ||r||^2: block sums, pairs, then the four words in turn
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      uint32_t Wm[2] = {0u, 0u};  // byte p: plane p of this lane's byte of word m
+      float pr[2] = {0.f, 0.f};
 #pragma unroll
-    for (int a = 0; a < KB; ++a) {
-      float zr[2][4];  // [h][r]: pre-scale rotation outputs of block a
-      if constexpr (DENSE) {
-        // tiles 2a, 2a+1; leading limb split over even / odd k-blocks, small
-        // limbs in their own accumulators, summed in fp32 at the end
-        float c[4][2][4];
+      for (int hh = 0; hh < 2; ++hh) {
+        const int a = 2 * m + hh;
+        float zr[2][4];  // [R][2h + e], before the 1 / n scale
+        if constexpr (DENSE) {
+          // tiles 2a, 2a+1; the leading limb split over even / odd k-blocks,
+          // the small limbs in their own accumulators
+          float c[4][2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) c[i][h][r] = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < KB; ++kk) {
+            const uint4& u0 = X[0][kk >> 1];
+            const uint4& u1 = X[1][kk >> 1];
+            const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
+            const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint2* pf = pfrag + ((2 * a + h) * KB + kk) * 32 + lane;
+              mma_bf16(c[kk & 1][h], a0, a1, a2, a3, pf[0]);
+              mma_bf16(c[2][h], a0, a1, a2, a3, pf[16 * KB * 32]);
+              mma_bf16(c[3][h], a0, a1, a2, a3, pf[2 * 16 * KB * 32]);
+            }
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) c[i][h][r] = 0.f;
+            for (int r = 0; r < 4; ++r)
+              zr[r >> 1][2 * h + (r & 1)] = (c[0][h][r] + c[1][h][r]) + (c[2][h][r] + c[3][h][r]);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < KB; ++kk) {
-          const uint4& u0 = X[0][kk >> 1];
-          const uint4& u1 = X[1][kk >> 1];
-          const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
-          const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int nt = 2 * a + h;
-            mma_bf16(c[kk & 1][h], a0, a1, a2, a3, pfrag[((0 * 16 + nt) * KB + kk) * 32 + lane]);
-            mma_bf16(c[2][h], a0, a1, a2, a3, pfrag[((1 * 16 + nt) * KB + kk) * 32 + lane]);
-            mma_bf16(c[3][h], a0, a1, a2, a3, pfrag[((2 * 16 + nt) * KB + kk) * 32 + lane]);
+          for (int R = 0; R < 2; ++R) {
+            const uint4 v = wb[(R * KB + a) * 32 + lane];
+            zr[R][0] = __uint_as_float(v.x);
+            zr[R][1] = __uint_as_float(v.y);
+            zr[R][2] = __uint_as_float(v.z);
+            zr[R][3] = __uint_as_float(v.w);
           }
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) zr[h][r] = (c[0][h][r] + c[1][h][r]) + (c[2][h][r] + c[3][h][r]);
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) zr[h][r] = acc[a][h][r];
-      }
-      float rv[2][4];  // [R][2h + e]
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int R = r >> 1, e = r & 1;
-          const float z = __fmaf_rn(zr[h][r], inv[R], 0.f);  // +0 for zero rows
-          const uint32_t zb = __float_as_uint(z);
-          const uint32_t neg = zb >> 31;
-          const int ai = (int)(zb & 0x7fffffffu) - (int)neg;  // for z < 0: |z| > t <=> ai >= bits(t)
-          int mag = 0;
-#pragma unroll
-          for (int l = 2; l >= 0; --l) {
-            if (l < levels) {
-              const int probe = mag + (1 << l);
-              mag = ai >= sh.tpi[probe - 1] ? probe : mag;
-            }
-          }
-          const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
-          const int pos = 4 * (a & 1) + 2 * h + e;
-          W[R][a >> 1] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
-          if (QJL) {
-            const float c = __uint_as_float(__float_as_uint(sh.cpos[mag]) ^ (neg << 31));
-            const float res = z - c;
-            rv[R][2 * h + e] = res;
-          }
-        }
-      if (QJL) {
-        // block sum (depth 2), then pairs of blocks, quads, all eight
-#pragma unroll
-        for (int R = 0; R < 2; ++R) {
-          const float b = (rv[R][0] * rv[R][0] + rv[R][1] * rv[R][1]) + (rv[R][2] * rv[R][2] + rv[R][3] * rv[R][3]);
-          if ((a & 1) == 0) rsum[R][a >> 1] = b;
-          else rsum[R][a >> 1] += b;
-          if ((a & 3) == 3) rsum[R][a >> 1 & 2] += rsum[R][(a >> 1 & 2) + 1];
-        }
-        const int c0 = blk_base(a) + 8 * t;
+        float rv[2][4];
 #pragma unroll
         for (int R = 0; R < 2; ++R)
-          *reinterpret_cast<float4*>(rb + (g + 8 * R) * RS + c0) = make_float4(rv[R][0], rv[R][1], rv[R][2], rv[R][3]);
-        rA[a][0] = pack_f16(rv[0][0], rv[0][1]);
-        rA[a][1] = pack_f16(rv[1][0], rv[1][1]);
-        rA[a][2] = pack_f16(rv[0][2], rv[0][3]);
-        rA[a][3] = pack_f16(rv[1][2], rv[1][3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);  // +0 for zero rows
+            const uint32_t zb = __float_as_uint(z);
+            const uint32_t neg = zb >> 31;
+            const int ai = (int)(zb & 0x7fffffffu) - (int)neg;  // for z < 0: |z| > t <=> ai >= bits(t)
+            const int mag = magnitude<BITS>(ai, bk);
+            const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
+            const int pos = 4 * hh + i;  // coordinate blk_base(a) + 8t + i is bit 8t + 4hh + i of word m
+            Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
+            if constexpr (QJL) rv[R][i] = z - __uint_as_float(__float_as_uint(centroid_pos<BITS>(mag, bk)) ^ (neg << 31));
+          }
+        if constexpr (QJL) {
+          // residual limbs in A-fragment order (rows g, g+8; coordinate pairs 8t+{0,1}, 8t+{2,3})
+          const float2 p0 = make_float2(rv[0][0], rv[0][1]), p1 = make_float2(rv[1][0], rv[1][1]);
+          const float2 p2 = make_float2(rv[0][2], rv[0][3]), p3 = make_float2(rv[1][2], rv[1][3]);
+          const uint32_t h0 = pack_f16(p0.x, p0.y), h1 = pack_f16(p1.x, p1.y);
+          const uint32_t h2 = pack_f16(p2.x, p2.y), h3 = pack_f16(p3.x, p3.y);
+          wb[(0 * KB + a) * 32 + lane] = make_uint4(h0, h1, h2, h3);
+          wb[(1 * KB + a) * 32 + lane] =
+              make_uint4(pack_f16(p0.x - f16lo(h0), p0.y - f16hi(h0)), pack_f16(p1.x - f16lo(h1), p1.y - f16hi(h1)),
+                         pack_f16(p2.x - f16lo(h2), p2.y - f16hi(h2)), pack_f16(p3.x - f16lo(h3), p3.y - f16hi(h3)));
+#pragma unroll
+          for (int R = 0; R < 2; ++R)
+            pr[R] += (rv[R][0] * rv[R][0] + rv[R][1] * rv[R][1]) + (rv[R][2] * rv[R][2] + rv[R][3] * rv[R][3]);
+        }
+      }
+#pragma unroll
+      for (int R = 0; R < 2; ++R) {
+        rs[R] += pr[R];
+        const uint32_t word = quad_transpose(Wm[R], t);  // plane t of word m
+        if (okrow[R] && t < BITS) codes[(size_t)nrow[R] * BITS * 4 + t * 4 + m] = word;
       }
     }
 
-    long long nrow[2];
-    bool okrow[2];
-#pragma unroll
-    for (int R = 0; R < 2; ++R) okrow[R] = row_index(mt, R, nrow[R]);
-
-    // packed code words: lane t gets plane t of words 0..3
-#pragma unroll
-    for (int R = 0; R < 2; ++R) {
-      uint4 cw;
-      cw.x = quad_transpose(W[R][0], t);
-      cw.y = quad_transpose(W[R][1], t);
-      cw.z = quad_transpose(W[R][2], t);
-      cw.w = quad_transpose(W[R][3], t);
-      if (okrow[R] && t < bits) reinterpret_cast<uint4*>(codes + (size_t)nrow[R] * bits * 4)[t] = cw;
-      if (okrow[R] && t == 0) norms[nrow[R]] = nrm[R];
-    }
-
-    if (QJL) {
-      float rn[2], gam[2], bA[2], bB[2];
+    if constexpr (QJL) {
+      float gam[2], bA[2], bB[2];
 #pragma unroll
       for (int R = 0; R < 2; ++R) {
-        float s2 = rsum[R][0] + rsum[R][2];
+        float s2 = rs[R];
         s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
         s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
         gam[R] = sqrtf(s2 * (1.0f / D));  // exact scaling by a power of two
-        rn[R] = sqrtf(s2);
-        bA[R] = fmaf(k1, rn[R], k2);
-        bB[R] = k2 * rn[R];
+        const float rn = sqrtf(s2);
+        bA[R] = fmaf(k1, rn, k2);
+        bB[R] = k2 * rn + k2;
       }
-      __syncwarp();  // residual rows visible to the whole warp
-      uint32_t SB[2] = {0u, 0u};
+      uint32_t rA[KB][4];
 #pragma unroll
+      for (int a = 0; a < KB; ++a) {
+        const uint4 v = wb[(0 * KB + a) * 32 + lane];
+        rA[a][0] = v.x;
+        rA[a][1] = v.y;
+        rA[a][2] = v.z;
+        rA[a][3] = v.w;
+      }
+      __syncwarp();  // residual limbs visible to the whole warp for the fp32 recomputations
+      const uint32_t zmask = (zero[0] ? 0xffu : 0u) | (zero[1] ? 0xff00u : 0u);
+      uint32_t SB[2] = {0u, 0u};
+#pragma unroll 1
       for (int w = 0; w < 4; ++w) {
         float sacc[4][4];
 #pragma unroll
@@ -448,10 +508,17 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
 #pragma unroll
           for (int r = 0; r < 4; ++r) sacc[q][r] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < KB; ++kk)
+        for (int kk = 0; kk < KB; ++kk) {
+          const uint4 lo = wb[(1 * KB + kk) * 32 + lane];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], sfrag[((4 * w + q) * KB + kk) * 32 + lane]);
+          for (int q = 0; q < 4; ++q) {
+            const uint2 bh = sfrag[((4 * w + q) * KB + kk) * 32 + lane];
+            const uint2 bl = sfrag[((16 + 4 * w + q) * KB + kk) * 32 + lane];
+            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], bh);
+            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], bl);
+            mma_f16(sacc[q], lo.x, lo.y, lo.z, lo.w, bh);
+          }
+        }
         const float4 sn0 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t]);
         const float4 sn1 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t + 4]);
         const float sn[8] = {sn0.x, sn0.y, sn0.z, sn0.w, sn1.x, sn1.y, sn1.z, sn1.w};
@@ -462,23 +529,32 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
           for (int r = 0; r < 4; ++r) {
             const int R = r >> 1, e = r & 1, bit = 8 * R + 2 * q + e;
             const float v = sacc[q][r];
-            sb |= (uint32_t)(v >= 0.f || zero[R]) << bit;
-            pend |= (uint32_t)(!zero[R] && fabsf(v) < fmaf(sn[2 * q + e], bA[R], bB[R] + k2)) << bit;
+            sb |= (uint32_t)(v >= 0.f) << bit;
+            pend |= (uint32_t)(fabsf(v) < fmaf(sn[2 * q + e], bA[R], bB[R])) << bit;
           }
-        // fp32 recomputation of the uncertain entries, one per pass of the warp
+        sb |= zmask;
+        pend &= ~zmask;
+        // fp32 recomputation of the uncertain entries, one per pass of the warp,
+        // from the f16 hi + lo limbs of r and S (22 bits each); lane l covers
+        // coordinates blk_base(l / 4) + 8 (l % 4) + 0..3, which are one B
+        // fragment of the sketch row
         while (true) {
           const unsigned ball = __ballot_sync(0xffffffffu, pend != 0);
           if (ball == 0) break;
           const int src = __ffs(ball) - 1;
           const int bit = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
-          const int row = (src >> 2) + 8 * (bit >> 3);
-          const int c = 32 * w + 8 * (src & 3) + (bit & 7);
-          const float4 rr = *reinterpret_cast<const float4*>(rb + row * RS + 4 * lane);
-          const float4 ss = __ldg(reinterpret_cast<const float4*>(S + (size_t)c * D) + lane);
-          float dsum = rr.x * ss.x;
-          dsum = fmaf(rr.y, ss.y, dsum);
-          dsum = fmaf(rr.z, ss.z, dsum);
-          dsum = fmaf(rr.w, ss.w, dsum);
+          const int row = (src >> 2) + 8 * (bit >> 3), R = row >> 3;
+          const int nt = 4 * w + ((bit >> 1) & 3), n = 2 * (src & 3) + (bit & 1);  // sketch coordinate sk_out(nt, n)
+          const int ab = lane >> 2, tl = lane & 3;
+          const uint32_t* hi = reinterpret_cast<const uint32_t*>(wb + (0 * KB + ab) * 32 + (row & 7) * 4 + tl);
+          const uint32_t* lo = reinterpret_cast<const uint32_t*>(wb + (1 * KB + ab) * 32 + (row & 7) * 4 + tl);
+          const uint32_t h01 = hi[R], h23 = hi[2 + R], l01 = lo[R], l23 = lo[2 + R];
+          const uint2 sh2 = sfrag[(nt * KB + ab) * 32 + 4 * n + tl];
+          const uint2 sl2 = sfrag[((16 + nt) * KB + ab) * 32 + 4 * n + tl];
+          float dsum = (f16lo(h01) + f16lo(l01)) * (f16lo(sh2.x) + f16lo(sl2.x));
+          dsum = fmaf(f16hi(h01) + f16hi(l01), f16hi(sh2.x) + f16hi(sl2.x), dsum);
+          dsum = fmaf(f16lo(h23) + f16lo(l23), f16lo(sh2.y) + f16lo(sl2.y), dsum);
+          dsum = fmaf(f16hi(h23) + f16hi(l23), f16hi(sh2.y) + f16hi(sl2.y), dsum);
           dsum = warp_sum_f(dsum);
           if (lane == src) {
             sb = (sb & ~(1u << bit)) | ((uint32_t)(dsum >= 0.f) << bit);
@@ -494,8 +570,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), DENSE ? 1 : 2)
         if (okrow[R]) signs[(size_t)nrow[R] * 4 + t] = word;
         if (okrow[R] && t == 0) rnorms[nrow[R]] = zero[R] ? 0.f : gam[R];
       }
-      __syncwarp();  // the residual buffer is rewritten by the next tile
     }
+    __syncwarp();  // the block buffer is rewritten by the next tile
   }
 }
 
