@@ -274,7 +274,8 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- GPU path
 
 def bench_quantize(tq, torch, n=1 << 20):
-    """Bulk quantize (d = 128, keys 3b + QJL, values 4b) of n token-heads: keys and values."""
+    """Bulk quantize (d = 128, keys 3b + QJL, values 4b) of n token-heads: keys and
+    values, each timed on its own (inputs of 256 MB each, larger than L2)."""
     out = {}
     x = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
     y = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
@@ -287,22 +288,28 @@ def bench_quantize(tq, torch, n=1 << 20):
         vcodes = torch.empty(n, 16, dtype=torch.int32, device="cuda")
         nv = torch.empty(n, device="cuda")
 
-        def run():
+        def keys():
             tq.quantize_keys(L.params, x, n, codes, signs, nk, rk)
+
+        def values():
             tq.quantize_values(L.params, y, n, vcodes, nv)
 
-        for _ in range(2):
-            run()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-        e0.record()
-        for _ in range(3):
-            run()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / 3
+        ms = {}
+        for role, f in (("keys", keys), ("values", values)):
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            for _ in range(5):
+                f()
+            e1.record()
+            torch.cuda.synchronize()
+            ms[role] = e0.elapsed_time(e1) / 5
+        tot = ms["keys"] + ms["values"]
         nbytes = n * (2 * 128 * 2 + 140)  # bf16 K, V in; 140 B of records out per token-head
-        out[name] = {"token_heads_per_s": n / (ms * 1e-3), "ms": ms, "GB_per_s": nbytes / ms / 1e6}
+        out[name] = {"token_heads_per_s": n / (tot * 1e-3), "ms": tot, "keys_ms": ms["keys"],
+                     "values_ms": ms["values"], "GB_per_s": nbytes / tot / 1e6}
     return out
 
 
@@ -435,7 +442,8 @@ def run_gpu(args):
                      "traffic": traffic, "kernel": "tq_decode_attention (prologue + split-K tensor-core + combine)",
                      "peak_source": peak_src},
         "quantize": {"metric": "bulk quantize token-heads/s (d=128, keys 3b+QJL, values 4b, 2^20 token-heads)",
-                     "fwht": quant["fwht"], "dense": quant["dense"]},
+                     "fwht": dict(quant["fwht"], hbm_fraction=quant["fwht"]["GB_per_s"] / peak),
+                     "dense": dict(quant["dense"], hbm_fraction=quant["dense"]["GB_per_s"] / peak)},
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
                 "d2h_bytes_per_step": int(hout.numel() * 4)},
