@@ -38,8 +38,16 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention compressed-KV GB/s & % HBM roofline; quantize tokens·heads/s"
-WORKLOAD = ("qwen-like full-attention layer: bf16, d=256, 4 KV / 24 q heads, batch 8, 32768 ctx, "
-            "keys 3b (2b Lloyd-Max + 1b QJL), values 2b, FWHT, page 16, fp16 window 128")
+
+
+def workload_name(w) -> str:
+    kind = "FWHT" if w.kind == 1 else "dense Pi"
+    return (f"{w.name}-like full-attention layer: {w.dtype}, d={w.d}, {w.n_kv_heads} KV / {w.n_q_heads} q heads, "
+            f"batch {w.batch}, {w.ctx} ctx, keys {w.key_bits + 1}b ({w.key_bits}b Lloyd-Max + 1b QJL), "
+            f"values {w.value_bits}b, {kind}, page 16, fp16 window {w.window}")
+
+
+DEFAULT_LAYERS = {"qwen": 4, "llama": 4, "long": 8}  # resident layer caches: working set far above L2
 
 
 def parse():
@@ -48,7 +56,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
-    ap.add_argument("--layers", type=int, default=4, help="resident layer caches rotated over")
+    ap.add_argument("--workload", default="qwen", choices=["qwen", "llama", "long"],
+                    help="decode configuration (default: the Qwen-like headline workload)")
+    ap.add_argument("--layers", type=int, default=0, help="resident layer caches rotated over (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -173,8 +183,8 @@ def dist_info():
 
 # ----------------------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample_setup():
-    """One sequence, one KV head (its 6 query heads) of the workload, quantized
+def oracle_sample_setup(name="qwen"):
+    """One sequence, one KV head (its G query heads) of the workload, quantized
     by the oracle; the step is one append + decode over it."""
     import numpy as np
 
@@ -183,7 +193,7 @@ def oracle_sample_setup():
     from oracle import codec as OC
     from oracle import transforms as OT
 
-    w = SK.workload("qwen")
+    w = SK.workload(name)
     kv = SK.keys_values(w, seqs=[0])
     G = w.n_q_heads // w.n_kv_heads
     T, W, d = w.ctx, w.window, w.d
@@ -203,26 +213,42 @@ def oracle_sample_setup():
     kr_b, vr_b = record_bytes(d, w.key_bits, True, w.value_bits)
     nbytes = nc * (kr_b + vr_b) + (T - nc) * d * 4 + d * (2 * 2 + 2 * 2) + G * d * 6
     return {"prm": prm, "comp": comp, "win_k": win_k, "win_v": win_v, "q": q, "d": d, "bytes": nbytes,
-            "new_k": K[-1:], "new_v": V[-1:], "kind": w.kind, "T": T, "nc": nc}
+            "new_k": K[-1:], "new_v": V[-1:], "kind": w.kind, "T": T, "nc": nc, "G": G, "W": W,
+            "k_cb": kcb, "v_cb": vcb}
 
 
 def oracle_step(S):
     from oracle import attention as OA
     from oracle import codec as OC
 
-    # append: the new token enters the float16 window (no page flush due at this length)
     import numpy as np
 
-    nk = S["new_k"].astype(np.float16)[None]
-    nv = S["new_v"].astype(np.float16)[None]
-    wk = np.concatenate([S["win_k"][:, 1:], nk], axis=1)
-    wv = np.concatenate([S["win_v"][:, 1:], nv], axis=1)
+    if S["W"] > 0:
+        # append: the new token enters the float16 window (no page flush due at this length)
+        nk = S["new_k"].astype(np.float16)[None]
+        nv = S["new_v"].astype(np.float16)[None]
+        wk = np.concatenate([S["win_k"][:, 1:], nk], axis=1)
+        wv = np.concatenate([S["win_v"][:, 1:], nv], axis=1)
+        comp = S["comp"]
+    else:
+        # no window: the new token is quantized into its page slot
+        prm = S["prm"]
+        kr = OC.quantize_prod(S["new_k"], S["kind"], prm["k_rot"][0], S["k_cb"], prm["qjl_s"][0])
+        vr = OC.quantize_mse(S["new_v"], S["kind"], prm["v_rot"][0], S["v_cb"])
+        c = S["comp"]
+        comp = {"knorm": np.concatenate([c["knorm"][:, 1:], kr["norm"][None]], axis=1),
+                "krnorm": np.concatenate([c["krnorm"][:, 1:], kr["rnorm"][None]], axis=1),
+                "kidx": np.concatenate([c["kidx"][:, 1:], kr["idx"][None]], axis=1),
+                "ksigns": np.concatenate([c["ksigns"][:, 1:], kr["signs"][None]], axis=1),
+                "vnorm": np.concatenate([c["vnorm"][:, 1:], vr["norm"][None]], axis=1),
+                "vidx": np.concatenate([c["vidx"][:, 1:], vr["idx"][None]], axis=1)}
+        wk = wv = None
     OC.qjl_constant(S["d"])
-    return OA.decode_one(S["q"], S["comp"], wk, wv, S["prm"], 1.0 / math.sqrt(S["d"]))
+    return OA.decode_one(S["q"], comp, wk, wv, S["prm"], 1.0 / math.sqrt(S["d"]))
 
 
-def run_cpu_sample(steps=3, warmup=1):
-    S = oracle_sample_setup()
+def run_cpu_sample(name="qwen", steps=3, warmup=1):
+    S = oracle_sample_setup(name)
     for _ in range(warmup):
         oracle_step(S)
     t0 = time.perf_counter()
@@ -230,16 +256,16 @@ def run_cpu_sample(steps=3, warmup=1):
         oracle_step(S)
     dt = (time.perf_counter() - t0) / steps
     return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"1 sequence x 1 KV head (6 q heads) of the workload, T={S['T']}, "
+            "sample": (f"1 sequence x 1 KV head ({S['G']} q heads) of the workload, T={S['T']}, "
                        f"{S['bytes'] / 1e6:.1f} MB per step, {steps} steps, 1 thread"),
             "s_per_step": dt}
 
 
-def cpu_baseline_subprocess():
+def cpu_baseline_subprocess(name="qwen"):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample"], capture_output=True, text=True,
-                       env=env, timeout=900)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", "--workload", name],
+                       capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
     return json.loads(r.stdout.strip().splitlines()[-1])
@@ -250,7 +276,9 @@ def run_reference(args):
     if rank != 0:
         return
     os.environ.setdefault("OMP_NUM_THREADS", "1")
-    S = oracle_sample_setup()
+    import synthetic_kv as SK
+
+    S = oracle_sample_setup(args.workload)
     for _ in range(args.warmup):
         oracle_step(S)
     times = []
@@ -260,12 +288,13 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     dt = sum(times) / len(times)
     value = S["bytes"] / dt / 1e9
-    sample = (f"each step: 1 sequence x 1 KV head (6 q heads) of the workload, T={S['T']}, "
+    sample = (f"each step: 1 sequence x 1 KV head ({S['G']} q heads) of the workload, T={S['T']}, "
               f"{S['bytes'] / 1e6:.1f} MB algorithmic bytes")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": "1 sequence x 1 KV head per step"},
+            "config": {"workload": workload_name(SK.workload(args.workload)),
+                       "sample": "1 sequence x 1 KV head per step"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -313,6 +342,34 @@ def bench_quantize(tq, torch, n=1 << 20):
     return out
 
 
+def bench_append_batch256(tq, torch, steps=200):
+    """Decode-step append latency: 256 sequences x 8 KV heads, d = 128, keys 3b + QJL,
+    values 4b, dense Pi, no window, into partially filled pages (37 tokens each at
+    the start); one call quantizes and stores one token per sequence."""
+    import synthetic_kv as SK
+
+    w = SK.workload("llama", batch=256, ctx=37, n_q_heads=8)
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=0, seed=w.seed)
+    pc = tq.PagedCache(L, w.batch, w.ctx + steps + 32)
+    K, V, _ = SK.keys_values_torch(w, ctx=w.ctx + steps + 8)
+    pc.prefill(K[:, :w.ctx], V[:, :w.ctx])
+    news = [(K[:, t].contiguous(), V[:, t].contiguous()) for t in range(w.ctx, w.ctx + steps + 8)]
+    for i in range(5):
+        pc.append(*news[i])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record()
+    for i in range(steps):
+        pc.append(*news[5 + i])
+    e1.record()
+    torch.cuda.synchronize()
+    if tq.check_device_error():
+        raise RuntimeError("device error in the append benchmark")
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    return {"us_per_call": us, "token_heads_per_s": w.batch * w.n_kv_heads / (us * 1e-6),
+            "config": "256 seqs x 8 KV heads, d=128, keys 3b+QJL, values 4b, dense Pi, 1 token per call"}
+
+
 def run_gpu(args):
     import torch
 
@@ -326,8 +383,10 @@ def run_gpu(args):
     import kv_cache_vector_head_gb300 as tq
     import synthetic_kv as SK
 
-    w = SK.workload("qwen", seed=1000 * rank)
+    w = SK.workload(args.workload, seed=1000 * rank)
     B, Hkv, Hq, d, T0, W = w.batch, w.n_kv_heads, w.n_q_heads, w.d, w.ctx, w.window
+    if args.layers <= 0:
+        args.layers = DEFAULT_LAYERS[args.workload]
     total_steps = args.warmup + 2 * args.steps
     per_layer = (total_steps + args.layers - 1) // args.layers + 1
     max_ctx = T0 + per_layer + 16
@@ -416,6 +475,7 @@ def run_gpu(args):
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms)
     quant = bench_quantize(tq, torch)
+    app = bench_append_batch256(tq, torch)
     if rank != 0:
         return
     peaks = measured_peaks()
@@ -432,7 +492,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch Philox on the device)",
-        "config": {"workload": WORKLOAD, "batch": B, "ctx": T0, "kv_heads": Hkv, "q_heads": Hq, "d": d,
+        "config": {"workload": workload_name(w), "batch": B, "ctx": T0, "kv_heads": Hkv, "q_heads": Hq, "d": d,
                    "key_bits": w.key_bits + 1, "value_bits": w.value_bits, "window": W, "page": 16,
                    "layer_caches": args.layers, "l2": f"inputs larger than L2: {args.layers} rotating layer caches "
                    f"of {step_bytes(T0, W, B, Hkv, Hq, d, w.key_bits, w.value_bits) / 1e6:.0f} MB",
@@ -444,6 +504,7 @@ def run_gpu(args):
         "quantize": {"metric": "bulk quantize token-heads/s (d=128, keys 3b+QJL, values 4b, 2^20 token-heads)",
                      "fwht": dict(quant["fwht"], hbm_fraction=quant["fwht"]["GB_per_s"] / peak),
                      "dense": dict(quant["dense"], hbm_fraction=quant["dense"]["GB_per_s"] / peak)},
+        "append_batch256": app,
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
                 "d2h_bytes_per_step": int(hout.numel() * 4)},
@@ -451,14 +512,14 @@ def run_gpu(args):
         "clocks": clk,
     }
     if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_subprocess()
+        line["cpu_baseline"] = cpu_baseline_subprocess(args.workload)
     print(json.dumps(line), flush=True)
 
 
 def main():
     args = parse()
     if args.cpu_sample:
-        print(json.dumps(run_cpu_sample()))
+        print(json.dumps(run_cpu_sample(args.workload)))
         return
     if args.impl == "reference":
         run_reference(args)

@@ -27,9 +27,11 @@
 // ~2^-22 relative query rounding instead of f16's 2^-11.
 //
 // Launches per call:
-//   decode_prologue_kernel  grid (Hkv, ceil(batch G / 16)): q' = Pi q,
-//                           q'' = S q' as tile products and the query rows
-//                           of the score operands in mma fragment order.
+//   decode_prologue_kernel  grid (Hkv, ceil(batch G / 4), d / 64): q' = Pi q,
+//                           q'' = S q' (64 rows of S per CTA) and the query
+//                           rows of the score operands in mma fragment order;
+//                           the decode kernel is launched as its programmatic
+//                           dependent and starts streaming pages meanwhile.
 //   decode_mma_kernel       grid (splits + 1, Hkv, batch): split-K over the page
 //                           list.  Pages stream into shared memory with 1-D
 //                           TMA bulk copies (cp.async.bulk + mbarrier, two or
@@ -198,54 +200,66 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constant__ KParams P, const void* q,
                                                             int dtype, unsigned char* ws, WsLayout L, int batch) {
   constexpr int KS = D / 16, WPL = D / 128;
+  constexpr int TPR = D / 64;  // threads per row of S: each CTA owns 64 rows (coordinates 64 z .. 64 z + 63)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
-  const int g = blockIdx.x, j = threadIdx.x;
+  const int g = blockIdx.x, z = blockIdx.z, j = threadIdx.x;
+  // the decode kernel may start streaming its pages now; it waits for these
+  // operands before its first score
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = P.G;
   const int n0 = blockIdx.y * kPrologueTile;
   const int nv = min(kPrologueTile, batch * G - n0);
-  for (int v = 0; v < nv; ++v) {
+  for (int v = 0; v < kPrologueTile; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
-    s.x[v][j] = load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * D + j));
+    s.x[v][j] = v < nv ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * D + j)) : 0.f;
   }
   if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
-  rotate_tile<D>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
+  rotate_tile<D, kPrologueTile>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
   if (P.kqjl) {
-    const float4* row = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)j * D);
-    float acc[kTile];
+    // q'' rows of this CTA: TPR neighbouring threads per row, 64 inputs each
+    const int row = 64 * z + j / TPR, u = j % TPR;
+    const float4* rp = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)row * D) + u * 16;
+    float acc[kPrologueTile];
 #pragma unroll
-    for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
+    for (int v = 0; v < kPrologueTile; ++v) acc[v] = 0.f;
 #pragma unroll 8
-    for (int i4 = 0; i4 < D / 4; ++i4) {
-      const float4 p = __ldg(row + i4);
+    for (int i4 = 0; i4 < 16; ++i4) {
+      const float4 p = __ldg(rp + i4);
 #pragma unroll
-      for (int v = 0; v < kTile; ++v) {
-        if (v < nv) {
-          const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][i4 * 4]);
-          acc[v] = fmaf(p.x, xv.x, fmaf(p.y, xv.y, fmaf(p.z, xv.z, fmaf(p.w, xv.w, acc[v]))));
-        }
+      for (int v = 0; v < kPrologueTile; ++v) {
+        const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][(u * 16 + i4) * 4]);  // rows >= nv hold zeros
+        acc[v] = fmaf(p.x, xv.x, fmaf(p.y, xv.y, fmaf(p.z, xv.z, fmaf(p.w, xv.w, acc[v]))));
       }
     }
 #pragma unroll
-    for (int v = 0; v < kTile; ++v)
-      if (v < nv) s.r[v][j] = acc[v];
+    for (int v = 0; v < kPrologueTile; ++v) {
+#pragma unroll
+      for (int o = 1; o < TPR; o <<= 1) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
+      if (v < nv && u == 0) s.r[v][row] = acc[v];
+    }
   }
   __syncthreads();
+  // fragment entries of this CTA: lanes t4 with (t4 * WPL + kk / 8) / 2 == z,
+  // i.e. t4 = z (d = 256) or t4 in {2z, 2z + 1} (d = 128)
+  constexpr int NT4 = 4 / (D / 64);
   const int nplanes = P.kp + (P.kqjl ? 1 : 0);
+  const int per_row = nplanes * KS * NT4 * 4;
   for (int v = 0; v < nv; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
     uint32_t* frag = reinterpret_cast<uint32_t*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
-    // this head's entries (lanes with lane / 4 == hl); head 0 also zeroes the rows of absent heads
+    // this head's rows (lanes with lane / 4 == hl); head 0 also zeroes the rows of absent heads
     const int nrow = (hl == 0) ? (8 - G + 1) : 1;
-    const int total = nplanes * KS * 4 * 4 * nrow;
-    for (int idx = j; idx < total; idx += D) {
-      const int r = idx & 3, t4 = (idx >> 2) & 3, rest = idx >> 4;
-      const int rowsel = rest % nrow, kk = (rest / nrow) % KS, pl = (rest / nrow) / KS;
+    for (int idx = j; idx < per_row * nrow; idx += D) {
+      const int rowsel = idx / per_row, e = idx - rowsel * per_row;
+      const int r = e & 3, ti = (e >> 2) % NT4, kk = ((e >> 2) / NT4) % KS, pl = ((e >> 2) / NT4) / KS;
+      const int t4 = z * NT4 + ti;
       const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
       uint32_t val = 0;
       if (rowsel == 0) {
-        const int w = t4 * WPL + kk / 8, i0 = 2 * (kk % 8) + ((r >= 2) ? 1 : 0);
+        const int w = t4 * WPL + kk / 8;
+        const int i0 = 2 * (kk % 8) + ((r >= 2) ? 1 : 0);
         const int ca = 32 * w + i0, cb = ca + 16;
         float va, vb;
         if (pl < P.kp) {
@@ -466,10 +480,6 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   const int nchunks = (npg + NW - 1) / NW;
   const int ncache = min(npg, kPidCache);
 
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
-    for (int i = tid; i < (int)(L.afrag_bytes_per_head / 16); i += kMmaThreads) afr[i] = src[i];
-  }
   for (int i = tid; i < ncache; i += kMmaThreads) {
     long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
     if (pid < 0 || pid >= C.n_pages) {
@@ -523,6 +533,14 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   };
   if (warp == 0)
     for (int k = 0; k < nst - 1 && k < nchunks; ++k) issue(k);
+  // the query fragments come from the prologue kernel (launched just before, with
+  // this grid allowed to start early): wait for it, then stage them; the first
+  // page copies are already in flight
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
+    for (int i = tid; i < (int)(L.afrag_bytes_per_head / 16); i += kMmaThreads) afr[i] = src[i];
+  }
 
   float accv[2][CB][4];
 #pragma unroll
@@ -898,8 +916,20 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dyn);
   if (e != cudaSuccess) return e;
-  dim3 grid(L.n_comp_splits + 1, P.hkv, C.batch);
-  decode_mma_kernel<D, VLUT><<<grid, kMmaThreads, dyn, st>>>(P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
+  // programmatic dependent launch: the grid may start while the prologue runs
+  // (it waits on it with griddepcontrol.wait before reading the query fragments)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.n_comp_splits + 1, P.hkv, C.batch);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, VLUT>, P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -911,7 +941,7 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   const size_t tsm = sizeof(TileSmem<D>);
   cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsm);
   if (e != cudaSuccess) return e;
-  const dim3 gp(P.hkv, (C.batch * P.G + kPrologueTile - 1) / kPrologueTile);
+  const dim3 gp(P.hkv, (C.batch * P.G + kPrologueTile - 1) / kPrologueTile, D / 64);
   decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, C.batch);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = P.vb >= 3 ? launch_mma<D, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)

@@ -21,11 +21,14 @@
 #include "tq_device.cuh"
 #include "tq_launch.h"
 #include "tq_tile.cuh"
+
+namespace tq {
+__device__ unsigned int g_quant_err = 0;
+}  // namespace tq
+
 #include "tq_quantize_mma.cuh"
 
 namespace tq {
-
-__device__ unsigned int g_quant_err = 0;
 
 // Quantize the tile held in s.x (nv vectors, rows >= nv are ignored).
 // is_key selects the key codebook/transform and the QJL stage.
@@ -366,9 +369,10 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
   } else {
     const int pidx = T / kPage, slot = T % kPage;
     long long page = -1;
-    if (pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
+    if (T >= 0 && pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
     if (page < 0 || page >= C.n_pages) {
-      if (threadIdx.x == 0) atomicOr(&g_quant_err, pidx < C.max_pages ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
+      if (threadIdx.x == 0)
+        atomicOr(&g_quant_err, (T >= 0 && pidx < C.max_pages) ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
       return;
     }
     s.x[0][threadIdx.x] = load_elem(x, dtype, src + threadIdx.x);
@@ -437,12 +441,12 @@ static bool antisymmetric(const float* c, const float* t, int bits) {
   return true;
 }
 
-template <int BITS, bool QJL, bool DENSE>
-static cudaError_t launch_quantize_warp(const KParams& P, const void* x, long long n_vec, bool is_key,
-                                        uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
+template <int BITS, bool QJL, bool DENSE, int MODE>
+static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const void* x, long long n_vec,
+                                        bool is_key, uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
                                         cudaStream_t st) {
   constexpr int warps = wq::warps_for(QJL, DENSE);
-  auto kern = wq::quantize_warp_kernel<BITS, QJL, DENSE>;
+  auto kern = wq::quantize_warp_kernel<BITS, QJL, DENSE, MODE>;
   const size_t sm = wq::smem_bytes(QJL, DENSE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
@@ -456,35 +460,46 @@ static cudaError_t launch_quantize_warp(const KParams& P, const void* x, long lo
   long long gx = std::max(1LL, (long long)std::max(occ, 1) * sms / P.hkv);
   gx = std::min(gx, (n_tiles + warps - 1) / warps);
   dim3 grid((int)std::min(gx, 65535LL), P.hkv);
-  kern<<<grid, 32 * warps, sm, st>>>(P, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, is_key ? 1 : 0, codes,
-                                      signs, norms, rnorms);
+  kern<<<grid, 32 * warps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, is_key ? 1 : 0,
+                                      codes, signs, norms, rnorms);
   return cudaGetLastError();
 }
 
-template <bool QJL, bool DENSE>
-static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const void* x, long long n_vec,
+template <bool QJL, bool DENSE, int MODE>
+static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const KCache& C, const void* x,
+                                             long long n_vec, bool is_key, uint32_t* codes, uint32_t* signs,
+                                             float* norms, float* rnorms, cudaStream_t st) {
+  switch (bits) {
+    case 1: return launch_quantize_warp<1, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 2: return launch_quantize_warp<2, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 3: return launch_quantize_warp<3, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    default: return launch_quantize_warp<4, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+  }
+}
+
+// Tensor-core path: d = 128, bf16, 16-byte aligned input, antisymmetric tables.
+static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key) {
+  const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
+  return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0;
+}
+
+template <int MODE>
+static cudaError_t launch_quantize_warp_role(const KParams& P, const KCache& C, const void* x, long long n_vec,
                                              bool is_key, uint32_t* codes, uint32_t* signs, float* norms,
                                              float* rnorms, cudaStream_t st) {
-  switch (bits) {
-    case 1: return launch_quantize_warp<1, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    case 2: return launch_quantize_warp<2, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    case 3: return launch_quantize_warp<3, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    default: return launch_quantize_warp<4, QJL, DENSE>(P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-  }
+  const bool qjl = is_key && P.kqjl;
+  const int bits = is_key ? P.kb : P.vb;
+  if (P.kind == TQ_FWHT)
+    return qjl ? launch_quantize_warp_bits<true, false, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+               : launch_quantize_warp_bits<false, false, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+  return qjl ? launch_quantize_warp_bits<true, true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st)
+             : launch_quantize_warp_bits<false, true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
 }
 
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
-  const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
-  if (P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0) {
-    const bool qjl = is_key && P.kqjl;
-    const int bits = is_key ? P.kb : P.vb;
-    if (P.kind == TQ_FWHT)
-      return qjl ? launch_quantize_warp_bits<true, false>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-                 : launch_quantize_warp_bits<false, false>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    return qjl ? launch_quantize_warp_bits<true, true>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-               : launch_quantize_warp_bits<false, true>(bits, P, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-  }
+  if (warp_path_ok(P, x, dtype, is_key))
+    return launch_quantize_warp_role<wq::kFlat>(P, KCache{}, x, n_vec, is_key, codes, signs, norms, rnorms, st);
   if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
   return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
 }
@@ -510,6 +525,16 @@ cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* 
 template <int D>
 static cudaError_t launch_append_step_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                         cudaStream_t st) {
+  if (P.window == 0 && warp_path_ok(P, k, dtype, true) && warp_path_ok(P, v, dtype, false)) {
+    // one sequence per row of the warp tiles: keys, values, then the counters
+    const long long n_vec = (long long)C.batch * P.hkv;
+    cudaError_t e = launch_quantize_warp_role<wq::kStep>(P, C, k, n_vec, true, nullptr, nullptr, nullptr, nullptr, st);
+    if (e != cudaSuccess) return e;
+    e = launch_quantize_warp_role<wq::kStep>(P, C, v, n_vec, false, nullptr, nullptr, nullptr, nullptr, st);
+    if (e != cudaSuccess) return e;
+    append_counters_kernel<<<(C.batch + 127) / 128, 128, 0, st>>>(C, P.window);
+    return cudaGetLastError();
+  }
   const size_t sm = tile_smem<D>();
   cudaError_t e = cudaFuncSetAttribute(append_step_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;

@@ -41,6 +41,10 @@
 #include "tq_device.cuh"
 
 namespace tq {
+
+// The including file defines tq::g_quant_err (the device error word of the
+// quantize / append kernels) before including this header.
+
 namespace wq {
 
 constexpr int D = 128;
@@ -133,17 +137,6 @@ __device__ __forceinline__ uint32_t quad_transpose(uint32_t v, int t) {
   return (t < 2) ? __byte_perm(u, o, 0x5410) : __byte_perm(o, u, 0x7632);
 }
 
-// B fragment of an m16n8k16 product: lane (g, t), register j, half e holds
-// k-row 2t + e + 8j of column g.  elem(L, n) returns the 16-bit pattern.
-template <class F>
-__device__ __forceinline__ uint2 make_frag(int lane, F&& elem) {
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t r[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) r[j] = elem(2 * t + 8 * j, g) | (elem(2 * t + 1 + 8 * j, g) << 16);
-  return make_uint2(r[0], r[1]);
-}
-
 // Positive half of an antisymmetric codebook: boundaries (as int bits,
 // ascending) and centroids.
 template <int BITS>
@@ -181,12 +174,19 @@ __device__ __forceinline__ float centroid_pos(int mag, const Book<BITS>& b) {
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
 __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
+// Where the records go: flat arrays (bulk quantize) or the page slot of each
+// sequence's next token (decode-step append without a window: rows are the
+// sequences, the token of sequence b lands in slot seq_len[b] % 16 of page
+// block_table[b][seq_len[b] / 16]).
+enum { kFlat = 0, kStep = 1 };
+
 // QJL: keys with the sketch; DENSE: dense rotation (else FWHT).  grid (x, Hkv).
-template <int BITS, bool QJL, bool DENSE>
+template <int BITS, bool QJL, bool DENSE, int MODE>
 __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENSE))
-    quantize_warp_kernel(const __grid_constant__ KParams P, const __nv_bfloat16* __restrict__ x, long long n_vec,
-                         int is_key, uint32_t* __restrict__ codes, uint32_t* __restrict__ signs,
-                         float* __restrict__ norms, float* __restrict__ rnorms) {
+    quantize_warp_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
+                         const __nv_bfloat16* __restrict__ x, long long n_vec, int is_key,
+                         uint32_t* __restrict__ codes, uint32_t* __restrict__ signs, float* __restrict__ norms,
+                         float* __restrict__ rnorms) {
   constexpr int WARPS = warps_for(QJL, DENSE);
   constexpr int NT = 32 * WARPS;
   constexpr int HALF = 1 << (BITS - 1);
@@ -213,55 +213,97 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
 #pragma unroll
   for (int m = 0; m < HALF; ++m) bk.cp[m] = ctab[HALF + m];
 
-  // ---- per-CTA constants
+  // ---- per-CTA constants.  The four elements of a B fragment (lane (g, t),
+  // k-rows 2t, 2t+1, 2t+8, 2t+9 of k-block kk) sit at columns
+  // blk_base(kk) + 8t + 0..3 of one row: one aligned float4 per fragment.
   if constexpr (!DENSE) {
     for (int i = tid; i < KB * 2 * 32; i += NT) {
       const int ln = i & 31, nt = (i >> 5) & 1, kk = i >> 6;
-      sh.hfrag[kk][nt][ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
-        const int in = blk_base(kk) + free_off(L);
-        const int out = 8 * (n >> 1) + 2 * nt + (n & 1);
-        const bool neg = (__ldg(rot + in) < 0.f) != (bool)(__popc(free_off(L) & out) & 1);
-        return neg ? 0xBF80u : 0x3F80u;
-      });
+      const int gg = ln >> 2, tt = ln & 3;
+      const float4 sg = __ldg(reinterpret_cast<const float4*>(rot + blk_base(kk) + 8 * tt));
+      const float sv[4] = {sg.x, sg.y, sg.z, sg.w};
+      const int out = 8 * (gg >> 1) + 2 * nt + (gg & 1);
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int L = 2 * tt + (e & 1) + 8 * (e >> 1);
+        const bool neg = (sv[e] < 0.f) != (bool)(__popc(free_off(L) & out) & 1);
+        h[e] = neg ? 0xBF80u : 0x3F80u;
+      }
+      sh.hfrag[kk][nt][ln] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
     }
   } else {
-    for (int i = tid; i < 16 * KB * 32; i += NT) {
-      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
-      const uint2 frag[3] = {
-          make_frag(ln, [&](int L, int n) -> uint32_t {
-            return bf16_bits(__ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L)));
-          }),
-          make_frag(ln, [&](int L, int n) -> uint32_t {
-            const float a = __ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L));
-            const float l0 = __bfloat162float(__float2bfloat16_rn(a));
-            return bf16_bits(a - l0);
-          }),
-          make_frag(ln, [&](int L, int n) -> uint32_t {
-            const float a = __ldg(rot + (size_t)rot_out(nt, n) * D + blk_base(kk) + free_off(L));
-            const float l0 = __bfloat162float(__float2bfloat16_rn(a));
-            const float l1 = __bfloat162float(__float2bfloat16_rn(a - l0));
-            return bf16_bits((a - l0) - l1);
-          })};
+    constexpr int PER = (16 * KB * 32 + NT - 1) / NT;  // fragments per thread: all loads issued first
+    float4 pv[PER];
 #pragma unroll
-      for (int l = 0; l < 3; ++l) pfrag[((l * 16 + nt) * KB + kk) * 32 + ln] = frag[l];
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = (i >> 8) & 15;
+      pv[j] = i < 16 * KB * 32
+                  ? __ldg(reinterpret_cast<const float4*>(rot + (size_t)rot_out(nt, ln >> 2) * D + blk_base(kk) + 8 * (ln & 3)))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      if (i >= 16 * KB * 32) break;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
+      const float4 v4 = pv[j];
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      uint32_t l[3][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float l0 = __bfloat162float(__float2bfloat16_rn(v[e]));
+        const float l1 = __bfloat162float(__float2bfloat16_rn(v[e] - l0));
+        l[0][e] = bf16_bits(v[e]);
+        l[1][e] = bf16_bits(v[e] - l0);
+        l[2][e] = bf16_bits((v[e] - l0) - l1);
+      }
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        pfrag[((k * 16 + nt) * KB + kk) * 32 + ln] = make_uint2(l[k][0] | (l[k][1] << 16), l[k][2] | (l[k][3] << 16));
     }
   }
   if constexpr (QJL) {
-    for (int i = tid; i < 16 * KB * 32; i += NT) {
-      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
-      sfrag[(nt * KB + kk) * 32 + ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
-        return f16_bits(__ldg(S + (size_t)sk_out(nt, n) * D + blk_base(kk) + free_off(L)));
-      });
-      sfrag[((16 + nt) * KB + kk) * 32 + ln] = make_frag(ln, [&](int L, int n) -> uint32_t {
-        const float v = __ldg(S + (size_t)sk_out(nt, n) * D + blk_base(kk) + free_off(L));
-        return f16_bits(v - __half2float(__float2half_rn(v)));
-      });
+    constexpr int PER = (16 * KB * 32 + NT - 1) / NT;
+    float4 sv4[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = (i >> 8) & 15;
+      sv4[j] = i < 16 * KB * 32
+                   ? __ldg(reinterpret_cast<const float4*>(S + (size_t)sk_out(nt, ln >> 2) * D + blk_base(kk) + 8 * (ln & 3)))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int c = warp; c < D; c += WARPS) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(S + (size_t)c * D) + lane);
-      float s2 = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      s2 = warp_sum_f(s2);
-      if (lane == 0) sh.snorm[c] = sqrtf(s2) * 1.0001f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      if (i >= 16 * KB * 32) break;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
+      const float4 v4 = sv4[j];
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = f16_bits(v[e]);
+        lo[e] = f16_bits(v[e] - __half2float(__float2half_rn(v[e])));
+      }
+      sfrag[(nt * KB + kk) * 32 + ln] = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+      sfrag[((16 + nt) * KB + kk) * 32 + ln] = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+    }
+    // ||S_c||: thread c sums its row from the fragments' source (fp32, L2-hot)
+    for (int c = tid; c < D; c += NT) {
+      const float4* row = reinterpret_cast<const float4*>(S + (size_t)c * D);
+      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int i = 0; i < D / 4; ++i) {
+        const float4 v = __ldg(row + i);
+        acc4.x = fmaf(v.x, v.x, acc4.x);
+        acc4.y = fmaf(v.y, v.y, acc4.y);
+        acc4.z = fmaf(v.z, v.z, acc4.z);
+        acc4.w = fmaf(v.w, v.w, acc4.w);
+      }
+      sh.snorm[c] = sqrtf((acc4.x + acc4.y) + (acc4.z + acc4.w)) * 1.0001f;
     }
   }
   __syncthreads();
@@ -317,8 +359,28 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
 
     long long nrow[2];
     bool okrow[2];
+    unsigned char* dst[2] = {nullptr, nullptr};  // step mode: this row's (page, head) sub-block
+    int slot[2] = {0, 0};
 #pragma unroll
-    for (int R = 0; R < 2; ++R) okrow[R] = row_index(mt, R, nrow[R]);
+    for (int R = 0; R < 2; ++R) {
+      okrow[R] = row_index(mt, R, nrow[R]);
+      if constexpr (MODE == kStep) {
+        if (okrow[R]) {
+          const int b = (int)(nrow[R] / P.hkv);
+          const int T = C.seq_len[b];
+          const int pidx = T >> 4;
+          long long page = -1;
+          if (T >= 0 && pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
+          if (page < 0 || page >= C.n_pages) {
+            if (t == 0) atomicOr(&g_quant_err, (T >= 0 && pidx < C.max_pages) ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
+            okrow[R] = false;
+          } else {
+            dst[R] = C.pool + ((size_t)page * P.hkv + head) * (size_t)P.sub_bytes;
+            slot[R] = T & 15;
+          }
+        }
+      }
+    }
 
     // norms of rows g (R = 0) and g + 8 (R = 1): squares of bf16 values are
     // exact in fp32; a balanced tree of depth 7 sums them
@@ -347,7 +409,10 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
       // z = sqrt(d) Pi x / n (dense) or H (sigma x) / n (FWHT): one division
       // and one square root of the sum's fp32 value
       inv[R] = zero[R] ? 0.f : sqrtf((DENSE ? (float)D : 1.0f) / s2);
-      if (okrow[R] && t == 0) norms[nrow[R]] = nrm[R];
+      if (okrow[R] && t == 0) {
+        if constexpr (MODE == kFlat) norms[nrow[R]] = nrm[R];
+        else reinterpret_cast<float*>(dst[R] + (is_key ? P.off_knorm : P.off_vnorm))[slot[R]] = nrm[R];
+      }
     }
 
     if constexpr (!DENSE) {
@@ -391,6 +456,7 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
 
     // codes, two blocks (one packed word) per pass
     float rs[2] = {0.f, 0.f};  // ||r||^2: block sums, pairs, then the four words in turn
+    uint32_t vword[2][4];      // step mode, values: plane t of words 0..3 of rows g, g + 8
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       uint32_t Wm[2] = {0u, 0u};  // byte p: plane p of this lane's byte of word m
@@ -472,7 +538,45 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
       for (int R = 0; R < 2; ++R) {
         rs[R] += pr[R];
         const uint32_t word = quad_transpose(Wm[R], t);  // plane t of word m
-        if (okrow[R] && t < BITS) codes[(size_t)nrow[R] * BITS * 4 + t * 4 + m] = word;
+        if (okrow[R] && t < BITS) {
+          if constexpr (MODE == kFlat) {
+            codes[(size_t)nrow[R] * BITS * 4 + t * 4 + m] = word;
+          } else if (is_key) {
+            reinterpret_cast<uint32_t*>(dst[R] + P.off_kcodes)[(t * 16 + slot[R]) * 4 + m] = word;
+          } else {
+            vword[R][m] = word;  // written into the coordinate-major planes after the loop
+          }
+        }
+      }
+    }
+
+    if constexpr (MODE == kStep) {
+      if (!is_key) {
+        // coordinate-major value planes: bit slot of the 16-bit entry (plane t, coordinate
+        // j), one 32-bit word per coordinate pair.  Lane t rewrites its plane's 256 bytes
+        // of the row's sub-block with two 16-byte accesses per word group; nothing else
+        // writes them in this launch (one token per sequence, pages not shared).
+#pragma unroll 1
+        for (int R = 0; R < 2; ++R) {
+          if (!okrow[R] || t >= BITS) continue;
+          uint4* pl = reinterpret_cast<uint4*>(dst[R] + P.off_vcodes + (size_t)t * D * 2);
+          uint4 wv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) wv[i] = pl[i];
+          const int sl = slot[R];
+          const uint32_t keep = ~((1u << sl) | (1u << (sl + 16)));
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t cw = vword[R][i >> 2];  // coordinates 32 (i / 4) .. + 31
+            uint32_t e[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int c = 8 * (i & 3) + 2 * k;  // pair (c, c + 1) of the word
+              e[k] = (e[k] & keep) | (((cw >> c) & 1u) << sl) | (((cw >> (c + 1)) & 1u) << (sl + 16));
+            }
+            pl[i] = make_uint4(e[0], e[1], e[2], e[3]);
+          }
+        }
       }
     }
 
@@ -567,8 +671,13 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
 #pragma unroll
       for (int R = 0; R < 2; ++R) {
         const uint32_t word = quad_transpose(SB[R], t);
-        if (okrow[R]) signs[(size_t)nrow[R] * 4 + t] = word;
-        if (okrow[R] && t == 0) rnorms[nrow[R]] = zero[R] ? 0.f : gam[R];
+        if constexpr (MODE == kFlat) {
+          if (okrow[R]) signs[(size_t)nrow[R] * 4 + t] = word;
+          if (okrow[R] && t == 0) rnorms[nrow[R]] = zero[R] ? 0.f : gam[R];
+        } else {
+          if (okrow[R]) reinterpret_cast<uint32_t*>(dst[R] + P.off_ksigns)[slot[R] * 4 + t] = word;
+          if (okrow[R] && t == 0) reinterpret_cast<float*>(dst[R] + P.off_krnorm)[slot[R]] = zero[R] ? 0.f : gam[R];
+        }
       }
     }
     __syncwarp();  // the block buffer is rewritten by the next tile

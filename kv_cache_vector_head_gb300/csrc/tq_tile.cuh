@@ -22,7 +22,7 @@ struct TileSmem {
 
 // out[v][j] = inv[v] * (R x_v)_j, R = Pi (dense) or H diag(sigma) (FWHT).
 // In place in s.x (the dense product goes through registers).
-template <int D>
+template <int D, int MAXV = kTile>
 __device__ void rotate_tile(TileSmem<D>& s, int nv, int kind, const float* rot) {
   constexpr int E = D / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -57,15 +57,15 @@ __device__ void rotate_tile(TileSmem<D>& s, int nv, int kind, const float* rot) 
     __syncthreads();
   } else {
     const int j = tid;
-    float acc[kTile];
+    float acc[MAXV];
 #pragma unroll
-    for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
+    for (int v = 0; v < MAXV; ++v) acc[v] = 0.f;
     const float4* row = reinterpret_cast<const float4*>(rot + (size_t)j * D);
 #pragma unroll 8
     for (int i4 = 0; i4 < D / 4; ++i4) {
       const float4 p = __ldg(row + i4);
 #pragma unroll
-      for (int v = 0; v < kTile; ++v) {
+      for (int v = 0; v < MAXV; ++v) {
         if (v < nv) {
           const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][i4 * 4]);
           acc[v] = fmaf(p.x, xv.x, acc[v]);
@@ -77,7 +77,7 @@ __device__ void rotate_tile(TileSmem<D>& s, int nv, int kind, const float* rot) 
     }
     __syncthreads();
 #pragma unroll
-    for (int v = 0; v < kTile; ++v)
+    for (int v = 0; v < MAXV; ++v)
       if (v < nv) s.x[v][j] = acc[v] * s.inv[v];
     __syncthreads();
   }

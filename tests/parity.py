@@ -100,6 +100,29 @@ def compare_records(ora, g_idx, g_norm, g_signs=None, g_rnorm=None, is_key=True,
     return {"exempt": n_exempt_codes, "flipped": int(diff.sum()), "total": total}
 
 
+def adopt_exempt(rec, g_idx, g_signs=None, g_rnorm=None):
+    """A copy of the oracle record that takes the GPU's decisions exactly where
+    the parity rules accept either one: codes of coordinates within BOUNDARY of
+    a boundary, QJL signs within BOUNDARY of zero, and the signs and residual
+    norm of a vector whose code changed.  Everything else stays the oracle's,
+    so a decode computed from the copy is compared without exemptions."""
+    out = dict(rec)
+    ex = rec["margin"] < BOUNDARY
+    idx = rec["idx"].copy()
+    idx[ex] = g_idx[ex]
+    out["idx"] = idx
+    if g_signs is not None and "signs" in rec:
+        flip = (idx != rec["idx"]).any(axis=1)
+        sex = (rec["sign_margin"] < BOUNDARY) | flip[:, None]
+        sg = rec["signs"].copy()
+        sg[sex] = g_signs[sex]
+        out["signs"] = sg
+        rn = rec["rnorm"].copy()
+        rn[flip] = g_rnorm[flip]
+        out["rnorm"] = rn
+    return out
+
+
 def unpack_flat_codes(words, bits, d):
     return OC.unpack_codes(words.reshape(-1, bits, d // 32), bits, d)
 

@@ -1,9 +1,12 @@
-"""Parity at the benchmark's full size (Qwen-like layer: batch 8, 32768
-tokens, window 128, FWHT, keys 2b + QJL, values 2b) in the launch
-configuration bench.py times (automatic split count), checked on sampled
-sequences the oracle recomputes on its own: every non-exempt score, the
-log-sum-exp and the output of all 24 query heads of sequences 0 and 5, plus
-the page records of sampled pages.
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (automatic split count), checked on sampled sequences the oracle
+recomputes on its own: every non-exempt score, the log-sum-exp and the output
+of all query heads of the sampled sequences, plus the page records of sampled
+pages.  Workloads: Qwen-like (batch 8, 32768 tokens, window 128, FWHT, keys
+2b + QJL, values 2b), Llama-like (batch 32, 8192 tokens, no window, dense Pi,
+outlier channels, keys 3b + QJL, values 4b) and long context (one sequence of
+131072 tokens, 8192 pages split over the grid).  Sequences are independent in
+decode, so the unsampled ones are filled on the device by another generator.
 """
 
 import math
@@ -18,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-SAMPLED = (0, 5)
+CASES = [("qwen", (0, 5)), ("llama", (0, 17)), ("long", (0,))]
 
 
 @pytest.fixture(scope="module")
@@ -33,25 +36,22 @@ def tq():
     return tq
 
 
-def test_fullsize_decode_sampled_sequences(tq):
-    w = SK.workload("qwen")
+@pytest.mark.parametrize("name,sampled", CASES)
+def test_fullsize_decode_sampled_sequences(tq, name, sampled):
+    w = SK.workload(name)
+    SAMPLED = sampled
     B, T, W = w.batch, w.ctx, w.window
     L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=W)
     O = PY.OracleLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=W)
     pc = tq.PagedCache(L, B, T)
+    K_all, V_all, q_all = SK.keys_values_torch(w)
     kv = {}
-    for b in range(B):  # one sequence at a time keeps host memory small
+    for b in SAMPLED:
         s = SK.keys_values(w, seqs=[b])
-        kt = SK.to_torch(s["K"], w.dtype).cuda()
-        vt = SK.to_torch(s["V"], w.dtype).cuda()
-        if b == 0:
-            K_all = torch.empty((B,) + tuple(kt.shape[1:]), dtype=kt.dtype, device="cuda")
-            V_all = torch.empty_like(K_all)
-            q_all = torch.empty((B,) + tuple(s["q"].shape[1:]), dtype=kt.dtype, device="cuda")
-        K_all[b], V_all[b] = kt[0], vt[0]
+        K_all[b] = SK.to_torch(s["K"][0], w.dtype).cuda()
+        V_all[b] = SK.to_torch(s["V"][0], w.dtype).cuda()
         q_all[b] = SK.to_torch(s["q"][0], w.dtype).cuda()
-        if b in SAMPLED:
-            kv[b] = s
+        kv[b] = s
     pc.prefill(K_all, V_all)
     del K_all, V_all
     ws = torch.empty(tq.decode_workspace_size(L.params, B, T), dtype=torch.uint8, device="cuda")
@@ -81,8 +81,8 @@ def test_fullsize_decode_sampled_sequences(tq):
                 PY.compare_records(sub_k, pg["kidx"], pg["knorm"], pg["ksigns"], pg["krnorm"], True, stats)
                 PY.compare_records(sub_v, pg["vidx"], pg["vnorm"], is_key=False, stats=stats)
         assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
-        win_k = s["K"][0, nc:T].transpose(1, 0, 2).astype(np.float16)
-        win_v = s["V"][0, nc:T].transpose(1, 0, 2).astype(np.float16)
+        win_k = s["K"][0, nc:T].transpose(1, 0, 2).astype(np.float16) if T > nc else None
+        win_v = s["V"][0, nc:T].transpose(1, 0, 2).astype(np.float16) if T > nc else None
         ref = PY.decode_reference(O, s["q"][0], PY.stack_comp(recs_k, recs_v), win_k, win_v, scale)
         g_sc = scores[b].cpu().numpy()
         G = w.n_q_heads // w.n_kv_heads
