@@ -441,13 +441,13 @@ static bool antisymmetric(const float* c, const float* t, int bits) {
   return true;
 }
 
-template <int BITS, bool QJL, bool DENSE, int MODE>
+template <int BITS, bool DENSE, int MODE>
 static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const void* x, long long n_vec,
                                         bool is_key, uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
                                         cudaStream_t st) {
-  constexpr int warps = wq::warps_for(QJL, DENSE);
-  auto kern = wq::quantize_warp_kernel<BITS, QJL, DENSE, MODE>;
-  const size_t sm = wq::smem_bytes(QJL, DENSE);
+  constexpr int warps = wq::warps_for(DENSE);
+  auto kern = wq::quantize_warp_kernel<BITS, DENSE, MODE>;
+  const size_t sm = wq::smem_bytes(DENSE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int occ = 0, dev = 0, sms = 0;
@@ -465,22 +465,56 @@ static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const
   return cudaGetLastError();
 }
 
-template <bool QJL, bool DENSE, int MODE>
+template <bool DENSE, int MODE>
 static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const KCache& C, const void* x,
                                              long long n_vec, bool is_key, uint32_t* codes, uint32_t* signs,
                                              float* norms, float* rnorms, cudaStream_t st) {
   switch (bits) {
-    case 1: return launch_quantize_warp<1, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    case 2: return launch_quantize_warp<2, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    case 3: return launch_quantize_warp<3, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-    default: return launch_quantize_warp<4, QJL, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 1: return launch_quantize_warp<1, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 2: return launch_quantize_warp<2, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    case 3: return launch_quantize_warp<3, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    default: return launch_quantize_warp<4, DENSE, MODE>(P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
   }
 }
 
 // Tensor-core path: d = 128, bf16, 16-byte aligned input, antisymmetric tables.
-static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key) {
+static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key, long long n_vec) {
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
-  return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0;
+  return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
+}
+
+template <int BITS, bool DENSE, int MODE>
+static cudaError_t launch_quantize_keys_tc(const KParams& P, const KCache& C, const void* x, long long n_vec,
+                                           uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
+                                           cudaStream_t st) {
+  auto kern = wq::quantize_keys_tc_kernel<BITS, DENSE, MODE>;
+  const size_t sm = wq::tc_smem_bytes(DENSE);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_ct = ((n_tok + 15) / 16 + wq::kTcWarps - 1) / wq::kTcWarps;
+  if (n_ct == 0) return cudaSuccess;
+  long long gx = std::max(1LL, (long long)sms / P.hkv);  // one CTA per SM (shared memory)
+  gx = std::min(gx, n_ct);
+  dim3 grid((int)std::min(gx, 65535LL), P.hkv);
+  kern<<<grid, 32 * wq::kTcWarps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, codes, signs,
+                                            norms, rnorms);
+  return cudaGetLastError();
+}
+
+template <bool DENSE, int MODE>
+static cudaError_t launch_quantize_keys_tc_bits(int bits, const KParams& P, const KCache& C, const void* x,
+                                                long long n_vec, uint32_t* codes, uint32_t* signs, float* norms,
+                                                float* rnorms, cudaStream_t st) {
+  switch (bits) {
+    case 1: return launch_quantize_keys_tc<1, DENSE, MODE>(P, C, x, n_vec, codes, signs, norms, rnorms, st);
+    case 2: return launch_quantize_keys_tc<2, DENSE, MODE>(P, C, x, n_vec, codes, signs, norms, rnorms, st);
+    case 3: return launch_quantize_keys_tc<3, DENSE, MODE>(P, C, x, n_vec, codes, signs, norms, rnorms, st);
+    default: return launch_quantize_keys_tc<4, DENSE, MODE>(P, C, x, n_vec, codes, signs, norms, rnorms, st);
+  }
 }
 
 template <int MODE>
@@ -489,16 +523,18 @@ static cudaError_t launch_quantize_warp_role(const KParams& P, const KCache& C, 
                                              float* rnorms, cudaStream_t st) {
   const bool qjl = is_key && P.kqjl;
   const int bits = is_key ? P.kb : P.vb;
+  if (qjl)  // keys with the sketch: tcgen05 for S r (record indices fit 32 bits)
+    return P.kind == TQ_FWHT
+               ? launch_quantize_keys_tc_bits<false, MODE>(bits, P, C, x, n_vec, codes, signs, norms, rnorms, st)
+               : launch_quantize_keys_tc_bits<true, MODE>(bits, P, C, x, n_vec, codes, signs, norms, rnorms, st);
   if (P.kind == TQ_FWHT)
-    return qjl ? launch_quantize_warp_bits<true, false, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-               : launch_quantize_warp_bits<false, false, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
-  return qjl ? launch_quantize_warp_bits<true, true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st)
-             : launch_quantize_warp_bits<false, true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+    return launch_quantize_warp_bits<false, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
+  return launch_quantize_warp_bits<true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
 }
 
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
-  if (warp_path_ok(P, x, dtype, is_key))
+  if (warp_path_ok(P, x, dtype, is_key, n_vec))
     return launch_quantize_warp_role<wq::kFlat>(P, KCache{}, x, n_vec, is_key, codes, signs, norms, rnorms, st);
   if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
   return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
@@ -525,7 +561,8 @@ cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* 
 template <int D>
 static cudaError_t launch_append_step_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                         cudaStream_t st) {
-  if (P.window == 0 && warp_path_ok(P, k, dtype, true) && warp_path_ok(P, v, dtype, false)) {
+  if (P.window == 0 && warp_path_ok(P, k, dtype, true, (long long)C.batch * P.hkv) &&
+      warp_path_ok(P, v, dtype, false, (long long)C.batch * P.hkv)) {
     // one sequence per row of the warp tiles: keys, values, then the counters
     const long long n_vec = (long long)C.batch * P.hkv;
     cudaError_t e = launch_quantize_warp_role<wq::kStep>(P, C, k, n_vec, true, nullptr, nullptr, nullptr, nullptr, st);

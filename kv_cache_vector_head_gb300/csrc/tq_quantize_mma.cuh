@@ -20,11 +20,13 @@
 //   * codes: sign and magnitude, the magnitude by binary search over the
 //     positive boundaries held in registers (bit width a template
 //     parameter); planes packed four at a time with one multiply;
-//   * QJL: S r as three f16 MMAs over hi / lo limbs of r and S (hi*hi +
-//     hi*lo + lo*hi).  Every entry whose magnitude is below a certified
-//     bound of the limb and accumulation errors (6e-5 ||r|| ||S_c||, a few
-//     per thousand vectors) is recomputed in fp32 by the warp from the
-//     limbs, so every sign is that of the fp32 product up to 2^-21 relative;
+//   * QJL keys (quantize_keys_tc_kernel): a CTA of 8 warps holds 128
+//     vectors, one UMMA M = 128 tile; S r runs as tcgen05.mma over hi / lo
+//     f16 limbs of r and S (hi*hi + hi*lo + lo*hi) into tensor memory.
+//     Every entry whose magnitude is below a certified bound of the limb and
+//     accumulation errors (6e-5 ||r|| ||S_c||, a few per thousand vectors)
+//     is recomputed in fp32 by the warp from the limbs, so every sign is
+//     that of the fp32 product up to 2^-21 relative;
 //   * norms in fp32 with balanced summation trees (relative error at most
 //     about 8 u before the square root halves it), scales taken as
 //     sqrt(d / s) and sqrt(s_r / d) (d a power of two).
@@ -65,31 +67,24 @@ __host__ __device__ constexpr int sk_out(int nt, int n) {
 }
 
 struct Shared {
-  float snorm[D];              // ||S_c|| (rounded up)
   uint2 hfrag[KB][2][32];      // FWHT H_16 * sigma fragments (bf16)
 };
-constexpr size_t kSfragBytes = (size_t)2 * 16 * KB * 32 * sizeof(uint2);  // S as f16 hi and lo limbs
 constexpr size_t kPfragBytes = (size_t)3 * 16 * KB * 32 * sizeof(uint2);  // Pi limbs (bf16)
-// Per-warp block buffer: [2][KB][32] uint4.  FWHT: the rotated tile (R = 0
-// rows in half 0, R = 1 rows in half 1); keys: then the residual's f16 hi
-// and lo limbs in A-fragment order, written over the same slots.
+// Per-warp block buffer: [2][KB][32] uint4, FWHT only: the rotated tile
+// (R = 0 rows in half 0, R = 1 rows in half 1).
 constexpr size_t kBlkBytes = (size_t)2 * KB * 32 * sizeof(uint4);
 
-// FWHT: 12 warps, next tile staged in shared memory by cp.async; dense: the
-// Pi limbs fill most of shared memory (7 warps with the sketch, 8 and two
-// CTAs per SM without), next tile prefetched into registers.
-__host__ __device__ constexpr int warps_for(bool qjl, bool dense) { return dense ? (qjl ? 7 : 8) : 12; }
-__host__ __device__ constexpr int ctas_for(bool qjl, bool dense) { return dense && !qjl ? 2 : 1; }
-__host__ __device__ constexpr size_t blk_bytes(bool qjl, bool dense) {
-  return (qjl || !dense) ? (size_t)warps_for(qjl, dense) * kBlkBytes : 0;
-}
-__host__ __device__ constexpr size_t stage_bytes(bool qjl, bool dense) {
-  return dense ? 0 : (size_t)warps_for(qjl, dense) * 8 * 32 * sizeof(uint4);
+// FWHT: 12 warps, next tile staged in shared memory by cp.async; dense: 8
+// warps, two CTAs per SM, next tile prefetched into registers.
+__host__ __device__ constexpr int warps_for(bool dense) { return dense ? 8 : 12; }
+__host__ __device__ constexpr int ctas_for(bool dense) { return dense ? 2 : 1; }
+__host__ __device__ constexpr size_t blk_bytes(bool dense) { return dense ? 0 : (size_t)warps_for(dense) * kBlkBytes; }
+__host__ __device__ constexpr size_t stage_bytes(bool dense) {
+  return dense ? 0 : (size_t)warps_for(dense) * 8 * 32 * sizeof(uint4);
 }
 
-__host__ __device__ constexpr size_t smem_bytes(bool qjl, bool dense) {
-  return sizeof(Shared) + (qjl ? kSfragBytes : 0) + (dense ? kPfragBytes : 0) + blk_bytes(qjl, dense) +
-         stage_bytes(qjl, dense);
+__host__ __device__ constexpr size_t smem_bytes(bool dense) {
+  return sizeof(Shared) + (dense ? kPfragBytes : 0) + blk_bytes(dense) + stage_bytes(dense);
 }
 
 // 16-byte global -> shared copy; src_bytes = 0 fills zeros.
@@ -118,6 +113,7 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t bf16_bits(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 __device__ __forceinline__ uint32_t f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -180,25 +176,24 @@ __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushor
 // block_table[b][seq_len[b] / 16]).
 enum { kFlat = 0, kStep = 1 };
 
-// QJL: keys with the sketch; DENSE: dense rotation (else FWHT).  grid (x, Hkv).
-template <int BITS, bool QJL, bool DENSE, int MODE>
-__global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENSE))
+// Values, and keys without the QJL sketch (keys with it: quantize_keys_tc_kernel).
+// DENSE: dense rotation (else FWHT).  grid (x, Hkv).
+template <int BITS, bool DENSE, int MODE>
+__global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
     quantize_warp_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
                          const __nv_bfloat16* __restrict__ x, long long n_vec, int is_key,
                          uint32_t* __restrict__ codes, uint32_t* __restrict__ signs, float* __restrict__ norms,
                          float* __restrict__ rnorms) {
-  constexpr int WARPS = warps_for(QJL, DENSE);
+  constexpr int WARPS = warps_for(DENSE);
   constexpr int NT = 32 * WARPS;
   constexpr int HALF = 1 << (BITS - 1);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned char* dyn = smem_raw + sizeof(Shared);
-  uint2* sfrag = reinterpret_cast<uint2*>(dyn);  // [2 limbs][16][KB][32]
-  dyn += QJL ? kSfragBytes : 0;
   uint2* pfrag = reinterpret_cast<uint2*>(dyn);  // [3][16][KB][32]
   dyn += DENSE ? kPfragBytes : 0;
   uint4* blk = reinterpret_cast<uint4*>(dyn);    // [WARPS][2][KB][32]
-  dyn += blk_bytes(QJL, DENSE);
+  dyn += blk_bytes(DENSE);
   uint4* stage = reinterpret_cast<uint4*>(dyn);  // [WARPS][8][32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
@@ -206,7 +201,6 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
   const float* ctab = is_key ? P.kc : P.vc;
   const float* ttab = is_key ? P.kt : P.vt;
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
-  const float* S = QJL ? P.qjl_s + (size_t)head * D * D : nullptr;
   Book<BITS> bk;
 #pragma unroll
   for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(ttab[HALF + k]);
@@ -264,48 +258,6 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
         pfrag[((k * 16 + nt) * KB + kk) * 32 + ln] = make_uint2(l[k][0] | (l[k][1] << 16), l[k][2] | (l[k][3] << 16));
     }
   }
-  if constexpr (QJL) {
-    constexpr int PER = (16 * KB * 32 + NT - 1) / NT;
-    float4 sv4[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int i = tid + j * NT;
-      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = (i >> 8) & 15;
-      sv4[j] = i < 16 * KB * 32
-                   ? __ldg(reinterpret_cast<const float4*>(S + (size_t)sk_out(nt, ln >> 2) * D + blk_base(kk) + 8 * (ln & 3)))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int i = tid + j * NT;
-      if (i >= 16 * KB * 32) break;
-      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
-      const float4 v4 = sv4[j];
-      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        hi[e] = f16_bits(v[e]);
-        lo[e] = f16_bits(v[e] - __half2float(__float2half_rn(v[e])));
-      }
-      sfrag[(nt * KB + kk) * 32 + ln] = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-      sfrag[((16 + nt) * KB + kk) * 32 + ln] = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
-    }
-    // ||S_c||: thread c sums its row from the fragments' source (fp32, L2-hot)
-    for (int c = tid; c < D; c += NT) {
-      const float4* row = reinterpret_cast<const float4*>(S + (size_t)c * D);
-      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int i = 0; i < D / 4; ++i) {
-        const float4 v = __ldg(row + i);
-        acc4.x = fmaf(v.x, v.x, acc4.x);
-        acc4.y = fmaf(v.y, v.y, acc4.y);
-        acc4.z = fmaf(v.z, v.z, acc4.z);
-        acc4.w = fmaf(v.w, v.w, acc4.w);
-      }
-      sh.snorm[c] = sqrtf((acc4.x + acc4.y) + (acc4.z + acc4.w)) * 1.0001f;
-    }
-  }
   __syncthreads();
 
   // ---- tiles of 16 tokens of this head
@@ -313,14 +265,6 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
   const long long n_tiles = (n_tok + 15) / 16;
   const long long stride = (long long)gridDim.x * WARPS;
   uint4* wb = blk + (size_t)warp * 2 * KB * 32;  // this warp's block buffer: wb[(half * KB + a) * 32 + lane]
-  // |three-limb f16 product - exact product of the fp32 values|
-  //   <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||):
-  // k1 covers the dropped lo*lo term and the limb roundings (3 * 2^-22) and
-  // the fp32 accumulation over 24 chained MMAs even if every MMA truncated
-  // each of its 17 addends by one unit in the last place (24 * 17 * 2^-23);
-  // k2 covers f16 subnormal limbs (2^-25 per element, times sqrt(d))
-  const float k1 = 6e-5f, k2 = 4e-7f;
-
   auto row_index = [&](long long mt, int R, long long& n) -> bool {
     const long long tok = mt * 16 + g + 8 * R;
     n = tok * P.hkv + head;
@@ -455,12 +399,10 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
     }
 
     // codes, two blocks (one packed word) per pass
-    float rs[2] = {0.f, 0.f};  // ||r||^2: block sums, pairs, then the four words in turn
     uint32_t vword[2][4];      // step mode, values: plane t of words 0..3 of rows g, g + 8
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       uint32_t Wm[2] = {0u, 0u};  // byte p: plane p of this lane's byte of word m
-      float pr[2] = {0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int a = 2 * m + hh;
@@ -504,7 +446,6 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
             zr[R][3] = __uint_as_float(v.w);
           }
         }
-        float rv[2][4];
 #pragma unroll
         for (int R = 0; R < 2; ++R)
 #pragma unroll
@@ -517,26 +458,10 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
             const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
             const int pos = 4 * hh + i;  // coordinate blk_base(a) + 8t + i is bit 8t + 4hh + i of word m
             Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
-            if constexpr (QJL) rv[R][i] = z - __uint_as_float(__float_as_uint(centroid_pos<BITS>(mag, bk)) ^ (neg << 31));
           }
-        if constexpr (QJL) {
-          // residual limbs in A-fragment order (rows g, g+8; coordinate pairs 8t+{0,1}, 8t+{2,3})
-          const float2 p0 = make_float2(rv[0][0], rv[0][1]), p1 = make_float2(rv[1][0], rv[1][1]);
-          const float2 p2 = make_float2(rv[0][2], rv[0][3]), p3 = make_float2(rv[1][2], rv[1][3]);
-          const uint32_t h0 = pack_f16(p0.x, p0.y), h1 = pack_f16(p1.x, p1.y);
-          const uint32_t h2 = pack_f16(p2.x, p2.y), h3 = pack_f16(p3.x, p3.y);
-          wb[(0 * KB + a) * 32 + lane] = make_uint4(h0, h1, h2, h3);
-          wb[(1 * KB + a) * 32 + lane] =
-              make_uint4(pack_f16(p0.x - f16lo(h0), p0.y - f16hi(h0)), pack_f16(p1.x - f16lo(h1), p1.y - f16hi(h1)),
-                         pack_f16(p2.x - f16lo(h2), p2.y - f16hi(h2)), pack_f16(p3.x - f16lo(h3), p3.y - f16hi(h3)));
-#pragma unroll
-          for (int R = 0; R < 2; ++R)
-            pr[R] += (rv[R][0] * rv[R][0] + rv[R][1] * rv[R][1]) + (rv[R][2] * rv[R][2] + rv[R][3] * rv[R][3]);
-        }
       }
 #pragma unroll
       for (int R = 0; R < 2; ++R) {
-        rs[R] += pr[R];
         const uint32_t word = quad_transpose(Wm[R], t);  // plane t of word m
         if (okrow[R] && t < BITS) {
           if constexpr (MODE == kFlat) {
@@ -580,108 +505,532 @@ __global__ void __launch_bounds__(32 * warps_for(QJL, DENSE), ctas_for(QJL, DENS
       }
     }
 
-    if constexpr (QJL) {
-      float gam[2], bA[2], bB[2];
+    __syncwarp();  // the block buffer is rewritten by the next tile
+  }
+}
+
+
+// ------------------------------------------------------------------ keys: QJL sketch on tcgen05
+//
+// Keys with the QJL sketch.  A CTA of 8 warps owns 128 vectors per pass (one
+// UMMA M = 128 tile): every warp rotates, codes and packs its 16 vectors as in
+// quantize_warp_kernel and writes the residual's f16 hi / lo limbs into the A
+// tiles; one thread then issues S r as tcgen05.mma kind::f16 (hi*hi + hi*lo +
+// lo*hi, fp32 accumulator of 128 x 128 in tensor memory) and the epilogue
+// reads one vector per thread (tcgen05.ld 32x32b), packs its sign words and
+// recomputes the uncertain entries in fp32 from the limbs in shared memory.
+
+constexpr int kTcWarps = 8;
+constexpr size_t kUmmaTile = (size_t)128 * 128 * 2;  // one 128 x 128 16-bit operand
+
+// Canonical K-major operand without swizzle: 8 x 8 core matrices of 16-byte
+// rows; K-chunk stride 128 B (leading byte offset), 8-row group stride 2048 B
+// (stride byte offset).
+__host__ __device__ constexpr uint32_t umma_off(int row, int k) {
+  return (uint32_t)((row >> 3) * 2048 + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(2048 >> 4) << 32) |
+         ((uint64_t)1 << 46);  // descriptor version 1, no swizzle
+}
+
+struct TcShared {
+  float snorm[D];      // ||S_c|| (rounded up)
+  float s2[128];       // ||r||^2 of each row (z units)
+  uint32_t rec[128];   // flat: record index; step: page * Hkv + head
+  uint8_t slot[128];   // step: slot in the page
+  uint8_t flags[128];  // bit 0 row holds a vector, bit 1 zero vector
+  uint64_t mbar;
+  uint32_t tmem;
+};
+
+__host__ __device__ constexpr size_t tc_rest_bytes(bool dense) {
+  return dense ? kPfragBytes : (size_t)KB * 2 * 32 * sizeof(uint2) + (size_t)kTcWarps * kBlkBytes;
+}
+__host__ __device__ constexpr size_t tc_smem_bytes(bool dense) {
+  return 4 * kUmmaTile + tc_rest_bytes(dense) + sizeof(TcShared);
+}
+
+template <int BITS, bool DENSE, int MODE>
+__global__ void __launch_bounds__(32 * kTcWarps, 1)
+    quantize_keys_tc_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
+                            const __nv_bfloat16* __restrict__ x, long long n_vec, uint32_t* __restrict__ codes,
+                            uint32_t* __restrict__ signs, float* __restrict__ norms, float* __restrict__ rnorms) {
+  constexpr int WARPS = kTcWarps;
+  constexpr int NT = 32 * WARPS;
+  constexpr int HALF = 1 << (BITS - 1);
+  extern __shared__ __align__(16) unsigned char smem_raw[];  // the no-swizzle operand layout needs 16-byte alignment
+  unsigned char* Ahi = smem_raw;
+  unsigned char* Alo = smem_raw + kUmmaTile;
+  unsigned char* Bhi = smem_raw + 2 * kUmmaTile;
+  unsigned char* Blo = smem_raw + 3 * kUmmaTile;
+  unsigned char* rest = smem_raw + 4 * kUmmaTile;
+  uint2* pfrag = reinterpret_cast<uint2*>(rest);                                     // dense: [3][16][KB][32]
+  uint2* hfrag = reinterpret_cast<uint2*>(rest);                                     // FWHT: [KB][2][32]
+  uint4* blk = reinterpret_cast<uint4*>(rest + (size_t)KB * 2 * 32 * sizeof(uint2));  // FWHT: [WARPS][2][KB][32]
+  TcShared& ts = *reinterpret_cast<TcShared*>(rest + tc_rest_bytes(DENSE));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  const int head = blockIdx.y;
+  const float* rot = P.k_rot + (size_t)head * (DENSE ? D * D : D);
+  const float* S = P.qjl_s + (size_t)head * D * D;
+  Book<BITS> bk;
 #pragma unroll
-      for (int R = 0; R < 2; ++R) {
-        float s2 = rs[R];
-        s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-        gam[R] = sqrtf(s2 * (1.0f / D));  // exact scaling by a power of two
-        const float rn = sqrtf(s2);
-        bA[R] = fmaf(k1, rn, k2);
-        bB[R] = k2 * rn + k2;
+  for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(P.kt[HALF + k]);
+#pragma unroll
+  for (int m = 0; m < HALF; ++m) bk.cp[m] = P.kc[HALF + m];
+
+  if (warp == 0) {  // tensor memory: the 128 x 128 fp32 accumulator of S r
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ts.tmem)),
+                 "r"(128));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&ts.mbar)), "r"(1));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  // ---- per-CTA constants: rotation fragments (mma.sync), S limbs (UMMA B tiles), ||S_c||
+  if constexpr (!DENSE) {
+    for (int i = tid; i < KB * 2 * 32; i += NT) {
+      const int ln = i & 31, nt = (i >> 5) & 1, kk = i >> 6;
+      const int gg = ln >> 2, tt = ln & 3;
+      const float4 sg = __ldg(reinterpret_cast<const float4*>(rot + blk_base(kk) + 8 * tt));
+      const float sv[4] = {sg.x, sg.y, sg.z, sg.w};
+      const int out = 8 * (gg >> 1) + 2 * nt + (gg & 1);
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int L = 2 * tt + (e & 1) + 8 * (e >> 1);
+        const bool neg = (sv[e] < 0.f) != (bool)(__popc(free_off(L) & out) & 1);
+        h[e] = neg ? 0xBF80u : 0x3F80u;
       }
-      uint32_t rA[KB][4];
+      hfrag[(kk * 2 + nt) * 32 + ln] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    }
+  } else {
+    constexpr int PER = (16 * KB * 32 + NT - 1) / NT;
+    float4 pv[PER];
 #pragma unroll
-      for (int a = 0; a < KB; ++a) {
-        const uint4 v = wb[(0 * KB + a) * 32 + lane];
-        rA[a][0] = v.x;
-        rA[a][1] = v.y;
-        rA[a][2] = v.z;
-        rA[a][3] = v.w;
-      }
-      __syncwarp();  // residual limbs visible to the whole warp for the fp32 recomputations
-      const uint32_t zmask = (zero[0] ? 0xffu : 0u) | (zero[1] ? 0xff00u : 0u);
-      uint32_t SB[2] = {0u, 0u};
-#pragma unroll 1
-      for (int w = 0; w < 4; ++w) {
-        float sacc[4][4];
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = (i >> 8) & 15;
+      pv[j] = i < 16 * KB * 32
+                  ? __ldg(reinterpret_cast<const float4*>(rot + (size_t)rot_out(nt, ln >> 2) * D + blk_base(kk) + 8 * (ln & 3)))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      if (i >= 16 * KB * 32) break;
+      const int ln = i & 31, kk = (i >> 5) & (KB - 1), nt = i >> 8;
+      const float v[4] = {pv[j].x, pv[j].y, pv[j].z, pv[j].w};
+      uint32_t l[3][4];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) sacc[q][r] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KB; ++kk) {
-          const uint4 lo = wb[(1 * KB + kk) * 32 + lane];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint2 bh = sfrag[((4 * w + q) * KB + kk) * 32 + lane];
-            const uint2 bl = sfrag[((16 + 4 * w + q) * KB + kk) * 32 + lane];
-            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], bh);
-            mma_f16(sacc[q], rA[kk][0], rA[kk][1], rA[kk][2], rA[kk][3], bl);
-            mma_f16(sacc[q], lo.x, lo.y, lo.z, lo.w, bh);
-          }
-        }
-        const float4 sn0 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t]);
-        const float4 sn1 = *reinterpret_cast<const float4*>(&sh.snorm[32 * w + 8 * t + 4]);
-        const float sn[8] = {sn0.x, sn0.y, sn0.z, sn0.w, sn1.x, sn1.y, sn1.z, sn1.w};
-        uint32_t sb = 0, pend = 0;  // bit 8R + 2q + e
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int R = r >> 1, e = r & 1, bit = 8 * R + 2 * q + e;
-            const float v = sacc[q][r];
-            sb |= (uint32_t)(v >= 0.f) << bit;
-            pend |= (uint32_t)(fabsf(v) < fmaf(sn[2 * q + e], bA[R], bB[R])) << bit;
-          }
-        sb |= zmask;
-        pend &= ~zmask;
-        // fp32 recomputation of the uncertain entries, one per pass of the warp,
-        // from the f16 hi + lo limbs of r and S (22 bits each); lane l covers
-        // coordinates blk_base(l / 4) + 8 (l % 4) + 0..3, which are one B
-        // fragment of the sketch row
-        while (true) {
-          const unsigned ball = __ballot_sync(0xffffffffu, pend != 0);
-          if (ball == 0) break;
-          const int src = __ffs(ball) - 1;
-          const int bit = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
-          const int row = (src >> 2) + 8 * (bit >> 3), R = row >> 3;
-          const int nt = 4 * w + ((bit >> 1) & 3), n = 2 * (src & 3) + (bit & 1);  // sketch coordinate sk_out(nt, n)
-          const int ab = lane >> 2, tl = lane & 3;
-          const uint32_t* hi = reinterpret_cast<const uint32_t*>(wb + (0 * KB + ab) * 32 + (row & 7) * 4 + tl);
-          const uint32_t* lo = reinterpret_cast<const uint32_t*>(wb + (1 * KB + ab) * 32 + (row & 7) * 4 + tl);
-          const uint32_t h01 = hi[R], h23 = hi[2 + R], l01 = lo[R], l23 = lo[2 + R];
-          const uint2 sh2 = sfrag[(nt * KB + ab) * 32 + 4 * n + tl];
-          const uint2 sl2 = sfrag[((16 + nt) * KB + ab) * 32 + 4 * n + tl];
-          float dsum = (f16lo(h01) + f16lo(l01)) * (f16lo(sh2.x) + f16lo(sl2.x));
-          dsum = fmaf(f16hi(h01) + f16hi(l01), f16hi(sh2.x) + f16hi(sl2.x), dsum);
-          dsum = fmaf(f16lo(h23) + f16lo(l23), f16lo(sh2.y) + f16lo(sl2.y), dsum);
-          dsum = fmaf(f16hi(h23) + f16hi(l23), f16hi(sh2.y) + f16hi(sl2.y), dsum);
-          dsum = warp_sum_f(dsum);
-          if (lane == src) {
-            sb = (sb & ~(1u << bit)) | ((uint32_t)(dsum >= 0.f) << bit);
-            pend &= ~(1u << bit);
-          }
-        }
-        SB[0] |= (sb & 0xffu) << (8 * w);
-        SB[1] |= ((sb >> 8) & 0xffu) << (8 * w);
+      for (int e = 0; e < 4; ++e) {
+        const float l0 = __bfloat162float(__float2bfloat16_rn(v[e]));
+        const float l1 = __bfloat162float(__float2bfloat16_rn(v[e] - l0));
+        l[0][e] = bf16_bits(v[e]);
+        l[1][e] = bf16_bits(v[e] - l0);
+        l[2][e] = bf16_bits((v[e] - l0) - l1);
       }
 #pragma unroll
-      for (int R = 0; R < 2; ++R) {
-        const uint32_t word = quad_transpose(SB[R], t);
-        if constexpr (MODE == kFlat) {
-          if (okrow[R]) signs[(size_t)nrow[R] * 4 + t] = word;
-          if (okrow[R] && t == 0) rnorms[nrow[R]] = zero[R] ? 0.f : gam[R];
-        } else {
-          if (okrow[R]) reinterpret_cast<uint32_t*>(dst[R] + P.off_ksigns)[slot[R] * 4 + t] = word;
-          if (okrow[R] && t == 0) reinterpret_cast<float*>(dst[R] + P.off_krnorm)[slot[R]] = zero[R] ? 0.f : gam[R];
+      for (int k = 0; k < 3; ++k)
+        pfrag[((k * 16 + nt) * KB + kk) * 32 + ln] = make_uint2(l[k][0] | (l[k][1] << 16), l[k][2] | (l[k][3] << 16));
+    }
+  }
+  {
+    // S as UMMA B operands: row c of S (sketch coordinate), K = input coordinate
+    constexpr int PER = 128 * 32 / NT;  // float4 chunks per thread
+    float4 sv[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT;
+      sv[j] = __ldg(reinterpret_cast<const float4*>(S + (size_t)(i >> 5) * D) + (i & 31));
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = tid + j * NT, c = i >> 5, k0 = 4 * (i & 31);
+      const float v[4] = {sv[j].x, sv[j].y, sv[j].z, sv[j].w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = f16_bits(v[e]);
+        lo[e] = f16_bits(v[e] - __half2float(__float2half_rn(v[e])));
+      }
+      *reinterpret_cast<uint2*>(Bhi + umma_off(c, k0)) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+      *reinterpret_cast<uint2*>(Blo + umma_off(c, k0)) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+    }
+    for (int c = tid; c < D; c += NT) {
+      const float4* row = reinterpret_cast<const float4*>(S + (size_t)c * D);
+      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int i = 0; i < D / 4; ++i) {
+        const float4 v = __ldg(row + i);
+        acc4.x = fmaf(v.x, v.x, acc4.x);
+        acc4.y = fmaf(v.y, v.y, acc4.y);
+        acc4.z = fmaf(v.z, v.z, acc4.z);
+        acc4.w = fmaf(v.w, v.w, acc4.w);
+      }
+      ts.snorm[c] = sqrtf((acc4.x + acc4.y) + (acc4.z + acc4.w)) * 1.0001f;
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = ts.tmem;
+
+  // ---- passes over 128 vectors (8 warp tiles of 16 tokens of this head)
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 15) / 16;
+  const long long n_ct = (n_tiles + WARPS - 1) / WARPS;
+  uint4* wb = blk + (size_t)warp * 2 * KB * 32;  // FWHT: this warp's rotated tile
+  // |three-limb f16 product - exact product of the fp32 values|
+  //   <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||):
+  // k1 covers the dropped lo*lo term and the limb roundings (3 * 2^-22) and
+  // the fp32 accumulation over 24 chained MMA steps even if every step
+  // truncated each of its 17 addends by one unit in the last place
+  // (24 * 17 * 2^-23); k2 covers f16 subnormal limbs (2^-25 per element,
+  // times sqrt(d))
+  const float k1 = 6e-5f, k2 = 4e-7f;
+  // instruction descriptor: D f32, A and B f16, both K-major, N = 128, M = 128
+  const uint32_t idesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+  auto row_index = [&](long long mt, int R, long long& n) -> bool {
+    const long long tok = mt * 16 + g + 8 * R;
+    n = tok * P.hkv + head;
+    return tok < n_tok && n < n_vec;
+  };
+  uint4 nxt[2][4];
+  auto load = [&](long long mt) {
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      long long n;
+      const bool ok = row_index(mt, R, n);
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * D) + t;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) nxt[R][m] = ok ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint32_t phase = 0;
+  bool failed = false;
+  if (blockIdx.x < n_ct) load((long long)blockIdx.x * WARPS + warp);
+  for (long long ct = blockIdx.x; ct < n_ct && !failed; ct += gridDim.x) {
+    const long long mt = ct * WARPS + warp;
+    uint4 X[2][4];
+#pragma unroll
+    for (int R = 0; R < 2; ++R)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) X[R][m] = nxt[R][m];
+    if (ct + gridDim.x < n_ct) load((ct + gridDim.x) * WARPS + warp);
+
+    long long nrow[2];
+    bool okrow[2];
+    unsigned char* dst[2] = {nullptr, nullptr};
+    uint32_t recv[2] = {0u, 0u};
+    int slot[2] = {0, 0};
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      okrow[R] = row_index(mt, R, nrow[R]);
+      recv[R] = (uint32_t)nrow[R];
+      if constexpr (MODE == kStep) {
+        if (okrow[R]) {
+          const int b = (int)(nrow[R] / P.hkv);
+          const int T = C.seq_len[b];
+          const int pidx = T >> 4;
+          long long page = -1;
+          if (T >= 0 && pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
+          if (page < 0 || page >= C.n_pages) {
+            if (t == 0) atomicOr(&g_quant_err, (T >= 0 && pidx < C.max_pages) ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
+            okrow[R] = false;
+          } else {
+            recv[R] = (uint32_t)(page * P.hkv + head);
+            dst[R] = C.pool + (size_t)recv[R] * (size_t)P.sub_bytes;
+            slot[R] = T & 15;
+          }
         }
       }
     }
-    __syncwarp();  // the block buffer is rewritten by the next tile
+
+    // norms (balanced fp32 tree over exact bf16 squares)
+    float inv[2];
+    bool zero[2];
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      float part[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t w[4] = {X[R][m].x, X[R][m].y, X[R][m].z, X[R][m].w};
+        float q2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+          q2[k] = lo * lo + hi * hi;
+        }
+        part[m] = (q2[0] + q2[1]) + (q2[2] + q2[3]);
+      }
+      float s2 = (part[0] + part[1]) + (part[2] + part[3]);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+      const float n = sqrtf(s2);
+      zero[R] = n < kZeroNorm;
+      inv[R] = zero[R] ? 0.f : sqrtf((DENSE ? (float)D : 1.0f) / s2);
+      if (okrow[R] && t == 0) {
+        if constexpr (MODE == kFlat) norms[nrow[R]] = zero[R] ? 0.f : n;
+        else reinterpret_cast<float*>(dst[R] + P.off_knorm)[slot[R]] = zero[R] ? 0.f : n;
+      }
+    }
+
+    if constexpr (!DENSE) {
+      float acc[KB][2][4];
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) {
+        const uint4& u0 = X[0][kk >> 1];
+        const uint4& u1 = X[1][kk >> 1];
+        const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
+        const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[kk][h][r] = 0.f;
+          mma_bf16(acc[kk][h], a0, a1, a2, a3, hfrag[(kk * 2 + h) * 32 + lane]);
+        }
+      }
+#pragma unroll
+      for (int s = 1; s < KB; s <<= 1)
+#pragma unroll
+        for (int a = 0; a < KB; ++a)
+          if ((a & s) == 0)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const float p = acc[a][h][r], q = acc[a + s][h][r];
+                acc[a][h][r] = p + q;
+                acc[a + s][h][r] = p - q;
+              }
+#pragma unroll
+      for (int a = 0; a < KB; ++a) {
+        wb[(0 * KB + a) * 32 + lane] = make_uint4(__float_as_uint(acc[a][0][0]), __float_as_uint(acc[a][0][1]),
+                                                  __float_as_uint(acc[a][1][0]), __float_as_uint(acc[a][1][1]));
+        wb[(1 * KB + a) * 32 + lane] = make_uint4(__float_as_uint(acc[a][0][2]), __float_as_uint(acc[a][0][3]),
+                                                  __float_as_uint(acc[a][1][2]), __float_as_uint(acc[a][1][3]));
+      }
+    }
+
+    // codes and the residual limbs (A tiles), two blocks per pass
+    float rs[2] = {0.f, 0.f};
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      uint32_t Wm[2] = {0u, 0u};
+      float pr[2] = {0.f, 0.f};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int a = 2 * m + hh;
+        float zr[2][4];
+        if constexpr (DENSE) {
+          float c[4][2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) c[i][h][r] = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < KB; ++kk) {
+            const uint4& u0 = X[0][kk >> 1];
+            const uint4& u1 = X[1][kk >> 1];
+            const uint32_t a0 = (kk & 1) ? u0.z : u0.x, a2 = (kk & 1) ? u0.w : u0.y;
+            const uint32_t a1 = (kk & 1) ? u1.z : u1.x, a3 = (kk & 1) ? u1.w : u1.y;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint2* pf = pfrag + ((2 * a + h) * KB + kk) * 32 + lane;
+              mma_bf16(c[kk & 1][h], a0, a1, a2, a3, pf[0]);
+              mma_bf16(c[2][h], a0, a1, a2, a3, pf[16 * KB * 32]);
+              mma_bf16(c[3][h], a0, a1, a2, a3, pf[2 * 16 * KB * 32]);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              zr[r >> 1][2 * h + (r & 1)] = (c[0][h][r] + c[1][h][r]) + (c[2][h][r] + c[3][h][r]);
+        } else {
+#pragma unroll
+          for (int R = 0; R < 2; ++R) {
+            const uint4 v = wb[(R * KB + a) * 32 + lane];
+            zr[R][0] = __uint_as_float(v.x);
+            zr[R][1] = __uint_as_float(v.y);
+            zr[R][2] = __uint_as_float(v.z);
+            zr[R][3] = __uint_as_float(v.w);
+          }
+        }
+        float rv[2][4];
+#pragma unroll
+        for (int R = 0; R < 2; ++R)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);
+            const uint32_t zb = __float_as_uint(z);
+            const uint32_t neg = zb >> 31;
+            const int ai = (int)(zb & 0x7fffffffu) - (int)neg;
+            const int mag = magnitude<BITS>(ai, bk);
+            const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
+            const int pos = 4 * hh + i;
+            Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
+            rv[R][i] = z - __uint_as_float(__float_as_uint(centroid_pos<BITS>(mag, bk)) ^ (neg << 31));
+          }
+        const int j0 = blk_base(a) + 8 * t;  // this lane's four coordinates of block a
+#pragma unroll
+        for (int R = 0; R < 2; ++R) {
+          const int row = 16 * warp + g + 8 * R;
+          const uint32_t h01 = pack_f16(rv[R][0], rv[R][1]), h23 = pack_f16(rv[R][2], rv[R][3]);
+          *reinterpret_cast<uint2*>(Ahi + umma_off(row, j0)) = make_uint2(h01, h23);
+          *reinterpret_cast<uint2*>(Alo + umma_off(row, j0)) =
+              make_uint2(pack_f16(rv[R][0] - f16lo(h01), rv[R][1] - f16hi(h01)),
+                         pack_f16(rv[R][2] - f16lo(h23), rv[R][3] - f16hi(h23)));
+          pr[R] += (rv[R][0] * rv[R][0] + rv[R][1] * rv[R][1]) + (rv[R][2] * rv[R][2] + rv[R][3] * rv[R][3]);
+        }
+      }
+#pragma unroll
+      for (int R = 0; R < 2; ++R) {
+        rs[R] += pr[R];
+        const uint32_t word = quad_transpose(Wm[R], t);
+        if (okrow[R] && t < BITS) {
+          if constexpr (MODE == kFlat) codes[(size_t)nrow[R] * BITS * 4 + t * 4 + m] = word;
+          else reinterpret_cast<uint32_t*>(dst[R] + P.off_kcodes)[(t * 16 + slot[R]) * 4 + m] = word;
+        }
+      }
+    }
+#pragma unroll
+    for (int R = 0; R < 2; ++R) {
+      float s2 = rs[R];
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+      if (t == 0) {
+        const int row = 16 * warp + g + 8 * R;
+        ts.s2[row] = s2;
+        ts.rec[row] = recv[R];
+        ts.slot[row] = (uint8_t)slot[R];
+        ts.flags[row] = (uint8_t)((okrow[R] ? 1 : 0) | (zero[R] ? 2 : 0));
+      }
+    }
+
+    // ---- S r on the tensor cores: 3 limb products x 8 k-steps into tensor memory
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tid == 0) {
+      const uint32_t a_hi = smem_u32(Ahi), a_lo = smem_u32(Alo), b_hi = smem_u32(Bhi), b_lo = smem_u32(Blo);
+      const uint32_t as_[3] = {a_hi, a_hi, a_lo}, bs_[3] = {b_hi, b_lo, b_hi};
+#pragma unroll
+      for (int pss = 0; pss < 3; ++pss)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t accum = (pss > 0 || ks > 0) ? 1u : 0u;
+          asm volatile(
+              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+              " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+              "l"(umma_desc(as_[pss] + 256 * ks)), "l"(umma_desc(bs_[pss] + 256 * ks)), "r"(idesc), "r"(accum));
+        }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(&ts.mbar)));
+    }
+    uint32_t done = 0;
+    for (unsigned it = 0; it < (1u << 22) && !done; ++it) {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(smem_u32(&ts.mbar)), "r"(phase));
+    }
+    phase ^= 1u;
+    if (__syncthreads_or(!done)) {  // the sketch never completed: flag it, stop cleanly
+      if (tid == 0) atomicOr(&g_quant_err, TQ_DEVERR_TIMEOUT);
+      failed = true;
+      break;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // ---- epilogue: vector row = 32 (warp % 4) + lane, sketch coordinates 64 (warp / 4) .. + 63
+    {
+      const int row = 32 * (warp & 3) + lane, hcol = 64 * (warp >> 2);
+      const uint32_t fl = ts.flags[row];
+      const bool ok = fl & 1u, zr = fl & 2u;
+      const float s2 = ts.s2[row];
+      const float rn = sqrtf(s2);
+      const float bA = fmaf(k1, rn, k2), bB = fmaf(k2, rn, k2);
+      const uint32_t rec = ts.rec[row];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = hcol + 32 * cc;
+        uint32_t v[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+            "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        // raw sign bits and "uncertain" bits, highest coordinate first through a
+        // funnel shift; -0 reads as negative but is always uncertain (bound > 0)
+        uint32_t neg = 0, pend = 0;
+#pragma unroll
+        for (int j = 31; j >= 0; --j) {
+          uint32_t lt;
+          asm("set.lt.u32.f32 %0, %1, %2;" : "=r"(lt) : "f"(fabsf(__uint_as_float(v[j]))), "f"(fmaf(ts.snorm[c0 + j], bA, bB)));
+          asm("shf.l.wrap.b32 %0, %1, %2, 1;" : "=r"(neg) : "r"(v[j]), "r"(neg));
+          asm("shf.l.wrap.b32 %0, %1, %2, 1;" : "=r"(pend) : "r"(lt), "r"(pend));
+        }
+        uint32_t word = ~neg;
+        if (zr) {
+          word = 0xffffffffu;
+          pend = 0u;
+        }
+        if (!ok) pend = 0u;
+        // fp32 recomputation of the uncertain entries from the limbs, one entry per
+        // pass of the warp (a few per thousand vectors); lane l covers coordinates 4l .. 4l + 3
+        while (true) {
+          const unsigned ball = __ballot_sync(0xffffffffu, pend != 0u);
+          if (ball == 0u) break;
+          const int src = __ffs(ball) - 1;
+          const int j = __shfl_sync(0xffffffffu, __ffs(pend) - 1, src);
+          const int frow = 32 * (warp & 3) + src, c = c0 + j, k0 = 4 * lane;
+          const uint2 ah = *reinterpret_cast<const uint2*>(Ahi + umma_off(frow, k0));
+          const uint2 al = *reinterpret_cast<const uint2*>(Alo + umma_off(frow, k0));
+          const uint2 bh = *reinterpret_cast<const uint2*>(Bhi + umma_off(c, k0));
+          const uint2 bl = *reinterpret_cast<const uint2*>(Blo + umma_off(c, k0));
+          float dsum = (f16lo(ah.x) + f16lo(al.x)) * (f16lo(bh.x) + f16lo(bl.x));
+          dsum = fmaf(f16hi(ah.x) + f16hi(al.x), f16hi(bh.x) + f16hi(bl.x), dsum);
+          dsum = fmaf(f16lo(ah.y) + f16lo(al.y), f16lo(bh.y) + f16lo(bl.y), dsum);
+          dsum = fmaf(f16hi(ah.y) + f16hi(al.y), f16hi(bh.y) + f16hi(bl.y), dsum);
+          dsum = warp_sum_f(dsum);
+          if (lane == src) {
+            word = (word & ~(1u << j)) | ((uint32_t)(dsum >= 0.f) << j);
+            pend &= ~(1u << j);
+          }
+        }
+        if (ok) {
+          const int wi = 2 * (warp >> 2) + cc;  // sign word index
+          if constexpr (MODE == kFlat) signs[(size_t)rec * 4 + wi] = word;
+          else reinterpret_cast<uint32_t*>(C.pool + (size_t)rec * P.sub_bytes + P.off_ksigns)[ts.slot[row] * 4 + wi] = word;
+        }
+      }
+      if (ok && (warp >> 2) == 0) {
+        const float gam = zr ? 0.f : sqrtf(s2 * (1.0f / D));  // exact scaling by a power of two
+        if constexpr (MODE == kFlat) rnorms[rec] = gam;
+        else reinterpret_cast<float*>(C.pool + (size_t)rec * P.sub_bytes + P.off_krnorm)[ts.slot[row]] = gam;
+      }
+    }
+    // the A tiles, the row table and the accumulator are rewritten by the next pass
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
   }
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128));
 }
 
 }  // namespace wq
