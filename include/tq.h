@@ -118,6 +118,15 @@ typedef struct {
   const float* qjl_s;  /* [device] [Hkv][d*d] QJL matrices; NULL if !key_qjl  */
   float k_centroids[16], k_bounds[16];
   float v_centroids[16], v_bounds[16];
+  /* Length of the key, value, query and output vectors the caller passes;
+   * 0 means d.  A head size that is not a power of two (a multiple of 8 with
+   * d/2 < head_dim < d, e.g. 80 or 96 with d = 128, 160 with d = 256) is
+   * zero-padded to d inside the kernels for the transforms and the codes, and
+   * outputs keep head_dim coordinates ([Design study] §Dense and structured
+   * transform comparison: temporary zero-padding during append and query
+   * transform).  Codes, signs and the float16 window rows keep d
+   * coordinates (the window's tail stays zero). */
+  int head_dim;
 } tq_layer_params;
 
 /*
@@ -126,7 +135,7 @@ typedef struct {
  * z = sqrt(d) y; residual r = y - c[idx]/sqrt(d) in the rotated basis;
  * gamma = ||r||; QJL signs of S r.  If n < 1e-7 the record is norm 0,
  * gamma 0, codes of z = 0, all signs +1 ([Reconstruction] §11 item 2, §13).
- *   k           [device] [n_vec][d] in dtype (vector n uses head n % Hkv);
+ *   k           [device] [n_vec][head_dim] in dtype (vector n uses head n % Hkv);
  *               16-byte aligned
  *   code_planes [device] out, uint32 [n_vec][key_bits][d/32]
  *   sign_planes [device] out, uint32 [n_vec][d/32]; NULL iff !key_qjl
@@ -142,7 +151,7 @@ tq_status tq_quantize_keys(const tq_layer_params* p, const void* k, tq_dtype dty
  * tq_quantize_values -- TurboQuant_mse of n_vec value vectors (flat output).
  * [Reconstruction] §5; [Design study] §Candidate key and value algorithms
  * (value path: MSE-oriented codec, no QJL residual).
- *   v           [device] [n_vec][d] in dtype (vector n uses head n % Hkv)
+ *   v           [device] [n_vec][head_dim] in dtype (vector n uses head n % Hkv)
  *   code_planes [device] out, uint32 [n_vec][value_bits][d/32]
  *   norms       [device] out, float [n_vec]
  */
@@ -185,7 +194,7 @@ size_t tq_subblock_bytes(const tq_layer_params* p);
  * tq_append_page -- quantize new tokens into the paged cache.
  * [Design study] §Append cost ("the append path runs once per new decode
  * token"), §Packed format ("Recent tokens" window), §Paging.
- *   k, v       [device] [n_tok][Hkv][d] in dtype
+ *   k, v       [device] [n_tok][Hkv][head_dim] in dtype
  *   slot_mapping == NULL (decode step): n_tok must equal cache->batch and
  *     token b is the next token of sequence b.  With window W > 0 it is
  *     written to the float16 ring; when the window then holds W + 16 tokens
@@ -219,9 +228,9 @@ size_t tq_decode_workspace_size(const tq_layer_params* p, int batch, int max_ctx
  *   window token i:      l_i = scale * <q, k_i>
  *   out = ( Pi_v^T sum_c p_i m_i C_v[vidx_i] / sqrt(d) + sum_w p_i v_i ),
  *   p = softmax(l) over all seq_len[b] tokens; lse = log sum exp(l).
- *   q        [device] [batch][Hq][d] in dtype
+ *   q        [device] [batch][Hq][head_dim] in dtype
  *   scale    softmax scale (usually 1/sqrt(d))
- *   out      [device] out, float [batch][Hq][d]
+ *   out      [device] out, float [batch][Hq][head_dim]
  *   lse      [device] out, nullable, float [batch][Hq]
  *   scores   [device] out, nullable, float [batch][Hq][max_ctx]: every l_i
  *            at its token position (for inspection; costs extra stores)

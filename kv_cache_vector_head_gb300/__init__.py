@@ -35,10 +35,15 @@ class TQLayer:
     """Codebooks, per-head transforms (device) and the tq_layer_params of one layer."""
 
     def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
-                 window: int = 0, key_qjl: bool = True, seed: int = 0, layer: int = 0, device="cuda"):
+                 window: int = 0, key_qjl: bool = True, seed: int = 0, layer: int = 0, device="cuda",
+                 head_dim: int | None = None):
+        """d: the transform and code dimension (128 or 256); head_dim (default d):
+        the length of the vectors the caller passes, zero-padded to d inside
+        the kernels (a multiple of 8 in (d/2, d])."""
         import torch
 
         self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
+        self.head_dim = d if head_dim is None else head_dim
         self.key_bits, self.value_bits, self.kind, self.window = key_bits, value_bits, kind, window
         self.key_qjl, self.seed, self.layer = bool(key_qjl), seed, layer
         self.k_cb = build_codebook(d, key_bits)
@@ -57,6 +62,7 @@ class TQLayer:
         p = LayerParams()
         p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = d, n_kv_heads, n_q_heads, PAGE_SIZE, window
         p.key_bits, p.key_qjl, p.value_bits, p.kind = key_bits, int(key_qjl), value_bits, kind
+        p.head_dim = self.head_dim
         p.k_rot, p.v_rot = self.k_rot.data_ptr(), self.v_rot.data_ptr()
         p.qjl_s = self.qjl_s.data_ptr() if key_qjl else None
         for name, (c, t, _) in (("k", self.k_cb), ("v", self.v_cb)):
@@ -122,8 +128,8 @@ class PagedCache:
         self.n_compressed.fill_(nc)
         if nc:
             slots = self.slot_mapping(nc)
-            kk = k[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.d).contiguous()
-            vv = v[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.d).contiguous()
+            kk = k[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.head_dim).contiguous()
+            vv = v[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.head_dim).contiguous()
             append_page(self.layer.params, self.cache, kk, vv, B * nc, slots, stream)
         for t in range(nc, T):
             append_page(self.layer.params, self.cache, k[:, t].contiguous(), v[:, t].contiguous(), B, None, stream)

@@ -43,6 +43,7 @@ class LayerParams(ctypes.Structure):
         ("k_rot", c_void_p), ("v_rot", c_void_p), ("qjl_s", c_void_p),
         ("k_centroids", c_float * 16), ("k_bounds", c_float * 16),
         ("v_centroids", c_float * 16), ("v_bounds", c_float * 16),
+        ("head_dim", c_int),
     ]
 
 

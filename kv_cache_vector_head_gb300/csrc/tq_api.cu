@@ -50,6 +50,8 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
     return fail(TQ_ERR_UNSUPPORTED, "key_bits and value_bits must be 1..4");
   if (p->key_qjl != 0 && p->key_qjl != 1) return fail(TQ_ERR_INVALID_ARG, "key_qjl must be 0 or 1");
   if (p->kind != TQ_DENSE && p->kind != TQ_FWHT) return fail(TQ_ERR_INVALID_ARG, "bad transform kind");
+  if (p->head_dim != 0 && (p->head_dim % 8 != 0 || p->head_dim <= p->d / 2 || p->head_dim > p->d))
+    return fail(TQ_ERR_INVALID_ARG, "head_dim must be 0 or a multiple of 8 in (d/2, d]");
   if (need_device_ptrs) {
     if (!p->k_rot || !p->v_rot) return fail(TQ_ERR_INVALID_ARG, "null k_rot / v_rot");
     if (p->key_qjl && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
@@ -57,6 +59,7 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
       return fail(TQ_ERR_INVALID_ARG, "transforms must be 16-byte aligned");
   }
   K->d = p->d;
+  K->dh = p->head_dim ? p->head_dim : p->d;
   K->hkv = p->n_kv_heads;
   K->hq = p->n_q_heads;
   K->G = p->n_q_heads / p->n_kv_heads;

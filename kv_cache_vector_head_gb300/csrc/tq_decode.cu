@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   const int nv = min(kPrologueTile, batch * G - n0);
   for (int v = 0; v < kPrologueTile; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
-    s.x[v][j] = v < nv ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * D + j)) : 0.f;
+    s.x[v][j] = (v < nv && j < P.dh) ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * P.dh + j))
+                                     : 0.f;  // zero-padded to D
   }
   if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
@@ -314,7 +315,10 @@ __device__ void window_split(const KParams& P, const KCache& C, const void* q, i
     if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
     nw = C.ring == 0 ? 0 : min(nw, C.ring);
   }
-  for (int i = tid; i < G * D; i += NT) qs[i] = load_elem(q, dtype, (long long)(head0 * D + i));
+  for (int i = tid; i < G * D; i += NT) {
+    const int h = i / D, j = i % D;
+    qs[i] = j < P.dh ? load_elem(q, dtype, (long long)((head0 + h) * P.dh + j)) : 0.f;  // zero-padded to D
+  }
   if (tid < TQ_MAX_GQA) {
     st_m[tid] = -INFINITY;
     st_l[tid] = 0.f;
@@ -894,7 +898,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
   const float fw = fsplit[st - 1];
   for (int j = tid; j < D; j += kCombThreads) {
     const float win = fw * acc[(size_t)(st - 1) * D + j];
-    out[head * D + j] = empty ? 0.f : (y[j] + win) / Lsum;
+    if (j < P.dh) out[head * P.dh + j] = empty ? 0.f : (y[j] + win) / Lsum;
   }
   if (lse && tid == 0) lse[head] = empty ? -INFINITY : M + logf(Lsum);
 }

@@ -17,6 +17,7 @@ constexpr float kZeroNorm = 1e-7f;
 // Kernel-side copy of tq_layer_params plus the derived page layout.
 struct KParams {
   int d, hkv, hq, G, window, kb, kqjl, vb, kind;
+  int dh;                              // length of the caller's vectors (<= d; zero-padded to d)
   const float* k_rot;
   const float* v_rot;
   const float* qjl_s;

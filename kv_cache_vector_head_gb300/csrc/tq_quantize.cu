@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(D) quantize_flat_kernel(const __grid_constant_
     }
     for (int v = 0; v < nv; ++v) {
       const long long n = (t0 + v) * P.hkv + head;
-      s.x[v][threadIdx.x] = load_elem(x, dtype, n * D + threadIdx.x);
+      s.x[v][threadIdx.x] = threadIdx.x < P.dh ? load_elem(x, dtype, n * P.dh + threadIdx.x) : 0.f;  // zero-padded to D
     }
     __syncthreads();
     quantize_tile<D>(P, s, nv, head, is_key != 0, nullptr);
@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
     }
     for (int i = 0; i < nv; ++i) {
       const long long n = (t0 + i) * P.hkv + head;
-      s.x[i][threadIdx.x] = page_of[i] >= 0 ? load_elem(x, dtype, n * D + threadIdx.x) : 0.f;
+      s.x[i][threadIdx.x] =
+          (page_of[i] >= 0 && threadIdx.x < P.dh) ? load_elem(x, dtype, n * P.dh + threadIdx.x) : 0.f;
     }
     __syncthreads();
     quantize_tile<D>(P, s, nv, head, is_key, slot_of);
@@ -337,14 +338,15 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
   const void* x = is_key ? k : v;
   const int T = C.seq_len[b];
   const int nc = C.n_compressed[b];
-  const long long src = ((long long)b * P.hkv + head) * D;
+  const long long src = ((long long)b * P.hkv + head) * P.dh;
+  const bool in_head = threadIdx.x < P.dh;  // coordinates >= dh are the zero padding
   if (P.window > 0) {
     __half* ring = (is_key ? C.win_k : C.win_v) + (((size_t)b * P.hkv + head) * C.ring) * D;
     if (T - nc < 0 || T - nc >= P.window + kPage) {
       if (threadIdx.x == 0) atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
       return;
     }
-    ring[(size_t)(T % C.ring) * D + threadIdx.x] = __float2half_rn(load_elem(x, dtype, src + threadIdx.x));
+    ring[(size_t)(T % C.ring) * D + threadIdx.x] = __float2half_rn(in_head ? load_elem(x, dtype, src + threadIdx.x) : 0.f);
     if (T + 1 - nc != P.window + kPage) return;
     // flush the oldest 16 window tokens into page nc / 16
     const int pidx = nc / kPage;
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
         atomicOr(&g_quant_err, (T >= 0 && pidx < C.max_pages) ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
       return;
     }
-    s.x[0][threadIdx.x] = load_elem(x, dtype, src + threadIdx.x);
+    s.x[0][threadIdx.x] = in_head ? load_elem(x, dtype, src + threadIdx.x) : 0.f;
     if (threadIdx.x == 0) slot_of[0] = slot;
     __syncthreads();
     quantize_tile<D>(P, s, 1, head, is_key, slot_of);

@@ -278,11 +278,13 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
     for (int R = 0; R < 2; ++R) {
       long long n;
       const bool ok = row_index(mt, R, n);
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * D) + t;
+      // row of dh elements, zero-padded to D: 16-byte chunk 4m + t holds coordinates 32m + 8t .. + 7
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * P.dh) + t;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        if constexpr (DENSE) nxt[R][m] = ok ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
-        else cp_async16(stg + 32 * (4 * R + m), src + 4 * m, ok ? 16 : 0);
+        const bool in = ok && 32 * m + 8 * t < P.dh;
+        if constexpr (DENSE) nxt[R][m] = in ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
+        else cp_async16(stg + 32 * (4 * R + m), in ? src + 4 * m : src, in ? 16 : 0);
       }
     }
     if constexpr (!DENSE) cp_async_commit();
@@ -707,9 +709,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     for (int R = 0; R < 2; ++R) {
       long long n;
       const bool ok = row_index(mt, R, n);
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * D) + t;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(ok ? n : 0) * P.dh) + t;  // zero-padded to D
 #pragma unroll
-      for (int m = 0; m < 4; ++m) nxt[R][m] = ok ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
+      for (int m = 0; m < 4; ++m) nxt[R][m] = (ok && 32 * m + 8 * t < P.dh) ? __ldg(src + 4 * m) : make_uint4(0, 0, 0, 0);
     }
   };
   uint32_t phase = 0;

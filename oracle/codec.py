@@ -43,6 +43,20 @@ from .codebook import Codebook
 ZERO_NORM = 1e-7
 
 
+def pad_head(x: np.ndarray, d: int) -> np.ndarray:
+    """Zero-pad the last axis (a head of head_dim <= d coordinates) to the
+    transform size d: [Design study] §Dense and structured transform
+    comparison treats non-power-of-two head sizes by temporary zero-padding
+    during append and query transform.  Inner products are unchanged."""
+    x = np.asarray(x, dtype=np.float64)
+    if x.shape[-1] == d:
+        return x
+    if x.shape[-1] > d:
+        raise ValueError("head longer than the transform size")
+    pad = [(0, 0)] * (x.ndim - 1) + [(0, d - x.shape[-1])]
+    return np.pad(x, pad)
+
+
 def qjl_constant(d: int) -> float:
     """sqrt(pi/2) / d: the QJL estimator constant for m = d sketch rows."""
     return math.sqrt(math.pi / 2.0) / d

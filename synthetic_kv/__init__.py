@@ -64,6 +64,11 @@ class Workload:
     value_scale: str = "none"
     rope: bool = True
     seed: int = 0
+    head_dim: int = 0      # length of the generated vectors (0: d); heads shorter than d are zero-padded to d
+
+    @property
+    def dh(self) -> int:
+        return self.head_dim or self.d
 
 
 WORKLOADS = {
@@ -163,7 +168,7 @@ def keys_values(w: Workload, layer: int = 0, seqs=None, ctx: int | None = None) 
     """
     T = w.ctx if ctx is None else ctx
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
-    H, Hq, d = w.n_kv_heads, w.n_q_heads, w.d
+    H, Hq, d = w.n_kv_heads, w.n_q_heads, w.dh
     Ks, Vs, Qs = [], [], []
     for b in seqs:
         K = normals(stream_start(w.seed, TENSOR_K, layer, b), T * H * d).reshape(T, H, d)
@@ -210,7 +215,7 @@ def keys_values_torch(w: Workload, layer: int = 0, ctx: int | None = None, devic
     T = w.ctx if ctx is None else ctx
     g = torch.Generator(device=device)
     g.manual_seed(stream_start(w.seed if seed is None else seed, 0xB0, layer) & ((1 << 63) - 1))
-    B, H, Hq, d = w.batch, w.n_kv_heads, w.n_q_heads, w.d
+    B, H, Hq, d = w.batch, w.n_kv_heads, w.n_q_heads, w.dh
     dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
     K = torch.randn(B, T, H, d, generator=g, device=device, dtype=torch.float32)
     V = torch.randn(B, T, H, d, generator=g, device=device, dtype=torch.float32)

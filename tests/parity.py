@@ -40,12 +40,13 @@ class OracleLayer:
         self.S = [OT.build_transform(kind, d, seed, layer, h, 2) for h in range(hkv)] if qjl else None
 
     def keys(self, x, head):
+        x = OC.pad_head(x, self.d)  # heads shorter than d: zero-padded to the transform size
         if self.qjl:
             return OC.quantize_prod(x, self.kind, self.k_rot[head], self.kcb, self.S[head])
         return OC.quantize_mse(x, self.kind, self.k_rot[head], self.kcb)
 
     def values(self, x, head):
-        return OC.quantize_mse(x, self.kind, self.v_rot[head], self.vcb)
+        return OC.quantize_mse(OC.pad_head(x, self.d), self.kind, self.v_rot[head], self.vcb)
 
     def attention_params(self):
         return {"kind": self.kind, "k_rot": self.k_rot, "v_rot": self.v_rot, "qjl_s": self.S,
@@ -132,7 +133,14 @@ def unpack_flat_bits(words, d):
 
 
 def decode_reference(ol: OracleLayer, q, comp, win_k, win_v, scale):
-    return OA.decode_one(q, comp, win_k, win_v, ol.attention_params(), scale)
+    """Decode of one sequence; q (and window tokens) of head_dim <= d
+    coordinates are zero-padded to d, the output keeps head_dim."""
+    dh = q.shape[-1]
+    pw = (lambda w: None if w is None else OC.pad_head(w, ol.d).astype(w.dtype))
+    r = OA.decode_one(OC.pad_head(q, ol.d), comp, pw(win_k), pw(win_v), ol.attention_params(), scale)
+    if dh != ol.d:
+        r = dict(r, out=r["out"][..., :dh])
+    return r
 
 
 def stack_comp(recs_k, recs_v):

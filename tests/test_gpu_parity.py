@@ -33,7 +33,7 @@ def tq():
 
 def _layer(tq, w, layer=0):
     L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
-                   key_qjl=w.key_qjl, seed=w.seed, layer=layer)
+                   key_qjl=w.key_qjl, seed=w.seed, layer=layer, head_dim=w.dh)
     O = PY.OracleLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
                        qjl=w.key_qjl, seed=w.seed, layer=layer)
     return L, O
@@ -55,6 +55,11 @@ CASES = [
     ("bulk", dict(ctx=5000, kind=SK.FWHT, key_bits=4, value_bits=3)),
     ("bulk", dict(ctx=20, kind=SK.FWHT, key_bits=1, key_qjl=False, value_bits=4)),
     ("bulk", dict(ctx=21, key_bits=2, key_qjl=False, value_bits=1)),
+    # head sizes that are not powers of two, zero-padded to the transform size
+    ("bulk", dict(ctx=300, kind=SK.FWHT, head_dim=80)),
+    ("bulk", dict(ctx=200, head_dim=96, key_bits=2, value_bits=3)),
+    ("tiny", dict(ctx=60, head_dim=120)),
+    ("long", dict(ctx=33, head_dim=160)),
 ]
 
 
@@ -64,8 +69,8 @@ def test_quantize_flat_parity(tq, name, over):
     kv = SK.keys_values(w)
     L, O = _layer(tq, w)
     dt = w.dtype
-    K = kv["K"].reshape(-1, w.d)
-    V = kv["V"].reshape(-1, w.d)
+    K = kv["K"].reshape(-1, w.dh)
+    V = kv["V"].reshape(-1, w.dh)
     n_vec = K.shape[0] - 1  # ragged: the last token is missing its last head
     kt = SK.to_torch(K, dt).cuda()
     vt = SK.to_torch(V, dt).cuda()
@@ -213,6 +218,9 @@ PAGED = [
     # no window, d = 128 bf16: decode-step appends through the tensor-core warp tiles
     ("llama", dict(batch=37, kind=SK.FWHT), 29, 21),
     ("bulk", dict(batch=20, key_qjl=False, key_bits=2, value_bits=2), 15, 20),
+    # head sizes that are not powers of two
+    ("llama", dict(batch=5, head_dim=96), 29, 21),
+    ("qwen", dict(batch=2, window=20, head_dim=160), 45, 30),
 ]
 
 
@@ -231,9 +239,9 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
     stats = {}
     q = kv["q"]
     qt = SK.to_torch(q, w.dtype).cuda()
-    scale = 1.0 / math.sqrt(w.d)
+    scale = 1.0 / math.sqrt(w.dh)
     ws = torch.empty(tq.decode_workspace_size(L.params, w.batch, T), dtype=torch.uint8, device="cuda")
-    out = torch.zeros(w.batch, w.n_q_heads, w.d, device="cuda")
+    out = torch.zeros(w.batch, w.n_q_heads, w.dh, device="cuda")
     lse = torch.zeros(w.batch, w.n_q_heads, device="cuda")
     scores = torch.full((w.batch, w.n_q_heads, T), float("nan"), device="cuda")
     tq.decode_attention(L.params, pc.cache, qt, scale, out, lse, scores, ws, T)
@@ -255,8 +263,9 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
             if w.window > 0 and T - nc > 0:
                 ring = pc.win_k[b, h].cpu().numpy()
                 slots = [p % pc.ring for p in range(nc, T)]
-                assert np.array_equal(ring[slots], win_k[h])
-                assert np.array_equal(pc.win_v[b, h].cpu().numpy()[slots], win_v[h])
+                assert np.array_equal(ring[slots][:, :w.dh], win_k[h])
+                assert np.array_equal(pc.win_v[b, h].cpu().numpy()[slots][:, :w.dh], win_v[h])
+                assert not ring[slots][:, w.dh:].any()  # the padding of the window rows stays zero
         if stats:
             assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
         comp = PY.stack_comp(recs_k, recs_v) if nc else None

@@ -87,6 +87,11 @@ def test_argument_checks_return_status_without_gpu(L):
     p.key_bits = 3
     p.value_bits = 4
     assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * 140
+    # head sizes below d are zero-padded to d: a multiple of 8 in (d/2, d]
+    for hd, ok in ((96, True), (80, True), (128, True), (0, True), (64, False), (70, False), (136, False)):
+        p.head_dim = hd
+        assert (lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * 140) == ok, hd
+    p.head_dim = 0
     assert lib.tq_build_codebook(2, 2, None, None, None) == L.TQ_ERR_INVALID_ARG
     assert lib.tq_build_transform(L.TQ_FWHT, 96, 0, 0, 0, 0, None) == L.TQ_ERR_INVALID_ARG
     out = np.zeros(96, np.float32)

@@ -79,6 +79,32 @@ def test_window_only_is_exact_attention():
     np.testing.assert_allclose(ex["out"], ref["out"], rtol=0, atol=1e-12)
 
 
+def test_zero_padded_head_is_the_unpadded_attention():
+    """A head shorter than the transform size, zero-padded (keys, values and
+    query): scores, lse and the first head_dim output coordinates are those of
+    textbook attention on the unpadded vectors; the padded outputs are zero;
+    and padding keeps norms and inner products."""
+    from oracle import codec as C
+
+    rng = np.random.default_rng(3)
+    Hkv, Hq, Tw, dh, d = 2, 6, 30, 40, 64
+    K = rng.standard_normal((Hkv, Tw, dh)).astype(np.float16)
+    V = rng.standard_normal((Hkv, Tw, dh)).astype(np.float16)
+    q = rng.standard_normal((Hq, dh))
+    Kp, Vp, qp = (C.pad_head(x, d) for x in (K, V, q))
+    assert Kp.shape == (Hkv, Tw, d) and not Kp[..., dh:].any()
+    np.testing.assert_array_equal(np.linalg.norm(Kp, axis=-1), np.linalg.norm(K.astype(np.float64), axis=-1))
+    p = _params(d, Hkv, T.FWHT, 2, 2)
+    got = A.decode_one(qp, None, Kp.astype(np.float16), Vp.astype(np.float16), p, 1 / math.sqrt(dh))
+    ref = _textbook(q, K.astype(np.float64), V.astype(np.float64), 1 / math.sqrt(dh))
+    for k in ("lse", "scores"):
+        np.testing.assert_allclose(got[k], ref[k], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got["out"][:, :dh], ref["out"], rtol=0, atol=1e-12)
+    assert not got["out"][:, dh:].any()
+    with pytest.raises(ValueError):
+        C.pad_head(np.zeros((2, 70)), 64)
+
+
 @pytest.mark.parametrize("kind", [T.DENSE, T.FWHT])
 @pytest.mark.parametrize("bits", [(2, 2), (3, 4)])
 def test_rotated_domain_equals_explicit_dequantization(kind, bits):
