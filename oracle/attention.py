@@ -45,7 +45,8 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
              ksigns [Hkv, Tc, d] (bool), vnorm [Hkv, Tc], vidx [Hkv, Tc, d].
     win_k, win_v : [Hkv, Tw, d] float16 window tokens (oldest first), or None.
     params : kind, k_rot[Hkv], v_rot[Hkv], qjl_s[Hkv] (stored float32 arrays),
-             k_cb, v_cb (Codebook), key_qjl (bool).
+             k_cb, v_cb (Codebook), key_qjl: key correction (0 none, 1 QJL,
+             2 EDEN scale, 3 length renormalization; krnorm holds gamma or s).
     Returns out [Hq, d], lse [Hq], scores [Hq, T] (compressed first, then window).
     """
     Hq, d = q.shape
@@ -67,10 +68,13 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
         if Tc:
             q1 = T.rotate(kind, params["k_rot"][g], qh[None, :])[0]
             l_c = Ck[comp["kidx"][g]] @ q1 / math.sqrt(d)
-            if params["key_qjl"]:
+            corr = int(params["key_qjl"])
+            if corr == 1:  # QJL residual term
                 q2 = np.asarray(params["qjl_s"][g], np.float32).astype(np.float64) @ q1
                 pm = np.where(comp["ksigns"][g], 1.0, -1.0)
                 l_c = l_c + kap * comp["krnorm"][g].astype(np.float64) * (pm @ q2)
+            elif corr >= 2:  # EDEN or renormalized keys: the per-key scale
+                l_c = l_c * comp["krnorm"][g].astype(np.float64)
             l_c = scale * comp["knorm"][g].astype(np.float64) * l_c
             parts.append(l_c)
         if Tw:

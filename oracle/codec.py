@@ -106,6 +106,40 @@ def quantize_prod(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, S: np
 
 # ----------------------------------------------------------------------------- packing
 
+# Key corrections.  QJL is TurboQuant_prod's residual sketch; the two others
+# spend no bit on a residual and keep one float32 scale s per key instead
+# (the "next" correction variants): EDEN's unbiased scale s = ||y||^2 /
+# <y, y_hat> ([Reconstruction] §10, §12.2: TurboQuant_mse is EDEN/DRIVE with
+# a fixed scale; the unbiased EDEN scalar has 2.75x lower 1-bit variance than
+# QJL) and TurboVec's length renormalization s = ||y|| / ||y_hat||
+# ([Reconstruction] §12: length-renormalized scoring in place of QJL).
+KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM = 0, 1, 2, 3
+
+
+def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mode: int) -> dict:
+    """TurboQuant_mse code of the rows of x plus the scale s of the key
+    correction `mode` (KEY_EDEN or KEY_RENORM), stored as float32 in the
+    record's "rnorm" slot; the key is reconstructed as n s Pi^T y_hat.  For a
+    zero vector s = 0."""
+    rec = quantize_mse(x, kind, rot, cb)
+    y, yhat, zero = rec["y"], rec["yhat"], rec["zero"]
+    if mode == KEY_EDEN:
+        den = np.sum(y * yhat, axis=-1)          # y is a unit vector: ||y||^2 = 1
+        s = 1.0 / np.where(zero, 1.0, den)
+    elif mode == KEY_RENORM:
+        s = 1.0 / np.where(zero, 1.0, np.linalg.norm(yhat, axis=-1))
+    else:
+        raise ValueError("mode must be KEY_EDEN or KEY_RENORM")
+    s = np.where(zero, 0.0, s)
+    rec.update({"rnorm": s.astype(np.float32), "rnorm_f64": s, "scale": s})
+    return rec
+
+
+def dequantize_scaled(norm, scale, idx, kind, rot, cb) -> np.ndarray:
+    """k_hat = n s Pi^T y_hat for the EDEN / renormalized keys."""
+    return np.asarray(scale, dtype=np.float64)[:, None] * dequantize_mse(norm, idx, kind, rot, cb)
+
+
 def code_planes(idx: np.ndarray, bits: int) -> np.ndarray:
     """Sign-magnitude planes as 0/1 arrays: [..., bits, d]."""
     half = 1 << (bits - 1)

@@ -40,7 +40,8 @@ def n_compressed(T: int, W: int, P: int = PAGE) -> int:
     return P * (max(0, T - W) // P)
 
 
-def subblock_layout(d: int, key_bits: int, key_qjl: bool, value_bits: int, P: int = PAGE) -> dict:
+def subblock_layout(d: int, key_bits: int, key_qjl: int, value_bits: int, P: int = PAGE) -> dict:
+    """key_qjl: key correction (0 none, 1 QJL: scale slot + sign plane, 2 / 3 EDEN / renormalized: scale slot)."""
     if P != PAGE:
         raise ValueError("page size is fixed at 16 tokens")
     w = d // 32
@@ -49,7 +50,7 @@ def subblock_layout(d: int, key_bits: int, key_qjl: bool, value_bits: int, P: in
     off["key_norm"] = o; o += 4 * P
     off["key_rnorm"] = o; o += 4 * P if key_qjl else 0
     off["key_codes"] = o; o += 4 * key_bits * P * w
-    off["key_signs"] = o; o += 4 * P * w if key_qjl else 0
+    off["key_signs"] = o; o += 4 * P * w if key_qjl == 1 else 0
     off["value_norm"] = o; o += 4 * P
     off["value_codes"] = o; o += 2 * value_bits * d
     off["bytes"] = o
@@ -59,7 +60,7 @@ def subblock_layout(d: int, key_bits: int, key_qjl: bool, value_bits: int, P: in
 def record_bytes(d: int, key_bits: int, key_qjl: bool, value_bits: int) -> int:
     """Bytes per (token, kv head): the D1 + D2 storage formulas of
     [Reconstruction] §8 with float32 norms."""
-    kb = 4 + (4 if key_qjl else 0) + key_bits * d // 8 + (d // 8 if key_qjl else 0)
+    kb = 4 + (4 if key_qjl else 0) + key_bits * d // 8 + (d // 8 if key_qjl == 1 else 0)
     vb = 4 + value_bits * d // 8
     return kb + vb
 
@@ -81,7 +82,7 @@ def write_page(pool: np.ndarray, lay: dict, n_heads: int, page: int, head: int, 
     for p in range(key_bits):
         o = lay["key_codes"] + 4 * ((p * PAGE + slot) * w)
         sb[o: o + 4 * w] = np.asarray(kcode_words[p], np.uint32).view(np.uint8)
-    if key_qjl:
+    if key_qjl == 1:
         o = lay["key_signs"] + 4 * slot * w
         sb[o: o + 4 * w] = np.asarray(ksign_words, np.uint32).view(np.uint8)
     sb[lay["value_norm"] + 4 * slot: lay["value_norm"] + 4 * slot + 4] = np.array([vnorm], np.float32).view(np.uint8)
@@ -103,6 +104,7 @@ def read_page(pool: np.ndarray, lay: dict, n_heads: int, page: int, head: int,
     out = {"knorm": sb[lay["key_norm"]: lay["key_norm"] + 4 * PAGE].view(np.float32).copy()}
     if key_qjl:
         out["krnorm"] = sb[lay["key_rnorm"]: lay["key_rnorm"] + 4 * PAGE].view(np.float32).copy()
+    if key_qjl == 1:
         sw = sb[lay["key_signs"]: lay["key_signs"] + 4 * PAGE * w].view(np.uint32).reshape(PAGE, w)
         out["ksigns"] = unpack_bits(sw, d).astype(bool)
     cw = sb[lay["key_codes"]: lay["key_codes"] + 4 * key_bits * PAGE * w].view(np.uint32).reshape(key_bits, PAGE, w)

@@ -31,18 +31,21 @@ EXEMPT_FRACTION = 1e-4
 
 class OracleLayer:
     def __init__(self, d, hkv, hq, kb, vb, kind, window=0, qjl=True, seed=0, layer=0):
+        """qjl: key correction (False/0 none, True/1 QJL, 2 EDEN scale, 3 length renormalization)."""
         self.d, self.hkv, self.hq, self.kb, self.vb, self.kind = d, hkv, hq, kb, vb, kind
-        self.window, self.qjl = window, qjl
+        self.window, self.qjl = window, int(qjl)
         self.kcb = OCB.lloyd_max(d, kb)
         self.vcb = OCB.lloyd_max(d, vb)
         self.k_rot = [OT.build_transform(kind, d, seed, layer, h, 0) for h in range(hkv)]
         self.v_rot = [OT.build_transform(kind, d, seed, layer, h, 1) for h in range(hkv)]
-        self.S = [OT.build_transform(kind, d, seed, layer, h, 2) for h in range(hkv)] if qjl else None
+        self.S = [OT.build_transform(kind, d, seed, layer, h, 2) for h in range(hkv)] if self.qjl == 1 else None
 
     def keys(self, x, head):
         x = OC.pad_head(x, self.d)  # heads shorter than d: zero-padded to the transform size
-        if self.qjl:
+        if self.qjl == 1:
             return OC.quantize_prod(x, self.kind, self.k_rot[head], self.kcb, self.S[head])
+        if self.qjl >= 2:
+            return OC.quantize_scaled(x, self.kind, self.k_rot[head], self.kcb, self.qjl)
         return OC.quantize_mse(x, self.kind, self.k_rot[head], self.kcb)
 
     def values(self, x, head):
@@ -83,6 +86,10 @@ def compare_records(ora, g_idx, g_norm, g_signs=None, g_rnorm=None, is_key=True,
     n_ref = ora["norm"].astype(np.float64)
     np.testing.assert_allclose(g_norm.astype(np.float64), n_ref, rtol=NORM_RTOL, atol=1e-30)
     n_exempt_codes = int(code_ex.sum())
+    if is_key and g_signs is None and g_rnorm is not None:  # EDEN / renormalized keys: the scale
+        ok = ~vec_flip
+        np.testing.assert_allclose(g_rnorm[ok].astype(np.float64), ora["rnorm"][ok].astype(np.float64),
+                                   rtol=NORM_RTOL, atol=1e-30)
     if is_key and g_signs is not None:
         sign_ex = (ora["sign_margin"] < BOUNDARY) | vec_flip[:, None]
         sbad = (g_signs != ora["signs"]) & ~sign_ex
@@ -112,6 +119,11 @@ def adopt_exempt(rec, g_idx, g_signs=None, g_rnorm=None):
     idx = rec["idx"].copy()
     idx[ex] = g_idx[ex]
     out["idx"] = idx
+    if g_signs is None and g_rnorm is not None and "rnorm" in rec:  # scale of EDEN / renormalized keys
+        flip = (idx != rec["idx"]).any(axis=1)
+        rn = rec["rnorm"].copy()
+        rn[flip] = g_rnorm[flip]
+        out["rnorm"] = rn
     if g_signs is not None and "signs" in rec:
         flip = (idx != rec["idx"]).any(axis=1)
         sex = (rec["sign_margin"] < BOUNDARY) | flip[:, None]
@@ -149,7 +161,8 @@ def stack_comp(recs_k, recs_v):
             "vnorm": np.stack([r["norm"] for r in recs_v]), "vidx": np.stack([r["idx"] for r in recs_v])}
     if "rnorm" in recs_k[0]:
         comp["krnorm"] = np.stack([r["rnorm"] for r in recs_k])
-        comp["ksigns"] = np.stack([r["signs"] for r in recs_k])
+        comp["ksigns"] = (np.stack([r["signs"] for r in recs_k]) if "signs" in recs_k[0]
+                          else np.ones(comp["kidx"].shape, dtype=bool))
     else:
         comp["krnorm"] = np.zeros_like(comp["knorm"])
         comp["ksigns"] = np.ones(comp["kidx"].shape, dtype=bool)

@@ -176,3 +176,61 @@ def test_value_cosine_two_bits_d256():
     xh = C.dequantize_mse(rec["norm"], rec["idx"], T.FWHT, rot, cb4)
     cos4 = np.sum(x * xh, 1) / np.linalg.norm(x, axis=1) / np.linalg.norm(xh, axis=1)
     assert 0.994 < cos4.mean() < 0.998  # [README] reports 0.997 for its own 4-bit value codec
+
+
+# ----------------------------------------------------------------------------- EDEN / renormalized keys
+
+def _pair(rng, n, d, rho):
+    """n pairs (y, q') of unit vectors with <y, q'> = rho and (y, q') uniform
+    over such pairs: the joint law of (Pi x, Pi q) under a Haar rotation."""
+    y = rng.standard_normal((n, d))
+    y /= np.linalg.norm(y, axis=1, keepdims=True)
+    w = rng.standard_normal((n, d))
+    w -= np.sum(w * y, axis=1, keepdims=True) * y
+    w /= np.linalg.norm(w, axis=1, keepdims=True)
+    return y, rho * y + math.sqrt(1 - rho * rho) * w
+
+
+def test_renormalized_keys_keep_their_length():
+    d = 128
+    cb = CB.lloyd_max(d, 2)
+    rot = T.build_transform(T.FWHT, d, 0, 0, 0, 0)
+    x = np.random.default_rng(4).standard_normal((64, d)) * 3.0
+    rec = C.quantize_scaled(x, T.FWHT, rot, cb, C.KEY_RENORM)
+    kh = C.dequantize_scaled(rec["norm"], rec["scale"], rec["idx"], T.FWHT, rot, cb)
+    np.testing.assert_allclose(np.linalg.norm(kh, axis=1), np.linalg.norm(x, axis=1), rtol=1e-6)
+    z = C.quantize_scaled(np.zeros((1, d)), T.FWHT, rot, cb, C.KEY_RENORM)
+    assert z["scale"][0] == 0 and z["norm"][0] == 0
+
+
+def test_eden_scale_is_unbiased_and_plain_code_is_not():
+    """E <q', s y_hat> = <q', y> over random rotations (rotation = identity on
+    a uniformly rotated pair); the same code with s = 1 underestimates."""
+    d, n, rho = 64, 20000, 0.6
+    rng = np.random.default_rng(5)
+    y, q = _pair(rng, n, d, rho)
+    cb = CB.lloyd_max(d, 2)
+    eye = np.eye(d)
+    rec = C.quantize_scaled(y, T.DENSE, eye, cb, C.KEY_EDEN)
+    est = np.sum(q * rec["scale"][:, None] * rec["yhat"], axis=1)
+    se = est.std() / math.sqrt(n)
+    assert abs(est.mean() - rho) < 4 * se
+    plain = np.sum(q * rec["yhat"], axis=1)
+    assert rho - plain.mean() > 10 * plain.std() / math.sqrt(n)
+
+
+def test_one_bit_eden_has_275x_lower_variance_than_qjl():
+    """1-bit estimators of <q, x> for orthogonal unit q, x: EDEN (1-bit code,
+    unbiased scale) has variance (pi/2 - 1)/d, the QJL sign sketch of the whole
+    vector pi/2/d, a ratio of 2.75 ([Reconstruction] §12.2)."""
+    d, n = 128, 3000
+    rng = np.random.default_rng(6)
+    y, q = _pair(rng, n, d, 0.0)
+    cb = CB.lloyd_max(d, 1)
+    rec = C.quantize_scaled(y, T.DENSE, np.eye(d), cb, C.KEY_EDEN)
+    eden = np.sum(q * rec["scale"][:, None] * rec["yhat"], axis=1)
+    S = rng.standard_normal((n, d, d))
+    qjl = C.qjl_estimate(q, 1.0, C.sketch(y, S) >= 0, S)
+    assert abs(eden.var() * d / (math.pi / 2 - 1) - 1) < 0.08
+    assert abs(qjl.var() * d / (math.pi / 2) - 1) < 0.08
+    assert 2.45 < qjl.var() / eden.var() < 3.05
