@@ -100,6 +100,14 @@ tq_status tq_build_transform(tq_transform_kind kind, int d, uint64_t seed, int l
                              int role, float* out);
 
 /*
+ * Key corrections on top of the Lloyd-Max code ([Reconstruction] §6 QJL;
+ * §10 / §12.2 EDEN's unbiased scale, 2.75x lower 1-bit variance than QJL;
+ * §12 TurboVec's length-renormalized scoring).  EDEN and RENORM keep the
+ * scale in the record slot QJL uses for gamma and spend no bit on a sketch.
+ */
+typedef enum { TQ_KEY_MSE = 0, TQ_KEY_QJL = 1, TQ_KEY_EDEN = 2, TQ_KEY_RENORM = 3 } tq_key_correction;
+
+/*
  * Per-layer parameters.  Transforms are per KV head.  The codebooks are held
  * by value (from tq_build_codebook); entries beyond 2^bits are ignored.
  */
@@ -110,7 +118,10 @@ typedef struct {
   int page_size;   /* must be 16 */
   int window;      /* W >= 0 recent tokens kept float16 */
   int key_bits;    /* MSE bits of the key code, 1..4 */
-  int key_qjl;     /* 1: TurboQuant_prod keys (QJL sign sketch); 0: MSE only */
+  int key_qjl;     /* key correction, a tq_key_correction: TQ_KEY_QJL = TurboQuant_prod (QJL sign
+                      sketch of the residual, gamma = ||r||); TQ_KEY_MSE = code only; TQ_KEY_EDEN /
+                      TQ_KEY_RENORM = code plus one float scale s per key (EDEN's unbiased
+                      ||y||^2 / <y, y_hat>, or TurboVec's ||y|| / ||y_hat||), score n s <q', y_hat> */
   int value_bits;  /* 1..4 */
   tq_transform_kind kind;
   const float* k_rot;  /* [device] [Hkv][d*d] (dense) or [Hkv][d] signs (FWHT) */
@@ -138,9 +149,9 @@ typedef struct {
  *   k           [device] [n_vec][head_dim] in dtype (vector n uses head n % Hkv);
  *               16-byte aligned
  *   code_planes [device] out, uint32 [n_vec][key_bits][d/32]
- *   sign_planes [device] out, uint32 [n_vec][d/32]; NULL iff !key_qjl
+ *   sign_planes [device] out, uint32 [n_vec][d/32]; NULL unless key_qjl == TQ_KEY_QJL
  *   norms       [device] out, float [n_vec]
- *   rnorms      [device] out, float [n_vec]; NULL iff !key_qjl
+ *   rnorms      [device] out, float [n_vec]: gamma (QJL) or the scale s (EDEN, RENORM); NULL iff MSE only
  * n_vec may be 0 (no launch).
  */
 tq_status tq_quantize_keys(const tq_layer_params* p, const void* k, tq_dtype dtype, int64_t n_vec,
@@ -163,9 +174,9 @@ tq_status tq_quantize_values(const tq_layer_params* p, const void* v, tq_dtype d
  * lifecycle).  Page pool: [n_pages][Hkv][sub-block]; the sub-block of one
  * (page, kv head) holds 16 tokens, in this order:
  *   key norms          float [16]
- *   key residual norms float [16]              (key_qjl only)
+ *   key residual norms float [16]              (key_qjl != 0: gamma or the scale s)
  *   key code planes    uint32 [key_bits][16][d/32]   token-major
- *   key sign plane     uint32 [16][d/32]       (key_qjl only)
+ *   key sign plane     uint32 [16][d/32]       (key_qjl == TQ_KEY_QJL only)
  *   value norms        float [16]
  *   value code planes  uint16 [value_bits][d]  coordinate-major: bit t of
  *                      entry (plane, j) is that plane's bit of token t at j

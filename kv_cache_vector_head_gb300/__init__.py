@@ -14,7 +14,7 @@ import math
 import numpy as np
 
 from . import _lib
-from ._lib import (PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
+from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
                    Cache, LayerParams, TQError, append_page, build_codebook, build_transform, check_device_error,
                    decode_attention, decode_workspace_size, quantize_keys, quantize_values, subblock_bytes)
 
@@ -22,7 +22,7 @@ __all__ = [
     "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
     "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
     "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
-    "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL",
+    "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
 ]
 
 
@@ -35,17 +35,22 @@ class TQLayer:
     """Codebooks, per-head transforms (device) and the tq_layer_params of one layer."""
 
     def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
-                 window: int = 0, key_qjl: bool = True, seed: int = 0, layer: int = 0, device="cuda",
+                 window: int = 0, key_qjl: int = KEY_QJL, seed: int = 0, layer: int = 0, device="cuda",
                  head_dim: int | None = None):
         """d: the transform and code dimension (128 or 256); head_dim (default d):
         the length of the vectors the caller passes, zero-padded to d inside
-        the kernels (a multiple of 8 in (d/2, d])."""
+        the kernels (a multiple of 8 in (d/2, d]).  key_qjl: the key
+        correction, KEY_QJL (TurboQuant_prod, default), KEY_MSE (code only),
+        KEY_EDEN (unbiased scale) or KEY_RENORM (length renormalization);
+        True / False stand for KEY_QJL / KEY_MSE."""
         import torch
 
         self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
         self.head_dim = d if head_dim is None else head_dim
         self.key_bits, self.value_bits, self.kind, self.window = key_bits, value_bits, kind, window
-        self.key_qjl, self.seed, self.layer = bool(key_qjl), seed, layer
+        self.key_qjl, self.seed, self.layer = int(key_qjl), seed, layer
+        if self.key_qjl not in (KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM):
+            raise ValueError(f"key_qjl must be one of KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM, got {key_qjl}")
         self.k_cb = build_codebook(d, key_bits)
         self.v_cb = build_codebook(d, value_bits)
         kr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_KEY_ROT) for h in range(n_kv_heads)])
@@ -53,7 +58,7 @@ class TQLayer:
         self.k_rot_host, self.v_rot_host = kr, vr
         self.k_rot = torch.from_numpy(kr).to(device)
         self.v_rot = torch.from_numpy(vr).to(device)
-        if key_qjl:
+        if self.key_qjl == KEY_QJL:
             s = np.stack([build_transform(kind, d, seed, layer, h, ROLE_QJL) for h in range(n_kv_heads)])
             self.qjl_s_host = s
             self.qjl_s = torch.from_numpy(s).to(device)
@@ -61,10 +66,10 @@ class TQLayer:
             self.qjl_s_host, self.qjl_s = None, None
         p = LayerParams()
         p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = d, n_kv_heads, n_q_heads, PAGE_SIZE, window
-        p.key_bits, p.key_qjl, p.value_bits, p.kind = key_bits, int(key_qjl), value_bits, kind
+        p.key_bits, p.key_qjl, p.value_bits, p.kind = key_bits, self.key_qjl, value_bits, kind
         p.head_dim = self.head_dim
         p.k_rot, p.v_rot = self.k_rot.data_ptr(), self.v_rot.data_ptr()
-        p.qjl_s = self.qjl_s.data_ptr() if key_qjl else None
+        p.qjl_s = self.qjl_s.data_ptr() if self.qjl_s is not None else None
         for name, (c, t, _) in (("k", self.k_cb), ("v", self.v_cb)):
             getattr(p, f"{name}_centroids")[: len(c)] = [float(x) for x in c]
             getattr(p, f"{name}_bounds")[: len(t)] = [float(x) for x in t]

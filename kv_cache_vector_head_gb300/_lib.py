@@ -20,6 +20,7 @@ TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_NO_CONVERGENC
 TQ_DENSE, TQ_FWHT = 0, 1
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 ROLE_KEY_ROT, ROLE_VALUE_ROT, ROLE_QJL = 0, 1, 2
+KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM = 0, 1, 2, 3  # tq_key_correction
 PAGE_SIZE = 16
 
 EXPORTED = [

@@ -48,13 +48,13 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   if (p->window < 0) return fail(TQ_ERR_INVALID_ARG, "window must be >= 0");
   if (p->key_bits < 1 || p->key_bits > TQ_MAX_BITS || p->value_bits < 1 || p->value_bits > TQ_MAX_BITS)
     return fail(TQ_ERR_UNSUPPORTED, "key_bits and value_bits must be 1..4");
-  if (p->key_qjl != 0 && p->key_qjl != 1) return fail(TQ_ERR_INVALID_ARG, "key_qjl must be 0 or 1");
+  if (p->key_qjl < 0 || p->key_qjl > 3) return fail(TQ_ERR_INVALID_ARG, "key_qjl must be 0..3 (see tq_key_correction)");
   if (p->kind != TQ_DENSE && p->kind != TQ_FWHT) return fail(TQ_ERR_INVALID_ARG, "bad transform kind");
   if (p->head_dim != 0 && (p->head_dim % 8 != 0 || p->head_dim <= p->d / 2 || p->head_dim > p->d))
     return fail(TQ_ERR_INVALID_ARG, "head_dim must be 0 or a multiple of 8 in (d/2, d]");
   if (need_device_ptrs) {
     if (!p->k_rot || !p->v_rot) return fail(TQ_ERR_INVALID_ARG, "null k_rot / v_rot");
-    if (p->key_qjl && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
+    if (p->key_qjl == TQ_KEY_QJL && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
     if (!aligned(p->k_rot, 16) || !aligned(p->v_rot, 16) || (p->qjl_s && !aligned(p->qjl_s, 16)))
       return fail(TQ_ERR_INVALID_ARG, "transforms must be 16-byte aligned");
   }
@@ -98,7 +98,7 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   K->off_knorm = o; o += 4 * P;
   K->off_krnorm = o; o += p->key_qjl ? 4 * P : 0;
   K->off_kcodes = o; o += 4 * p->key_bits * P * w;
-  K->off_ksigns = o; o += p->key_qjl ? 4 * P * w : 0;
+  K->off_ksigns = o; o += p->key_qjl == TQ_KEY_QJL ? 4 * P * w : 0;
   K->off_vnorm = o; o += 4 * P;
   K->off_vcodes = o; o += 2 * p->value_bits * d;
   K->sub_bytes = o;
@@ -162,7 +162,9 @@ extern "C" tq_status tq_quantize_keys(const tq_layer_params* p, const void* k, t
   if (n_vec < 0) return fail(TQ_ERR_INVALID_ARG, "n_vec < 0");
   if (n_vec == 0) return ok();
   if (!k || !code_planes || !norms) return fail(TQ_ERR_INVALID_ARG, "null input or output");
-  if (K.kqjl && (!sign_planes || !rnorms)) return fail(TQ_ERR_INVALID_ARG, "key_qjl needs sign_planes and rnorms");
+  if (K.kqjl == TQ_KEY_QJL && (!sign_planes || !rnorms))
+    return fail(TQ_ERR_INVALID_ARG, "key_qjl needs sign_planes and rnorms");
+  if (K.kqjl >= TQ_KEY_EDEN && !rnorms) return fail(TQ_ERR_INVALID_ARG, "scaled keys need rnorms (the scale)");
   if (!aligned(k, 16)) return fail(TQ_ERR_INVALID_ARG, "k must be 16-byte aligned");
   return cuda_status(launch_quantize_flat(K, k, dtype, n_vec, true, code_planes, sign_planes, norms, rnorms,
                                           reinterpret_cast<cudaStream_t>(stream)),

@@ -7,6 +7,9 @@
 // basis with ONE inverse transform per head.  [Reconstruction] §6: score
 //   l = scale * n * ( <q', C[idx]> / sqrt(d) + sqrt(pi/2)/d * gamma * <q'', 2s - 1> ),
 //   q' = Pi q, q'' = S q'.
+// Keys with EDEN's unbiased scale or the renormalized length in place of the
+// sketch ([Reconstruction] §10, §12) drop the second term and multiply the
+// first by the stored scale s:  l = scale * n * s * <q', C[idx]> / sqrt(d).
 //
 // The two contractions of a decode step are dense products over the G query
 // heads of a KV head:  scores[h, t] = sum_j Q[h, j] K_hat[t, j] and
@@ -63,7 +66,7 @@ constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-static int key_frag_planes(const KParams& P) { return P.kp + (P.kqjl ? 1 : 0); }
+static int key_frag_planes(const KParams& P) { return P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0); }
 
 WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits, int num_sms) {
   WsLayout L{};
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
   rotate_tile<D, kPrologueTile>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
-  if (P.kqjl) {
+  if (P.kqjl == TQ_KEY_QJL) {
     // q'' rows of this CTA: TPR neighbouring threads per row, 64 inputs each
     const int row = 64 * z + j / TPR, u = j % TPR;
     const float4* rp = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)row * D) + u * 16;
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   // fragment entries of this CTA: lanes t4 with (t4 * WPL + kk / 8) / 2 == z,
   // i.e. t4 = z (d = 256) or t4 in {2z, 2z + 1} (d = 128)
   constexpr int NT4 = 4 / (D / 64);
-  const int nplanes = P.kp + (P.kqjl ? 1 : 0);
+  const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
   const int per_row = nplanes * KS * NT4 * 4;
   for (int v = 0; v < nv; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
                        pm1_pair(nw[nt][kk / 8], 2 * (kk % 8) + 1, pmM, pmO));
           }
         }
-        if (P.kqjl) {
+        if (P.kqjl == TQ_KEY_QJL) {
           const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
           uint32_t nq[2][WPL];
 #pragma unroll
@@ -643,8 +646,10 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
           if (live) {
             const float mse = accm[0][nt][e] + accm[0][nt][e + 2] + accm[1][nt][e] + accm[1][nt][e + 2];
             const float qj = accq[0][nt][e] + accq[0][nt][e + 2] + accq[1][nt][e] + accq[1][nt][e + 2];
-            const float gm = P.kqjl ? krn[t] : 0.f;
-            l = scale * knorm[t] * (mse * inv_sqrt_d + kappa * gm * qj);
+            // QJL: gamma times the sketch term; EDEN / renormalized keys: the scale s on the code's term
+            const float gm = P.kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
+            const float sk = P.kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
+            l = scale * knorm[t] * (sk * (mse * inv_sqrt_d) + kappa * gm * qj);
             if (scores) scores[(head0 + g8) * (size_t)max_ctx + tok] = l;
           }
           sc[nt][e] = l;

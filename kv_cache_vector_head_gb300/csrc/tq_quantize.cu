@@ -15,7 +15,9 @@
 //   3. bucketize z = sqrt(d) * (Pi x) / n against the float32 boundaries and
 //      pack sign-magnitude planes with warp ballots (warp w owns word w);
 //   4. keys: residual (in z units) z - C[idx], its norm, and the QJL sketch
-//      S (z - C[idx]) as a second tile product; signs packed by ballot.
+//      S (z - C[idx]) as a second tile product; signs packed by ballot.  The
+//      scaled corrections keep s instead: EDEN d / sum z C[idx], renormalized
+//      sqrt(d / sum C[idx]^2) (both from the same per-coordinate pass).
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -81,7 +83,11 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
         if (slot_of && slot_of[v] >= 0) vm[p] |= b << slot_of[v];
       }
     }
-    if (is_key) s.r[v][j] = z - s.cb[idx];
+    if (is_key) {
+      const float c = s.cb[idx];
+      // QJL: residual; EDEN: z c (z and c share a sign, so the terms are >= 0); renormalized: c^2
+      s.r[v][j] = P.kqjl == TQ_KEY_EDEN ? z * c : P.kqjl == TQ_KEY_RENORM ? c * c : z - c;
+    }
   }
   if (!is_key && slot_of) {
 #pragma unroll
@@ -89,18 +95,24 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
   }
   __syncthreads();
   if (!is_key) return;
-  // 4. residual norm gamma = ||z - C|| / sqrt(d)
+  // 4. residual norm gamma = ||z - C|| / sqrt(d), or the key scale s from the sum of the r entries
+  const bool scaled = P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM;
   for (int v = warp; v < nv; v += D / 32) {
     double acc = 0.0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const double rv = s.r[v][e * 32 + lane];
-      acc += rv * rv;
+      acc += scaled ? rv : rv * rv;
     }
     acc = warp_sum_d(acc);
-    if (lane == 0) s.gam[v] = s.zero[v] ? 0.f : (float)(sqrt(acc) / (double)sqrt_d);
+    if (lane == 0) {
+      const double g = P.kqjl == TQ_KEY_EDEN     ? (double)D / acc
+                       : P.kqjl == TQ_KEY_RENORM ? sqrt((double)D / acc)
+                                                 : sqrt(acc) / (double)sqrt_d;
+      s.gam[v] = s.zero[v] ? 0.f : (float)g;
+    }
   }
-  if (!P.kqjl) {
+  if (P.kqjl != TQ_KEY_QJL) {
     __syncthreads();
     return;
   }
@@ -164,7 +176,7 @@ __global__ void __launch_bounds__(D) quantize_flat_kernel(const __grid_constant_
       const long long n = (t0 + v) * P.hkv + head;
       codes[n * words + k] = s.codes[v][k / E][k % E];
     }
-    if (is_key && P.kqjl) {
+    if (is_key && P.kqjl == TQ_KEY_QJL) {
       for (int i = threadIdx.x; i < nv * E; i += D) {
         const int v = i / E, k = i % E;
         const long long n = (t0 + v) * P.hkv + head;
@@ -174,7 +186,7 @@ __global__ void __launch_bounds__(D) quantize_flat_kernel(const __grid_constant_
     if (threadIdx.x < nv) {
       const long long n = (t0 + threadIdx.x) * P.hkv + head;
       norms[n] = s.norm[threadIdx.x];
-      if (is_key && P.kqjl) rnorms[n] = s.gam[threadIdx.x];
+      if (is_key && P.kqjl) rnorms[n] = s.gam[threadIdx.x];  // gamma or the scale
     }
     __syncthreads();
   }
@@ -195,7 +207,7 @@ __device__ void store_key_slot(const KParams& P, const TileSmem<D>& s, unsigned 
     const int p = i / E, w = i % E;
     kc[(p * kPage + slot) * E + w] = s.codes[v][p][w];
   }
-  if (P.kqjl) {
+  if (P.kqjl == TQ_KEY_QJL) {
     uint32_t* ks = reinterpret_cast<uint32_t*>(sb + P.off_ksigns);
     for (int w = threadIdx.x; w < E; w += D) ks[slot * E + w] = s.signs[v][w];
   }
@@ -523,7 +535,7 @@ template <int MODE>
 static cudaError_t launch_quantize_warp_role(const KParams& P, const KCache& C, const void* x, long long n_vec,
                                              bool is_key, uint32_t* codes, uint32_t* signs, float* norms,
                                              float* rnorms, cudaStream_t st) {
-  const bool qjl = is_key && P.kqjl;
+  const bool qjl = is_key && P.kqjl == TQ_KEY_QJL;
   const int bits = is_key ? P.kb : P.vb;
   if (qjl)  // keys with the sketch: tcgen05 for S r (record indices fit 32 bits)
     return P.kind == TQ_FWHT

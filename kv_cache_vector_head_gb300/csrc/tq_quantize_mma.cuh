@@ -176,7 +176,8 @@ __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushor
 // block_table[b][seq_len[b] / 16]).
 enum { kFlat = 0, kStep = 1 };
 
-// Values, and keys without the QJL sketch (keys with it: quantize_keys_tc_kernel).
+// Values, and keys without the QJL sketch (keys with it: quantize_keys_tc_kernel),
+// with the EDEN / renormalized key scale where the layer keeps one.
 // DENSE: dense rotation (else FWHT).  grid (x, Hkv).
 template <int BITS, bool DENSE, int MODE>
 __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
@@ -201,6 +202,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
   const float* ctab = is_key ? P.kc : P.vc;
   const float* ttab = is_key ? P.kt : P.vt;
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
+  // keys with a scale in place of the sketch (EDEN / renormalized); 0 otherwise
+  const int corr = (is_key && (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM)) ? P.kqjl : 0;
   Book<BITS> bk;
 #pragma unroll
   for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(ttab[HALF + k]);
@@ -402,9 +405,11 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
 
     // codes, two blocks (one packed word) per pass
     uint32_t vword[2][4];      // step mode, values: plane t of words 0..3 of rows g, g + 8
+    float ssum[2] = {0.f, 0.f};  // scaled keys: this lane's share of sum |z| c (EDEN) or sum c^2
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       uint32_t Wm[2] = {0u, 0u};  // byte p: plane p of this lane's byte of word m
+      float spart[2] = {0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int a = 2 * m + hh;
@@ -449,7 +454,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
           }
         }
 #pragma unroll
-        for (int R = 0; R < 2; ++R)
+        for (int R = 0; R < 2; ++R) {
+          float term[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);  // +0 for zero rows
@@ -460,7 +466,18 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
             const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
             const int pos = 4 * hh + i;  // coordinate blk_base(a) + 8t + i is bit 8t + 4hh + i of word m
             Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
+            if (corr) {
+              // z and its centroid share a sign: z C = |z| C+
+              const float c = centroid_pos<BITS>(mag, bk);
+              term[i] = corr == TQ_KEY_EDEN ? fabsf(z) * c : c * c;
+            }
           }
+          if (corr) spart[R] += (term[0] + term[1]) + (term[2] + term[3]);
+        }
+      }
+      if (corr) {
+        ssum[0] += spart[0];
+        ssum[1] += spart[1];
       }
 #pragma unroll
       for (int R = 0; R < 2; ++R) {
@@ -473,6 +490,22 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
           } else {
             vword[R][m] = word;  // written into the coordinate-major planes after the loop
           }
+        }
+      }
+    }
+
+    if (corr) {
+      // key scale: EDEN s = d / sum z C, renormalized s = sqrt(d / sum C^2) (balanced
+      // trees of positive terms: depth 3 within a word pair, 4 words, 2 across the quad)
+#pragma unroll
+      for (int R = 0; R < 2; ++R) {
+        float a = ssum[R];
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        const float sc = zero[R] ? 0.f : (corr == TQ_KEY_EDEN ? (float)D / a : sqrtf((float)D / a));
+        if (okrow[R] && t == 0) {
+          if constexpr (MODE == kFlat) rnorms[nrow[R]] = sc;
+          else reinterpret_cast<float*>(dst[R] + P.off_krnorm)[slot[R]] = sc;
         }
       }
     }

@@ -54,7 +54,7 @@ class Workload:
     d: int
     ctx: int
     key_bits: int          # MSE bits of the key code (QJL adds one more bit)
-    key_qjl: bool
+    key_qjl: int           # key correction: 0 MSE only, 1 QJL, 2 EDEN scale, 3 length renormalization
     value_bits: int
     kind: int              # DENSE or FWHT
     window: int

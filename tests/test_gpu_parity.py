@@ -60,6 +60,14 @@ CASES = [
     ("bulk", dict(ctx=200, head_dim=96, key_bits=2, value_bits=3)),
     ("tiny", dict(ctx=60, head_dim=120)),
     ("long", dict(ctx=33, head_dim=160)),
+    # EDEN-unbiased (2) and length-renormalized (3) keys: a scale in place of the QJL sketch,
+    # through the warp tiles (d = 128 bf16, FWHT and dense) and the CUDA-core tiles
+    ("bulk", dict(ctx=300, kind=SK.FWHT, key_qjl=2)),
+    ("bulk", dict(ctx=400, key_bits=4, key_qjl=3)),
+    ("bulk", dict(ctx=130, kind=SK.FWHT, key_bits=1, key_qjl=2)),
+    ("bulk", dict(ctx=90, key_bits=3, key_qjl=2, head_dim=96)),
+    ("tiny", dict(ctx=70, key_qjl=3)),
+    ("long", dict(ctx=30, key_qjl=2)),
 ]
 
 
@@ -76,9 +84,9 @@ def test_quantize_flat_parity(tq, name, over):
     vt = SK.to_torch(V, dt).cuda()
     E = w.d // 32
     codes = torch.zeros(n_vec, w.key_bits * E, dtype=torch.int32, device="cuda")
-    signs = torch.zeros(n_vec, E, dtype=torch.int32, device="cuda") if w.key_qjl else None
+    signs = torch.zeros(n_vec, E, dtype=torch.int32, device="cuda") if w.key_qjl == 1 else None
     norms = torch.zeros(n_vec, device="cuda")
-    rn = torch.zeros(n_vec, device="cuda") if w.key_qjl else None
+    rn = torch.zeros(n_vec, device="cuda") if w.key_qjl else None  # gamma or the key scale
     tq.quantize_keys(L.params, kt, n_vec, codes, signs, norms, rn)
     vcodes = torch.zeros(n_vec, w.value_bits * E, dtype=torch.int32, device="cuda")
     vnorms = torch.zeros(n_vec, device="cuda")
@@ -91,7 +99,7 @@ def test_quantize_flat_parity(tq, name, over):
         sel = heads == h
         ok = O.keys(K[:n_vec][sel], h)
         g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d)
-        g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d) if w.key_qjl else None
+        g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d) if w.key_qjl == 1 else None
         g_r = rn.cpu().numpy()[sel] if w.key_qjl else None
         PY.compare_records(ok, g_idx, norms.cpu().numpy()[sel], g_s, g_r, True, stats)
         ov = O.values(V[:n_vec][sel], h)
@@ -221,6 +229,11 @@ PAGED = [
     # head sizes that are not powers of two
     ("llama", dict(batch=5, head_dim=96), 29, 21),
     ("qwen", dict(batch=2, window=20, head_dim=160), 45, 30),
+    # EDEN-unbiased and length-renormalized keys
+    ("llama", dict(batch=6, kind=SK.FWHT, key_qjl=2), 29, 21),
+    ("qwen", dict(batch=2, window=20, key_qjl=3), 75, 30),
+    ("bulk", dict(batch=9, key_qjl=3, key_bits=3), 40, 9),
+    ("tiny", dict(key_qjl=2), 37, 12),
 ]
 
 
@@ -266,8 +279,6 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
                 assert np.array_equal(ring[slots][:, :w.dh], win_k[h])
                 assert np.array_equal(pc.win_v[b, h].cpu().numpy()[slots][:, :w.dh], win_v[h])
                 assert not ring[slots][:, w.dh:].any()  # the padding of the window rows stays zero
-        if stats:
-            assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
         comp = PY.stack_comp(recs_k, recs_v) if nc else None
         r = PY.decode_reference(O, q[b], comp, win_k if T > nc else None, win_v if T > nc else None, scale)
         g_sc = scores[b].cpu().numpy()
@@ -276,6 +287,8 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
         assert sc_err.max() < PY.SCORE_ATOL, sc_err.max()
         assert np.abs(out[b].cpu().numpy() - r["out"]).max() < PY.OUT_ATOL
         assert np.abs(lse[b].cpu().numpy() - r["lse"]).max() < PY.SCORE_ATOL
+    if stats:  # the cap holds for the codes of the whole call
+        assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
 
 
 def test_decode_split_invariance_and_determinism(tq):

@@ -92,6 +92,16 @@ def test_argument_checks_return_status_without_gpu(L):
         p.head_dim = hd
         assert (lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * 140) == ok, hd
     p.head_dim = 0
+    # key corrections: scale-only records drop the sign plane (d / 8 bytes a token), 0..3 only
+    p.key_qjl = L.KEY_EDEN
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (140 - 16)
+    p.key_qjl = L.KEY_RENORM
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (140 - 16)
+    p.key_qjl = L.KEY_MSE
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (140 - 16 - 4)
+    p.key_qjl = 4
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"key_qjl" in lib.tq_last_error()
+    p.key_qjl = 1
     assert lib.tq_build_codebook(2, 2, None, None, None) == L.TQ_ERR_INVALID_ARG
     assert lib.tq_build_transform(L.TQ_FWHT, 96, 0, 0, 0, 0, None) == L.TQ_ERR_INVALID_ARG
     out = np.zeros(96, np.float32)
@@ -102,8 +112,9 @@ def test_argument_checks_return_status_without_gpu(L):
 def test_subblock_layout_matches_oracle(L):
     from oracle import paging as PG
 
-    for d, kb, qjl, vb in [(128, 2, 1, 2), (256, 2, 1, 2), (128, 3, 1, 4), (256, 4, 0, 1)]:
+    for d, kb, qjl, vb in [(128, 2, 1, 2), (256, 2, 1, 2), (128, 3, 1, 4), (256, 4, 0, 1), (128, 3, 2, 4),
+                           (256, 2, 3, 2)]:
         p = L.LayerParams()
         p.d, p.n_kv_heads, p.n_q_heads, p.page_size = d, 2, 4, 16
         p.key_bits, p.value_bits, p.key_qjl, p.kind = kb, vb, qjl, L.TQ_FWHT
-        assert L.subblock_bytes(p) == PG.subblock_layout(d, kb, bool(qjl), vb)["bytes"]
+        assert L.subblock_bytes(p) == PG.subblock_layout(d, kb, qjl, vb)["bytes"]
