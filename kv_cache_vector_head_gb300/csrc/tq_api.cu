@@ -89,8 +89,6 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   };
   walsh(p->k_centroids, p->key_bits, K->akw);
   walsh(p->v_centroids, p->value_bits, K->avw);
-  K->pm_mask = 0x80008000u;
-  K->pm_one = 0x3C003C00u;
   K->kp = 1 << (p->key_bits - 1);
   K->vp = 1 << (p->value_bits - 1);
   const int d = p->d, w = d / 32, P = TQ_PAGE_SIZE;

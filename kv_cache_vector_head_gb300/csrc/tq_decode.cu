@@ -18,16 +18,19 @@
 // EXACT in f16:
 //   * a b-bit code with sign s and magnitude bits m has centroid
 //     s * sum_S a_S prod_{i in S} (1 - 2 m_i) (Walsh expansion over the
-//     magnitude bits), so the token side is a sum of +-1 "planes" P_S whose
-//     sign bit is s ^ parity(m & S) -- built from the packed words with one
-//     shift and one LOP3 per pair of coordinates, no lookup;
+//     magnitude bits), so the token side is a sum of +-1 "planes" whose
+//     bit is s ^ parity(m & S); each f16 pair of an operand register comes
+//     from one LOP3 on the packed word (or a copy shifted by 6 or 10): the
+//     bit, kept at an exponent or sign position of 1.0 (2.0), reads as
+//     base + b delta, the other operand carries x / delta, and the +-1
+//     plane contracts to 2 D - K with a per-head constant K;
 //   * the query side a_S q' (and q'') and the softmax weights are split into
 //     f16 hi + lo limbs that occupy rows h and h + 8 of the 16-row tile
 //     (G <= 8 heads), so the second limb costs no extra instruction;
 //   * values with b >= 3 bits use f16 hi / lo limbs of the centroid itself
 //     (two planes) read from a 16-entry table, instead of 2^(b-1) planes.
-// Every product is exact and accumulation is f32, so the scores carry
-// ~2^-22 relative query rounding instead of f16's 2^-11.
+// Products are exact and accumulation is f32, so the scores carry ~2^-22
+// relative query rounding instead of f16's 2^-11.
 //
 // Launches per call:
 //   decode_prologue_kernel  grid (Hkv, ceil(batch G / 4), d / 64): q' = Pi q,
@@ -74,7 +77,10 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
   int S = n_splits;
   if (S <= 0) {
     const int units = std::max(1, batch * P.hkv);
-    S = (4 * num_sms + units - 1) / units;  // two waves of two CTAs per SM
+    // two waves of three CTAs per SM, or one wave where that would leave a split fewer
+    // than four 8-page chunks (the per-CTA start-up would not amortise)
+    S = (6 * num_sms + units - 1) / units;
+    if (max_pages / S < 32) S = (3 * num_sms + units - 1) / units;
     S = std::max(1, std::min(S, (max_pages + 7) / 8));
   }
   S = std::min(S, max_pages);
@@ -107,19 +113,27 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, uint32_t
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-// f16 pair (+-1, +-1) from bits i and i + 16 of nw = ~plane_word (bit set -> -1):
-// ((nw << (15 - i)) & 0x80008000) | 0x3C003C00.  The shift is an integer
-// multiply (FMA pipe); the mask-and-merge is one LOP3 whose two constants come
-// in registers (mask = 0x80008000, one = 0x3C003C00).
-__device__ __forceinline__ uint32_t pm1_mul(uint32_t nw, uint32_t mult, uint32_t mask, uint32_t one) {
-  uint32_t x, r;
-  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(nw), "r"(mult));
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(one));
-  return r;
+// One-LOP3 +-1 planes.  An f16 pair whose halves are 1.0 (0x3C00; 2.0 for
+// position 14) gets bit p of each half XORed in: p = 10..13 clear an
+// exponent bit of 1.0 (0.5, 0.25, 2^-4, 2^-8), p = 14 clears 2.0 to 0, p = 15
+// flips the sign.  A plane bit b then reads v = base_p + b delta_p; the other
+// operand carries x / delta_p, so the product sums to sum x b plus a
+// constant, and the +-1 plane (2 b - 1) contracts to 2 D - K with
+// K = sum_k A_k (2 base_k + delta_k) over the operand's entries.
+__host__ __device__ constexpr int xpos_key(int i) { return i >= 10 ? i : (i >= 4 ? i + 6 : i + 10); }
+__host__ __device__ constexpr uint32_t xbase(int p) { return p == 14 ? 0x40004000u : 0x3C003C00u; }
+__host__ __device__ inline float xdelta(int p) {
+  return p == 10 ? -0.5f : p == 11 ? -0.75f : p == 12 ? -0.9375f : p == 13 ? -0.99609375f : -2.0f;
 }
-__device__ __forceinline__ uint32_t pm1_pair(uint32_t nw, int i, uint32_t mask, uint32_t one) {
-  return pm1_mul(nw, 1u << (15 - i), mask, one);
+__host__ __device__ inline float xkfac(int p) { return 2.0f * (p == 14 ? 2.0f : 1.0f) + xdelta(p); }
+// B register of key bit i (and i + 16) from the word's copies shifted by 0, 6 and 10
+__device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t w10, int i) {
+  const int p = xpos_key(i);
+  const uint32_t src = i >= 10 ? w0 : (i >= 4 ? w6 : w10);
+  return (src & (0x00010001u << p)) ^ xbase(p);
 }
+// value token slot s of a page pair: position 10 + (s & 1) for s < 8, 14 + (s & 1) above
+__host__ __device__ constexpr int xpos_val(int s) { return (s < 8 ? 10 : 14) + (s & 1); }
 
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
@@ -273,6 +287,9 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
           va = s.r[v][ca];
           vb = s.r[v][cb];
         }
+        const float rd = 1.0f / xdelta(xpos_key(i0));  // the B side reads bit i0 as base + b delta
+        va *= rd;
+        vb *= rd;
         __half ha, la, hb, lb;
         split_f16(va, ha, la);
         split_f16(vb, hb, lb);
@@ -433,11 +450,13 @@ struct MmaShared {
   float redm[kMmaPages][TQ_MAX_GQA];  // per-warp chunk maxima
   float lsum[kMmaPages][TQ_MAX_GQA];  // per-warp softmax denominators
   float mfin[TQ_MAX_GQA];
+  float kvsum[kMmaPages][TQ_MAX_GQA];  // per-warp sums of the value operand's constant
+  float kcon[2][TQ_MAX_GQA];           // constant K of the key operand: MSE planes, QJL plane
   uint32_t vlut[16];  // values with b >= 3: raw sign-magnitude bits -> (hi, lo) f16 of the centroid
 };
 
 template <int D, bool VLUT>
-__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_constant__ KParams P,
+__global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ KCache C, const void* q,
                                                                  int dtype, float scale, float* scores,
                                                                  unsigned char* ws, WsLayout L, int max_ctx,
@@ -460,10 +479,6 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
   const float inv_sqrt_d = rsqrtf((float)D);
   const float kappa = sqrtf(1.57079632679489662f) / (float)D;
   const int sub = P.sub_bytes;
-  const uint32_t pmM = P.pm_mask, pmO = P.pm_one;
-  // value-phase shift multipliers of this lane: bits 2t, 2t+1, 8+2t, 9+2t -> bit 15
-  const uint32_t vm0 = 1u << (15 - 2 * t4), vm1 = 1u << (14 - 2 * t4), vm2 = 1u << (7 - 2 * t4),
-                 vm3 = 1u << (6 - 2 * t4);
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -548,6 +563,33 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
     const uint4* src = reinterpret_cast<const uint4*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
     for (int i = tid; i < (int)(L.afrag_bytes_per_head / 16); i += kMmaThreads) afr[i] = src[i];
   }
+  __syncthreads();
+  if (warp < G) {
+    // K of head `warp`: its A-fragment rows (lanes 4 warp .. 4 warp + 3) over all planes and k-blocks;
+    // register r of block kk pairs with key bit 2 (kk mod 8) + (r >= 2)
+    const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
+    float km = 0.f, kq = 0.f;
+    for (int it = lane; it < nplanes * KS * 4; it += 32) {
+      const int pl = it / (KS * 4), kk = (it / 4) % KS, t4i = it % 4;
+      const uint4 a = afr[(pl * KS + kk) * 32 + warp * 4 + t4i];
+      const uint32_t rr[4] = {a.x, a.y, a.z, a.w};
+      float sum = 0.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float f = xkfac(xpos_key(2 * (kk % 8) + (r >= 2 ? 1 : 0)));
+        sum += f * (__half2float(__ushort_as_half((unsigned short)(rr[r] & 0xffffu))) +
+                    __half2float(__ushort_as_half((unsigned short)(rr[r] >> 16))));
+      }
+      if (pl < P.kp) km += sum;
+      else kq += sum;
+    }
+    km = warp_sum_f(km);
+    kq = warp_sum_f(kq);
+    if (lane == 0) {
+      sh.kcon[0][warp] = km;
+      sh.kcon[1][warp] = kq;
+    }
+  }
 
   float accv[2][CB][4];
 #pragma unroll
@@ -557,6 +599,7 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
 #pragma unroll
       for (int r = 0; r < 4; ++r) accv[p][c][r] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;  // softmax state of head g8 (identical across warps for m)
+  float kv_run = 0.f;                     // this lane's share of the value operand's constant K
   bool timed_out = false;
 
   for (int k = 0; k < nchunks; ++k) {
@@ -597,38 +640,47 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
             for (int m = 0; m < 3; ++m) rm[m][nt][jw] = (m + 1 < P.kb) ? kc[((m + 1) * kPage + tk) * E + w] : 0u;
           }
         for (int S = 0; S < P.kp; ++S) {
-          uint32_t nw[2][WPL];
+          uint32_t w0[2][WPL], w6[2][WPL], w10[2][WPL];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int jw = 0; jw < WPL; ++jw)
-              nw[nt][jw] = ~(rs[nt][jw] ^ ((S & 1) ? rm[0][nt][jw] : 0u) ^ ((S & 2) ? rm[1][nt][jw] : 0u) ^
-                             ((S & 4) ? rm[2][nt][jw] : 0u));
+            for (int jw = 0; jw < WPL; ++jw) {
+              w0[nt][jw] = rs[nt][jw] ^ ((S & 1) ? rm[0][nt][jw] : 0u) ^ ((S & 2) ? rm[1][nt][jw] : 0u) ^
+                           ((S & 4) ? rm[2][nt][jw] : 0u);
+              w6[nt][jw] = w0[nt][jw] << 6;
+              w10[nt][jw] = w0[nt][jw] << 10;
+            }
           const uint4* ap = afr + (size_t)S * KS * 32 + lane;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const uint4 a = ap[kk * 32];
+            const int jw = kk / 8, i0 = 2 * (kk % 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accm[kk & 1][nt], a, pm1_pair(nw[nt][kk / 8], 2 * (kk % 8), pmM, pmO),
-                       pm1_pair(nw[nt][kk / 8], 2 * (kk % 8) + 1, pmM, pmO));
+              mma16816(accm[kk & 1][nt], a, xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0),
+                       xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0 + 1));
           }
         }
         if (P.kqjl == TQ_KEY_QJL) {
           const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
-          uint32_t nq[2][WPL];
+          uint32_t q0[2][WPL], q6[2][WPL], q10[2][WPL];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int jw = 0; jw < WPL; ++jw) nq[nt][jw] = ~ks[(8 * nt + g8) * E + t4 * WPL + jw];
+            for (int jw = 0; jw < WPL; ++jw) {
+              q0[nt][jw] = ks[(8 * nt + g8) * E + t4 * WPL + jw];
+              q6[nt][jw] = q0[nt][jw] << 6;
+              q10[nt][jw] = q0[nt][jw] << 10;
+            }
           const uint4* ap = afr + (size_t)P.kp * KS * 32 + lane;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const uint4 a = ap[kk * 32];
+            const int jw = kk / 8, i0 = 2 * (kk % 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accq[kk & 1][nt], a, pm1_pair(nq[nt][kk / 8], 2 * (kk % 8), pmM, pmO),
-                       pm1_pair(nq[nt][kk / 8], 2 * (kk % 8) + 1, pmM, pmO));
+              mma16816(accq[kk & 1][nt], a, xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0),
+                       xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0 + 1));
           }
         }
       }
@@ -644,8 +696,13 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
           const bool live = pvalid && g8 < G && tok < nc;
           float l = -INFINITY;
           if (live) {
-            const float mse = accm[0][nt][e] + accm[0][nt][e + 2] + accm[1][nt][e] + accm[1][nt][e + 2];
-            const float qj = accq[0][nt][e] + accq[0][nt][e + 2] + accq[1][nt][e] + accq[1][nt][e + 2];
+            // +-1 plane sums from the operand sums: 2 D - K
+            const float mse =
+                2.f * (accm[0][nt][e] + accm[0][nt][e + 2] + accm[1][nt][e] + accm[1][nt][e + 2]) - sh.kcon[0][g8];
+            const float qj = P.kqjl == TQ_KEY_QJL
+                                 ? 2.f * (accq[0][nt][e] + accq[0][nt][e + 2] + accq[1][nt][e] + accq[1][nt][e + 2]) -
+                                       sh.kcon[1][g8]
+                                 : 0.f;
             // QJL: gamma times the sketch term; EDEN / renormalized keys: the scale s on the code's term
             const float gm = P.kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
             const float sk = P.kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
@@ -677,7 +734,7 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
       // half = page parity within the pair
       const float* vnorm = reinterpret_cast<const float*>(pb + P.off_vnorm);
       uint16_t* wfh = reinterpret_cast<uint16_t*>(&sh.wf[warp >> 1][0][0]);
-      float ls = 0.f;
+      float ls = 0.f, kvs = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -689,13 +746,18 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
             ls += ex;
             wgt = ex * vnorm[t] * inv_sqrt_d;
           }
+          // +-1 value planes read slot t as base + b delta: the weight carries 1 / delta
+          const int xp = xpos_val(t);
+          if (!VLUT) wgt *= 1.0f / xdelta(xp);
           __half hi, lo;
           split_f16(wgt, hi, lo);
+          if (!VLUT) kvs += (__half2float(hi) + __half2float(lo)) * xkfac(xp);
           uint16_t* dst = wfh + ((nt * 32 + lane) * 4 + 2 * e) * 2 + (warp & 1);
           dst[0] = __half_as_ushort(hi);
           dst[2] = __half_as_ushort(lo);
         }
       l_run = l_run * alpha + ls;
+      kv_run = kv_run * alpha + kvs;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int p = 0; p < 2; ++p)
@@ -713,25 +775,32 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
       const uint16_t* vbp = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg + 1) * sub + P.off_vcodes);
       const uint4 wf0 = sh.wf[jg][0][lane], wf1 = sh.wf[jg][1][lane];
       if (!VLUT) {
-        uint32_t n0[CB], n1[CB];
+        // plane words (token slot s <-> bit s of each half), shifted so that slots 2 t4 + e sit at
+        // positions 10 + e (k-step 0) and slots 8 + 2 t4 + e at 14 + e (k-step 1)
+        uint32_t u0[CB], u1[CB];
 #pragma unroll
         for (int cbk = 0; cbk < CB; ++cbk) {
           const int c = warp * CPW + cbk * 8 + g8;
-          const uint32_t u0 = (uint32_t)va[c] | ((uint32_t)vbp[c] << 16);
-          n0[cbk] = ~u0;
-          n1[cbk] = P.vb == 2 ? ~(u0 ^ ((uint32_t)va[D + c] | ((uint32_t)vbp[D + c] << 16))) : 0u;
+          u0[cbk] = (uint32_t)va[c] | ((uint32_t)vbp[c] << 16);
+          u1[cbk] = P.vb == 2 ? (u0[cbk] ^ ((uint32_t)va[D + c] | ((uint32_t)vbp[D + c] << 16))) : 0u;
         }
 #pragma unroll
         for (int ksx = 0; ksx < 2; ++ksx) {
           const uint4 wfk = ksx ? wf1 : wf0;
-          const uint32_t ma = ksx ? vm2 : vm0, mb = ksx ? vm3 : vm1;
+          const int sft = (ksx ? 6 : 10) - 2 * t4, pa = ksx ? 14 : 10;
 #pragma unroll
-          for (int cbk = 0; cbk < CB; ++cbk)
-            mma16816(accv[0][cbk], wfk, pm1_mul(n0[cbk], ma, pmM, pmO), pm1_mul(n0[cbk], mb, pmM, pmO));
+          for (int cbk = 0; cbk < CB; ++cbk) {
+            const uint32_t x = u0[cbk] << sft;
+            mma16816(accv[0][cbk], wfk, (x & (0x00010001u << pa)) ^ xbase(pa),
+                     (x & (0x00010001u << (pa + 1))) ^ xbase(pa + 1));
+          }
           if (P.vb == 2) {
 #pragma unroll
-            for (int cbk = 0; cbk < CB; ++cbk)
-              mma16816(accv[1][cbk], wfk, pm1_mul(n1[cbk], ma, pmM, pmO), pm1_mul(n1[cbk], mb, pmM, pmO));
+            for (int cbk = 0; cbk < CB; ++cbk) {
+              const uint32_t x = u1[cbk] << sft;
+              mma16816(accv[1][cbk], wfk, (x & (0x00010001u << pa)) ^ xbase(pa),
+                       (x & (0x00010001u << (pa + 1))) ^ xbase(pa + 1));
+            }
           }
         }
       } else {
@@ -769,10 +838,15 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
     for (int k = 0; k < nchunks; ++k) (void)mbar_wait_bounded(&sh.full[k % nst], (uint32_t)((k / nst) & 1));
   }
   // ---- partials
-  float ls = l_run;
+  float ls = l_run, kvl = kv_run;
   ls += __shfl_xor_sync(0xffffffffu, ls, 1);
   ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-  if (t4 == 0) sh.lsum[warp][g8] = ls;
+  kvl += __shfl_xor_sync(0xffffffffu, kvl, 1);
+  kvl += __shfl_xor_sync(0xffffffffu, kvl, 2);
+  if (t4 == 0) {
+    sh.lsum[warp][g8] = ls;
+    sh.kvsum[warp][g8] = kvl;
+  }
   if (warp == 0 && t4 == 0) sh.mfin[g8] = m_run;
   __syncthreads();
   float* ml = reinterpret_cast<float*>(ws + L.ml);
@@ -781,11 +855,20 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const __grid_co
     // acc_rot[h][c] = sum over planes of coefficient x (hi-limb row + lo-limb row)
     const float c0 = VLUT ? 1.f : P.avw[0];
     const float c1 = VLUT ? 1.f : (P.vb == 2 ? P.avw[1] : 0.f);
+    // +-1 value planes: 2 D - K with K summed over every warp's tokens (the LUT limbs need no correction)
+    float kv = 0.f;
+    if (!VLUT) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) kv += sh.kvsum[w][g8];
+    }
+    const float pm = VLUT ? 1.f : 2.f;
 #pragma unroll
     for (int cbk = 0; cbk < CB; ++cbk) {
       const int c = warp * CPW + cbk * 8 + 2 * t4;
-      const float v0 = c0 * (accv[0][cbk][0] + accv[0][cbk][2]) + c1 * (accv[1][cbk][0] + accv[1][cbk][2]);
-      const float v1 = c0 * (accv[0][cbk][1] + accv[0][cbk][3]) + c1 * (accv[1][cbk][1] + accv[1][cbk][3]);
+      const float v0 = c0 * (pm * (accv[0][cbk][0] + accv[0][cbk][2]) - kv) +
+                       c1 * (pm * (accv[1][cbk][0] + accv[1][cbk][2]) - kv);
+      const float v1 = c0 * (pm * (accv[0][cbk][1] + accv[0][cbk][3]) - kv) +
+                       c1 * (pm * (accv[1][cbk][1] + accv[1][cbk][3]) - kv);
       float* dst = acc + ((head0 + g8) * st + s) * D + c;
       dst[0] = v0;
       dst[1] = v1;
@@ -917,7 +1000,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
   const size_t stage_bytes = (size_t)kMmaPages * P.sub_bytes;
   int nst = kStages;
   size_t dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
-  if (dyn > 110 * 1024) {  // keep two CTAs per SM where the pages are large
+  if (dyn > 72 * 1024) {  // keep three CTAs per SM where the pages are large
     nst = 2;
     dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
   }

@@ -26,8 +26,6 @@ struct KParams {
   // s * sum_S a_S * prod_{i in S} (1 - 2 m_i); plane S has bit s ^ parity(m & S).
   float akw[8], avw[8];
   int kp, vp;                          // 2^(bits-1) planes
-  uint32_t pm_mask, pm_one;            // 0x80008000 and 0x3C003C00, passed as data so that the
-                                       // +-1 operand merge stays a single three-register LOP3
   int sub_bytes;                       // bytes of one (page, head) sub-block
   int off_knorm, off_krnorm, off_kcodes, off_ksigns, off_vnorm, off_vcodes;
 };
