@@ -89,6 +89,8 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   };
   walsh(p->k_centroids, p->key_bits, K->akw);
   walsh(p->v_centroids, p->value_bits, K->avw);
+  K->xb1 = 0x3C003C00u;
+  K->xb2 = 0x40004000u;
   K->kp = 1 << (p->key_bits - 1);
   K->vp = 1 << (p->value_bits - 1);
   const int d = p->d, w = d / 32, P = TQ_PAGE_SIZE;

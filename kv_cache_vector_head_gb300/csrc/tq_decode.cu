@@ -69,6 +69,10 @@ constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Resident decode CTAs per SM: three at d = 128 (80 registers), two at d = 256,
+// whose larger register tiles would spill under the three-CTA cap.
+__host__ __device__ constexpr int mma_ctas_per_sm(int d) { return d == 128 ? 3 : 2; }
+
 static int key_frag_planes(const KParams& P) { return P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0); }
 
 WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits, int num_sms) {
@@ -77,10 +81,11 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
   int S = n_splits;
   if (S <= 0) {
     const int units = std::max(1, batch * P.hkv);
-    // two waves of three CTAs per SM, or one wave where that would leave a split fewer
-    // than four 8-page chunks (the per-CTA start-up would not amortise)
-    S = (6 * num_sms + units - 1) / units;
-    if (max_pages / S < 32) S = (3 * num_sms + units - 1) / units;
+    // two waves of resident CTAs, or one wave where that would leave a split fewer than
+    // four 8-page chunks (the per-CTA start-up would not amortise)
+    const int cps = mma_ctas_per_sm(P.d);
+    S = (2 * cps * num_sms + units - 1) / units;
+    if (max_pages / S < 32) S = (cps * num_sms + units - 1) / units;
     S = std::max(1, std::min(S, (max_pages + 7) / 8));
   }
   S = std::min(S, max_pages);
@@ -126,11 +131,12 @@ __host__ __device__ inline float xdelta(int p) {
   return p == 10 ? -0.5f : p == 11 ? -0.75f : p == 12 ? -0.9375f : p == 13 ? -0.99609375f : -2.0f;
 }
 __host__ __device__ inline float xkfac(int p) { return 2.0f * (p == 14 ? 2.0f : 1.0f) + xdelta(p); }
-// B register of key bit i (and i + 16) from the word's copies shifted by 0, 6 and 10
-__device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t w10, int i) {
+// B register of key bit i (and i + 16) from the word's copies shifted by 0, 6 and 10;
+// b1, b2 = xbase(10), xbase(14) in registers
+__device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t w10, int i, uint32_t b1, uint32_t b2) {
   const int p = xpos_key(i);
   const uint32_t src = i >= 10 ? w0 : (i >= 4 ? w6 : w10);
-  return (src & (0x00010001u << p)) ^ xbase(p);
+  return (src & (0x00010001u << p)) ^ (p == 14 ? b2 : b1);
 }
 // value token slot s of a page pair: position 10 + (s & 1) for s < 8, 14 + (s & 1) above
 __host__ __device__ constexpr int xpos_val(int s) { return (s < 8 ? 10 : 14) + (s & 1); }
@@ -456,7 +462,7 @@ struct MmaShared {
 };
 
 template <int D, bool VLUT>
-__global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid_constant__ KParams P,
+__global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ KCache C, const void* q,
                                                                  int dtype, float scale, float* scores,
                                                                  unsigned char* ws, WsLayout L, int max_ctx,
@@ -479,6 +485,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid
   const float inv_sqrt_d = rsqrtf((float)D);
   const float kappa = sqrtf(1.57079632679489662f) / (float)D;
   const int sub = P.sub_bytes;
+  const uint32_t xb1 = P.xb1, xb2 = P.xb2;
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -657,8 +664,8 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid
             const int jw = kk / 8, i0 = 2 * (kk % 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accm[kk & 1][nt], a, xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0),
-                       xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0 + 1));
+              mma16816(accm[kk & 1][nt], a, xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0, xb1, xb2),
+                       xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0 + 1, xb1, xb2));
           }
         }
         if (P.kqjl == TQ_KEY_QJL) {
@@ -679,8 +686,8 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid
             const int jw = kk / 8, i0 = 2 * (kk % 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma16816(accq[kk & 1][nt], a, xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0),
-                       xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0 + 1));
+              mma16816(accq[kk & 1][nt], a, xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0, xb1, xb2),
+                       xreg_key(q0[nt][jw], q6[nt][jw], q10[nt][jw], i0 + 1, xb1, xb2));
           }
         }
       }
@@ -791,15 +798,15 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const __grid
 #pragma unroll
           for (int cbk = 0; cbk < CB; ++cbk) {
             const uint32_t x = u0[cbk] << sft;
-            mma16816(accv[0][cbk], wfk, (x & (0x00010001u << pa)) ^ xbase(pa),
-                     (x & (0x00010001u << (pa + 1))) ^ xbase(pa + 1));
+            mma16816(accv[0][cbk], wfk, (x & (0x00010001u << pa)) ^ (ksx ? xb2 : xb1),
+                     (x & (0x00010001u << (pa + 1))) ^ xb1);
           }
           if (P.vb == 2) {
 #pragma unroll
             for (int cbk = 0; cbk < CB; ++cbk) {
               const uint32_t x = u1[cbk] << sft;
-              mma16816(accv[1][cbk], wfk, (x & (0x00010001u << pa)) ^ xbase(pa),
-                       (x & (0x00010001u << (pa + 1))) ^ xbase(pa + 1));
+              mma16816(accv[1][cbk], wfk, (x & (0x00010001u << pa)) ^ (ksx ? xb2 : xb1),
+                       (x & (0x00010001u << (pa + 1))) ^ xb1);
             }
           }
         }
@@ -1000,7 +1007,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
   const size_t stage_bytes = (size_t)kMmaPages * P.sub_bytes;
   int nst = kStages;
   size_t dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
-  if (dyn > 72 * 1024) {  // keep three CTAs per SM where the pages are large
+  if (dyn > (mma_ctas_per_sm(D) == 3 ? 72 : 110) * 1024) {  // keep the resident CTAs where the pages are large
     nst = 2;
     dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
   }

@@ -26,6 +26,8 @@ struct KParams {
   // s * sum_S a_S * prod_{i in S} (1 - 2 m_i); plane S has bit s ^ parity(m & S).
   float akw[8], avw[8];
   int kp, vp;                          // 2^(bits-1) planes
+  uint32_t xb1, xb2;                   // 0x3C003C00 and 0x40004000 (f16 pairs 1.0, 2.0), passed as data so
+                                       // that an operand register stays one LOP3 with a register operand
   int sub_bytes;                       // bytes of one (page, head) sub-block
   int off_knorm, off_krnorm, off_kcodes, off_ksigns, off_vnorm, off_vcodes;
 };
