@@ -32,7 +32,7 @@ import math
 import numpy as np
 
 from . import transforms as T
-from .codec import qjl_constant
+from .codec import centroid_values, qjl_constant
 
 
 def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v: np.ndarray | None,
@@ -46,7 +46,9 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
     win_k, win_v : [Hkv, Tw, d] float16 window tokens (oldest first), or None.
     params : kind, k_rot[Hkv], v_rot[Hkv], qjl_s[Hkv] (stored float32 arrays),
              k_cb, v_cb (Codebook), key_qjl: key correction (0 none, 1 QJL,
-             2 EDEN scale, 3 length renormalization; krnorm holds gamma or s).
+             2 EDEN scale, 3 length renormalization; krnorm holds gamma or s);
+             optional k_cb_hi: mixed-channel key rate (coordinates < d/2 read
+             this book).  knorm holds decoded norms (byte norms decoded).
     Returns out [Hq, d], lse [Hq], scores [Hq, T] (compressed first, then window).
     """
     Hq, d = q.shape
@@ -54,7 +56,6 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
     G = Hq // Hkv
     kind = params["kind"]
     kap = qjl_constant(d)
-    Ck = np.asarray(params["k_cb"].centroids, np.float32).astype(np.float64)
     Cv = np.asarray(params["v_cb"].centroids, np.float32).astype(np.float64)
     Tc = 0 if comp is None else comp["knorm"].shape[1]
     Tw = 0 if win_k is None else win_k.shape[1]
@@ -67,7 +68,7 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
         parts = []
         if Tc:
             q1 = T.rotate(kind, params["k_rot"][g], qh[None, :])[0]
-            l_c = Ck[comp["kidx"][g]] @ q1 / math.sqrt(d)
+            l_c = centroid_values(comp["kidx"][g], params["k_cb"], params.get("k_cb_hi")) @ q1 / math.sqrt(d)
             corr = int(params["key_qjl"])
             if corr == 1:  # QJL residual term
                 q2 = np.asarray(params["qjl_s"][g], np.float32).astype(np.float64) @ q1

@@ -29,6 +29,14 @@ idx >= 2^(b-1)); planes 1..b-1 hold the magnitude m (LSB first), where
 m = idx - 2^(b-1) on the non-negative side and m = 2^(b-1) - 1 - idx on the
 negative side.  Coordinate j sits at bit (j mod 32) of 32-bit word j // 32.
 The QJL sketch is one plane, bit = 1 iff (S r)_j >= 0.
+
+Mixed-channel rate ([Design study] §Packed format and complete bit
+accounting: fractional rates by channel allocation, e.g. 3.5 bits per channel
+= half the channels at 3 bits and half at 4, fixed offsets, no decoder
+state).  Reading: the rotated coordinates 0 .. d/2 - 1 take the (b+1)-bit
+Lloyd-Max book and the rest the b-bit book (the page does not say which
+half; after the rotation every coordinate has the same law).  Byte norms
+(same section, "u8 log-norm"): see norm_u8_encode.
 """
 
 from __future__ import annotations
@@ -73,8 +81,20 @@ def boundary_margin(z: np.ndarray, boundaries: np.ndarray) -> np.ndarray:
     return np.min(np.abs(z[..., None] - t), axis=-1)
 
 
-def quantize_mse(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook) -> dict:
-    """TurboQuant_mse of the rows of x ([N, d]); everything in float64."""
+def centroid_values(idx: np.ndarray, cb: Codebook, cb_hi: Codebook | None = None) -> np.ndarray:
+    """Float64 copies of the float32 RMS-scaled centroids C[idx], per coordinate.
+    Mixed-channel rate (cb_hi given): coordinates 0 .. d/2 - 1 read cb_hi."""
+    book = lambda c: np.asarray(c.centroids, dtype=np.float32).astype(np.float64)
+    if cb_hi is None:
+        return book(cb)[idx]
+    h = idx.shape[-1] // 2
+    return np.concatenate([book(cb_hi)[idx[..., :h]], book(cb)[idx[..., h:]]], axis=-1)
+
+
+def quantize_mse(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, cb_hi: Codebook | None = None) -> dict:
+    """TurboQuant_mse of the rows of x ([N, d]); everything in float64.
+    cb_hi (mixed-channel rate): rotated coordinates 0 .. d/2 - 1 are coded
+    with cb_hi, the rest with cb (see centroid_values)."""
     x = np.asarray(x, dtype=np.float64)
     d = x.shape[-1]
     n = np.sqrt(np.sum(x * x, axis=-1))
@@ -82,15 +102,23 @@ def quantize_mse(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook) -> dic
     u = np.where(zero[:, None], 0.0, x / np.where(zero, 1.0, n)[:, None])
     y = T.rotate(kind, rot, u)
     z = math.sqrt(d) * y
-    idx = bucketize(z, cb.boundaries)
-    yhat = np.asarray(cb.centroids, dtype=np.float32).astype(np.float64)[idx] / math.sqrt(d)
+    if cb_hi is None:
+        idx = bucketize(z, cb.boundaries)
+        margin = boundary_margin(z, cb.boundaries)
+    else:
+        h = d // 2
+        idx = np.concatenate([bucketize(z[:, :h], cb_hi.boundaries), bucketize(z[:, h:], cb.boundaries)], axis=-1)
+        margin = np.concatenate([boundary_margin(z[:, :h], cb_hi.boundaries),
+                                 boundary_margin(z[:, h:], cb.boundaries)], axis=-1)
+    yhat = centroid_values(idx, cb, cb_hi) / math.sqrt(d)
     norm32 = np.where(zero, 0.0, n).astype(np.float32)
     return {"norm": norm32, "norm_f64": np.where(zero, 0.0, n), "idx": idx, "y": y, "z": z,
-            "yhat": yhat, "zero": zero, "margin": boundary_margin(z, cb.boundaries)}
+            "yhat": yhat, "zero": zero, "margin": margin}
 
 
 def quantize_prod(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, S: np.ndarray) -> dict:
-    """TurboQuant_prod of the rows of x: MSE code + residual norm + QJL signs."""
+    """TurboQuant_prod of the rows of x: MSE code + residual norm + QJL signs
+    (uniform rate only: the mixed-channel key mode carries no sketch)."""
     rec = quantize_mse(x, kind, rot, cb)
     r = rec["y"] - rec["yhat"]
     gamma = np.sqrt(np.sum(r * r, axis=-1))
@@ -116,12 +144,13 @@ def quantize_prod(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, S: np
 KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM = 0, 1, 2, 3
 
 
-def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mode: int) -> dict:
+def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mode: int,
+                    cb_hi: Codebook | None = None) -> dict:
     """TurboQuant_mse code of the rows of x plus the scale s of the key
     correction `mode` (KEY_EDEN or KEY_RENORM), stored as float32 in the
     record's "rnorm" slot; the key is reconstructed as n s Pi^T y_hat.  For a
-    zero vector s = 0."""
-    rec = quantize_mse(x, kind, rot, cb)
+    zero vector s = 0.  cb_hi: mixed-channel rate as in quantize_mse."""
+    rec = quantize_mse(x, kind, rot, cb, cb_hi)
     y, yhat, zero = rec["y"], rec["yhat"], rec["zero"]
     if mode == KEY_EDEN:
         den = np.sum(y * yhat, axis=-1)          # y is a unit vector: ||y||^2 = 1
@@ -135,9 +164,9 @@ def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mod
     return rec
 
 
-def dequantize_scaled(norm, scale, idx, kind, rot, cb) -> np.ndarray:
+def dequantize_scaled(norm, scale, idx, kind, rot, cb, cb_hi=None) -> np.ndarray:
     """k_hat = n s Pi^T y_hat for the EDEN / renormalized keys."""
-    return np.asarray(scale, dtype=np.float64)[:, None] * dequantize_mse(norm, idx, kind, rot, cb)
+    return np.asarray(scale, dtype=np.float64)[:, None] * dequantize_mse(norm, idx, kind, rot, cb, cb_hi)
 
 
 def code_planes(idx: np.ndarray, bits: int) -> np.ndarray:
@@ -187,10 +216,11 @@ def unpack_codes(words: np.ndarray, bits: int, d: int) -> np.ndarray:
 
 # ----------------------------------------------------------------------------- reconstruction
 
-def dequantize_mse(norm: np.ndarray, idx: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook) -> np.ndarray:
+def dequantize_mse(norm: np.ndarray, idx: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook,
+                   cb_hi: Codebook | None = None) -> np.ndarray:
     """x_hat = n Pi^T c[idx] / sqrt(d)  ([Reconstruction] §5 Step 5)."""
     d = idx.shape[-1]
-    yhat = np.asarray(cb.centroids, dtype=np.float32).astype(np.float64)[idx] / math.sqrt(d)
+    yhat = centroid_values(idx, cb, cb_hi) / math.sqrt(d)
     return np.asarray(norm, dtype=np.float64)[:, None] * T.rotate_inverse(kind, rot, yhat)
 
 
@@ -219,3 +249,61 @@ def qjl_estimate(q: np.ndarray, r_norm, signs: np.ndarray, S: np.ndarray) -> np.
     d = q.shape[-1]
     pm = np.where(np.asarray(signs, dtype=bool), 1.0, -1.0)
     return qjl_constant(d) * np.asarray(r_norm, dtype=np.float64) * np.sum(sketch(q, S) * pm, axis=-1)
+
+
+# ----------------------------------------------------------------------------- mixed-channel rate, byte norms
+
+def pack_codes_split(idx: np.ndarray, bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Mixed-channel rate ([Design study] §Packed format: 3.5 bits per
+    channel = half the channels at 3 bits, half at 4): coordinates 0 .. d/2-1
+    hold (bits + 1)-bit codes, the rest bits-bit codes, both sign-magnitude.
+    Planes 0 .. bits-1 mean the same in both halves (sign, then magnitude
+    bits LSB first) and cover all d coordinates; plane `bits` (the top
+    magnitude bit of the wider codes) exists for the first half only.
+    Returns (uint32 [N, bits, d/32], uint32 [N, d/64])."""
+    d = idx.shape[-1]
+    h = d // 2
+    hi = code_planes(idx[..., :h], bits + 1)
+    lo = code_planes(idx[..., h:], bits)
+    main = np.concatenate([hi[..., :bits, :], lo], axis=-1)
+    return pack_bits(main), pack_bits(hi[..., bits, :])
+
+
+def unpack_codes_split(words: np.ndarray, extra: np.ndarray, bits: int, d: int) -> np.ndarray:
+    h = d // 2
+    planes = unpack_bits(words, d)                        # [..., bits, d]
+    top = unpack_bits(extra, h)[..., None, :]             # [..., 1, d/2]
+    hi = np.concatenate([planes[..., :, :h], top], axis=-2)
+    return np.concatenate([planes_to_idx(hi), planes_to_idx(planes[..., :, h:])], axis=-1)
+
+
+NORM_U8_LEVELS = 255  # codes 1..255; code 0 marks a zero vector
+
+
+def norm_u8_step(lo: float, hi: float) -> float:
+    """log2 spacing of the byte norm codes over [2^lo, 2^hi]."""
+    return (hi - lo) / (NORM_U8_LEVELS - 1)
+
+
+def norm_u8_encode(n: np.ndarray, lo: float, hi: float) -> tuple[np.ndarray, np.ndarray]:
+    """u8 log-norm ([Design study] §Packed format: one byte per token-head
+    for the key norm, 8 / d bits per channel).  Reading: codes 1..255 are
+    uniform in log2 over [lo, hi] (a per-layer range), round to nearest with
+    ties up, clamped at both ends; code 0 is the zero vector (n < 1e-7).
+      t = (log2 n - lo) / step,  code = 1 + min(254, max(0, floor(t + 1/2))).
+    Returns (codes uint8, margin): margin is |t - decision point| in code
+    units for the nearest of the 254 decision points t = k + 1/2."""
+    n = np.asarray(n, dtype=np.float64)
+    zero = n < ZERO_NORM
+    t = (np.log2(np.where(zero, 1.0, n)) - lo) / norm_u8_step(lo, hi)
+    k = np.clip(np.floor(t + 0.5), 0, NORM_U8_LEVELS - 1)
+    codes = np.where(zero, 0, 1 + k).astype(np.uint8)
+    kd = np.clip(np.round(t - 0.5), 0, NORM_U8_LEVELS - 2)
+    margin = np.where(zero, np.inf, np.abs(t - (kd + 0.5)))
+    return codes, margin
+
+
+def norm_u8_decode(codes: np.ndarray, lo: float, hi: float) -> np.ndarray:
+    """n_hat = 2^(lo + (code - 1) step); 0 for code 0."""
+    c = np.asarray(codes, dtype=np.float64)
+    return np.where(c == 0, 0.0, np.exp2(lo + (c - 1.0) * norm_u8_step(lo, hi)))

@@ -10,9 +10,10 @@ the hot path and are not stored (the sidecar is deferred by the page itself:
 "no outlier sidecar initially").
 
 Sub-block of one (page, kv head), P = 16 tokens, in this order (byte sizes):
-  key norms          float32[P]                               4 P
+  key norms          float32[P]  (uint8[P] as byte codes)     4 P  (P)
   key residual norms float32[P]          (only with QJL)      4 P
   key code planes    uint32[b_k][P][d/32]  token-major        b_k P d / 8
+  key top plane      uint32[P][d/64]  (mixed-channel rate)    P d / 16
   key sign plane     uint32[P][d/32]       (only with QJL)    P d / 8
   value norms        float32[P]                               4 P
   value code planes  uint16[b_v][d]        coordinate-major:  b_v P d / 8
@@ -40,16 +41,22 @@ def n_compressed(T: int, W: int, P: int = PAGE) -> int:
     return P * (max(0, T - W) // P)
 
 
-def subblock_layout(d: int, key_bits: int, key_qjl: int, value_bits: int, P: int = PAGE) -> dict:
-    """key_qjl: key correction (0 none, 1 QJL: scale slot + sign plane, 2 / 3 EDEN / renormalized: scale slot)."""
+def subblock_layout(d: int, key_bits: int, key_qjl: int, value_bits: int, P: int = PAGE,
+                    key_split: int = 0, key_norm_u8: int = 0) -> dict:
+    """key_qjl: key correction (0 none, 1 QJL: scale slot + sign plane, 2 / 3 EDEN / renormalized: scale slot).
+    key_split: mixed-channel key rate (the first d/2 coordinates carry one more plane, stored after the
+    key_bits full planes as uint32 [P][d/64]).  key_norm_u8: key norms as one byte per token."""
     if P != PAGE:
         raise ValueError("page size is fixed at 16 tokens")
+    if key_split and (key_qjl == 1 or d % 64):
+        raise ValueError("the mixed-channel key rate needs d % 64 == 0 and no QJL sketch")
     w = d // 32
     off = {}
     o = 0
-    off["key_norm"] = o; o += 4 * P
+    off["key_norm"] = o; o += (1 if key_norm_u8 else 4) * P
     off["key_rnorm"] = o; o += 4 * P if key_qjl else 0
     off["key_codes"] = o; o += 4 * key_bits * P * w
+    off["key_xcodes"] = o; o += 4 * P * (w // 2) if key_split else 0
     off["key_signs"] = o; o += 4 * P * w if key_qjl == 1 else 0
     off["value_norm"] = o; o += 4 * P
     off["value_codes"] = o; o += 2 * value_bits * d
@@ -57,31 +64,42 @@ def subblock_layout(d: int, key_bits: int, key_qjl: int, value_bits: int, P: int
     return off
 
 
-def record_bytes(d: int, key_bits: int, key_qjl: bool, value_bits: int) -> int:
+def record_bytes(d: int, key_bits: int, key_qjl: bool, value_bits: int, key_split: int = 0,
+                 key_norm_u8: int = 0) -> int:
     """Bytes per (token, kv head): the D1 + D2 storage formulas of
-    [Reconstruction] §8 with float32 norms."""
-    kb = 4 + (4 if key_qjl else 0) + key_bits * d // 8 + (d // 8 if key_qjl == 1 else 0)
+    [Reconstruction] §8 with float32 norms, or the [Design study] bit
+    accounting with a byte key norm and mixed-channel key rates."""
+    kb = (1 if key_norm_u8 else 4) + (4 if key_qjl else 0) + key_bits * d // 8 + (d // 16 if key_split else 0)
+    kb += d // 8 if key_qjl == 1 else 0
     vb = 4 + value_bits * d // 8
     return kb + vb
 
 
 def write_page(pool: np.ndarray, lay: dict, n_heads: int, page: int, head: int, slot: int,
                d: int, key_bits: int, key_qjl: bool, value_bits: int,
-               knorm, krnorm, kcode_words, ksign_words, vnorm, vcode_planes_bits) -> None:
+               knorm, krnorm, kcode_words, ksign_words, vnorm, vcode_planes_bits,
+               kxcode_words=None, key_norm_u8: int = 0) -> None:
     """Write one token record into the byte pool (uint8 [n_pages * n_heads * bytes]).
 
     kcode_words: uint32 [key_bits, d/32]; ksign_words: uint32 [d/32];
-    vcode_planes_bits: uint8 0/1 [value_bits, d].
+    vcode_planes_bits: uint8 0/1 [value_bits, d]; kxcode_words: uint32 [d/64]
+    (mixed-channel keys); knorm: the float32 norm, or its byte code with key_norm_u8.
     """
     base = (page * n_heads + head) * lay["bytes"]
     sb = pool[base: base + lay["bytes"]]
     w = d // 32
-    sb[lay["key_norm"] + 4 * slot: lay["key_norm"] + 4 * slot + 4] = np.array([knorm], np.float32).view(np.uint8)
+    if key_norm_u8:
+        sb[lay["key_norm"] + slot] = np.uint8(knorm)
+    else:
+        sb[lay["key_norm"] + 4 * slot: lay["key_norm"] + 4 * slot + 4] = np.array([knorm], np.float32).view(np.uint8)
     if key_qjl:
         sb[lay["key_rnorm"] + 4 * slot: lay["key_rnorm"] + 4 * slot + 4] = np.array([krnorm], np.float32).view(np.uint8)
     for p in range(key_bits):
         o = lay["key_codes"] + 4 * ((p * PAGE + slot) * w)
         sb[o: o + 4 * w] = np.asarray(kcode_words[p], np.uint32).view(np.uint8)
+    if kxcode_words is not None:
+        o = lay["key_xcodes"] + 4 * slot * (w // 2)
+        sb[o: o + 4 * (w // 2)] = np.asarray(kxcode_words, np.uint32).view(np.uint8)
     if key_qjl == 1:
         o = lay["key_signs"] + 4 * slot * w
         sb[o: o + 4 * w] = np.asarray(ksign_words, np.uint32).view(np.uint8)
@@ -94,22 +112,33 @@ def write_page(pool: np.ndarray, lay: dict, n_heads: int, page: int, head: int, 
 
 
 def read_page(pool: np.ndarray, lay: dict, n_heads: int, page: int, head: int,
-              d: int, key_bits: int, key_qjl: bool, value_bits: int) -> dict:
-    """Decode all P records of one (page, head) sub-block back to arrays."""
-    from .codec import planes_to_idx, unpack_bits
+              d: int, key_bits: int, key_qjl: bool, value_bits: int,
+              key_split: int = 0, norm_range: tuple[float, float] | None = None) -> dict:
+    """Decode all P records of one (page, head) sub-block back to arrays.
+    norm_range = (lo, hi): key norms are byte codes (kept as "knorm_code",
+    decoded into "knorm")."""
+    from .codec import norm_u8_decode, planes_to_idx, unpack_bits, unpack_codes_split
 
     base = (page * n_heads + head) * lay["bytes"]
     sb = np.ascontiguousarray(pool[base: base + lay["bytes"]])
     w = d // 32
-    out = {"knorm": sb[lay["key_norm"]: lay["key_norm"] + 4 * PAGE].view(np.float32).copy()}
+    if norm_range is not None:
+        code = sb[lay["key_norm"]: lay["key_norm"] + PAGE].copy()
+        out = {"knorm_code": code, "knorm": norm_u8_decode(code, *norm_range)}
+    else:
+        out = {"knorm": sb[lay["key_norm"]: lay["key_norm"] + 4 * PAGE].view(np.float32).copy()}
     if key_qjl:
         out["krnorm"] = sb[lay["key_rnorm"]: lay["key_rnorm"] + 4 * PAGE].view(np.float32).copy()
     if key_qjl == 1:
         sw = sb[lay["key_signs"]: lay["key_signs"] + 4 * PAGE * w].view(np.uint32).reshape(PAGE, w)
         out["ksigns"] = unpack_bits(sw, d).astype(bool)
     cw = sb[lay["key_codes"]: lay["key_codes"] + 4 * key_bits * PAGE * w].view(np.uint32).reshape(key_bits, PAGE, w)
-    kplanes = np.stack([unpack_bits(cw[p], d) for p in range(key_bits)], axis=1)  # [P, bits, d]
-    out["kidx"] = planes_to_idx(kplanes)
+    if key_split:
+        xw = sb[lay["key_xcodes"]: lay["key_xcodes"] + 4 * PAGE * (w // 2)].view(np.uint32).reshape(PAGE, w // 2)
+        out["kidx"] = unpack_codes_split(cw.transpose(1, 0, 2), xw, key_bits, d)
+    else:
+        kplanes = np.stack([unpack_bits(cw[p], d) for p in range(key_bits)], axis=1)  # [P, bits, d]
+        out["kidx"] = planes_to_idx(kplanes)
     out["vnorm"] = sb[lay["value_norm"]: lay["value_norm"] + 4 * PAGE].view(np.float32).copy()
     vc = sb[lay["value_codes"]: lay["value_codes"] + 2 * value_bits * d].view(np.uint16).reshape(value_bits, d)
     vplanes = ((vc[None, :, :] >> np.arange(PAGE, dtype=np.uint16)[:, None, None]) & 1).astype(np.uint8)
