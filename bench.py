@@ -40,14 +40,25 @@ if ROOT not in sys.path:
 METRIC = "decode-attention compressed-KV GB/s & % HBM roofline; quantize tokens·heads/s"
 
 
+def key_mode(w) -> str:
+    if w.key_split:
+        code = f"{w.key_bits + 0.5}b per channel (coordinates < d/2 at {w.key_bits + 1}b, the rest {w.key_bits}b)"
+    else:
+        code = f"{w.key_bits}b Lloyd-Max"
+    corr = {0: "", 1: " + 1b QJL", 2: " + EDEN scale", 3: " + length renormalization"}[int(w.key_qjl)]
+    total = f"{w.key_bits + 1}b " if int(w.key_qjl) == 1 and not w.key_split else ""
+    norm = f", byte log-norms over [2^{w.key_norm_range[0]:g}, 2^{w.key_norm_range[1]:g}]" if w.key_norm_range else ""
+    return f"keys {total}({code}{corr}{norm})"
+
+
 def workload_name(w) -> str:
     kind = "FWHT" if w.kind == 1 else "dense Pi"
     return (f"{w.name}-like full-attention layer: {w.dtype}, d={w.d}, {w.n_kv_heads} KV / {w.n_q_heads} q heads, "
-            f"batch {w.batch}, {w.ctx} ctx, keys {w.key_bits + 1}b ({w.key_bits}b Lloyd-Max + 1b QJL), "
+            f"batch {w.batch}, {w.ctx} ctx, {key_mode(w)}, "
             f"values {w.value_bits}b, {kind}, page 16, fp16 window {w.window}")
 
 
-DEFAULT_LAYERS = {"qwen": 4, "llama": 4, "long": 8}  # resident layer caches: working set far above L2
+DEFAULT_LAYERS = {"qwen": 4, "llama": 4, "long": 8, "mixed": 4}  # resident layer caches: far above L2
 
 
 def parse():
@@ -56,7 +67,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
-    ap.add_argument("--workload", default="qwen", choices=["qwen", "llama", "long"],
+    ap.add_argument("--workload", default="qwen", choices=["qwen", "llama", "long", "mixed"],
                     help="decode configuration (default: the Qwen-like headline workload)")
     ap.add_argument("--layers", type=int, default=0, help="resident layer caches rotated over (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -66,21 +77,30 @@ def parse():
 
 # ----------------------------------------------------------------------------- helpers
 
-def record_bytes(d, kb, qjl, vb):
-    return 8 + (kb + 1) * d // 8 if qjl else 4 + kb * d // 8, 4 + vb * d // 8
+def record_bytes(d, kb, qjl, vb, split=0, norm_u8=False):
+    """Bytes of one key and one value record: norm (float32 or a byte), the correction's
+    float32 slot, the code planes (half a bit more per channel with the mixed rate), the
+    sign sketch (QJL)."""
+    qjl = int(qjl)
+    key = (1 if norm_u8 else 4) + (4 if qjl else 0) + kb * d // 8 + (d // 16 if split else 0) + (d // 8 if qjl == 1 else 0)
+    return key, 4 + vb * d // 8
 
 
-def decode_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True):
+def workload_records(w):
+    return record_bytes(w.d, w.key_bits, w.key_qjl, w.value_bits, w.key_split, w.key_norm_range is not None)
+
+
+def decode_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True, rec=None):
     """Algorithmic bytes one decode call reads and writes for sequences of length T:
     compressed records, the float16 window K and V, q (bf16) and the output (fp32)."""
-    kr, vr = record_bytes(d, kb, qjl, vb)
+    kr, vr = rec if rec is not None else record_bytes(d, kb, qjl, vb)
     nc = 16 * (max(0, T - W) // 16)
     return B * Hkv * (nc * (kr + vr) + (T - nc) * d * 2 * 2) + B * Hq * d * (2 + 4)
 
 
-def step_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True):
+def step_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True, rec=None):
     """Algorithmic bytes of one step for sequences of length T (after the append)."""
-    kr, vr = record_bytes(d, kb, qjl, vb)
+    kr, vr = rec if rec is not None else record_bytes(d, kb, qjl, vb)
     nc = 16 * (max(0, T - W) // 16)
     nw = T - nc
     per_head = nc * (kr + vr) + nw * d * 2 * 2           # compressed records + fp16 window K,V
@@ -199,22 +219,47 @@ def oracle_sample_setup(name="qwen"):
     T, W, d = w.ctx, w.window, w.d
     nc = 16 * (max(0, T - W) // 16)
     kcb, vcb = OCB.lloyd_max(d, w.key_bits), OCB.lloyd_max(d, w.value_bits)
-    prm = {"kind": w.kind, "k_cb": kcb, "v_cb": vcb, "key_qjl": True,
+    kcb_hi = OCB.lloyd_max(d, w.key_bits + 1) if w.key_split else None
+    corr = int(w.key_qjl)
+    prm = {"kind": w.kind, "k_cb": kcb, "k_cb_hi": kcb_hi, "v_cb": vcb, "key_qjl": corr,
            "k_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 0)], "v_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 1)],
-           "qjl_s": [OT.build_transform(w.kind, d, 0, 0, 0, 2)]}
+           "qjl_s": [OT.build_transform(w.kind, d, 0, 0, 0, 2)] if corr == 1 else None}
     K, V = kv["K"][0, :, 0], kv["V"][0, :, 0]
-    kr = OC.quantize_prod(K[:nc], w.kind, prm["k_rot"][0], kcb, prm["qjl_s"][0])
+    S = {"prm": prm, "kind": w.kind, "k_cb": kcb, "v_cb": vcb, "norm_range": w.key_norm_range}
+    kr = oracle_keys(S, K[:nc])
     vr = OC.quantize_mse(V[:nc], w.kind, prm["v_rot"][0], vcb)
     comp = {"knorm": kr["norm"][None], "krnorm": kr["rnorm"][None], "kidx": kr["idx"][None],
             "ksigns": kr["signs"][None], "vnorm": vr["norm"][None], "vidx": vr["idx"][None]}
     win_k = K[nc:].astype(np.float16)[None]
     win_v = V[nc:].astype(np.float16)[None]
     q = kv["q"][0, :G]
-    kr_b, vr_b = record_bytes(d, w.key_bits, True, w.value_bits)
+    kr_b, vr_b = workload_records(w)
     nbytes = nc * (kr_b + vr_b) + (T - nc) * d * 4 + d * (2 * 2 + 2 * 2) + G * d * 6
-    return {"prm": prm, "comp": comp, "win_k": win_k, "win_v": win_v, "q": q, "d": d, "bytes": nbytes,
-            "new_k": K[-1:], "new_v": V[-1:], "kind": w.kind, "T": T, "nc": nc, "G": G, "W": W,
-            "k_cb": kcb, "v_cb": vcb}
+    S.update({"comp": comp, "win_k": win_k, "win_v": win_v, "q": q, "d": d, "bytes": nbytes,
+              "new_k": K[-1:], "new_v": V[-1:], "T": T, "nc": nc, "G": G, "W": W})
+    return S
+
+
+def oracle_keys(S, K):
+    """The oracle's key records in the workload's key mode, with the norms as stored
+    (byte norms decoded) and neutral sketch fields where the mode has none."""
+    import numpy as np
+
+    from oracle import codec as OC
+
+    prm = S["prm"]
+    corr = prm["key_qjl"]
+    if corr == 1:
+        kr = OC.quantize_prod(K, S["kind"], prm["k_rot"][0], S["k_cb"], prm["qjl_s"][0])
+    elif corr >= 2:
+        kr = OC.quantize_scaled(K, S["kind"], prm["k_rot"][0], S["k_cb"], corr, cb_hi=prm["k_cb_hi"])
+    else:
+        kr = OC.quantize_mse(K, S["kind"], prm["k_rot"][0], S["k_cb"], cb_hi=prm["k_cb_hi"])
+        kr["rnorm"] = np.zeros(K.shape[0], np.float32)
+    kr.setdefault("signs", np.ones(kr["idx"].shape, dtype=bool))
+    if S["norm_range"] is not None:
+        kr["norm"] = OC.norm_u8_decode(OC.norm_u8_encode(kr["norm_f64"], *S["norm_range"])[0], *S["norm_range"])
+    return kr
 
 
 def oracle_step(S):
@@ -233,7 +278,7 @@ def oracle_step(S):
     else:
         # no window: the new token is quantized into its page slot
         prm = S["prm"]
-        kr = OC.quantize_prod(S["new_k"], S["kind"], prm["k_rot"][0], S["k_cb"], prm["qjl_s"][0])
+        kr = oracle_keys(S, S["new_k"])
         vr = OC.quantize_mse(S["new_v"], S["kind"], prm["v_rot"][0], S["v_cb"])
         c = S["comp"]
         comp = {"knorm": np.concatenate([c["knorm"][:, 1:], kr["norm"][None]], axis=1),
@@ -385,6 +430,7 @@ def run_gpu(args):
 
     w = SK.workload(args.workload, seed=1000 * rank)
     B, Hkv, Hq, d, T0, W = w.batch, w.n_kv_heads, w.n_q_heads, w.d, w.ctx, w.window
+    recs = workload_records(w)
     if args.layers <= 0:
         args.layers = DEFAULT_LAYERS[args.workload]
     total_steps = args.warmup + 2 * args.steps
@@ -392,7 +438,8 @@ def run_gpu(args):
     max_ctx = T0 + per_layer + 16
     layers, caches, qs, news = [], [], [], []
     for l in range(args.layers):
-        L = tq.TQLayer(d, Hkv, Hq, w.key_bits, w.value_bits, w.kind, window=W, seed=w.seed, layer=l)
+        L = tq.TQLayer(d, Hkv, Hq, w.key_bits, w.value_bits, w.kind, window=W, key_qjl=w.key_qjl, seed=w.seed,
+                       layer=l, key_split=w.key_split, key_norm_range=w.key_norm_range)
         pc = tq.PagedCache(L, B, max_ctx)
         K, V, q = SK.keys_values_torch(w, layer=l, ctx=T0 + per_layer)
         pc.prefill(K[:, :T0], V[:, :T0])
@@ -425,7 +472,7 @@ def run_gpu(args):
                             work, max_ctx)
         if dec_ev is not None:
             dec_ev[1].record()
-        return step_bytes(T[l], W, B, Hkv, Hq, d, w.key_bits, w.value_bits)
+        return step_bytes(T[l], W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs)
 
     for i in range(args.warmup):
         step(i)
@@ -484,18 +531,20 @@ def run_gpu(args):
     value = total_bytes * ws / (ms * 1e-3) / 1e9
     # roofline of the decode call (prologue + tensor-core split-K kernel + combine),
     # algorithmic bytes of its reads and writes per launch over its measured duration
-    dec_bytes = decode_bytes(T0 + 1 + args.warmup // args.layers, W, B, Hkv, Hq, d, w.key_bits, w.value_bits)
+    dec_bytes = decode_bytes(T0 + 1 + args.warmup // args.layers, W, B, Hkv, Hq, d, w.key_bits, w.value_bits,
+                             rec=recs)
     dec_avg = statistics.mean(dec_ms)
     achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if args.workload == "qwen" else None  # the capture is of the Qwen-like call
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch Philox on the device)",
         "config": {"workload": workload_name(w), "batch": B, "ctx": T0, "kv_heads": Hkv, "q_heads": Hq, "d": d,
-                   "key_bits": w.key_bits + 1, "value_bits": w.value_bits, "window": W, "page": 16,
+                   "key_bits": w.key_bits + (0.5 if w.key_split else (1 if int(w.key_qjl) == 1 else 0)),
+                   "value_bits": w.value_bits, "window": W, "page": 16,
                    "layer_caches": args.layers, "l2": f"inputs larger than L2: {args.layers} rotating layer caches "
-                   f"of {step_bytes(T0, W, B, Hkv, Hq, d, w.key_bits, w.value_bits) / 1e6:.0f} MB",
+                   f"of {step_bytes(T0, W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs) / 1e6:.0f} MB",
                    "parallelism": f"replicas x{ws}"},
         "hbm_fraction": value / ws / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

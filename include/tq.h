@@ -138,6 +138,23 @@ typedef struct {
    * transform).  Codes, signs and the float16 window rows keep d
    * coordinates (the window's tail stays zero). */
   int head_dim;
+  /* Mixed-channel key rate ([Design study] §Packed format and complete bit
+   * accounting: fractional nominal rates by channel allocation, fixed offsets,
+   * no decoder state).  0: every rotated coordinate takes key_bits bits.
+   * 1: coordinates 0 .. d/2-1 take key_bits + 1 bits with the k_hi_* book
+   * (a (key_bits+1)-bit tq_build_codebook), the rest key_bits bits with the
+   * k_* book, e.g. key_bits = 3 for the 3.5 bits-per-channel key mode.
+   * Needs key_bits <= 3 and key_qjl != TQ_KEY_QJL. */
+  int key_split;
+  float k_hi_centroids[16], k_hi_bounds[16];
+  /* Key norms in the pages ([Design study] §Packed format, "u8 log-norm").
+   * 0: float32.  1: one byte per token-head, code 0 for a zero vector, else
+   * code = 1 + clamp(floor(t + 1/2), 0, 254) with
+   * t = (log2 n - key_norm_log2_lo) / step, step = (hi - lo) / 254, decoded
+   * as 2^(lo + (code - 1) step).  lo < hi, both finite; the flat
+   * tq_quantize_keys output keeps float32 norms. */
+  int key_norm_u8;
+  float key_norm_log2_lo, key_norm_log2_hi;
 } tq_layer_params;
 
 /*
@@ -148,7 +165,9 @@ typedef struct {
  * gamma 0, codes of z = 0, all signs +1 ([Reconstruction] §11 item 2, §13).
  *   k           [device] [n_vec][head_dim] in dtype (vector n uses head n % Hkv);
  *               16-byte aligned
- *   code_planes [device] out, uint32 [n_vec][key_bits][d/32]
+ *   code_planes [device] out, uint32 [n_vec][key_bits][d/32]; with key_split,
+ *               uint32 [n_vec][key_bits * d/32 + d/64]: the key_bits planes over
+ *               all coordinates, then the top plane of coordinates 0 .. d/2-1
  *   sign_planes [device] out, uint32 [n_vec][d/32]; NULL unless key_qjl == TQ_KEY_QJL
  *   norms       [device] out, float [n_vec]
  *   rnorms      [device] out, float [n_vec]: gamma (QJL) or the scale s (EDEN, RENORM); NULL iff MSE only
@@ -173,9 +192,10 @@ tq_status tq_quantize_values(const tq_layer_params* p, const void* v, tq_dtype d
  * The paged cache of one layer ([Design study] §Packed format; §Paging,
  * lifecycle).  Page pool: [n_pages][Hkv][sub-block]; the sub-block of one
  * (page, kv head) holds 16 tokens, in this order:
- *   key norms          float [16]
+ *   key norms          float [16]               (uint8 [16] with key_norm_u8)
  *   key residual norms float [16]              (key_qjl != 0: gamma or the scale s)
  *   key code planes    uint32 [key_bits][16][d/32]   token-major
+ *   key top plane      uint32 [16][d/64]       (key_split only: coordinates < d/2)
  *   key sign plane     uint32 [16][d/32]       (key_qjl == TQ_KEY_QJL only)
  *   value norms        float [16]
  *   value code planes  uint16 [value_bits][d]  coordinate-major: bit t of

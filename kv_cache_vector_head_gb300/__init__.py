@@ -36,13 +36,17 @@ class TQLayer:
 
     def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
                  window: int = 0, key_qjl: int = KEY_QJL, seed: int = 0, layer: int = 0, device="cuda",
-                 head_dim: int | None = None):
+                 head_dim: int | None = None, key_split: bool = False,
+                 key_norm_range: tuple[float, float] | None = None):
         """d: the transform and code dimension (128 or 256); head_dim (default d):
         the length of the vectors the caller passes, zero-padded to d inside
         the kernels (a multiple of 8 in (d/2, d]).  key_qjl: the key
         correction, KEY_QJL (TurboQuant_prod, default), KEY_MSE (code only),
         KEY_EDEN (unbiased scale) or KEY_RENORM (length renormalization);
-        True / False stand for KEY_QJL / KEY_MSE."""
+        True / False stand for KEY_QJL / KEY_MSE.  key_split: mixed-channel
+        key rate, rotated coordinates < d/2 at key_bits + 1 bits (key_bits = 3
+        gives 3.5 bits per channel; not with KEY_QJL).  key_norm_range =
+        (lo, hi): key norms stored as one byte, log2-uniform over [2^lo, 2^hi]."""
         import torch
 
         self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
@@ -51,7 +55,9 @@ class TQLayer:
         self.key_qjl, self.seed, self.layer = int(key_qjl), seed, layer
         if self.key_qjl not in (KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM):
             raise ValueError(f"key_qjl must be one of KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM, got {key_qjl}")
+        self.key_split, self.key_norm_range = bool(key_split), key_norm_range
         self.k_cb = build_codebook(d, key_bits)
+        self.k_cb_hi = build_codebook(d, key_bits + 1) if key_split else None
         self.v_cb = build_codebook(d, value_bits)
         kr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_KEY_ROT) for h in range(n_kv_heads)])
         vr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_VALUE_ROT) for h in range(n_kv_heads)])
@@ -73,6 +79,14 @@ class TQLayer:
         for name, (c, t, _) in (("k", self.k_cb), ("v", self.v_cb)):
             getattr(p, f"{name}_centroids")[: len(c)] = [float(x) for x in c]
             getattr(p, f"{name}_bounds")[: len(t)] = [float(x) for x in t]
+        if key_split:
+            c, t, _ = self.k_cb_hi
+            p.key_split = 1
+            p.k_hi_centroids[: len(c)] = [float(x) for x in c]
+            p.k_hi_bounds[: len(t)] = [float(x) for x in t]
+        if key_norm_range is not None:
+            p.key_norm_u8 = 1
+            p.key_norm_log2_lo, p.key_norm_log2_hi = float(key_norm_range[0]), float(key_norm_range[1])
         self.params = p
         self.sub_bytes = subblock_bytes(p)
 

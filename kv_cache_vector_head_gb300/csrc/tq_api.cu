@@ -1,6 +1,7 @@
 // C ABI entry points of libtq: argument checks on the host, then launches.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -52,6 +53,15 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   if (p->kind != TQ_DENSE && p->kind != TQ_FWHT) return fail(TQ_ERR_INVALID_ARG, "bad transform kind");
   if (p->head_dim != 0 && (p->head_dim % 8 != 0 || p->head_dim <= p->d / 2 || p->head_dim > p->d))
     return fail(TQ_ERR_INVALID_ARG, "head_dim must be 0 or a multiple of 8 in (d/2, d]");
+  if (p->key_split != 0 && p->key_split != 1) return fail(TQ_ERR_INVALID_ARG, "key_split must be 0 or 1");
+  if (p->key_split && p->key_bits + 1 > TQ_MAX_BITS)
+    return fail(TQ_ERR_UNSUPPORTED, "key_split needs key_bits <= 3");
+  if (p->key_split && p->key_qjl == TQ_KEY_QJL)
+    return fail(TQ_ERR_UNSUPPORTED, "key_split does not combine with the QJL sketch");
+  if (p->key_norm_u8 != 0 && p->key_norm_u8 != 1) return fail(TQ_ERR_INVALID_ARG, "key_norm_u8 must be 0 or 1");
+  if (p->key_norm_u8 && !(std::isfinite(p->key_norm_log2_lo) && std::isfinite(p->key_norm_log2_hi) &&
+                          p->key_norm_log2_lo < p->key_norm_log2_hi))
+    return fail(TQ_ERR_INVALID_ARG, "key_norm_u8 needs finite key_norm_log2_lo < key_norm_log2_hi");
   if (need_device_ptrs) {
     if (!p->k_rot || !p->v_rot) return fail(TQ_ERR_INVALID_ARG, "null k_rot / v_rot");
     if (p->key_qjl == TQ_KEY_QJL && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
@@ -89,15 +99,27 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   };
   walsh(p->k_centroids, p->key_bits, K->akw);
   walsh(p->v_centroids, p->value_bits, K->avw);
+  K->ksplit = p->key_split;
+  for (int i = 0; i < 16; ++i) {
+    K->kc_hi[i] = p->key_split ? p->k_hi_centroids[i] : p->k_centroids[i];
+    K->kt_hi[i] = p->key_split ? p->k_hi_bounds[i] : p->k_bounds[i];
+  }
+  if (p->key_split) walsh(p->k_hi_centroids, p->key_bits + 1, K->akw_hi);
+  else for (int i = 0; i < 8; ++i) K->akw_hi[i] = K->akw[i];
+  K->knu8 = p->key_norm_u8;
+  K->kn_lo = p->key_norm_u8 ? p->key_norm_log2_lo : 0.f;
+  K->kn_step = p->key_norm_u8 ? (float)(((double)p->key_norm_log2_hi - p->key_norm_log2_lo) / 254.0) : 1.f;
+  K->kn_inv_step = p->key_norm_u8 ? (float)(254.0 / ((double)p->key_norm_log2_hi - p->key_norm_log2_lo)) : 1.f;
   K->xb1 = 0x3C003C00u;
   K->xb2 = 0x40004000u;
-  K->kp = 1 << (p->key_bits - 1);
+  K->kp = 1 << (p->key_bits - 1 + p->key_split);
   K->vp = 1 << (p->value_bits - 1);
   const int d = p->d, w = d / 32, P = TQ_PAGE_SIZE;
   int o = 0;
-  K->off_knorm = o; o += 4 * P;
+  K->off_knorm = o; o += (p->key_norm_u8 ? 1 : 4) * P;
   K->off_krnorm = o; o += p->key_qjl ? 4 * P : 0;
   K->off_kcodes = o; o += 4 * p->key_bits * P * w;
+  K->off_kx = o; o += p->key_split ? 4 * P * (w / 2) : 0;
   K->off_ksigns = o; o += p->key_qjl == TQ_KEY_QJL ? 4 * P * w : 0;
   K->off_vnorm = o; o += 4 * P;
   K->off_vcodes = o; o += 2 * p->value_bits * d;

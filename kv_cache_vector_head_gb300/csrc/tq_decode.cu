@@ -287,8 +287,10 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
         const int ca = 32 * w + i0, cb = ca + 16;
         float va, vb;
         if (pl < P.kp) {
-          va = P.akw[pl] * s.x[v][ca];
-          vb = P.akw[pl] * s.x[v][cb];
+          // mixed-channel keys: coordinates < d/2 (words < d/64) follow the wider book
+          const float a = ca < D / 2 ? P.akw_hi[pl] : P.akw[pl];
+          va = a * s.x[v][ca];
+          vb = a * s.x[v][cb];
         } else {
           va = s.r[v][ca];
           vb = s.r[v][cb];
@@ -635,7 +637,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
           for (int r = 0; r < 4; ++r) accm[x][nt][r] = accq[x][nt][r] = 0.f;
       if (pvalid) {
         const uint32_t* kc = reinterpret_cast<const uint32_t*>(pb + P.off_kcodes);
-        // raw words of token 8 nt + g8, words t4 * WPL + jw
+        const uint32_t* kx = reinterpret_cast<const uint32_t*>(pb + P.off_kx);
+        // raw words of token 8 nt + g8, words t4 * WPL + jw; mixed-channel keys: magnitude plane kb
+        // (the wider codes' top bit) exists for words < E / 2 only and reads 0 elsewhere, where the
+        // query operand of every plane S containing it is 0
         uint32_t rs[2][WPL], rm[3][2][WPL];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -644,7 +649,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             const int tk = 8 * nt + g8, w = t4 * WPL + jw;
             rs[nt][jw] = kc[tk * E + w];
 #pragma unroll
-            for (int m = 0; m < 3; ++m) rm[m][nt][jw] = (m + 1 < P.kb) ? kc[((m + 1) * kPage + tk) * E + w] : 0u;
+            for (int m = 0; m < 3; ++m)
+              rm[m][nt][jw] = (m + 1 < P.kb)                                 ? kc[((m + 1) * kPage + tk) * E + w]
+                              : (P.ksplit && m + 1 == P.kb && w < E / 2) ? kx[tk * (E / 2) + w]
+                                                                           : 0u;
           }
         for (int S = 0; S < P.kp; ++S) {
           uint32_t w0[2][WPL], w6[2][WPL], w10[2][WPL];
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
           }
         }
       }
-      const float* knorm = reinterpret_cast<const float*>(pb + P.off_knorm);
+      const float* knorm = reinterpret_cast<const float*>(pb + P.off_knorm);  // or bytes (knu8)
       const float* krn = reinterpret_cast<const float*>(pb + P.off_krnorm);
       float mx = -INFINITY;
 #pragma unroll
@@ -713,7 +721,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             // QJL: gamma times the sketch term; EDEN / renormalized keys: the scale s on the code's term
             const float gm = P.kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
             const float sk = P.kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
-            l = scale * knorm[t] * (sk * (mse * inv_sqrt_d) + kappa * gm * qj);
+            const float kn = P.knu8 ? norm_u8_decode(pb[P.off_knorm + t], P) : knorm[t];
+            l = scale * kn * (sk * (mse * inv_sqrt_d) + kappa * gm * qj);
             if (scores) scores[(head0 + g8) * (size_t)max_ctx + tok] = l;
           }
           sc[nt][e] = l;

@@ -25,12 +25,32 @@ struct KParams {
   // Walsh-plane coefficients: a code (sign s, magnitude bits m) has centroid
   // s * sum_S a_S * prod_{i in S} (1 - 2 m_i); plane S has bit s ^ parity(m & S).
   float akw[8], avw[8];
+  // mixed-channel key rate: coordinates < d/2 take kb + 1 bits with the kc_hi / kt_hi book
+  // (Walsh coefficients akw_hi); kp counts the planes of the wider code
+  int ksplit;
+  float kc_hi[16], kt_hi[16], akw_hi[8];
+  // byte key norms: code c > 0 decodes to 2^(kn_lo + (c - 1) kn_step)
+  int knu8;
+  float kn_lo, kn_step, kn_inv_step;
   int kp, vp;                          // 2^(bits-1) planes
   uint32_t xb1, xb2;                   // 0x3C003C00 and 0x40004000 (f16 pairs 1.0, 2.0), passed as data so
                                        // that an operand register stays one LOP3 with a register operand
   int sub_bytes;                       // bytes of one (page, head) sub-block
-  int off_knorm, off_krnorm, off_kcodes, off_ksigns, off_vnorm, off_vcodes;
+  int off_knorm, off_krnorm, off_kcodes, off_kx, off_ksigns, off_vnorm, off_vcodes;
 };
+
+// Byte key norm ([Design study] §Packed format, u8 log-norm): 0 for a zero
+// vector, else 1 + round-half-up of (log2 n - lo) / step clamped to 0..254.
+__device__ __forceinline__ uint8_t norm_u8_encode(float n, const KParams& P) {
+  if (n < kZeroNorm) return 0;
+  const float t = (log2f(n) - P.kn_lo) * P.kn_inv_step;
+  const float k = fminf(fmaxf(floorf(t + 0.5f), 0.f), 254.f);
+  return (uint8_t)(1 + (int)k);
+}
+
+__device__ __forceinline__ float norm_u8_decode(unsigned c, const KParams& P) {
+  return c == 0 ? 0.f : exp2f(P.kn_lo + (float)(c - 1) * P.kn_step);
+}
 
 // Cache descriptor as seen by the kernels.
 struct KCache {

@@ -18,6 +18,10 @@
 //      S (z - C[idx]) as a second tile product; signs packed by ballot.  The
 //      scaled corrections keep s instead: EDEN d / sum z C[idx], renormalized
 //      sqrt(d / sum C[idx]^2) (both from the same per-coordinate pass).
+// Mixed-channel keys ([Design study] §Packed format: fractional rates by
+// channel allocation) take coordinates < d/2 one bit wider with their own
+// book; the wider codes' top plane is kept for the first d/64 words only.
+// Byte key norms (u8 log-norm) are encoded when the page slot is written.
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -42,10 +46,13 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
   constexpr int E = D / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bits = is_key ? P.kb : P.vb;
+  const bool split = is_key && P.ksplit;  // coordinates < d/2 one bit wider, own book
   const float sqrt_d = sqrtf((float)D);
   if (tid < 16) {
     s.cb[tid] = is_key ? P.kc[tid] : P.vc[tid];
     s.tb[tid] = is_key ? P.kt[tid] : P.vt[tid];
+    s.cb_hi[tid] = P.kc_hi[tid];
+    s.tb_hi[tid] = P.kt_hi[tid];
   }
   // 1. norms (double accumulation)
   for (int v = warp; v < nv; v += D / 32) {
@@ -70,21 +77,26 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
   rotate_tile<D>(s, nv, P.kind, rot);
   // 3. codes, planes, residual
   const int j = tid;
+  const bool wide = split && j < D / 2;
+  const int bj = bits + (wide ? 1 : 0);         // bits of this coordinate
+  const int nplanes = bits + (split ? 1 : 0);   // planes of the tile (warp-uniform)
+  const float* tbj = wide ? s.tb_hi : s.tb;
+  const float* cbj = wide ? s.cb_hi : s.cb;
   unsigned vm[TQ_MAX_BITS] = {0u, 0u, 0u, 0u};
   for (int v = 0; v < nv; ++v) {
     const float z = s.x[v][j];
-    const int idx = bucketize(z, s.tb, bits);
+    const int idx = bucketize(z, tbj, bj);
 #pragma unroll
     for (int p = 0; p < TQ_MAX_BITS; ++p) {
-      if (p < bits) {
-        const unsigned b = plane_bit(idx, bits, p);
+      if (p < nplanes) {
+        const unsigned b = p < bj ? plane_bit(idx, bj, p) : 0u;  // the top plane: first half only
         const unsigned w = __ballot_sync(0xffffffffu, b);
         if (lane == 0) s.codes[v][p][warp] = w;
         if (slot_of && slot_of[v] >= 0) vm[p] |= b << slot_of[v];
       }
     }
     if (is_key) {
-      const float c = s.cb[idx];
+      const float c = cbj[idx];
       // QJL: residual; EDEN: z c (z and c share a sign, so the terms are >= 0); renormalized: c^2
       s.r[v][j] = P.kqjl == TQ_KEY_EDEN ? z * c : P.kqjl == TQ_KEY_RENORM ? c * c : z - c;
     }
@@ -170,7 +182,8 @@ __global__ void __launch_bounds__(D) quantize_flat_kernel(const __grid_constant_
     __syncthreads();
     quantize_tile<D>(P, s, nv, head, is_key != 0, nullptr);
     // stores: record words are contiguous per vector
-    const int words = bits * E;
+    // mixed-channel keys: the top plane's first d/64 words follow the full planes
+    const int words = bits * E + ((is_key && P.ksplit) ? E / 2 : 0);
     for (int i = threadIdx.x; i < nv * words; i += D) {
       const int v = i / words, k = i % words;
       const long long n = (t0 + v) * P.hkv + head;
@@ -207,12 +220,17 @@ __device__ void store_key_slot(const KParams& P, const TileSmem<D>& s, unsigned 
     const int p = i / E, w = i % E;
     kc[(p * kPage + slot) * E + w] = s.codes[v][p][w];
   }
+  if (P.ksplit) {
+    uint32_t* kx = reinterpret_cast<uint32_t*>(sb + P.off_kx);
+    for (int w = threadIdx.x; w < E / 2; w += D) kx[slot * (E / 2) + w] = s.codes[v][P.kb][w];
+  }
   if (P.kqjl == TQ_KEY_QJL) {
     uint32_t* ks = reinterpret_cast<uint32_t*>(sb + P.off_ksigns);
     for (int w = threadIdx.x; w < E; w += D) ks[slot * E + w] = s.signs[v][w];
   }
   if (threadIdx.x == 0) {
-    reinterpret_cast<float*>(sb + P.off_knorm)[slot] = s.norm[v];
+    if (P.knu8) sb[P.off_knorm + slot] = norm_u8_encode(s.norm[v], P);
+    else reinterpret_cast<float*>(sb + P.off_knorm)[slot] = s.norm[v];
     if (P.kqjl) reinterpret_cast<float*>(sb + P.off_krnorm)[slot] = s.gam[v];
   }
 }
@@ -493,6 +511,7 @@ static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const K
 
 // Tensor-core path: d = 128, bf16, 16-byte aligned input, antisymmetric tables.
 static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key, long long n_vec) {
+  if (is_key && (P.ksplit || P.knu8)) return false;  // mixed-channel keys and byte norms: CUDA-core tiles
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
   return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
 }

@@ -18,6 +18,7 @@ struct TileSmem {
   uint32_t signs[kTile][D / 32];
   uint32_t vmask[TQ_MAX_BITS][D];  // coordinate-major value bits per slot
   float cb[16], tb[16];
+  float cb_hi[16], tb_hi[16];      // mixed-channel keys: the book of coordinates < d/2
 };
 
 // out[v][j] = inv[v] * (R x_v)_j, R = Pi (dense) or H diag(sigma) (FWHT).

@@ -27,6 +27,11 @@ Workloads (the "configs" of the hot-path statement):
   bulk      65536 tokens x 32 layers x 8 KV heads, d = 128, bf16 N(0,1) K and V
             times lognormal(sigma = 1) per (layer, head, channel) scales;
             keys 3b + QJL, values 4b; dense and FWHT.
+  mixed     the qwen shape in the recommended first product mode of the
+            design study: keys 3.5 bits per channel (rotated coordinates
+            < d/2 at 4 bits, the rest at 3), no residual sketch, byte
+            log-norms over [2^0, 2^8] (N(0,1) keys of d = 256 have norms near
+            2^4); values 3b; FWHT; fp16 window 128.
 """
 
 from __future__ import annotations
@@ -65,6 +70,8 @@ class Workload:
     rope: bool = True
     seed: int = 0
     head_dim: int = 0      # length of the generated vectors (0: d); heads shorter than d are zero-padded to d
+    key_split: int = 0     # mixed-channel key rate: the first d/2 rotated coordinates one bit wider
+    key_norm_range: tuple | None = None  # (lo, hi): byte key norms, log2-uniform over [2^lo, 2^hi]
 
     @property
     def dh(self) -> int:
@@ -79,6 +86,8 @@ WORKLOADS = {
     "long": Workload("long", 1, 2, 16, 256, 131072, 2, True, 2, FWHT, 0, "bf16"),
     "bulk": Workload("bulk", 1, 8, 8, 128, 65536, 3, True, 4, DENSE, 0, "bf16", layers=32,
                      key_scale="lognormal", value_scale="lognormal", rope=False),
+    "mixed": Workload("mixed", 8, 4, 24, 256, 32768, 3, 0, 3, FWHT, 128, "bf16", key_split=1,
+                      key_norm_range=(0.0, 8.0)),
 }
 
 

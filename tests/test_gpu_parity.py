@@ -33,9 +33,11 @@ def tq():
 
 def _layer(tq, w, layer=0):
     L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
-                   key_qjl=w.key_qjl, seed=w.seed, layer=layer, head_dim=w.dh)
+                   key_qjl=w.key_qjl, seed=w.seed, layer=layer, head_dim=w.dh, key_split=w.key_split,
+                   key_norm_range=w.key_norm_range)
     O = PY.OracleLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
-                       qjl=w.key_qjl, seed=w.seed, layer=layer)
+                       qjl=w.key_qjl, seed=w.seed, layer=layer, key_split=w.key_split,
+                       key_norm_range=w.key_norm_range)
     return L, O
 
 
@@ -68,6 +70,13 @@ CASES = [
     ("bulk", dict(ctx=90, key_bits=3, key_qjl=2, head_dim=96)),
     ("tiny", dict(ctx=70, key_qjl=3)),
     ("long", dict(ctx=30, key_qjl=2)),
+    # mixed-channel keys (coordinates < d/2 one bit wider) with every correction but the sketch;
+    # byte norms leave the flat output's float norms as they are
+    ("mixed", dict(batch=1, ctx=40)),
+    ("bulk", dict(ctx=300, kind=SK.FWHT, key_bits=3, key_qjl=0, key_split=1, value_bits=3)),
+    ("qwen", dict(batch=1, ctx=40, key_bits=2, key_qjl=2, key_split=1)),
+    ("tiny", dict(ctx=60, key_bits=1, key_qjl=3, key_split=1, key_norm_range=(-4.0, 12.0))),
+    ("bulk", dict(ctx=90, key_bits=3, key_qjl=0, key_split=1, head_dim=96)),
 ]
 
 
@@ -83,7 +92,8 @@ def test_quantize_flat_parity(tq, name, over):
     kt = SK.to_torch(K, dt).cuda()
     vt = SK.to_torch(V, dt).cuda()
     E = w.d // 32
-    codes = torch.zeros(n_vec, w.key_bits * E, dtype=torch.int32, device="cuda")
+    kwords = w.key_bits * E + (E // 2 if w.key_split else 0)
+    codes = torch.zeros(n_vec, kwords, dtype=torch.int32, device="cuda")
     signs = torch.zeros(n_vec, E, dtype=torch.int32, device="cuda") if w.key_qjl == 1 else None
     norms = torch.zeros(n_vec, device="cuda")
     rn = torch.zeros(n_vec, device="cuda") if w.key_qjl else None  # gamma or the key scale
@@ -98,7 +108,7 @@ def test_quantize_flat_parity(tq, name, over):
     for h in range(w.n_kv_heads):
         sel = heads == h
         ok = O.keys(K[:n_vec][sel], h)
-        g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d)
+        g_idx = PY.unpack_flat_codes(codes.cpu().numpy().view(np.uint32)[sel], w.key_bits, w.d, w.key_split)
         g_s = PY.unpack_flat_bits(signs.cpu().numpy().view(np.uint32)[sel], w.d) if w.key_qjl == 1 else None
         g_r = rn.cpu().numpy()[sel] if w.key_qjl else None
         PY.compare_records(ok, g_idx, norms.cpu().numpy()[sel], g_s, g_r, True, stats)
@@ -234,6 +244,15 @@ PAGED = [
     ("qwen", dict(batch=2, window=20, key_qjl=3), 75, 30),
     ("bulk", dict(batch=9, key_qjl=3, key_bits=3), 40, 9),
     ("tiny", dict(key_qjl=2), 37, 12),
+    # the recommended key mode (3.5 bits per channel, byte norms) with a window, and variants
+    ("mixed", dict(batch=2, window=20), 75, 30),
+    ("llama", dict(batch=5, kind=SK.FWHT, key_bits=3, key_qjl=0, value_bits=3, key_split=1,
+                   key_norm_range=(-2.0, 10.0)), 29, 21),
+    ("tiny", dict(key_bits=2, key_qjl=2, key_split=1, key_norm_range=(-4.0, 12.0)), 37, 12),
+    ("bulk", dict(batch=7, key_bits=1, key_qjl=3, key_split=1), 21, 12),
+    # byte norms alone, with the sketch; a narrow range that clamps the outlier keys' norms
+    ("llama", dict(batch=3, key_norm_range=(3.0, 5.0)), 33, 10),
+    ("qwen", dict(batch=1, window=20, key_norm_range=(2.0, 6.0)), 50, 20),
 ]
 
 
@@ -268,10 +287,11 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
             cat = {k: np.concatenate([pg[k] for pg in pages])[:nc] for k in pages[0]} if npg else None
             if nc:
                 PY.compare_records(recs_k[h], cat["kidx"], cat["knorm"], cat.get("ksigns"), cat.get("krnorm"),
-                                   True, stats)
+                                   True, stats, g_norm_code=cat.get("knorm_code"))
                 PY.compare_records(recs_v[h], cat["vidx"], cat["vnorm"], is_key=False, stats=stats)
                 # the reference decode takes the GPU's choice where either is correct
-                recs_k[h] = PY.adopt_exempt(recs_k[h], cat["kidx"], cat.get("ksigns"), cat.get("krnorm"))
+                recs_k[h] = PY.adopt_exempt(recs_k[h], cat["kidx"], cat.get("ksigns"), cat.get("krnorm"),
+                                            cat.get("knorm_code"), w.key_norm_range)
                 recs_v[h] = PY.adopt_exempt(recs_v[h], cat["vidx"])
             if w.window > 0 and T - nc > 0:
                 ring = pc.win_k[b, h].cpu().numpy()

@@ -118,3 +118,33 @@ def test_subblock_layout_matches_oracle(L):
         p.d, p.n_kv_heads, p.n_q_heads, p.page_size = d, 2, 4, 16
         p.key_bits, p.value_bits, p.key_qjl, p.kind = kb, vb, qjl, L.TQ_FWHT
         assert L.subblock_bytes(p) == PG.subblock_layout(d, kb, qjl, vb)["bytes"]
+
+
+def test_mixed_rate_and_byte_norm_layout_and_checks(L):
+    from oracle import paging as PG
+
+    lib = L.lib()
+    for d, kb, qjl, vb, split, u8 in [(128, 3, 0, 3, 1, 1), (256, 3, 2, 3, 1, 1), (128, 2, 3, 2, 1, 0),
+                                      (128, 1, 0, 4, 1, 0), (256, 2, 1, 2, 0, 1), (128, 4, 0, 4, 0, 1)]:
+        p = L.LayerParams()
+        p.d, p.n_kv_heads, p.n_q_heads, p.page_size = d, 2, 4, 16
+        p.key_bits, p.value_bits, p.key_qjl, p.kind = kb, vb, qjl, L.TQ_FWHT
+        p.key_split, p.key_norm_u8, p.key_norm_log2_lo, p.key_norm_log2_hi = split, u8, -4.0, 12.0
+        assert L.subblock_bytes(p) == PG.subblock_layout(d, kb, qjl, vb, key_split=split, key_norm_u8=u8)["bytes"]
+    # the recommended key mode: 3.5 bits per channel + a byte norm = 57 bytes a key at d = 128
+    assert PG.record_bytes(128, 3, 0, 3, key_split=1, key_norm_u8=1) == 57 + 4 + 48
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size = 128, 2, 4, 16
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 4, 2, 0, L.TQ_FWHT
+    p.key_split = 1
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"key_bits <= 3" in lib.tq_last_error()
+    p.key_bits, p.key_qjl = 3, 1
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"QJL" in lib.tq_last_error()
+    p.key_qjl, p.key_split = 0, 2
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.key_split, p.key_norm_u8, p.key_norm_log2_lo, p.key_norm_log2_hi = 1, 1, 3.0, 3.0
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"key_norm_log2_lo" in lib.tq_last_error()
+    p.key_norm_log2_hi = float("inf")
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.key_norm_log2_hi = 9.0
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (57 + 4 + 32)  # values 2 bits
