@@ -73,7 +73,29 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // whose larger register tiles would spill under the three-CTA cap.
 __host__ __device__ constexpr int mma_ctas_per_sm(int d) { return d == 128 ? 3 : 2; }
 
-static int key_frag_planes(const KParams& P) { return P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0); }
+// Query operand of the score products, per (sequence, kv head): units of one k-step
+// (32 lanes x 16 bytes), plane S at units frag_plane_base(S) ..  Mixed-channel keys keep
+// the planes that hold the wider codes' top bit (S >= kp / 2) for the first KS / 2 k-steps
+// only: those cover the coordinates < d/2, the other coordinates' operand would be zero.
+__host__ __device__ inline int frag_plane_base(const KParams& P, int S, int KS) {
+  const int h = P.kp / 2;
+  return (!P.ksplit || S < h) ? S * KS : h * KS + (S - h) * (KS / 2);
+}
+// Coordinate ca of A-fragment entry (k-step kk, lane t4, register r) and the bit ib of the B
+// side's word it meets (ca + 16 meets bit ib + 16).  Lane t4 reads word t4 + 4 (kk / 8), bits
+// 2 (kk mod 8) + (r >= 2): at d = 256 the first KS / 2 k-steps are the coordinates < d/2.  At
+// d = 128 the planes of the wider codes' top bit (mixed-channel keys) cover words 0 and 1 in
+// KS / 2 k-steps instead: lane t4 reads word t4 & 1 shifted right by 8 (t4 >> 1).
+template <int D>
+__host__ __device__ inline void frag_entry(bool half_plane, int kk, int t4, int r, int& ca, int& ib) {
+  ib = 2 * (kk % 8) + (r >= 2 ? 1 : 0);
+  if (D == 128 && half_plane) ca = 32 * (t4 & 1) + 8 * (t4 >> 1) + ib;
+  else ca = 32 * (t4 + 4 * (kk / 8)) + ib;
+}
+static int key_frag_units(const KParams& P) {
+  const int KS = P.d / 16;
+  return P.ksplit ? frag_plane_base(P, P.kp, KS) : (P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0)) * KS;
+}
 
 WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits, int num_sms) {
   WsLayout L{};
@@ -95,7 +117,7 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
   L.pages_per_split = pps;
   const size_t heads = (size_t)batch * P.hq;
   const int st = S + 1;
-  L.afrag_bytes_per_head = (size_t)key_frag_planes(P) * (P.d / 16) * 32 * 16;
+  L.afrag_bytes_per_head = (size_t)key_frag_units(P) * 32 * 16;
   size_t o = 0;
   L.afrag = o; o = align256(o + (size_t)batch * P.hkv * L.afrag_bytes_per_head);
   L.ml = o;    o = align256(o + heads * st * 2 * sizeof(float));
@@ -217,12 +239,13 @@ __device__ __forceinline__ void warp_fwht(float (&a)[E], int lane) {
 // of the score products, in mma.m16n8k16 A-fragment order:
 //   frag[plane][kk][lane] = 4 x f16x2, rows h_local (hi limb) and h_local + 8
 //   (lo limb), k-pair (2t, 2t+1) <-> bits (i0, i0+16) and (2t+8, 2t+9) <->
-//   (i0+1, i0+17) of plane word w = t * (d/128) + kk / 8, i0 = 2 (kk mod 8),
-//   t = lane mod 4.  Rows of absent heads (h_local >= G) are zero.
+//   (i0+1, i0+17) of plane word w = t + 4 (kk / 8), i0 = 2 (kk mod 8),
+//   t = lane mod 4 (see frag_entry for the mixed-channel planes at d = 128).
+//   Rows of absent heads (h_local >= G) are zero.
 template <int D>
 __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constant__ KParams P, const void* q,
                                                             int dtype, unsigned char* ws, WsLayout L, int batch) {
-  constexpr int KS = D / 16, WPL = D / 128;
+  constexpr int KS = D / 16;
   constexpr int TPR = D / 64;  // threads per row of S: each CTA owns 64 rows (coordinates 64 z .. 64 z + 63)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
@@ -265,11 +288,12 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
     }
   }
   __syncthreads();
-  // fragment entries of this CTA: lanes t4 with (t4 * WPL + kk / 8) / 2 == z,
-  // i.e. t4 = z (d = 256) or t4 in {2z, 2z + 1} (d = 128)
-  constexpr int NT4 = 4 / (D / 64);
+  // fragment entries whose coordinate lies in this CTA's rows 64 z .. 64 z + 63 (the rows of S q'
+  // it computed): words 2z and 2z + 1, i.e. k-steps 8 (z / 2) .. 8 (z / 2) + 7 of lanes
+  // t4 = 2 (z mod 2) + {0, 1}, 64 entries a plane; the top-bit planes of mixed-channel keys only
+  // where they are stored (coordinates < d/2)
   const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
-  const int per_row = nplanes * KS * NT4 * 4;
+  const int per_row = nplanes * 64;
   for (int v = 0; v < nv; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
     uint32_t* frag = reinterpret_cast<uint32_t*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
@@ -277,17 +301,27 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
     const int nrow = (hl == 0) ? (8 - G + 1) : 1;
     for (int idx = j; idx < per_row * nrow; idx += D) {
       const int rowsel = idx / per_row, e = idx - rowsel * per_row;
-      const int r = e & 3, ti = (e >> 2) % NT4, kk = ((e >> 2) / NT4) % KS, pl = ((e >> 2) / NT4) / KS;
-      const int t4 = z * NT4 + ti;
+      const int r = e & 3, pl = e >> 6, qe = e & 63;
+      const bool half_plane = P.ksplit && pl >= P.kp / 2;
+      int kk, t4;
+      if (D == 128 && half_plane) {  // words 0 and 1 across all four lanes, 4 k-steps
+        if (z != 0) continue;
+        kk = qe >> 4;
+        t4 = (qe >> 2) & 3;
+      } else {
+        if (half_plane && z >= 2) continue;  // d = 256: not stored beyond the first half
+        kk = 8 * (z >> 1) + (qe >> 3);
+        t4 = 2 * (z & 1) + ((qe >> 2) & 1);
+      }
+      int ca, ib;
+      frag_entry<D>(half_plane, kk, t4, r, ca, ib);
       const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
       uint32_t val = 0;
       if (rowsel == 0) {
-        const int w = t4 * WPL + kk / 8;
-        const int i0 = 2 * (kk % 8) + ((r >= 2) ? 1 : 0);
-        const int ca = 32 * w + i0, cb = ca + 16;
+        const int cb = ca + 16;
         float va, vb;
         if (pl < P.kp) {
-          // mixed-channel keys: coordinates < d/2 (words < d/64) follow the wider book
+          // mixed-channel keys: coordinates < d/2 follow the wider book
           const float a = ca < D / 2 ? P.akw_hi[pl] : P.akw[pl];
           va = a * s.x[v][ca];
           vb = a * s.x[v][cb];
@@ -295,7 +329,7 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
           va = s.r[v][ca];
           vb = s.r[v][cb];
         }
-        const float rd = 1.0f / xdelta(xpos_key(i0));  // the B side reads bit i0 as base + b delta
+        const float rd = 1.0f / xdelta(xpos_key(ib));  // the B side reads bit ib as base + b delta
         va *= rd;
         vb *= rd;
         __half ha, la, hb, lb;
@@ -303,7 +337,7 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
         split_f16(vb, hb, lb);
         val = (r & 1) ? pack_h2(la, lb) : pack_h2(ha, hb);
       }
-      frag[((pl * KS + kk) * 32 + g8 * 4 + t4) * 4 + r] = val;
+      frag[((frag_plane_base(P, pl, KS) + kk) * 32 + g8 * 4 + t4) * 4 + r] = val;
     }
   }
 }
@@ -463,7 +497,8 @@ struct MmaShared {
   uint32_t vlut[16];  // values with b >= 3: raw sign-magnitude bits -> (hi, lo) f16 of the centroid
 };
 
-template <int D, bool VLUT>
+// KMIX: the layer uses mixed-channel keys or byte key norms (compiled out otherwise).
+template <int D, bool VLUT, bool KMIX>
 __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ KCache C, const void* q,
                                                                  int dtype, float scale, float* scores,
@@ -488,6 +523,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   const float kappa = sqrtf(1.57079632679489662f) / (float)D;
   const int sub = P.sub_bytes;
   const uint32_t xb1 = P.xb1, xb2 = P.xb2;
+  const bool ksplit = KMIX && P.ksplit, knu8 = KMIX && P.knu8;
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -574,13 +610,14 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   }
   __syncthreads();
   if (warp < G) {
-    // K of head `warp`: its A-fragment rows (lanes 4 warp .. 4 warp + 3) over all planes and k-blocks;
-    // register r of block kk pairs with key bit 2 (kk mod 8) + (r >= 2)
+    // K of head `warp`: its A-fragment rows (lanes 4 warp .. 4 warp + 3) over all stored planes and
+    // k-blocks; register r of block kk pairs with key bit 2 (kk mod 8) + (r >= 2)
     const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
     float km = 0.f, kq = 0.f;
     for (int it = lane; it < nplanes * KS * 4; it += 32) {
       const int pl = it / (KS * 4), kk = (it / 4) % KS, t4i = it % 4;
-      const uint4 a = afr[(pl * KS + kk) * 32 + warp * 4 + t4i];
+      if (ksplit && pl >= P.kp / 2 && kk >= KS / 2) continue;  // not stored: zero operand
+      const uint4 a = afr[(frag_plane_base(P, pl, KS) + kk) * 32 + warp * 4 + t4i];
       const uint32_t rr[4] = {a.x, a.y, a.z, a.w};
       float sum = 0.f;
 #pragma unroll
@@ -638,23 +675,24 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       if (pvalid) {
         const uint32_t* kc = reinterpret_cast<const uint32_t*>(pb + P.off_kcodes);
         const uint32_t* kx = reinterpret_cast<const uint32_t*>(pb + P.off_kx);
-        // raw words of token 8 nt + g8, words t4 * WPL + jw; mixed-channel keys: magnitude plane kb
-        // (the wider codes' top bit) exists for words < E / 2 only and reads 0 elsewhere, where the
-        // query operand of every plane S containing it is 0
+        // raw words of token 8 nt + g8: word t4 + 4 jw (jw = kk / 8); mixed-channel keys: magnitude
+        // plane kb (the wider codes' top bit) exists for words < E / 2 only
         uint32_t rs[2][WPL], rm[3][2][WPL];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int jw = 0; jw < WPL; ++jw) {
-            const int tk = 8 * nt + g8, w = t4 * WPL + jw;
+            const int tk = 8 * nt + g8, w = t4 + 4 * jw;
             rs[nt][jw] = kc[tk * E + w];
 #pragma unroll
             for (int m = 0; m < 3; ++m)
               rm[m][nt][jw] = (m + 1 < P.kb)                                 ? kc[((m + 1) * kPage + tk) * E + w]
-                              : (P.ksplit && m + 1 == P.kb && w < E / 2) ? kx[tk * (E / 2) + w]
+                              : (ksplit && m + 1 == P.kb && w < E / 2) ? kx[tk * (E / 2) + w]
                                                                            : 0u;
           }
-        for (int S = 0; S < P.kp; ++S) {
+        // planes over all k-steps; mixed-channel keys: the planes holding the top bit follow
+        const int s_full = ksplit ? P.kp / 2 : P.kp;
+        for (int S = 0; S < s_full; ++S) {
           uint32_t w0[2][WPL], w6[2][WPL], w10[2][WPL];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
@@ -665,7 +703,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
               w6[nt][jw] = w0[nt][jw] << 6;
               w10[nt][jw] = w0[nt][jw] << 10;
             }
-          const uint4* ap = afr + (size_t)S * KS * 32 + lane;
+          const uint4* ap = afr + (size_t)frag_plane_base(P, S, KS) * 32 + lane;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const uint4 a = ap[kk * 32];
@@ -676,6 +714,44 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
                        xreg_key(w0[nt][jw], w6[nt][jw], w10[nt][jw], i0 + 1, xb1, xb2));
           }
         }
+        if (ksplit) {
+          // the planes with the top bit over the coordinates < d/2 only (KS / 2 k-steps)
+          uint32_t hs[2], hm[3][2];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            if (D == 256) {  // words t4 < E / 2: the jw = 0 words already loaded
+              hs[nt] = rs[nt][0];
+#pragma unroll
+              for (int m = 0; m < 3; ++m) hm[m][nt] = rm[m][nt][0];
+            } else {  // d = 128: word t4 & 1 shifted right by 8 (t4 >> 1)
+              const int tk = 8 * nt + g8, w = t4 & 1, sh = 8 * (t4 >> 1);
+              hs[nt] = kc[tk * E + w] >> sh;
+#pragma unroll
+              for (int m = 0; m < 3; ++m)
+                hm[m][nt] = ((m + 1 < P.kb) ? kc[((m + 1) * kPage + tk) * E + w]
+                                            : (m + 1 == P.kb) ? kx[tk * (E / 2) + w] : 0u) >> sh;
+            }
+          }
+          for (int S = P.kp / 2; S < P.kp; ++S) {
+            uint32_t w0[2], w6[2], w10[2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              w0[nt] = hs[nt] ^ ((S & 1) ? hm[0][nt] : 0u) ^ ((S & 2) ? hm[1][nt] : 0u) ^ ((S & 4) ? hm[2][nt] : 0u);
+              w6[nt] = w0[nt] << 6;
+              w10[nt] = w0[nt] << 10;
+            }
+            const uint4* ap = afr + (size_t)frag_plane_base(P, S, KS) * 32 + lane;
+#pragma unroll
+            for (int kk = 0; kk < KS / 2; ++kk) {
+              const uint4 a = ap[kk * 32];
+              const int i0 = 2 * (kk % 8);
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+                mma16816(accm[kk & 1][nt], a, xreg_key(w0[nt], w6[nt], w10[nt], i0, xb1, xb2),
+                         xreg_key(w0[nt], w6[nt], w10[nt], i0 + 1, xb1, xb2));
+            }
+          }
+        }
         if (P.kqjl == TQ_KEY_QJL) {
           const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
           uint32_t q0[2][WPL], q6[2][WPL], q10[2][WPL];
@@ -683,7 +759,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int jw = 0; jw < WPL; ++jw) {
-              q0[nt][jw] = ks[(8 * nt + g8) * E + t4 * WPL + jw];
+              q0[nt][jw] = ks[(8 * nt + g8) * E + t4 + 4 * jw];
               q6[nt][jw] = q0[nt][jw] << 6;
               q10[nt][jw] = q0[nt][jw] << 10;
             }
@@ -721,7 +797,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             // QJL: gamma times the sketch term; EDEN / renormalized keys: the scale s on the code's term
             const float gm = P.kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
             const float sk = P.kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
-            const float kn = P.knu8 ? norm_u8_decode(pb[P.off_knorm + t], P) : knorm[t];
+            const float kn = knu8 ? norm_u8_decode(pb[P.off_knorm + t], P) : knorm[t];
             l = scale * kn * (sk * (mse * inv_sqrt_d) + kappa * gm * qj);
             if (scores) scores[(head0 + g8) * (size_t)max_ctx + tok] = l;
           }
@@ -1009,7 +1085,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
 
 // ------------------------------------------------------------------ launcher
 
-template <int D, bool VLUT>
+template <int D, bool VLUT, bool KMIX>
 static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, int dtype, float scale,
                               float* scores, unsigned char* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
   const size_t pid_bytes = (size_t)std::min(L.pages_per_split, kPidCache) * sizeof(long long);
@@ -1021,7 +1097,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
     dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
   }
   dyn = std::max(dyn, window_smem_bytes(D));
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT, KMIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dyn);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the grid may start while the prologue runs
@@ -1036,7 +1112,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, VLUT>, P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, VLUT, KMIX>, P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1052,8 +1128,13 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   const dim3 gp(P.hkv, (C.batch * P.G + kPrologueTile - 1) / kPrologueTile, D / 64);
   decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, C.batch);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = P.vb >= 3 ? launch_mma<D, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
-                : launch_mma<D, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
+  const bool kmix = P.ksplit || P.knu8;
+  if (P.vb >= 3)
+    e = kmix ? launch_mma<D, true, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+             : launch_mma<D, true, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
+  else
+    e = kmix ? launch_mma<D, false, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+             : launch_mma<D, false, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
   if (e != cudaSuccess) return e;
   const size_t cdyn = (size_t)(L.n_comp_splits + 1) * sizeof(float);
   if (cdyn > 48 * 1024) {
