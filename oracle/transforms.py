@@ -11,10 +11,20 @@
   Sylvester-ordered Walsh-Hadamard matrix H_ij = (-1)^popcount(i & j).
 * QJL matrix S ([Reconstruction] §6 "The 1-Bit QJL Transform": i.i.d. standard
   normal entries), d x d (m = d rows; reading of the lost row count, matching
-  the sqrt(pi/2)/d constant of the estimator), row-major, float32.  S stays
-  Gaussian in the structured mode too: unbiasedness is stated for Gaussian S.
+  the sqrt(pi/2)/d constant of the estimator), row-major, float32.
+* Structured QJL matrix (next-row option; [Design study] §Candidate key and
+  value algorithms, the structured key arm with an optional residual QJL
+  stage, "another transform-domain residual stage" costing p log p): the
+  subsampled-randomised-Hadamard form with all d rows kept,
+  S = H diag(sigma_S), entries +-1, rows orthogonal with squared norm d like
+  the expected squared norm of a Gaussian row.  Reading: the estimator keeps
+  its Gaussian constant sqrt(pi/2)/d; for a residual spread over the
+  coordinates (the rotated basis) the Rademacher sums <s_i, r> are close to
+  Gaussian, so the estimate is close to unbiased, not exactly unbiased (a
+  residual on one coordinate is over-estimated by sqrt(pi/2), pinned).
 
-Roles: 0 = key rotation, 1 = value rotation, 2 = QJL matrix S.
+Roles: 0 = key rotation, 1 = value rotation, 2 = QJL matrix S, 3 = the signs
+sigma_S of the structured QJL matrix.
 Stored forms are float32: Pi as d*d row-major, sigma as d values of +-1.
 """
 
@@ -30,6 +40,7 @@ FWHT = 1
 ROLE_KEY_ROT = 0
 ROLE_VALUE_ROT = 1
 ROLE_QJL = 2
+ROLE_QJL_SIGNS = 3
 
 
 def gaussian_matrix(d: int, seed: int, layer: int, head: int, role: int) -> np.ndarray:
@@ -68,6 +79,8 @@ def build_transform(kind: int, d: int, seed: int, layer: int, head: int, role: i
     """The stored float32 array for (kind, role): d*d matrix or d signs."""
     if role == ROLE_QJL:
         return gaussian_matrix(d, seed, layer, head, role).astype(np.float32)
+    if role == ROLE_QJL_SIGNS:
+        return rademacher_signs(d, seed, layer, head, role).astype(np.float32)
     if kind == DENSE:
         return haar_rotation_f64(d, seed, layer, head, role).astype(np.float32)
     if kind == FWHT:
@@ -93,3 +106,9 @@ def rotate_inverse(kind: int, stored: np.ndarray, y: np.ndarray) -> np.ndarray:
     """x = Pi^T y for the rows of y ([..., d]) in float64."""
     d = y.shape[-1]
     return np.asarray(y, dtype=np.float64) @ rotation_matrix(kind, stored, d)
+
+
+def structured_qjl_matrix(stored_signs: np.ndarray, d: int) -> np.ndarray:
+    """S = H diag(sigma_S) (float64, entries +-1) from the stored d signs."""
+    sigma = np.asarray(stored_signs, dtype=np.float64).reshape(d)
+    return walsh_hadamard(d) * sigma[None, :]

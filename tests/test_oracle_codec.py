@@ -234,3 +234,34 @@ def test_one_bit_eden_has_275x_lower_variance_than_qjl():
     assert abs(eden.var() * d / (math.pi / 2 - 1) - 1) < 0.08
     assert abs(qjl.var() * d / (math.pi / 2) - 1) < 0.08
     assert 2.45 < qjl.var() / eden.var() < 3.05
+
+
+def test_structured_sketch_estimator():
+    """S = H diag(sigma_S): a residual on one coordinate e_k gives the closed form sqrt(pi/2) q_k
+    (sign(S e_k) is column k of S and S^T S = d I); for spread (Gaussian) residuals the estimate is
+    unbiased -- Sr / sqrt(d) is then an orthonormal transform of a Gaussian vector -- and with
+    orthogonal rows its distortion stays below the dense Gaussian sketch's."""
+    d = 128
+    rng = np.random.default_rng(5)
+    sig = T.build_transform(T.FWHT, d, 1, 0, 0, T.ROLE_QJL_SIGNS)
+    S = T.structured_qjl_matrix(sig, d)
+    q = rng.standard_normal(d)
+    for k in (0, 7, 100):
+        e = np.zeros(d)
+        e[k] = 1.0
+        est = C.qjl_estimate(q, 1.0, (S @ e) >= 0, S)
+        assert abs(est - math.sqrt(math.pi / 2) * q[k]) < 1e-12
+    n = 20000
+    r = rng.standard_normal((n, d))
+    qq = r + 2.0 * rng.standard_normal((n, d))
+    true = np.sum(qq * r, axis=1)
+    dist = {}
+    for name, M in (("srht", S), ("gauss", T.build_transform(T.FWHT, d, 1, 0, 0, T.ROLE_QJL).astype(np.float64))):
+        signs = (r @ M.T) >= 0
+        est = C.qjl_constant(d) * np.linalg.norm(r, axis=1) * np.sum((qq @ M.T) * np.where(signs, 1.0, -1.0), axis=1)
+        slope = np.sum(est * true) / np.sum(true * true)
+        err = (est - true) ** 2 / (np.sum(qq * qq, axis=1) * np.sum(r * r, axis=1))
+        dist[name] = d * err.mean()
+        se = math.sqrt(np.mean((est - slope * true) ** 2) / np.sum(true * true))
+        assert abs(slope - 1.0) < 5 * se + 1e-3, (name, slope, se)
+    assert dist["srht"] < dist["gauss"]

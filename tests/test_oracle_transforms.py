@@ -105,3 +105,18 @@ def test_seed_determinism_and_streams():
     S = T.build_transform(T.FWHT, 64, 7, 3, 1, T.ROLE_QJL)
     assert S.shape == (64, 64) and S.dtype == np.float32
     assert abs(S.astype(np.float64).var() - 1) < 0.1
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_structured_qjl_matrix(d):
+    """S = H diag(sigma_S): entries +-1 and S S^T = d I exactly; the signs come from their own stream."""
+    sig = T.build_transform(T.FWHT, d, 3, 2, 1, T.ROLE_QJL_SIGNS)
+    assert sig.shape == (d,) and set(np.unique(sig)) <= {-1.0, 1.0}
+    assert not np.array_equal(sig, T.build_transform(T.FWHT, d, 3, 2, 1, T.ROLE_KEY_ROT))
+    assert np.array_equal(sig, T.build_transform(T.DENSE, d, 3, 2, 1, T.ROLE_QJL_SIGNS))
+    S = T.structured_qjl_matrix(sig, d)
+    assert np.array_equal(np.abs(S), np.ones((d, d)))
+    assert np.array_equal(S @ S.T, d * np.eye(d))
+    # column j is sigma_j times column j of the Sylvester matrix
+    H = T.walsh_hadamard(d)
+    assert np.array_equal(S[:, 5], sig[5] * H[:, 5])
