@@ -55,7 +55,7 @@ typedef enum {
 
 typedef enum { TQ_DENSE = 0, TQ_FWHT = 1 } tq_transform_kind;
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
-typedef enum { TQ_ROLE_KEY_ROT = 0, TQ_ROLE_VALUE_ROT = 1, TQ_ROLE_QJL = 2 } tq_role;
+typedef enum { TQ_ROLE_KEY_ROT = 0, TQ_ROLE_VALUE_ROT = 1, TQ_ROLE_QJL = 2, TQ_ROLE_QJL_SIGNS = 3 } tq_role;
 
 /* Device error word bits (tq_check_device_error). */
 #define TQ_DEVERR_PAGE_INDEX 0x1u   /* block-table entry outside [0, n_pages) */
@@ -94,6 +94,8 @@ tq_status tq_build_codebook(int d, int bits, float* centroids, float* boundaries
  *   kind=TQ_FWHT,  role 0/1: out = float[d] Rademacher signs sigma; the
  *                            rotation is Pi u = H (sigma * u) / sqrt(d).
  *   role 2 (either kind):    out = float[d*d] row-major QJL matrix S.
+ *   role 3 (either kind):    out = float[d] Rademacher signs sigma_S of the
+ *                            structured QJL matrix S = H diag(sigma_S).
  *   out [host]. d must be a power of two for TQ_FWHT; 2 <= d <= 4096.
  */
 tq_status tq_build_transform(tq_transform_kind kind, int d, uint64_t seed, int layer, int head,
@@ -126,7 +128,8 @@ typedef struct {
   tq_transform_kind kind;
   const float* k_rot;  /* [device] [Hkv][d*d] (dense) or [Hkv][d] signs (FWHT) */
   const float* v_rot;  /* [device] same shape as k_rot                        */
-  const float* qjl_s;  /* [device] [Hkv][d*d] QJL matrices; NULL if !key_qjl  */
+  const float* qjl_s;  /* [device] [Hkv][d*d] QJL matrices ([Hkv][d] signs with qjl_structured);
+                          NULL unless key_qjl == TQ_KEY_QJL */
   float k_centroids[16], k_bounds[16];
   float v_centroids[16], v_bounds[16];
   /* Length of the key, value, query and output vectors the caller passes;
@@ -155,6 +158,14 @@ typedef struct {
    * tq_quantize_keys output keeps float32 norms. */
   int key_norm_u8;
   float key_norm_log2_lo, key_norm_log2_hi;
+  /* Structured QJL matrix ([Design study] §Candidate key and value
+   * algorithms: the structured key arm with a residual QJL stage done in the
+   * transform domain).  0: qjl_s holds [Hkv][d*d] i.i.d. N(0,1) matrices.
+   * 1: qjl_s holds [Hkv][d] signs sigma_S (tq_build_transform role 3) and
+   * S = H diag(sigma_S), H the unnormalised Sylvester Walsh-Hadamard matrix
+   * (entries +-1, S S^T = d I); S r and S q' are computed with the fast
+   * transform, the estimator keeps sqrt(pi/2)/d.  Needs key_qjl == TQ_KEY_QJL. */
+  int qjl_structured;
 } tq_layer_params;
 
 /*

@@ -14,7 +14,7 @@ import math
 import numpy as np
 
 from . import _lib
-from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
+from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_QJL_SIGNS, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
                    Cache, LayerParams, TQError, append_page, build_codebook, build_transform, check_device_error,
                    decode_attention, decode_workspace_size, quantize_keys, quantize_values, subblock_bytes)
 
@@ -22,7 +22,7 @@ __all__ = [
     "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
     "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
     "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
-    "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
+    "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "ROLE_QJL_SIGNS", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
 ]
 
 
@@ -37,7 +37,7 @@ class TQLayer:
     def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
                  window: int = 0, key_qjl: int = KEY_QJL, seed: int = 0, layer: int = 0, device="cuda",
                  head_dim: int | None = None, key_split: bool = False,
-                 key_norm_range: tuple[float, float] | None = None):
+                 key_norm_range: tuple[float, float] | None = None, qjl_structured: bool = False):
         """d: the transform and code dimension (128 or 256); head_dim (default d):
         the length of the vectors the caller passes, zero-padded to d inside
         the kernels (a multiple of 8 in (d/2, d]).  key_qjl: the key
@@ -46,7 +46,9 @@ class TQLayer:
         True / False stand for KEY_QJL / KEY_MSE.  key_split: mixed-channel
         key rate, rotated coordinates < d/2 at key_bits + 1 bits (key_bits = 3
         gives 3.5 bits per channel; not with KEY_QJL).  key_norm_range =
-        (lo, hi): key norms stored as one byte, log2-uniform over [2^lo, 2^hi]."""
+        (lo, hi): key norms stored as one byte, log2-uniform over [2^lo, 2^hi].
+        qjl_structured (with KEY_QJL): the sketch matrix is S = H diag(sigma_S),
+        applied as a fast Walsh-Hadamard transform, instead of a dense Gaussian."""
         import torch
 
         self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
@@ -64,8 +66,10 @@ class TQLayer:
         self.k_rot_host, self.v_rot_host = kr, vr
         self.k_rot = torch.from_numpy(kr).to(device)
         self.v_rot = torch.from_numpy(vr).to(device)
+        self.qjl_structured = bool(qjl_structured)
         if self.key_qjl == KEY_QJL:
-            s = np.stack([build_transform(kind, d, seed, layer, h, ROLE_QJL) for h in range(n_kv_heads)])
+            role = ROLE_QJL_SIGNS if qjl_structured else ROLE_QJL
+            s = np.stack([build_transform(kind, d, seed, layer, h, role) for h in range(n_kv_heads)])
             self.qjl_s_host = s
             self.qjl_s = torch.from_numpy(s).to(device)
         else:
@@ -84,6 +88,7 @@ class TQLayer:
             p.key_split = 1
             p.k_hi_centroids[: len(c)] = [float(x) for x in c]
             p.k_hi_bounds[: len(t)] = [float(x) for x in t]
+        p.qjl_structured = int(self.qjl_structured)
         if key_norm_range is not None:
             p.key_norm_u8 = 1
             p.key_norm_log2_lo, p.key_norm_log2_hi = float(key_norm_range[0]), float(key_norm_range[1])

@@ -19,7 +19,7 @@ TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_NO_CONVERGENC
     TQ_ERR_DEVICE_CHECK = range(7)
 TQ_DENSE, TQ_FWHT = 0, 1
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
-ROLE_KEY_ROT, ROLE_VALUE_ROT, ROLE_QJL = 0, 1, 2
+ROLE_KEY_ROT, ROLE_VALUE_ROT, ROLE_QJL, ROLE_QJL_SIGNS = 0, 1, 2, 3
 KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM = 0, 1, 2, 3  # tq_key_correction
 PAGE_SIZE = 16
 
@@ -47,6 +47,7 @@ class LayerParams(ctypes.Structure):
         ("head_dim", c_int),
         ("key_split", c_int), ("k_hi_centroids", c_float * 16), ("k_hi_bounds", c_float * 16),
         ("key_norm_u8", c_int), ("key_norm_log2_lo", c_float), ("key_norm_log2_hi", c_float),
+        ("qjl_structured", c_int),
     ]
 
 
@@ -127,7 +128,7 @@ def build_codebook(d: int, bits: int):
 
 
 def build_transform(kind: int, d: int, seed: int, layer: int, head: int, role: int) -> np.ndarray:
-    n = d if (kind == TQ_FWHT and role != ROLE_QJL) else d * d
+    n = d if ((kind == TQ_FWHT and role != ROLE_QJL) or role == ROLE_QJL_SIGNS) else d * d
     out = np.zeros(n, dtype=np.float32)
     _check(lib().tq_build_transform(kind, d, seed, layer, head, role, out.ctypes.data_as(POINTER(c_float))))
     return out

@@ -59,6 +59,10 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   if (p->key_split && p->key_qjl == TQ_KEY_QJL)
     return fail(TQ_ERR_UNSUPPORTED, "key_split does not combine with the QJL sketch");
   if (p->key_norm_u8 != 0 && p->key_norm_u8 != 1) return fail(TQ_ERR_INVALID_ARG, "key_norm_u8 must be 0 or 1");
+  if (p->qjl_structured != 0 && p->qjl_structured != 1)
+    return fail(TQ_ERR_INVALID_ARG, "qjl_structured must be 0 or 1");
+  if (p->qjl_structured && p->key_qjl != TQ_KEY_QJL)
+    return fail(TQ_ERR_INVALID_ARG, "qjl_structured needs key_qjl == TQ_KEY_QJL");
   if (p->key_norm_u8 && !(std::isfinite(p->key_norm_log2_lo) && std::isfinite(p->key_norm_log2_hi) &&
                           p->key_norm_log2_lo < p->key_norm_log2_hi))
     return fail(TQ_ERR_INVALID_ARG, "key_norm_u8 needs finite key_norm_log2_lo < key_norm_log2_hi");
@@ -81,6 +85,7 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   K->k_rot = p->k_rot;
   K->v_rot = p->v_rot;
   K->qjl_s = p->qjl_s;
+  K->qjl_srht = p->qjl_structured;
   for (int i = 0; i < 16; ++i) {
     K->kc[i] = p->k_centroids[i];
     K->kt[i] = p->k_bounds[i];

@@ -206,31 +206,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// In-register Walsh-Hadamard transform of one d-vector held by a warp
-// (coordinate e * 32 + lane in a[e]); unnormalised, Sylvester order.
-template <int E>
-__device__ __forceinline__ void warp_fwht(float (&a)[E], int lane) {
-#pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float o = __shfl_xor_sync(0xffffffffu, a[e], h);
-      a[e] = (lane & h) ? (o - a[e]) : (a[e] + o);
-    }
-  }
-#pragma unroll
-  for (int h = 1; h < E; h <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      if ((e & h) == 0) {
-        const float lo = a[e], hi = a[e + h];
-        a[e] = lo + hi;
-        a[e + h] = lo - hi;
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ prologue
 
 // One CTA per (kv head g, tile of 4 query vectors of that head across the
@@ -264,7 +239,20 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
   rotate_tile<D, kPrologueTile>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
-  if (P.kqjl == TQ_KEY_QJL) {
+  if (P.kqjl == TQ_KEY_QJL && P.qjl_srht) {
+    // q'' = H (sigma_S * q'), one warp per query vector (every CTA computes all d rows)
+    constexpr int E = D / 32;
+    const int lane = j & 31, warp = j >> 5;
+    const float* sg = P.qjl_s + (size_t)g * D;
+    for (int v = warp; v < nv; v += D / 32) {
+      float a[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[e] = s.x[v][e * 32 + lane] * __ldg(sg + e * 32 + lane);
+      warp_wht<E>(a, lane);
+#pragma unroll
+      for (int e = 0; e < E; ++e) s.r[v][e * 32 + lane] = a[e];
+    }
+  } else if (P.kqjl == TQ_KEY_QJL) {
     // q'' rows of this CTA: TPR neighbouring threads per row, 64 inputs each
     const int row = 64 * z + j / TPR, u = j % TPR;
     const float4* rp = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)row * D) + u * 16;
@@ -1056,7 +1044,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
       float a[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) a[e] = y[e * 32 + lane];
-      warp_fwht<E>(a, lane);
+      warp_wht<E>(a, lane);
       const float sc = rsqrtf((float)D);
       __syncwarp();
 #pragma unroll

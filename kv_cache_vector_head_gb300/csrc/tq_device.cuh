@@ -21,6 +21,7 @@ struct KParams {
   const float* k_rot;
   const float* v_rot;
   const float* qjl_s;
+  int qjl_srht;                        // qjl_s holds the signs of S = H diag(sigma_S)
   float kc[16], kt[16], vc[16], vt[16];
   // Walsh-plane coefficients: a code (sign s, magnitude bits m) has centroid
   // s * sum_S a_S * prod_{i in S} (1 - 2 m_i); plane S has bit s ^ parity(m & S).

@@ -201,7 +201,7 @@ extern "C" tq_status tq_build_transform(tq_transform_kind kind, int d, uint64_t 
   using namespace tq;
   if (!out) return fail(TQ_ERR_INVALID_ARG, "tq_build_transform: null output");
   if (d < 2 || d > 4096) return fail(TQ_ERR_INVALID_ARG, "tq_build_transform: d must be in [2, 4096]");
-  if (layer < 0 || layer >= (1 << 20) || head < 0 || head >= (1 << 16) || role < 0 || role > 2)
+  if (layer < 0 || layer >= (1 << 20) || head < 0 || head >= (1 << 16) || role < 0 || role > 3)
     return fail(TQ_ERR_INVALID_ARG, "tq_build_transform: layer/head/role out of range");
   if (kind != TQ_DENSE && kind != TQ_FWHT) return fail(TQ_ERR_INVALID_ARG, "tq_build_transform: bad kind");
   if (kind == TQ_FWHT && (d & (d - 1)))
@@ -213,7 +213,8 @@ extern "C" tq_status tq_build_transform(tq_transform_kind kind, int d, uint64_t 
     for (size_t i = 0; i < s.size(); ++i) out[i] = (float)s[i];
     return ok();
   }
-  if (kind == TQ_FWHT) {
+  if (kind == TQ_FWHT || role == TQ_ROLE_QJL_SIGNS) {
+    if (d & (d - 1)) return fail(TQ_ERR_UNSUPPORTED, "tq_build_transform: sign vectors need a power-of-two d");
     for (int i = 0; i < d; ++i) out[i] = (g.next() & 1ull) ? -1.0f : 1.0f;
     return ok();
   }

@@ -22,6 +22,8 @@
 // channel allocation) take coordinates < d/2 one bit wider with their own
 // book; the wider codes' top plane is kept for the first d/64 words only.
 // Byte key norms (u8 log-norm) are encoded when the page slot is written.
+// The structured sketch S = H diag(sigma_S) takes the signs of a warp
+// Walsh-Hadamard transform of sigma_S * r instead of the tile product.
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -125,6 +127,24 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
     }
   }
   if (P.kqjl != TQ_KEY_QJL) {
+    __syncthreads();
+    return;
+  }
+  if (P.qjl_srht) {
+    // 5. structured sketch S = H diag(sigma_S): signs of the fast transform of sigma_S * r,
+    //    one warp per vector (coordinate e * 32 + lane in register e, word e of the signs)
+    const float* sg = P.qjl_s + (size_t)head * D;
+    for (int v = warp; v < nv; v += D / 32) {
+      float a[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[e] = s.r[v][e * 32 + lane] * __ldg(sg + e * 32 + lane);
+      warp_wht<E>(a, lane);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned w = __ballot_sync(0xffffffffu, (s.zero[v] || a[e] >= 0.f) ? 1u : 0u);
+        if (lane == 0) s.signs[v][e] = w;
+      }
+    }
     __syncthreads();
     return;
   }
@@ -511,7 +531,8 @@ static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const K
 
 // Tensor-core path: d = 128, bf16, 16-byte aligned input, antisymmetric tables.
 static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key, long long n_vec) {
-  if (is_key && (P.ksplit || P.knu8)) return false;  // mixed-channel keys and byte norms: CUDA-core tiles
+  // mixed-channel keys, byte norms and the structured sketch: CUDA-core tiles
+  if (is_key && (P.ksplit || P.knu8 || P.qjl_srht)) return false;
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
   return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
 }

@@ -21,6 +21,31 @@ struct TileSmem {
   float cb_hi[16], tb_hi[16];      // mixed-channel keys: the book of coordinates < d/2
 };
 
+// In-register Walsh-Hadamard transform of one d-vector held by a warp
+// (coordinate e * 32 + lane in a[e]); unnormalised, Sylvester order.
+template <int E>
+__device__ __forceinline__ void warp_wht(float (&a)[E], int lane) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, a[e], h);
+      a[e] = (lane & h) ? (o - a[e]) : (a[e] + o);
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & h) == 0) {
+        const float lo = a[e], hi = a[e + h];
+        a[e] = lo + hi;
+        a[e + h] = lo - hi;
+      }
+    }
+  }
+}
+
 // out[v][j] = inv[v] * (R x_v)_j, R = Pi (dense) or H diag(sigma) (FWHT).
 // In place in s.x (the dense product goes through registers).
 template <int D, int MAXV = kTile>
@@ -32,25 +57,7 @@ __device__ void rotate_tile(TileSmem<D>& s, int nv, int kind, const float* rot) 
       float a[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) a[e] = s.x[v][e * 32 + lane] * __ldg(rot + e * 32 + lane);
-#pragma unroll
-      for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float o = __shfl_xor_sync(0xffffffffu, a[e], h);
-          a[e] = (lane & h) ? (o - a[e]) : (a[e] + o);
-        }
-      }
-#pragma unroll
-      for (int h = 1; h < E; h <<= 1) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if ((e & h) == 0) {
-            const float lo = a[e], hi = a[e + h];
-            a[e] = lo + hi;
-            a[e + h] = lo - hi;
-          }
-        }
-      }
+      warp_wht<E>(a, lane);
       const float sc = s.inv[v];
 #pragma unroll
       for (int e = 0; e < E; ++e) s.x[v][e * 32 + lane] = a[e] * sc;

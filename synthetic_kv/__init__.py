@@ -72,6 +72,7 @@ class Workload:
     head_dim: int = 0      # length of the generated vectors (0: d); heads shorter than d are zero-padded to d
     key_split: int = 0     # mixed-channel key rate: the first d/2 rotated coordinates one bit wider
     key_norm_range: tuple | None = None  # (lo, hi): byte key norms, log2-uniform over [2^lo, 2^hi]
+    qjl_structured: int = 0  # QJL sketch S = H diag(sigma_S) in place of a dense Gaussian
 
     @property
     def dh(self) -> int:

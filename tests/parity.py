@@ -35,7 +35,7 @@ NORM_CODE_BAND = 1e-4
 
 class OracleLayer:
     def __init__(self, d, hkv, hq, kb, vb, kind, window=0, qjl=True, seed=0, layer=0, key_split=0,
-                 key_norm_range=None):
+                 key_norm_range=None, qjl_structured=0):
         """qjl: key correction (False/0 none, True/1 QJL, 2 EDEN scale, 3 length renormalization).
         key_split: mixed-channel key rate; key_norm_range: (lo, hi) of the byte key norms."""
         self.d, self.hkv, self.hq, self.kb, self.vb, self.kind = d, hkv, hq, kb, vb, kind
@@ -46,7 +46,13 @@ class OracleLayer:
         self.vcb = OCB.lloyd_max(d, vb)
         self.k_rot = [OT.build_transform(kind, d, seed, layer, h, 0) for h in range(hkv)]
         self.v_rot = [OT.build_transform(kind, d, seed, layer, h, 1) for h in range(hkv)]
-        self.S = [OT.build_transform(kind, d, seed, layer, h, 2) for h in range(hkv)] if self.qjl == 1 else None
+        if self.qjl == 1 and qjl_structured:  # S = H diag(sigma_S), +-1 entries
+            self.S = [OT.structured_qjl_matrix(OT.build_transform(kind, d, seed, layer, h, OT.ROLE_QJL_SIGNS), d)
+                      for h in range(hkv)]
+        elif self.qjl == 1:
+            self.S = [OT.build_transform(kind, d, seed, layer, h, 2) for h in range(hkv)]
+        else:
+            self.S = None
 
     def keys(self, x, head):
         """Key records; with byte norms also norm_code, its margin and norm_dec (the decoded norm)."""

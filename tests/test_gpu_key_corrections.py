@@ -16,7 +16,8 @@ For each (correction, MSE bits) the test measures over 131072 (q, k) pairs of
 isotropic bf16 keys (d = 128, dense Pi and FWHT):
     slope = sum est * true / sum true^2      (1 for an unbiased estimator)
     D     = d * mean((est - true)^2 / (||q||^2 ||k||^2))
-and prints the table (`pytest -m gpu -s tests/test_gpu_key_corrections.py`).
+and prints the table (`pytest -m gpu -s tests/test_gpu_key_corrections.py`); the same for the structured
+sketch S = H diag(sigma_S) in place of the Gaussian one.
 """
 
 import numpy as np
@@ -44,9 +45,9 @@ def tq():
     return tq
 
 
-def _estimates(tq, w, corr, bits):
+def _estimates(tq, w, corr, bits, structured=False):
     """Decode scores (estimates of <q, k>), the exact products and ||q||^2 ||k||^2."""
-    L = tq.TQLayer(D, 1, HQ, bits, 2, w.kind, window=0, key_qjl=corr, seed=w.seed)
+    L = tq.TQLayer(D, 1, HQ, bits, 2, w.kind, window=0, key_qjl=corr, seed=w.seed, qjl_structured=structured)
     pc = tq.PagedCache(L, B, T)
     kv = SK.keys_values(w)
     k = SK.to_torch(kv["K"], w.dtype).cuda()
@@ -84,6 +85,16 @@ def test_key_correction_estimators(tq, kind):
         print(f"{bits:>4}  " + "  ".join(f"{table[c, bits][0]:7.4f} {table[c, bits][1]:8.5f}" for c in range(4)))
     n = B * HQ * T
     print("Lloyd-Max unit MSE: " + ", ".join(f"{b}: {mse[b]:.5f}" for b in (1, 2, 3, 4)))
+    # the structured sketch S = H diag(sigma_S): close to unbiased on the rotated residuals, and its
+    # orthogonal rows give a lower distortion than the dense Gaussian sketch
+    for bits in (1, 2, 3, 4):
+        est, true, qk2 = _estimates(tq, w, 1, bits, structured=True)
+        slope = float((est * true).sum() / (true * true).sum())
+        dist = float(D * np.mean((est - true) ** 2 / qk2))
+        print(f"structured QJL, {bits} bits: slope {slope:.4f}, d * distortion {dist:.5f}")
+        tol = 4.0 * np.sqrt(dist / (B * T))
+        assert abs(slope - 1.0) < max(tol, 0.01), (bits, slope)
+        assert dist < 1.05 * table[1, bits][1], (bits, dist, table[1, bits][1])
     for bits in (1, 2, 3, 4):
         s_mse, d_mse = table[0, bits]
         s_qjl, d_qjl = table[1, bits]

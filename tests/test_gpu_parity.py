@@ -34,10 +34,10 @@ def tq():
 def _layer(tq, w, layer=0):
     L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
                    key_qjl=w.key_qjl, seed=w.seed, layer=layer, head_dim=w.dh, key_split=w.key_split,
-                   key_norm_range=w.key_norm_range)
+                   key_norm_range=w.key_norm_range, qjl_structured=w.qjl_structured)
     O = PY.OracleLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
                        qjl=w.key_qjl, seed=w.seed, layer=layer, key_split=w.key_split,
-                       key_norm_range=w.key_norm_range)
+                       key_norm_range=w.key_norm_range, qjl_structured=w.qjl_structured)
     return L, O
 
 
@@ -77,6 +77,11 @@ CASES = [
     ("qwen", dict(batch=1, ctx=40, key_bits=2, key_qjl=2, key_split=1)),
     ("tiny", dict(ctx=60, key_bits=1, key_qjl=3, key_split=1, key_norm_range=(-4.0, 12.0))),
     ("bulk", dict(ctx=90, key_bits=3, key_qjl=0, key_split=1, head_dim=96)),
+    # the structured sketch S = H diag(sigma_S), FWHT and dense rotations
+    ("qwen", dict(batch=1, ctx=40, qjl_structured=1)),
+    ("bulk", dict(ctx=300, kind=SK.FWHT, qjl_structured=1)),
+    ("tiny", dict(ctx=60, qjl_structured=1, key_bits=1)),
+    ("long", dict(ctx=30, qjl_structured=1, head_dim=160)),
 ]
 
 
@@ -253,6 +258,10 @@ PAGED = [
     # byte norms alone, with the sketch; a narrow range that clamps the outlier keys' norms
     ("llama", dict(batch=3, key_norm_range=(3.0, 5.0)), 33, 10),
     ("qwen", dict(batch=1, window=20, key_norm_range=(2.0, 6.0)), 50, 20),
+    # the structured sketch
+    ("qwen", dict(batch=2, window=20, qjl_structured=1), 75, 30),
+    ("llama", dict(batch=5, kind=SK.FWHT, qjl_structured=1), 29, 21),
+    ("tiny", dict(qjl_structured=1, key_norm_range=(-4.0, 12.0)), 37, 12),
 ]
 
 

@@ -148,3 +148,20 @@ def test_mixed_rate_and_byte_norm_layout_and_checks(L):
     assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
     p.key_norm_log2_hi = 9.0
     assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (57 + 4 + 32)  # values 2 bits
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_structured_sketch_signs_and_checks(L, d):
+    for kind in (L.TQ_FWHT, L.TQ_DENSE):
+        s = L.build_transform(kind, d, 7, 3, 1, L.ROLE_QJL_SIGNS)
+        assert np.array_equal(s, OT.build_transform(kind, d, 7, 3, 1, OT.ROLE_QJL_SIGNS))
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size = d, 2, 4, 16
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 2, 2, 1, L.TQ_FWHT
+    p.qjl_structured = 1
+    lib = L.lib()
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 16 * (8 + 3 * d // 8 + 4 + 2 * d // 8)
+    p.key_qjl = L.KEY_EDEN
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"qjl_structured" in lib.tq_last_error()
+    p.key_qjl, p.qjl_structured = 1, 2
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
