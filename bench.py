@@ -353,8 +353,9 @@ def bench_quantize(tq, torch, n=1 << 20):
     out = {}
     x = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
     y = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
-    for name, kind in (("fwht", tq.TQ_FWHT), ("dense", tq.TQ_DENSE)):
-        L = tq.TQLayer(128, 8, 8, 3, 4, kind)
+    for name, kind, structured in (("fwht", tq.TQ_FWHT, False), ("dense", tq.TQ_DENSE, False),
+                                   ("fwht_structured_sketch", tq.TQ_FWHT, True)):
+        L = tq.TQLayer(128, 8, 8, 3, 4, kind, qjl_structured=structured)
         codes = torch.empty(n, 12, dtype=torch.int32, device="cuda")
         signs = torch.empty(n, 4, dtype=torch.int32, device="cuda")
         nk = torch.empty(n, device="cuda")
@@ -552,7 +553,9 @@ def run_gpu(args):
                      "peak_source": peak_src},
         "quantize": {"metric": "bulk quantize token-heads/s (d=128, keys 3b+QJL, values 4b, 2^20 token-heads)",
                      "fwht": dict(quant["fwht"], hbm_fraction=quant["fwht"]["GB_per_s"] / peak),
-                     "dense": dict(quant["dense"], hbm_fraction=quant["dense"]["GB_per_s"] / peak)},
+                     "dense": dict(quant["dense"], hbm_fraction=quant["dense"]["GB_per_s"] / peak),
+                     "fwht_structured_sketch": dict(quant["fwht_structured_sketch"],
+                                                    hbm_fraction=quant["fwht_structured_sketch"]["GB_per_s"] / peak)},
         "append_batch256": app,
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
