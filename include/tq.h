@@ -166,6 +166,18 @@ typedef struct {
    * (entries +-1, S S^T = d I); S r and S q' are computed with the fast
    * transform, the estimator keeps sqrt(pi/2)/d.  Needs key_qjl == TQ_KEY_QJL. */
   int qjl_structured;
+  /* KIVI-like control arm ([Design study] §Candidate key and value
+   * algorithms, arm 3: per-channel keys, per-token values, float16 recent
+   * window).  1: asymmetric min-max integer codes of key_bits / value_bits
+   * bits (2 or 4) in place of the TurboQuant records; a key group is one
+   * channel over a page's 16 tokens, a value group one token over its d
+   * channels; zero = float16(min), scale = float16((max - min) / (2^b - 1))
+   * formed in float32; code = clamp(floor((x - zero) / scale + 1/2)), 0 where
+   * the scale is 0.  No rotation or sketch (k_rot, v_rot, qjl_s unused; kind
+   * ignored); key_qjl, key_split, key_norm_u8, qjl_structured must be 0;
+   * head_dim == d; window >= 1 (pages are written whole: at a window flush,
+   * or by page-aligned direct appends).  Flat tq_quantize_* do not apply. */
+  int kivi;
 } tq_layer_params;
 
 /*
@@ -212,6 +224,10 @@ tq_status tq_quantize_values(const tq_layer_params* p, const void* v, tq_dtype d
  *   value code planes  uint16 [value_bits][d]  coordinate-major: bit t of
  *                      entry (plane, j) is that plane's bit of token t at j
  * (16 x the per-token record bytes; see tq_subblock_bytes).
+ * KIVI arm (kivi = 1): key scales float16 [d], key zeros float16 [d], key
+ * codes uint32 [16][d key_bits / 32] (code j of a token at bits
+ * (j b) mod 32 of word (j b) / 32), value scales float16 [16], value zeros
+ * float16 [16], value codes uint32 [16][d value_bits / 32].
  * Token position p of sequence b, p < n_compressed[b], lives in page
  * block_table[b][p / 16], slot p % 16.  Positions n_compressed[b] ..
  * seq_len[b]-1 are the float16 window; position p lives at ring slot

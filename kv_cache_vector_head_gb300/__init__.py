@@ -37,7 +37,8 @@ class TQLayer:
     def __init__(self, d: int, n_kv_heads: int, n_q_heads: int, key_bits: int, value_bits: int, kind: int,
                  window: int = 0, key_qjl: int = KEY_QJL, seed: int = 0, layer: int = 0, device="cuda",
                  head_dim: int | None = None, key_split: bool = False,
-                 key_norm_range: tuple[float, float] | None = None, qjl_structured: bool = False):
+                 key_norm_range: tuple[float, float] | None = None, qjl_structured: bool = False,
+                 kivi: bool = False):
         """d: the transform and code dimension (128 or 256); head_dim (default d):
         the length of the vectors the caller passes, zero-padded to d inside
         the kernels (a multiple of 8 in (d/2, d]).  key_qjl: the key
@@ -48,7 +49,10 @@ class TQLayer:
         gives 3.5 bits per channel; not with KEY_QJL).  key_norm_range =
         (lo, hi): key norms stored as one byte, log2-uniform over [2^lo, 2^hi].
         qjl_structured (with KEY_QJL): the sketch matrix is S = H diag(sigma_S),
-        applied as a fast Walsh-Hadamard transform, instead of a dense Gaussian."""
+        applied as a fast Walsh-Hadamard transform, instead of a dense Gaussian.
+        kivi: the KIVI-like control arm (asymmetric min-max codes of key_bits /
+        value_bits = 2 or 4 bits, keys per channel over a page, values per
+        token; no rotation; key_qjl must be KEY_MSE and window >= 1)."""
         import torch
 
         self.d, self.n_kv_heads, self.n_q_heads = d, n_kv_heads, n_q_heads
@@ -58,14 +62,18 @@ class TQLayer:
         if self.key_qjl not in (KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM):
             raise ValueError(f"key_qjl must be one of KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM, got {key_qjl}")
         self.key_split, self.key_norm_range = bool(key_split), key_norm_range
+        self.kivi = bool(kivi)
         self.k_cb = build_codebook(d, key_bits)
         self.k_cb_hi = build_codebook(d, key_bits + 1) if key_split else None
         self.v_cb = build_codebook(d, value_bits)
-        kr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_KEY_ROT) for h in range(n_kv_heads)])
-        vr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_VALUE_ROT) for h in range(n_kv_heads)])
-        self.k_rot_host, self.v_rot_host = kr, vr
-        self.k_rot = torch.from_numpy(kr).to(device)
-        self.v_rot = torch.from_numpy(vr).to(device)
+        if self.kivi:  # no transforms
+            self.k_rot_host = self.v_rot_host = self.k_rot = self.v_rot = None
+        else:
+            kr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_KEY_ROT) for h in range(n_kv_heads)])
+            vr = np.stack([build_transform(kind, d, seed, layer, h, ROLE_VALUE_ROT) for h in range(n_kv_heads)])
+            self.k_rot_host, self.v_rot_host = kr, vr
+            self.k_rot = torch.from_numpy(kr).to(device)
+            self.v_rot = torch.from_numpy(vr).to(device)
         self.qjl_structured = bool(qjl_structured)
         if self.key_qjl == KEY_QJL:
             role = ROLE_QJL_SIGNS if qjl_structured else ROLE_QJL
@@ -78,7 +86,9 @@ class TQLayer:
         p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = d, n_kv_heads, n_q_heads, PAGE_SIZE, window
         p.key_bits, p.key_qjl, p.value_bits, p.kind = key_bits, self.key_qjl, value_bits, kind
         p.head_dim = self.head_dim
-        p.k_rot, p.v_rot = self.k_rot.data_ptr(), self.v_rot.data_ptr()
+        p.k_rot = self.k_rot.data_ptr() if self.k_rot is not None else None
+        p.v_rot = self.v_rot.data_ptr() if self.v_rot is not None else None
+        p.kivi = int(self.kivi)
         p.qjl_s = self.qjl_s.data_ptr() if self.qjl_s is not None else None
         for name, (c, t, _) in (("k", self.k_cb), ("v", self.v_cb)):
             getattr(p, f"{name}_centroids")[: len(c)] = [float(x) for x in c]

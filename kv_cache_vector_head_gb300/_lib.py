@@ -47,7 +47,7 @@ class LayerParams(ctypes.Structure):
         ("head_dim", c_int),
         ("key_split", c_int), ("k_hi_centroids", c_float * 16), ("k_hi_bounds", c_float * 16),
         ("key_norm_u8", c_int), ("key_norm_log2_lo", c_float), ("key_norm_log2_hi", c_float),
-        ("qjl_structured", c_int),
+        ("qjl_structured", c_int), ("kivi", c_int),
     ]
 
 

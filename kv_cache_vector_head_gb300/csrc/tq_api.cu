@@ -63,10 +63,20 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
     return fail(TQ_ERR_INVALID_ARG, "qjl_structured must be 0 or 1");
   if (p->qjl_structured && p->key_qjl != TQ_KEY_QJL)
     return fail(TQ_ERR_INVALID_ARG, "qjl_structured needs key_qjl == TQ_KEY_QJL");
+  if (p->kivi != 0 && p->kivi != 1) return fail(TQ_ERR_INVALID_ARG, "kivi must be 0 or 1");
+  if (p->kivi) {
+    auto kbits_ok = [](int b) { return b == 2 || b == 4; };
+    if (!kbits_ok(p->key_bits) || !kbits_ok(p->value_bits))
+      return fail(TQ_ERR_UNSUPPORTED, "kivi: key_bits and value_bits must be 2 or 4");
+    if (p->key_qjl || p->key_split || p->key_norm_u8 || p->qjl_structured)
+      return fail(TQ_ERR_INVALID_ARG, "kivi: key_qjl, key_split, key_norm_u8, qjl_structured must be 0");
+    if (p->head_dim != 0 && p->head_dim != p->d) return fail(TQ_ERR_UNSUPPORTED, "kivi: head_dim must be d");
+    if (p->window < 1) return fail(TQ_ERR_INVALID_ARG, "kivi: window must be >= 1 (pages are written whole)");
+  }
   if (p->key_norm_u8 && !(std::isfinite(p->key_norm_log2_lo) && std::isfinite(p->key_norm_log2_hi) &&
                           p->key_norm_log2_lo < p->key_norm_log2_hi))
     return fail(TQ_ERR_INVALID_ARG, "key_norm_u8 needs finite key_norm_log2_lo < key_norm_log2_hi");
-  if (need_device_ptrs) {
+  if (need_device_ptrs && !p->kivi) {
     if (!p->k_rot || !p->v_rot) return fail(TQ_ERR_INVALID_ARG, "null k_rot / v_rot");
     if (p->key_qjl == TQ_KEY_QJL && !p->qjl_s) return fail(TQ_ERR_INVALID_ARG, "null qjl_s with key_qjl");
     if (!aligned(p->k_rot, 16) || !aligned(p->v_rot, 16) || (p->qjl_s && !aligned(p->qjl_s, 16)))
@@ -129,6 +139,19 @@ static tq_status make_params(const tq_layer_params* p, KParams* K, bool need_dev
   K->off_vnorm = o; o += 4 * P;
   K->off_vcodes = o; o += 2 * p->value_bits * d;
   K->sub_bytes = o;
+  K->kivi = p->kivi;
+  K->off_kscale = K->off_kzero = K->off_vscale = K->off_vzero = 0;
+  if (p->kivi) {
+    o = 0;
+    K->off_kscale = o; o += 2 * d;
+    K->off_kzero = o; o += 2 * d;
+    K->off_kcodes = o; o += 4 * P * (d * p->key_bits / 32);
+    K->off_vscale = o; o += 2 * P;
+    K->off_vzero = o; o += 2 * P;
+    K->off_vcodes = o; o += 4 * P * (d * p->value_bits / 32);
+    K->sub_bytes = o;
+    K->off_knorm = K->off_krnorm = K->off_kx = K->off_ksigns = K->off_vnorm = 0;
+  }
   return TQ_OK;
 }
 
@@ -186,6 +209,7 @@ extern "C" tq_status tq_quantize_keys(const tq_layer_params* p, const void* k, t
   tq_status s = make_params(p, &K, true);
   if (s != TQ_OK) return s;
   if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if (K.kivi) return fail(TQ_ERR_UNSUPPORTED, "kivi: keys are quantized into pages only");
   if (n_vec < 0) return fail(TQ_ERR_INVALID_ARG, "n_vec < 0");
   if (n_vec == 0) return ok();
   if (!k || !code_planes || !norms) return fail(TQ_ERR_INVALID_ARG, "null input or output");
@@ -204,6 +228,7 @@ extern "C" tq_status tq_quantize_values(const tq_layer_params* p, const void* v,
   tq_status s = make_params(p, &K, true);
   if (s != TQ_OK) return s;
   if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if (K.kivi) return fail(TQ_ERR_UNSUPPORTED, "kivi: values are quantized into pages only");
   if (n_vec < 0) return fail(TQ_ERR_INVALID_ARG, "n_vec < 0");
   if (n_vec == 0) return ok();
   if (!v || !code_planes || !norms) return fail(TQ_ERR_INVALID_ARG, "null input or output");
@@ -229,6 +254,8 @@ extern "C" tq_status tq_append_page(const tq_layer_params* p, tq_cache* cache, c
     if (n_tok != cache->batch) return fail(TQ_ERR_INVALID_ARG, "decode-step append needs n_tok == batch");
     return cuda_status(launch_append_step(K, C, k, v, dtype, st), "tq_append_page");
   }
+  if (K.kivi && n_tok % TQ_PAGE_SIZE)
+    return fail(TQ_ERR_INVALID_ARG, "kivi: direct appends write whole pages (n_tok a multiple of 16)");
   return cuda_status(launch_append_direct(K, C, k, v, dtype, n_tok, reinterpret_cast<const long long*>(slot_mapping), st),
                      "tq_append_page");
 }

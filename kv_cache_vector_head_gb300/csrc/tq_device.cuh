@@ -38,6 +38,10 @@ struct KParams {
                                        // that an operand register stays one LOP3 with a register operand
   int sub_bytes;                       // bytes of one (page, head) sub-block
   int off_knorm, off_krnorm, off_kcodes, off_kx, off_ksigns, off_vnorm, off_vcodes;
+  // KIVI arm: integer codes with float16 scale / zero (key per channel, value per token);
+  // off_kcodes / off_vcodes hold the codes
+  int kivi;
+  int off_kscale, off_kzero, off_vscale, off_vzero;
 };
 
 // Byte key norm ([Design study] §Packed format, u8 log-norm): 0 for a zero

@@ -292,6 +292,87 @@ __device__ void store_value_slot(const KParams& P, const TileSmem<D>& s, unsigne
   }
 }
 
+// ------------------------------------------------------------------ KIVI control arm
+
+// [Design study] §Candidate key and value algorithms, arm 3: asymmetric
+// min-max integer codes, keys per channel over a page's 16 tokens, values per
+// token over the d channels; scale = float16((max - min) / (2^b - 1)) formed in
+// float32, zero = float16(min), code = clamp(floor((x - zero) / scale + 1/2)).
+
+__device__ __forceinline__ void kivi_scale_zero(float mn, float mx, int bits, __half& hs, __half& hz) {
+  hs = __float2half_rn(__fdiv_rn(mx - mn, (float)((1 << bits) - 1)));
+  hz = __float2half_rn(mn);
+}
+
+__device__ __forceinline__ uint32_t kivi_code(float x, float sf, float zf, int bits) {
+  if (!(sf > 0.f)) return 0u;
+  const float t = __fdiv_rn(x - zf, sf);
+  return (uint32_t)fminf(fmaxf(floorf(t + 0.5f), 0.f), (float)((1 << bits) - 1));
+}
+
+// The packed word of the lanes sharing it (32 / bits consecutive lanes): code of
+// lane l at bits (l mod (32 / bits)) * bits.
+__device__ __forceinline__ uint32_t kivi_word(uint32_t c, int bits, int lane) {
+  const int per = 32 / bits;
+  uint32_t w = c << ((lane % per) * bits);
+  for (int o = 1; o < per; o <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, o);
+  return w;
+}
+
+// One whole page (16 tokens of one head, s.x[0..15][0..d)) into its sub-block:
+// the key half (is_key) or the value half.
+template <int D>
+__device__ void kivi_store_page(const KParams& P, TileSmem<D>& s, bool is_key, unsigned char* sb) {
+  const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  const int bits = is_key ? P.kb : P.vb;
+  const int per = 32 / bits, wpt = D * bits / 32;
+  uint32_t* codes = reinterpret_cast<uint32_t*>(sb + (is_key ? P.off_kcodes : P.off_vcodes));
+  if (is_key) {
+    float mn = s.x[0][j], mx = mn;
+    for (int t = 1; t < kPage; ++t) {
+      mn = fminf(mn, s.x[t][j]);
+      mx = fmaxf(mx, s.x[t][j]);
+    }
+    __half hs, hz;
+    kivi_scale_zero(mn, mx, bits, hs, hz);
+    reinterpret_cast<__half*>(sb + P.off_kscale)[j] = hs;
+    reinterpret_cast<__half*>(sb + P.off_kzero)[j] = hz;
+    const float sf = __half2float(hs), zf = __half2float(hz);
+    for (int t = 0; t < kPage; ++t) {
+      const uint32_t w = kivi_word(kivi_code(s.x[t][j], sf, zf, bits), bits, lane);
+      if (lane % per == 0) codes[t * wpt + j / per] = w;
+    }
+  } else {
+    for (int t = warp; t < kPage; t += D / 32) {  // warp w: tokens w, w + d/32, ...
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) {
+        const float x = s.x[t][e * 32 + lane];
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        __half hs, hz;
+        kivi_scale_zero(mn, mx, bits, hs, hz);
+        reinterpret_cast<__half*>(sb + P.off_vscale)[t] = hs;
+        reinterpret_cast<__half*>(sb + P.off_vzero)[t] = hz;
+        s.norm[t] = __half2float(hs);
+        s.gam[t] = __half2float(hz);
+      }
+    }
+    __syncthreads();
+    for (int t = 0; t < kPage; ++t) {
+      const uint32_t w = kivi_word(kivi_code(s.x[t][j], s.norm[t], s.gam[t], bits), bits, lane);
+      if (lane % per == 0) codes[t * wpt + j / per] = w;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ append: direct slots
 
 template <int D>
@@ -343,6 +424,15 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
           (page_of[i] >= 0 && threadIdx.x < P.dh) ? load_elem(x, dtype, n * P.dh + threadIdx.x) : 0.f;
     }
     __syncthreads();
+    if (P.kivi) {
+      // whole pages only: the tile's 16 tokens fill slots 0..15 of one page in order
+      bool whole = nv == kTile && same_page && page_of[0] >= 0;
+      for (int i = 0; i < nv && whole; ++i) whole = slot_of[i] == i;
+      if (whole) kivi_store_page<D>(P, s, is_key, subblock(P, C, page_of[0], head));
+      else if (threadIdx.x == 0) atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+      __syncthreads();
+      continue;
+    }
     quantize_tile<D>(P, s, nv, head, is_key, slot_of);
     if (is_key) {
       for (int i = 0; i < nv; ++i)
@@ -410,6 +500,10 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
       s.x[i][threadIdx.x] = __half2float(ring[(size_t)((nc + i) % C.ring) * D + threadIdx.x]);
     if (threadIdx.x < kTile) slot_of[threadIdx.x] = threadIdx.x;
     __syncthreads();
+    if (P.kivi) {
+      kivi_store_page<D>(P, s, is_key, subblock(P, C, page, head));
+      return;
+    }
     quantize_tile<D>(P, s, kPage, head, is_key, slot_of);
     unsigned char* sb = subblock(P, C, page, head);
     if (is_key) {
@@ -419,6 +513,10 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
       if (threadIdx.x < kPage) reinterpret_cast<float*>(sb + P.off_vnorm)[threadIdx.x] = s.norm[threadIdx.x];
     }
   } else {
+    if (P.kivi) {  // the KIVI arm needs a window (checked on the host)
+      if (threadIdx.x == 0) atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
+      return;
+    }
     const int pidx = T / kPage, slot = T % kPage;
     long long page = -1;
     if (T >= 0 && pidx < C.max_pages) page = C.block_table[(size_t)b * C.max_pages + pidx];
@@ -533,6 +631,7 @@ static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const K
 static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key, long long n_vec) {
   // mixed-channel keys, byte norms and the structured sketch: CUDA-core tiles
   if (is_key && (P.ksplit || P.knu8 || P.qjl_srht)) return false;
+  if (P.kivi) return false;
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
   return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
 }

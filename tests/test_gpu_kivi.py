@@ -1,0 +1,132 @@
+"""GPU-vs-oracle parity of the KIVI-like control arm, through the C ABI.
+
+[Design study] §Candidate key and value algorithms, arm 3.  Pages written by
+the prefill (direct page-aligned appends) and by window flushes are read back
+and compared with oracle/kivi.py: float16 scales and zeros bit-exact, codes
+bit-exact except decisions within 1e-5 code units of a rounding point
+(counted, under 1e-4 of the codes); then the decode (pages + float16 window)
+is compared with textbook attention over the dequantized cache, scores 1e-3
+and outputs 2e-3 absolute.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import synthetic_kv as SK
+from oracle import kivi as OKV
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+BAND = 1e-5
+EXEMPT_FRACTION = 1e-4
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    from kv_cache_vector_head_gb300 import build
+
+    build.build()
+    import kv_cache_vector_head_gb300 as tq
+
+    return tq
+
+
+CASES = [
+    ("llama", dict(batch=3, key_bits=2, value_bits=2), 20, 75, 30),
+    ("qwen", dict(batch=2, key_bits=2, value_bits=4), 20, 61, 25),
+    ("llama", dict(batch=2, key_bits=4, value_bits=4), 128, 200, 20),
+    ("tiny", dict(key_bits=4, value_bits=2), 16, 50, 40),
+    ("long", dict(key_bits=2, value_bits=2), 32, 300, 17),
+]
+
+
+def _compare_codes(g, o, stats):
+    diff = g != o["codes"]
+    band = o["margin"] < BAND
+    assert not (diff & ~band).any(), f"{int((diff & ~band).sum())} code mismatches outside the band"
+    assert np.abs(g - o["codes"]).max(initial=0) <= 1
+    stats["exempt"] += int(band.sum())
+    stats["codes"] += band.size
+    return np.where(band, g, o["codes"])
+
+
+@pytest.mark.parametrize("name,over,W,T0,steps", CASES)
+def test_kivi_paged_append_and_decode_parity(tq, name, over, W, T0, steps):
+    w = SK.workload(name, window=W, key_qjl=0, **over)
+    T = T0 + steps
+    kv = SK.keys_values(w, ctx=T)
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=W, key_qjl=0,
+                   seed=w.seed, kivi=True)
+    pc = tq.PagedCache(L, w.batch, T)
+    kt = SK.to_torch(kv["K"], w.dtype).cuda()
+    vt = SK.to_torch(kv["V"], w.dtype).cuda()
+    pc.prefill(kt[:, :T0], vt[:, :T0])
+    for t in range(T0, T):
+        pc.append(kt[:, t].contiguous(), vt[:, t].contiguous())
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    nc0 = 16 * (max(0, T0 - W) // 16)
+    nc = 16 * (max(0, T - W) // 16)
+    assert pc.n_compressed.cpu().tolist() == [nc] * w.batch
+    qt = SK.to_torch(kv["q"], w.dtype).cuda()
+    scale = 1.0 / math.sqrt(w.d)
+    ws = torch.empty(tq.decode_workspace_size(L.params, w.batch, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.batch, w.n_q_heads, w.d, device="cuda")
+    lse = torch.zeros(w.batch, w.n_q_heads, device="cuda")
+    scores = torch.full((w.batch, w.n_q_heads, T), float("nan"), device="cuda")
+    tq.decode_attention(L.params, pc.cache, qt, scale, out, lse, scores, ws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    pool = pc.pool.cpu().numpy()
+    bt = pc.block_table.cpu().numpy()
+    lay = OKV.subblock_layout(w.d, w.key_bits, w.value_bits)
+    stats = {"exempt": 0, "codes": 0}
+    for b in range(w.batch):
+        Kh, Vh = [], []
+        for h in range(w.n_kv_heads):
+            K = kv["K"][b, :nc, h].copy()
+            V = kv["V"][b, :nc, h].copy()
+            K[nc0:] = K[nc0:].astype(np.float16).astype(np.float64)  # flushed from the float16 window
+            V[nc0:] = V[nc0:].astype(np.float16).astype(np.float64)
+            kh, vh = [], []
+            for p in range(nc // 16):
+                g = OKV.read_page(pool, lay, w.n_kv_heads, int(bt[b, p]), h, w.d, w.key_bits, w.value_bits)
+                ok = OKV.quantize_key_page(K[16 * p:16 * p + 16], w.key_bits)
+                ov = OKV.quantize_values(V[16 * p:16 * p + 16], w.value_bits)
+                assert np.array_equal(g["kscale"].view(np.uint16), ok["scale"].view(np.uint16))
+                assert np.array_equal(g["kzero"].view(np.uint16), ok["zero"].view(np.uint16))
+                assert np.array_equal(g["vscale"].view(np.uint16), ov["scale"].view(np.uint16))
+                assert np.array_equal(g["vzero"].view(np.uint16), ov["zero"].view(np.uint16))
+                kc = _compare_codes(g["kcodes"], ok, stats)
+                vc = _compare_codes(g["vcodes"], ov, stats)
+                kh.append(OKV.dequantize(kc, ok["scale"][None, :], ok["zero"][None, :]))
+                vh.append(OKV.dequantize(vc, ov["scale"][:, None], ov["zero"][:, None]))
+            Kh.append(np.concatenate(kh) if kh else np.zeros((0, w.d)))
+            Vh.append(np.concatenate(vh) if vh else np.zeros((0, w.d)))
+        win_k = kv["K"][b, nc:T].transpose(1, 0, 2).astype(np.float16)
+        win_v = kv["V"][b, nc:T].transpose(1, 0, 2).astype(np.float16)
+        r = OKV.decode_one(kv["q"][b], np.stack(Kh), np.stack(Vh), win_k, win_v, scale)
+        g_sc = scores[b].cpu().numpy()
+        assert np.isfinite(g_sc).all()
+        assert np.abs(g_sc - r["scores"]).max() < 1e-3
+        assert np.abs(out[b].cpu().numpy() - r["out"]).max() < 2e-3
+        assert np.abs(lse[b].cpu().numpy() - r["lse"]).max() < 1e-3
+    assert stats["exempt"] <= max(3, EXEMPT_FRACTION * stats["codes"]), stats
+
+
+def test_kivi_direct_append_needs_whole_pages(tq):
+    w = SK.workload("llama", batch=1, window=16, key_qjl=0, key_bits=2, value_bits=2)
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, 2, 2, w.kind, window=16, key_qjl=0, kivi=True)
+    pc = tq.PagedCache(L, 1, 64)
+    k = torch.randn(16, w.n_kv_heads, w.d, device="cuda", dtype=torch.bfloat16)
+    slots = torch.arange(16, dtype=torch.int64, device="cuda").flip(0)  # one page, slots out of order
+    tq.append_page(L.params, pc.cache, k, k, 16, slots)
+    assert tq.check_device_error() & 0x4  # flagged on the device, nothing written
+    with pytest.raises(tq.TQError):
+        tq.append_page(L.params, pc.cache, k[:15].contiguous(), k[:15].contiguous(), 15, slots[:15])

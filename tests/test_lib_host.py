@@ -165,3 +165,25 @@ def test_structured_sketch_signs_and_checks(L, d):
     assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"qjl_structured" in lib.tq_last_error()
     p.key_qjl, p.qjl_structured = 1, 2
     assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+
+
+def test_kivi_layout_and_checks(L):
+    from oracle import kivi as OKV
+
+    lib = L.lib()
+    for d, kb, vb in [(128, 2, 2), (256, 4, 2), (128, 2, 4), (256, 4, 4)]:
+        p = L.LayerParams()
+        p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = d, 2, 4, 16, 16
+        p.key_bits, p.value_bits, p.key_qjl, p.kivi = kb, vb, 0, 1
+        assert L.subblock_bytes(p) == OKV.subblock_layout(d, kb, vb)["bytes"]
+    p.key_bits = 3
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"kivi" in lib.tq_last_error()
+    p.key_bits, p.window = 2, 0
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0 and b"window" in lib.tq_last_error()
+    p.window, p.key_qjl = 16, 1
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.key_qjl, p.head_dim = 0, 96
+    assert lib.tq_subblock_bytes(ctypes.byref(p)) == 0
+    p.head_dim = 0
+    # flat quantize does not apply to the KIVI arm (checked before any pointer)
+    assert lib.tq_quantize_keys(ctypes.byref(p), None, 1, 16, None, None, None, None, None) == L.TQ_ERR_UNSUPPORTED
