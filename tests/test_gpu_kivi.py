@@ -3,8 +3,9 @@
 [Design study] §Candidate key and value algorithms, arm 3.  Pages written by
 the prefill (direct page-aligned appends) and by window flushes are read back
 and compared with oracle/kivi.py: float16 scales and zeros bit-exact, codes
-bit-exact except decisions within 1e-5 code units of a rounding point
-(counted, under 1e-4 of the codes); then the decode (pages + float16 window)
+bit-exact except decisions within 1e-5 code units of a rounding point but
+not on it (counted, under 1e-4 of the codes; exact ties go up on both
+sides); then the decode (pages + float16 window)
 is compared with textbook attention over the dequantized cache, scores 1e-3
 and outputs 2e-3 absolute.
 """
@@ -47,8 +48,11 @@ CASES = [
 
 
 def _compare_codes(g, o, stats):
+    """Exact ties (margin 0 in float64) are not exempt: x - z is then a multiple of the
+    float16 scale by k + 1/2, at most 16 significant bits, so the float32 difference and
+    quotient are exact and both sides take the tie up; decisions near a tie are exempt."""
     diff = g != o["codes"]
-    band = o["margin"] < BAND
+    band = (o["margin"] < BAND) & (o["margin"] > 0)
     assert not (diff & ~band).any(), f"{int((diff & ~band).sum())} code mismatches outside the band"
     assert np.abs(g - o["codes"]).max(initial=0) <= 1
     stats["exempt"] += int(band.sum())
