@@ -41,6 +41,9 @@ METRIC = "decode-attention compressed-KV GB/s & % HBM roofline; quantize tokensÂ
 
 
 def key_mode(w) -> str:
+    if w.kivi:
+        return (f"KIVI-like control arm: keys {w.key_bits}b per channel over 16-token pages, "
+                f"float16 scale and zero")
     if w.key_split:
         code = f"{w.key_bits + 0.5}b per channel (coordinates < d/2 at {w.key_bits + 1}b, the rest {w.key_bits}b)"
     else:
@@ -58,7 +61,7 @@ def workload_name(w) -> str:
             f"values {w.value_bits}b, {kind}, page 16, fp16 window {w.window}")
 
 
-DEFAULT_LAYERS = {"qwen": 4, "llama": 4, "long": 8, "mixed": 4}  # resident layer caches: far above L2
+DEFAULT_LAYERS = {"qwen": 4, "llama": 4, "long": 8, "mixed": 4, "kivi": 4}  # resident layer caches: far above L2
 
 
 def parse():
@@ -67,7 +70,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
-    ap.add_argument("--workload", default="qwen", choices=["qwen", "llama", "long", "mixed"],
+    ap.add_argument("--workload", default="qwen", choices=["qwen", "llama", "long", "mixed", "kivi"],
                     help="decode configuration (default: the Qwen-like headline workload)")
     ap.add_argument("--layers", type=int, default=0, help="resident layer caches rotated over (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -87,6 +90,8 @@ def record_bytes(d, kb, qjl, vb, split=0, norm_u8=False):
 
 
 def workload_records(w):
+    if w.kivi:  # key scale and zero per channel shared by a page's 16 tokens; value scale and zero per token
+        return w.d // 4 + w.key_bits * w.d // 8, 4 + w.value_bits * w.d // 8
     return record_bytes(w.d, w.key_bits, w.key_qjl, w.value_bits, w.key_split, w.key_norm_range is not None)
 
 
@@ -226,10 +231,17 @@ def oracle_sample_setup(name="qwen"):
            "qjl_s": [OT.build_transform(w.kind, d, 0, 0, 0, 2)] if corr == 1 else None}
     K, V = kv["K"][0, :, 0], kv["V"][0, :, 0]
     S = {"prm": prm, "kind": w.kind, "k_cb": kcb, "v_cb": vcb, "norm_range": w.key_norm_range}
-    kr = oracle_keys(S, K[:nc])
-    vr = OC.quantize_mse(V[:nc], w.kind, prm["v_rot"][0], vcb)
-    comp = {"knorm": kr["norm"][None], "krnorm": kr["rnorm"][None], "kidx": kr["idx"][None],
-            "ksigns": kr["signs"][None], "vnorm": vr["norm"][None], "vidx": vr["idx"][None]}
+    if w.kivi:  # the control arm: dequantized pages, attention over them and the window
+        from oracle import kivi as OKV
+
+        S["kivi"] = (OKV.dequantize_keys(OKV.quantize_keys(K[:nc], w.key_bits))[None],
+                     OKV.dequantize_values(OKV.quantize_values(V[:nc], w.value_bits))[None])
+        comp = None
+    else:
+        kr = oracle_keys(S, K[:nc])
+        vr = OC.quantize_mse(V[:nc], w.kind, prm["v_rot"][0], vcb)
+        comp = {"knorm": kr["norm"][None], "krnorm": kr["rnorm"][None], "kidx": kr["idx"][None],
+                "ksigns": kr["signs"][None], "vnorm": vr["norm"][None], "vidx": vr["idx"][None]}
     win_k = K[nc:].astype(np.float16)[None]
     win_v = V[nc:].astype(np.float16)[None]
     q = kv["q"][0, :G]
@@ -275,6 +287,10 @@ def oracle_step(S):
         wk = np.concatenate([S["win_k"][:, 1:], nk], axis=1)
         wv = np.concatenate([S["win_v"][:, 1:], nv], axis=1)
         comp = S["comp"]
+        if "kivi" in S:
+            from oracle import kivi as OKV
+
+            return OKV.decode_one(S["q"], S["kivi"][0], S["kivi"][1], wk, wv, 1.0 / math.sqrt(S["d"]))
     else:
         # no window: the new token is quantized into its page slot
         prm = S["prm"]
@@ -440,7 +456,7 @@ def run_gpu(args):
     layers, caches, qs, news = [], [], [], []
     for l in range(args.layers):
         L = tq.TQLayer(d, Hkv, Hq, w.key_bits, w.value_bits, w.kind, window=W, key_qjl=w.key_qjl, seed=w.seed,
-                       layer=l, key_split=w.key_split, key_norm_range=w.key_norm_range)
+                       layer=l, key_split=w.key_split, key_norm_range=w.key_norm_range, kivi=w.kivi)
         pc = tq.PagedCache(L, B, max_ctx)
         K, V, q = SK.keys_values_torch(w, layer=l, ctx=T0 + per_layer)
         pc.prefill(K[:, :T0], V[:, :T0])
@@ -542,7 +558,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch Philox on the device)",
         "config": {"workload": workload_name(w), "batch": B, "ctx": T0, "kv_heads": Hkv, "q_heads": Hq, "d": d,
-                   "key_bits": w.key_bits + (0.5 if w.key_split else (1 if int(w.key_qjl) == 1 else 0)),
+                   "key_bits": w.key_bits + (0.5 if w.key_split else (1 if int(w.key_qjl) == 1 and not w.kivi else 0)),
                    "value_bits": w.value_bits, "window": W, "page": 16,
                    "layer_caches": args.layers, "l2": f"inputs larger than L2: {args.layers} rotating layer caches "
                    f"of {step_bytes(T0, W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs) / 1e6:.0f} MB",

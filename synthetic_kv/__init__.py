@@ -32,6 +32,9 @@ Workloads (the "configs" of the hot-path statement):
             < d/2 at 4 bits, the rest at 3), no residual sketch, byte
             log-norms over [2^0, 2^8] (N(0,1) keys of d = 256 have norms near
             2^4); values 3b; FWHT; fp16 window 128.
+  kivi      the qwen shape through the KIVI-like control arm of the design
+            study: 2-bit keys per channel (page groups) and 2-bit values per
+            token, float16 scale and zero, fp16 window 128; no rotation.
 """
 
 from __future__ import annotations
@@ -73,6 +76,7 @@ class Workload:
     key_split: int = 0     # mixed-channel key rate: the first d/2 rotated coordinates one bit wider
     key_norm_range: tuple | None = None  # (lo, hi): byte key norms, log2-uniform over [2^lo, 2^hi]
     qjl_structured: int = 0  # QJL sketch S = H diag(sigma_S) in place of a dense Gaussian
+    kivi: int = 0          # KIVI-like control arm (integer codes, key_bits / value_bits 2 or 4)
 
     @property
     def dh(self) -> int:
@@ -89,6 +93,7 @@ WORKLOADS = {
                      key_scale="lognormal", value_scale="lognormal", rope=False),
     "mixed": Workload("mixed", 8, 4, 24, 256, 32768, 3, 0, 3, FWHT, 128, "bf16", key_split=1,
                       key_norm_range=(0.0, 8.0)),
+    "kivi": Workload("kivi", 8, 4, 24, 256, 32768, 2, 0, 2, FWHT, 128, "bf16", kivi=1),
 }
 
 
