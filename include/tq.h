@@ -326,6 +326,30 @@ tq_status tq_decode_attention_static(const tq_layer_params* p, const tq_cache* c
                                      tq_dtype dtype, float scale, float* out, float* lse, float* scores,
                                      int max_ctx, int n_splits, tq_stream_t stream);
 
+/*
+ * tq_prefill_attention -- attention of a prefill chunk over the compressed
+ * cache ([Design study] §Transform placement and §Packed format: the chunk's
+ * queries are scored against the packed pages, not a decoded history; the
+ * second workload next to decode).  The chunk's n_query tokens are the last
+ * n_query tokens already appended to every sequence: query i of sequence b
+ * sits at position p = seq_len[b] - n_query + i and attends causally to the
+ * cached positions 0 .. p (compressed pages and the float16 window), with the
+ * same score and output rules as tq_decode_attention.  Each query runs as a
+ * virtual decode sequence of visible length p + 1 over its sequence's block
+ * table and window ring (one launch of the decode pipeline for all queries).
+ *   q         [device] [batch][n_query][Hq][head_dim] in dtype
+ *   out       [device] out, float [batch][n_query][Hq][head_dim]
+ *   lse       [device] out, float [batch][n_query][Hq] (nullable)
+ *   workspace [device] 256-byte aligned, >= tq_prefill_workspace_size bytes
+ *   max_ctx   upper bound of seq_len over the batch
+ * seq_len[b] < n_query sets TQ_DEVERR_SEQ_LEN (those queries see the tokens
+ * that exist).  batch * n_query <= 2^24.
+ */
+size_t tq_prefill_workspace_size(const tq_layer_params* p, int batch, int n_query, int max_ctx);
+tq_status tq_prefill_attention(const tq_layer_params* p, const tq_cache* cache, int n_query, const void* q,
+                               tq_dtype dtype, float scale, float* out, float* lse, void* workspace,
+                               size_t workspace_bytes, int max_ctx, tq_stream_t stream);
+
 /* Synchronises the stream, reads and clears the device error word.
  * Returns TQ_ERR_DEVICE_CHECK if any bit was set (bits in *bits_out, nullable). */
 tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_out);

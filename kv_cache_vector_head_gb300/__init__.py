@@ -16,11 +16,13 @@ import numpy as np
 from . import _lib
 from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_QJL_SIGNS, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
                    Cache, LayerParams, TQError, append_page, build_codebook, build_transform, check_device_error,
-                   decode_attention, decode_workspace_size, quantize_keys, quantize_values, subblock_bytes)
+                   decode_attention, decode_workspace_size, prefill_attention, prefill_workspace_size, quantize_keys,
+                   quantize_values, subblock_bytes)
 
 __all__ = [
     "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
     "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
+    "prefill_workspace_size", "prefill_attention",
     "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
     "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "ROLE_QJL_SIGNS", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
 ]

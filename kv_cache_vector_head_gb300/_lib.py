@@ -26,7 +26,7 @@ PAGE_SIZE = 16
 EXPORTED = [
     "tq_build_codebook", "tq_build_transform", "tq_quantize_keys", "tq_quantize_values", "tq_subblock_bytes",
     "tq_append_page", "tq_decode_workspace_size", "tq_decode_attention", "tq_check_device_error", "tq_last_error",
-    "tq_decode_attention_static",
+    "tq_decode_attention_static", "tq_prefill_workspace_size", "tq_prefill_attention",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -84,10 +84,15 @@ def lib():
                                           c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_int, c_void_p]
         L.tq_decode_attention_static.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_int, c_float,
                                                  c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]
+        L.tq_prefill_workspace_size.argtypes = [POINTER(LayerParams), c_int, c_int, c_int]
+        L.tq_prefill_workspace_size.restype = c_size_t
+        L.tq_prefill_attention.argtypes = [POINTER(LayerParams), POINTER(Cache), c_int, c_void_p, c_int, c_float,
+                                           c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_void_p]
         L.tq_check_device_error.argtypes = [c_void_p, POINTER(c_uint32)]
         L.tq_last_error.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("tq_subblock_bytes", "tq_decode_workspace_size", "tq_last_error"):
+            if name not in ("tq_subblock_bytes", "tq_decode_workspace_size", "tq_prefill_workspace_size",
+                            "tq_last_error"):
                 getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -177,6 +182,22 @@ def decode_attention_static(p: LayerParams, cache: Cache, q, scale: float, out, 
     """tq_decode_attention with the library's own static scratch (no workspace)."""
     _check(lib().tq_decode_attention_static(ctypes.byref(p), ctypes.byref(cache), _ptr(q), dtype_code(q), scale,
                                             _ptr(out), _ptr(lse), _ptr(scores), max_ctx, n_splits, _stream(stream)))
+
+
+def prefill_workspace_size(p: LayerParams, batch: int, n_query: int, max_ctx: int) -> int:
+    n = lib().tq_prefill_workspace_size(ctypes.byref(p), batch, n_query, max_ctx)
+    if n == 0:
+        _check(TQ_ERR_INVALID_ARG)
+    return n
+
+
+def prefill_attention(p: LayerParams, cache: Cache, n_query: int, q, scale: float, out, lse, workspace, max_ctx: int,
+                      stream=None) -> None:
+    """The last n_query appended tokens of every sequence attend causally to the cache:
+    q, out [batch, n_query, Hq, head_dim], lse [batch, n_query, Hq] (or None)."""
+    _check(lib().tq_prefill_attention(ctypes.byref(p), ctypes.byref(cache), n_query, _ptr(q), dtype_code(q), scale,
+                                      _ptr(out), _ptr(lse), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), max_ctx, _stream(stream)))
 
 
 def check_device_error(stream=None) -> int:

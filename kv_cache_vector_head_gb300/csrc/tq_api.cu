@@ -186,7 +186,16 @@ static tq_status make_cache(const tq_cache* c, const KParams& K, KCache* C, bool
   C->win_v = reinterpret_cast<__half*>(c->win_v);
   C->batch = c->batch;
   C->ring = K.window > 0 ? K.window + TQ_PAGE_SIZE : 0;
+  C->parent = nullptr;
   return TQ_OK;
+}
+
+// Prefill workspace: the virtual sequences' counters and parent rows, then a decode workspace
+// for batch * n_query sequences.
+static size_t prefill_layout(const KParams& K, int batch, int n_query, int max_ctx, WsLayout* L) {
+  const size_t head = ((size_t)3 * batch * n_query * sizeof(int32_t) + 255) & ~(size_t)255;
+  *L = decode_ws_layout(K, batch * n_query, max_ctx, 0, num_sms());
+  return head + L->total;
 }
 
 }  // namespace tq
@@ -288,6 +297,53 @@ extern "C" tq_status tq_decode_attention(const tq_layer_params* p, const tq_cach
   return cuda_status(launch_decode(K, C, q, dtype, scale, out, lse, scores, workspace, L, max_ctx,
                                    reinterpret_cast<cudaStream_t>(stream)),
                      "tq_decode_attention");
+}
+
+extern "C" size_t tq_prefill_workspace_size(const tq_layer_params* p, int batch, int n_query, int max_ctx) {
+  KParams K;
+  if (make_params(p, &K, false) != TQ_OK || batch < 1 || n_query < 1 || max_ctx < 0) return 0;
+  if ((long long)batch * n_query > (1LL << 24)) return 0;
+  clear_error();
+  WsLayout L;
+  return prefill_layout(K, batch, n_query, max_ctx, &L);
+}
+
+extern "C" tq_status tq_prefill_attention(const tq_layer_params* p, const tq_cache* cache, int n_query, const void* q,
+                                          tq_dtype dtype, float scale, float* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, int max_ctx, tq_stream_t stream) {
+  KParams K;
+  KCache C;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if ((s = make_cache(cache, K, &C, true)) != TQ_OK) return s;
+  if (n_query < 1 || (long long)cache->batch * n_query > (1LL << 24))
+    return fail(TQ_ERR_INVALID_ARG, "n_query must be >= 1 and batch * n_query <= 2^24");
+  if (!q || !out || !workspace) return fail(TQ_ERR_INVALID_ARG, "null q / out / workspace");
+  if (!aligned(workspace, 256)) return fail(TQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (max_ctx < 0) return fail(TQ_ERR_INVALID_ARG, "max_ctx must be >= 0");
+  if (!(scale == scale)) return fail(TQ_ERR_INVALID_ARG, "scale is NaN");
+  WsLayout L;
+  const size_t need = prefill_layout(K, cache->batch, n_query, max_ctx, &L);
+  if (workspace_bytes < need) {
+    set_error("workspace too small: %zu < %zu", workspace_bytes, need);
+    return TQ_ERR_CAPACITY;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nv = (size_t)cache->batch * n_query;
+  int32_t* seq_v = reinterpret_cast<int32_t*>(workspace);
+  int32_t* nc_v = seq_v + nv;
+  int32_t* parent = nc_v + nv;
+  unsigned char* dws = reinterpret_cast<unsigned char*>(workspace) + (need - L.total);
+  cudaError_t e = launch_prefill_virtual(C, n_query, seq_v, nc_v, parent, st);
+  if (e != cudaSuccess) return cuda_status(e, "tq_prefill_attention");
+  KCache V = C;
+  V.seq_len = seq_v;
+  V.n_compressed = nc_v;
+  V.parent = parent;
+  V.batch = (int)nv;
+  return cuda_status(launch_decode(K, V, q, dtype, scale, out, lse, nullptr, dws, L, max_ctx, st),
+                     "tq_prefill_attention");
 }
 
 extern "C" tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_out) {

@@ -355,6 +355,7 @@ __device__ void window_split(const KParams& P, const KCache& C, const void* q, i
   const int G = P.G;
   const int st = L.n_comp_splits + 1;
   const size_t head0 = (size_t)b * P.hq + (size_t)g * G;
+  const int cb = C.parent ? C.parent[b] : b;  // cache row of (virtual) sequence b
   int T = C.seq_len[b], nc = C.n_compressed[b];
   if (T < 0 || T > max_ctx || nc < 0 || nc > T) {
     if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
@@ -378,7 +379,7 @@ __device__ void window_split(const KParams& P, const KCache& C, const void* q, i
   float acc[TQ_MAX_GQA];
 #pragma unroll
   for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] = 0.f;
-  const size_t ring0 = ((size_t)b * P.hkv + g) * (size_t)C.ring;
+  const size_t ring0 = ((size_t)cb * P.hkv + g) * (size_t)C.ring;
   for (int c0 = 0; c0 < nw; c0 += kPage) {
     __syncthreads();
     constexpr int V16 = D / 8;  // 16-byte vectors per row
@@ -519,6 +520,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   unsigned char* stage0 = dyn + L.afrag_bytes_per_head;                        // [nst][NW][sub]
   long long* pids = reinterpret_cast<long long*>(stage0 + (size_t)nst * NW * sub);  // [<= kPidCache]
 
+  const int cb = C.parent ? C.parent[b] : b;  // cache row of (virtual) sequence b
   int T = C.seq_len[b], nc = C.n_compressed[b];
   if (T < 0 || T > max_ctx || nc < 0 || nc > T) {
     if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   const int ncache = min(npg, kPidCache);
 
   for (int i = tid; i < ncache; i += kMmaThreads) {
-    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
     if (pid < 0 || pid >= C.n_pages) {
       atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
       pid = -1;
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   auto page_id = [&](int i) -> long long {  // i = page index within the split
     if (i >= npg) return -1;
     if (i < ncache) return pids[i];
-    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
     if (pid < 0 || pid >= C.n_pages) {
       atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
       pid = -1;
@@ -1120,6 +1122,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
   unsigned char* stage0 = dyn;                                                     // [nst][NW][sub]
   long long* pids = reinterpret_cast<long long*>(stage0 + (size_t)nst * NW * sub);  // [<= kPidCache]
 
+  const int cb = C.parent ? C.parent[b] : b;  // cache row of (virtual) sequence b
   int T = C.seq_len[b], nc = C.n_compressed[b];
   if (T < 0 || T > max_ctx || nc < 0 || nc > T) {
     if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
@@ -1138,7 +1141,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
   const int ncache = min(npg, kPidCache);
 
   for (int i = tid; i < ncache; i += kMmaThreads) {
-    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
     if (pid < 0 || pid >= C.n_pages) {
       atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
       pid = -1;
@@ -1165,7 +1168,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
   auto page_id = [&](int i) -> long long {
     if (i >= npg) return -1;
     if (i < ncache) return pids[i];
-    long long pid = C.block_table[(size_t)b * C.max_pages + p0 + i];
+    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
     if (pid < 0 || pid >= C.n_pages) {
       atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
       pid = -1;
@@ -1449,6 +1452,29 @@ cudaError_t launch_decode(const KParams& P, const KCache& C, const void* q, int 
                           float* lse, float* scores, void* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
   if (P.d == 128) return launch_decode_d<128>(P, C, q, dtype, scale, out, lse, scores, ws, L, max_ctx, st);
   return launch_decode_d<256>(P, C, q, dtype, scale, out, lse, scores, ws, L, max_ctx, st);
+}
+
+__global__ void prefill_virtual_kernel(const __grid_constant__ KCache C, int n_query, int32_t* seq_v,
+                                       int32_t* nc_v, int32_t* parent) {
+  const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= (long long)C.batch * n_query) return;
+  const int b = (int)(v / n_query), i = (int)(v % n_query);
+  const int T = C.seq_len[b], nc = C.n_compressed[b];
+  int tv = T - n_query + i + 1;  // query i sees positions 0 .. T - n_query + i
+  if (T < n_query || nc < 0 || nc > T) {
+    if (i == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
+    tv = max(tv, 0);
+  }
+  seq_v[v] = tv;
+  nc_v[v] = min(max(nc, 0), tv);
+  parent[v] = b;
+}
+
+cudaError_t launch_prefill_virtual(const KCache& C, int n_query, int32_t* seq_v, int32_t* nc_v, int32_t* parent,
+                                   cudaStream_t st) {
+  const long long n = (long long)C.batch * n_query;
+  prefill_virtual_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(C, n_query, seq_v, nc_v, parent);
+  return cudaGetLastError();
 }
 
 cudaError_t read_clear_decode_error(unsigned* bits) {

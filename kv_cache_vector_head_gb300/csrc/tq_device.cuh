@@ -69,6 +69,9 @@ struct KCache {
   __half* win_v;
   int batch;
   int ring;                            // window + 16 (0 without window)
+  // prefill attention: row b of seq_len / n_compressed is a virtual sequence (one query of a
+  // chunk with its causal length) reading block-table row and window ring parent[b]; NULL = b
+  const int32_t* parent;
 };
 
 __device__ __forceinline__ float load_elem(const void* p, int dtype, long long i) {

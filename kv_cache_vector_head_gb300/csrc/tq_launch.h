@@ -28,6 +28,11 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
 cudaError_t launch_decode(const KParams& P, const KCache& C, const void* q, int dtype, float scale, float* out,
                           float* lse, float* scores, void* ws, const WsLayout& L, int max_ctx, cudaStream_t st);
 
+// Virtual sequences of a prefill chunk: query i of sequence b is row v = b n_query + i,
+// visible length seq_len[b] - n_query + i + 1, its compressed part clipped to it.
+cudaError_t launch_prefill_virtual(const KCache& C, int n_query, int32_t* seq_v, int32_t* nc_v, int32_t* parent,
+                                   cudaStream_t st);
+
 cudaError_t read_clear_quant_error(unsigned* bits);
 cudaError_t read_clear_decode_error(unsigned* bits);
 

@@ -134,3 +134,61 @@ def test_kivi_direct_append_needs_whole_pages(tq):
     assert tq.check_device_error() & 0x4  # flagged on the device, nothing written
     with pytest.raises(tq.TQError):
         tq.append_page(L.params, pc.cache, k[:15].contiguous(), k[:15].contiguous(), 15, slots[:15])
+
+
+def test_kivi_prefill_attention(tq):
+    """The last 40 appended tokens attend causally to a KIVI cache with a window."""
+    w = SK.workload("llama", batch=2, window=20, key_qjl=0, key_bits=2, value_bits=4)
+    T0, steps, nq = 60, 25, 40
+    T = T0 + steps
+    kv = SK.keys_values(w, ctx=T)
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, 2, 4, w.kind, window=20, key_qjl=0, seed=w.seed, kivi=True)
+    pc = tq.PagedCache(L, w.batch, T)
+    kt = SK.to_torch(kv["K"], w.dtype).cuda()
+    vt = SK.to_torch(kv["V"], w.dtype).cuda()
+    pc.prefill(kt[:, :T0], vt[:, :T0])
+    for t in range(T0, T):
+        pc.append(kt[:, t].contiguous(), vt[:, t].contiguous())
+    rng = np.random.default_rng(5)
+    qt = SK.to_torch(rng.standard_normal((w.batch, nq, w.n_q_heads, w.d)), w.dtype).cuda()
+    q = qt.float().cpu().numpy().astype(np.float64)
+    scale = 1.0 / math.sqrt(w.d)
+    ws = torch.empty(tq.prefill_workspace_size(L.params, w.batch, nq, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.batch, nq, w.n_q_heads, w.d, device="cuda")
+    lse = torch.zeros(w.batch, nq, w.n_q_heads, device="cuda")
+    tq.prefill_attention(L.params, pc.cache, nq, qt, scale, out, lse, ws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    nc0 = 16 * (max(0, T0 - 20) // 16)
+    nc = 16 * (max(0, T - 20) // 16)
+    pool = pc.pool.cpu().numpy()
+    bt = pc.block_table.cpu().numpy()
+    lay = OKV.subblock_layout(w.d, 2, 4)
+    stats = {"exempt": 0, "codes": 0}
+    for b in range(w.batch):
+        Kh, Vh = [], []
+        for h in range(w.n_kv_heads):
+            K = kv["K"][b, :nc, h].copy()
+            V = kv["V"][b, :nc, h].copy()
+            K[nc0:] = K[nc0:].astype(np.float16).astype(np.float64)
+            V[nc0:] = V[nc0:].astype(np.float16).astype(np.float64)
+            kh, vh = [], []
+            for p in range(nc // 16):
+                g = OKV.read_page(pool, lay, w.n_kv_heads, int(bt[b, p]), h, w.d, 2, 4)
+                ok = OKV.quantize_key_page(K[16 * p:16 * p + 16], 2)
+                ov = OKV.quantize_values(V[16 * p:16 * p + 16], 4)
+                kh.append(OKV.dequantize(_compare_codes(g["kcodes"], ok, stats), ok["scale"][None, :],
+                                         ok["zero"][None, :]))
+                vh.append(OKV.dequantize(_compare_codes(g["vcodes"], ov, stats), ov["scale"][:, None],
+                                         ov["zero"][:, None]))
+            Kh.append(np.concatenate(kh))
+            Vh.append(np.concatenate(vh))
+        Kh, Vh = np.stack(Kh), np.stack(Vh)
+        for i in range(nq):
+            Ti = T - nq + i + 1
+            nci = min(nc, Ti)
+            wk = kv["K"][b, nc:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nc else None
+            wv = kv["V"][b, nc:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nc else None
+            r = OKV.decode_one(q[b, i], Kh[:, :nci], Vh[:, :nci], wk, wv, scale)
+            assert np.abs(out[b, i].cpu().numpy() - r["out"]).max() < 2e-3, (b, i)
+            assert np.abs(lse[b, i].cpu().numpy() - r["lse"]).max() < 1e-3, (b, i)

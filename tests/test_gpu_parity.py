@@ -393,3 +393,64 @@ def test_direct_slot_append_with_skips(tq):
                                pg["krnorm"][sl: sl + 1], True)
             subv = {k: v[t: t + 1] for k, v in ov.items() if isinstance(v, np.ndarray) and v.shape[:1] == (40,)}
             PY.compare_records(subv, pg["vidx"][sl: sl + 1], pg["vnorm"][sl: sl + 1], is_key=False)
+
+
+def _trunc(rec, n_all, n):
+    """The first n token records of an oracle record dict holding n_all tokens."""
+    return {k: (v[:n] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == n_all else v)
+            for k, v in rec.items()}
+
+
+PREFILL = [
+    # window with flushes; the chunk straddles the compressed frontier
+    ("qwen", dict(batch=2, window=20), 75, 30, 40),
+    # no window: partial pages; EDEN keys; structured sketch; mixed keys with byte norms
+    ("llama", dict(batch=3), 33, 18, 20),
+    ("tiny", dict(key_qjl=2), 37, 12, 49),
+    ("llama", dict(batch=2, kind=SK.FWHT, qjl_structured=1), 40, 9, 16),
+    ("mixed", dict(batch=1, window=20), 61, 20, 33),
+]
+
+
+@pytest.mark.parametrize("name,over,T0,steps,nq", PREFILL)
+def test_prefill_attention_parity(tq, name, over, T0, steps, nq):
+    """The last nq appended tokens attend causally to the cache: query i at position
+    p = T - nq + i against the oracle's decode over positions 0..p."""
+    w = SK.workload(name, **over)
+    kv, L, O, pc = _paged_roundtrip(tq, w, T0, steps)
+    T = T0 + steps
+    nc0 = 16 * (max(0, T0 - w.window) // 16)
+    ref = _oracle_cache(w, O, kv, T, nc0 if w.window > 0 else T)
+    pool = pc.pool.cpu().numpy()
+    bt = pc.block_table.cpu().numpy()
+    rng = np.random.default_rng(1234)
+    qt = SK.to_torch(rng.standard_normal((w.batch, nq, w.n_q_heads, w.dh)), w.dtype).cuda()
+    q = qt.float().cpu().numpy().astype(np.float64)
+    scale = 1.0 / math.sqrt(w.dh)
+    ws = torch.empty(tq.prefill_workspace_size(L.params, w.batch, nq, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.batch, nq, w.n_q_heads, w.dh, device="cuda")
+    lse = torch.zeros(w.batch, nq, w.n_q_heads, device="cuda")
+    tq.prefill_attention(L.params, pc.cache, nq, qt, scale, out, lse, ws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    g_out, g_lse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(w.batch):
+        recs_k, recs_v, _, _, nc = ref[b]
+        npg = (nc + 15) // 16
+        for h in range(w.n_kv_heads):
+            if nc:
+                pages = [PY.read_pool(pool, O, int(bt[b, p]), h) for p in range(npg)]
+                cat = {k: np.concatenate([pg[k] for pg in pages])[:nc] for k in pages[0]}
+                recs_k[h] = PY.adopt_exempt(recs_k[h], cat["kidx"], cat.get("ksigns"), cat.get("krnorm"),
+                                            cat.get("knorm_code"), w.key_norm_range)
+                recs_v[h] = PY.adopt_exempt(recs_v[h], cat["vidx"])
+        for i in range(nq):
+            Ti = T - nq + i + 1
+            nci = min(nc, Ti)
+            comp = (PY.stack_comp([_trunc(r, nc, nci) for r in recs_k], [_trunc(r, nc, nci) for r in recs_v])
+                    if nci else None)
+            wk = kv["K"][b, nc:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nc else None
+            wv = kv["V"][b, nc:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nc else None
+            r = PY.decode_reference(O, q[b, i], comp, wk, wv, scale)
+            assert np.abs(g_out[b, i] - r["out"]).max() < PY.OUT_ATOL, (b, i)
+            assert np.abs(g_lse[b, i] - r["lse"]).max() < PY.SCORE_ATOL, (b, i)
