@@ -404,6 +404,33 @@ def bench_quantize(tq, torch, n=1 << 20):
     return out
 
 
+def bench_prefill(tq, torch, L, pc, w, recs, nq=64, calls=5):
+    """Prefill attention: the last nq appended tokens of every sequence of one layer
+    cache attend causally to it (one launch of the decode pipeline over batch x nq
+    virtual sequences).  Algorithmic bytes: every query's visible records, window,
+    q and output, as for a decode call of its length."""
+    B, Hkv, Hq, d, W = w.batch, w.n_kv_heads, w.n_q_heads, w.d, w.window
+    T = int(pc.seq_len[0].item())
+    q = torch.randn(B, nq, Hq, d, device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(tq.prefill_workspace_size(L.params, B, nq, T), dtype=torch.uint8, device="cuda")
+    out = torch.empty(B, nq, Hq, d, device="cuda")
+    for _ in range(2):
+        tq.prefill_attention(L.params, pc.cache, nq, q, 1.0 / math.sqrt(d), out, None, ws, T)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record()
+    for _ in range(calls):
+        tq.prefill_attention(L.params, pc.cache, nq, q, 1.0 / math.sqrt(d), out, None, ws, T)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / calls
+    nbytes = sum(decode_bytes(T - nq + i + 1, W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs)
+                 for i in range(nq))
+    return {"n_query": nq, "ctx": T, "ms": ms, "query_tokens_per_s": B * nq / (ms * 1e-3),
+            "visible_GB_per_s": nbytes / (ms * 1e-3) / 1e9,
+            "note": "each query re-reads its visible pages (L2-resident across a sequence's queries)"}
+
+
 def bench_append_batch256(tq, torch, steps=200):
     """Decode-step append latency: 256 sequences x 8 KV heads, d = 128, keys 3b + QJL,
     values 4b, dense Pi, no window, into partially filled pages (37 tokens each at
@@ -538,6 +565,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms)
+    pre = bench_prefill(tq, torch, layers[0], caches[0], w, recs)
     quant = bench_quantize(tq, torch)
     app = bench_append_batch256(tq, torch)
     if rank != 0:
@@ -573,6 +601,7 @@ def run_gpu(args):
                      "fwht_structured_sketch": dict(quant["fwht_structured_sketch"],
                                                     hbm_fraction=quant["fwht_structured_sketch"]["GB_per_s"] / peak)},
         "append_batch256": app,
+        "prefill": pre,
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
                 "d2h_bytes_per_step": int(hout.numel() * 4)},
