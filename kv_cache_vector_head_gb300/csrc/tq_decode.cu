@@ -164,6 +164,28 @@ __device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t 
 // value token slot s of a page pair: position 10 + (s & 1) for s < 8, 14 + (s & 1) above
 __host__ __device__ constexpr int xpos_val(int s) { return (s < 8 ? 10 : 14) + (s & 1); }
 
+// N adjacent 16-bit entries (N = 2 or 4, 4N-byte aligned) in one shared-memory load.
+template <int N>
+__device__ __forceinline__ void vload_u16(uint16_t (&out)[N], const uint16_t* p) {
+  if (N == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    out[0] = (uint16_t)(v.x & 0xffffu);
+    out[1] = (uint16_t)(v.x >> 16);
+    out[N > 2 ? 2 : 0] = (uint16_t)(v.y & 0xffffu);
+    out[N > 3 ? 3 : 0] = (uint16_t)(v.y >> 16);
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    out[0] = (uint16_t)(v & 0xffffu);
+    out[N > 1 ? 1 : 0] = (uint16_t)(v >> 16);
+  }
+}
+// N adjacent floats (N = 2 or 4, 4N-byte aligned) in one global store.
+template <int N>
+__device__ __forceinline__ void vstore_f32(float* p, const float (&v)[N]) {
+  if (N == 4) *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[N > 2 ? 2 : 0], v[N > 3 ? 3 : 0]);
+  else *reinterpret_cast<float2*>(p) = make_float2(v[0], v[N > 1 ? 1 : 0]);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
@@ -488,7 +510,9 @@ struct MmaShared {
 };
 
 // KMIX: the layer uses mixed-channel keys or byte key norms (compiled out otherwise).
-template <int D, bool VLUT, bool KMIX>
+// KPF > 0: TurboQuant_prod keys (QJL sketch) with KPF Walsh planes, fixed at compile time
+// (kp = 2 for 2-bit codes, 4 for 3-bit); KPF = 0 reads the plane count and correction at run time.
+template <int D, bool VLUT, bool KMIX, int KPF>
 __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ KCache C, const void* q,
                                                                  int dtype, float scale, float* scores,
@@ -514,6 +538,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   const int sub = P.sub_bytes;
   const uint32_t xb1 = P.xb1, xb2 = P.xb2;
   const bool ksplit = KMIX && P.ksplit, knu8 = KMIX && P.knu8;
+  const int kp = KPF > 0 ? KPF : P.kp;
+  const int kqjl = KPF > 0 ? (int)TQ_KEY_QJL : P.kqjl;
+  const int kbits = KPF > 0 ? (KPF == 2 ? 2 : 3) : P.kb;
+  constexpr int kUnrollS = KPF > 0 ? KPF : 1;
+  auto pbase = [&](int S) { return ksplit ? frag_plane_base(P, S, KS) : S * KS; };
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -603,12 +632,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   if (warp < G) {
     // K of head `warp`: its A-fragment rows (lanes 4 warp .. 4 warp + 3) over all stored planes and
     // k-blocks; register r of block kk pairs with key bit 2 (kk mod 8) + (r >= 2)
-    const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
+    const int nplanes = kp + (kqjl == TQ_KEY_QJL ? 1 : 0);
     float km = 0.f, kq = 0.f;
     for (int it = lane; it < nplanes * KS * 4; it += 32) {
       const int pl = it / (KS * 4), kk = (it / 4) % KS, t4i = it % 4;
-      if (ksplit && pl >= P.kp / 2 && kk >= KS / 2) continue;  // not stored: zero operand
-      const uint4 a = afr[(frag_plane_base(P, pl, KS) + kk) * 32 + warp * 4 + t4i];
+      if (ksplit && pl >= kp / 2 && kk >= KS / 2) continue;  // not stored: zero operand
+      const uint4 a = afr[(pbase(pl) + kk) * 32 + warp * 4 + t4i];
       const uint32_t rr[4] = {a.x, a.y, a.z, a.w};
       float sum = 0.f;
 #pragma unroll
@@ -617,7 +646,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
         sum += f * (__half2float(__ushort_as_half((unsigned short)(rr[r] & 0xffffu))) +
                     __half2float(__ushort_as_half((unsigned short)(rr[r] >> 16))));
       }
-      if (pl < P.kp) km += sum;
+      if (pl < kp) km += sum;
       else kq += sum;
     }
     km = warp_sum_f(km);
@@ -677,12 +706,13 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             rs[nt][jw] = kc[tk * E + w];
 #pragma unroll
             for (int m = 0; m < 3; ++m)
-              rm[m][nt][jw] = (m + 1 < P.kb)                                 ? kc[((m + 1) * kPage + tk) * E + w]
-                              : (ksplit && m + 1 == P.kb && w < E / 2) ? kx[tk * (E / 2) + w]
-                                                                           : 0u;
+              rm[m][nt][jw] = (m + 1 < kbits)                                 ? kc[((m + 1) * kPage + tk) * E + w]
+                              : (ksplit && m + 1 == kbits && w < E / 2) ? kx[tk * (E / 2) + w]
+                                                                          : 0u;
           }
         // planes over all k-steps; mixed-channel keys: the planes holding the top bit follow
-        const int s_full = ksplit ? P.kp / 2 : P.kp;
+        const int s_full = ksplit ? kp / 2 : kp;
+#pragma unroll kUnrollS
         for (int S = 0; S < s_full; ++S) {
           uint32_t w0[2][WPL], w6[2][WPL], w10[2][WPL];
 #pragma unroll
@@ -694,7 +724,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
               w6[nt][jw] = w0[nt][jw] << 6;
               w10[nt][jw] = w0[nt][jw] << 10;
             }
-          const uint4* ap = afr + (size_t)frag_plane_base(P, S, KS) * 32 + lane;
+          const uint4* ap = afr + (size_t)pbase(S) * 32 + lane;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const uint4 a = ap[kk * 32];
@@ -719,11 +749,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
               hs[nt] = kc[tk * E + w] >> sh;
 #pragma unroll
               for (int m = 0; m < 3; ++m)
-                hm[m][nt] = ((m + 1 < P.kb) ? kc[((m + 1) * kPage + tk) * E + w]
-                                            : (m + 1 == P.kb) ? kx[tk * (E / 2) + w] : 0u) >> sh;
+                hm[m][nt] = ((m + 1 < kbits) ? kc[((m + 1) * kPage + tk) * E + w]
+                                             : (m + 1 == kbits) ? kx[tk * (E / 2) + w] : 0u) >> sh;
             }
           }
-          for (int S = P.kp / 2; S < P.kp; ++S) {
+          for (int S = kp / 2; S < kp; ++S) {
             uint32_t w0[2], w6[2], w10[2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -743,7 +773,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             }
           }
         }
-        if (P.kqjl == TQ_KEY_QJL) {
+        if (kqjl == TQ_KEY_QJL) {
           const uint32_t* ks = reinterpret_cast<const uint32_t*>(pb + P.off_ksigns);
           uint32_t q0[2][WPL], q6[2][WPL], q10[2][WPL];
 #pragma unroll
@@ -754,7 +784,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
               q6[nt][jw] = q0[nt][jw] << 6;
               q10[nt][jw] = q0[nt][jw] << 10;
             }
-          const uint4* ap = afr + (size_t)P.kp * KS * 32 + lane;
+          const uint4* ap = afr + (size_t)kp * KS * 32 + lane;
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             const uint4 a = ap[kk * 32];
@@ -781,13 +811,13 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             // +-1 plane sums from the operand sums: 2 D - K
             const float mse =
                 2.f * (accm[0][nt][e] + accm[0][nt][e + 2] + accm[1][nt][e] + accm[1][nt][e + 2]) - sh.kcon[0][g8];
-            const float qj = P.kqjl == TQ_KEY_QJL
+            const float qj = kqjl == TQ_KEY_QJL
                                  ? 2.f * (accq[0][nt][e] + accq[0][nt][e + 2] + accq[1][nt][e] + accq[1][nt][e + 2]) -
                                        sh.kcon[1][g8]
                                  : 0.f;
             // QJL: gamma times the sketch term; EDEN / renormalized keys: the scale s on the code's term
-            const float gm = P.kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
-            const float sk = P.kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
+            const float gm = kqjl == TQ_KEY_QJL ? krn[t] : 0.f;
+            const float sk = kqjl >= TQ_KEY_EDEN ? krn[t] : 1.f;
             const float kn = knu8 ? norm_u8_decode(pb[P.off_knorm + t], P) : knorm[t];
             l = scale * kn * (sk * (mse * inv_sqrt_d) + kappa * gm * qj);
             if (scores) scores[(head0 + g8) * (size_t)max_ctx + tok] = l;
@@ -860,12 +890,23 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       if (!VLUT) {
         // plane words (token slot s <-> bit s of each half), shifted so that slots 2 t4 + e sit at
         // positions 10 + e (k-step 0) and slots 8 + 2 t4 + e at 14 + e (k-step 1)
+        // column g8 of n-tile cbk is coordinate warp * CPW + g8 * CB + cbk: a lane's CB entries of a
+        // plane are adjacent (one vector load per page and plane)
         uint32_t u0[CB], u1[CB];
+        {
+          const int c0 = warp * CPW + g8 * CB;
+          uint16_t a0[CB], b0[CB], a1[CB], b1[CB];
+          vload_u16<CB>(a0, va + c0);
+          vload_u16<CB>(b0, vbp + c0);
+          if (P.vb == 2) {
+            vload_u16<CB>(a1, va + D + c0);
+            vload_u16<CB>(b1, vbp + D + c0);
+          }
 #pragma unroll
-        for (int cbk = 0; cbk < CB; ++cbk) {
-          const int c = warp * CPW + cbk * 8 + g8;
-          u0[cbk] = (uint32_t)va[c] | ((uint32_t)vbp[c] << 16);
-          u1[cbk] = P.vb == 2 ? (u0[cbk] ^ ((uint32_t)va[D + c] | ((uint32_t)vbp[D + c] << 16))) : 0u;
+          for (int cbk = 0; cbk < CB; ++cbk) {
+            u0[cbk] = (uint32_t)a0[cbk] | ((uint32_t)b0[cbk] << 16);
+            u1[cbk] = P.vb == 2 ? (u0[cbk] ^ ((uint32_t)a1[cbk] | ((uint32_t)b1[cbk] << 16))) : 0u;
+          }
         }
 #pragma unroll
         for (int ksx = 0; ksx < 2; ++ksx) {
@@ -889,7 +930,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       } else {
 #pragma unroll
         for (int cbk = 0; cbk < CB; ++cbk) {
-          const int c = warp * CPW + cbk * 8 + g8;
+          const int c = warp * CPW + g8 * CB + cbk;
           uint32_t u[TQ_MAX_BITS];
 #pragma unroll
           for (int p = 0; p < TQ_MAX_BITS; ++p)
@@ -945,17 +986,19 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       for (int w = 0; w < NW; ++w) kv += sh.kvsum[w][g8];
     }
     const float pm = VLUT ? 1.f : 2.f;
+    // columns 2 t4 and 2 t4 + 1 of n-tile cbk are coordinates warp * CPW + (2 t4) CB + cbk and
+    // warp * CPW + (2 t4 + 1) CB + cbk: CB adjacent coordinates each, one vector store apiece
+    float v0[CB], v1[CB];
 #pragma unroll
     for (int cbk = 0; cbk < CB; ++cbk) {
-      const int c = warp * CPW + cbk * 8 + 2 * t4;
-      const float v0 = c0 * (pm * (accv[0][cbk][0] + accv[0][cbk][2]) - kv) +
-                       c1 * (pm * (accv[1][cbk][0] + accv[1][cbk][2]) - kv);
-      const float v1 = c0 * (pm * (accv[0][cbk][1] + accv[0][cbk][3]) - kv) +
-                       c1 * (pm * (accv[1][cbk][1] + accv[1][cbk][3]) - kv);
-      float* dst = acc + ((head0 + g8) * st + s) * D + c;
-      dst[0] = v0;
-      dst[1] = v1;
+      v0[cbk] = c0 * (pm * (accv[0][cbk][0] + accv[0][cbk][2]) - kv) +
+                c1 * (pm * (accv[1][cbk][0] + accv[1][cbk][2]) - kv);
+      v1[cbk] = c0 * (pm * (accv[0][cbk][1] + accv[0][cbk][3]) - kv) +
+                c1 * (pm * (accv[1][cbk][1] + accv[1][cbk][3]) - kv);
     }
+    float* dst = acc + ((head0 + g8) * st + s) * D + warp * CPW + 2 * t4 * CB;
+    vstore_f32<CB>(dst, v0);
+    vstore_f32<CB>(dst + CB, v1);
   }
   if (tid < G) {
     float l = 0.f;
@@ -1348,7 +1391,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
 
 // ------------------------------------------------------------------ launcher
 
-template <int D, bool VLUT, bool KMIX>
+template <int D, bool VLUT, bool KMIX, int KPF>
 static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, int dtype, float scale,
                               float* scores, unsigned char* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
   const size_t pid_bytes = (size_t)std::min(L.pages_per_split, kPidCache) * sizeof(long long);
@@ -1360,7 +1403,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
     dyn = L.afrag_bytes_per_head + nst * stage_bytes + pid_bytes;
   }
   dyn = std::max(dyn, window_smem_bytes(D));
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT, KMIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, VLUT, KMIX, KPF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dyn);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the grid may start while the prologue runs
@@ -1375,7 +1418,7 @@ static cudaError_t launch_mma(const KParams& P, const KCache& C, const void* q, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, VLUT, KMIX>, P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, VLUT, KMIX, KPF>, P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1432,12 +1475,18 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, C.batch);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const bool kmix = P.ksplit || P.knu8;
+  // TurboQuant_prod keys with 2 or 3 code bits: plane count and sketch fixed at compile time
+  const int kpf = (!kmix && P.kqjl == TQ_KEY_QJL && (P.kp == 2 || P.kp == 4)) ? P.kp : 0;
   if (P.vb >= 3)
-    e = kmix ? launch_mma<D, true, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
-             : launch_mma<D, true, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
+    e = kmix       ? launch_mma<D, true, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kpf == 2 ? launch_mma<D, true, false, 2>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kpf == 4 ? launch_mma<D, true, false, 4>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+                   : launch_mma<D, true, false, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
   else
-    e = kmix ? launch_mma<D, false, true>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
-             : launch_mma<D, false, false>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
+    e = kmix       ? launch_mma<D, false, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kpf == 2 ? launch_mma<D, false, false, 2>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kpf == 4 ? launch_mma<D, false, false, 4>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+                   : launch_mma<D, false, false, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
   if (e != cudaSuccess) return e;
   const size_t cdyn = (size_t)(L.n_comp_splits + 1) * sizeof(float);
   if (cdyn > 48 * 1024) {
