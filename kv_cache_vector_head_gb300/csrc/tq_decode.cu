@@ -511,7 +511,8 @@ struct MmaShared {
 
 // KMIX: the layer uses mixed-channel keys or byte key norms (compiled out otherwise).
 // KPF > 0: TurboQuant_prod keys (QJL sketch) with KPF Walsh planes, fixed at compile time
-// (kp = 2 for 2-bit codes, 4 for 3-bit); KPF = 0 reads the plane count and correction at run time.
+// (kp = 2 for 2-bit codes, 4 for 3-bit), values of 2 bits or more (2-bit planes when !VLUT);
+// KPF = 0 reads the plane count, correction and value bits at run time.
 template <int D, bool VLUT, bool KMIX, int KPF>
 __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ KCache C, const void* q,
@@ -543,6 +544,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   const int kbits = KPF > 0 ? (KPF == 2 ? 2 : 3) : P.kb;
   constexpr int kUnrollS = KPF > 0 ? KPF : 1;
   auto pbase = [&](int S) { return ksplit ? frag_plane_base(P, S, KS) : S * KS; };
+  const bool vb2 = (KPF > 0 && !VLUT) ? true : P.vb == 2;  // the specialised variants carry 2-bit planes
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -898,14 +900,14 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
           uint16_t a0[CB], b0[CB], a1[CB], b1[CB];
           vload_u16<CB>(a0, va + c0);
           vload_u16<CB>(b0, vbp + c0);
-          if (P.vb == 2) {
+          if (vb2) {
             vload_u16<CB>(a1, va + D + c0);
             vload_u16<CB>(b1, vbp + D + c0);
           }
 #pragma unroll
           for (int cbk = 0; cbk < CB; ++cbk) {
             u0[cbk] = (uint32_t)a0[cbk] | ((uint32_t)b0[cbk] << 16);
-            u1[cbk] = P.vb == 2 ? (u0[cbk] ^ ((uint32_t)a1[cbk] | ((uint32_t)b1[cbk] << 16))) : 0u;
+            u1[cbk] = vb2 ? (u0[cbk] ^ ((uint32_t)a1[cbk] | ((uint32_t)b1[cbk] << 16))) : 0u;
           }
         }
 #pragma unroll
@@ -918,7 +920,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             mma16816(accv[0][cbk], wfk, (x & (0x00010001u << pa)) ^ (ksx ? xb2 : xb1),
                      (x & (0x00010001u << (pa + 1))) ^ xb1);
           }
-          if (P.vb == 2) {
+          if (vb2) {
 #pragma unroll
             for (int cbk = 0; cbk < CB; ++cbk) {
               const uint32_t x = u1[cbk] << sft;
@@ -978,7 +980,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   if (g8 < G) {
     // acc_rot[h][c] = sum over planes of coefficient x (hi-limb row + lo-limb row)
     const float c0 = VLUT ? 1.f : P.avw[0];
-    const float c1 = VLUT ? 1.f : (P.vb == 2 ? P.avw[1] : 0.f);
+    const float c1 = VLUT ? 1.f : (vb2 ? P.avw[1] : 0.f);
     // +-1 value planes: 2 D - K with K summed over every warp's tokens (the LUT limbs need no correction)
     float kv = 0.f;
     if (!VLUT) {
@@ -1476,7 +1478,7 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const bool kmix = P.ksplit || P.knu8;
   // TurboQuant_prod keys with 2 or 3 code bits: plane count and sketch fixed at compile time
-  const int kpf = (!kmix && P.kqjl == TQ_KEY_QJL && (P.kp == 2 || P.kp == 4)) ? P.kp : 0;
+  const int kpf = (!kmix && P.kqjl == TQ_KEY_QJL && (P.kp == 2 || P.kp == 4) && P.vb >= 2) ? P.kp : 0;
   if (P.vb >= 3)
     e = kmix       ? launch_mma<D, true, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
         : kpf == 2 ? launch_mma<D, true, false, 2>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)

@@ -187,3 +187,21 @@ def test_kivi_layout_and_checks(L):
     p.head_dim = 0
     # flat quantize does not apply to the KIVI arm (checked before any pointer)
     assert lib.tq_quantize_keys(ctypes.byref(p), None, 1, 16, None, None, None, None, None) == L.TQ_ERR_UNSUPPORTED
+
+
+def test_prefill_workspace_and_checks(L):
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = 128, 2, 8, 16, 16
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 2, 2, 1, L.TQ_FWHT
+    lib = L.lib()
+    # the prefill workspace holds a decode workspace for batch * n_query virtual sequences plus
+    # three int32 counters a query, 256-byte aligned
+    w = lib.tq_prefill_workspace_size(ctypes.byref(p), 3, 5, 100)
+    d = lib.tq_decode_workspace_size(ctypes.byref(p), 15, 100, 0)
+    assert w == d + ((3 * 15 * 4 + 255) // 256) * 256
+    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 3, 0, 100) == 0
+    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 1 << 13, 1 << 12, 100) == 0  # > 2^24 queries
+    c = L.Cache()
+    st = lib.tq_prefill_attention(ctypes.byref(p), ctypes.byref(c), 4, None, 1, ctypes.c_float(1.0), None, None,
+                                  None, 0, 100, None)
+    assert st == L.TQ_ERR_INVALID_ARG  # null transforms (checked before anything touches the GPU)
