@@ -33,7 +33,7 @@
 // relative query rounding instead of f16's 2^-11.
 //
 // Launches per call:
-//   decode_prologue_kernel  grid (Hkv, ceil(batch G / 4), d / 64): q' = Pi q,
+//   decode_prologue_kernel  grid (Hkv, ceil(batch G / 2), d / 64): q' = Pi q,
 //                           q'' = S q' (64 rows of S per CTA) and the query
 //                           rows of the score operands in mma fragment order;
 //                           the decode kernel is launched as its programmatic
@@ -64,7 +64,7 @@ constexpr int kMmaThreads = 256;
 constexpr int kMmaPages = kMmaThreads / 32;  // pages per chunk: one per warp in the key phase
 constexpr int kStages = 3;
 constexpr int kCombThreads = 256;
-constexpr int kPrologueTile = 4;  // query vectors per prologue CTA (more CTAs, shorter walks)
+constexpr int kPrologueTile = 2;  // query vectors per prologue CTA (measured best of 1, 2, 4: shortest critical path)
 constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -231,7 +231,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // ------------------------------------------------------------------ prologue
 
-// One CTA per (kv head g, tile of 4 query vectors of that head across the
+// One CTA per (kv head g, tile of kPrologueTile query vectors of that head across the
 // batch): q' = Pi_g q and q'' = S_g q' as tile products (each row of Pi_g and
 // S_g is read once per tile), then every vector's rows of the query operand
 // of the score products, in mma.m16n8k16 A-fragment order:
