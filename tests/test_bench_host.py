@@ -23,6 +23,26 @@ def test_byte_accounting_matches_record_formulas():
     assert abs(exp / 1e6 - 183.8) < 0.5
 
 
+@pytest.mark.parametrize("name", ["qwen", "llama", "long", "mixed", "kivi"])
+def test_workload_records_match_the_page_formats(name):
+    """bench.py's bytes per (token, kv head) for every bench workload equal the oracle's page
+    layouts divided by the 16 tokens of a page (key and value parts separately where the
+    layout splits them)."""
+    import synthetic_kv as SK
+    from oracle import kivi as OKV
+
+    w = SK.workload(name)
+    kr, vr = bench.workload_records(w)
+    if w.kivi:
+        lay = OKV.subblock_layout(w.d, w.key_bits, w.value_bits)
+        assert 16 * kr == lay["value_scale"] and 16 * vr == lay["bytes"] - lay["value_scale"]
+    else:
+        lay = PG.subblock_layout(w.d, w.key_bits, int(w.key_qjl), w.value_bits, key_split=w.key_split,
+                                 key_norm_u8=int(w.key_norm_range is not None))
+        assert 16 * kr == lay["value_norm"] and 16 * vr == lay["bytes"] - lay["value_norm"]
+    assert bench.workload_name(w).startswith(name)
+
+
 def _worker(rank, port, q):
     import torch.distributed as dist
 
