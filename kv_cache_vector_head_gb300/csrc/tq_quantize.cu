@@ -629,8 +629,8 @@ static cudaError_t launch_quantize_warp_bits(int bits, const KParams& P, const K
 
 // Tensor-core path: d = 128, bf16, 16-byte aligned input, antisymmetric tables.
 static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key, long long n_vec) {
-  // mixed-channel keys, byte norms and the structured sketch: CUDA-core tiles
-  if (is_key && (P.ksplit || P.knu8 || P.qjl_srht)) return false;
+  // mixed-channel keys and byte norms: CUDA-core tiles
+  if (is_key && (P.ksplit || P.knu8)) return false;
   if (P.kivi) return false;
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
   return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);

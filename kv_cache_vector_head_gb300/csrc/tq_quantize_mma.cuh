@@ -22,7 +22,9 @@
 //     parameter); planes packed four at a time with one multiply;
 //   * QJL keys (quantize_keys_tc_kernel): a CTA of 8 warps holds 128
 //     vectors, one UMMA M = 128 tile; S r runs as tcgen05.mma over hi / lo
-//     f16 limbs of r and S (hi*hi + hi*lo + lo*hi) into tensor memory.
+//     f16 limbs of r and S (hi*hi + hi*lo + lo*hi) into tensor memory (the
+//     structured S = H diag(sigma_S) is synthesised from its signs: exact
+//     +-1 limbs).
 //     Every entry whose magnitude is below a certified bound of the limb and
 //     accumulation errors (6e-5 ||r|| ||S_c||, a few per thousand vectors)
 //     is recomputed in fp32 by the warp from the limbs, so every sign is
@@ -609,7 +611,8 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int head = blockIdx.y;
   const float* rot = P.k_rot + (size_t)head * (DENSE ? D * D : D);
-  const float* S = P.qjl_s + (size_t)head * D * D;
+  // Gaussian S: [D][D] rows; structured S = H diag(sigma_S): the D signs, entries synthesised
+  const float* S = P.qjl_s + (size_t)head * (P.qjl_srht ? D : D * D);
   Book<BITS> bk;
 #pragma unroll
   for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(P.kt[HALF + k]);
@@ -680,8 +683,14 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     float4 sv[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-      const int i = tid + j * NT;
-      sv[j] = __ldg(reinterpret_cast<const float4*>(S + (size_t)(i >> 5) * D) + (i & 31));
+      const int i = tid + j * NT, c = i >> 5, k0 = 4 * (i & 31);
+      if (P.qjl_srht) {  // S[c][k] = (-1)^popcount(c & k) sigma_S[k], exact in f16 (lo limb 0)
+        const float4 sg = __ldg(reinterpret_cast<const float4*>(S) + (i & 31));
+        sv[j] = make_float4((__popc(c & k0) & 1) ? -sg.x : sg.x, (__popc(c & (k0 + 1)) & 1) ? -sg.y : sg.y,
+                            (__popc(c & (k0 + 2)) & 1) ? -sg.z : sg.z, (__popc(c & (k0 + 3)) & 1) ? -sg.w : sg.w);
+      } else {
+        sv[j] = __ldg(reinterpret_cast<const float4*>(S + (size_t)c * D) + (i & 31));
+      }
     }
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -697,6 +706,10 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
       *reinterpret_cast<uint2*>(Blo + umma_off(c, k0)) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
     }
     for (int c = tid; c < D; c += NT) {
+      if (P.qjl_srht) {  // +-1 rows
+        ts.snorm[c] = sqrtf((float)D) * 1.0001f;
+        continue;
+      }
       const float4* row = reinterpret_cast<const float4*>(S + (size_t)c * D);
       float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8

@@ -80,6 +80,7 @@ CASES = [
     # the structured sketch S = H diag(sigma_S), FWHT and dense rotations
     ("qwen", dict(batch=1, ctx=40, qjl_structured=1)),
     ("bulk", dict(ctx=300, kind=SK.FWHT, qjl_structured=1)),
+    ("bulk", dict(ctx=4100, kind=SK.DENSE, qjl_structured=1, key_bits=2)),
     ("tiny", dict(ctx=60, qjl_structured=1, key_bits=1)),
     ("long", dict(ctx=30, qjl_structured=1, head_dim=160)),
 ]
