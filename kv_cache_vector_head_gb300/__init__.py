@@ -22,10 +22,32 @@ from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_R
 __all__ = [
     "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
     "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
-    "prefill_workspace_size", "prefill_attention",
+    "prefill_workspace_size", "prefill_attention", "norm_range_for", "bits_per_channel",
     "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
     "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "ROLE_QJL_SIGNS", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
 ]
+
+
+def norm_range_for(norms, margin: float = 1.0) -> tuple[float, float]:
+    """A byte-norm range (log2 lo, hi) covering sample key norms with `margin` octaves on each
+    side: the per-layer calibration the u8 log-norm takes ([Design study] §Packed format).
+    Zero norms are ignored; integer bounds keep the code grid reproducible."""
+    n = np.asarray(norms, dtype=np.float64).ravel()
+    n = n[n > 1e-7]
+    if n.size == 0:
+        raise ValueError("no nonzero norms to calibrate from")
+    lo = math.floor(math.log2(n.min()) - margin)
+    hi = math.ceil(math.log2(n.max()) + margin)
+    return float(lo), float(max(hi, lo + 1))
+
+
+def bits_per_channel(layer: "TQLayer") -> dict:
+    """Bits per channel of the layer's compressed records ([Design study] §Packed format and
+    complete bit accounting): the 16-token sub-block bytes of a (page, kv head) over
+    16 tokens x d channels, for keys and values together, next to the float16 cache's 16."""
+    total = subblock_bytes(layer.params) * 8 / (PAGE_SIZE * layer.d)
+    return {"kv_bits_per_channel": total / 2, "kv_total_bits_per_channel": total,
+            "compression_vs_fp16": 32.0 / total}
 
 
 def n_compressed(T: int, window: int) -> int:

@@ -205,3 +205,29 @@ def test_prefill_workspace_and_checks(L):
     st = lib.tq_prefill_attention(ctypes.byref(p), ctypes.byref(c), 4, None, 1, ctypes.c_float(1.0), None, None,
                                   None, 0, 100, None)
     assert st == L.TQ_ERR_INVALID_ARG  # null transforms (checked before anything touches the GPU)
+
+
+def test_norm_range_and_bit_accounting_helpers(L):
+    import kv_cache_vector_head_gb300 as tq
+    from oracle import codec as OC
+
+    rng = np.random.default_rng(0)
+    n = np.linalg.norm(rng.standard_normal((1000, 256)), axis=1) * np.exp(rng.standard_normal(1000))
+    lo, hi = tq.norm_range_for(np.concatenate([n, [0.0]]))
+    assert lo == int(lo) and hi == int(hi)
+    assert 2.0 ** (lo + 1) <= n.min() and n.max() <= 2.0 ** (hi - 1)
+    codes, _ = OC.norm_u8_encode(n, lo, hi)
+    assert codes.min() > 1 and codes.max() < 255  # nothing clamped
+    with pytest.raises(ValueError):
+        tq.norm_range_for([0.0])
+    # bit accounting from the library's own sub-block size (no GPU needed)
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size, p.window = 256, 4, 24, 16, 128
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 2, 2, 1, L.TQ_FWHT
+
+    class _Layer:
+        params, d = p, 256
+
+    b = tq.bits_per_channel(_Layer)
+    assert b["kv_total_bits_per_channel"] == 172 * 8 / 256  # 2b + QJL keys, 2b values, float norms
+    assert abs(b["compression_vs_fp16"] - 32 / (172 * 8 / 256)) < 1e-12
