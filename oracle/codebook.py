@@ -20,7 +20,7 @@ the cell first moment has the closed form
 The solver works on the positive half only, so the codebook is exactly
 symmetric and the middle boundary is exactly 0.
 
-Stored form (the reading of "RMS-scaled" in the hot-path statement): the
+Stored form (the reading of "RMS-scaled" keys): the
 centroids are multiplied by sqrt(d) (unit-RMS coordinates, ~N(0,1)) and
 rounded to float32; the decision boundaries are the float32 midpoints
 (c_j + c_{j+1}) * 0.5f computed in float32 from the float32 centroids, and

@@ -9,7 +9,7 @@ the workloads below.
 Generator: SplitMix64 over counters (one stream per (tensor, layer, sequence)),
 uniform (x >> 11) * 2^-53, Box-Muller normals; this module's own copy.
 
-Workloads (the "configs" of the hot-path statement):
+Workloads:
   tiny      1 seq, 1 layer, 2 KV / 4 q heads, d = 128, T = 1024; K, V, q fp32
             N(0,1); keys times exp(g_c), g_c ~ N(0,1) per (head, channel),
             before RoPE; RoPE theta = 1e4 (rotate-half pairs (j, j + d/2)) at

@@ -1,6 +1,6 @@
 """Parity helpers: the oracle's expected records and the comparison rules.
 
-Tolerances (the hot-path statement):
+Tolerances:
 * packed codes and QJL signs bit-exact, except coordinates within 1e-5 of a
   decision boundary (z units for codes; (S r)_j for the sign of a unit-vector
   residual), which must stay under 1e-4 of all codes and are counted; a code
