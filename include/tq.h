@@ -104,8 +104,13 @@ tq_status tq_build_transform(tq_transform_kind kind, int d, uint64_t seed, int l
 /*
  * Key corrections on top of the Lloyd-Max code ([Reconstruction] §6 QJL;
  * §10 / §12.2 EDEN's unbiased scale, 2.75x lower 1-bit variance than QJL;
- * §12 TurboVec's length-renormalized scoring).  EDEN and RENORM keep the
- * scale in the record slot QJL uses for gamma and spend no bit on a sketch.
+ * §12 item 2 and §13 step 6 TurboVec's length-renormalized correction, one
+ * scalar per key, norm / <y, y_hat>, said there to restore unbiasedness).
+ * EDEN and RENORM keep the scale in the record slot QJL uses for gamma and
+ * spend no bit on a sketch.  With the norm stored in its own field both store
+ * the same number, s = ||y||^2 / <y, y_hat> = 1 / <y, y_hat> (y the rotated
+ * unit key, y_hat its centroids); the two names are kept so that a caller can
+ * ask for either method by name.
  */
 typedef enum { TQ_KEY_MSE = 0, TQ_KEY_QJL = 1, TQ_KEY_EDEN = 2, TQ_KEY_RENORM = 3 } tq_key_correction;
 
@@ -123,7 +128,8 @@ typedef struct {
   int key_qjl;     /* key correction, a tq_key_correction: TQ_KEY_QJL = TurboQuant_prod (QJL sign
                       sketch of the residual, gamma = ||r||); TQ_KEY_MSE = code only; TQ_KEY_EDEN /
                       TQ_KEY_RENORM = code plus one float scale s per key (EDEN's unbiased
-                      ||y||^2 / <y, y_hat>, or TurboVec's ||y|| / ||y_hat||), score n s <q', y_hat> */
+                      ||y||^2 / <y, y_hat>; TurboVec's norm / <y, y_hat> divided by the stored
+                      norm, the same number), score n s <q', y_hat> */
   int value_bits;  /* 1..4 */
   tq_transform_kind kind;
   const float* k_rot;  /* [device] [Hkv][d*d] (dense) or [Hkv][d] signs (FWHT) */

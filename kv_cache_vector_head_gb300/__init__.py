@@ -67,7 +67,8 @@ class TQLayer:
         the length of the vectors the caller passes, zero-padded to d inside
         the kernels (a multiple of 8 in (d/2, d]).  key_qjl: the key
         correction, KEY_QJL (TurboQuant_prod, default), KEY_MSE (code only),
-        KEY_EDEN (unbiased scale) or KEY_RENORM (length renormalization);
+        KEY_EDEN (unbiased scale) or KEY_RENORM (TurboVec's length-renormalized
+        correction norm / <y, y_hat>, stored as the same scale as KEY_EDEN);
         True / False stand for KEY_QJL / KEY_MSE.  key_split: mixed-channel
         key rate, rotated coordinates < d/2 at key_bits + 1 bits (key_bits = 3
         gives 3.5 bits per channel; not with KEY_QJL).  key_norm_range =

@@ -7,8 +7,8 @@
 // basis with ONE inverse transform per head.  [Reconstruction] §6: score
 //   l = scale * n * ( <q', C[idx]> / sqrt(d) + sqrt(pi/2)/d * gamma * <q'', 2s - 1> ),
 //   q' = Pi q, q'' = S q'.
-// Keys with EDEN's unbiased scale or the renormalized length in place of the
-// sketch ([Reconstruction] §10, §12) drop the second term and multiply the
+// Keys with EDEN's unbiased scale or TurboVec's length-renormalized correction in
+// place of the sketch ([Reconstruction] §10, §12) drop the second term and multiply the
 // first by the stored scale s:  l = scale * n * s * <q', C[idx]> / sqrt(d).
 //
 // The two contractions of a decode step are dense products over the G query

@@ -16,8 +16,10 @@
 //      pack sign-magnitude planes with warp ballots (warp w owns word w);
 //   4. keys: residual (in z units) z - C[idx], its norm, and the QJL sketch
 //      S (z - C[idx]) as a second tile product; signs packed by ballot.  The
-//      scaled corrections keep s instead: EDEN d / sum z C[idx], renormalized
-//      sqrt(d / sum C[idx]^2) (both from the same per-coordinate pass).
+//      scaled corrections keep s instead: EDEN's unbiased scale and TurboVec's
+//      length-renormalized correction ([Reconstruction] §12 item 2, §13 step 6:
+//      norm / <y, y_hat>, with the norm kept in its own field) are the same
+//      number, s = 1 / <y, y_hat> = d / sum z C[idx].
 // Mixed-channel keys ([Design study] §Packed format: fractional rates by
 // channel allocation) take coordinates < d/2 one bit wider with their own
 // book; the wider codes' top plane is kept for the first d/64 words only.
@@ -99,8 +101,8 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
     }
     if (is_key) {
       const float c = cbj[idx];
-      // QJL: residual; EDEN: z c (z and c share a sign, so the terms are >= 0); renormalized: c^2
-      s.r[v][j] = P.kqjl == TQ_KEY_EDEN ? z * c : P.kqjl == TQ_KEY_RENORM ? c * c : z - c;
+      // QJL: residual; EDEN / length-renormalized: z c (z and c share a sign, so the terms are >= 0)
+      s.r[v][j] = (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM) ? z * c : z - c;
     }
   }
   if (!is_key && slot_of) {
@@ -120,9 +122,7 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
     }
     acc = warp_sum_d(acc);
     if (lane == 0) {
-      const double g = P.kqjl == TQ_KEY_EDEN     ? (double)D / acc
-                       : P.kqjl == TQ_KEY_RENORM ? sqrt((double)D / acc)
-                                                 : sqrt(acc) / (double)sqrt_d;
+      const double g = scaled ? (double)D / acc : sqrt(acc) / (double)sqrt_d;
       s.gam[v] = s.zero[v] ? 0.f : (float)g;
     }
   }

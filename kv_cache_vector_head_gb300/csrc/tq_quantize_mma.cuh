@@ -179,7 +179,9 @@ __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushor
 enum { kFlat = 0, kStep = 1 };
 
 // Values, and keys without the QJL sketch (keys with it: quantize_keys_tc_kernel),
-// with the EDEN / renormalized key scale where the layer keeps one.
+// with the key scale where the layer keeps one (EDEN's unbiased scale, which is
+// also TurboVec's length-renormalized correction norm / <y, y_hat> once the norm
+// is stored on its own: s = 1 / <y, y_hat>).
 // DENSE: dense rotation (else FWHT).  grid (x, Hkv).
 template <int BITS, bool DENSE, int MODE>
 __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
@@ -204,8 +206,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
   const float* ctab = is_key ? P.kc : P.vc;
   const float* ttab = is_key ? P.kt : P.vt;
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
-  // keys with a scale in place of the sketch (EDEN / renormalized); 0 otherwise
-  const int corr = (is_key && (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM)) ? P.kqjl : 0;
+  // keys with a scale in place of the sketch (EDEN / length-renormalized, one formula); false otherwise
+  const bool corr = is_key && (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM);
   Book<BITS> bk;
 #pragma unroll
   for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(ttab[HALF + k]);
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
             if (corr) {
               // z and its centroid share a sign: z C = |z| C+
               const float c = centroid_pos<BITS>(mag, bk);
-              term[i] = corr == TQ_KEY_EDEN ? fabsf(z) * c : c * c;
+              term[i] = fabsf(z) * c;
             }
           }
           if (corr) spart[R] += (term[0] + term[1]) + (term[2] + term[3]);
@@ -497,14 +499,14 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
     }
 
     if (corr) {
-      // key scale: EDEN s = d / sum z C, renormalized s = sqrt(d / sum C^2) (balanced
-      // trees of positive terms: depth 3 within a word pair, 4 words, 2 across the quad)
+      // key scale s = d / sum z C (balanced trees of positive terms: depth 3 within a
+      // word pair, 4 words, 2 across the quad)
 #pragma unroll
       for (int R = 0; R < 2; ++R) {
         float a = ssum[R];
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
-        const float sc = zero[R] ? 0.f : (corr == TQ_KEY_EDEN ? (float)D / a : sqrtf((float)D / a));
+        const float sc = zero[R] ? 0.f : (float)D / a;
         if (okrow[R] && t == 0) {
           if constexpr (MODE == kFlat) rnorms[nrow[R]] = sc;
           else reinterpret_cast<float*>(dst[R] + P.off_krnorm)[slot[R]] = sc;

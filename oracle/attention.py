@@ -46,7 +46,7 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
     win_k, win_v : [Hkv, Tw, d] float16 window tokens (oldest first), or None.
     params : kind, k_rot[Hkv], v_rot[Hkv], qjl_s[Hkv] (stored float32 arrays),
              k_cb, v_cb (Codebook), key_qjl: key correction (0 none, 1 QJL,
-             2 EDEN scale, 3 length renormalization; krnorm holds gamma or s);
+             2 EDEN scale, 3 TurboVec length-renormalized correction; krnorm holds gamma or s);
              optional k_cb_hi: mixed-channel key rate (coordinates < d/2 read
              this book).  knorm holds decoded norms (byte norms decoded).
     Returns out [Hq, d], lse [Hq], scores [Hq, T] (compressed first, then window).
@@ -74,7 +74,7 @@ def decode_one(q: np.ndarray, comp: dict | None, win_k: np.ndarray | None, win_v
                 q2 = np.asarray(params["qjl_s"][g], np.float32).astype(np.float64) @ q1
                 pm = np.where(comp["ksigns"][g], 1.0, -1.0)
                 l_c = l_c + kap * comp["krnorm"][g].astype(np.float64) * (pm @ q2)
-            elif corr >= 2:  # EDEN or renormalized keys: the per-key scale
+            elif corr >= 2:  # EDEN or length-renormalized keys: the per-key scale
                 l_c = l_c * comp["krnorm"][g].astype(np.float64)
             l_c = scale * comp["knorm"][g].astype(np.float64) * l_c
             parts.append(l_c)

@@ -136,11 +136,20 @@ def quantize_prod(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, S: np
 
 # Key corrections.  QJL is TurboQuant_prod's residual sketch; the two others
 # spend no bit on a residual and keep one float32 scale s per key instead
-# (the "next" correction variants): EDEN's unbiased scale s = ||y||^2 /
-# <y, y_hat> ([Reconstruction] §10, §12.2: TurboQuant_mse is EDEN/DRIVE with
-# a fixed scale; the unbiased EDEN scalar has 2.75x lower 1-bit variance than
-# QJL) and TurboVec's length renormalization s = ||y|| / ||y_hat||
-# ([Reconstruction] §12: length-renormalized scoring in place of QJL).
+# (the "next" correction variants), so that the key is reconstructed as
+# n s Pi^T y_hat:
+#  * EDEN's unbiased scale ([Reconstruction] §10, §12.2: TurboQuant_mse is
+#    EDEN/DRIVE with a fixed scale; the unbiased EDEN scalar has 2.75x lower
+#    1-bit variance than QJL): the scale that makes <y, s y_hat> = ||y||^2,
+#    s = ||y||^2 / <y, y_hat>, with y the rotated unit vector (||y|| = 1);
+#  * TurboVec's length-renormalized correction ([Reconstruction] §12 item 2,
+#    §13 reference logic, step 6): one scalar per vector computed at
+#    ingestion, the vector's norm divided by the inner product of the
+#    rotated unit vector with its reconstruction, norm / <y, y_hat>; the
+#    page says it restores unbiasedness.  The record keeps the norm n in its
+#    own field, so the stored scale is that scalar divided by n.  Both
+#    readings give the same number: the page notes that TurboVec mirrors the
+#    EDEN strategy.
 KEY_MSE, KEY_QJL, KEY_EDEN, KEY_RENORM = 0, 1, 2, 3
 
 
@@ -149,14 +158,17 @@ def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mod
     """TurboQuant_mse code of the rows of x plus the scale s of the key
     correction `mode` (KEY_EDEN or KEY_RENORM), stored as float32 in the
     record's "rnorm" slot; the key is reconstructed as n s Pi^T y_hat.  For a
-    zero vector s = 0.  cb_hi: mixed-channel rate as in quantize_mse."""
+    zero vector s = 0 (its norm is 0, so its score is 0 whatever s is).
+    cb_hi: mixed-channel rate as in quantize_mse."""
     rec = quantize_mse(x, kind, rot, cb, cb_hi)
     y, yhat, zero = rec["y"], rec["yhat"], rec["zero"]
+    dot = np.where(zero, 1.0, np.sum(y * yhat, axis=-1))
     if mode == KEY_EDEN:
-        den = np.sum(y * yhat, axis=-1)          # y is a unit vector: ||y||^2 = 1
-        s = 1.0 / np.where(zero, 1.0, den)
+        s = np.sum(y * y, axis=-1) / dot
     elif mode == KEY_RENORM:
-        s = 1.0 / np.where(zero, 1.0, np.linalg.norm(yhat, axis=-1))
+        n = rec["norm_f64"]
+        correction = n / dot                       # norm / <y, y_hat>
+        s = correction / np.where(zero, 1.0, n)    # the norm is stored separately
     else:
         raise ValueError("mode must be KEY_EDEN or KEY_RENORM")
     s = np.where(zero, 0.0, s)
@@ -165,7 +177,7 @@ def quantize_scaled(x: np.ndarray, kind: int, rot: np.ndarray, cb: Codebook, mod
 
 
 def dequantize_scaled(norm, scale, idx, kind, rot, cb, cb_hi=None) -> np.ndarray:
-    """k_hat = n s Pi^T y_hat for the EDEN / renormalized keys."""
+    """k_hat = n s Pi^T y_hat for the EDEN / length-renormalized keys."""
     return np.asarray(scale, dtype=np.float64)[:, None] * dequantize_mse(norm, idx, kind, rot, cb, cb_hi)
 
 

@@ -43,7 +43,7 @@ def n_compressed(T: int, W: int, P: int = PAGE) -> int:
 
 def subblock_layout(d: int, key_bits: int, key_qjl: int, value_bits: int, P: int = PAGE,
                     key_split: int = 0, key_norm_u8: int = 0) -> dict:
-    """key_qjl: key correction (0 none, 1 QJL: scale slot + sign plane, 2 / 3 EDEN / renormalized: scale slot).
+    """key_qjl: key correction (0 none, 1 QJL: scale slot + sign plane, 2 / 3 EDEN / length-renormalized: scale slot).
     key_split: mixed-channel key rate (the first d/2 coordinates carry one more plane, stored after the
     key_bits full planes as uint32 [P][d/64]).  key_norm_u8: key norms as one byte per token."""
     if P != PAGE:

@@ -121,7 +121,7 @@ def compare_records(ora, g_idx, g_norm, g_signs=None, g_rnorm=None, is_key=True,
         np.testing.assert_allclose(g_norm.astype(np.float64), ora["norm"].astype(np.float64), rtol=NORM_RTOL,
                                    atol=1e-30)
     n_exempt_codes = int(code_ex.sum())
-    if is_key and g_signs is None and g_rnorm is not None:  # EDEN / renormalized keys: the scale
+    if is_key and g_signs is None and g_rnorm is not None:  # EDEN / length-renormalized keys: the scale
         ok = ~vec_flip
         np.testing.assert_allclose(g_rnorm[ok].astype(np.float64), ora["rnorm"][ok].astype(np.float64),
                                    rtol=NORM_RTOL, atol=1e-30)
@@ -158,7 +158,7 @@ def adopt_exempt(rec, g_idx, g_signs=None, g_rnorm=None, g_norm_code=None, norm_
     idx = rec["idx"].copy()
     idx[ex] = g_idx[ex]
     out["idx"] = idx
-    if g_signs is None and g_rnorm is not None and "rnorm" in rec:  # scale of EDEN / renormalized keys
+    if g_signs is None and g_rnorm is not None and "rnorm" in rec:  # scale of EDEN / length-renormalized keys
         flip = (idx != rec["idx"]).any(axis=1)
         rn = rec["rnorm"].copy()
         rn[flip] = g_rnorm[flip]

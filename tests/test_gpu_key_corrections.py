@@ -5,8 +5,9 @@ the C ABI: keys quantized into pages, scores read back from the decode
 [Reconstruction] §6: TurboQuant_prod's QJL term makes the inner product
 unbiased; §10 / §12.2: EDEN's scale s = ||y||^2 / <y, y_hat> is unbiased as
 well, the plain MSE code shrinks it (slope 2/pi at one bit), and the 1-bit
-EDEN scalar has a lower variance than a 1-bit QJL sketch; §12: TurboVec's
-length renormalization sits between the two.  For a query independent of the
+EDEN scalar has a lower variance than a 1-bit QJL sketch; §12 item 2, §13
+step 6: TurboVec's length-renormalized correction norm / <y, y_hat> restores
+unbiasedness (with the norm stored on its own it is EDEN's scale).  For a query independent of the
 key, the code's error r = y - y_hat gives d E<q/||q||, r>^2 = E||r||^2 = D_mse
 (the Lloyd-Max unit MSE), and the QJL sketch of r (Gaussian S, d rows) has
 variance (pi/2 ||q||^2 ||r||^2 - <q, r>^2) / d, so its distortion is
@@ -99,14 +100,18 @@ def test_key_correction_estimators(tq, kind):
         s_mse, d_mse = table[0, bits]
         s_qjl, d_qjl = table[1, bits]
         s_eden, d_eden = table[2, bits]
-        s_ren, _ = table[3, bits]
+        s_ren, d_ren = table[3, bits]
         # unbiased estimators: slope 1 within a few standard errors (keys counted once: the
         # eight queries of a key share its code)
         tol = 4.0 * np.sqrt(max(d_qjl, d_eden) / (n / HQ))
         assert abs(s_qjl - 1.0) < max(tol, 0.01), (bits, s_qjl)
         assert abs(s_eden - 1.0) < max(tol, 0.01), (bits, s_eden)
-        # the plain code shrinks; renormalization removes part of the shrinkage
-        assert s_mse < s_ren < s_eden + 0.01, (bits, s_mse, s_ren, s_eden)
+        # TurboVec's correction restores unbiasedness; it stores EDEN's number, so the two agree
+        assert abs(s_ren - 1.0) < max(tol, 0.01), (bits, s_ren)
+        assert abs(s_ren - s_eden) < 1e-6 and abs(d_ren - d_eden) < 1e-6 * d_eden, (bits, s_ren, s_eden)
+        # the plain Lloyd-Max code shrinks the product by 1 - D_mse (centroid condition: E<y, y_hat> =
+        # E||y_hat||^2 = 1 - D_mse for a unit y, and the rotation spreads that over every direction)
+        assert abs(s_mse - (1.0 - mse[bits])) < max(tol, 0.01), (bits, s_mse, mse[bits])
         # distortion of the plain code D_mse, of the sketch (pi/2 - 1/d) D_mse (sampling: 10 %)
         assert 0.9 < d_mse / mse[bits] < 1.1, (bits, d_mse, mse[bits])
         assert 0.9 < d_qjl / ((np.pi / 2 - 1.0 / D) * mse[bits]) < 1.1, (bits, d_qjl, mse[bits])

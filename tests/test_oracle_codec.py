@@ -191,16 +191,37 @@ def _pair(rng, n, d, rho):
     return y, rho * y + math.sqrt(1 - rho * rho) * w
 
 
-def test_renormalized_keys_keep_their_length():
+def test_length_renormalized_keys_are_unbiased():
+    """TurboVec's per-vector correction norm / <y, y_hat> ([Reconstruction] §12
+    item 2, §13 step 6) restores unbiasedness: over uniformly rotated pairs of
+    correlation rho the mean estimate n s <q', y_hat> equals n rho, where the
+    uncorrected code shrinks it.  Checked for 1 to 3 bits and a key norm of 3."""
+    d, n, rho = 64, 20000, 0.6
+    rng = np.random.default_rng(7)
+    y, q = _pair(rng, n, d, rho)
+    for bits in (1, 2, 3):
+        cb = CB.lloyd_max(d, bits)
+        rec = C.quantize_scaled(3.0 * y, T.DENSE, np.eye(d), cb, C.KEY_RENORM)
+        np.testing.assert_allclose(rec["norm_f64"], 3.0, rtol=1e-12)
+        est = rec["norm_f64"] * rec["scale"] * np.sum(q * rec["yhat"], axis=1)
+        assert abs(est.mean() - 3.0 * rho) < 4 * est.std() / math.sqrt(n), bits
+        plain = rec["norm_f64"] * np.sum(q * rec["yhat"], axis=1)
+        assert 3.0 * rho - plain.mean() > 10 * plain.std() / math.sqrt(n), bits
+    z = C.quantize_scaled(np.zeros((1, d)), T.FWHT, T.build_transform(T.FWHT, d, 0, 0, 0, 0),
+                          CB.lloyd_max(d, 2), C.KEY_RENORM)
+    assert z["scale"][0] == 0 and z["norm"][0] == 0
+
+
+def test_length_renormalization_is_the_eden_scale():
+    """The page relates TurboVec's correction to EDEN's unbiased scalar: with the
+    norm kept in its own field both stored scales agree on arbitrary keys."""
     d = 128
     cb = CB.lloyd_max(d, 2)
     rot = T.build_transform(T.FWHT, d, 0, 0, 0, 0)
-    x = np.random.default_rng(4).standard_normal((64, d)) * 3.0
-    rec = C.quantize_scaled(x, T.FWHT, rot, cb, C.KEY_RENORM)
-    kh = C.dequantize_scaled(rec["norm"], rec["scale"], rec["idx"], T.FWHT, rot, cb)
-    np.testing.assert_allclose(np.linalg.norm(kh, axis=1), np.linalg.norm(x, axis=1), rtol=1e-6)
-    z = C.quantize_scaled(np.zeros((1, d)), T.FWHT, rot, cb, C.KEY_RENORM)
-    assert z["scale"][0] == 0 and z["norm"][0] == 0
+    x = np.random.default_rng(4).standard_normal((64, d)) * np.exp(np.random.default_rng(5).standard_normal(d))
+    a = C.quantize_scaled(x, T.FWHT, rot, cb, C.KEY_RENORM)
+    b = C.quantize_scaled(x, T.FWHT, rot, cb, C.KEY_EDEN)
+    np.testing.assert_allclose(a["scale"], b["scale"], rtol=1e-12)
 
 
 def test_eden_scale_is_unbiased_and_plain_code_is_not():

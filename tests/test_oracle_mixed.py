@@ -223,16 +223,12 @@ def test_mixed_page_round_trip_with_byte_norms():
 
 
 def test_scalar_corrections_with_mixed_books():
-    """Length renormalization gives mixed-rate keys their exact length; the EDEN scale keeps the
-    mixed-rate estimate unbiased (uniformly rotated unit pairs with correlation rho, identity
-    rotation), where the plain mixed code shrinks it."""
+    """With mixed-rate books both scalar corrections keep the estimate unbiased
+    (uniformly rotated unit pairs with correlation rho, identity rotation): the
+    EDEN scale and TurboVec's length-renormalized correction norm / <y, y_hat>,
+    where the plain mixed code shrinks it."""
     d = 128
     lo, hi = CB.lloyd_max(d, 2), CB.lloyd_max(d, 3)
-    rot = T.build_transform(T.FWHT, d, 0, 0, 0, 0)
-    x = np.random.default_rng(4).standard_normal((64, d)) * 3.0
-    rec = C.quantize_scaled(x, T.FWHT, rot, lo, C.KEY_RENORM, cb_hi=hi)
-    kh = C.dequantize_scaled(rec["norm"], rec["scale"], rec["idx"], T.FWHT, rot, lo, hi)
-    np.testing.assert_allclose(np.linalg.norm(kh, axis=1), np.linalg.norm(x, axis=1), rtol=1e-6)
     n, rho = 20000, 0.6
     rng = np.random.default_rng(6)
     g = rng.standard_normal((n, d))
@@ -241,8 +237,9 @@ def test_scalar_corrections_with_mixed_books():
     h -= np.sum(h * y, axis=1, keepdims=True) * y
     h /= np.linalg.norm(h, axis=1, keepdims=True)
     q = rho * y + math.sqrt(1 - rho * rho) * h
-    rec = C.quantize_scaled(y, T.DENSE, np.eye(d), lo, C.KEY_EDEN, cb_hi=hi)
-    est = np.sum(q * rec["scale"][:, None] * rec["yhat"], axis=1)
-    assert abs(est.mean() - rho) < 4 * est.std() / math.sqrt(n)
+    for mode in (C.KEY_EDEN, C.KEY_RENORM):
+        rec = C.quantize_scaled(2.0 * y, T.DENSE, np.eye(d), lo, mode, cb_hi=hi)
+        est = rec["norm_f64"] * rec["scale"] * np.sum(q * rec["yhat"], axis=1)
+        assert abs(est.mean() - 2.0 * rho) < 4 * est.std() / math.sqrt(n), mode
     plain = np.sum(q * rec["yhat"], axis=1)
     assert rho - plain.mean() > 10 * plain.std() / math.sqrt(n)
