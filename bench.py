@@ -114,53 +114,103 @@ def step_bytes(T, W, B, Hkv, Hq, d, kb, vb, qjl=True, rec=None):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region (skipped if unavailable)."""
+    """nvidia-smi sampling around the timed region.  A reader thread stamps every
+    sample with the host clock, so the samples that fall inside a marked window
+    (plus a margin of one sampling period) can be picked out afterwards; if the
+    window is shorter than the sampling period, the samples just before and just
+    after it bracket it.  The GPU's row is matched by PCI bus id."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_MS = 50
 
-    def __init__(self, index):
-        self.index, self.proc, self.path = index, None, None
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc, self.samples, self.thread = None, [], None
+        self.windows = {}
 
     def start(self):
+        import threading
+
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", str(self.PERIOD_MS)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    rec = {"t": time.monotonic(), "bus": p[0].lower(), "sm": float(p[1]), "max": float(p[2]),
+                           "reasons": [n for n, v in zip(self.NAMES, p[5:9]) if v.lower().startswith("active")]}
+                except ValueError:
+                    continue
+                self.samples.append(rec)
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        t0 = time.monotonic()
+        while not self.samples and time.monotonic() - t0 < 5.0:  # the first sample, so the window is bracketed
+            time.sleep(0.01)
+
+    def mark(self, name, which):
+        w = self.windows.setdefault(name, [None, None])
+        w[0 if which == "start" else 1] = time.monotonic()
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
+        t0 = time.monotonic()
+        last = max((w[1] or 0.0) for w in self.windows.values()) if self.windows else t0
+        while time.monotonic() - t0 < 2.0 and not any(r["t"] > last for r in self.samples):
+            time.sleep(0.01)  # one sample after the last window
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.f.close()
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
-                continue
-            try:
-                sm.append(float(p[1]))
-                mx = max(mx, float(p[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    @staticmethod
+    def bus_key(s):
+        """'bus:device' in hex from nvidia-smi's 'domain:bus:device.function'."""
+        p = s.lower().split(":")
+        try:
+            return f"{int(p[-2], 16):02x}:{int(p[-1].split('.')[0], 16):02x}"
+        except (IndexError, ValueError):
+            return s.lower()
+
+    def summary(self, name):
+        rows = self.samples
+        buses = {self.bus_key(r["bus"]) for r in rows}
+        if self.bus_id and self.bus_id in buses:
+            rows = [r for r in rows if self.bus_key(r["bus"]) == self.bus_id]
+        elif len(buses) > 1:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if not rows or name not in self.windows or None in self.windows[name]:
+            return None
+        a, b = self.windows[name]
+        pad = self.PERIOD_MS * 1e-3
+        inside = [r for r in rows if a - pad <= r["t"] <= b + pad]
+        how = "inside the window"
+        if not inside:
+            before = [r for r in rows if r["t"] < a]
+            after = [r for r in rows if r["t"] > b]
+            inside = before[-1:] + after[:1]
+            how = "bracketing samples (window shorter than the sampling period)"
+        if not inside:
+            return None
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["max"] for r in inside),
+                "reasons": sorted({n for r in inside for n in r["reasons"]}), "samples": len(inside),
+                "window_s": round(b - a, 4), "how": how}
 
 
 def measured_peaks():
@@ -208,9 +258,9 @@ def dist_info():
 
 # ----------------------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample_setup(name="qwen"):
-    """One sequence, one KV head (its G query heads) of the workload, quantized
-    by the oracle; the step is one append + decode over it."""
+def oracle_sample_setup(name="qwen", seq=0, head=0):
+    """One (sequence, KV head) unit of the workload (its G query heads), quantized
+    by the oracle; a step is one append + decode over it."""
     import numpy as np
 
     import synthetic_kv as SK
@@ -219,7 +269,7 @@ def oracle_sample_setup(name="qwen"):
     from oracle import transforms as OT
 
     w = SK.workload(name)
-    kv = SK.keys_values(w, seqs=[0])
+    kv = SK.keys_values(w, seqs=[seq])
     G = w.n_q_heads // w.n_kv_heads
     T, W, d = w.ctx, w.window, w.d
     nc = 16 * (max(0, T - W) // 16)
@@ -227,9 +277,12 @@ def oracle_sample_setup(name="qwen"):
     kcb_hi = OCB.lloyd_max(d, w.key_bits + 1) if w.key_split else None
     corr = int(w.key_qjl)
     prm = {"kind": w.kind, "k_cb": kcb, "k_cb_hi": kcb_hi, "v_cb": vcb, "key_qjl": corr,
-           "k_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 0)], "v_rot": [OT.build_transform(w.kind, d, 0, 0, 0, 1)],
-           "qjl_s": [OT.build_transform(w.kind, d, 0, 0, 0, 2)] if corr == 1 else None}
-    K, V = kv["K"][0, :, 0], kv["V"][0, :, 0]
+           "k_rot": [OT.build_transform(w.kind, d, 0, 0, head, 0)],
+           "v_rot": [OT.build_transform(w.kind, d, 0, 0, head, 1)],
+           "qjl_s": [OT.build_transform(w.kind, d, 0, 0, head, 2)] if corr == 1 else None}
+    K, V = kv["K"][0, :, head].copy(), kv["V"][0, :, head].copy()
+    q = kv["q"][0, head * G:(head + 1) * G].copy()
+    del kv
     S = {"prm": prm, "kind": w.kind, "k_cb": kcb, "v_cb": vcb, "norm_range": w.key_norm_range}
     if w.kivi:  # the control arm: dequantized pages, attention over them and the window
         from oracle import kivi as OKV
@@ -244,7 +297,6 @@ def oracle_sample_setup(name="qwen"):
                 "ksigns": kr["signs"][None], "vnorm": vr["norm"][None], "vidx": vr["idx"][None]}
     win_k = K[nc:].astype(np.float16)[None]
     win_v = V[nc:].astype(np.float16)[None]
-    q = kv["q"][0, :G]
     kr_b, vr_b = workload_records(w)
     nbytes = nc * (kr_b + vr_b) + (T - nc) * d * 4 + d * (2 * 2 + 2 * 2) + G * d * 6
     S.update({"comp": comp, "win_k": win_k, "win_v": win_v, "q": q, "d": d, "bytes": nbytes,
@@ -308,23 +360,131 @@ def oracle_step(S):
     return OA.decode_one(S["q"], comp, wk, wv, S["prm"], 1.0 / math.sqrt(S["d"]))
 
 
-def run_cpu_sample(name="qwen", steps=3, warmup=1):
-    S = oracle_sample_setup(name)
-    for _ in range(warmup):
+def host_cores():
+    """(os.cpu_count(), CPUs this process may run on)."""
+    n = os.cpu_count() or 1
+    try:
+        return n, len(os.sched_getaffinity(0))
+    except AttributeError:
+        return n, n
+
+
+def _one_thread_env():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        os.environ[k] = "1"
+
+
+def _decode_worker(name, seq, head, steps, barrier, conn):
+    """Spawned worker: set up one (sequence, KV head) unit, then time `steps` oracle
+    steps (after the barrier) or, with steps == 0, run one step per request on conn."""
+    _one_thread_env()
+    S = oracle_sample_setup(name, seq, head)
+    oracle_step(S)  # warm-up
+    barrier.wait()
+    if steps > 0:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            oracle_step(S)
+        conn.send((S["bytes"] * steps, time.perf_counter() - t0))
+        return
+    conn.send(S["bytes"])
+    while conn.recv():
         oracle_step(S)
+        conn.send(True)
+
+
+def _quantize_worker(n_vec, kind, layer, barrier, conn):
+    """Spawned worker: the oracle's bulk quantize (keys 3b + QJL, values 4b, d = 128) of
+    n_vec token-heads of the bulk recipe (bf16 N(0,1) x lognormal channel scales)."""
+    _one_thread_env()
+    import synthetic_kv as SK
+    from oracle import codebook as OCB
+    from oracle import codec as OC
+    from oracle import transforms as OT
+
+    w = SK.workload("bulk", kind=kind)
+    H, d = w.n_kv_heads, w.d
+    kv = SK.keys_values(w, layer=layer, ctx=n_vec // H)
+    K, V = kv["K"][0], kv["V"][0]                      # [T, H, d]
+    kcb, vcb = OCB.lloyd_max(d, w.key_bits), OCB.lloyd_max(d, w.value_bits)
+    tr = [(OT.build_transform(kind, d, 0, layer, h, 0), OT.build_transform(kind, d, 0, layer, h, 1),
+           OT.build_transform(kind, d, 0, layer, h, 2)) for h in range(H)]
+    barrier.wait()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle_step(S)
-    dt = (time.perf_counter() - t0) / steps
-    return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"1 sequence x 1 KV head ({S['G']} q heads) of the workload, T={S['T']}, "
-                       f"{S['bytes'] / 1e6:.1f} MB per step, {steps} steps, 1 thread"),
-            "s_per_step": dt}
+    for h in range(H):
+        kr = OC.quantize_prod(K[:, h], kind, tr[h][0], kcb, tr[h][2])
+        vr = OC.quantize_mse(V[:, h], kind, tr[h][1], vcb)
+        OC.pack_codes(kr["idx"], w.key_bits), OC.pack_bits(kr["signs"]), OC.pack_codes(vr["idx"], w.value_bits)
+    conn.send((K.shape[0] * H, time.perf_counter() - t0))
+
+
+def _spawn_timed(target, argsets):
+    """Run target(*args, barrier, conn) in one spawned process per argset, all timed
+    from a common barrier; returns their (work, seconds) results."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(len(argsets), timeout=600)
+    procs, conns = [], []
+    for a in argsets:
+        r, w_ = ctx.Pipe(duplex=False)
+        p = ctx.Process(target=target, args=(*a, barrier, w_))
+        p.start()
+        w_.close()  # a worker that dies then ends our recv with EOFError
+        procs.append(p)
+        conns.append(r)
+    try:
+        out = [_recv(c, 900) for c in conns]
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+    return out
+
+
+def _recv(conn, timeout):
+    if not conn.poll(timeout):
+        raise TimeoutError("oracle worker did not answer")
+    return conn.recv()
+
+
+def run_cpu_sample(name="qwen"):
+    """The oracle on the host cores: decode of the workload on (sequence, KV head) units,
+    one per core in parallel and one on a single core, and the bulk quantize of the bulk
+    recipe (FWHT and dense Pi), multi- and single-core.  Bounded samples."""
+    import synthetic_kv as SK
+
+    ncpu, cores = host_cores()
+    w = SK.workload(name)
+    units = [(b, g) for b in range(w.batch) for g in range(w.n_kv_heads)]
+    par = max(1, min(cores, len(units), 16))
+    steps = 2
+    one = _spawn_timed(_decode_worker, [(name, 0, 0, steps)])[0]
+    multi = _spawn_timed(_decode_worker, [(name, b, g, steps) for b, g in units[:par]])
+    mbytes, msec = sum(x[0] for x in multi), max(x[1] for x in multi)
+    out = {"value": mbytes / msec / 1e9, "unit": "GB/s", "cores": par, "kind": "oracle",
+           "sample": (f"decode: {par} (sequence, KV head) units of the workload in parallel (one process per core, "
+                      f"1 BLAS thread each), {steps} append + decode steps each, T={w.ctx}"),
+           "host_cpu_count": ncpu, "host_cpus_usable": cores,
+           "single_core": {"value": one[0] / one[1] / 1e9, "unit": "GB/s", "cores": 1,
+                           "sample": f"1 unit, {steps} steps"}}
+    qn1, qn = 1 << 15, 1 << 15
+    qpar = max(1, min(cores, 16))
+    quant = {}
+    for kname, kind in (("fwht", SK.FWHT), ("dense", SK.DENSE)):
+        s1 = _spawn_timed(_quantize_worker, [(qn1, kind, 0)])[0]
+        sm = _spawn_timed(_quantize_worker, [(qn, kind, l) for l in range(qpar)])
+        quant[kname] = {"token_heads_per_s": sum(x[0] for x in sm) / max(x[1] for x in sm), "cores": qpar,
+                        "single_core_token_heads_per_s": s1[0] / s1[1]}
+    quant["sample"] = (f"keys 3b + QJL and values 4b, d = 128, bulk recipe; {qn} token-heads per core "
+                       f"({qpar} cores, one process each), {qn1} on one core")
+    out["quantize"] = quant
+    return out
 
 
 def cpu_baseline_subprocess(name="qwen"):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", "--workload", name],
                        capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
@@ -333,42 +493,98 @@ def cpu_baseline_subprocess(name="qwen"):
 
 
 def run_reference(args):
+    """The oracle as the reference arm: each step runs one append + decode on one
+    (sequence, KV head) unit per host core, in parallel (spawned processes, one BLAS
+    thread each); the step's bytes are the units' algorithmic bytes."""
+    import multiprocessing as mp
+
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
     import synthetic_kv as SK
 
-    S = oracle_sample_setup(args.workload)
-    for _ in range(args.warmup):
-        oracle_step(S)
-    times = []
-    for _ in range(args.steps):
+    w = SK.workload(args.workload)
+    _, cores = host_cores()
+    units = [(b, g) for b in range(w.batch) for g in range(w.n_kv_heads)]
+    par = max(1, min(cores, len(units), 16))
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(par, timeout=600)
+    procs, conns = [], []
+    for b, g in units[:par]:
+        a, c = ctx.Pipe()
+        p = ctx.Process(target=_decode_worker, args=(args.workload, b, g, 0, barrier, c))
+        p.start()
+        c.close()
+        procs.append(p)
+        conns.append(a)
+    step_bytes_ = sum(_recv(c, 900) for c in conns)
+
+    def one_step():
         t0 = time.perf_counter()
-        oracle_step(S)
-        times.append(time.perf_counter() - t0)
+        for c in conns:
+            c.send(True)
+        for c in conns:
+            _recv(c, 300)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one_step()
+    times = [one_step() for _ in range(args.steps)]
+    for c in conns:
+        c.send(False)
+    for p in procs:
+        p.join(timeout=30)
+        if p.is_alive():
+            p.terminate()
     dt = sum(times) / len(times)
-    value = S["bytes"] / dt / 1e9
-    sample = (f"each step: 1 sequence x 1 KV head ({S['G']} q heads) of the workload, T={S['T']}, "
-              f"{S['bytes'] / 1e6:.1f} MB algorithmic bytes")
+    value = step_bytes_ / dt / 1e9
+    sample = (f"each step: {par} (sequence, KV head) units of the workload ({w.n_q_heads // w.n_kv_heads} q heads "
+              f"each), one per host core in parallel, T={w.ctx}, {step_bytes_ / 1e6:.1f} MB algorithmic bytes")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_name(SK.workload(args.workload)),
-                       "sample": "1 sequence x 1 KV head per step"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "config": {"workload": workload_name(w), "sample": f"{par} (sequence, KV head) units per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": par, "kind": "oracle", "sample": sample,
+                             "host_cpu_count": os.cpu_count()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- GPU path
 
-def bench_quantize(tq, torch, n=1 << 20):
-    """Bulk quantize (d = 128, keys 3b + QJL, values 4b) of n token-heads: keys and
-    values, each timed on its own (inputs of 256 MB each, larger than L2)."""
+QUANT_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2 + 140   # bf16 K and V in, 140 B of records out (d = 128, 3b + QJL / 4b)
+
+
+def quantize_roofline(ms, n, kind, peaks, structured=False):
+    """Roofline of bulk quantize over n token-heads: max(bytes / HBM bandwidth, flops / tensor
+    peak).  Algorithmic flops per token-head: 2 d^2 for each dense product (Pi k, S r, Pi_v v)
+    and 2 d log2 d for each fast transform."""
+    d = 128
+    dense, fwht = 2 * d * d, 2 * d * int(math.log2(d))
+    flops = (3 * dense if kind == 0 else (2 * fwht + (fwht if structured else dense))) * n
+    nbytes = QUANT_BYTES_PER_TOKEN_HEAD * n
+    bw = peaks.get("hbm_gbs", 6800.0) * 1e9
+    tc = peaks.get("bf16_tflops", 1900.0) * 1e12
+    t_b, t_f = nbytes / bw, flops / tc
+    t = ms * 1e-3
+    bound = "hbm" if t_b >= t_f else "tensor"
+    return {"bound": bound, "achieved": (nbytes / t / 1e9) if bound == "hbm" else (flops / t / 1e12),
+            "peak": bw / 1e9 if bound == "hbm" else tc / 1e12, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": max(t_b, t_f) / t, "flops_per_token_head": flops / n, "bytes_per_token_head": nbytes / n}
+
+
+def bench_quantize(tq, torch, peaks, n=1 << 20):
+    """Bulk prefill quantize of n token-heads (d = 128, 8 KV heads, keys 3b + QJL, values 4b) on
+    the bulk recipe: bf16 N(0,1) K and V times lognormal(sigma = 1) channel scales per head.
+    Keys and values are timed separately (inputs of 256 MB each, larger than L2)."""
+    import synthetic_kv as SK
+
     out = {}
-    x = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
-    y = torch.randn(n, 128, device="cuda", dtype=torch.bfloat16)
+    w = SK.workload("bulk")
+    K, V, _ = SK.keys_values_torch(w, ctx=n // w.n_kv_heads)
+    x = K.reshape(n, w.d).contiguous()        # vector index = token * Hkv + head
+    y = V.reshape(n, w.d).contiguous()
+    del K, V
     for name, kind, structured in (("fwht", tq.TQ_FWHT, False), ("dense", tq.TQ_DENSE, False),
                                    ("fwht_structured_sketch", tq.TQ_FWHT, True)):
         L = tq.TQLayer(128, 8, 8, 3, 4, kind, qjl_structured=structured)
@@ -398,10 +614,89 @@ def bench_quantize(tq, torch, n=1 << 20):
             torch.cuda.synchronize()
             ms[role] = e0.elapsed_time(e1) / 5
         tot = ms["keys"] + ms["values"]
-        nbytes = n * (2 * 128 * 2 + 140)  # bf16 K, V in; 140 B of records out per token-head
         out[name] = {"token_heads_per_s": n / (tot * 1e-3), "ms": tot, "keys_ms": ms["keys"],
-                     "values_ms": ms["values"], "GB_per_s": nbytes / tot / 1e6}
+                     "values_ms": ms["values"], "GB_per_s": n * QUANT_BYTES_PER_TOKEN_HEAD / tot / 1e6,
+                     "roofline": quantize_roofline(tot, n, kind, peaks, structured)}
     return out
+
+
+def bench_prefill_quantize(tq, torch, L, w, peaks, calls=3):
+    """Prefill of the workload's cache: every sequence's n_c compressed tokens quantized
+    straight into their pages in one direct-slot append call (keys and values), as
+    PagedCache.prefill does.  Bytes per token-head: bf16 K, V in, one record out."""
+    import synthetic_kv as SK
+
+    B, Hkv, T, W = w.batch, w.n_kv_heads, w.ctx, w.window
+    nc = 16 * (max(0, T - W) // 16)
+    pc = tq.PagedCache(L, B, T)
+    K, V, _ = SK.keys_values_torch(w, layer=7, ctx=nc)
+    kk = K.reshape(B * nc, Hkv, w.dh).contiguous()
+    vv = V.reshape(B * nc, Hkv, w.dh).contiguous()
+    del K, V
+    slots = pc.slot_mapping(nc)
+    tq.append_page(L.params, pc.cache, kk, vv, B * nc, slots, None)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record()
+    for _ in range(calls):
+        tq.append_page(L.params, pc.cache, kk, vv, B * nc, slots, None)
+    e1.record()
+    torch.cuda.synchronize()
+    if tq.check_device_error():
+        raise RuntimeError("device error in the prefill benchmark")
+    ms = e0.elapsed_time(e1) / calls
+    kr, vr = workload_records(w)
+    per = 2 * 2 * w.dh + kr + vr
+    n = B * nc * Hkv
+    bw = peaks.get("hbm_gbs", 6800.0)
+    gbs = n * per / (ms * 1e-3) / 1e9
+    return {"token_heads": n, "ms": ms, "token_heads_per_s": n / (ms * 1e-3), "GB_per_s": gbs,
+            "hbm_fraction": gbs / bw, "bytes_per_token_head": per,
+            "config": f"{B} sequences x {nc} tokens x {Hkv} KV heads into pages (one call)"}
+
+
+def quality_report(tq, torch, T=4096):
+    """Attention quality on the long-context workload's first T tokens (d = 256, 2 KV / 16 q heads,
+    FWHT, keys 2b + QJL, values 2b, no window): the GPU decode over the compressed cache against
+    exact attention in float64 on the same bf16 K, V and q.  Reports the largest output error, the
+    output cosine and KL(p_exact || p_tq) of the attention weights per query head
+    ([Reconstruction] §15, Experiment A's metric).  A report, not a gate."""
+    import numpy as np
+
+    import synthetic_kv as SK
+
+    w = SK.workload("long")
+    K, V, q = SK.keys_values_torch(w, ctx=T)
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window, seed=w.seed)
+    pc = tq.PagedCache(L, 1, T)
+    pc.prefill(K, V)
+    ws = torch.empty(tq.decode_workspace_size(L.params, 1, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(1, w.n_q_heads, w.d, device="cuda")
+    scores = torch.zeros(1, w.n_q_heads, T, device="cuda")
+    tq.decode_attention(L.params, pc.cache, q, 1.0 / math.sqrt(w.d), out, None, scores, ws, T)
+    torch.cuda.synchronize()
+    if tq.check_device_error():
+        raise RuntimeError("device error in the quality report")
+    G = w.n_q_heads // w.n_kv_heads
+    Kf = K[0].double().cpu().numpy()          # [T, Hkv, d]
+    Vf = V[0].double().cpu().numpy()
+    qf = q[0].double().cpu().numpy()          # [Hq, d]
+    kv = np.arange(w.n_q_heads) // G
+    logits = np.einsum("hd,thd->ht", qf, Kf[:, kv]) / math.sqrt(w.d)
+    pe = np.exp(logits - logits.max(1, keepdims=True))
+    pe /= pe.sum(1, keepdims=True)
+    oe = np.einsum("ht,thd->hd", pe, Vf[:, kv])
+    st = scores[0].double().cpu().numpy()
+    pt = np.exp(st - st.max(1, keepdims=True))
+    pt /= pt.sum(1, keepdims=True)
+    ot = out[0].double().cpu().numpy()
+    kl = np.sum(pe * (np.log(pe) - np.log(pt)), axis=1)
+    cos = np.sum(oe * ot, 1) / (np.linalg.norm(oe, axis=1) * np.linalg.norm(ot, axis=1))
+    return {"tokens": T,
+            "workload": "long-context first 4096 tokens: d=256, 2 KV / 16 q heads, FWHT, keys 2b+QJL, values 2b",
+            "max_abs_out_err": float(np.abs(ot - oe).max()), "out_cosine_mean": float(cos.mean()),
+            "out_cosine_min": float(cos.min()), "kl_mean": float(kl.mean()), "kl_max": float(kl.max()),
+            "logit_max_abs_err": float(np.abs(st - logits).max())}
 
 
 def bench_prefill(tq, torch, L, pc, w, recs, nq=64, calls=5):
@@ -518,15 +813,26 @@ def run_gpu(args):
             dec_ev[1].record()
         return step_bytes(T[l], W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs)
 
+    props = torch.cuda.get_device_properties(local)
+    bus = (f"{getattr(props, 'pci_bus_id', 0):02x}:{getattr(props, 'pci_device_id', 0):02x}"
+           if hasattr(props, "pci_bus_id") else None)
+    clocks = Clocks(bus)
+    clocks.start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    # the clock sampler sees the GPU under this load for ~0.4 s before the timed steps (decode
+    # calls only: the caches are not appended to)
+    t_soak = time.monotonic()
+    while time.monotonic() - t_soak < 0.4:
+        for l in range(args.layers):
+            tq.decode_attention(layers[l].params, caches[l].cache, qs[l], scale, out, None, None, work, max_ctx)
+        torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clocks = Clocks(local)
-    clocks.start()
     ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    clocks.mark("timed", "start")
     torch.cuda.nvtx.range_push("timed")
     t0.record()
     total_bytes = 0
@@ -535,7 +841,9 @@ def run_gpu(args):
     t1.record()
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clocks.mark("timed", "end")
+    clocks.stop()
+    clk = clocks.summary("timed")
     ms = t0.elapsed_time(t1)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
     if tq.check_device_error():
@@ -565,14 +873,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms)
+    peaks = measured_peaks() or {}
     pre = bench_prefill(tq, torch, layers[0], caches[0], w, recs)
-    quant = bench_quantize(tq, torch)
+    del caches
+    pre_q = bench_prefill_quantize(tq, torch, layers[0], w, peaks) if not w.kivi else None
+    quant = bench_quantize(tq, torch, peaks)
     app = bench_append_batch256(tq, torch)
+    qual = quality_report(tq, torch)
     if rank != 0:
         return
-    peaks = measured_peaks()
-    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else 6800.0
-    peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
+    peak = peaks["hbm_gbs"] if "hbm_gbs" in peaks else 6800.0
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     value = total_bytes * ws / (ms * 1e-3) / 1e9
     # roofline of the decode call (prologue + tensor-core split-K kernel + combine),
     # algorithmic bytes of its reads and writes per launch over its measured duration
@@ -595,13 +906,16 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "tq_decode_attention (prologue + split-K tensor-core + combine)",
                      "peak_source": peak_src},
-        "quantize": {"metric": "bulk quantize token-heads/s (d=128, keys 3b+QJL, values 4b, 2^20 token-heads)",
+        "quantize": {"metric": ("bulk quantize token-heads/s (d=128, 8 KV heads, keys 3b+QJL, values 4b, 2^20 "
+                                "token-heads of the bulk recipe: bf16 N(0,1) x lognormal(sigma=1) channel scales)"),
                      "fwht": dict(quant["fwht"], hbm_fraction=quant["fwht"]["GB_per_s"] / peak),
                      "dense": dict(quant["dense"], hbm_fraction=quant["dense"]["GB_per_s"] / peak),
                      "fwht_structured_sketch": dict(quant["fwht_structured_sketch"],
                                                     hbm_fraction=quant["fwht_structured_sketch"]["GB_per_s"] / peak)},
+        "prefill_quantize": pre_q,
         "append_batch256": app,
         "prefill": pre,
+        "quality": qual,
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
                 "d2h_bytes_per_step": int(hout.numel() * 4)},

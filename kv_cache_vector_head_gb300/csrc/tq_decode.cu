@@ -64,7 +64,7 @@ constexpr int kMmaThreads = 256;
 constexpr int kMmaPages = kMmaThreads / 32;  // pages per chunk: one per warp in the key phase
 constexpr int kStages = 3;
 constexpr int kCombThreads = 256;
-constexpr int kPrologueTile = 2;  // query vectors per prologue CTA (measured best of 1, 2, 4: shortest critical path)
+constexpr int kPrologueTile = 4;  // query vectors per prologue CTA: one wave of CTAs at the bench shapes
 constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -161,24 +161,11 @@ __device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t 
   const uint32_t src = i >= 10 ? w0 : (i >= 4 ? w6 : w10);
   return (src & (0x00010001u << p)) ^ (p == 14 ? b2 : b1);
 }
-// value token slot s of a page pair: position 10 + (s & 1) for s < 8, 14 + (s & 1) above
-__host__ __device__ constexpr int xpos_val(int s) { return (s < 8 ? 10 : 14) + (s & 1); }
+// Token slot t = 4 t4 + 2 e + k of a page (lane t4, register e, k-step k of the value
+// tiles): a lane's 32-bit plane word (page A's 16 slots low, page B's high) shifted left by
+// 12 - 4 t4 puts its slots at f16 bit positions 12 + 2 e + k, i.e. 12..15.
+__host__ __device__ constexpr int xpos_val(int t) { return 12 + (t & 3); }
 
-// N adjacent 16-bit entries (N = 2 or 4, 4N-byte aligned) in one shared-memory load.
-template <int N>
-__device__ __forceinline__ void vload_u16(uint16_t (&out)[N], const uint16_t* p) {
-  if (N == 4) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    out[0] = (uint16_t)(v.x & 0xffffu);
-    out[1] = (uint16_t)(v.x >> 16);
-    out[N > 2 ? 2 : 0] = (uint16_t)(v.y & 0xffffu);
-    out[N > 3 ? 3 : 0] = (uint16_t)(v.y >> 16);
-  } else {
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-    out[0] = (uint16_t)(v & 0xffffu);
-    out[N > 1 ? 1 : 0] = (uint16_t)(v >> 16);
-  }
-}
 // N adjacent floats (N = 2 or 4, 4N-byte aligned) in one global store.
 template <int N>
 __device__ __forceinline__ void vstore_f32(float* p, const float (&v)[N]) {
@@ -244,7 +231,6 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constant__ KParams P, const void* q,
                                                             int dtype, unsigned char* ws, WsLayout L, int batch) {
   constexpr int KS = D / 16;
-  constexpr int TPR = D / 64;  // threads per row of S: each CTA owns 64 rows (coordinates 64 z .. 64 z + 63)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
   const int g = blockIdx.x, z = blockIdx.z, j = threadIdx.x;
@@ -254,6 +240,19 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   const int G = P.G;
   const int n0 = blockIdx.y * kPrologueTile;
   const int nv = min(kPrologueTile, batch * G - n0);
+  // the rows of S this thread multiplies do not depend on the query: their loads are issued
+  // first and land while the query is loaded and rotated
+  constexpr int TPR = D / 64;  // threads per row of S: each CTA owns 64 rows (coordinates 64 z .. 64 z + 63)
+  const bool dense_s = P.kqjl == TQ_KEY_QJL && !P.qjl_srht;
+  // thread su of a row takes the float4 columns i4 * TPR + su: TPR neighbouring threads read
+  // contiguous 16-byte pieces of S and of the query (no shared-memory bank conflicts)
+  const int srow = 64 * z + j / TPR, su = j % TPR;
+  float4 sreg[16];
+  if (dense_s) {
+    const float4* rp = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)srow * D) + su;
+#pragma unroll
+    for (int i4 = 0; i4 < 16; ++i4) sreg[i4] = __ldg(rp + i4 * TPR);
+  }
   for (int v = 0; v < kPrologueTile; ++v) {
     const int n = n0 + v, b = n / G, hl = n % G;
     s.x[v][j] = (v < nv && j < P.dh) ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * P.dh + j))
@@ -275,19 +274,17 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
 #pragma unroll
       for (int e = 0; e < E; ++e) s.r[v][e * 32 + lane] = a[e];
     }
-  } else if (P.kqjl == TQ_KEY_QJL) {
-    // q'' rows of this CTA: TPR neighbouring threads per row, 64 inputs each
-    const int row = 64 * z + j / TPR, u = j % TPR;
-    const float4* rp = reinterpret_cast<const float4*>(P.qjl_s + (size_t)g * D * D + (size_t)row * D) + u * 16;
+  } else if (dense_s) {
+    // q'' rows of this CTA: TPR neighbouring threads per row, 64 inputs each (row segment in sreg)
     float acc[kPrologueTile];
 #pragma unroll
     for (int v = 0; v < kPrologueTile; ++v) acc[v] = 0.f;
-#pragma unroll 8
+#pragma unroll
     for (int i4 = 0; i4 < 16; ++i4) {
-      const float4 p = __ldg(rp + i4);
+      const float4 p = sreg[i4];
 #pragma unroll
       for (int v = 0; v < kPrologueTile; ++v) {
-        const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][(u * 16 + i4) * 4]);  // rows >= nv hold zeros
+        const float4 xv = *reinterpret_cast<const float4*>(&s.x[v][(i4 * TPR + su) * 4]);  // rows >= nv hold zeros
         acc[v] = fmaf(p.x, xv.x, fmaf(p.y, xv.y, fmaf(p.z, xv.z, fmaf(p.w, xv.w, acc[v]))));
       }
     }
@@ -295,7 +292,7 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
     for (int v = 0; v < kPrologueTile; ++v) {
 #pragma unroll
       for (int o = 1; o < TPR; o <<= 1) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
-      if (v < nv && u == 0) s.r[v][row] = acc[v];
+      if (v < nv && su == 0) s.r[v][srow] = acc[v];
     }
   }
   __syncthreads();
@@ -526,6 +523,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ MmaShared sh;
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // the combine kernel may be scheduled once every CTA of this grid has started; it waits
+  // for the whole grid before it reads the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (s == L.n_comp_splits) {  // the float16 window runs as the last split
     window_split<D>(P, C, q, dtype, scale, scores, ws, L, max_ctx, g, b, dyn);
     return;
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int jw = 0; jw < WPL; ++jw) {
-            const int tk = 8 * nt + g8, w = t4 + 4 * jw;
+            const int tk = 2 * g8 + nt, w = t4 + 4 * jw;
             rs[nt][jw] = kc[tk * E + w];
 #pragma unroll
             for (int m = 0; m < 3; ++m)
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
 #pragma unroll
               for (int m = 0; m < 3; ++m) hm[m][nt] = rm[m][nt][0];
             } else {  // d = 128: word t4 & 1 shifted right by 8 (t4 >> 1)
-              const int tk = 8 * nt + g8, w = t4 & 1, sh = 8 * (t4 >> 1);
+              const int tk = 2 * g8 + nt, w = t4 & 1, sh = 8 * (t4 >> 1);
               hs[nt] = kc[tk * E + w] >> sh;
 #pragma unroll
               for (int m = 0; m < 3; ++m)
@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int jw = 0; jw < WPL; ++jw) {
-              q0[nt][jw] = ks[(8 * nt + g8) * E + t4 + 4 * jw];
+              q0[nt][jw] = ks[(2 * g8 + nt) * E + t4 + 4 * jw];
               q6[nt][jw] = q0[nt][jw] << 6;
               q10[nt][jw] = q0[nt][jw] << 10;
             }
@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int t = 8 * nt + 2 * t4 + e;
+          const int t = 4 * t4 + 2 * e + nt;  // column 2 t4 + e of n-tile nt (column g of n-tile nt is token 2 g + nt)
           const int tok = pg * kPage + t;
           const bool live = pvalid && g8 < G && tok < nc;
           float l = -INFINITY;
@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
         m_run = mnew;
       }
       // weights of this warp's page, written in A-fragment order of its page pair:
-      // token t = 8 nt + 2 t4 + e -> k-step nt, lane (g8, t4), component 2 e (hi) / 2 e + 1 (lo),
+      // token t = 4 t4 + 2 e + nt -> k-step nt, lane (g8, t4), component 2 e (hi) / 2 e + 1 (lo),
       // half = page parity within the pair
       const float* vnorm = reinterpret_cast<const float*>(pb + P.off_vnorm);
       uint16_t* wfh = reinterpret_cast<uint16_t*>(&sh.wf[warp >> 1][0][0]);
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int t = 8 * nt + 2 * t4 + e;
+          const int t = 4 * t4 + 2 * e + nt;
           float wgt = 0.f;
           if (sc[nt][e] != -INFINITY) {
             const float ex = expf(sc[nt][e] - m_run);
@@ -890,43 +890,54 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       const uint16_t* vbp = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg + 1) * sub + P.off_vcodes);
       const uint4 wf0 = sh.wf[jg][0][lane], wf1 = sh.wf[jg][1][lane];
       if (!VLUT) {
-        // plane words (token slot s <-> bit s of each half), shifted so that slots 2 t4 + e sit at
-        // positions 10 + e (k-step 0) and slots 8 + 2 t4 + e at 14 + e (k-step 1)
-        // column g8 of n-tile cbk is coordinate warp * CPW + g8 * CB + cbk: a lane's CB entries of a
-        // plane are adjacent (one vector load per page and plane)
+        // plane words: page A's 16 slots in bits 0..15, page B's in 16..31 (one byte permute per
+        // word); column g8 of n-tile cbk is coordinate warp * CPW + g8 * CB + cbk, so a lane's CB
+        // entries of a plane are adjacent (one vector load per page and plane).  Shifted left by
+        // 12 - 4 t4, the lane's slots 4 t4 + 2 e + k sit at bit 12 + 2 e + k of each half: operand
+        // register e of k-step k is one LOP3 (mask, then XOR into 1.0 / 2.0)
         uint32_t u0[CB], u1[CB];
         {
           const int c0 = warp * CPW + g8 * CB;
-          uint16_t a0[CB], b0[CB], a1[CB], b1[CB];
-          vload_u16<CB>(a0, va + c0);
-          vload_u16<CB>(b0, vbp + c0);
-          if (vb2) {
-            vload_u16<CB>(a1, va + D + c0);
-            vload_u16<CB>(b1, vbp + D + c0);
-          }
-#pragma unroll
-          for (int cbk = 0; cbk < CB; ++cbk) {
-            u0[cbk] = (uint32_t)a0[cbk] | ((uint32_t)b0[cbk] << 16);
-            u1[cbk] = vb2 ? (u0[cbk] ^ ((uint32_t)a1[cbk] | ((uint32_t)b1[cbk] << 16))) : 0u;
+          if constexpr (CB == 4) {
+            const uint2 a0 = *reinterpret_cast<const uint2*>(va + c0), b0 = *reinterpret_cast<const uint2*>(vbp + c0);
+            u0[0] = __byte_perm(a0.x, b0.x, 0x5410);
+            u0[1] = __byte_perm(a0.x, b0.x, 0x7632);
+            u0[CB > 2 ? 2 : 0] = __byte_perm(a0.y, b0.y, 0x5410);
+            u0[CB > 3 ? 3 : 0] = __byte_perm(a0.y, b0.y, 0x7632);
+            if (vb2) {
+              const uint2 a1 = *reinterpret_cast<const uint2*>(va + D + c0),
+                          b1 = *reinterpret_cast<const uint2*>(vbp + D + c0);
+              u1[0] = __byte_perm(a1.x, b1.x, 0x5410);
+              u1[1] = __byte_perm(a1.x, b1.x, 0x7632);
+              u1[CB > 2 ? 2 : 0] = __byte_perm(a1.y, b1.y, 0x5410);
+              u1[CB > 3 ? 3 : 0] = __byte_perm(a1.y, b1.y, 0x7632);
+            }
+          } else {
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(va + c0),
+                           b0 = *reinterpret_cast<const uint32_t*>(vbp + c0);
+            u0[0] = __byte_perm(a0, b0, 0x5410);
+            u0[CB > 1 ? 1 : 0] = __byte_perm(a0, b0, 0x7632);
+            if (vb2) {
+              const uint32_t a1 = *reinterpret_cast<const uint32_t*>(va + D + c0),
+                             b1 = *reinterpret_cast<const uint32_t*>(vbp + D + c0);
+              u1[0] = __byte_perm(a1, b1, 0x5410);
+              u1[CB > 1 ? 1 : 0] = __byte_perm(a1, b1, 0x7632);
+            }
           }
         }
+        const int vsh = 12 - 4 * t4;
 #pragma unroll
-        for (int ksx = 0; ksx < 2; ++ksx) {
-          const uint4 wfk = ksx ? wf1 : wf0;
-          const int sft = (ksx ? 6 : 10) - 2 * t4, pa = ksx ? 14 : 10;
+        for (int cbk = 0; cbk < CB; ++cbk) {
+          const uint32_t x0 = u0[cbk] << vsh;
+          const uint32_t xm = vb2 ? (u1[cbk] << vsh) : 0u;
 #pragma unroll
-          for (int cbk = 0; cbk < CB; ++cbk) {
-            const uint32_t x = u0[cbk] << sft;
-            mma16816(accv[0][cbk], wfk, (x & (0x00010001u << pa)) ^ (ksx ? xb2 : xb1),
-                     (x & (0x00010001u << (pa + 1))) ^ xb1);
-          }
-          if (vb2) {
-#pragma unroll
-            for (int cbk = 0; cbk < CB; ++cbk) {
-              const uint32_t x = u1[cbk] << sft;
-              mma16816(accv[1][cbk], wfk, (x & (0x00010001u << pa)) ^ (ksx ? xb2 : xb1),
-                       (x & (0x00010001u << (pa + 1))) ^ xb1);
-            }
+          for (int ksx = 0; ksx < 2; ++ksx) {
+            const uint4 wfk = ksx ? wf1 : wf0;
+            const int pA = 12 + ksx, pB = 14 + ksx;  // register e = 0, 1
+            const uint32_t mA = 0x00010001u << pA, mB = 0x00010001u << pB;
+            const uint32_t bA = (x0 & mA) ^ (pA == 14 ? xb2 : xb1), bB = (x0 & mB) ^ (pB == 14 ? xb2 : xb1);
+            mma16816(accv[0][cbk], wfk, bA, bB);
+            if (vb2) mma16816(accv[1][cbk], wfk, bA ^ (xm & mA), bB ^ (xm & mB));  // Walsh plane sign ^ magnitude
           }
         }
       } else {
@@ -939,14 +950,14 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
 #pragma unroll
           for (int ksx = 0; ksx < 2; ++ksx) {
-            const int i0 = 8 * ksx + 2 * t4;
+            const int i0 = 4 * t4 + ksx, i1 = i0 + 2;  // slots of registers e = 0 and e = 1
             uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
 #pragma unroll
             for (int p = 0; p < TQ_MAX_BITS; ++p) {
               rA0 |= ((u[p] >> i0) & 1u) << p;
               rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
-              rA1 |= ((u[p] >> (i0 + 1)) & 1u) << p;
-              rB1 |= ((u[p] >> (i0 + 17)) & 1u) << p;
+              rA1 |= ((u[p] >> i1) & 1u) << p;
+              rB1 |= ((u[p] >> (i1 + 16)) & 1u) << p;
             }
             const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
             const uint4 wfk = ksx ? wf1 : wf0;
@@ -1030,10 +1041,22 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
   __shared__ float Msh, Lsh;
   const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.G, g = hq / G;
+  // launched as a programmatic dependent of the decode kernel: wait for all of its partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int st = L.n_comp_splits + 1;
   const size_t head = (size_t)b * P.hq + hq;
   const float* ml = reinterpret_cast<const float*>(ws + L.ml) + head * st * 2;
   const float* acc = reinterpret_cast<const float*>(ws + L.acc) + head * st * D;
+  // the first kPre partial rows of this thread's split group are loaded up front, together with
+  // the split maxima (one memory round trip instead of three)
+  constexpr int kPre = 8;
+  const int sg = tid / TPR, c4 = tid % TPR;
+  float4 pre[kPre];
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) {
+    const int k = sg + r * SG;
+    pre[r] = k < st - 1 ? reinterpret_cast<const float4*>(acc + (size_t)k * D)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float m = -INFINITY;
   for (int k = tid; k < st; k += kCombThreads) m = fmaxf(m, ml[2 * k]);
   m = warp_max_f(m);
@@ -1062,12 +1085,22 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
     for (int w = 0; w < kCombThreads / 32; ++w) s2 += red[w];
     Lsh = s2;
   }
-  // compressed splits 0 .. st-2: group sg sums splits sg, sg + SG, ...
+  // compressed splits 0 .. st-2: group sg sums splits sg, sg + SG, ... in a fixed order
   {
-    const int sg = tid / TPR, c4 = tid % TPR;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kPre; ++r) {
+      const int k = sg + r * SG;
+      if (k < st - 1) {
+        const float f = fsplit[k];
+        a.x = fmaf(f, pre[r].x, a.x);
+        a.y = fmaf(f, pre[r].y, a.y);
+        a.z = fmaf(f, pre[r].z, a.z);
+        a.w = fmaf(f, pre[r].w, a.w);
+      }
+    }
 #pragma unroll 4
-    for (int k = sg; k < st - 1; k += SG) {
+    for (int k = sg + kPre * SG; k < st - 1; k += SG) {
       const float f = fsplit[k];
       const float4 v = reinterpret_cast<const float4*>(acc + (size_t)k * D)[c4];
       a.x = fmaf(f, v.x, a.x);
@@ -1495,7 +1528,19 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
     e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cdyn);
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<D><<<dim3(P.hq, C.batch), kCombThreads, cdyn, st>>>(P, w, L, out, lse);
+  // programmatic dependent launch: scheduled while the decode grid drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.hq, C.batch);
+  cfg.blockDim = dim3(kCombThreads);
+  cfg.dynamicSmemBytes = cdyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, P, (const unsigned char*)w, L, out, lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

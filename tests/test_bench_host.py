@@ -69,3 +69,35 @@ def test_max_over_ranks_gloo_two_ranks():
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 11.0), (1, 11.0)]
     assert bench.max_over_ranks(3.5) == 3.5  # single process: identity
+
+
+def test_clock_summary_picks_the_gpu_and_the_window():
+    """The sampler keeps the rows of the bench's GPU (PCI bus:device) and the samples inside the
+    timed window; a window shorter than the sampling period is bracketed by its neighbours."""
+    c = bench.Clocks("1b:00")
+    row = lambda t, bus, sm, why=(): {"t": t, "bus": bus, "sm": sm, "max": 2070.0, "reasons": list(why)}
+    c.samples = [row(1.00, "00000000:1B:00.0", 2070.0), row(1.05, "00000000:1C:00.0", 300.0),
+                 row(1.50, "00000000:1B:00.0", 1900.0, ["sw_power_cap"]), row(3.0, "00000000:1B:00.0", 2070.0)]
+    c.windows = {"timed": [1.2, 1.3]}
+    s = c.summary("timed")
+    assert s["how"].startswith("bracketing") and s["samples"] == 2 and s["sm_mhz"] == 1985.0
+    assert s["reasons"] == ["sw_power_cap"]
+    c.windows = {"timed": [0.9, 1.6]}
+    s = c.summary("timed")
+    assert s["how"] == "inside the window" and s["samples"] == 2 and s["sm_max_mhz"] == 2070.0
+    assert bench.Clocks.bus_key("00000009:01:00.0") == "01:00"
+    assert bench.Clocks(None).summary("timed") is None  # no samples, no window
+
+
+def test_quantize_roofline_bounds():
+    """Dense-mode bulk quantize is HBM-bound at the measured peaks: 652 B and 3 x 2 d^2 flops per
+    token-head (d = 128); FWHT mode keeps one dense product (the Gaussian sketch)."""
+    peaks = {"hbm_gbs": 6694.2, "bf16_tflops": 1942.3}
+    n = 1 << 20
+    r = bench.quantize_roofline(1.0, n, 0, peaks)
+    assert r["bound"] == "hbm" and r["bytes_per_token_head"] == 652 and r["flops_per_token_head"] == 3 * 2 * 128 ** 2
+    assert abs(r["frac"] - 652 * n / 6694.2e9 / 1e-3) < 1e-12
+    f = bench.quantize_roofline(1.0, n, 1, peaks)
+    assert f["flops_per_token_head"] == 2 * 128 ** 2 + 2 * 2 * 128 * 7
+    s = bench.quantize_roofline(1.0, n, 1, peaks, structured=True)
+    assert s["flops_per_token_head"] == 3 * 2 * 128 * 7
