@@ -251,6 +251,30 @@ typedef struct {
   int batch;
 } tq_cache;
 
+/*
+ * tq_prefill_cache -- fill every sequence of a cache with its first n_tok
+ * tokens, applying the window rule of this page format in the library
+ * ([Design study] §Packed format "Recent tokens", §Paging): with a window
+ * W > 0 the
+ *   n_c = 16 * floor(max(0, n_tok - W) / 16)
+ * oldest tokens are quantized into their pages (position p of sequence b into
+ * page block_table[b][p / 16], slot p % 16; whole pages, so the KIVI arm is
+ * served too); without a window n_c = n_tok (the last page may be partly
+ * filled, as decode-step appends leave it).  The remaining n_tok - n_c
+ * (W .. W + 15 once n_tok >= W) are
+ * written to the float16 window ring (position p at ring slot p mod (W + 16),
+ * rows zero-padded past head_dim), and seq_len[b] = n_tok,
+ * n_compressed[b] = n_c.  Decode-step appends (tq_append_page without a slot
+ * mapping) continue from that state.
+ *   k, v    [device] [batch][n_tok][Hkv][head_dim] in dtype, 16-byte aligned
+ *   n_tok   tokens per sequence, >= 0
+ * The sequences' previous contents are overwritten.  TQ_ERR_CAPACITY if n_c
+ * needs more than max_pages_per_seq pages.  Page ids outside the pool set
+ * TQ_DEVERR_SLOT in the device error word (those tokens are skipped).
+ */
+tq_status tq_prefill_cache(const tq_layer_params* p, tq_cache* cache, const void* k, const void* v,
+                           tq_dtype dtype, int n_tok, tq_stream_t stream);
+
 /* Bytes of one (page, kv head) sub-block; 0 for invalid parameters. */
 size_t tq_subblock_bytes(const tq_layer_params* p);
 
@@ -321,6 +345,10 @@ tq_status tq_decode_attention(const tq_layer_params* p, const tq_cache* cache, c
  * returns TQ_ERR_CAPACITY and launches nothing.  Nothing is allocated.
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: after cudaDeviceReset
+ *     (or anything else that destroys the device's primary context) it no
+ *     longer refers to the array, so a process that resets a device must not
+ *     call this entry point on that device again.
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (other streams, other host threads) race and corrupt each other's
  *     scratch.  Serialise them on one stream.  The array keeps the last call's

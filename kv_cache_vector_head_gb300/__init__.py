@@ -16,13 +16,13 @@ import numpy as np
 from . import _lib
 from ._lib import (KEY_EDEN, KEY_MSE, KEY_QJL, KEY_RENORM, PAGE_SIZE, ROLE_KEY_ROT, ROLE_QJL, ROLE_QJL_SIGNS, ROLE_VALUE_ROT, TQ_BF16, TQ_DENSE, TQ_F16, TQ_F32, TQ_FWHT,
                    Cache, LayerParams, TQError, append_page, build_codebook, build_transform, check_device_error,
-                   decode_attention, decode_workspace_size, prefill_attention, prefill_workspace_size, quantize_keys,
-                   quantize_values, subblock_bytes)
+                   decode_attention, decode_workspace_size, prefill_attention, prefill_cache, prefill_workspace_size,
+                   quantize_keys, quantize_values, subblock_bytes)
 
 __all__ = [
     "TQLayer", "PagedCache", "LayerParams", "Cache", "TQError", "build_codebook", "build_transform",
     "quantize_keys", "quantize_values", "append_page", "decode_workspace_size", "decode_attention",
-    "prefill_workspace_size", "prefill_attention", "norm_range_for", "bits_per_channel",
+    "prefill_workspace_size", "prefill_attention", "prefill_cache", "norm_range_for", "bits_per_channel",
     "check_device_error", "subblock_bytes", "TQ_DENSE", "TQ_FWHT", "TQ_F32", "TQ_BF16", "TQ_F16", "PAGE_SIZE",
     "ROLE_KEY_ROT", "ROLE_VALUE_ROT", "ROLE_QJL", "ROLE_QJL_SIGNS", "KEY_MSE", "KEY_QJL", "KEY_EDEN", "KEY_RENORM",
 ]
@@ -48,11 +48,6 @@ def bits_per_channel(layer: "TQLayer") -> dict:
     total = subblock_bytes(layer.params) * 8 / (PAGE_SIZE * layer.d)
     return {"kv_bits_per_channel": total / 2, "kv_total_bits_per_channel": total,
             "compression_vs_fp16": 32.0 / total}
-
-
-def n_compressed(T: int, window: int) -> int:
-    """Compressed tokens at length T: 16 * floor(max(0, T - W) / 16)."""
-    return PAGE_SIZE * (max(0, T - window) // PAGE_SIZE)
 
 
 class TQLayer:
@@ -175,23 +170,11 @@ class PagedCache:
         return (pages * PAGE_SIZE + (pos % PAGE_SIZE)[None, :]).reshape(-1)
 
     def prefill(self, k, v, stream=None) -> None:
-        """Fill every sequence with T tokens: k, v [batch, T, Hkv, d].
-
-        Tokens 0..n_c-1 are quantized straight into their pages (direct
-        slots); the remaining T - n_c (< W + 16) go through decode-step
-        appends into the float16 window, exactly as live decoding would.
-        """
-        B, T = k.shape[0], k.shape[1]
-        nc = n_compressed(T, self.layer.window)
-        self.seq_len.fill_(nc)
-        self.n_compressed.fill_(nc)
-        if nc:
-            slots = self.slot_mapping(nc)
-            kk = k[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.head_dim).contiguous()
-            vv = v[:, :nc].reshape(B * nc, self.layer.n_kv_heads, self.layer.head_dim).contiguous()
-            append_page(self.layer.params, self.cache, kk, vv, B * nc, slots, stream)
-        for t in range(nc, T):
-            append_page(self.layer.params, self.cache, k[:, t].contiguous(), v[:, t].contiguous(), B, None, stream)
+        """Fill every sequence with T tokens: k, v [batch, T, Hkv, head_dim].  The library
+        (tq_prefill_cache) applies the window rule: the oldest whole pages are quantized
+        straight into their pages, the last W .. W + 15 tokens go to the float16 window, and
+        the counters are set, as live decoding would leave them."""
+        prefill_cache(self.layer.params, self.cache, k.contiguous(), v.contiguous(), k.shape[1], stream)
 
     def append(self, k, v, stream=None) -> None:
         """One decode step: k, v [batch, Hkv, d]."""

@@ -26,7 +26,7 @@ PAGE_SIZE = 16
 EXPORTED = [
     "tq_build_codebook", "tq_build_transform", "tq_quantize_keys", "tq_quantize_values", "tq_subblock_bytes",
     "tq_append_page", "tq_decode_workspace_size", "tq_decode_attention", "tq_check_device_error", "tq_last_error",
-    "tq_decode_attention_static", "tq_prefill_workspace_size", "tq_prefill_attention",
+    "tq_decode_attention_static", "tq_prefill_workspace_size", "tq_prefill_attention", "tq_prefill_cache",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -78,6 +78,7 @@ def lib():
         L.tq_subblock_bytes.restype = c_size_t
         L.tq_append_page.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_void_p, c_int, c_int64,
                                      c_void_p, c_void_p]
+        L.tq_prefill_cache.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_void_p, c_int, c_int, c_void_p]
         L.tq_decode_workspace_size.argtypes = [POINTER(LayerParams), c_int, c_int, c_int]
         L.tq_decode_workspace_size.restype = c_size_t
         L.tq_decode_attention.argtypes = [POINTER(LayerParams), POINTER(Cache), c_void_p, c_int, c_float, c_void_p,
@@ -161,6 +162,13 @@ def quantize_values(p: LayerParams, v, n_vec: int, codes, norms, stream=None) ->
 def append_page(p: LayerParams, cache: Cache, k, v, n_tok: int, slot_mapping=None, stream=None) -> None:
     _check(lib().tq_append_page(ctypes.byref(p), ctypes.byref(cache), _ptr(k), _ptr(v), dtype_code(k), n_tok,
                                 _ptr(slot_mapping), _stream(stream)))
+
+
+def prefill_cache(p: LayerParams, cache: Cache, k, v, n_tok: int, stream=None) -> None:
+    """Every sequence gets its first n_tok tokens (k, v [batch, n_tok, Hkv, head_dim]); the
+    library splits them into pages and the float16 window and sets the counters."""
+    _check(lib().tq_prefill_cache(ctypes.byref(p), ctypes.byref(cache), _ptr(k), _ptr(v), dtype_code(k), n_tok,
+                                  _stream(stream)))
 
 
 def decode_workspace_size(p: LayerParams, batch: int, max_ctx: int, n_splits: int = 0) -> int:

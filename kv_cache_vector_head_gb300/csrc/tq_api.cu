@@ -1,6 +1,7 @@
 // C ABI entry points of libtq: argument checks on the host, then launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -269,6 +270,27 @@ extern "C" tq_status tq_append_page(const tq_layer_params* p, tq_cache* cache, c
                      "tq_append_page");
 }
 
+extern "C" tq_status tq_prefill_cache(const tq_layer_params* p, tq_cache* cache, const void* k, const void* v,
+                                      tq_dtype dtype, int n_tok, tq_stream_t stream) {
+  KParams K;
+  KCache C;
+  tq_status s = make_params(p, &K, true);
+  if (s != TQ_OK) return s;
+  if ((s = check_dtype(dtype)) != TQ_OK) return s;
+  if ((s = make_cache(cache, K, &C, true)) != TQ_OK) return s;
+  if (n_tok < 0) return fail(TQ_ERR_INVALID_ARG, "n_tok < 0");
+  if (n_tok > 0 && (!k || !v || !aligned(k, 16) || !aligned(v, 16)))
+    return fail(TQ_ERR_INVALID_ARG, "k / v null or not 16-byte aligned");
+  // the window rule of the page format: whole pages of the tokens older than the last W;
+  // without a window every token is in its page (the last one may be partly filled)
+  const int n_c = K.window > 0 ? TQ_PAGE_SIZE * (std::max(0, n_tok - K.window) / TQ_PAGE_SIZE) : n_tok;
+  if ((n_c + TQ_PAGE_SIZE - 1) / TQ_PAGE_SIZE > cache->max_pages_per_seq)
+    return fail(TQ_ERR_CAPACITY, "tq_prefill_cache: n_tok needs more pages than max_pages_per_seq");
+  if ((long long)cache->batch * n_c >= (1LL << 40)) return fail(TQ_ERR_INVALID_ARG, "tq_prefill_cache: too many tokens");
+  return cuda_status(launch_prefill_cache(K, C, k, v, dtype, n_tok, n_c, reinterpret_cast<cudaStream_t>(stream)),
+                     "tq_prefill_cache");
+}
+
 extern "C" size_t tq_decode_workspace_size(const tq_layer_params* p, int batch, int max_ctx, int n_splits) {
   KParams K;
   if (make_params(p, &K, false) != TQ_OK || batch < 1 || max_ctx < 0 || n_splits < 0) return 0;
@@ -359,6 +381,16 @@ extern "C" tq_status tq_check_device_error(tq_stream_t stream, uint32_t* bits_ou
   }
   return ok();
 }
+
+#ifdef TQ_TEST_HOOKS
+// Test build only (libtq_testhooks.so; not part of the C ABI in include/tq.h): on = 1 makes
+// the first chunk of every decode page split expect 16 bytes more than its copies deliver,
+// so that split's bounded wait runs out and reports TQ_DEVERR_TIMEOUT; on = 0 restores
+// normal decoding.
+extern "C" tq_status tq_test_wait_fault(int on) {
+  return cuda_status(set_test_wait_fault(on ? 1 : 0), "tq_test_wait_fault");
+}
+#endif
 
 // ------------------------------------------------------------------ decode without a workspace argument
 

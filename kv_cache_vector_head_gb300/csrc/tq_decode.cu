@@ -60,12 +60,28 @@ namespace tq {
 
 __device__ unsigned int g_decode_err = 0;
 
+#ifdef TQ_TEST_HOOKS
+// Test build only: when set, the first chunk of every page split expects 16 bytes more than
+// its copies deliver, so its barrier phase never completes and the bounded wait runs out.
+__device__ int g_test_wait_fault = 0;
+__device__ __forceinline__ uint32_t test_extra_tx(int k) { return (g_test_wait_fault && k == 0) ? 16u : 0u; }
+#else
+__device__ __forceinline__ uint32_t test_extra_tx(int) { return 0u; }
+#endif
+
 constexpr int kMmaThreads = 256;
 constexpr int kMmaPages = kMmaThreads / 32;  // pages per chunk: one per warp in the key phase
 constexpr int kStages = 3;
 constexpr int kCombThreads = 256;
 constexpr int kPrologueTile = 4;  // query vectors per prologue CTA: one wave of CTAs at the bench shapes
-constexpr unsigned kWaitLimit = 1u << 24;  // bounded mbarrier polling
+// Bounded mbarrier waits: at most kWaitLimit polls, each suspending at most kPollNs: about
+// a second in the library; the test build (TQ_TEST_HOOKS) gives up after ~16 ms.
+#ifdef TQ_TEST_HOOKS
+constexpr unsigned kWaitLimit = 1u << 14;
+#else
+constexpr unsigned kWaitLimit = 1u << 20;
+#endif
+constexpr unsigned kPollNs = 1000;
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -194,9 +210,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kPollNs)
       : "memory");
   return ok != 0;
 }
@@ -206,6 +222,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   for (unsigned i = 0; i < kWaitLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+
+// After a bounded wait ran out (stopped at chunk kstop, the same in every thread): flag it,
+// then give the copies still in flight (chunks kstop - 1 .. kstop + nst - 2) a second bounded
+// chance to land before the CTA's shared memory is released.  The partials of such a split
+// are not meaningful; the error word reports it.
+__device__ __forceinline__ void drain_after_timeout(uint64_t* full, bool timed_out, int kstop, int nchunks, int nst) {
+  if (!__syncthreads_or(timed_out)) return;
+  if (threadIdx.x == 0) atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
+  const int last = min(kstop + nst - 2, nchunks - 1);
+  for (int j = max(kstop - 1, 0); j <= last; ++j) (void)mbar_wait_bounded(&full[j % nst], (uint32_t)((j / nst) & 1));
 }
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -613,7 +640,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
     const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub);
+      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub + test_extra_tx(k));
     }
     __syncwarp();
     if (pid >= 0)
@@ -669,15 +696,18 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   float m_run = -INFINITY, l_run = 0.f;  // softmax state of head g8 (identical across warps for m)
   float kv_run = 0.f;                     // this lane's share of the value operand's constant K
   bool timed_out = false;
+  int kstop = nchunks;  // chunks consumed
 
   for (int k = 0; k < nchunks; ++k) {
-    __syncthreads();  // chunk k-1 fully consumed: its stage and sh.wf may be rewritten
+    // chunk k-1 fully consumed: its stage and sh.wf may be rewritten.  A wait that ran out
+    // stops the split here, for every thread alike (no new copies into unfinished phases)
+    if (__syncthreads_or(timed_out)) {
+      kstop = k;
+      break;
+    }
     if (warp == 0 && k + nst - 1 < nchunks) issue(k + nst - 1);
     const int stg = k % nst;
-    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) {
-      if (!timed_out) atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
-      timed_out = true;
-    }
+    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) timed_out = true;
     unsigned char* stbase = stage0 + (size_t)stg * NW * sub;
 
     // ---------------- key phase: warp w scores page w of the chunk
@@ -969,11 +999,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       }
     }
   }
-  if (timed_out) {
-    // a bounded wait ran out: give the copies still in flight a second bounded
-    // chance to land before the CTA's shared memory is released
-    for (int k = 0; k < nchunks; ++k) (void)mbar_wait_bounded(&sh.full[k % nst], (uint32_t)((k / nst) & 1));
-  }
+  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst);
   // ---- partials
   float ls = l_run, kvl = kv_run;
   ls += __shfl_xor_sync(0xffffffffu, ls, 1);
@@ -1259,7 +1285,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
     const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub);
+      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub + test_extra_tx(k));
     }
     __syncwarp();
     if (pid >= 0)
@@ -1274,15 +1300,18 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
 #pragma unroll
   for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] = 0.f;
   bool timed_out = false;
+  int kstop = nchunks;  // chunks consumed
 
   for (int k = 0; k < nchunks; ++k) {
-    __syncthreads();  // chunk k-1 consumed
+    // chunk k-1 fully consumed: its stage and sh.wf may be rewritten.  A wait that ran out
+    // stops the split here, for every thread alike (no new copies into unfinished phases)
+    if (__syncthreads_or(timed_out)) {
+      kstop = k;
+      break;
+    }
     if (warp == 0 && k + nst - 1 < nchunks) issue(k + nst - 1);
     const int stg = k % nst;
-    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) {
-      if (!timed_out) atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
-      timed_out = true;
-    }
+    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) timed_out = true;
     unsigned char* stbase = stage0 + (size_t)stg * NW * sub;
 
     // ---------------- scores: warp w, page w of the chunk; lane = (token t, coordinate half hf),
@@ -1396,6 +1425,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
       }
     }
   }
+  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst);
   __syncthreads();
   // token groups -> one partial per coordinate (the key scale rows are free now)
   float* red = &sh.ks[0][0];  // [TQ_MAX_GQA][D]
@@ -1572,6 +1602,10 @@ cudaError_t launch_prefill_virtual(const KCache& C, int n_query, int32_t* seq_v,
   prefill_virtual_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(C, n_query, seq_v, nc_v, parent);
   return cudaGetLastError();
 }
+
+#ifdef TQ_TEST_HOOKS
+cudaError_t set_test_wait_fault(int on) { return cudaMemcpyToSymbol(g_test_wait_fault, &on, sizeof(int)); }
+#endif
 
 cudaError_t read_clear_decode_error(unsigned* bits) {
   unsigned zero = 0;

@@ -13,6 +13,9 @@ cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, lon
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st);
 cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                  long long n_tok, const long long* slots, cudaStream_t st);
+// Whole sequences of seq_tok tokens: n_c into their pages, the rest into the window ring, counters set.
+cudaError_t launch_prefill_cache(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                 int seq_tok, int n_c, cudaStream_t st);
 cudaError_t launch_append_step(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                cudaStream_t st);
 
@@ -35,5 +38,8 @@ cudaError_t launch_prefill_virtual(const KCache& C, int n_query, int32_t* seq_v,
 
 cudaError_t read_clear_quant_error(unsigned* bits);
 cudaError_t read_clear_decode_error(unsigned* bits);
+#ifdef TQ_TEST_HOOKS
+cudaError_t set_test_wait_fault(int on);
+#endif
 
 }  // namespace tq

@@ -375,15 +375,19 @@ __device__ void kivi_store_page(const KParams& P, TileSmem<D>& s, bool is_key, u
 
 // ------------------------------------------------------------------ append: direct slots
 
+// Direct slots.  With slot_mapping: token t of the input goes to pool slot slot_mapping[t].
+// Without (prefill of whole sequences): token i = b n_c + p is position p of sequence b, read
+// from input row b seq_tok + p and stored in page block_table[b][p / 16], slot p % 16.
 template <int D>
 __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant__ KParams P,
                                                           const __grid_constant__ KCache C, const void* k,
                                                           const void* v, int dtype, long long n_tok,
-                                                          const long long* slot_mapping) {
+                                                          const long long* slot_mapping, int seq_tok, int n_c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TileSmem<D>& s = *reinterpret_cast<TileSmem<D>*>(smem_raw);
   __shared__ int slot_of[kTile];
   __shared__ long long page_of[kTile];
+  __shared__ long long row_of[kTile];
   __shared__ int same_page;
   const int head = blockIdx.y;
   const bool is_key = blockIdx.z == 0;
@@ -393,8 +397,24 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
     if (threadIdx.x < kTile) {
       long long pg = -1;
       int sl = 0;
+      long long row = t0 + threadIdx.x;
       if (threadIdx.x < nv) {
-        const long long sm = slot_mapping[t0 + threadIdx.x];
+        long long sm = -1;
+        if (slot_mapping) {
+          sm = slot_mapping[t0 + threadIdx.x];
+        } else {
+          const long long i = t0 + threadIdx.x;
+          const long long bq = i / n_c;
+          const int pos = (int)(i - bq * n_c);
+          row = bq * seq_tok + pos;
+          if (pos / kPage < C.max_pages) {
+            const long long pid = C.block_table[(size_t)bq * C.max_pages + pos / kPage];
+            sm = pid >= 0 ? pid * kPage + pos % kPage : -1;
+            if (pid < 0) atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+          } else {
+            atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
+          }
+        }
         if (sm >= 0) {
           pg = sm / kPage;
           sl = (int)(sm % kPage);
@@ -406,6 +426,7 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
       }
       page_of[threadIdx.x] = pg;
       slot_of[threadIdx.x] = pg >= 0 ? sl : -1;
+      row_of[threadIdx.x] = row;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -419,7 +440,7 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
       same_page = same;
     }
     for (int i = 0; i < nv; ++i) {
-      const long long n = (t0 + i) * P.hkv + head;
+      const long long n = row_of[i] * P.hkv + head;
       s.x[i][threadIdx.x] =
           (page_of[i] >= 0 && threadIdx.x < P.dh) ? load_elem(x, dtype, n * P.dh + threadIdx.x) : 0.f;
     }
@@ -537,6 +558,29 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
       if (threadIdx.x == 0) reinterpret_cast<float*>(sb + P.off_vnorm)[slot] = s.norm[0];
     }
   }
+}
+
+// Prefill of whole sequences: positions n_c .. seq_tok - 1 of every (sequence, kv head) into the
+// float16 window ring (slot p mod ring, rows of d with a zero tail past head_dim).  grid (batch, hkv, 2).
+template <int D>
+__global__ void __launch_bounds__(D) prefill_window_kernel(const __grid_constant__ KParams P,
+                                                           const __grid_constant__ KCache C, const void* k,
+                                                           const void* v, int dtype, int seq_tok, int n_c) {
+  const int b = blockIdx.x, head = blockIdx.y, j = threadIdx.x;
+  const bool is_key = blockIdx.z == 0;
+  const void* x = is_key ? k : v;
+  __half* ring = (is_key ? C.win_k : C.win_v) + (((size_t)b * P.hkv + head) * C.ring) * D;
+  for (int p = n_c; p < seq_tok; ++p) {
+    const long long n = ((long long)b * seq_tok + p) * P.hkv + head;
+    ring[(size_t)(p % C.ring) * D + j] = __float2half_rn(j < P.dh ? load_elem(x, dtype, n * P.dh + j) : 0.f);
+  }
+}
+
+__global__ void prefill_counters_kernel(const __grid_constant__ KCache C, int seq_tok, int n_c) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= C.batch) return;
+  C.seq_len[b] = seq_tok;
+  C.n_compressed[b] = n_c;
 }
 
 __global__ void append_counters_kernel(const __grid_constant__ KCache C, int window) {
@@ -695,20 +739,43 @@ cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, lon
 
 template <int D>
 static cudaError_t launch_append_direct_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
-                                          long long n_tok, const long long* slots, cudaStream_t st) {
+                                          long long n_tok, const long long* slots, int seq_tok, int n_c,
+                                          cudaStream_t st) {
   const size_t sm = tile_smem<D>();
   cudaError_t e = cudaFuncSetAttribute(append_direct_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   const long long tiles = (n_tok + kTile - 1) / kTile;
   dim3 grid((int)std::min<long long>(tiles, 65535), P.hkv, 2);
-  append_direct_kernel<D><<<grid, D, sm, st>>>(P, C, k, v, dtype, n_tok, slots);
+  append_direct_kernel<D><<<grid, D, sm, st>>>(P, C, k, v, dtype, n_tok, slots, seq_tok, n_c);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                  long long n_tok, const long long* slots, cudaStream_t st) {
-  if (P.d == 128) return launch_append_direct_d<128>(P, C, k, v, dtype, n_tok, slots, st);
-  return launch_append_direct_d<256>(P, C, k, v, dtype, n_tok, slots, st);
+  if (P.d == 128) return launch_append_direct_d<128>(P, C, k, v, dtype, n_tok, slots, 0, 1, st);
+  return launch_append_direct_d<256>(P, C, k, v, dtype, n_tok, slots, 0, 1, st);
+}
+
+template <int D>
+static cudaError_t launch_prefill_cache_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                          int seq_tok, int n_c, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (n_c > 0) {
+    e = launch_append_direct_d<D>(P, C, k, v, dtype, (long long)C.batch * n_c, nullptr, seq_tok, n_c, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (seq_tok > n_c) {
+    prefill_window_kernel<D><<<dim3(C.batch, P.hkv, 2), D, 0, st>>>(P, C, k, v, dtype, seq_tok, n_c);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  prefill_counters_kernel<<<(C.batch + 127) / 128, 128, 0, st>>>(C, seq_tok, n_c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_cache(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                 int seq_tok, int n_c, cudaStream_t st) {
+  if (P.d == 128) return launch_prefill_cache_d<128>(P, C, k, v, dtype, seq_tok, n_c, st);
+  return launch_prefill_cache_d<256>(P, C, k, v, dtype, seq_tok, n_c, st);
 }
 
 template <int D>

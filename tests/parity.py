@@ -217,3 +217,28 @@ def read_pool(pool_bytes: np.ndarray, ol: OracleLayer, page: int, head: int) -> 
                              key_norm_u8=int(ol.norm_range is not None))
     return OP.read_page(pool_bytes, lay, ol.hkv, page, head, ol.d, ol.kb, ol.qjl, ol.vb, key_split=ol.key_split,
                         norm_range=ol.norm_range)
+
+
+def read_pages(pool_bytes: np.ndarray, ol: OracleLayer, pages, head: int) -> dict:
+    """The records of the (page, head) sub-blocks of `pages`, in order, as arrays over all their
+    tokens: the same decoding as oracle.paging.read_page, batched over pages (uniform-rate keys
+    with float32 norms).  Returns kidx [n, d], knorm, krnorm, ksigns (QJL), vidx, vnorm."""
+    lay = OP.subblock_layout(ol.d, ol.kb, ol.qjl, ol.vb)
+    P, w, d = OP.PAGE, ol.d // 32, ol.d
+    pages = np.asarray(pages, dtype=np.int64)
+    sb = pool_bytes.reshape(-1, ol.hkv, lay["bytes"])[pages, head]          # [np, bytes]
+    f32 = lambda off, n: np.ascontiguousarray(sb[:, off: off + 4 * n]).view(np.float32).reshape(-1)
+    u32 = lambda off, n: np.ascontiguousarray(sb[:, off: off + 4 * n]).view(np.uint32)
+    out = {"knorm": f32(lay["key_norm"], P)}
+    if ol.qjl:
+        out["krnorm"] = f32(lay["key_rnorm"], P)
+    if ol.qjl == 1:
+        out["ksigns"] = OC.unpack_bits(u32(lay["key_signs"], P * w).reshape(-1, P, w), d).reshape(-1, d).astype(bool)
+    cw = u32(lay["key_codes"], ol.kb * P * w).reshape(-1, ol.kb, P, w).transpose(0, 2, 1, 3)   # [np, P, kb, w]
+    out["kidx"] = OC.unpack_codes(cw.reshape(-1, ol.kb, w), ol.kb, d)
+    out["vnorm"] = f32(lay["value_norm"], P)
+    vc = np.ascontiguousarray(sb[:, lay["value_codes"]: lay["value_codes"] + 2 * ol.vb * d]).view(np.uint16)
+    vc = vc.reshape(-1, ol.vb, d)
+    vplanes = ((vc[:, None, :, :] >> np.arange(P, dtype=np.uint16)[None, :, None, None]) & 1).astype(np.uint8)
+    out["vidx"] = OC.planes_to_idx(vplanes.reshape(-1, ol.vb, d))
+    return out

@@ -231,3 +231,25 @@ def test_norm_range_and_bit_accounting_helpers(L):
     b = tq.bits_per_channel(_Layer)
     assert b["kv_total_bits_per_channel"] == 172 * 8 / 256  # 2b + QJL keys, 2b values, float norms
     assert abs(b["compression_vs_fp16"] - 32 / (172 * 8 / 256)) < 1e-12
+
+
+def test_prefill_cache_checks_capacity_before_any_launch(L):
+    """tq_prefill_cache applies the window rule in the library: with W = 0, 40 tokens need
+    3 pages per sequence, more than a block table of 2 pages holds (refused on the host); a
+    window of 16 leaves n_c = 16 (one page) and passes the check."""
+    p = L.LayerParams()
+    p.d, p.n_kv_heads, p.n_q_heads, p.page_size = 128, 2, 4, 16
+    p.key_bits, p.value_bits, p.key_qjl, p.kind = 2, 2, 1, L.TQ_FWHT
+    fake = 1 << 20  # 16-byte aligned stand-ins: nothing is launched on these paths
+    p.k_rot = p.v_rot = p.qjl_s = fake
+    c = L.Cache()
+    c.page_pool, c.n_pages, c.block_table, c.max_pages_per_seq = fake, 8, fake, 2
+    c.seq_len = c.n_compressed = fake
+    c.batch = 1
+    lib = L.lib()
+    st = lib.tq_prefill_cache(ctypes.byref(p), ctypes.byref(c), fake, fake, L.TQ_BF16, 40, None)
+    assert st == L.TQ_ERR_CAPACITY and b"max_pages_per_seq" in lib.tq_last_error()
+    assert lib.tq_prefill_cache(ctypes.byref(p), ctypes.byref(c), fake, fake, L.TQ_BF16, -1, None) == L.TQ_ERR_INVALID_ARG
+    p.window = 16
+    st = lib.tq_prefill_cache(ctypes.byref(p), ctypes.byref(c), fake, fake, L.TQ_BF16, 40, None)
+    assert st == L.TQ_ERR_INVALID_ARG and b"win_k" in lib.tq_last_error()  # window needs the ring buffers

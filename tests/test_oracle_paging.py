@@ -78,3 +78,29 @@ def test_window_policy_brute_force(W):
         else:
             assert not flushed
         assert nc1 == compressed
+
+
+@pytest.mark.parametrize("d,kb,qjl,vb", [(128, 3, 1, 4), (256, 2, 1, 2), (128, 2, 2, 3)])
+def test_batched_page_reader_equals_read_page(d, kb, qjl, vb):
+    """tests/parity.read_pages (every page of a sequence at once) decodes the same records as
+    read_page page by page."""
+    import parity as PY
+
+    rng = np.random.default_rng(3)
+    H, n_pages = 2, 5
+    O = PY.OracleLayer(d, H, H, kb, vb, 1, qjl=qjl)
+    lay = PG.subblock_layout(d, kb, qjl, vb)
+    pool = rng.integers(0, 256, size=n_pages * H * lay["bytes"], dtype=np.uint8)
+    pages = [3, 0, 4]
+    for h in range(H):
+        got = PY.read_pages(pool, O, pages, h)
+        for i, pg in enumerate(pages):
+            ref = PG.read_page(pool, lay, H, pg, h, d, kb, qjl, vb)
+            sl = slice(16 * i, 16 * i + 16)
+            assert np.array_equal(got["kidx"][sl], ref["kidx"]) and np.array_equal(got["vidx"][sl], ref["vidx"])
+            assert np.array_equal(got["knorm"][sl].view(np.uint32), ref["knorm"].view(np.uint32))
+            assert np.array_equal(got["vnorm"][sl].view(np.uint32), ref["vnorm"].view(np.uint32))
+            if qjl:
+                assert np.array_equal(got["krnorm"][sl].view(np.uint32), ref["krnorm"].view(np.uint32))
+            if qjl == 1:
+                assert np.array_equal(got["ksigns"][sl], ref["ksigns"])
