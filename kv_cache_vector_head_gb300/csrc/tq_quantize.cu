@@ -483,6 +483,12 @@ __global__ void __launch_bounds__(D) append_direct_kernel(const __grid_constant_
   }
 }
 
+}  // namespace tq
+
+#include "tq_quantize256.cuh"
+
+namespace tq {
+
 // ------------------------------------------------------------------ append: decode step
 
 // grid (batch, hkv, 2): blockIdx.z = 0 keys, 1 values.  Reads the counters;
@@ -737,6 +743,41 @@ cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, lon
   return launch_quantize_flat_d<256>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);
 }
 
+// d = 256 direct slots through q256::direct256_kernel (FWHT kind, uniform key rate, float norms).
+static bool direct256_ok(const KParams& P) {
+  return P.d == 256 && P.kind == TQ_FWHT && !P.kivi && !P.ksplit && !P.knu8 && antisymmetric(P.kc, P.kt, P.kb) &&
+         antisymmetric(P.vc, P.vt, P.vb);
+}
+
+template <bool KEY, int SK>
+static cudaError_t launch_direct256_role(const KParams& P, const KCache& C, const void* x, int dtype, long long n_tok,
+                                         const long long* slots, int seq_tok, int n_c, cudaStream_t st) {
+  auto kern = q256::direct256_kernel<KEY, SK>;
+  const size_t sm = q256::smem_bytes(SK == 1);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long tiles = (n_tok + q256::TILE - 1) / q256::TILE;
+  const int per_sm = (KEY && SK == 1) ? 1 : 2;  // the sketch stages S in 128 KB of shared memory
+  const long long gx = std::min<long long>(std::max(1, per_sm * sms / std::max(1, P.hkv)), tiles);
+  kern<<<dim3((unsigned)std::max<long long>(gx, 1), P.hkv), q256::NT, sm, st>>>(P, C, x, dtype, n_tok, slots, seq_tok, n_c);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_direct256(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
+                                    long long n_tok, const long long* slots, int seq_tok, int n_c, cudaStream_t st) {
+  cudaError_t e;
+  if (P.kqjl == TQ_KEY_QJL)
+    e = P.qjl_srht ? launch_direct256_role<true, 2>(P, C, k, dtype, n_tok, slots, seq_tok, n_c, st)
+                   : launch_direct256_role<true, 1>(P, C, k, dtype, n_tok, slots, seq_tok, n_c, st);
+  else
+    e = launch_direct256_role<true, 0>(P, C, k, dtype, n_tok, slots, seq_tok, n_c, st);
+  if (e != cudaSuccess) return e;
+  return launch_direct256_role<false, 0>(P, C, v, dtype, n_tok, slots, seq_tok, n_c, st);
+}
+
 template <int D>
 static cudaError_t launch_append_direct_d(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                           long long n_tok, const long long* slots, int seq_tok, int n_c,
@@ -753,6 +794,7 @@ static cudaError_t launch_append_direct_d(const KParams& P, const KCache& C, con
 cudaError_t launch_append_direct(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                  long long n_tok, const long long* slots, cudaStream_t st) {
   if (P.d == 128) return launch_append_direct_d<128>(P, C, k, v, dtype, n_tok, slots, 0, 1, st);
+  if (direct256_ok(P)) return launch_direct256(P, C, k, v, dtype, n_tok, slots, 0, 1, st);
   return launch_append_direct_d<256>(P, C, k, v, dtype, n_tok, slots, 0, 1, st);
 }
 
@@ -761,7 +803,8 @@ static cudaError_t launch_prefill_cache_d(const KParams& P, const KCache& C, con
                                           int seq_tok, int n_c, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (n_c > 0) {
-    e = launch_append_direct_d<D>(P, C, k, v, dtype, (long long)C.batch * n_c, nullptr, seq_tok, n_c, st);
+    e = direct256_ok(P) ? launch_direct256(P, C, k, v, dtype, (long long)C.batch * n_c, nullptr, seq_tok, n_c, st)
+                        : launch_append_direct_d<D>(P, C, k, v, dtype, (long long)C.batch * n_c, nullptr, seq_tok, n_c, st);
     if (e != cudaSuccess) return e;
   }
   if (seq_tok > n_c) {

@@ -1,0 +1,452 @@
+// Direct-slot quantize of d = 256 keys and values into the paged cache (sm_103a):
+// included by tq_quantize.cu after the page-store helpers.
+//
+// [Reconstruction] §5 Steps 1-5 (norm, rotation, Lloyd-Max code) and §6 (residual,
+// gamma, QJL signs of S r); [Design study] §CPU and WASM kernel design ("Append-time key
+// kernel"), §Packed format.  Same decisions as quantize_tile, organised for throughput:
+//
+//   * a CTA of 16 warps owns a tile of 64 tokens of one kv head and loops over tiles
+//     (persistent per head); warp w quantizes tokens 4 w .. 4 w + 3 of the tile with the
+//     vector in registers (coordinate 32 e + lane in register e): fp32 norm by a balanced
+//     tree, the rotation as a shuffle Walsh-Hadamard transform with the sign flips (FWHT
+//     kind), codes against the float32 boundaries, sign-magnitude planes by warp ballots;
+//   * keys with the Gaussian sketch: S is staged once per CTA in shared memory as f16 in
+//     mma.m16n8k16 B-fragment order (128 KB, with its row norms), the residuals of the
+//     tile as f16 hi / lo limbs in A-fragment order; S r runs on the tensor cores with
+//     the hi limb (warp w: rows 16 w .. 16 w + 15 for all 64 tokens).  An entry whose
+//     magnitude lies within a certified bound of the f16 rounding and accumulation error
+//     (2^-10 (1 + 2^-5) ||r|| ||S_j|| + 2^-20 (||r|| + ||S_j||)) is recomputed in fp32 by
+//     the warp (r from its two limbs, S_j from global memory), so every sign is that of
+//     the fp32 product, as in quantize_tile.  The structured sketch takes the signs of a
+//     warp transform of sigma_S * r instead;
+//   * values: the code-plane bits of the tile are staged in shared memory and written as
+//     whole 16-slot words where the tile fills a page (prefill), bitwise atomics elsewhere.
+// Layers outside this kernel's scope (dense rotation, mixed-channel keys, byte norms, the
+// KIVI arm) take append_direct_kernel.
+
+namespace tq {
+namespace q256 {
+
+constexpr int D = 256, E = D / 32;
+constexpr int NW = 16, NT = 32 * NW;  // warps, threads
+constexpr int TILE = 64;              // tokens per tile
+constexpr int VPW = TILE / NW;        // tokens per warp in the vector phase
+constexpr int MT = TILE / 16;         // m-tiles of the sketch product
+constexpr int KS = D / 16;            // k-steps
+constexpr int NTL = D / 8;            // n-tiles (rows of S)
+constexpr int NTW = NTL / NW;         // n-tiles per warp (2)
+
+struct Tile {
+  uint32_t words[TILE][TQ_MAX_BITS][E];  // value code planes of the tile (page assembly)
+  uint32_t sw[TILE][E];                  // sign words
+  float rn[TILE];                        // ||r|| of each token, z units (certification bound)
+  long long page[TILE];
+  int slot[TILE];
+  int full[MT];                          // value stores: group g fills page page[16 g] in slot order
+};
+constexpr size_t kSBBytes = (size_t)NTL * KS * 32 * sizeof(uint2);        // S, f16 B fragments
+constexpr size_t kSABytes = (size_t)MT * KS * 32 * 4 * sizeof(uint32_t);   // one residual limb
+__host__ __device__ constexpr size_t smem_bytes(bool sketch) {
+  return sizeof(Tile) + (sketch ? kSBBytes + D * sizeof(float) + 2 * kSABytes : 0);
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, const uint2& b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
+}
+
+// Halfword index of A-fragment element (token row rr of m-tile mt, coordinate k) in a limb array.
+__device__ __forceinline__ int a_index(int mt, int rr, int k) {
+  const int ks = k >> 4, kk = k & 15;
+  const int tl = (rr & 7) * 4 + ((kk & 7) >> 1), reg = (rr >> 3) + 2 * (kk >> 3);
+  return ((((mt * KS + ks) * 32 + tl) * 4 + reg) << 1) + (kk & 1);
+}
+
+// Element offset of (m-tile mt, token row rr, coordinate 32 e + lane) is a_base(mt, rr, lane) + 512 e.
+__device__ __forceinline__ int a_base(int mt, int rr, int lane) { return a_index(mt, rr, lane); }
+
+__device__ __forceinline__ float tree8(const float (&v)[E]) {
+  return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
+// Unnormalised Walsh-Hadamard transform of a warp-held 256-vector (coordinate 32 e + lane in
+// v[e], Sylvester order): across lanes a butterfly step is o + s a with s = -1 on the lanes
+// whose bit h is set, then the register levels.
+__device__ __forceinline__ void wht256(float (&v)[E], int lane) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    const float sg = (lane & h) ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = fmaf(sg, v[e], __shfl_xor_sync(0xffffffffu, v[e], h));
+  }
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if ((e & h) == 0) {
+        const float lo = v[e], hi = v[e + h];
+        v[e] = lo + hi;
+        v[e + h] = lo - hi;
+      }
+}
+
+// Code of z against an antisymmetric table (t[half - 1] = 0, t[half - 1 + k] = -t[half - 1 - k]):
+// idx = #{i : z >= t_i}, from the positive boundaries tp[k] = t[half + k] only.  z >= 0:
+// idx = half + #{k : z >= tp_k}; z < 0: z >= -tp_k <=> |z| <= tp_k, so idx = half - 1 -
+// #{k : |z| > tp_k}.  Returns the sign-magnitude pair: pos = (idx >= half), mag.
+__device__ __forceinline__ void code_sm(float z, const float (&tp)[7], int nb, unsigned& pos, int& mag) {
+  const float a = fabsf(z);
+  pos = z >= 0.f ? 1u : 0u;
+  int m = 0;
+#pragma unroll
+  for (int k = 0; k < 7; ++k)
+    if (k < nb) m += pos ? (z >= tp[k] ? 1 : 0) : (a > tp[k] ? 1 : 0);
+  mag = m;
+}
+
+// KEY: keys (else values).  SK: 0 no sketch (values, MSE-only / scaled keys), 1 Gaussian S on
+// the tensor cores, 2 structured S = H diag(sigma_S).  Direct slots as in append_direct_kernel:
+// slot_mapping[t] for input token t, or (slot_mapping == NULL) position p of sequence b at
+// input row b seq_tok + p, page block_table[b][p / 16], slot p % 16, for t = b n_c + p.
+template <bool KEY, int SK>
+__global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel(const __grid_constant__ KParams P,
+                                                          const __grid_constant__ KCache C, const void* x, int dtype,
+                                                          long long n_tok, const long long* slot_mapping, int seq_tok,
+                                                          int n_c) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Tile& tl = *reinterpret_cast<Tile*>(smem_raw);
+  uint2* sB = reinterpret_cast<uint2*>(smem_raw + sizeof(Tile));                       // [NTL][KS][32]
+  float* sN = reinterpret_cast<float*>(smem_raw + sizeof(Tile) + kSBBytes);            // [D] row norms
+  uint16_t* sAh = reinterpret_cast<uint16_t*>(smem_raw + sizeof(Tile) + kSBBytes + D * sizeof(float));
+  uint16_t* sAl = reinterpret_cast<uint16_t*>(smem_raw + sizeof(Tile) + kSBBytes + D * sizeof(float) + kSABytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, t4 = lane & 3;
+  const int head = blockIdx.y;
+  const int bits = KEY ? P.kb : P.vb;
+  const int half = 1 << (bits - 1);
+  const float* ctab = KEY ? P.kc : P.vc;
+  const float* ttab = KEY ? P.kt : P.vt;
+  const float* sigma = (KEY ? P.k_rot : P.v_rot) + (size_t)head * D;
+  const float* Sg = P.qjl_s + (size_t)head * (SK == 1 ? D * D : D);
+  const int corr = KEY ? P.kqjl : 0;  // TQ_KEY_*: the scale modes keep s in gamma's slot
+
+  if constexpr (SK == 1) {
+    // S of this head: f16 in B-fragment order (n-tile nt = rows 8 nt .., k-step ks), and row norms
+    for (int i = tid; i < NTL * KS * 32; i += NT) {
+      const int ln = i & 31, ks = (i >> 5) % KS, nt = i / (32 * KS);
+      const int j = 8 * nt + (ln >> 2), k0 = 16 * ks + 2 * (ln & 3);
+      const float2 p0 = *reinterpret_cast<const float2*>(Sg + (size_t)j * D + k0);
+      const float2 p1 = *reinterpret_cast<const float2*>(Sg + (size_t)j * D + k0 + 8);
+      const __half2 h0 = __floats2half2_rn(p0.x, p0.y), h1 = __floats2half2_rn(p1.x, p1.y);
+      sB[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    }
+    for (int j = warp; j < D; j += NW) {
+      float sq[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float v = __ldg(Sg + (size_t)j * D + e * 32 + lane);
+        sq[e] = v * v;
+      }
+      const float s = warp_sum_f(tree8(sq));
+      if (lane == 0) sN[j] = sqrtf(s);
+    }
+  }
+  float sig[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sig[e] = __ldg(sigma + e * 32 + lane);
+  float tp[7], cpos[8];  // positive boundaries and centroids of the antisymmetric table
+  const int nb = half - 1;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) tp[k] = k < nb ? ttab[half + k] : 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) cpos[k] = k < half ? ctab[half + k] : 0.f;
+  float sgs[E];
+  if constexpr (SK == 2) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) sgs[e] = __ldg(Sg + e * 32 + lane);
+  }
+
+  const long long n_tiles = (n_tok + TILE - 1) / TILE;
+  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const long long t0 = tile * TILE;
+    // ---- destinations of the tile's tokens
+    if (tid < TILE) {
+      const long long t = t0 + tid;
+      long long pg = -1, row = t;
+      int sl = 0;
+      if (t < n_tok) {
+        long long sm = -1;
+        if (slot_mapping) {
+          sm = slot_mapping[t];
+        } else {
+          const long long bq = t / n_c;
+          const int pos = (int)(t - bq * n_c);
+          row = bq * seq_tok + pos;
+          if (pos / kPage < C.max_pages) {
+            const long long pid = C.block_table[(size_t)bq * C.max_pages + pos / kPage];
+            sm = pid >= 0 ? pid * kPage + pos % kPage : -1;
+            if (pid < 0) atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+          } else {
+            atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
+          }
+        }
+        if (sm >= 0) {
+          pg = sm / kPage;
+          sl = (int)(sm % kPage);
+          if (pg >= C.n_pages) {
+            atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+            pg = -1;
+          }
+        }
+      }
+      tl.page[tid] = pg;
+      tl.slot[tid] = pg >= 0 ? sl : -1;
+      reinterpret_cast<long long*>(tl.words)[tid] = row;  // rows parked in the (not yet used) word buffer
+    }
+    for (int i = tid; i < TILE * E; i += NT) (&tl.sw[0][0])[i] = 0u;
+    __syncthreads();
+    long long rows[VPW];
+#pragma unroll
+    for (int i = 0; i < VPW; ++i) rows[i] = reinterpret_cast<const long long*>(tl.words)[VPW * warp + i];
+    if (tid < MT) {  // a 16-token group that fills one page in slot order: whole value words
+      int f = tl.page[16 * tid] >= 0;
+      for (int i = 0; i < 16 && f; ++i) f = tl.page[16 * tid + i] == tl.page[16 * tid] && tl.slot[16 * tid + i] == i;
+      tl.full[tid] = f;
+    }
+    __syncthreads();  // the row copies are read: the word buffer is free
+
+    // ---- vector phase: warp w, tokens VPW w .. VPW w + VPW - 1
+#pragma unroll 1
+    for (int i = 0; i < VPW; ++i) {
+      const int v = VPW * warp + i;
+      const long long pg = tl.page[v];
+      const int sl = tl.slot[v];
+      float xv[E];
+      {
+        const long long base = (rows[i] * P.hkv + head) * P.dh;
+        const bool ok = pg >= 0;
+        if (dtype == TQ_BF16) {
+          const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(x) + base;
+#pragma unroll
+          for (int e = 0; e < E; ++e) xv[e] = (ok && e * 32 + lane < P.dh) ? __bfloat162float(xp[e * 32 + lane]) : 0.f;
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            xv[e] = (ok && e * 32 + lane < P.dh) ? load_elem(x, dtype, base + e * 32 + lane) : 0.f;
+        }
+      }
+      float sq[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) sq[e] = xv[e] * xv[e];
+      const float n = sqrtf(warp_sum_f(tree8(sq)));
+      const bool zero = n < kZeroNorm;
+      const float inv = zero ? 0.f : 1.0f / n;
+      // z = sqrt(d) Pi x / n with Pi = H diag(sigma) / sqrt(d): z = H (sigma x) / n
+      float z[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) z[e] = xv[e] * sig[e];
+      wht256(z, lane);
+#pragma unroll
+      for (int e = 0; e < E; ++e) z[e] *= inv;
+      unsigned pos[E];
+      int mag[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) code_sm(z[e], tp, nb, pos[e], mag[e]);
+      unsigned char* sb = pg >= 0 ? C.pool + ((size_t)pg * P.hkv + head) * (size_t)P.sub_bytes : nullptr;
+      // code planes: word e of plane p from one ballot (plane 0: sign side, planes 1..: magnitude bits)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        uint32_t wv = __ballot_sync(0xffffffffu, pos[e]);
+        for (int p = 0; p < bits; ++p) {
+          if (p > 0) wv = __ballot_sync(0xffffffffu, (mag[e] >> (p - 1)) & 1);
+          if (KEY) {
+            if (lane == e && sb) reinterpret_cast<uint32_t*>(sb + P.off_kcodes)[(p * kPage + sl) * E + e] = wv;
+          } else if (lane == e) {
+            tl.words[v][p][e] = wv;
+          }
+        }
+      }
+      if (!KEY) {
+        if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_vnorm)[sl] = zero ? 0.f : n;
+        continue;
+      }
+      if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_knorm)[sl] = zero ? 0.f : n;
+      // centroid of each coordinate: sign times the positive centroid of its magnitude
+      float cz[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        float c = cpos[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) c = (k < half && mag[e] == k) ? cpos[k] : c;
+        cz[e] = pos[e] ? c : -c;
+      }
+      if (corr == TQ_KEY_EDEN || corr == TQ_KEY_RENORM) {
+        // the unbiased scale s = d / sum_j z_j C[idx_j] (z and its centroid share a sign)
+        float tz[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) tz[e] = z[e] * cz[e];
+        const float a = warp_sum_f(tree8(tz));
+        if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_krnorm)[sl] = zero ? 0.f : (float)D / a;
+      }
+      if (corr != TQ_KEY_QJL) continue;
+      // residual (z units) and gamma = ||r|| / sqrt(d)
+      float r[E], r2[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        r[e] = zero ? 0.f : z[e] - cz[e];
+        r2[e] = r[e] * r[e];
+      }
+      const float rr = sqrtf(warp_sum_f(tree8(r2)));
+      if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_krnorm)[sl] = zero ? 0.f : rr * 0.0625f;
+      if constexpr (SK == 2) {
+        // structured sketch: signs of H (sigma_S * r), one word per register
+        float a[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[e] = r[e] * sgs[e];
+        wht256(a, lane);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned w = __ballot_sync(0xffffffffu, (zero || a[e] >= 0.f) ? 1u : 0u);
+          if (lane == e) tl.sw[v][e] = w;
+        }
+      } else if constexpr (SK == 1) {
+        if (lane == 0) tl.rn[v] = rr;
+        const int ab = a_base(v >> 4, v & 15, lane);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const __half h = __float2half_rn(r[e]);
+          const __half lo = __float2half_rn(r[e] - __half2float(h));
+          sAh[ab + 512 * e] = __half_as_ushort(h);
+          sAl[ab + 512 * e] = __half_as_ushort(lo);
+        }
+      }
+    }
+    __syncthreads();
+
+    if constexpr (KEY && SK == 1) {
+      if (corr == TQ_KEY_QJL) {
+        // ---- sketch phase: warp w, rows 16 w .. 16 w + 15 of S r for all 64 tokens
+        float acc[MT][NTW][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int q = 0; q < NTW; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[m][q][c] = 0.f;
+        const uint4* A4 = reinterpret_cast<const uint4*>(sAh);
+#pragma unroll 2
+        for (int ks = 0; ks < KS; ++ks) {
+          uint2 b[NTW];
+#pragma unroll
+          for (int q = 0; q < NTW; ++q) b[q] = sB[((NTW * warp + q) * KS + ks) * 32 + lane];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4 a = A4[(m * KS + ks) * 32 + lane];
+#pragma unroll
+            for (int q = 0; q < NTW; ++q) mma_f16(acc[m][q], a, b[q]);
+          }
+        }
+        // signs; entries within the certified bound are recomputed in fp32 by the whole warp
+        uint32_t sbits = 0, unc = 0;  // bit (m NTW + q) 4 + c
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int q = 0; q < NTW; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int v = 16 * m + g8 + 8 * (c >> 1);
+              const int j = 8 * (NTW * warp + q) + 2 * t4 + (c & 1);
+              const float rnv = tl.rn[v], snj = sN[j];
+              const float bound = 1.0322265625f * 0x1p-10f * rnv * snj + 0x1p-20f * (rnv + snj);
+              const int bit = (m * NTW + q) * 4 + c;
+              if (acc[m][q][c] >= 0.f) sbits |= 1u << bit;
+              if (fabsf(acc[m][q][c]) <= bound) unc |= 1u << bit;
+            }
+#pragma unroll 1
+        for (int bit = 0; bit < MT * NTW * 4; ++bit) {
+          unsigned todo = __ballot_sync(0xffffffffu, (unc >> bit) & 1u);
+          while (todo) {
+            const int l = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int c = bit & 3, q = (bit >> 2) % NTW, m = bit / (4 * NTW);
+            const int v = 16 * m + (l >> 2) + 8 * (c >> 1);
+            const int j = 8 * (NTW * warp + q) + 2 * (l & 3) + (c & 1);
+            float prod[E];
+            const int ab = a_base(v >> 4, v & 15, lane);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const int ai = ab + 512 * e;
+              const float rv = __half2float(__ushort_as_half(sAh[ai])) + __half2float(__ushort_as_half(sAl[ai]));
+              prod[e] = rv * __ldg(Sg + (size_t)j * D + e * 32 + lane);
+            }
+            const float dot = warp_sum_f(tree8(prod));
+            if (lane == l) sbits = (sbits & ~(1u << bit)) | ((dot >= 0.f ? 1u : 0u) << bit);
+          }
+        }
+        // sign words: token v, rows 16 w .. 16 w + 15 are bits 16 (w & 1) .. of word w / 2
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int hv = 0; hv < 2; ++hv) {
+            uint32_t part = 0;
+#pragma unroll
+            for (int q = 0; q < NTW; ++q)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int bit = (m * NTW + q) * 4 + 2 * hv + e;
+                part |= ((sbits >> bit) & 1u) << (8 * q + 2 * t4 + e);
+              }
+            part |= __shfl_xor_sync(0xffffffffu, part, 1);
+            part |= __shfl_xor_sync(0xffffffffu, part, 2);
+            if (t4 == 0) atomicOr(&tl.sw[16 * m + g8 + 8 * hv][warp >> 1], part << (16 * (warp & 1)));
+          }
+      }
+      __syncthreads();
+    }
+    if constexpr (KEY) {
+      if (corr == TQ_KEY_QJL && SK != 0) {
+        for (int i = tid; i < TILE * E; i += NT) {
+          const int v = i / E, e = i % E;
+          if (tl.page[v] >= 0)
+            reinterpret_cast<uint32_t*>(C.pool + ((size_t)tl.page[v] * P.hkv + head) * (size_t)P.sub_bytes +
+                                        P.off_ksigns)[tl.slot[v] * E + e] = tl.sw[v][e];
+        }
+      }
+    } else {
+      // value planes: coordinate j, plane p of each 16-token group
+      for (int i = tid; i < MT * D; i += NT) {
+        const int grp = i / D, j = i % D;
+        const int v0 = 16 * grp;
+        for (int p = 0; p < bits; ++p) {
+          if (tl.full[grp]) {
+            uint32_t w16 = 0;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) w16 |= ((tl.words[v0 + t][p][j >> 5] >> (j & 31)) & 1u) << t;
+            uint16_t* vc16 = reinterpret_cast<uint16_t*>(C.pool + ((size_t)tl.page[v0] * P.hkv + head) *
+                                                                       (size_t)P.sub_bytes + P.off_vcodes);
+            vc16[p * D + j] = (uint16_t)w16;
+          } else {
+            for (int t = 0; t < 16; ++t) {
+              const int v = v0 + t;
+              if (tl.page[v] < 0) continue;
+              const unsigned bit = (tl.words[v][p][j >> 5] >> (j & 31)) & 1u;
+              uint16_t* vc16 = reinterpret_cast<uint16_t*>(C.pool + ((size_t)tl.page[v] * P.hkv + head) *
+                                                                         (size_t)P.sub_bytes + P.off_vcodes);
+              unsigned int* w32 = reinterpret_cast<unsigned int*>(vc16 + p * D + (j & ~1));
+              const int sh = (j & 1) * 16 + tl.slot[v];
+              atomicAnd(w32, ~(1u << sh));
+              atomicOr(w32, bit << sh);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  (void)half;
+}
+
+}  // namespace q256
+}  // namespace tq
