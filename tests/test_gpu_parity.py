@@ -259,6 +259,9 @@ PAGED = [
     # byte norms alone, with the sketch; a narrow range that clamps the outlier keys' norms
     ("llama", dict(batch=3, key_norm_range=(3.0, 5.0)), 33, 10),
     ("qwen", dict(batch=1, window=20, key_norm_range=(2.0, 6.0)), 50, 20),
+    # d = 256 without a window: prefill ends in a partly filled page (64-token tiles, bitwise value planes)
+    ("long", dict(batch=3), 37, 12),
+    ("long", dict(batch=2, key_qjl=0, key_bits=3, value_bits=1), 70, 9),
     # the structured sketch
     ("qwen", dict(batch=2, window=20, qjl_structured=1), 75, 30),
     ("llama", dict(batch=5, kind=SK.FWHT, qjl_structured=1), 29, 21),
@@ -365,8 +368,12 @@ def test_empty_sequence_and_device_error(tq):
     assert tq.check_device_error() == 0  # cleared
 
 
-def test_direct_slot_append_with_skips(tq):
-    w = SK.workload("llama", batch=1, ctx=40)
+@pytest.mark.parametrize("name,over", [("llama", {}), ("long", {}), ("long", dict(qjl_structured=1)),
+                                       ("qwen", dict(key_qjl=2, head_dim=160))])
+def test_direct_slot_append_with_skips(tq, name, over):
+    """Direct slots scattered over pages 0..7 with one skipped token; the d = 256 cases run the
+    64-token-tile kernel, whose value planes then take the bitwise path (no page filled in order)."""
+    w = SK.workload(name, batch=1, ctx=40, **over)
     kv = SK.keys_values(w, ctx=40)
     L, O = _layer(tq, w)
     pc = tq.PagedCache(L, 1, 64, pool_pages=8)
@@ -390,8 +397,9 @@ def test_direct_slot_append_with_skips(tq):
             pg = PY.read_pool(pool, O, int(s // 16), h)
             sl = int(s % 16)
             sub = {k: v[t: t + 1] for k, v in ok.items() if isinstance(v, np.ndarray) and v.shape[:1] == (40,)}
-            PY.compare_records(sub, pg["kidx"][sl: sl + 1], pg["knorm"][sl: sl + 1], pg["ksigns"][sl: sl + 1],
-                               pg["krnorm"][sl: sl + 1], True)
+            gs = pg["ksigns"][sl: sl + 1] if "ksigns" in pg else None
+            gr = pg["krnorm"][sl: sl + 1] if "krnorm" in pg else None
+            PY.compare_records(sub, pg["kidx"][sl: sl + 1], pg["knorm"][sl: sl + 1], gs, gr, True)
             subv = {k: v[t: t + 1] for k, v in ov.items() if isinstance(v, np.ndarray) and v.shape[:1] == (40,)}
             PY.compare_records(subv, pg["vidx"][sl: sl + 1], pg["vnorm"][sl: sl + 1], is_key=False)
 
