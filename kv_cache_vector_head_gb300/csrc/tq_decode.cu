@@ -228,10 +228,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // then give the copies still in flight (chunks kstop - 1 .. kstop + nst - 2) a second bounded
 // chance to land before the CTA's shared memory is released.  The partials of such a split
 // are not meaningful; the error word reports it.
-__device__ __forceinline__ void drain_after_timeout(uint64_t* full, bool timed_out, int kstop, int nchunks, int nst) {
+// `ahead`: how many chunks beyond the one being consumed are issued (nst - 1, or nst - 2 where the
+// previous chunk's stage is still read while the next key phase runs).
+__device__ __forceinline__ void drain_after_timeout(uint64_t* full, bool timed_out, int kstop, int nchunks, int nst,
+                                                    int ahead) {
   if (!__syncthreads_or(timed_out)) return;
   if (threadIdx.x == 0) atomicOr(&g_decode_err, TQ_DEVERR_TIMEOUT);
-  const int last = min(kstop + nst - 2, nchunks - 1);
+  const int last = min(kstop - 1 + ahead, nchunks - 1);
   for (int j = max(kstop - 1, 0); j <= last; ++j) (void)mbar_wait_bounded(&full[j % nst], (uint32_t)((j / nst) & 1));
 }
 
@@ -524,7 +527,7 @@ constexpr int kPidCache = 1024;  // block-table entries of a split staged in sha
 
 struct MmaShared {
   uint64_t full[kStages];
-  uint4 wf[kMmaPages / 2][2][32];     // softmax weights in mma A-fragment order, per page pair
+  uint4 wf[2][kMmaPages / 2][2][32];  // softmax weights in mma A-fragment order, per page pair (chunk parity)
   float redm[kMmaPages][TQ_MAX_GQA];  // per-warp chunk maxima
   float lsum[kMmaPages][TQ_MAX_GQA];  // per-warp softmax denominators
   float mfin[TQ_MAX_GQA];
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
                (uint32_t)sub, &sh.full[stg]);
   };
   if (warp == 0)
-    for (int k = 0; k < nst - 1 && k < nchunks; ++k) issue(k);
+    for (int k = 0; k < nst - 2 && k < nchunks; ++k) issue(k);
   // the query fragments come from the prologue kernel (launched just before, with
   // this grid allowed to start early): wait for it, then stage them; the first
   // page copies are already in flight
@@ -695,17 +698,111 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       for (int r = 0; r < 4; ++r) accv[p][c][r] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;  // softmax state of head g8 (identical across warps for m)
   float kv_run = 0.f;                     // this lane's share of the value operand's constant K
+  // value phase of chunk kc (its stage, weights buffer kc & 1): warp w owns coordinates
+  // [w*CPW, (w+1)*CPW); runs at the top of iteration kc + 1, overlapping that chunk's key phase
+  auto value_phase = [&](int kc) {
+    unsigned char* stbase = stage0 + (size_t)(kc % nst) * NW * sub;
+    const uint4(&wfb)[kMmaPages / 2][2][32] = sh.wf[kc & 1];
+#pragma unroll 1
+    for (int jg = 0; jg < NW / 2; ++jg) {
+      const uint16_t* va = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg) * sub + P.off_vcodes);
+      const uint16_t* vbp = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg + 1) * sub + P.off_vcodes);
+      const uint4 wf0 = wfb[jg][0][lane], wf1 = wfb[jg][1][lane];
+      if (!VLUT) {
+        // plane words: page A's 16 slots in bits 0..15, page B's in 16..31 (one byte permute per
+        // word); column g8 of n-tile cbk is coordinate warp * CPW + g8 * CB + cbk, so a lane's CB
+        // entries of a plane are adjacent (one vector load per page and plane).  Shifted left by
+        // 12 - 4 t4, the lane's slots 4 t4 + 2 e + k sit at bit 12 + 2 e + k of each half: operand
+        // register e of k-step k is one LOP3 (mask, then XOR into 1.0 / 2.0)
+        uint32_t u0[CB], u1[CB];
+        {
+          const int c0 = warp * CPW + g8 * CB;
+          if constexpr (CB == 4) {
+            const uint2 a0 = *reinterpret_cast<const uint2*>(va + c0), b0 = *reinterpret_cast<const uint2*>(vbp + c0);
+            u0[0] = __byte_perm(a0.x, b0.x, 0x5410);
+            u0[1] = __byte_perm(a0.x, b0.x, 0x7632);
+            u0[CB > 2 ? 2 : 0] = __byte_perm(a0.y, b0.y, 0x5410);
+            u0[CB > 3 ? 3 : 0] = __byte_perm(a0.y, b0.y, 0x7632);
+            if (vb2) {
+              const uint2 a1 = *reinterpret_cast<const uint2*>(va + D + c0),
+                          b1 = *reinterpret_cast<const uint2*>(vbp + D + c0);
+              u1[0] = __byte_perm(a1.x, b1.x, 0x5410);
+              u1[1] = __byte_perm(a1.x, b1.x, 0x7632);
+              u1[CB > 2 ? 2 : 0] = __byte_perm(a1.y, b1.y, 0x5410);
+              u1[CB > 3 ? 3 : 0] = __byte_perm(a1.y, b1.y, 0x7632);
+            }
+          } else {
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(va + c0),
+                           b0 = *reinterpret_cast<const uint32_t*>(vbp + c0);
+            u0[0] = __byte_perm(a0, b0, 0x5410);
+            u0[CB > 1 ? 1 : 0] = __byte_perm(a0, b0, 0x7632);
+            if (vb2) {
+              const uint32_t a1 = *reinterpret_cast<const uint32_t*>(va + D + c0),
+                             b1 = *reinterpret_cast<const uint32_t*>(vbp + D + c0);
+              u1[0] = __byte_perm(a1, b1, 0x5410);
+              u1[CB > 1 ? 1 : 0] = __byte_perm(a1, b1, 0x7632);
+            }
+          }
+        }
+        const int vsh = 12 - 4 * t4;
+#pragma unroll
+        for (int cbk = 0; cbk < CB; ++cbk) {
+          const uint32_t x0 = u0[cbk] << vsh;
+          const uint32_t xm = vb2 ? (u1[cbk] << vsh) : 0u;
+#pragma unroll
+          for (int ksx = 0; ksx < 2; ++ksx) {
+            const uint4 wfk = ksx ? wf1 : wf0;
+            const int pA = 12 + ksx, pB = 14 + ksx;  // register e = 0, 1
+            const uint32_t mA = 0x00010001u << pA, mB = 0x00010001u << pB;
+            const uint32_t bA = (x0 & mA) ^ (pA == 14 ? xb2 : xb1), bB = (x0 & mB) ^ (pB == 14 ? xb2 : xb1);
+            mma16816(accv[0][cbk], wfk, bA, bB);
+            if (vb2) mma16816(accv[1][cbk], wfk, bA ^ (xm & mA), bB ^ (xm & mB));  // Walsh plane sign ^ magnitude
+          }
+        }
+      } else {
+#pragma unroll
+        for (int cbk = 0; cbk < CB; ++cbk) {
+          const int c = warp * CPW + g8 * CB + cbk;
+          uint32_t u[TQ_MAX_BITS];
+#pragma unroll
+          for (int p = 0; p < TQ_MAX_BITS; ++p)
+            u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
+#pragma unroll
+          for (int ksx = 0; ksx < 2; ++ksx) {
+            const int i0 = 4 * t4 + ksx, i1 = i0 + 2;  // slots of registers e = 0 and e = 1
+            uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
+#pragma unroll
+            for (int p = 0; p < TQ_MAX_BITS; ++p) {
+              rA0 |= ((u[p] >> i0) & 1u) << p;
+              rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
+              rA1 |= ((u[p] >> i1) & 1u) << p;
+              rB1 |= ((u[p] >> (i1 + 16)) & 1u) << p;
+            }
+            const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
+            const uint4 wfk = ksx ? wf1 : wf0;
+            // hi halves -> plane 0, lo halves -> plane 1; pair = (token of page A, token of page B)
+            mma16816(accv[0][cbk], wfk, __byte_perm(eA0, eB0, 0x5410), __byte_perm(eA1, eB1, 0x5410));
+            mma16816(accv[1][cbk], wfk, __byte_perm(eA0, eB0, 0x7632), __byte_perm(eA1, eB1, 0x7632));
+          }
+        }
+      }
+    }
+  };
   bool timed_out = false;
   int kstop = nchunks;  // chunks consumed
 
-  for (int k = 0; k < nchunks; ++k) {
-    // chunk k-1 fully consumed: its stage and sh.wf may be rewritten.  A wait that ran out
+  for (int k = 0; k <= nchunks; ++k) {
+    // softmax of chunk k-1 done (its weights are in sh.wf[(k-1) & 1]).  A wait that ran out
     // stops the split here, for every thread alike (no new copies into unfinished phases)
     if (__syncthreads_or(timed_out)) {
       kstop = k;
       break;
     }
-    if (warp == 0 && k + nst - 1 < nchunks) issue(k + nst - 1);
+    // chunk k + nst - 2 goes to the stage of chunk k - 2 (its values were accumulated in the
+    // previous iteration): stages k - 1 (values below) and k (keys below) stay untouched
+    if (warp == 0 && k < nchunks && k + nst - 2 < nchunks) issue(k + nst - 2);
+    if (k > 0) value_phase(k - 1);
+    if (k == nchunks) break;
     const int stg = k % nst;
     if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) timed_out = true;
     unsigned char* stbase = stage0 + (size_t)stg * NW * sub;
@@ -878,7 +975,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
       // token t = 4 t4 + 2 e + nt -> k-step nt, lane (g8, t4), component 2 e (hi) / 2 e + 1 (lo),
       // half = page parity within the pair
       const float* vnorm = reinterpret_cast<const float*>(pb + P.off_vnorm);
-      uint16_t* wfh = reinterpret_cast<uint16_t*>(&sh.wf[warp >> 1][0][0]);
+      uint16_t* wfh = reinterpret_cast<uint16_t*>(&sh.wf[k & 1][warp >> 1][0][0]);
       float ls = 0.f, kvs = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -912,94 +1009,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
             for (int r = 0; r < 4; ++r) accv[p][c][r] *= alpha;
       }
     }
-    __syncthreads();
-    // ---------------- value phase: warp w owns coordinates [w*CPW, (w+1)*CPW)
-#pragma unroll 1
-    for (int jg = 0; jg < NW / 2; ++jg) {
-      const uint16_t* va = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg) * sub + P.off_vcodes);
-      const uint16_t* vbp = reinterpret_cast<const uint16_t*>(stbase + (size_t)(2 * jg + 1) * sub + P.off_vcodes);
-      const uint4 wf0 = sh.wf[jg][0][lane], wf1 = sh.wf[jg][1][lane];
-      if (!VLUT) {
-        // plane words: page A's 16 slots in bits 0..15, page B's in 16..31 (one byte permute per
-        // word); column g8 of n-tile cbk is coordinate warp * CPW + g8 * CB + cbk, so a lane's CB
-        // entries of a plane are adjacent (one vector load per page and plane).  Shifted left by
-        // 12 - 4 t4, the lane's slots 4 t4 + 2 e + k sit at bit 12 + 2 e + k of each half: operand
-        // register e of k-step k is one LOP3 (mask, then XOR into 1.0 / 2.0)
-        uint32_t u0[CB], u1[CB];
-        {
-          const int c0 = warp * CPW + g8 * CB;
-          if constexpr (CB == 4) {
-            const uint2 a0 = *reinterpret_cast<const uint2*>(va + c0), b0 = *reinterpret_cast<const uint2*>(vbp + c0);
-            u0[0] = __byte_perm(a0.x, b0.x, 0x5410);
-            u0[1] = __byte_perm(a0.x, b0.x, 0x7632);
-            u0[CB > 2 ? 2 : 0] = __byte_perm(a0.y, b0.y, 0x5410);
-            u0[CB > 3 ? 3 : 0] = __byte_perm(a0.y, b0.y, 0x7632);
-            if (vb2) {
-              const uint2 a1 = *reinterpret_cast<const uint2*>(va + D + c0),
-                          b1 = *reinterpret_cast<const uint2*>(vbp + D + c0);
-              u1[0] = __byte_perm(a1.x, b1.x, 0x5410);
-              u1[1] = __byte_perm(a1.x, b1.x, 0x7632);
-              u1[CB > 2 ? 2 : 0] = __byte_perm(a1.y, b1.y, 0x5410);
-              u1[CB > 3 ? 3 : 0] = __byte_perm(a1.y, b1.y, 0x7632);
-            }
-          } else {
-            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(va + c0),
-                           b0 = *reinterpret_cast<const uint32_t*>(vbp + c0);
-            u0[0] = __byte_perm(a0, b0, 0x5410);
-            u0[CB > 1 ? 1 : 0] = __byte_perm(a0, b0, 0x7632);
-            if (vb2) {
-              const uint32_t a1 = *reinterpret_cast<const uint32_t*>(va + D + c0),
-                             b1 = *reinterpret_cast<const uint32_t*>(vbp + D + c0);
-              u1[0] = __byte_perm(a1, b1, 0x5410);
-              u1[CB > 1 ? 1 : 0] = __byte_perm(a1, b1, 0x7632);
-            }
-          }
-        }
-        const int vsh = 12 - 4 * t4;
-#pragma unroll
-        for (int cbk = 0; cbk < CB; ++cbk) {
-          const uint32_t x0 = u0[cbk] << vsh;
-          const uint32_t xm = vb2 ? (u1[cbk] << vsh) : 0u;
-#pragma unroll
-          for (int ksx = 0; ksx < 2; ++ksx) {
-            const uint4 wfk = ksx ? wf1 : wf0;
-            const int pA = 12 + ksx, pB = 14 + ksx;  // register e = 0, 1
-            const uint32_t mA = 0x00010001u << pA, mB = 0x00010001u << pB;
-            const uint32_t bA = (x0 & mA) ^ (pA == 14 ? xb2 : xb1), bB = (x0 & mB) ^ (pB == 14 ? xb2 : xb1);
-            mma16816(accv[0][cbk], wfk, bA, bB);
-            if (vb2) mma16816(accv[1][cbk], wfk, bA ^ (xm & mA), bB ^ (xm & mB));  // Walsh plane sign ^ magnitude
-          }
-        }
-      } else {
-#pragma unroll
-        for (int cbk = 0; cbk < CB; ++cbk) {
-          const int c = warp * CPW + g8 * CB + cbk;
-          uint32_t u[TQ_MAX_BITS];
-#pragma unroll
-          for (int p = 0; p < TQ_MAX_BITS; ++p)
-            u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
-#pragma unroll
-          for (int ksx = 0; ksx < 2; ++ksx) {
-            const int i0 = 4 * t4 + ksx, i1 = i0 + 2;  // slots of registers e = 0 and e = 1
-            uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
-#pragma unroll
-            for (int p = 0; p < TQ_MAX_BITS; ++p) {
-              rA0 |= ((u[p] >> i0) & 1u) << p;
-              rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
-              rA1 |= ((u[p] >> i1) & 1u) << p;
-              rB1 |= ((u[p] >> (i1 + 16)) & 1u) << p;
-            }
-            const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
-            const uint4 wfk = ksx ? wf1 : wf0;
-            // hi halves -> plane 0, lo halves -> plane 1; pair = (token of page A, token of page B)
-            mma16816(accv[0][cbk], wfk, __byte_perm(eA0, eB0, 0x5410), __byte_perm(eA1, eB1, 0x5410));
-            mma16816(accv[1][cbk], wfk, __byte_perm(eA0, eB0, 0x7632), __byte_perm(eA1, eB1, 0x7632));
-          }
-        }
-      }
-    }
   }
-  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst);
+  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst, nst - 2);
   // ---- partials
   float ls = l_run, kvl = kv_run;
   ls += __shfl_xor_sync(0xffffffffu, ls, 1);
@@ -1425,7 +1436,7 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
       }
     }
   }
-  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst);
+  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst, nst - 1);
   __syncthreads();
   // token groups -> one partial per coordinate (the key scale rows are free now)
   float* red = &sh.ks[0][0];  // [TQ_MAX_GQA][D]
