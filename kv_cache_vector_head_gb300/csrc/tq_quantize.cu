@@ -641,13 +641,27 @@ static bool antisymmetric(const float* c, const float* t, int bits) {
   return true;
 }
 
+// Scale J of the code cell table (wq::code_cell): the smallest J <= kLutMaxJ for which
+// the 2^bits - 1 boundaries fall in distinct cells, else -1.
+static int code_lut_scale(const float* t, int bits) {
+  const int nb = (1 << bits) - 1;
+  for (int J = 0; J <= wq::kLutMaxJ; ++J) {
+    const float sc = (float)(32 << J);
+    bool ok = true;
+    for (int k = 0; k + 1 < nb && ok; ++k) ok = wq::code_cell(t[k], sc) < wq::code_cell(t[k + 1], sc);
+    if (ok) return J;
+  }
+  return -1;
+}
+
 template <int BITS, bool DENSE, int MODE>
 static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const void* x, long long n_vec,
                                         bool is_key, uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
                                         cudaStream_t st) {
   constexpr int warps = wq::warps_for(DENSE);
   auto kern = wq::quantize_warp_kernel<BITS, DENSE, MODE>;
-  const size_t sm = wq::smem_bytes(DENSE);
+  const int J = code_lut_scale(is_key ? P.kt : P.vt, BITS);
+  const size_t sm = wq::smem_bytes(DENSE) + wq::lut_bytes(J);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int occ = 0, dev = 0, sms = 0;
@@ -661,7 +675,7 @@ static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const
   gx = std::min(gx, (n_tiles + warps - 1) / warps);
   dim3 grid((int)std::min(gx, 65535LL), P.hkv);
   kern<<<grid, 32 * warps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, is_key ? 1 : 0,
-                                      codes, signs, norms, rnorms);
+                                      codes, signs, norms, rnorms, J);
   return cudaGetLastError();
 }
 
@@ -683,7 +697,10 @@ static bool warp_path_ok(const KParams& P, const void* x, int dtype, bool is_key
   if (is_key && (P.ksplit || P.knu8)) return false;
   if (P.kivi) return false;
   const bool sym = is_key ? antisymmetric(P.kc, P.kt, P.kb) : antisymmetric(P.vc, P.vt, P.vb);
-  return P.d == 128 && dtype == TQ_BF16 && sym && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
+  const int J = is_key ? code_lut_scale(P.kt, P.kb) : code_lut_scale(P.vt, P.vb);
+  // the dense key kernel's shared memory (operand tiles and Pi limbs) leaves room for J <= 2
+  const bool fits = J >= 0 && !(is_key && P.kqjl == TQ_KEY_QJL && P.kind != TQ_FWHT && J > 2);
+  return P.d == 128 && dtype == TQ_BF16 && sym && fits && ((uintptr_t)x & 15) == 0 && n_vec < (1LL << 32);
 }
 
 template <int BITS, bool DENSE, int MODE>
@@ -691,7 +708,8 @@ static cudaError_t launch_quantize_keys_tc(const KParams& P, const KCache& C, co
                                            uint32_t* codes, uint32_t* signs, float* norms, float* rnorms,
                                            cudaStream_t st) {
   auto kern = wq::quantize_keys_tc_kernel<BITS, DENSE, MODE>;
-  const size_t sm = wq::tc_smem_bytes(DENSE);
+  const int J = code_lut_scale(P.kt, BITS);
+  const size_t sm = wq::tc_smem_bytes(DENSE) + wq::lut_bytes(J);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -704,7 +722,7 @@ static cudaError_t launch_quantize_keys_tc(const KParams& P, const KCache& C, co
   gx = std::min(gx, n_ct);
   dim3 grid((int)std::min(gx, 65535LL), P.hkv);
   kern<<<grid, 32 * wq::kTcWarps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, codes, signs,
-                                            norms, rnorms);
+                                            norms, rnorms, J);
   return cudaGetLastError();
 }
 

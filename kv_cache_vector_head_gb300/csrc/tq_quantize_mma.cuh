@@ -41,6 +41,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <limits.h>
+#include <math.h>
+#include <string.h>
 
 #include "tq_device.cuh"
 
@@ -53,6 +55,10 @@ namespace wq {
 
 constexpr int D = 128;
 constexpr int KB = D / 16;     // k-blocks
+// code cell tables (see code_cell): 2^(5 + J) + 1 cells of 8 bytes, then 16 records
+constexpr int kLutMaxJ = 4;
+__host__ __device__ constexpr size_t lut_cells_bytes(int J) { return ((size_t)(32 << J) + 1) * 8; }
+__host__ __device__ constexpr size_t lut_bytes(int J) { return lut_cells_bytes(J) + 16 * 8; }
 
 // Permuted coordinates.  Logical index L in [0, 16) of k-block kk sits at
 // blk_base(kk) + free_off(L): bits 2, 5, 6 of the coordinate come from the
@@ -135,38 +141,96 @@ __device__ __forceinline__ uint32_t quad_transpose(uint32_t v, int t) {
   return (t < 2) ? __byte_perm(u, o, 0x5410) : __byte_perm(o, u, 0x7632);
 }
 
-// Positive half of an antisymmetric codebook: boundaries (as int bits,
-// ascending) and centroids.
-template <int BITS>
-struct Book {
-  int tp[BITS > 1 ? (1 << (BITS - 1)) - 1 : 1];
-  float cp[1 << (BITS - 1)];
-};
+// Code search by a cell table ([Reconstruction] §5 Step 3: the code of z is
+// the number of boundaries t_k <= z, ties up).  The real line is cut into
+// cells by
+//   cell(z) = RN( sat(RN(z / 32 + 1/2)) * 2^(5 + J) ),
+// two fp32 fmas with exact power-of-two scalings, so cell() is monotone and
+// the same on the host and the device; J is the smallest scale for which no
+// two boundaries share a cell (chosen by the launcher).  Entry i of the cell
+// table holds the one boundary b_i in cell i (+inf if none) and the number
+// base_i of boundaries in lower cells, so code(z) = base_i + [z >= b_i]
+// exactly.  Record c holds centroid c and the sign-magnitude code of c with
+// plane p moved to bit 8 p ("spread"), ready to be shifted into a packed word.
+// Per coordinate: three fmas, two shared loads, one compare.
 
-// Number of positive boundaries t with ai >= bits(t) (binary search).
-template <int BITS>
-__device__ __forceinline__ int magnitude(int ai, const Book<BITS>& b) {
-  if constexpr (BITS == 1) {
-    return 0;
-  } else if constexpr (BITS == 2) {
-    return ai >= b.tp[0] ? 1 : 0;
-  } else if constexpr (BITS == 3) {
-    const int m1 = ai >= b.tp[1] ? 2 : 0;
-    return m1 + (ai >= (m1 ? b.tp[2] : b.tp[0]) ? 1 : 0);
-  } else {
-    const int m2 = ai >= b.tp[3] ? 4 : 0;
-    const int m1 = ai >= (m2 ? b.tp[5] : b.tp[1]) ? 2 : 0;
-    const int th = m2 ? (m1 ? b.tp[6] : b.tp[4]) : (m1 ? b.tp[2] : b.tp[0]);
-    return m2 + m1 + (ai >= th ? 1 : 0);
-  }
+__host__ __device__ inline int code_cell(float z, float sc) {
+#ifdef __CUDA_ARCH__
+  const float s = __saturatef(__fmaf_rn(z, 0.03125f, 0.5f));
+  return __float_as_int(__fmaf_rn(s, sc, 12582912.0f)) - 0x4B400000;
+#else
+  float s = fmaf(z, 0.03125f, 0.5f);
+  s = s < 0.f ? 0.f : (s > 1.f ? 1.f : s);
+  const float c = fmaf(s, sc, 12582912.0f);
+  int bits;
+  memcpy(&bits, &c, sizeof bits);
+  return bits - 0x4B400000;
+#endif
 }
 
+// Sign-magnitude code of natural index c of a 2^bits-level antisymmetric book
+// (bit 0: z >= 0, bits 1..: number of boundaries between z and 0), spread.
+__host__ __device__ constexpr uint32_t spread_code(int c, int bits) {
+  return (((c >= (1 << (bits - 1))) ? (1u | ((uint32_t)(c - (1 << (bits - 1))) << 1))
+                                    : ((uint32_t)((1 << (bits - 1)) - 1 - c) << 1)) *
+          0x204081u) & 0x01010101u;
+}
+
+struct CodeLut {
+  uint32_t cells;  // shared address of the cell table minus 8 * bits(2^23 + 2^22): cell i at cells + 8 bits(fma)
+  float sc;        // 2^(5 + J)
+};
+
+// Builds the tables (all threads of the CTA; a barrier must follow).  bnd:
+// the 2^BITS - 1 ascending boundaries, cent: the 2^BITS centroids.  Cell i:
+// {b_i, shared address of record base_i}; record c: {centroid c, spread code}.
 template <int BITS>
-__device__ __forceinline__ float centroid_pos(int mag, const Book<BITS>& b) {
-  float c = b.cp[0];
-#pragma unroll
-  for (int i = 1; i < (1 << (BITS - 1)); ++i) c = mag == i ? b.cp[i] : c;
-  return c;
+__device__ void build_code_lut(unsigned char* at, int J, const float* bnd, const float* cent, int tid, int nt) {
+  constexpr int NB = (1 << BITS) - 1;
+  float2* cells = reinterpret_cast<float2*>(at);
+  uint2* recs = reinterpret_cast<uint2*>(at + lut_cells_bytes(J));
+  const int nc = (32 << J) + 1;
+  const float sc = (float)(32 << J);
+  for (int i = tid; i < nc; i += nt) {
+    int base = 0;
+    float b = __int_as_float(0x7f800000);
+    for (int k = 0; k < NB; ++k) {
+      const int ck = code_cell(bnd[k], sc);
+      base += ck < i ? 1 : 0;
+      if (ck == i) b = bnd[k];  // one boundary per cell (the launcher's choice of J)
+    }
+    cells[i] = make_float2(b, __uint_as_float((uint32_t)__cvta_generic_to_shared(recs + base)));
+  }
+  for (int c = tid; c <= NB; c += nt) recs[c] = make_uint2(__float_as_uint(cent[c]), spread_code(c, BITS));
+}
+
+__device__ __forceinline__ CodeLut code_lut_at(const unsigned char* at, int J) {
+  return CodeLut{(uint32_t)__cvta_generic_to_shared(at) - 8u * 0x4B400000u, (float)(32 << J)};
+}
+
+// Shared address of the record of z's code: cell entry, one exact compare
+// (z >= b_i: 0 or ~0), record base_i or base_i + 1.
+__device__ __forceinline__ uint32_t code_record_addr(float z, const CodeLut& L) {
+  const float s = __saturatef(__fmaf_rn(z, 0.03125f, 0.5f));
+  const uint32_t cb = __float_as_uint(__fmaf_rn(s, L.sc, 12582912.0f));
+  uint32_t ca, ra, ge;
+  float b;
+  asm("mad.lo.u32 %0, %1, 8, %2;" : "=r"(ca) : "r"(cb), "r"(L.cells));
+  asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(b), "=r"(ra) : "r"(ca));
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(ge) : "f"(z), "f"(b));
+  return ra - 8u * ge;  // ge = ~0: the next record
+}
+// Record of the code of z: .x centroid bits, .y spread code.
+__device__ __forceinline__ uint2 code_record(float z, const CodeLut& L) {
+  uint2 r;
+  asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(code_record_addr(z, L)));
+  return r;
+}
+// Spread code of z only.
+__device__ __forceinline__ uint32_t code_spread(float z, const CodeLut& L) {
+  uint32_t q;
+  asm("ld.shared.b32 %0, [%1 + 4];" : "=r"(q) : "r"(code_record_addr(z, L)));
+  return q;
 }
 
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
@@ -188,10 +252,9 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
     quantize_warp_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
                          const __nv_bfloat16* __restrict__ x, long long n_vec, int is_key,
                          uint32_t* __restrict__ codes, uint32_t* __restrict__ signs, float* __restrict__ norms,
-                         float* __restrict__ rnorms) {
+                         float* __restrict__ rnorms, int lut_j) {
   constexpr int WARPS = warps_for(DENSE);
   constexpr int NT = 32 * WARPS;
-  constexpr int HALF = 1 << (BITS - 1);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned char* dyn = smem_raw + sizeof(Shared);
@@ -200,6 +263,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
   uint4* blk = reinterpret_cast<uint4*>(dyn);    // [WARPS][2][KB][32]
   dyn += blk_bytes(DENSE);
   uint4* stage = reinterpret_cast<uint4*>(dyn);  // [WARPS][8][32]
+  dyn += stage_bytes(DENSE);
+  unsigned char* lut_at = dyn;                   // code cell table and records
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int head = blockIdx.y;
@@ -208,11 +273,8 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
   // keys with a scale in place of the sketch (EDEN / length-renormalized, one formula); false otherwise
   const bool corr = is_key && (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM);
-  Book<BITS> bk;
-#pragma unroll
-  for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(ttab[HALF + k]);
-#pragma unroll
-  for (int m = 0; m < HALF; ++m) bk.cp[m] = ctab[HALF + m];
+  build_code_lut<BITS>(lut_at, lut_j, ttab, ctab, tid, NT);
+  const CodeLut lut = code_lut_at(lut_at, lut_j);
 
   // ---- per-CTA constants.  The four elements of a B fragment (lane (g, t),
   // k-rows 2t, 2t+1, 2t+8, 2t+9 of k-block kk) sit at columns
@@ -462,18 +524,16 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
           float term[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);  // +0 for zero rows
-            const uint32_t zb = __float_as_uint(z);
-            const uint32_t neg = zb >> 31;
-            const int ai = (int)(zb & 0x7fffffffu) - (int)neg;  // for z < 0: |z| > t <=> ai >= bits(t)
-            const int mag = magnitude<BITS>(ai, bk);
-            const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
+            // +0 for zero rows (never -0: the +0 addend)
+            const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);
             const int pos = 4 * hh + i;  // coordinate blk_base(a) + 8t + i is bit 8t + 4hh + i of word m
-            Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
             if (corr) {
-              // z and its centroid share a sign: z C = |z| C+
-              const float c = centroid_pos<BITS>(mag, bk);
-              term[i] = fabsf(z) * c;
+              // z and its centroid share a sign: z C = |z| |C|
+              const uint2 rec = code_record(z, lut);
+              Wm[R] += rec.y << pos;
+              term[i] = fabsf(z) * fabsf(__uint_as_float(rec.x));
+            } else {
+              Wm[R] += code_spread(z, lut) << pos;
             }
           }
           if (corr) spart[R] += (term[0] + term[1]) + (term[2] + term[3]);
@@ -588,17 +648,17 @@ __host__ __device__ constexpr size_t tc_rest_bytes(bool dense) {
   return dense ? kPfragBytes : (size_t)KB * 2 * 32 * sizeof(uint2) + (size_t)kTcWarps * kBlkBytes;
 }
 __host__ __device__ constexpr size_t tc_smem_bytes(bool dense) {
-  return 4 * kUmmaTile + tc_rest_bytes(dense) + sizeof(TcShared);
+  return 4 * kUmmaTile + tc_rest_bytes(dense) + sizeof(TcShared);  // + lut_bytes(J)
 }
 
 template <int BITS, bool DENSE, int MODE>
 __global__ void __launch_bounds__(32 * kTcWarps, 1)
     quantize_keys_tc_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
                             const __nv_bfloat16* __restrict__ x, long long n_vec, uint32_t* __restrict__ codes,
-                            uint32_t* __restrict__ signs, float* __restrict__ norms, float* __restrict__ rnorms) {
+                            uint32_t* __restrict__ signs, float* __restrict__ norms, float* __restrict__ rnorms,
+                            int lut_j) {
   constexpr int WARPS = kTcWarps;
   constexpr int NT = 32 * WARPS;
-  constexpr int HALF = 1 << (BITS - 1);
   extern __shared__ __align__(16) unsigned char smem_raw[];  // the no-swizzle operand layout needs 16-byte alignment
   unsigned char* Ahi = smem_raw;
   unsigned char* Alo = smem_raw + kUmmaTile;
@@ -609,17 +669,15 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   uint2* hfrag = reinterpret_cast<uint2*>(rest);                                     // FWHT: [KB][2][32]
   uint4* blk = reinterpret_cast<uint4*>(rest + (size_t)KB * 2 * 32 * sizeof(uint2));  // FWHT: [WARPS][2][KB][32]
   TcShared& ts = *reinterpret_cast<TcShared*>(rest + tc_rest_bytes(DENSE));
+  unsigned char* lut_at = rest + tc_rest_bytes(DENSE) + sizeof(TcShared);  // code cell table and records
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int head = blockIdx.y;
   const float* rot = P.k_rot + (size_t)head * (DENSE ? D * D : D);
   // Gaussian S: [D][D] rows; structured S = H diag(sigma_S): the D signs, entries synthesised
   const float* S = P.qjl_s + (size_t)head * (P.qjl_srht ? D : D * D);
-  Book<BITS> bk;
-#pragma unroll
-  for (int k = 0; k + 1 < HALF; ++k) bk.tp[k] = __float_as_int(P.kt[HALF + k]);
-#pragma unroll
-  for (int m = 0; m < HALF; ++m) bk.cp[m] = P.kc[HALF + m];
+  build_code_lut<BITS>(lut_at, lut_j, P.kt, P.kc, tid, NT);
+  const CodeLut lut = code_lut_at(lut_at, lut_j);
 
   if (warp == 0) {  // tensor memory: the 128 x 128 fp32 accumulator of S r
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ts.tmem)),
@@ -729,6 +787,8 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = ts.tmem;
+  float smax = 0.f;
+  for (int c = 0; c < D; ++c) smax = fmaxf(smax, ts.snorm[c]);
 
   // ---- passes over 128 vectors (8 warp tiles of 16 tokens of this head)
   const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
@@ -921,14 +981,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float z = __fmaf_rn(zr[R][i], inv[R], 0.f);
-            const uint32_t zb = __float_as_uint(z);
-            const uint32_t neg = zb >> 31;
-            const int ai = (int)(zb & 0x7fffffffu) - (int)neg;
-            const int mag = magnitude<BITS>(ai, bk);
-            const uint32_t q = (neg ^ 1u) | ((uint32_t)mag << 1);
-            const int pos = 4 * hh + i;
-            Wm[R] |= (q * (0x204081u << pos)) & (0x01010101u << pos);
-            rv[R][i] = z - __uint_as_float(__float_as_uint(centroid_pos<BITS>(mag, bk)) ^ (neg << 31));
+            const uint2 rec = code_record(z, lut);
+            Wm[R] += rec.y << (4 * hh + i);
+            rv[R][i] = z - __uint_as_float(rec.x);
           }
         const int j0 = blk_base(a) + 8 * t;  // this lane's four coordinates of block a
 #pragma unroll
@@ -1010,6 +1065,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
       const float s2 = ts.s2[row];
       const float rn = sqrtf(s2);
       const float bA = fmaf(k1, rn, k2), bB = fmaf(k2, rn, k2);
+      const float bmax = fmaf(smax, bA, bB);  // the bound of the row's largest ||S_c||, for every c
       const uint32_t rec = ts.rec[row];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -1031,7 +1087,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
 #pragma unroll
         for (int j = 31; j >= 0; --j) {
           uint32_t lt;
-          asm("set.lt.u32.f32 %0, %1, %2;" : "=r"(lt) : "f"(fabsf(__uint_as_float(v[j]))), "f"(fmaf(ts.snorm[c0 + j], bA, bB)));
+          asm("set.lt.u32.f32 %0, %1, %2;" : "=r"(lt) : "f"(fabsf(__uint_as_float(v[j]))), "f"(bmax));
           asm("shf.l.wrap.b32 %0, %1, %2, 1;" : "=r"(neg) : "r"(v[j]), "r"(neg));
           asm("shf.l.wrap.b32 %0, %1, %2, 1;" : "=r"(pend) : "r"(lt), "r"(pend));
         }
