@@ -37,6 +37,7 @@ __device__ unsigned int g_quant_err = 0;
 }  // namespace tq
 
 #include "tq_quantize_mma.cuh"
+#include "tq_quantize_tc.cuh"
 
 namespace tq {
 
@@ -661,7 +662,7 @@ static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const
   constexpr int warps = wq::warps_for(DENSE);
   auto kern = wq::quantize_warp_kernel<BITS, DENSE, MODE>;
   const int J = code_lut_scale(is_key ? P.kt : P.vt, BITS);
-  const size_t sm = wq::smem_bytes(DENSE) + wq::lut_bytes(J);
+  const size_t sm = wq::smem_bytes(DENSE) + wq::lut_bytes(J, true);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int occ = 0, dev = 0, sms = 0;
@@ -709,7 +710,7 @@ static cudaError_t launch_quantize_keys_tc(const KParams& P, const KCache& C, co
                                            cudaStream_t st) {
   auto kern = wq::quantize_keys_tc_kernel<BITS, DENSE, MODE>;
   const int J = code_lut_scale(P.kt, BITS);
-  const size_t sm = wq::tc_smem_bytes(DENSE) + wq::lut_bytes(J);
+  const size_t sm = wq::tc_smem_bytes(DENSE) + wq::lut_bytes(J, false);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -753,8 +754,51 @@ static cudaError_t launch_quantize_warp_role(const KParams& P, const KCache& C, 
   return launch_quantize_warp_bits<true, MODE>(bits, P, C, x, n_vec, is_key, codes, signs, norms, rnorms, st);
 }
 
+// FWHT keys with the QJL sketch, both products on tcgen05 (wq::quantize_bt_kernel).
+template <int BITS>
+static cudaError_t launch_quantize_bt(const KParams& P, const void* x, long long n_vec, uint32_t* codes,
+                                      uint32_t* signs, float* norms, float* rnorms, int J, cudaStream_t st) {
+  auto kern = wq::quantize_bt_kernel<BITS>;
+  const size_t sm = wq::bt_smem_bytes(J);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 127) / 128;
+  if (n_tiles == 0) return cudaSuccess;
+  long long gx = std::max(1LL, (long long)sms / P.hkv);  // one CTA (two groups) per SM
+  gx = std::min(gx, (n_tiles + 1) / 2);
+  dim3 grid((int)std::min(gx, 65535LL), P.hkv);
+  kern<<<grid, wq::kBtThreads, sm, st>>>(P, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, codes, signs, norms,
+                                        rnorms, J);
+  return cudaGetLastError();
+}
+
+// Keys with the QJL sketch, FWHT: the tcgen05 kernel, when its shared memory (the operand
+// tiles leave room for cell tables with J <= 1) fits the device's opt-in limit.
+static bool bt_path_ok(const KParams& P, bool is_key) {
+  if (!is_key || P.kqjl != TQ_KEY_QJL || P.kind != TQ_FWHT || P.dh > 128 || P.dh % 8 != 0) return false;
+  const int J = code_lut_scale(P.kt, P.kb);
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return false;
+  return J >= 0 && wq::bt_smem_bytes(J) <= (size_t)optin;
+}
+
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
+  if (warp_path_ok(P, x, dtype, is_key, n_vec) && bt_path_ok(P, is_key)) {
+    const int J = code_lut_scale(P.kt, P.kb);
+    switch (P.kb) {
+      case 1: return launch_quantize_bt<1>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
+      case 2: return launch_quantize_bt<2>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
+      case 3: return launch_quantize_bt<3>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
+      default: return launch_quantize_bt<4>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
+    }
+  }
   if (warp_path_ok(P, x, dtype, is_key, n_vec))
     return launch_quantize_warp_role<wq::kFlat>(P, KCache{}, x, n_vec, is_key, codes, signs, norms, rnorms, st);
   if (P.d == 128) return launch_quantize_flat_d<128>(P, x, dtype, n_vec, is_key, codes, signs, norms, rnorms, st);

@@ -58,7 +58,10 @@ constexpr int KB = D / 16;     // k-blocks
 // code cell tables (see code_cell): 2^(5 + J) + 1 cells of 8 bytes, then 16 records
 constexpr int kLutMaxJ = 4;
 __host__ __device__ constexpr size_t lut_cells_bytes(int J) { return ((size_t)(32 << J) + 1) * 8; }
-__host__ __device__ constexpr size_t lut_bytes(int J) { return lut_cells_bytes(J) + 16 * 8; }
+// spread: a second cell table for code-only lookups (see code_spread)
+__host__ __device__ constexpr size_t lut_bytes(int J, bool spread) {
+  return lut_cells_bytes(J) + 16 * 8 + (spread ? lut_cells_bytes(J) : 0);
+}
 
 // Permuted coordinates.  Logical index L in [0, 16) of k-block kk sits at
 // blk_base(kk) + free_off(L): bits 2, 5, 6 of the coordinate come from the
@@ -148,7 +151,7 @@ __device__ __forceinline__ uint32_t quad_transpose(uint32_t v, int t) {
 // two fp32 fmas with exact power-of-two scalings, so cell() is monotone and
 // the same on the host and the device; J is the smallest scale for which no
 // two boundaries share a cell (chosen by the launcher).  Entry i of the cell
-// table holds the one boundary b_i in cell i (+inf if none) and the number
+// table holds the one boundary b_i in cell i (NaN if none) and the number
 // base_i of boundaries in lower cells, so code(z) = base_i + [z >= b_i]
 // exactly.  Record c holds centroid c and the sign-magnitude code of c with
 // plane p moved to bit 8 p ("spread"), ready to be shifted into a packed word.
@@ -177,35 +180,41 @@ __host__ __device__ constexpr uint32_t spread_code(int c, int bits) {
 }
 
 struct CodeLut {
-  uint32_t cells;  // shared address of the cell table minus 8 * bits(2^23 + 2^22): cell i at cells + 8 bits(fma)
-  float sc;        // 2^(5 + J)
+  uint32_t cells;   // shared address of the cell table minus 8 * bits(2^23 + 2^22): cell i at cells + 8 bits(fma)
+  uint32_t scells;  // the same for the code-only cell table
+  float sc;         // 2^(5 + J)
 };
 
 // Builds the tables (all threads of the CTA; a barrier must follow).  bnd:
 // the 2^BITS - 1 ascending boundaries, cent: the 2^BITS centroids.  Cell i:
-// {b_i, shared address of record base_i}; record c: {centroid c, spread code}.
-template <int BITS>
+// {b_i, shared address of record base_i}; record c: {centroid c, spread code};
+// code-only cell i (SPREAD): {b_i, spread(base_i) | spread(base_i + 1) << 1}.
+template <int BITS, bool SPREAD>
 __device__ void build_code_lut(unsigned char* at, int J, const float* bnd, const float* cent, int tid, int nt) {
   constexpr int NB = (1 << BITS) - 1;
   float2* cells = reinterpret_cast<float2*>(at);
   uint2* recs = reinterpret_cast<uint2*>(at + lut_cells_bytes(J));
+  float2* scells = reinterpret_cast<float2*>(at + lut_cells_bytes(J) + 16 * 8);
   const int nc = (32 << J) + 1;
   const float sc = (float)(32 << J);
   for (int i = tid; i < nc; i += nt) {
     int base = 0;
-    float b = __int_as_float(0x7f800000);
+    float b = __int_as_float(0x7fc00000);  // no boundary: NaN, so z >= b is false for every z
     for (int k = 0; k < NB; ++k) {
       const int ck = code_cell(bnd[k], sc);
       base += ck < i ? 1 : 0;
       if (ck == i) b = bnd[k];  // one boundary per cell (the launcher's choice of J)
     }
     cells[i] = make_float2(b, __uint_as_float((uint32_t)__cvta_generic_to_shared(recs + base)));
+    if (SPREAD)
+      scells[i] = make_float2(b, __uint_as_float(spread_code(base, BITS) | (spread_code(min(base + 1, NB), BITS) << 1)));
   }
   for (int c = tid; c <= NB; c += nt) recs[c] = make_uint2(__float_as_uint(cent[c]), spread_code(c, BITS));
 }
 
 __device__ __forceinline__ CodeLut code_lut_at(const unsigned char* at, int J) {
-  return CodeLut{(uint32_t)__cvta_generic_to_shared(at) - 8u * 0x4B400000u, (float)(32 << J)};
+  const uint32_t c = (uint32_t)__cvta_generic_to_shared(at) - 8u * 0x4B400000u;
+  return CodeLut{c, c + (uint32_t)(lut_cells_bytes(J) + 16 * 8), (float)(32 << J)};
 }
 
 // Shared address of the record of z's code: cell entry, one exact compare
@@ -226,11 +235,16 @@ __device__ __forceinline__ uint2 code_record(float z, const CodeLut& L) {
   asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(code_record_addr(z, L)));
   return r;
 }
-// Spread code of z only.
+// Spread code of z only, from the code-only cell table: one shared load, one compare.
 __device__ __forceinline__ uint32_t code_spread(float z, const CodeLut& L) {
-  uint32_t q;
-  asm("ld.shared.b32 %0, [%1 + 4];" : "=r"(q) : "r"(code_record_addr(z, L)));
-  return q;
+  const float s = __saturatef(__fmaf_rn(z, 0.03125f, 0.5f));
+  const uint32_t cb = __float_as_uint(__fmaf_rn(s, L.sc, 12582912.0f));
+  uint32_t ca, w, ge;
+  float b;
+  asm("mad.lo.u32 %0, %1, 8, %2;" : "=r"(ca) : "r"(cb), "r"(L.scells));
+  asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(b), "=r"(w) : "r"(ca));
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(ge) : "f"(z), "f"(b));
+  return (w >> (ge & 1u)) & 0x01010101u;
 }
 
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
   const float* rot = (is_key ? P.k_rot : P.v_rot) + (size_t)head * (DENSE ? D * D : D);
   // keys with a scale in place of the sketch (EDEN / length-renormalized, one formula); false otherwise
   const bool corr = is_key && (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM);
-  build_code_lut<BITS>(lut_at, lut_j, ttab, ctab, tid, NT);
+  build_code_lut<BITS, true>(lut_at, lut_j, ttab, ctab, tid, NT);
   const CodeLut lut = code_lut_at(lut_at, lut_j);
 
   // ---- per-CTA constants.  The four elements of a B fragment (lane (g, t),
@@ -676,7 +690,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const float* rot = P.k_rot + (size_t)head * (DENSE ? D * D : D);
   // Gaussian S: [D][D] rows; structured S = H diag(sigma_S): the D signs, entries synthesised
   const float* S = P.qjl_s + (size_t)head * (P.qjl_srht ? D : D * D);
-  build_code_lut<BITS>(lut_at, lut_j, P.kt, P.kc, tid, NT);
+  build_code_lut<BITS, false>(lut_at, lut_j, P.kt, P.kc, tid, NT);
   const CodeLut lut = code_lut_at(lut_at, lut_j);
 
   if (warp == 0) {  // tensor memory: the 128 x 128 fp32 accumulator of S r

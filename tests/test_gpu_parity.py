@@ -55,6 +55,8 @@ CASES = [
     ("llama", dict(batch=2, ctx=45, kind=SK.FWHT, key_bits=2, value_bits=1)),
     ("bulk", dict(ctx=400, key_bits=4, value_bits=2)),
     ("bulk", dict(ctx=5000, kind=SK.FWHT, key_bits=4, value_bits=3)),
+    # FWHT with the rotation on tcgen05: more 128-token tiles per head than the grid's groups
+    ("bulk", dict(ctx=6000, kind=SK.FWHT)),
     ("bulk", dict(ctx=20, kind=SK.FWHT, key_bits=1, key_qjl=False, value_bits=4)),
     ("bulk", dict(ctx=21, key_bits=2, key_qjl=False, value_bits=1)),
     # head sizes that are not powers of two, zero-padded to the transform size
