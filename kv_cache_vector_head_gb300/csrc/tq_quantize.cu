@@ -808,14 +808,15 @@ cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, lon
 // d = 256 direct slots through q256::direct256_kernel (FWHT kind, uniform key rate, float norms).
 static bool direct256_ok(const KParams& P) {
   return P.d == 256 && P.kind == TQ_FWHT && !P.kivi && !P.ksplit && !P.knu8 && antisymmetric(P.kc, P.kt, P.kb) &&
-         antisymmetric(P.vc, P.vt, P.vb);
+         antisymmetric(P.vc, P.vt, P.vb) && code_lut_scale(P.kt, P.kb) >= 0 && code_lut_scale(P.vt, P.vb) >= 0;
 }
 
 template <bool KEY, int SK>
 static cudaError_t launch_direct256_role(const KParams& P, const KCache& C, const void* x, int dtype, long long n_tok,
                                          const long long* slots, int seq_tok, int n_c, cudaStream_t st) {
   auto kern = q256::direct256_kernel<KEY, SK>;
-  const size_t sm = q256::smem_bytes(SK == 1);
+  const int J = KEY ? code_lut_scale(P.kt, P.kb) : code_lut_scale(P.vt, P.vb);
+  const size_t sm = q256::smem_bytes(SK == 1) + wq::lut_bytes(J, false);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -824,7 +825,8 @@ static cudaError_t launch_direct256_role(const KParams& P, const KCache& C, cons
   const long long tiles = (n_tok + q256::TILE - 1) / q256::TILE;
   const int per_sm = (KEY && SK == 1) ? 1 : 2;  // the sketch stages S in 128 KB of shared memory
   const long long gx = std::min<long long>(std::max(1, per_sm * sms / std::max(1, P.hkv)), tiles);
-  kern<<<dim3((unsigned)std::max<long long>(gx, 1), P.hkv), q256::NT, sm, st>>>(P, C, x, dtype, n_tok, slots, seq_tok, n_c);
+  kern<<<dim3((unsigned)std::max<long long>(gx, 1), P.hkv), q256::NT, sm, st>>>(P, C, x, dtype, n_tok, slots, seq_tok, n_c,
+                                                                               J);
   return cudaGetLastError();
 }
 

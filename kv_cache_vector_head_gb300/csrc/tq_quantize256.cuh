@@ -93,20 +93,6 @@ __device__ __forceinline__ void wht256(float (&v)[E], int lane) {
       }
 }
 
-// Code of z against an antisymmetric table (t[half - 1] = 0, t[half - 1 + k] = -t[half - 1 - k]):
-// idx = #{i : z >= t_i}, from the positive boundaries tp[k] = t[half + k] only.  z >= 0:
-// idx = half + #{k : z >= tp_k}; z < 0: z >= -tp_k <=> |z| <= tp_k, so idx = half - 1 -
-// #{k : |z| > tp_k}.  Returns the sign-magnitude pair: pos = (idx >= half), mag.
-__device__ __forceinline__ void code_sm(float z, const float (&tp)[7], int nb, unsigned& pos, int& mag) {
-  const float a = fabsf(z);
-  pos = z >= 0.f ? 1u : 0u;
-  int m = 0;
-#pragma unroll
-  for (int k = 0; k < 7; ++k)
-    if (k < nb) m += pos ? (z >= tp[k] ? 1 : 0) : (a > tp[k] ? 1 : 0);
-  mag = m;
-}
-
 // KEY: keys (else values).  SK: 0 no sketch (values, MSE-only / scaled keys), 1 Gaussian S on
 // the tensor cores, 2 structured S = H diag(sigma_S).  Direct slots as in append_direct_kernel:
 // slot_mapping[t] for input token t, or (slot_mapping == NULL) position p of sequence b at
@@ -115,7 +101,7 @@ template <bool KEY, int SK>
 __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel(const __grid_constant__ KParams P,
                                                           const __grid_constant__ KCache C, const void* x, int dtype,
                                                           long long n_tok, const long long* slot_mapping, int seq_tok,
-                                                          int n_c) {
+                                                          int n_c, int lut_j) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Tile& tl = *reinterpret_cast<Tile*>(smem_raw);
   uint2* sB = reinterpret_cast<uint2*>(smem_raw + sizeof(Tile));                       // [NTL][KS][32]
@@ -156,12 +142,10 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
   float sig[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) sig[e] = __ldg(sigma + e * 32 + lane);
-  float tp[7], cpos[8];  // positive boundaries and centroids of the antisymmetric table
-  const int nb = half - 1;
-#pragma unroll
-  for (int k = 0; k < 7; ++k) tp[k] = k < nb ? ttab[half + k] : 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) cpos[k] = k < half ? ctab[half + k] : 0.f;
+  // codes through the exact cell table (wq::code_record), after the tile's first barrier
+  unsigned char* lut_at = smem_raw + smem_bytes(SK == 1);
+  wq::build_code_lut_n<false>(lut_at, lut_j, ttab, ctab, bits, tid, NT);
+  const wq::CodeLut lut = wq::code_lut_at(lut_at, lut_j);
   float sgs[E];
   if constexpr (SK == 2) {
 #pragma unroll
@@ -250,17 +234,20 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
       wht256(z, lane);
 #pragma unroll
       for (int e = 0; e < E; ++e) z[e] *= inv;
-      unsigned pos[E];
-      int mag[E];
+      uint32_t q[E];  // sign-magnitude code, plane p at bit 8 p
+      float cz[E];    // its centroid
 #pragma unroll
-      for (int e = 0; e < E; ++e) code_sm(z[e], tp, nb, pos[e], mag[e]);
+      for (int e = 0; e < E; ++e) {
+        const uint2 rec = wq::code_record(z[e], lut);
+        q[e] = rec.y;
+        cz[e] = __uint_as_float(rec.x);
+      }
       unsigned char* sb = pg >= 0 ? C.pool + ((size_t)pg * P.hkv + head) * (size_t)P.sub_bytes : nullptr;
       // code planes: word e of plane p from one ballot (plane 0: sign side, planes 1..: magnitude bits)
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        uint32_t wv = __ballot_sync(0xffffffffu, pos[e]);
         for (int p = 0; p < bits; ++p) {
-          if (p > 0) wv = __ballot_sync(0xffffffffu, (mag[e] >> (p - 1)) & 1);
+          const uint32_t wv = __ballot_sync(0xffffffffu, (q[e] >> (8 * p)) & 1u);
           if (KEY) {
             if (lane == e && sb) reinterpret_cast<uint32_t*>(sb + P.off_kcodes)[(p * kPage + sl) * E + e] = wv;
           } else if (lane == e) {
@@ -273,15 +260,6 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
         continue;
       }
       if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_knorm)[sl] = zero ? 0.f : n;
-      // centroid of each coordinate: sign times the positive centroid of its magnitude
-      float cz[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        float c = cpos[0];
-#pragma unroll
-        for (int k = 1; k < 8; ++k) c = (k < half && mag[e] == k) ? cpos[k] : c;
-        cz[e] = pos[e] ? c : -c;
-      }
       if (corr == TQ_KEY_EDEN || corr == TQ_KEY_RENORM) {
         // the unbiased scale s = d / sum_j z_j C[idx_j] (z and its centroid share a sign)
         float tz[E];

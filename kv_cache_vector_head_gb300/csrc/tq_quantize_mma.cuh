@@ -189,9 +189,11 @@ struct CodeLut {
 // the 2^BITS - 1 ascending boundaries, cent: the 2^BITS centroids.  Cell i:
 // {b_i, shared address of record base_i}; record c: {centroid c, spread code};
 // code-only cell i (SPREAD): {b_i, spread(base_i) | spread(base_i + 1) << 1}.
-template <int BITS, bool SPREAD>
-__device__ void build_code_lut(unsigned char* at, int J, const float* bnd, const float* cent, int tid, int nt) {
-  constexpr int NB = (1 << BITS) - 1;
+template <bool SPREAD>
+__device__ void build_code_lut_n(unsigned char* at, int J, const float* bnd, const float* cent, int bits, int tid,
+                                 int nt) {
+  const int NB = (1 << bits) - 1;
+  const int BITS = bits;
   float2* cells = reinterpret_cast<float2*>(at);
   uint2* recs = reinterpret_cast<uint2*>(at + lut_cells_bytes(J));
   float2* scells = reinterpret_cast<float2*>(at + lut_cells_bytes(J) + 16 * 8);
@@ -210,6 +212,10 @@ __device__ void build_code_lut(unsigned char* at, int J, const float* bnd, const
       scells[i] = make_float2(b, __uint_as_float(spread_code(base, BITS) | (spread_code(min(base + 1, NB), BITS) << 1)));
   }
   for (int c = tid; c <= NB; c += nt) recs[c] = make_uint2(__float_as_uint(cent[c]), spread_code(c, BITS));
+}
+template <int BITS, bool SPREAD>
+__device__ void build_code_lut(unsigned char* at, int J, const float* bnd, const float* cent, int tid, int nt) {
+  build_code_lut_n<SPREAD>(at, J, bnd, cent, BITS, tid, nt);
 }
 
 __device__ __forceinline__ CodeLut code_lut_at(const unsigned char* at, int J) {

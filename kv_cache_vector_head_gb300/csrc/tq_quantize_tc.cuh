@@ -358,13 +358,14 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     ts.part[G][h][row] = rsum;  // every thread of the group has read the norm sums (barrier above)
     if (gt == 0 && !failed) {
       const uint32_t a_hi = smem_u32(buf), a_lo = smem_u32(buf + kBtTile), b_hi = smem_u32(Bhi), b_lo = smem_u32(Blo);
-      const uint32_t as_[3] = {a_hi, a_lo, a_hi}, bs_[3] = {b_hi, b_hi, b_lo};
-      const int npass = P.qjl_srht ? 2 : 3;  // structured S: exact in f16, no lo limb
-      for (int pss = 0; pss < npass; ++pss)
+#pragma unroll
+      for (int pss = 0; pss < 3; ++pss) {
+        if (pss == 2 && P.qjl_srht) break;  // structured S: exact in f16, no lo limb
+        const uint32_t a = pss == 1 ? a_lo : a_hi, b = pss == 2 ? b_lo : b_hi;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          bt_mma(tmem + 128, umma_desc(as_[pss] + 256 * ks), umma_desc(bs_[pss] + 256 * ks), id_f16,
-                 (pss > 0 || ks > 0) ? 1u : 0u);
+          bt_mma(tmem + 128, umma_desc(a + 256 * ks), umma_desc(b + 256 * ks), id_f16, (pss > 0 || ks > 0) ? 1u : 0u);
+      }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(&ts.mbar[G][1])));
     }
