@@ -788,6 +788,50 @@ static bool bt_path_ok(const KParams& P, bool is_key) {
   return J >= 0 && wq::bt_smem_bytes(J) <= (size_t)optin;
 }
 
+// Dense Pi, values and keys without the sketch: the rotation on tcgen05 (wq::quantize_bv_kernel).
+template <int BITS, int ROLE>
+static cudaError_t launch_quantize_bv(const KParams& P, const void* x, long long n_vec, uint32_t* codes,
+                                      float* norms, float* rnorms, int J, cudaStream_t st) {
+  auto kern = wq::quantize_bv_kernel<BITS, ROLE>;
+  const size_t sm = wq::bv_smem_bytes(J);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 127) / 128;
+  if (n_tiles == 0) return cudaSuccess;
+  long long gx = std::max(1LL, (long long)sms / P.hkv);  // one CTA (four groups) per SM
+  gx = std::min(gx, (n_tiles + wq::kBvGroups - 1) / wq::kBvGroups);
+  dim3 grid((int)std::min(gx, 65535LL), P.hkv);
+  kern<<<grid, wq::kBtThreads, sm, st>>>(P, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, codes, norms, rnorms,
+                                        J);
+  return cudaGetLastError();
+}
+
+template <int ROLE>
+static cudaError_t launch_quantize_bv_bits(int bits, const KParams& P, const void* x, long long n_vec,
+                                           uint32_t* codes, float* norms, float* rnorms, int J, cudaStream_t st) {
+  switch (bits) {
+    case 1: return launch_quantize_bv<1, ROLE>(P, x, n_vec, codes, norms, rnorms, J, st);
+    case 2: return launch_quantize_bv<2, ROLE>(P, x, n_vec, codes, norms, rnorms, J, st);
+    case 3: return launch_quantize_bv<3, ROLE>(P, x, n_vec, codes, norms, rnorms, J, st);
+    default: return launch_quantize_bv<4, ROLE>(P, x, n_vec, codes, norms, rnorms, J, st);
+  }
+}
+
+// Dense Pi without the sketch: the tcgen05 kernel when its shared memory fits.
+static bool bv_path_ok(const KParams& P, bool is_key) {
+  if (P.kind == TQ_FWHT || (is_key && P.kqjl == TQ_KEY_QJL) || P.dh > 128 || P.dh % 8 != 0) return false;
+  const int J = is_key ? code_lut_scale(P.kt, P.kb) : code_lut_scale(P.vt, P.vb);
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return false;
+  return J >= 0 && wq::bv_smem_bytes(J) <= (size_t)optin;
+}
+
 cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, long long n_vec, bool is_key,
                                  uint32_t* codes, uint32_t* signs, float* norms, float* rnorms, cudaStream_t st) {
   if (warp_path_ok(P, x, dtype, is_key, n_vec) && bt_path_ok(P, is_key)) {
@@ -798,6 +842,14 @@ cudaError_t launch_quantize_flat(const KParams& P, const void* x, int dtype, lon
       case 3: return launch_quantize_bt<3>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
       default: return launch_quantize_bt<4>(P, x, n_vec, codes, signs, norms, rnorms, J, st);
     }
+  }
+  if (warp_path_ok(P, x, dtype, is_key, n_vec) && bv_path_ok(P, is_key)) {
+    const int bits = is_key ? P.kb : P.vb;
+    const int J = code_lut_scale(is_key ? P.kt : P.vt, bits);
+    if (!is_key) return launch_quantize_bv_bits<0>(bits, P, x, n_vec, codes, norms, rnorms, J, st);
+    if (P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM)
+      return launch_quantize_bv_bits<2>(bits, P, x, n_vec, codes, norms, rnorms, J, st);
+    return launch_quantize_bv_bits<3>(bits, P, x, n_vec, codes, norms, rnorms, J, st);
   }
   if (warp_path_ok(P, x, dtype, is_key, n_vec))
     return launch_quantize_warp_role<wq::kFlat>(P, KCache{}, x, n_vec, is_key, codes, signs, norms, rnorms, st);

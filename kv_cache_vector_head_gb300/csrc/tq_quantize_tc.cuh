@@ -434,5 +434,210 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(512));
 }
 
+
+// ------------------------------------------------------------------ dense Pi without the sketch
+//
+// Values, and keys without the QJL sketch, with the dense rotation: the
+// rotation Z = X Pi^T runs on tcgen05 against Pi's three bf16 limbs (24
+// significant bits, as in quantize_warp_kernel) staged once per CTA as B
+// tiles: 24 steps per 128-token tile instead of the 384 mma.sync of the
+// warp tiles, which are tensor-bound.  Four groups of 4 warps, one row per
+// thread (its 128 rotated coordinates in four tcgen05.ld chunks); the next
+// tile is copied as soon as the rotation has read the current one.
+constexpr int kBvGroups = 4;
+
+struct BvShared {
+  uint64_t mbar[kBvGroups];
+  uint32_t tmem;
+};
+
+__host__ __device__ constexpr size_t bv_smem_bytes(int J) {
+  return 3 * kBtTile + kBvGroups * kBtTile + sizeof(BvShared) + lut_bytes(J, true);
+}
+
+// ROLE: 0 values, 2 keys with a scale (EDEN / length-renormalized: rnorms = d / sum z C),
+// 3 keys without either.  grid (x, Hkv): CTA (x, h) takes tiles 4 x + G (+ 4 gridDim.x).
+template <int BITS, int ROLE>
+__global__ void __launch_bounds__(kBtThreads, 1)
+    quantize_bv_kernel(const __grid_constant__ KParams P, const __nv_bfloat16* __restrict__ x, long long n_vec,
+                       uint32_t* __restrict__ codes, float* __restrict__ norms, float* __restrict__ rnorms,
+                       int lut_j) {
+  constexpr int NG = kBvGroups, GT = kBtThreads / NG;  // 4 warps per group
+  constexpr bool KEY = ROLE != 0;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* Bpi = smem_raw;  // [3 limbs][128 x 128 bf16]
+  unsigned char* buf0 = smem_raw + 3 * kBtTile;
+  BvShared& ts = *reinterpret_cast<BvShared*>(buf0 + NG * kBtTile);
+  unsigned char* lut_at = reinterpret_cast<unsigned char*>(&ts) + sizeof(BvShared);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = warp >> 2, sp = warp & 3, gt = tid % GT;  // group, TMEM sub-partition, thread in group
+  const int head = blockIdx.y;
+  const float* rot = (KEY ? P.k_rot : P.v_rot) + (size_t)head * D * D;
+  unsigned char* buf = buf0 + (size_t)G * kBtTile;
+
+  build_code_lut<BITS, ROLE != 2>(lut_at, lut_j, KEY ? P.kt : P.vt, KEY ? P.kc : P.vc, tid, kBtThreads);
+  if (warp == 0) {  // tensor memory: one 128-column rotation accumulator per group
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ts.tmem)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int g = 0; g < NG; ++g) asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&ts.mbar[g])), "r"(1));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // ---- Pi in three bf16 limbs as B tiles: B_l[n][k] = limb l of Pi[n][k]
+  for (int i = tid; i < D * (D / 8); i += kBtThreads) {
+    const int n = i >> 4, k0 = 8 * (i & 15);
+    const float4 a = __ldg(reinterpret_cast<const float4*>(rot + (size_t)n * D + k0));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(rot + (size_t)n * D + k0 + 4));
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t l[3][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t h[3][2];
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        const float x0 = v[2 * e + f];
+        const float l0 = __bfloat162float(__float2bfloat16_rn(x0));
+        const float l1 = __bfloat162float(__float2bfloat16_rn(x0 - l0));
+        h[0][f] = bf16_bits(x0);
+        h[1][f] = bf16_bits(x0 - l0);
+        h[2][f] = bf16_bits((x0 - l0) - l1);
+      }
+#pragma unroll
+      for (int t = 0; t < 3; ++t) l[t][e] = h[t][0] | (h[t][1] << 16);
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+      *reinterpret_cast<uint4*>(Bpi + t * kBtTile + umma_off(n, k0)) = make_uint4(l[t][0], l[t][1], l[t][2], l[t][3]);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B tiles: read by the tensor cores
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const CodeLut lut = code_lut_at(lut_at, lut_j);
+  const uint32_t tmem = ts.tmem + (uint32_t)G * 128u;
+  const uint32_t trow = tmem + ((uint32_t)(32 * sp) << 16);
+
+  const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
+  const long long n_tiles = (n_tok + 127) / 128;
+  const uint32_t id_bf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+  const int row = 32 * sp + lane;
+  uint32_t ph = 0;
+  bool failed = false;
+
+  // a warp copies 8 rows x 4 chunks of 16 bytes per step: chunk 4 ci + lane / 8 of row
+  // 32 sp + 8 rh + (lane & 7)
+  const int lr = 32 * sp + (lane & 7), lc = lane >> 3;
+  auto load_tile = [&](long long tl) {
+#pragma unroll
+    for (int rh = 0; rh < 4; ++rh) {
+      const long long tk = tl * 128 + lr + 8 * rh;
+      const long long n = tk * P.hkv + head;
+      const bool rin = tk < n_tok && n < n_vec;
+      const __nv_bfloat16* rp = x + (rin ? (size_t)n * P.dh : 0);
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) {
+        const int c = 4 * ci + lc;
+        const bool in = rin && 8 * c < P.dh;
+        cp_async16(buf + umma_off(lr + 8 * rh, 8 * c), in ? rp + 8 * c : x, in ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+  const long long tstride = (long long)NG * gridDim.x;
+  long long tile = (long long)blockIdx.x * NG + G;
+  if (tile < n_tiles) load_tile(tile);
+  for (; tile < n_tiles && !failed; tile += tstride) {
+    cp_async_wait_all();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    bt_bar(G, GT);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (gt == 0) {  // Z = X Pi^T: 3 limbs x 8 k-steps
+      const uint32_t a = smem_u32(buf), b = smem_u32(Bpi);
+#pragma unroll
+      for (int t = 0; t < 3; ++t)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          bt_mma(tmem, umma_desc(a + 256 * ks), umma_desc(b + (uint32_t)(t * kBtTile) + 256 * ks), id_bf16,
+                 (t > 0 || ks > 0) ? 1u : 0u);
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(&ts.mbar[G])));
+    }
+    // ---- norm of the row from its bf16 inputs (exact squares, balanced fp32 trees), while the rotation runs
+    const long long tok = tile * 128 + row;
+    const long long nrow = tok * P.hkv + head;
+    const bool ok = tok < n_tok && nrow < n_vec;
+    float hs[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float q2[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + umma_off(row, 64 * q + 8 * c));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+          q2[4 * c + k] = lo * lo + hi * hi;
+        }
+      }
+      hs[q] = tree32(q2);
+    }
+    const float s2 = hs[0] + hs[1];
+    if (!bt_wait(&ts.mbar[G], ph)) {
+      atomicOr(&g_quant_err, TQ_DEVERR_TIMEOUT);
+      failed = true;
+    }
+    ph ^= 1u;
+    failed = bt_bar_or(G, GT, failed);  // the input tile is read; one verdict on the wait
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tile + tstride < n_tiles && !failed) load_tile(tile + tstride);
+    const float nrm = sqrtf(s2);
+    const bool zero = nrm < kZeroNorm;
+    const float inv = zero ? 0.f : sqrtf((float)D / s2);  // z = sqrt(d) Pi x / n
+    if (ok && !failed) norms[nrow] = zero ? 0.f : nrm;
+
+    // ---- codes of the row's 128 coordinates (four words per plane)
+    uint32_t cw[4][4];
+    float ssum = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[32];
+      if (!failed) bt_ld32(trow + (uint32_t)(32 * cc), v);
+      uint32_t acc[4] = {0u, 0u, 0u, 0u};
+      float sq[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float z = __fmaf_rn(__uint_as_float(v[j]), inv, 0.f);  // +0 for zero rows
+        if constexpr (ROLE == 2) {
+          const uint2 rec = code_record(z, lut);
+          acc[j >> 3] += rec.y << (j & 7);
+          sq[j] = fabsf(z) * fabsf(__uint_as_float(rec.x));  // z C >= 0
+        } else {
+          acc[j >> 3] += code_spread(z, lut) << (j & 7);
+        }
+      }
+      planes_of(acc, cw[cc]);
+      if constexpr (ROLE == 2) ssum += tree32(sq);
+    }
+    if (ok && !failed) {
+      uint32_t* cp = codes + (size_t)nrow * BITS * 4;
+#pragma unroll
+      for (int p = 0; p < BITS; ++p)
+        *reinterpret_cast<uint4*>(cp + 4 * p) = make_uint4(cw[0][p], cw[1][p], cw[2][p], cw[3][p]);
+      if constexpr (ROLE == 2) rnorms[nrow] = zero ? 0.f : (float)D / ssum;
+    }
+    // the accumulator is rewritten by the next tile
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    failed = bt_bar_or(G, GT, failed);
+  }
+  cp_async_wait_all();  // a prefetch issued before a failed wait
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(ts.tmem), "r"(512));
+}
+
 }  // namespace wq
 }  // namespace tq
