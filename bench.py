@@ -75,6 +75,10 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="resident layer caches rotated over (0: per workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--quantize-only", action="store_true",
+                    help="only the bulk quantize measurement (one JSON line), e.g. under a profiler")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the prefill of the workload's cache into pages (one JSON line)")
     return ap.parse_args()
 
 
@@ -927,6 +931,28 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_part(args):
+    """One measurement of run_gpu on its own (bulk quantize, or the workload's prefill into pages)."""
+    import torch
+
+    from kv_cache_vector_head_gb300 import build
+
+    build.build()
+    import kv_cache_vector_head_gb300 as tq
+    import synthetic_kv as SK
+
+    peaks = measured_peaks() or {}
+    if args.quantize_only:
+        print(json.dumps(bench_quantize(tq, torch, peaks)))
+        return
+    w = SK.workload(args.workload)
+    if w.kivi:
+        raise SystemExit("--prefill-only: the KIVI arm fills pages in its own layout")
+    L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
+                   key_qjl=w.key_qjl, seed=w.seed, layer=0, key_split=w.key_split, key_norm_range=w.key_norm_range)
+    print(json.dumps(bench_prefill_quantize(tq, torch, L, w, peaks)))
+
+
 def main():
     args = parse()
     if args.cpu_sample:
@@ -934,6 +960,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.quantize_only or args.prefill_only:
+        run_gpu_part(args)
         return
     run_gpu(args)
 
