@@ -121,10 +121,14 @@ WsLayout decode_ws_layout(const KParams& P, int batch, int max_ctx, int n_splits
   if (S <= 0) {
     const int units = std::max(1, batch * P.hkv);
     // two waves of resident CTAs, or one wave where that would leave a split fewer than
-    // four 8-page chunks (the per-CTA start-up would not amortise)
+    // four 8-page chunks (the per-CTA start-up would not amortise).  With a window every unit
+    // also runs a window split, which holds a slot too: counting it keeps the grid from
+    // spilling a few CTAs into a further wave (Qwen-like call: 18 + 1 splits a unit fill two
+    // waves exactly and take 174 us, 19 + 1 take 199 us)
     const int cps = mma_ctas_per_sm(P.d);
-    S = (2 * cps * num_sms + units - 1) / units;
-    if (max_pages / S < 32) S = (cps * num_sms + units - 1) / units;
+    const int win = P.window > 0 ? 1 : 0;
+    S = (2 * cps * num_sms + units - 1) / units - win;
+    if (S < 1 || max_pages / S < 32) S = (cps * num_sms + units - 1) / units - win;
     S = std::max(1, std::min(S, (max_pages + 7) / 8));
   }
   S = std::min(S, max_pages);
