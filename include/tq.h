@@ -62,6 +62,10 @@ typedef enum { TQ_ROLE_KEY_ROT = 0, TQ_ROLE_VALUE_ROT = 1, TQ_ROLE_QJL = 2, TQ_R
 #define TQ_DEVERR_SEQ_LEN    0x2u   /* seq_len beyond block table + window   */
 #define TQ_DEVERR_SLOT       0x4u   /* slot_mapping entry outside the pool   */
 #define TQ_DEVERR_TIMEOUT    0x8u   /* a bounded wait on a TMA copy ran out  */
+#define TQ_DEVERR_CODEBOOK   0x10u  /* two code boundaries in one cell of the
+                                       quantize kernels' code table (their
+                                       codes are then unreliable; not expected:
+                                       the host picks the table's scale)     */
 
 #define TQ_PAGE_SIZE 16
 #define TQ_MAX_BITS 4

@@ -200,13 +200,17 @@ __device__ void build_code_lut_n(unsigned char* at, int J, const float* bnd, con
   const int nc = (32 << J) + 1;
   const float sc = (float)(32 << J);
   for (int i = tid; i < nc; i += nt) {
-    int base = 0;
+    int base = 0, in_cell = 0;
     float b = __int_as_float(0x7fc00000);  // no boundary: NaN, so z >= b is false for every z
     for (int k = 0; k < NB; ++k) {
       const int ck = code_cell(bnd[k], sc);
       base += ck < i ? 1 : 0;
-      if (ck == i) b = bnd[k];  // one boundary per cell (the launcher's choice of J)
+      if (ck == i) {  // one boundary per cell (the launcher's choice of J)
+        b = bnd[k];
+        ++in_cell;
+      }
     }
+    if (in_cell > 1) atomicOr(&g_quant_err, TQ_DEVERR_CODEBOOK);
     cells[i] = make_float2(b, __uint_as_float((uint32_t)__cvta_generic_to_shared(recs + base)));
     if (SPREAD)
       scells[i] = make_float2(b, __uint_as_float(spread_code(base, BITS) | (spread_code(min(base + 1, NB), BITS) << 1)));
