@@ -174,6 +174,10 @@ __host__ __device__ inline float xdelta(int p) {
   return p == 10 ? -0.5f : p == 11 ? -0.75f : p == 12 ? -0.9375f : p == 13 ? -0.99609375f : -2.0f;
 }
 __host__ __device__ inline float xkfac(int p) { return 2.0f * (p == 14 ? 2.0f : 1.0f) + xdelta(p); }
+// RN(1 / xdelta(p)) (the correctly rounded quotients: -2, -4/3, -16/15, -256/255, -1/2)
+__host__ __device__ inline float xdelta_inv(int p) {
+  return p == 10 ? -2.0f : p == 11 ? -1.33333337f : p == 12 ? -1.06666672f : p == 13 ? -1.00392163f : -0.5f;
+}
 // B register of key bit i (and i + 16) from the word's copies shifted by 0, 6 and 10;
 // b1, b2 = xbase(10), xbase(14) in registers
 __device__ __forceinline__ uint32_t xreg_key(uint32_t w0, uint32_t w6, uint32_t w10, int i, uint32_t b1, uint32_t b2) {
@@ -274,8 +278,15 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   const int G = P.G;
   const int n0 = blockIdx.y * kPrologueTile;
   const int nv = min(kPrologueTile, batch * G - n0);
-  // the rows of S this thread multiplies do not depend on the query: their loads are issued
-  // first and land while the query is loaded and rotated
+  // the query first (the rotation needs it at once); the rows of S this thread multiplies do
+  // not depend on it: their loads follow and land while the query is rotated
+  float qv[kPrologueTile];
+#pragma unroll
+  for (int v = 0; v < kPrologueTile; ++v) {
+    const int n = n0 + v, b = n / G, hl = n % G;
+    qv[v] = (v < nv && j < P.dh) ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * P.dh + j))
+                                 : 0.f;  // zero-padded to D
+  }
   constexpr int TPR = D / 64;  // threads per row of S: each CTA owns 64 rows (coordinates 64 z .. 64 z + 63)
   const bool dense_s = P.kqjl == TQ_KEY_QJL && !P.qjl_srht;
   // thread su of a row takes the float4 columns i4 * TPR + su: TPR neighbouring threads read
@@ -287,11 +298,8 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
 #pragma unroll
     for (int i4 = 0; i4 < 16; ++i4) sreg[i4] = __ldg(rp + i4 * TPR);
   }
-  for (int v = 0; v < kPrologueTile; ++v) {
-    const int n = n0 + v, b = n / G, hl = n % G;
-    s.x[v][j] = (v < nv && j < P.dh) ? load_elem(q, dtype, (long long)((((size_t)b * P.hq + (size_t)g * G + hl)) * P.dh + j))
-                                     : 0.f;  // zero-padded to D
-  }
+#pragma unroll
+  for (int v = 0; v < kPrologueTile; ++v) s.x[v][j] = qv[v];
   if (j < kTile) s.inv[j] = P.kind == TQ_FWHT ? rsqrtf((float)D) : 1.0f;
   __syncthreads();
   rotate_tile<D, kPrologueTile>(s, nv, P.kind, P.k_rot + (size_t)g * (P.kind == TQ_FWHT ? D : D * D));
@@ -336,51 +344,60 @@ __global__ void __launch_bounds__(D) decode_prologue_kernel(const __grid_constan
   // where they are stored (coordinates < d/2)
   const int nplanes = P.kp + (P.kqjl == TQ_KEY_QJL ? 1 : 0);
   const int per_row = nplanes * 64;
-  for (int v = 0; v < nv; ++v) {
+  // the entries of all nv query vectors in one pass: vector v has per_row entries of its own
+  // rows (lanes with lane / 4 == hl) and, for the sequence's first head, per_row of every row of
+  // an absent head (zeroed)
+  const int nabs = 8 - G;
+  int ntot = 0;
+  for (int v = 0; v < nv; ++v) ntot += per_row * (((n0 + v) % G == 0) ? 1 + nabs : 1);
+  for (int idx = j; idx < ntot; idx += D) {
+    int v = 0, rem = idx;
+    for (;;) {  // the vector of entry idx (at most kPrologueTile steps)
+      const int cnt = per_row * (((n0 + v) % G == 0) ? 1 + nabs : 1);
+      if (rem < cnt) break;
+      rem -= cnt;
+      ++v;
+    }
     const int n = n0 + v, b = n / G, hl = n % G;
     uint32_t* frag = reinterpret_cast<uint32_t*>(ws + L.afrag + ((size_t)b * P.hkv + g) * L.afrag_bytes_per_head);
-    // this head's rows (lanes with lane / 4 == hl); head 0 also zeroes the rows of absent heads
-    const int nrow = (hl == 0) ? (8 - G + 1) : 1;
-    for (int idx = j; idx < per_row * nrow; idx += D) {
-      const int rowsel = idx / per_row, e = idx - rowsel * per_row;
-      const int r = e & 3, pl = e >> 6, qe = e & 63;
-      const bool half_plane = P.ksplit && pl >= P.kp / 2;
-      int kk, t4;
-      if (D == 128 && half_plane) {  // words 0 and 1 across all four lanes, 4 k-steps
-        if (z != 0) continue;
-        kk = qe >> 4;
-        t4 = (qe >> 2) & 3;
-      } else {
-        if (half_plane && z >= 2) continue;  // d = 256: not stored beyond the first half
-        kk = 8 * (z >> 1) + (qe >> 3);
-        t4 = 2 * (z & 1) + ((qe >> 2) & 1);
-      }
-      int ca, ib;
-      frag_entry<D>(half_plane, kk, t4, r, ca, ib);
-      const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
-      uint32_t val = 0;
-      if (rowsel == 0) {
-        const int cb = ca + 16;
-        float va, vb;
-        if (pl < P.kp) {
-          // mixed-channel keys: coordinates < d/2 follow the wider book
-          const float a = ca < D / 2 ? P.akw_hi[pl] : P.akw[pl];
-          va = a * s.x[v][ca];
-          vb = a * s.x[v][cb];
-        } else {
-          va = s.r[v][ca];
-          vb = s.r[v][cb];
-        }
-        const float rd = 1.0f / xdelta(xpos_key(ib));  // the B side reads bit ib as base + b delta
-        va *= rd;
-        vb *= rd;
-        __half ha, la, hb, lb;
-        split_f16(va, ha, la);
-        split_f16(vb, hb, lb);
-        val = (r & 1) ? pack_h2(la, lb) : pack_h2(ha, hb);
-      }
-      frag[((frag_plane_base(P, pl, KS) + kk) * 32 + g8 * 4 + t4) * 4 + r] = val;
+    const int rowsel = rem / per_row, e = rem - rowsel * per_row;
+    const int r = e & 3, pl = e >> 6, qe = e & 63;
+    const bool half_plane = P.ksplit && pl >= P.kp / 2;
+    int kk, t4;
+    if (D == 128 && half_plane) {  // words 0 and 1 across all four lanes, 4 k-steps
+      if (z != 0) continue;
+      kk = qe >> 4;
+      t4 = (qe >> 2) & 3;
+    } else {
+      if (half_plane && z >= 2) continue;  // d = 256: not stored beyond the first half
+      kk = 8 * (z >> 1) + (qe >> 3);
+      t4 = 2 * (z & 1) + ((qe >> 2) & 1);
     }
+    int ca, ib;
+    frag_entry<D>(half_plane, kk, t4, r, ca, ib);
+    const int g8 = rowsel == 0 ? hl : (G - 1 + rowsel);
+    uint32_t val = 0;
+    if (rowsel == 0) {
+      const int cb = ca + 16;
+      float va, vb;
+      if (pl < P.kp) {
+        // mixed-channel keys: coordinates < d/2 follow the wider book
+        const float a = ca < D / 2 ? P.akw_hi[pl] : P.akw[pl];
+        va = a * s.x[v][ca];
+        vb = a * s.x[v][cb];
+      } else {
+        va = s.r[v][ca];
+        vb = s.r[v][cb];
+      }
+      const float rd = xdelta_inv(xpos_key(ib));  // the B side reads bit ib as base + b delta
+      va *= rd;
+      vb *= rd;
+      __half ha, la, hb, lb;
+      split_f16(va, ha, la);
+      split_f16(vb, hb, lb);
+      val = (r & 1) ? pack_h2(la, lb) : pack_h2(ha, hb);
+    }
+    frag[((frag_plane_base(P, pl, KS) + kk) * 32 + g8 * 4 + t4) * 4 + r] = val;
   }
 }
 
