@@ -77,6 +77,8 @@ def parse():
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--quantize-only", action="store_true",
                     help="only the bulk quantize measurement (one JSON line), e.g. under a profiler")
+    ap.add_argument("--prefill-attention-only", action="store_true",
+                    help="only the prefill attention of 64-token chunks on the workload's cache (one JSON line)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the prefill of the workload's cache into pages (one JSON line)")
     return ap.parse_args()
@@ -705,9 +707,10 @@ def quality_report(tq, torch, T=4096):
 
 def bench_prefill(tq, torch, L, pc, w, recs, nq=64, calls=5):
     """Prefill attention: the last nq appended tokens of every sequence of one layer
-    cache attend causally to it (one launch of the decode pipeline over batch x nq
-    virtual sequences).  Algorithmic bytes: every query's visible records, window,
-    q and output, as for a decode call of its length."""
+    cache attend causally to it (one tq_prefill_attention call: query tiles of 16
+    (query, head) rows per page pass where the layer allows it, else batch x nq
+    virtual decode sequences).  Algorithmic bytes: every query's visible records,
+    window, q and output, as for a decode call of its length."""
     B, Hkv, Hq, d, W = w.batch, w.n_kv_heads, w.n_q_heads, w.d, w.window
     T = int(pc.seq_len[0].item())
     q = torch.randn(B, nq, Hq, d, device="cuda", dtype=torch.bfloat16)
@@ -727,7 +730,7 @@ def bench_prefill(tq, torch, L, pc, w, recs, nq=64, calls=5):
                  for i in range(nq))
     return {"n_query": nq, "ctx": T, "ms": ms, "query_tokens_per_s": B * nq / (ms * 1e-3),
             "visible_GB_per_s": nbytes / (ms * 1e-3) / 1e9,
-            "note": "each query re-reads its visible pages (L2-resident across a sequence's queries)"}
+            "note": "visible bytes count every query's records; a page pass serves 16 (query, head) rows"}
 
 
 def bench_append_batch256(tq, torch, steps=200):
@@ -946,6 +949,19 @@ def run_gpu_part(args):
         print(json.dumps(bench_quantize(tq, torch, peaks)))
         return
     w = SK.workload(args.workload)
+    if args.prefill_attention_only:
+        L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
+                       key_qjl=w.key_qjl, seed=w.seed, layer=0, key_split=w.key_split,
+                       key_norm_range=w.key_norm_range, kivi=w.kivi)
+        pc = tq.PagedCache(L, w.batch, w.ctx + 16)
+        K, V, _ = SK.keys_values_torch(w, layer=0, ctx=w.ctx)
+        pc.prefill(K, V)
+        del K, V
+        torch.cuda.synchronize()
+        if tq.check_device_error():
+            raise RuntimeError("device error after prefill")
+        print(json.dumps(bench_prefill(tq, torch, L, pc, w, workload_records(w))))
+        return
     if w.kivi:
         raise SystemExit("--prefill-only: the KIVI arm fills pages in its own layout")
     L = tq.TQLayer(w.d, w.n_kv_heads, w.n_q_heads, w.key_bits, w.value_bits, w.kind, window=w.window,
@@ -961,7 +977,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
-    if args.quantize_only or args.prefill_only:
+    if args.quantize_only or args.prefill_only or args.prefill_attention_only:
         run_gpu_part(args)
         return
     run_gpu(args)

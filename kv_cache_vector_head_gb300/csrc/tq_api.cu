@@ -195,7 +195,8 @@ static tq_status make_cache(const tq_cache* c, const KParams& K, KCache* C, bool
 // for batch * n_query sequences.
 static size_t prefill_layout(const KParams& K, int batch, int n_query, int max_ctx, WsLayout* L) {
   const size_t head = ((size_t)3 * batch * n_query * sizeof(int32_t) + 255) & ~(size_t)255;
-  *L = decode_ws_layout(K, batch * n_query, max_ctx, 0, num_sms());
+  const int S = prefill_tiles_ok(K) ? prefill_tile_splits(K, batch, n_query, max_ctx, num_sms()) : 0;
+  *L = decode_ws_layout(K, batch * n_query, max_ctx, S, num_sms());
   return head + L->total;
 }
 
@@ -364,6 +365,9 @@ extern "C" tq_status tq_prefill_attention(const tq_layer_params* p, const tq_cac
   V.n_compressed = nc_v;
   V.parent = parent;
   V.batch = (int)nv;
+  if (prefill_tiles_ok(K))
+    return cuda_status(launch_prefill_tiles(K, V, n_query, cache->batch, q, dtype, scale, out, lse, dws, L, max_ctx, st),
+                       "tq_prefill_attention");
   return cuda_status(launch_decode(K, V, q, dtype, scale, out, lse, nullptr, dws, L, max_ctx, st),
                      "tq_prefill_attention");
 }

@@ -1486,6 +1486,8 @@ __global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_c
   }
 }
 
+#include "tq_prefill_mma.cuh"
+
 // ------------------------------------------------------------------ launcher
 
 template <int D, bool VLUT, bool KMIX, int KPF>
@@ -1610,6 +1612,119 @@ cudaError_t launch_decode(const KParams& P, const KCache& C, const void* q, int 
                           float* lse, float* scores, void* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
   if (P.d == 128) return launch_decode_d<128>(P, C, q, dtype, scale, out, lse, scores, ws, L, max_ctx, st);
   return launch_decode_d<256>(P, C, q, dtype, scale, out, lse, scores, ws, L, max_ctx, st);
+}
+
+// ------------------------------------------------------------------ prefill tiles
+
+bool prefill_tiles_ok(const KParams& P) {
+  if (P.kivi || P.ksplit || P.knu8 || P.kqjl != TQ_KEY_QJL || (P.kp != 2 && P.kp != 4) || P.vb < 2) return false;
+  if (P.d != 128 && P.d != 256) return false;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    optin = 232448;  // sm_103a: 227 KB a block
+  }
+  const size_t afr = (size_t)kPfTiles * (P.kp + 1) * (P.d / 16) * 32 * 16;
+  const size_t need = afr + (size_t)2 * kPfWarps * P.sub_bytes + (size_t)kPfPidCache * sizeof(long long) + sizeof(PfShared);
+  return need <= (size_t)optin;
+}
+
+// Compressed splits of the tile path: the split count (1..8, at least 32 pages a split) whose
+// CTAs (one per SM) fill their last wave best, a point of fill outweighing one more split.
+int prefill_tile_splits(const KParams& P, int batch, int n_query, int max_ctx, int num_sms) {
+  const long long ups = ((long long)n_query * P.G + kPfRows - 1) / kPfRows;
+  const long long units = std::max(1LL, (long long)batch * P.hkv * ups);
+  const int max_pages = std::max(1, (max_ctx + kPage - 1) / kPage);
+  int best = 1;
+  double best_eff = -1.0;
+  for (int S = 1; S <= 8; ++S) {
+    if (S > 1 && max_pages / S < 32) break;
+    const double w = (double)(units * S) / std::max(1, num_sms);
+    const double eff = w / ceil(w) - 0.01 * (S - 1);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = S;
+    }
+  }
+  return best;
+}
+
+template <int D, bool VLUT, int KPF>
+static cudaError_t launch_tiles(const KParams& P, const KCache& C, int n_query, int batch, float scale,
+                                unsigned char* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
+  const int ups = (n_query * P.G + kPfRows - 1) / kPfRows;
+  const size_t pid_bytes = (size_t)std::min(L.pages_per_split, kPfPidCache) * sizeof(long long);
+  const size_t afr = (size_t)kPfTiles * L.afrag_bytes_per_head;
+  const size_t stage_bytes = (size_t)kPfWarps * P.sub_bytes;
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  int nst = kStages;
+  size_t dyn = afr + nst * stage_bytes + pid_bytes;
+  if (dyn + sizeof(PfShared) > (size_t)optin) {
+    nst = 2;
+    dyn = afr + nst * stage_bytes + pid_bytes;
+  }
+  e = cudaFuncSetAttribute(prefill_tiles_kernel<D, VLUT, KPF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  // programmatic dependent of the prologue: pages stream while it runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.n_comp_splits, P.hkv, batch * ups);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_tiles_kernel<D, VLUT, KPF>, P, C, n_query, ups, scale, ws, L, max_ctx, nst);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_prefill_tiles_d(const KParams& P, const KCache& V, int n_query, int batch, const void* q,
+                                          int dtype, float scale, float* out, float* lse, unsigned char* w,
+                                          const WsLayout& L, int max_ctx, cudaStream_t st) {
+  const int nv = V.batch;
+  const size_t tsm = sizeof(TileSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsm);
+  if (e != cudaSuccess) return e;
+  const dim3 gp(P.hkv, (nv * P.G + kPrologueTile - 1) / kPrologueTile, D / 64);
+  decode_prologue_kernel<D><<<gp, D, tsm, st>>>(P, q, dtype, w, L, nv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (P.vb >= 3)
+    e = P.kp == 2 ? launch_tiles<D, true, 2>(P, V, n_query, batch, scale, w, L, max_ctx, st)
+                  : launch_tiles<D, true, 4>(P, V, n_query, batch, scale, w, L, max_ctx, st);
+  else
+    e = P.kp == 2 ? launch_tiles<D, false, 2>(P, V, n_query, batch, scale, w, L, max_ctx, st)
+                  : launch_tiles<D, false, 4>(P, V, n_query, batch, scale, w, L, max_ctx, st);
+  if (e != cudaSuccess) return e;
+  const size_t wdyn = window_smem_bytes(D);
+  if (wdyn > 48 * 1024) {
+    e = cudaFuncSetAttribute(prefill_window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wdyn);
+    if (e != cudaSuccess) return e;
+  }
+  prefill_window_kernel<D><<<dim3(P.hkv, nv), kMmaThreads, wdyn, st>>>(P, V, q, dtype, scale, w, L, max_ctx);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t cdyn = (size_t)(L.n_comp_splits + 1) * sizeof(float);
+  if (cdyn > 48 * 1024) {
+    e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cdyn);
+    if (e != cudaSuccess) return e;
+  }
+  decode_combine_kernel<D><<<dim3(P.hq, nv), kCombThreads, cdyn, st>>>(P, w, L, out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tiles(const KParams& P, const KCache& V, int n_query, int batch, const void* q, int dtype,
+                                 float scale, float* out, float* lse, void* ws, const WsLayout& L, int max_ctx,
+                                 cudaStream_t st) {
+  unsigned char* w = reinterpret_cast<unsigned char*>(ws);
+  if (P.d == 128)
+    return launch_prefill_tiles_d<128>(P, V, n_query, batch, q, dtype, scale, out, lse, w, L, max_ctx, st);
+  return launch_prefill_tiles_d<256>(P, V, n_query, batch, q, dtype, scale, out, lse, w, L, max_ctx, st);
 }
 
 __global__ void prefill_virtual_kernel(const __grid_constant__ KCache C, int n_query, int32_t* seq_v,

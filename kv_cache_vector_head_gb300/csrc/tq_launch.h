@@ -36,6 +36,16 @@ cudaError_t launch_decode(const KParams& P, const KCache& C, const void* q, int 
 cudaError_t launch_prefill_virtual(const KCache& C, int n_query, int32_t* seq_v, int32_t* nc_v, int32_t* parent,
                                    cudaStream_t st);
 
+// Prefill attention with query tiles: 16 (query, head) rows of a chunk per CTA share every page
+// (TurboQuant_prod keys with 2 or 4 Walsh planes, values of 2..4 bits, no mixed-channel keys or
+// byte norms, d = 128 or 256).  V is the chunk's virtual-sequence cache; the workspace layout
+// takes prefill_tile_splits() compressed splits.
+bool prefill_tiles_ok(const KParams& P);
+int prefill_tile_splits(const KParams& P, int batch, int n_query, int max_ctx, int num_sms);
+cudaError_t launch_prefill_tiles(const KParams& P, const KCache& V, int n_query, int batch, const void* q, int dtype,
+                                 float scale, float* out, float* lse, void* ws, const WsLayout& L, int max_ctx,
+                                 cudaStream_t st);
+
 cudaError_t read_clear_quant_error(unsigned* bits);
 cudaError_t read_clear_decode_error(unsigned* bits);
 #ifdef TQ_TEST_HOOKS

@@ -420,6 +420,11 @@ PREFILL = [
     ("tiny", dict(key_qjl=2), 37, 12, 49),
     ("llama", dict(batch=2, kind=SK.FWHT, qjl_structured=1), 40, 9, 16),
     ("mixed", dict(batch=1, window=20), 61, 20, 33),
+    # query tiles: a ragged last unit (42 rows), one query, 4-bit values with a window, several splits
+    ("qwen", dict(batch=2, window=20), 75, 30, 7),
+    ("qwen", dict(batch=1), 50, 3, 1),
+    ("llama", dict(batch=2, window=20), 60, 25, 37),
+    ("qwen", dict(batch=1, window=20), 1500, 6, 11),
 ]
 
 
