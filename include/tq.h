@@ -372,9 +372,13 @@ tq_status tq_decode_attention_static(const tq_layer_params* p, const tq_cache* c
  * n_query tokens already appended to every sequence: query i of sequence b
  * sits at position p = seq_len[b] - n_query + i and attends causally to the
  * cached positions 0 .. p (compressed pages and the float16 window), with the
- * same score and output rules as tq_decode_attention.  Each query runs as a
+ * same score and output rules as tq_decode_attention.  Each query is a
  * virtual decode sequence of visible length p + 1 over its sequence's block
- * table and window ring (one launch of the decode pipeline for all queries).
+ * table and window ring.  For TurboQuant_prod keys (QJL sketch, 2 or 3 code
+ * bits, no mixed-channel rate or byte norms) with values of 2..4 bits the
+ * compressed pages are scored for 16 (query, head) rows of the chunk per page
+ * pass (query tiles); other layers run the decode pipeline over the virtual
+ * sequences.  The workspace size accounts for either.
  *   q         [device] [batch][n_query][Hq][head_dim] in dtype
  *   out       [device] out, float [batch][n_query][Hq][head_dim]
  *   lse       [device] out, float [batch][n_query][Hq] (nullable)
