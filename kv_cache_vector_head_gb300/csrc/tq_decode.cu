@@ -1704,10 +1704,10 @@ static cudaError_t launch_prefill_tiles_d(const KParams& P, const KCache& V, int
   if (e != cudaSuccess) return e;
   const size_t wdyn = window_smem_bytes(D);
   if (wdyn > 48 * 1024) {
-    e = cudaFuncSetAttribute(prefill_window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wdyn);
+    e = cudaFuncSetAttribute(prefill_attn_window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wdyn);
     if (e != cudaSuccess) return e;
   }
-  prefill_window_kernel<D><<<dim3(P.hkv, nv), kMmaThreads, wdyn, st>>>(P, V, q, dtype, scale, w, L, max_ctx);
+  prefill_attn_window_kernel<D><<<dim3(P.hkv, nv), kMmaThreads, wdyn, st>>>(P, V, q, dtype, scale, w, L, max_ctx);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t cdyn = (size_t)(L.n_comp_splits + 1) * sizeof(float);
   if (cdyn > 48 * 1024) {

@@ -563,10 +563,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // The float16 window of every virtual sequence of the chunk (decode's window split), grid
 // (Hkv, batch x n_query).
 template <int D>
-__global__ void __launch_bounds__(kMmaThreads) prefill_window_kernel(const __grid_constant__ KParams P,
-                                                                     const __grid_constant__ KCache C, const void* q,
-                                                                     int dtype, float scale, unsigned char* ws,
-                                                                     WsLayout L, int max_ctx) {
+__global__ void __launch_bounds__(kMmaThreads)
+    prefill_attn_window_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C, const void* q,
+                               int dtype, float scale, unsigned char* ws, WsLayout L, int max_ctx) {
   extern __shared__ __align__(128) unsigned char dyn[];
   window_split<D>(P, C, q, dtype, scale, nullptr, ws, L, max_ctx, blockIdx.x, blockIdx.y, dyn);
 }
