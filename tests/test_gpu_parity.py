@@ -425,6 +425,7 @@ PREFILL = [
     ("qwen", dict(batch=1), 50, 3, 1),
     ("llama", dict(batch=2, window=20), 60, 25, 37),
     ("qwen", dict(batch=1, window=20), 1500, 6, 11),
+    ("qwen", dict(batch=2, window=20, head_dim=160), 45, 30, 13),
 ]
 
 
@@ -470,3 +471,26 @@ def test_prefill_attention_parity(tq, name, over, T0, steps, nq):
             r = PY.decode_reference(O, q[b, i], comp, wk, wv, scale)
             assert np.abs(g_out[b, i] - r["out"]).max() < PY.OUT_ATOL, (b, i)
             assert np.abs(g_lse[b, i] - r["lse"]).max() < PY.SCORE_ATOL, (b, i)
+
+
+def test_prefill_attention_short_sequence_is_flagged(tq):
+    """A sequence shorter than the chunk is flagged on the device (TQ_DEVERR_SEQ_LEN), its
+    queries see the tokens that exist, and the other sequence's result is unaffected."""
+    w = SK.workload("qwen", batch=2, window=20)
+    kv, L, O, pc = _paged_roundtrip(tq, w, 40, 4)
+    T, nq = 44, 8
+    rng = np.random.default_rng(7)
+    qt = SK.to_torch(rng.standard_normal((w.batch, nq, w.n_q_heads, w.dh)), w.dtype).cuda()
+    ws = torch.empty(tq.prefill_workspace_size(L.params, w.batch, nq, T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.batch, nq, w.n_q_heads, w.dh, device="cuda")
+    tq.prefill_attention(L.params, pc.cache, nq, qt, 0.0625, out, None, ws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    ref = out.clone()
+    pc.seq_len[1] = 5
+    pc.n_compressed[1] = 0
+    tq.prefill_attention(L.params, pc.cache, nq, qt, 0.0625, out, None, ws, T)
+    bits = tq.check_device_error()
+    assert bits & 0x2
+    assert torch.isfinite(out).all()
+    assert torch.equal(out[0], ref[0])
