@@ -5,7 +5,9 @@ kv head is compared with the oracle's (codes and signs bit-exact outside the
 boundary band, norms to 1e-6), and the decode is compared on every score, the
 log-sum-exp and the output of all query heads against the oracle's decode of
 its own records with the GPU's choices adopted exactly where the rules accept
-either decision (so no token is skipped).  Workloads: Qwen-like (batch 8,
+either decision (so no token is skipped).  The same cache then serves a
+64-token prefill-attention chunk (the bench's), its first and last queries
+checked against the oracle's decode over their visible positions.  Workloads: Qwen-like (batch 8,
 32768 tokens, window 128, FWHT, keys 2b + QJL, values 2b), Llama-like (batch
 32, 8192 tokens, no window, dense Pi, outlier channels, keys 3b + QJL, values
 4b) and long context (one sequence of 131072 tokens, 8192 pages split over the
@@ -71,6 +73,7 @@ def test_fullsize_decode_sampled_sequences(tq, name, sampled):
     pool = pc.pool.cpu().numpy()
     bt = pc.block_table.cpu().numpy()
     stats = {}
+    adopted = {}
     for b in SAMPLED:
         s = kv[b]
         recs_k = [O.keys(s["K"][0, :nc, h], h) for h in range(w.n_kv_heads)]
@@ -91,3 +94,37 @@ def test_fullsize_decode_sampled_sequences(tq, name, sampled):
         assert err.max() < PY.SCORE_ATOL, err.max()
         assert np.abs(out[b].cpu().numpy() - ref["out"]).max() < PY.OUT_ATOL
         assert np.abs(lse[b].cpu().numpy() - ref["lse"]).max() < PY.SCORE_ATOL
+        adopted[b] = (ad_k, ad_v)
+
+    # prefill attention of the last 64 tokens (the bench's chunk) on the same cache: sampled
+    # queries against the oracle's decode over positions 0 .. p of the adopted records
+    nq = 64
+    rng = np.random.default_rng(4321)
+    qp = rng.standard_normal((B, nq, w.n_q_heads, w.dh)).astype(np.float32)
+    qpt = SK.to_torch(qp, w.dtype).cuda()
+    qp = qpt.float().cpu().numpy().astype(np.float64)
+    pws = torch.empty(tq.prefill_workspace_size(L.params, B, nq, T), dtype=torch.uint8, device="cuda")
+    pout = torch.zeros(B, nq, w.n_q_heads, w.dh, device="cuda")
+    plse = torch.zeros(B, nq, w.n_q_heads, device="cuda")
+    tq.prefill_attention(L.params, pc.cache, nq, qpt, scale, pout, plse, pws, T)
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    pout, plse = pout.cpu().numpy(), plse.cpu().numpy()
+    for b in SAMPLED:
+        s = kv[b]
+        ad_k, ad_v = adopted[b]
+        for i in (0, nq - 1):
+            Ti = T - nq + i + 1
+            nci = min(nc, Ti)
+            comp = PY.stack_comp([_trunc(r, nc, nci) for r in ad_k], [_trunc(r, nc, nci) for r in ad_v])
+            wk = s["K"][0, nci:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nci else None
+            wv = s["V"][0, nci:Ti].transpose(1, 0, 2).astype(np.float16) if Ti > nci else None
+            r = PY.decode_reference(O, qp[b, i], comp, wk, wv, scale)
+            assert np.abs(pout[b, i] - r["out"]).max() < PY.OUT_ATOL, (b, i)
+            assert np.abs(plse[b, i] - r["lse"]).max() < PY.SCORE_ATOL, (b, i)
+
+
+def _trunc(rec, n_all, n):
+    """The first n token records of an oracle record dict holding n_all tokens."""
+    return {k: (v[:n] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == n_all else v)
+            for k, v in rec.items()}
