@@ -673,7 +673,8 @@ static cudaError_t launch_quantize_warp(const KParams& P, const KCache& C, const
   const long long n_tiles = (n_tok + 15) / 16;
   if (n_tiles == 0) return cudaSuccess;
   long long gx = std::max(1LL, (long long)std::max(occ, 1) * sms / P.hkv);
-  gx = std::min(gx, (n_tiles + warps - 1) / warps);
+  // bulk: adjacent tiles per CTA; a decode-step append interleaves its tiles over as many CTAs
+  gx = std::min(gx, MODE == wq::kStep ? n_tiles : (n_tiles + warps - 1) / warps);
   dim3 grid((int)std::min(gx, 65535LL), P.hkv);
   kern<<<grid, 32 * warps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, is_key ? 1 : 0,
                                       codes, signs, norms, rnorms, J);
@@ -717,13 +718,19 @@ static cudaError_t launch_quantize_keys_tc(const KParams& P, const KCache& C, co
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
-  const long long n_ct = ((n_tok + 15) / 16 + wq::kTcWarps - 1) / wq::kTcWarps;
-  if (n_ct == 0) return cudaSuccess;
+  const long long n_tiles = (n_tok + 15) / 16;
+  if (n_tiles == 0) return cudaSuccess;
+  // warp tiles a CTA pass: all 8 for bulk calls; a decode-step append spreads its tiles over
+  // the SMs (one CTA per SM for the shared memory) when it has fewer than 8 a CTA
+  int tp = wq::kTcWarps;
+  if (MODE == wq::kStep)
+    tp = (int)std::min<long long>(wq::kTcWarps, std::max<long long>(1, (n_tiles * P.hkv + sms - 1) / sms));
+  const long long n_ct = (n_tiles + tp - 1) / tp;
   long long gx = std::max(1LL, (long long)sms / P.hkv);  // one CTA per SM (shared memory)
   gx = std::min(gx, n_ct);
   dim3 grid((int)std::min(gx, 65535LL), P.hkv);
   kern<<<grid, 32 * wq::kTcWarps, sm, st>>>(P, C, reinterpret_cast<const __nv_bfloat16*>(x), n_vec, codes, signs,
-                                            norms, rnorms, J);
+                                            norms, rnorms, J, tp);
   return cudaGetLastError();
 }
 

@@ -382,7 +382,9 @@ __global__ void __launch_bounds__(32 * warps_for(DENSE), ctas_for(DENSE))
     }
     if constexpr (!DENSE) cp_async_commit();
   };
-  long long mt = (long long)blockIdx.x * WARPS + warp;
+  // bulk calls: a CTA's warps take adjacent tiles; a decode-step append spreads its few tiles
+  // over CTAs (warp w of CTA c: tile c + gridDim.x w), so each CTA holds one or two
+  long long mt = MODE == kStep ? (long long)blockIdx.x + (long long)gridDim.x * warp : (long long)blockIdx.x * WARPS + warp;
   if (mt < n_tiles) load(mt);
   for (; mt < n_tiles; mt += stride) {
     uint4 X[2][4];
@@ -680,7 +682,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     quantize_keys_tc_kernel(const __grid_constant__ KParams P, const __grid_constant__ KCache C,
                             const __nv_bfloat16* __restrict__ x, long long n_vec, uint32_t* __restrict__ codes,
                             uint32_t* __restrict__ signs, float* __restrict__ norms, float* __restrict__ rnorms,
-                            int lut_j) {
+                            int lut_j, int tp) {
   constexpr int WARPS = kTcWarps;
   constexpr int NT = 32 * WARPS;
   extern __shared__ __align__(16) unsigned char smem_raw[];  // the no-swizzle operand layout needs 16-byte alignment
@@ -817,7 +819,10 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   // ---- passes over 128 vectors (8 warp tiles of 16 tokens of this head)
   const long long n_tok = (n_vec + P.hkv - 1) / P.hkv;
   const long long n_tiles = (n_tok + 15) / 16;
-  const long long n_ct = (n_tiles + WARPS - 1) / WARPS;
+  // a pass covers tp warp tiles (tp = WARPS for bulk calls; fewer spread a small decode-step
+  // append over more CTAs): warp w < tp takes tile ct tp + w, the others hold no rows
+  const long long n_ct = (n_tiles + tp - 1) / tp;
+  auto warp_tile = [&](long long ct) -> long long { return warp < tp ? ct * tp + warp : n_tiles; };
   uint4* wb = blk + (size_t)warp * 2 * KB * 32;  // FWHT: this warp's rotated tile
   // |three-limb f16 product - exact product of the fp32 values|
   //   <= k1 ||r|| ||S_c|| + k2 (||r|| + ||S_c||):
@@ -848,15 +853,15 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   };
   uint32_t phase = 0;
   bool failed = false;
-  if (blockIdx.x < n_ct) load((long long)blockIdx.x * WARPS + warp);
+  if (blockIdx.x < n_ct) load(warp_tile(blockIdx.x));
   for (long long ct = blockIdx.x; ct < n_ct && !failed; ct += gridDim.x) {
-    const long long mt = ct * WARPS + warp;
+    const long long mt = warp_tile(ct);
     uint4 X[2][4];
 #pragma unroll
     for (int R = 0; R < 2; ++R)
 #pragma unroll
       for (int m = 0; m < 4; ++m) X[R][m] = nxt[R][m];
-    if (ct + gridDim.x < n_ct) load((ct + gridDim.x) * WARPS + warp);
+    if (ct + gridDim.x < n_ct) load(warp_tile(ct + gridDim.x));
 
     long long nrow[2];
     bool okrow[2];
