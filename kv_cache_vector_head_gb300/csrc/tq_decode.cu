@@ -1212,280 +1212,9 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const __gr
   if (lse && tid == 0) lse[head] = empty ? -INFINITY : M + logf(Lsum);
 }
 
-// ------------------------------------------------------------------ KIVI control arm (CUDA cores)
+// ------------------------------------------------------------------ KIVI control arm (tensor cores)
 
-// [Design study] §Candidate key and value algorithms, arm 3.  Pages hold
-// integer codes with float16 scale / zero: a key's channel j dequantizes to
-// zk_j + sk_j c (per page), a value of token t to zv_t + sv_t c.  The per-page
-// key scales make the query operand page dependent, so the contraction runs on
-// CUDA cores: warp w scores page w of each 8-page chunk (lane = token t,
-// coordinate half), then every thread accumulates its coordinate's values,
-// sum_t p_t (zv_t + sv_t c_tj) = sum_t (p_t sv_t) c_tj + sum_t p_t zv_t.
-template <int D>
-struct KiviShared {
-  alignas(16) float q[TQ_MAX_GQA][D];                     // query rows of the G heads
-  alignas(16) float ks[kMmaPages][D];                     // key scales of the chunk's pages (float)
-  alignas(16) float kz[kMmaPages][D];                     // key zeros
-  alignas(16) float sc[kMmaPages * kPage][TQ_MAX_GQA];    // scores
-  alignas(16) float ps[kMmaPages * kPage][TQ_MAX_GQA];    // softmax weight x value scale
-  float pz[TQ_MAX_GQA], alpha[TQ_MAX_GQA], m_run[TQ_MAX_GQA], l_run[TQ_MAX_GQA];
-  uint64_t full[kStages];
-};
-
-template <int D, int KB, int VB>
-__global__ void __launch_bounds__(kMmaThreads) kivi_decode_kernel(const __grid_constant__ KParams P,
-                                                                  const __grid_constant__ KCache C, const void* q,
-                                                                  int dtype, float scale, float* scores,
-                                                                  unsigned char* ws, WsLayout L, int max_ctx,
-                                                                  int nst) {
-  constexpr int NW = kMmaThreads / 32;   // pages per chunk
-  constexpr int CT = NW * kPage;          // tokens per chunk
-  constexpr int KPW = 32 / KB, VPW = 32 / VB;
-  constexpr int KW = D * KB / 32, VW = D * VB / 32;  // code words per token
-  constexpr int NTH = kMmaThreads / D;    // value phase: threads per coordinate (token groups)
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ KiviShared<D> sh;
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  if (s == L.n_comp_splits) {  // the float16 window runs as the last split
-    window_split<D>(P, C, q, dtype, scale, scores, ws, L, max_ctx, g, b, dyn);
-    return;
-  }
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = P.G;
-  const int st = L.n_comp_splits + 1;
-  const size_t head0 = (size_t)b * P.hq + (size_t)g * G;
-  const int sub = P.sub_bytes;
-  unsigned char* stage0 = dyn;                                                     // [nst][NW][sub]
-  long long* pids = reinterpret_cast<long long*>(stage0 + (size_t)nst * NW * sub);  // [<= kPidCache]
-
-  const int cb = C.parent ? C.parent[b] : b;  // cache row of (virtual) sequence b
-  int T = C.seq_len[b], nc = C.n_compressed[b];
-  if (T < 0 || T > max_ctx || nc < 0 || nc > T) {
-    if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
-    T = min(max(T, 0), max_ctx);
-    nc = min(max(nc, 0), T);
-  }
-  int np = (nc + kPage - 1) / kPage;
-  if (np > C.max_pages) {
-    if (tid == 0) atomicOr(&g_decode_err, TQ_DEVERR_SEQ_LEN);
-    np = C.max_pages;
-  }
-  const int p0 = s * L.pages_per_split;
-  const int p1 = min(p0 + L.pages_per_split, np);
-  const int npg = max(0, p1 - p0);
-  const int nchunks = (npg + NW - 1) / NW;
-  const int ncache = min(npg, kPidCache);
-
-  for (int i = tid; i < ncache; i += kMmaThreads) {
-    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
-    if (pid < 0 || pid >= C.n_pages) {
-      atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
-      pid = -1;
-    }
-    pids[i] = pid;
-  }
-  for (int i = tid; i < TQ_MAX_GQA * D; i += kMmaThreads) {
-    const int h = i / D, j = i % D;
-    sh.q[h][j] = h < G ? load_elem(q, dtype, (long long)((head0 + h) * P.dh + j)) : 0.f;
-  }
-  for (int i = tid; i < CT * TQ_MAX_GQA; i += kMmaThreads) (&sh.ps[0][0])[i] = 0.f;  // heads >= G stay 0
-  if (tid < TQ_MAX_GQA) {
-    sh.m_run[tid] = -INFINITY;
-    sh.l_run[tid] = 0.f;
-    sh.alpha[tid] = 1.f;
-    sh.pz[tid] = 0.f;
-  }
-  if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  auto page_id = [&](int i) -> long long {
-    if (i >= npg) return -1;
-    if (i < ncache) return pids[i];
-    long long pid = C.block_table[(size_t)cb * C.max_pages + p0 + i];
-    if (pid < 0 || pid >= C.n_pages) {
-      atomicOr(&g_decode_err, TQ_DEVERR_PAGE_INDEX);
-      pid = -1;
-    }
-    return pid;
-  };
-  auto issue = [&](int k) {  // warp 0: chunk k into stage k % nst, lane i < NW copies page i
-    const int stg = k % nst;
-    const long long pid = lane < NW ? page_id(k * NW + lane) : -1;
-    const unsigned valid = __ballot_sync(0xffffffffu, pid >= 0);
-    if (lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sh.full[stg], (uint32_t)__popc(valid) * (uint32_t)sub + test_extra_tx(k));
-    }
-    __syncwarp();
-    if (pid >= 0)
-      bulk_g2s(stage0 + ((size_t)stg * NW + lane) * sub, C.pool + ((size_t)pid * P.hkv + g) * (size_t)sub,
-               (uint32_t)sub, &sh.full[stg]);
-  };
-  if (warp == 0)
-    for (int k = 0; k < nst - 1 && k < nchunks; ++k) issue(k);
-
-  const int vj = tid % D, th = tid / D;  // value phase: coordinate vj, token group th
-  float acc[TQ_MAX_GQA];
-#pragma unroll
-  for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] = 0.f;
-  bool timed_out = false;
-  int kstop = nchunks;  // chunks consumed
-
-  for (int k = 0; k < nchunks; ++k) {
-    // chunk k-1 fully consumed: its stage and sh.wf may be rewritten.  A wait that ran out
-    // stops the split here, for every thread alike (no new copies into unfinished phases)
-    if (__syncthreads_or(timed_out)) {
-      kstop = k;
-      break;
-    }
-    if (warp == 0 && k + nst - 1 < nchunks) issue(k + nst - 1);
-    const int stg = k % nst;
-    if (!mbar_wait_bounded(&sh.full[stg], (uint32_t)((k / nst) & 1))) timed_out = true;
-    unsigned char* stbase = stage0 + (size_t)stg * NW * sub;
-
-    // ---------------- scores: warp w, page w of the chunk; lane = (token t, coordinate half hf),
-    // the half interleaved in groups of 4 (coordinates 8 i + 4 hf .. 8 i + 4 hf + 3)
-    const int pi = k * NW + warp;
-    const bool pvalid = pi < npg && page_id(pi) >= 0;
-    const unsigned char* pb = stbase + (size_t)warp * sub;
-    {
-      const __half* ks16 = reinterpret_cast<const __half*>(pb + P.off_kscale);
-      const __half* kz16 = reinterpret_cast<const __half*>(pb + P.off_kzero);
-      for (int j = lane; j < D; j += 32) {
-        sh.ks[warp][j] = pvalid ? __half2float(ks16[j]) : 0.f;
-        sh.kz[warp][j] = pvalid ? __half2float(kz16[j]) : 0.f;
-      }
-    }
-    __syncwarp();
-    {
-      const int t = lane >> 1, hf = lane & 1;
-      float a[TQ_MAX_GQA];
-#pragma unroll
-      for (int h = 0; h < TQ_MAX_GQA; ++h) a[h] = 0.f;
-      if (pvalid) {
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(pb + P.off_kcodes) + t * KW;
-#pragma unroll 4
-        for (int i = 0; i < D / 8; ++i) {
-          const int j = 8 * i + 4 * hf;
-          const uint32_t w = kc[(j * KB) / 32] >> ((j * KB) % 32);
-          const float4 s4 = *reinterpret_cast<const float4*>(&sh.ks[warp][j]);
-          const float4 z4 = *reinterpret_cast<const float4*>(&sh.kz[warp][j]);
-          const float k0 = fmaf(s4.x, (float)(w & ((1u << KB) - 1)), z4.x);
-          const float k1 = fmaf(s4.y, (float)((w >> KB) & ((1u << KB) - 1)), z4.y);
-          const float k2 = fmaf(s4.z, (float)((w >> (2 * KB)) & ((1u << KB) - 1)), z4.z);
-          const float k3 = fmaf(s4.w, (float)((w >> (3 * KB)) & ((1u << KB) - 1)), z4.w);
-#pragma unroll
-          for (int h = 0; h < TQ_MAX_GQA; ++h) {
-            if (h < G) {
-              const float4 q4 = *reinterpret_cast<const float4*>(&sh.q[h][j]);
-              a[h] = fmaf(q4.x, k0, fmaf(q4.y, k1, fmaf(q4.z, k2, fmaf(q4.w, k3, a[h]))));
-            }
-          }
-        }
-      }
-      const int tok = (p0 + pi) * kPage + t;
-      const bool live = pvalid && tok < nc;
-#pragma unroll
-      for (int h = 0; h < TQ_MAX_GQA; ++h) {
-        const float v = a[h] + __shfl_xor_sync(0xffffffffu, a[h], 1);
-        if (hf == 0 && h < G) {
-          const float l = live ? scale * v : -INFINITY;
-          sh.sc[warp * kPage + t][h] = l;
-          if (scores && live) scores[(head0 + h) * (size_t)max_ctx + tok] = l;
-        }
-      }
-    }
-    __syncthreads();
-    // ---------------- online softmax: warp h updates head h over the chunk's 128 tokens
-    if (warp < G) {
-      const int h = warp;
-      float mx = -INFINITY;
-      for (int tt = lane; tt < CT; tt += 32) mx = fmaxf(mx, sh.sc[tt][h]);
-      mx = warp_max_f(mx);
-      const float m_old = sh.m_run[h];
-      const float mnew = fmaxf(m_old, mx);
-      float ls = 0.f, zs = 0.f;
-      for (int tt = lane; tt < CT; tt += 32) {
-        const float l = sh.sc[tt][h];
-        const float p = (l == -INFINITY) ? 0.f : expf(l - mnew);
-        float pv = 0.f;
-        if (p != 0.f) {  // a live token: its page is valid
-          const unsigned char* pp = stbase + (size_t)(tt / kPage) * sub;
-          const float vs = __half2float(reinterpret_cast<const __half*>(pp + P.off_vscale)[tt % kPage]);
-          const float vz = __half2float(reinterpret_cast<const __half*>(pp + P.off_vzero)[tt % kPage]);
-          pv = p * vs;
-          zs = fmaf(p, vz, zs);
-        }
-        sh.ps[tt][h] = pv;
-        ls += p;
-      }
-      ls = warp_sum_f(ls);
-      zs = warp_sum_f(zs);
-      if (lane == 0) {
-        const float al = (mnew == -INFINITY) ? 1.f : expf(m_old - mnew);
-        sh.alpha[h] = al;
-        sh.pz[h] = zs;
-        sh.l_run[h] = sh.l_run[h] * al + ls;
-        if (mnew != -INFINITY) sh.m_run[h] = mnew;
-      }
-    }
-    __syncthreads();
-    // ---------------- values: coordinate vj, tokens of group th
-#pragma unroll
-    for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] = acc[h] * sh.alpha[h] + (th == 0 ? sh.pz[h] : 0.f);
-    {
-      const int word = (vj * VB) / 32, shift = (vj * VB) % 32;
-#pragma unroll 4
-      for (int tt = th * (CT / NTH); tt < (th + 1) * (CT / NTH); ++tt) {
-        const int pw = tt / kPage;
-        if (k * NW + pw >= npg) break;  // past the split's last page: weights are 0
-        const uint32_t* vc = reinterpret_cast<const uint32_t*>(stbase + (size_t)pw * sub + P.off_vcodes);
-        const float c = (float)((vc[(tt % kPage) * VW + word] >> shift) & ((1u << VB) - 1));
-        const float4 w0 = *reinterpret_cast<const float4*>(&sh.ps[tt][0]);
-        const float4 w1 = *reinterpret_cast<const float4*>(&sh.ps[tt][4]);
-        acc[0] = fmaf(w0.x, c, acc[0]);
-        acc[1] = fmaf(w0.y, c, acc[1]);
-        acc[2] = fmaf(w0.z, c, acc[2]);
-        acc[3] = fmaf(w0.w, c, acc[3]);
-        acc[4] = fmaf(w1.x, c, acc[4]);
-        acc[5] = fmaf(w1.y, c, acc[5]);
-        acc[6] = fmaf(w1.z, c, acc[6]);
-        acc[7] = fmaf(w1.w, c, acc[7]);
-      }
-    }
-  }
-  drain_after_timeout(sh.full, timed_out, kstop, nchunks, nst, nst - 1);
-  __syncthreads();
-  // token groups -> one partial per coordinate (the key scale rows are free now)
-  float* red = &sh.ks[0][0];  // [TQ_MAX_GQA][D]
-  for (int r = 1; r < NTH; ++r) {
-    if (th == r) {
-#pragma unroll
-      for (int h = 0; h < TQ_MAX_GQA; ++h) red[h * D + vj] = acc[h];
-    }
-    __syncthreads();
-    if (th == 0) {
-#pragma unroll
-      for (int h = 0; h < TQ_MAX_GQA; ++h) acc[h] += red[h * D + vj];
-    }
-    __syncthreads();
-  }
-  float* ml = reinterpret_cast<float*>(ws + L.ml);
-  float* accw = reinterpret_cast<float*>(ws + L.acc);
-  if (th == 0) {
-#pragma unroll
-    for (int h = 0; h < TQ_MAX_GQA; ++h)
-      if (h < G) accw[((head0 + h) * st + s) * D + vj] = acc[h];
-  }
-  if (tid < G) {
-    ml[((head0 + tid) * st + s) * 2 + 0] = sh.m_run[tid];
-    ml[((head0 + tid) * st + s) * 2 + 1] = sh.l_run[tid];
-  }
-}
-
+#include "tq_kivi_mma.cuh"
 #include "tq_prefill_mma.cuh"
 
 // ------------------------------------------------------------------ launcher
@@ -1527,18 +1256,19 @@ static cudaError_t launch_kivi(const KParams& P, const KCache& C, const void* q,
                                float* scores, unsigned char* ws, const WsLayout& L, int max_ctx, cudaStream_t st) {
   const size_t pid_bytes = (size_t)std::min(L.pages_per_split, kPidCache) * sizeof(long long);
   const size_t stage_bytes = (size_t)kMmaPages * P.sub_bytes;
+  const size_t head_bytes = (size_t)(D / 16) * 32 * sizeof(uint4) + (size_t)TQ_MAX_GQA * D * sizeof(float);
   int nst = kStages;
-  size_t dyn = nst * stage_bytes + pid_bytes;
-  if (dyn > 80 * 1024) {
+  size_t dyn = head_bytes + nst * stage_bytes + pid_bytes;
+  if (dyn > 100 * 1024) {  // two resident CTAs
     nst = 2;
-    dyn = nst * stage_bytes + pid_bytes;
+    dyn = head_bytes + nst * stage_bytes + pid_bytes;
   }
   dyn = std::max(dyn, window_smem_bytes(D));
-  cudaError_t e = cudaFuncSetAttribute(kivi_decode_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(kivi_mma_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dyn);
   if (e != cudaSuccess) return e;
   const dim3 grid(L.n_comp_splits + 1, P.hkv, C.batch);
-  kivi_decode_kernel<D, KB, VB><<<grid, kMmaThreads, dyn, st>>>(P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
+  kivi_mma_kernel<D, KB, VB><<<grid, kMmaThreads, dyn, st>>>(P, C, q, dtype, scale, scores, ws, L, max_ctx, nst);
   return cudaGetLastError();
 }
 
