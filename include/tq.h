@@ -329,7 +329,8 @@ size_t tq_decode_workspace_size(const tq_layer_params* p, int batch, int max_ctx
  *   workspace [device] scratch of tq_decode_workspace_size bytes, 256-byte
  *            aligned; contents need not be initialised
  *   max_ctx  upper bound on every seq_len[b] (sizes the split-K grid)
- * A sequence with seq_len 0 gets out = 0 and lse = -inf.
+ * A sequence with seq_len 0 gets out = 0 and lse = -inf.  batch <= 65535 and
+ * batch * G <= 262140 (TQ_ERR_INVALID_ARG otherwise; the workspace size is then 0).
  */
 tq_status tq_decode_attention(const tq_layer_params* p, const tq_cache* cache, const void* q,
                               tq_dtype dtype, float scale, float* out, float* lse, float* scores,
@@ -385,7 +386,8 @@ tq_status tq_decode_attention_static(const tq_layer_params* p, const tq_cache* c
  *   workspace [device] 256-byte aligned, >= tq_prefill_workspace_size bytes
  *   max_ctx   upper bound of seq_len over the batch
  * seq_len[b] < n_query sets TQ_DEVERR_SEQ_LEN (those queries see the tokens
- * that exist).  batch * n_query <= 2^24.
+ * that exist).  batch * n_query <= 65535 and batch * n_query * G <= 262140
+ * (TQ_ERR_INVALID_ARG otherwise; the workspace size is then 0).
  */
 size_t tq_prefill_workspace_size(const tq_layer_params* p, int batch, int n_query, int max_ctx);
 tq_status tq_prefill_attention(const tq_layer_params* p, const tq_cache* cache, int n_query, const void* q,

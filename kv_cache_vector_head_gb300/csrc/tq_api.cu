@@ -169,6 +169,13 @@ static tq_status cuda_status(cudaError_t e, const char* what) {
   return ok();
 }
 
+// Rows (sequences, or a prefill chunk's queries) one decode launch can take: the page grid
+// and the merge put them on a grid dimension of at most 65535, the query transform their
+// (row, head) vectors in tiles of 4.
+static bool decode_rows_ok(const KParams& K, long long rows) {
+  return rows >= 1 && rows <= 65535 && rows * K.G <= 4LL * 65535;
+}
+
 static tq_status make_cache(const tq_cache* c, const KParams& K, KCache* C, bool need_window) {
   if (!c) return fail(TQ_ERR_INVALID_ARG, "null tq_cache");
   if (!c->page_pool || !aligned(c->page_pool, 16)) return fail(TQ_ERR_INVALID_ARG, "page_pool null or not 16-byte aligned");
@@ -295,6 +302,7 @@ extern "C" tq_status tq_prefill_cache(const tq_layer_params* p, tq_cache* cache,
 extern "C" size_t tq_decode_workspace_size(const tq_layer_params* p, int batch, int max_ctx, int n_splits) {
   KParams K;
   if (make_params(p, &K, false) != TQ_OK || batch < 1 || max_ctx < 0 || n_splits < 0) return 0;
+  if (!decode_rows_ok(K, batch)) return 0;
   clear_error();
   return decode_ws_layout(K, batch, max_ctx, n_splits, num_sms()).total;
 }
@@ -312,6 +320,7 @@ extern "C" tq_status tq_decode_attention(const tq_layer_params* p, const tq_cach
   if (!aligned(workspace, 256)) return fail(TQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (max_ctx < 0 || n_splits < 0) return fail(TQ_ERR_INVALID_ARG, "max_ctx and n_splits must be >= 0");
   if (!(scale == scale)) return fail(TQ_ERR_INVALID_ARG, "scale is NaN");
+  if (!decode_rows_ok(K, cache->batch)) return fail(TQ_ERR_INVALID_ARG, "batch must be <= 65535 and batch * G <= 262140");
   const WsLayout L = decode_ws_layout(K, cache->batch, max_ctx, n_splits, num_sms());
   if (workspace_bytes < L.total) {
     set_error("workspace too small: %zu < %zu", workspace_bytes, L.total);
@@ -325,7 +334,7 @@ extern "C" tq_status tq_decode_attention(const tq_layer_params* p, const tq_cach
 extern "C" size_t tq_prefill_workspace_size(const tq_layer_params* p, int batch, int n_query, int max_ctx) {
   KParams K;
   if (make_params(p, &K, false) != TQ_OK || batch < 1 || n_query < 1 || max_ctx < 0) return 0;
-  if ((long long)batch * n_query > (1LL << 24)) return 0;
+  if (!decode_rows_ok(K, (long long)batch * n_query)) return 0;
   clear_error();
   WsLayout L;
   return prefill_layout(K, batch, n_query, max_ctx, &L);
@@ -340,8 +349,8 @@ extern "C" tq_status tq_prefill_attention(const tq_layer_params* p, const tq_cac
   if (s != TQ_OK) return s;
   if ((s = check_dtype(dtype)) != TQ_OK) return s;
   if ((s = make_cache(cache, K, &C, true)) != TQ_OK) return s;
-  if (n_query < 1 || (long long)cache->batch * n_query > (1LL << 24))
-    return fail(TQ_ERR_INVALID_ARG, "n_query must be >= 1 and batch * n_query <= 2^24");
+  if (n_query < 1 || !decode_rows_ok(K, (long long)cache->batch * n_query))
+    return fail(TQ_ERR_INVALID_ARG, "n_query must be >= 1, batch * n_query <= 65535 and batch * n_query * G <= 262140");
   if (!q || !out || !workspace) return fail(TQ_ERR_INVALID_ARG, "null q / out / workspace");
   if (!aligned(workspace, 256)) return fail(TQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (max_ctx < 0) return fail(TQ_ERR_INVALID_ARG, "max_ctx must be >= 0");
@@ -416,6 +425,7 @@ extern "C" tq_status tq_decode_attention_static(const tq_layer_params* p, const 
   if (s != TQ_OK) return s;
   if (!cache || cache->batch < 1 || max_ctx < 0 || n_splits < 0)
     return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention_static: bad cache, max_ctx or n_splits");
+  if (!decode_rows_ok(K, cache->batch)) return fail(TQ_ERR_INVALID_ARG, "batch must be <= 65535 and batch * G <= 262140");
   const size_t need = decode_ws_layout(K, cache->batch, max_ctx, n_splits, num_sms()).total;
   if (need > (size_t)TQ_STATIC_SCRATCH_BYTES) {
     set_error("tq_decode_attention_static: this configuration needs %zu bytes of scratch, more than the %u-byte "

@@ -200,7 +200,12 @@ def test_prefill_workspace_and_checks(L):
     d = lib.tq_decode_workspace_size(ctypes.byref(p), 15, 100, 0)
     assert w == d + ((3 * 15 * 4 + 255) // 256) * 256
     assert lib.tq_prefill_workspace_size(ctypes.byref(p), 3, 0, 100) == 0
-    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 1 << 13, 1 << 12, 100) == 0  # > 2^24 queries
+    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 1 << 13, 1 << 12, 100) == 0  # > 65535 queries
+    # one decode launch takes at most 65535 rows (grid dimension) and 262140 (row, head) vectors
+    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 5, 13107, 100) > 0  # 65535 rows, G = 4
+    assert lib.tq_prefill_workspace_size(ctypes.byref(p), 2, 32768, 100) == 0
+    assert lib.tq_decode_workspace_size(ctypes.byref(p), 65535, 100, 0) > 0
+    assert lib.tq_decode_workspace_size(ctypes.byref(p), 65536, 100, 0) == 0
     c = L.Cache()
     st = lib.tq_prefill_attention(ctypes.byref(p), ctypes.byref(c), 4, None, 1, ctypes.c_float(1.0), None, None,
                                   None, 0, 100, None)
