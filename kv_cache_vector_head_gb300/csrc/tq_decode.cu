@@ -784,21 +784,22 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
 #pragma unroll
         for (int cbk = 0; cbk < CB; ++cbk) {
           const int c = warp * CPW + g8 * CB + cbk;
-          uint32_t u[TQ_MAX_BITS];
+          // the table index of each of this lane's slots 4 t4 .. 4 t4 + 3 (pages A and B) as a
+          // nibble: slot j of page A at nibble j, of page B at nibble 4 + j, plane p at bit p
+          uint32_t iw = 0;
 #pragma unroll
-          for (int p = 0; p < TQ_MAX_BITS; ++p)
-            u[p] = p < P.vb ? ((uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16)) : 0u;
+          for (int p = 0; p < TQ_MAX_BITS; ++p) {
+            if (p < P.vb) {
+              const uint32_t u = (uint32_t)va[p * D + c] | ((uint32_t)vbp[p * D + c] << 16);
+              const uint32_t x = (u >> (4 * t4)) & 0x000F000Fu;
+              iw |= ((x | (x << 3) | (x << 6) | (x << 9)) & 0x11111111u) << p;
+            }
+          }
 #pragma unroll
           for (int ksx = 0; ksx < 2; ++ksx) {
-            const int i0 = 4 * t4 + ksx, i1 = i0 + 2;  // slots of registers e = 0 and e = 1
-            uint32_t rA0 = 0, rB0 = 0, rA1 = 0, rB1 = 0;
-#pragma unroll
-            for (int p = 0; p < TQ_MAX_BITS; ++p) {
-              rA0 |= ((u[p] >> i0) & 1u) << p;
-              rB0 |= ((u[p] >> (i0 + 16)) & 1u) << p;
-              rA1 |= ((u[p] >> i1) & 1u) << p;
-              rB1 |= ((u[p] >> (i1 + 16)) & 1u) << p;
-            }
+            // slots 4 t4 + ksx (register e = 0) and 4 t4 + 2 + ksx (e = 1)
+            const uint32_t rA0 = (iw >> (4 * ksx)) & 15u, rB0 = (iw >> (16 + 4 * ksx)) & 15u;
+            const uint32_t rA1 = (iw >> (8 + 4 * ksx)) & 15u, rB1 = (iw >> (24 + 4 * ksx)) & 15u;
             const uint32_t eA0 = sh.vlut[rA0], eB0 = sh.vlut[rB0], eA1 = sh.vlut[rA1], eB1 = sh.vlut[rB1];
             const uint4 wfk = ksx ? wf1 : wf0;
             // hi halves -> plane 0, lo halves -> plane 1; pair = (token of page A, token of page B)
