@@ -558,7 +558,9 @@ struct MmaShared {
 };
 
 // KMIX: the layer uses mixed-channel keys or byte key norms (compiled out otherwise).
-// KPF > 0: TurboQuant_prod keys (QJL sketch) with KPF Walsh planes, fixed at compile time
+// KPF > 0: TurboQuant_prod keys (QJL sketch) with KPF Walsh planes, fixed at compile time;
+// with KMIX, KPF = 8: mixed-channel keys of 3 + 1 bits (eight planes for the wider half, the
+// key correction read at run time)
 // (kp = 2 for 2-bit codes, 4 for 3-bit), values of 2 bits or more (2-bit planes when !VLUT);
 // KPF = 0 reads the plane count, correction and value bits at run time.
 template <int D, bool VLUT, bool KMIX, int KPF>
@@ -591,11 +593,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
   const uint32_t xb1 = P.xb1, xb2 = P.xb2;
   const bool ksplit = KMIX && P.ksplit, knu8 = KMIX && P.knu8;
   const int kp = KPF > 0 ? KPF : P.kp;
-  const int kqjl = KPF > 0 ? (int)TQ_KEY_QJL : P.kqjl;
+  const int kqjl = (KPF > 0 && !KMIX) ? (int)TQ_KEY_QJL : P.kqjl;
   const int kbits = KPF > 0 ? (KPF == 2 ? 2 : 3) : P.kb;
-  constexpr int kUnrollS = KPF > 0 ? KPF : 1;
+  constexpr int kUnrollS = (KPF > 0 && !KMIX) ? KPF : (KMIX && KPF > 0 ? 2 : 1);
   auto pbase = [&](int S) { return ksplit ? frag_plane_base(P, S, KS) : S * KS; };
-  const bool vb2 = (KPF > 0 && !VLUT) ? true : P.vb == 2;  // the specialised variants carry 2-bit planes
+  const bool vb2 = (KPF > 0 && !KMIX && !VLUT) ? true : P.vb == 2;  // the QJL variants carry 2-bit planes
 
   // shared memory: query fragments | page stages | page ids of this split
   uint4* afr = reinterpret_cast<uint4*>(dyn);                                  // [planes][KS][32]
@@ -904,6 +906,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(D)) decode_mma_ke
                                              : (m + 1 == kbits) ? kx[tk * (E / 2) + w] : 0u) >> sh;
             }
           }
+#pragma unroll kUnrollS
           for (int S = kp / 2; S < kp; ++S) {
             uint32_t w0[2], w6[2], w10[2];
 #pragma unroll
@@ -1307,13 +1310,17 @@ static cudaError_t launch_decode_d(const KParams& P, const KCache& C, const void
   const bool kmix = P.ksplit || P.knu8;
   // TurboQuant_prod keys with 2 or 3 code bits: plane count and sketch fixed at compile time
   const int kpf = (!kmix && P.kqjl == TQ_KEY_QJL && (P.kp == 2 || P.kp == 4) && P.vb >= 2) ? P.kp : 0;
+  // mixed-channel keys of 3 + 1 bits: eight Walsh planes fixed at compile time
+  const bool kmix8 = kmix && P.ksplit && P.kp == 8 && P.kb == 3;
   if (P.vb >= 3)
-    e = kmix       ? launch_mma<D, true, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+    e = kmix8      ? launch_mma<D, true, true, 8>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kmix     ? launch_mma<D, true, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
         : kpf == 2 ? launch_mma<D, true, false, 2>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
         : kpf == 4 ? launch_mma<D, true, false, 4>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
                    : launch_mma<D, true, false, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
   else
-    e = kmix       ? launch_mma<D, false, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+    e = kmix8      ? launch_mma<D, false, true, 8>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
+        : kmix     ? launch_mma<D, false, true, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
         : kpf == 2 ? launch_mma<D, false, false, 2>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
         : kpf == 4 ? launch_mma<D, false, false, 4>(P, C, q, dtype, scale, scores, w, L, max_ctx, st)
                    : launch_mma<D, false, false, 0>(P, C, q, dtype, scale, scores, w, L, max_ctx, st);
