@@ -13,9 +13,9 @@
 //   * keys with the Gaussian sketch: S is staged once per CTA in shared memory as f16 in
 //     mma.m16n8k16 B-fragment order (128 KB, with its row norms), the residuals of the
 //     tile as f16 hi / lo limbs in A-fragment order; S r runs on the tensor cores with
-//     the hi limb (warp w: rows 16 w .. 16 w + 15 for all 64 tokens).  An entry whose
-//     magnitude lies within a certified bound of the f16 rounding and accumulation error
-//     (2^-10 (1 + 2^-5) ||r|| ||S_j|| + 2^-20 (||r|| + ||S_j||)) is recomputed in fp32 by
+//     both limbs of r against S's hi limb (warp w: rows 16 w .. 16 w + 15 for all 64
+//     tokens).  An entry whose magnitude lies within a certified bound of the f16 rounding
+//     and accumulation error (1.16 * 2^-11 ||r|| ||S_j|| + 2^-20 (||r|| + ||S_j||)) is recomputed in fp32 by
 //     the warp (r from its two limbs, S_j from global memory), so every sign is that of
 //     the fp32 product, as in quantize_tile.  The structured sketch takes the signs of a
 //     warp transform of sigma_S * r instead;
@@ -313,7 +313,10 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
           for (int q = 0; q < NTW; ++q)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[m][q][c] = 0.f;
+        // both limbs of r against S's hi limb: the products are exact, so the error left is S's
+        // own rounding (2^-11 relative), the 32 chained fp32 accumulations and subnormal limbs
         const uint4* A4 = reinterpret_cast<const uint4*>(sAh);
+        const uint4* A4l = reinterpret_cast<const uint4*>(sAl);
 #pragma unroll 2
         for (int ks = 0; ks < KS; ++ks) {
           uint2 b[NTW];
@@ -322,8 +325,12 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
             const uint4 a = A4[(m * KS + ks) * 32 + lane];
+            const uint4 al = A4l[(m * KS + ks) * 32 + lane];
 #pragma unroll
-            for (int q = 0; q < NTW; ++q) mma_f16(acc[m][q], a, b[q]);
+            for (int q = 0; q < NTW; ++q) {
+              mma_f16(acc[m][q], a, b[q]);
+              mma_f16(acc[m][q], al, b[q]);
+            }
           }
         }
         // signs; entries within the certified bound are recomputed in fp32 by the whole warp
@@ -337,7 +344,9 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
               const int v = 16 * m + g8 + 8 * (c >> 1);
               const int j = 8 * (NTW * warp + q) + 2 * t4 + (c & 1);
               const float rnv = tl.rn[v], snj = sN[j];
-              const float bound = 1.0322265625f * 0x1p-10f * rnv * snj + 0x1p-20f * (rnv + snj);
+              // 2^-11 (S's hi limb) + 32 * 17 * 2^-23 (chained accumulation, each step truncating
+              // every addend by an ulp) < 1.16 * 2^-11, relative to ||r|| ||S_j||
+              const float bound = 1.16f * 0x1p-11f * rnv * snj + 0x1p-20f * (rnv + snj);
               const int bit = (m * NTW + q) * 4 + c;
               if (acc[m][q][c] >= 0.f) sbits |= 1u << bit;
               if (fabsf(acc[m][q][c]) <= bound) unc |= 1u << bit;
