@@ -201,7 +201,16 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
     }
     __syncthreads();  // the row copies are read: the word buffer is free
 
-    // ---- vector phase: warp w, tokens VPW w .. VPW w + VPW - 1
+    // ---- vector phase: warp w, tokens VPW w .. VPW w + VPW - 1; bf16 inputs of the next
+    // vector are loaded while the current one is quantized
+    unsigned short xn[E];
+    auto load_raw = [&](int i) {
+      const bool ok = tl.page[VPW * warp + i] >= 0;
+      const unsigned short* xp = reinterpret_cast<const unsigned short*>(x) + (rows[i] * P.hkv + head) * P.dh;
+#pragma unroll
+      for (int e = 0; e < E; ++e) xn[e] = (ok && e * 32 + lane < P.dh) ? xp[e * 32 + lane] : (unsigned short)0;
+    };
+    if (dtype == TQ_BF16) load_raw(0);
 #pragma unroll 1
     for (int i = 0; i < VPW; ++i) {
       const int v = VPW * warp + i;
@@ -212,9 +221,9 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
         const long long base = (rows[i] * P.hkv + head) * P.dh;
         const bool ok = pg >= 0;
         if (dtype == TQ_BF16) {
-          const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(x) + base;
 #pragma unroll
-          for (int e = 0; e < E; ++e) xv[e] = (ok && e * 32 + lane < P.dh) ? __bfloat162float(xp[e * 32 + lane]) : 0.f;
+          for (int e = 0; e < E; ++e) xv[e] = __uint_as_float((uint32_t)xn[e] << 16);  // bf16 -> fp32, exact
+          if (i + 1 < VPW) load_raw(i + 1);
         } else {
 #pragma unroll
           for (int e = 0; e < E; ++e)
