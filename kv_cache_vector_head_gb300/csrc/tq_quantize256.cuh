@@ -360,12 +360,14 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
               if (acc[m][q][c] >= 0.f) sbits |= 1u << bit;
               if (fabsf(acc[m][q][c]) <= bound) unc |= 1u << bit;
             }
-#pragma unroll 1
-        for (int bit = 0; bit < MT * NTW * 4; ++bit) {
-          unsigned todo = __ballot_sync(0xffffffffu, (unc >> bit) & 1u);
-          while (todo) {
-            const int l = __ffs(todo) - 1;
-            todo &= todo - 1;
+        // one pass per uncertain entry (lane l's lowest pending bit), none where the warp has none
+        while (true) {
+          const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
+          if (who == 0u) break;
+          const int l = __ffs(who) - 1;
+          const int bit = __shfl_sync(0xffffffffu, __ffs(unc) - 1, l);
+          if (lane == l) unc &= unc - 1u;
+          {
             const int c = bit & 3, q = (bit >> 2) % NTW, m = bit / (4 * NTW);
             const int v = 16 * m + (l >> 2) + 8 * (c >> 1);
             const int j = 8 * (NTW * warp + q) + 2 * (l & 3) + (c & 1);
