@@ -360,28 +360,43 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
               if (acc[m][q][c] >= 0.f) sbits |= 1u << bit;
               if (fabsf(acc[m][q][c]) <= bound) unc |= 1u << bit;
             }
-        // one pass per uncertain entry (lane l's lowest pending bit), none where the warp has none
+        // the uncertain entries two at a time (lane l's lowest pending bit; both rows of S are
+        // loaded before either dot product is reduced), no pass where the warp has none
         while (true) {
-          const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
-          if (who == 0u) break;
-          const int l = __ffs(who) - 1;
-          const int bit = __shfl_sync(0xffffffffu, __ffs(unc) - 1, l);
-          if (lane == l) unc &= unc - 1u;
-          {
-            const int c = bit & 3, q = (bit >> 2) % NTW, m = bit / (4 * NTW);
-            const int v = 16 * m + (l >> 2) + 8 * (c >> 1);
-            const int j = 8 * (NTW * warp + q) + 2 * (l & 3) + (c & 1);
-            float prod[E];
+          int l[2], bit[2];
+          bool have[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const unsigned who = __ballot_sync(0xffffffffu, unc != 0u);
+            have[u] = who != 0u;
+            l[u] = have[u] ? __ffs(who) - 1 : 0;
+            bit[u] = __shfl_sync(0xffffffffu, __ffs(unc) - 1, l[u]);
+            if (have[u] && lane == l[u]) unc &= unc - 1u;
+          }
+          if (!have[0]) break;
+          float prod[2][E];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int b = have[u] ? bit[u] : bit[0], ll = have[u] ? l[u] : l[0];
+            const int c = b & 3, q = (b >> 2) % NTW, m = b / (4 * NTW);
+            const int v = 16 * m + (ll >> 2) + 8 * (c >> 1);
+            const int j = 8 * (NTW * warp + q) + 2 * (ll & 3) + (c & 1);
             const int ab = a_base(v >> 4, v & 15, lane);
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               const int ai = ab + 512 * e;
               const float rv = __half2float(__ushort_as_half(sAh[ai])) + __half2float(__ushort_as_half(sAl[ai]));
-              prod[e] = rv * __ldg(Sg + (size_t)j * D + e * 32 + lane);
+              prod[u][e] = rv * __ldg(Sg + (size_t)j * D + e * 32 + lane);
             }
-            const float dot = warp_sum_f(tree8(prod));
-            if (lane == l) sbits = (sbits & ~(1u << bit)) | ((dot >= 0.f ? 1u : 0u) << bit);
           }
+          float dot[2] = {tree8(prod[0]), tree8(prod[1])};
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], o);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (have[u] && lane == l[u]) sbits = (sbits & ~(1u << bit[u])) | ((dot[u] >= 0.f ? 1u : 0u) << bit[u]);
         }
         // sign words: token v, rows 16 w .. 16 w + 15 are bits 16 (w & 1) .. of word w / 2
 #pragma unroll
