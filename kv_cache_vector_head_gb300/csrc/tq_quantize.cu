@@ -154,7 +154,8 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
   float acc[kTile];
 #pragma unroll
   for (int v = 0; v < kTile; ++v) acc[v] = 0.f;
-#pragma unroll 2
+  // eight rows of S in flight: a decode-step append (one vector) waits on these loads alone
+#pragma unroll 8
   for (int i4 = 0; i4 < D / 4; ++i4) {
     const float4 p = __ldg(row + i4);
 #pragma unroll
