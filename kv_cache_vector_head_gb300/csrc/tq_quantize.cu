@@ -44,8 +44,8 @@ namespace tq {
 // Quantize the tile held in s.x (nv vectors, rows >= nv are ignored).
 // is_key selects the key codebook/transform and the QJL stage.
 // slot_of[v] (when non-null) gives the page slot of vector v for the
-// coordinate-major value masks.
-template <int D>
+// coordinate-major value masks.  ONE: nv is 1 (a decode-step append), which takes its own sketch loop.
+template <int D, bool ONE = false>
 __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head, bool is_key,
                               const int* slot_of) {
   constexpr int E = D / 32;
@@ -59,8 +59,39 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
     s.cb_hi[tid] = P.kc_hi[tid];
     s.tb_hi[tid] = P.kt_hi[tid];
   }
-  // 1. norms (double accumulation)
-  for (int v = warp; v < nv; v += D / 32) {
+  // 1. norms (double accumulation; one vector: float, pairwise, relative error below 13 ulp on the sum)
+  if constexpr (ONE) {
+    if (warp == 0) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc = fmaf(s.x[0][e * 32 + lane], s.x[0][e * 32 + lane], acc);
+      acc = warp_sum_f(acc);  // the same in every lane
+      if (acc >= 1e-30f && acc <= 1e37f) {
+        if (lane == 0) {
+          const float n = sqrtf(acc);
+          const bool zero = n < kZeroNorm;
+          s.zero[0] = zero;
+          s.norm[0] = zero ? 0.f : n;
+          s.inv[0] = zero ? 0.f : (P.kind == TQ_FWHT ? 1.f / n : sqrt_d / n);
+        }
+      } else {  // squares near the float range's ends (or a non-finite input): the double sum
+        double dacc = 0.0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const double xv = s.x[0][e * 32 + lane];
+          dacc += xv * xv;
+        }
+        dacc = warp_sum_d(dacc);
+        if (lane == 0) {
+          const double n = sqrt(dacc);
+          const bool zero = n < (double)kZeroNorm;
+          s.zero[0] = zero;
+          s.norm[0] = zero ? 0.f : (float)n;
+          s.inv[0] = zero ? 0.f : (P.kind == TQ_FWHT ? (float)(1.0 / n) : (float)((double)sqrt_d / n));
+        }
+      }
+    }
+  } else for (int v = warp; v < nv; v += D / 32) {
     double acc = 0.0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -114,7 +145,21 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
   if (!is_key) return;
   // 4. residual norm gamma = ||z - C|| / sqrt(d), or the key scale s from the sum of the r entries
   const bool scaled = P.kqjl == TQ_KEY_EDEN || P.kqjl == TQ_KEY_RENORM;
-  for (int v = warp; v < nv; v += D / 32) {
+  if constexpr (ONE) {
+    if (warp == 0) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float rv = s.r[0][e * 32 + lane];
+        acc = scaled ? acc + rv : fmaf(rv, rv, acc);
+      }
+      acc = warp_sum_f(acc);
+      if (lane == 0) {
+        const float g = scaled ? (float)D / acc : sqrtf(acc) / sqrt_d;
+        s.gam[0] = s.zero[0] ? 0.f : g;
+      }
+    }
+  } else for (int v = warp; v < nv; v += D / 32) {
     double acc = 0.0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -150,6 +195,46 @@ __device__ void quantize_tile(const KParams& P, TileSmem<D>& s, int nv, int head
     return;
   }
   // 5. QJL signs of S r (r in z units; the sign is scale free)
+  if constexpr (ONE) {
+    // one vector: warp w takes rows 32 w .. 32 w + 31 of S, its lanes along a row (coalesced loads,
+    // a warp sum a row) instead of a thread a row, sixteen rows of loads in flight
+    const float* S0 = P.qjl_s + (size_t)head * D * D;
+    constexpr int kRows = 16, kH = D / 128;  // rows of S a batch, float4 loads a lane and row
+    unsigned mine = 0u;
+#pragma unroll 1
+    for (int r0 = 0; r0 < 32; r0 += kRows) {
+      float4 p[kRows][kH];
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const float4* srow = reinterpret_cast<const float4*>(S0 + (size_t)(32 * warp + r0 + rr) * D);
+#pragma unroll
+        for (int h = 0; h < kH; ++h) p[rr][h] = __ldg(srow + lane + 32 * h);
+      }
+      float a[kRows];
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        a[rr] = 0.f;
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+          const float4 rv = *reinterpret_cast<const float4*>(&s.r[0][(lane + 32 * h) * 4]);
+          const float4 q = p[rr][h];
+          a[rr] = fmaf(q.x, rv.x, fmaf(q.y, rv.y, fmaf(q.z, rv.z, fmaf(q.w, rv.w, a[rr]))));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) a[rr] += __shfl_xor_sync(0xffffffffu, a[rr], o);
+      }
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr)
+        if (lane == r0 + rr && (s.zero[0] || a[rr] >= 0.f)) mine = 1u;
+    }
+    const unsigned w = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) s.signs[0][warp] = w;
+    __syncthreads();
+    return;
+  }
   const float4* row = reinterpret_cast<const float4*>(P.qjl_s + (size_t)head * D * D + (size_t)j * D);
   float acc[kTile];
 #pragma unroll
@@ -505,10 +590,21 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
   const int b = blockIdx.x, head = blockIdx.y;
   const bool is_key = blockIdx.z == 0;
   const void* x = is_key ? k : v;
-  const int T = C.seq_len[b];
-  const int nc = C.n_compressed[b];
   const long long src = ((long long)b * P.hkv + head) * P.dh;
   const bool in_head = threadIdx.x < P.dh;  // coordinates >= dh are the zero padding
+  // no window: every step quantizes its vector, so its load and (keys) the head's sketch rows toward
+  // L2 are issued before the counters and the page lookup they would otherwise wait behind
+  float x0 = 0.f;
+  if (P.window == 0 && !P.kivi) {
+    if (in_head) x0 = load_elem(x, dtype, src + threadIdx.x);
+    if (is_key && P.kqjl == TQ_KEY_QJL && !P.qjl_srht) {
+      const char* S0 = reinterpret_cast<const char*>(P.qjl_s + (size_t)head * D * D);
+      for (int off = threadIdx.x * 128; off < D * D * (int)sizeof(float); off += D * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(S0 + off));
+    }
+  }
+  const int T = C.seq_len[b];
+  const int nc = C.n_compressed[b];
   if (P.window > 0) {
     __half* ring = (is_key ? C.win_k : C.win_v) + (((size_t)b * P.hkv + head) * C.ring) * D;
     if (T - nc < 0 || T - nc >= P.window + kPage) {
@@ -554,10 +650,10 @@ __global__ void __launch_bounds__(D) append_step_kernel(const __grid_constant__ 
         atomicOr(&g_quant_err, (T >= 0 && pidx < C.max_pages) ? TQ_DEVERR_PAGE_INDEX : TQ_DEVERR_SEQ_LEN);
       return;
     }
-    s.x[0][threadIdx.x] = in_head ? load_elem(x, dtype, src + threadIdx.x) : 0.f;
+    s.x[0][threadIdx.x] = x0;
     if (threadIdx.x == 0) slot_of[0] = slot;
     __syncthreads();
-    quantize_tile<D>(P, s, 1, head, is_key, slot_of);
+    quantize_tile<D, true>(P, s, 1, head, is_key, slot_of);
     unsigned char* sb = subblock(P, C, page, head);
     if (is_key) {
       store_key_slot<D>(P, s, sb, 0, slot);
