@@ -326,6 +326,59 @@ def test_paged_append_and_decode_parity(tq, name, over, T0, steps):
         assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
 
 
+@pytest.mark.parametrize("name", ["long", "tiny"])
+def test_step_append_extreme_norms(tq, name):
+    """Decode-step appends without a window (one vector a CTA) at norms far from 1: a float sum of squares
+    outside [1e-30, 1e37] (scales 1e-21, 1e20) takes the double sum, one inside it (1e17, 1e-6) the float
+    sum; zero and sub-threshold vectors give zero records, compared exactly.  Records only: the logits of a
+    1e20-scale key overflow float32."""
+    scales = [1.0, 1e-21, 1e20, 1e17, 1e-6, 0.0, None]
+    w = SK.workload(name, batch=len(scales), window=0)
+    T0, T = 16, 20
+    kv = SK.keys_values(w, ctx=T)
+    K, V = kv["K"].copy(), kv["V"].copy()
+    for b, sc in enumerate(scales):
+        for X in (K, V):
+            if sc is None:  # one coordinate, norm 5e-8: below the zero-norm guard
+                X[b, T0:] = 0.0
+                X[b, T0:, :, 5] = 5e-8
+            else:
+                X[b, T0:] *= sc
+    kt = SK.to_torch(K, w.dtype).cuda()
+    vt = SK.to_torch(V, w.dtype).cuda()
+    K = kt.double().cpu().numpy()  # both sides see the stored dtype's values
+    V = vt.double().cpu().numpy()
+    L, O = _layer(tq, w)
+    pc = tq.PagedCache(L, w.batch, T)
+    pc.prefill(kt[:, :T0], vt[:, :T0])
+    for t in range(T0, T):
+        pc.append(kt[:, t].contiguous(), vt[:, t].contiguous())
+    torch.cuda.synchronize()
+    assert tq.check_device_error() == 0
+    assert pc.n_compressed.cpu().tolist() == [T] * w.batch
+    pool = pc.pool.cpu().numpy()
+    bt = pc.block_table.cpu().numpy()
+    npg = (T + 15) // 16
+    stats = {}
+    for b, sc in enumerate(scales):
+        zero = sc is None or sc < 1e-20
+        for h in range(w.n_kv_heads):
+            pages = [PY.read_pool(pool, O, int(bt[b, p]), h) for p in range(npg)]
+            cat = {k: np.concatenate([pg[k] for pg in pages])[:T] for k in pages[0]}
+            for lo, hi in ((0, T0), (T0, T)):
+                g = {k: v[lo:hi] for k, v in cat.items()}
+                exact = zero and lo == T0
+                PY.compare_records(O.keys(K[b, lo:hi, h], h), g["kidx"], g["knorm"], g.get("ksigns"),
+                                   g.get("krnorm"), True, None if exact else stats, exact=exact)
+                PY.compare_records(O.values(V[b, lo:hi, h], h), g["vidx"], g["vnorm"], is_key=False,
+                                   stats=None if exact else stats, exact=exact)
+                if exact:
+                    assert not g["knorm"].any() and not g["vnorm"].any()
+                if sc is not None and sc > 1e10 and lo == T0:
+                    assert np.isfinite(g["knorm"]).all() and g["knorm"].min() > 1e15
+    assert stats["exempt"] <= max(3, PY.EXEMPT_FRACTION * stats["codes"])
+
+
 def test_decode_split_invariance_and_determinism(tq):
     w = SK.workload("qwen", batch=2, window=16)
     kv, L, O, pc = _paged_roundtrip(tq, w, 300, 5)
