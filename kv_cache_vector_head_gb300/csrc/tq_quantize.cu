@@ -986,6 +986,25 @@ static cudaError_t launch_direct256_role(const KParams& P, const KCache& C, cons
   return cudaGetLastError();
 }
 
+static cudaError_t launch_direct256_values(const KParams& P, const KCache& C, const void* v, int dtype, long long n_tok,
+                                           const long long* slots, int seq_tok, int n_c, cudaStream_t st) {
+  const int J = code_lut_scale(P.vt, P.vb);
+  const size_t sm = wq::lut_bytes(J, true);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q256::direct256_values_kernel, 32 * q256::VNW, sm)) !=
+      cudaSuccess)
+    return e;
+  const long long groups = slots ? (n_tok + 15) / 16 : (n_c > 0 ? n_tok / n_c : 0) * ((n_c + kPage - 1) / kPage);
+  const long long ctas = (groups + q256::VNW - 1) / q256::VNW;
+  const long long gx = std::min<long long>(std::max(1, std::max(1, per_sm) * sms / std::max(1, P.hkv)), ctas);
+  q256::direct256_values_kernel<<<dim3((unsigned)std::max<long long>(gx, 1), P.hkv), 32 * q256::VNW, sm, st>>>(
+      P, C, v, dtype, n_tok, slots, seq_tok, n_c, J);
+  return cudaGetLastError();
+}
+
 static cudaError_t launch_direct256(const KParams& P, const KCache& C, const void* k, const void* v, int dtype,
                                     long long n_tok, const long long* slots, int seq_tok, int n_c, cudaStream_t st) {
   cudaError_t e;
@@ -995,7 +1014,7 @@ static cudaError_t launch_direct256(const KParams& P, const KCache& C, const voi
   else
     e = launch_direct256_role<true, 0>(P, C, k, dtype, n_tok, slots, seq_tok, n_c, st);
   if (e != cudaSuccess) return e;
-  return launch_direct256_role<false, 0>(P, C, v, dtype, n_tok, slots, seq_tok, n_c, st);
+  return launch_direct256_values(P, C, v, dtype, n_tok, slots, seq_tok, n_c, st);
 }
 
 template <int D>

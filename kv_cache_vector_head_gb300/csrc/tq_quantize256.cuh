@@ -19,8 +19,10 @@
 //     the warp (r from its two limbs, S_j from global memory), so every sign is that of
 //     the fp32 product, as in quantize_tile.  The structured sketch takes the signs of a
 //     warp transform of sigma_S * r instead;
-//   * values: the code-plane bits of the tile are staged in shared memory and written as
-//     whole 16-slot words where the tile fills a page (prefill), bitwise atomics elsewhere.
+//   * values (direct256_values_kernel): one warp owns a page group of 16 tokens with lane l
+//     holding coordinates 8 l .. 8 l + 7, the coordinate-major 16-slot plane words built in
+//     registers and written whole where the group fills a page (prefill), bitwise atomics
+//     elsewhere.
 // Layers outside this kernel's scope (dense rotation, mixed-channel keys, byte norms, the
 // KIVI arm) take append_direct_kernel.
 
@@ -37,12 +39,11 @@ constexpr int NTL = D / 8;            // n-tiles (rows of S)
 constexpr int NTW = NTL / NW;         // n-tiles per warp (2)
 
 struct Tile {
-  uint32_t words[TILE][TQ_MAX_BITS][E];  // value code planes of the tile (page assembly)
+  long long row[TILE];                   // input row of each token
   uint32_t sw[TILE][E];                  // sign words
   float rn[TILE];                        // ||r|| of each token, z units (certification bound)
   long long page[TILE];
   int slot[TILE];
-  int full[MT];                          // value stores: group g fills page page[16 g] in slot order
 };
 constexpr size_t kSBBytes = (size_t)NTL * KS * 32 * sizeof(uint2);        // S, f16 B fragments
 constexpr size_t kSABytes = (size_t)MT * KS * 32 * 4 * sizeof(uint32_t);   // one residual limb
@@ -93,7 +94,7 @@ __device__ __forceinline__ void wht256(float (&v)[E], int lane) {
       }
 }
 
-// KEY: keys (else values).  SK: 0 no sketch (values, MSE-only / scaled keys), 1 Gaussian S on
+// Keys (KEY is true; values take direct256_values_kernel).  SK: 0 no sketch (MSE-only / scaled keys), 1 Gaussian S on
 // the tensor cores, 2 structured S = H diag(sigma_S).  Direct slots as in append_direct_kernel:
 // slot_mapping[t] for input token t, or (slot_mapping == NULL) position p of sequence b at
 // input row b seq_tok + p, page block_table[b][p / 16], slot p % 16, for t = b n_c + p.
@@ -110,13 +111,14 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
   uint16_t* sAl = reinterpret_cast<uint16_t*>(smem_raw + sizeof(Tile) + kSBBytes + D * sizeof(float) + kSABytes);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, t4 = lane & 3;
   const int head = blockIdx.y;
-  const int bits = KEY ? P.kb : P.vb;
+  static_assert(KEY, "values take direct256_values_kernel");
+  const int bits = P.kb;
   const int half = 1 << (bits - 1);
-  const float* ctab = KEY ? P.kc : P.vc;
-  const float* ttab = KEY ? P.kt : P.vt;
-  const float* sigma = (KEY ? P.k_rot : P.v_rot) + (size_t)head * D;
+  const float* ctab = P.kc;
+  const float* ttab = P.kt;
+  const float* sigma = P.k_rot + (size_t)head * D;
   const float* Sg = P.qjl_s + (size_t)head * (SK == 1 ? D * D : D);
-  const int corr = KEY ? P.kqjl : 0;  // TQ_KEY_*: the scale modes keep s in gamma's slot
+  const int corr = P.kqjl;  // TQ_KEY_*: the scale modes keep s in gamma's slot
 
   if constexpr (SK == 1) {
     // S of this head: f16 in B-fragment order (n-tile nt = rows 8 nt .., k-step ks), and row norms
@@ -187,19 +189,13 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
       }
       tl.page[tid] = pg;
       tl.slot[tid] = pg >= 0 ? sl : -1;
-      reinterpret_cast<long long*>(tl.words)[tid] = row;  // rows parked in the (not yet used) word buffer
+      tl.row[tid] = row;
     }
     for (int i = tid; i < TILE * E; i += NT) (&tl.sw[0][0])[i] = 0u;
     __syncthreads();
     long long rows[VPW];
 #pragma unroll
-    for (int i = 0; i < VPW; ++i) rows[i] = reinterpret_cast<const long long*>(tl.words)[VPW * warp + i];
-    if (tid < MT) {  // a 16-token group that fills one page in slot order: whole value words
-      int f = tl.page[16 * tid] >= 0;
-      for (int i = 0; i < 16 && f; ++i) f = tl.page[16 * tid + i] == tl.page[16 * tid] && tl.slot[16 * tid + i] == i;
-      tl.full[tid] = f;
-    }
-    __syncthreads();  // the row copies are read: the word buffer is free
+    for (int i = 0; i < VPW; ++i) rows[i] = tl.row[VPW * warp + i];
 
     // ---- vector phase: warp w, tokens VPW w .. VPW w + VPW - 1; bf16 inputs of the next
     // vector are loaded while the current one is quantized
@@ -257,16 +253,8 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
       for (int e = 0; e < E; ++e) {
         for (int p = 0; p < bits; ++p) {
           const uint32_t wv = __ballot_sync(0xffffffffu, (q[e] >> (8 * p)) & 1u);
-          if (KEY) {
-            if (lane == e && sb) reinterpret_cast<uint32_t*>(sb + P.off_kcodes)[(p * kPage + sl) * E + e] = wv;
-          } else if (lane == e) {
-            tl.words[v][p][e] = wv;
-          }
+          if (lane == e && sb) reinterpret_cast<uint32_t*>(sb + P.off_kcodes)[(p * kPage + sl) * E + e] = wv;
         }
-      }
-      if (!KEY) {
-        if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_vnorm)[sl] = zero ? 0.f : n;
-        continue;
       }
       if (lane == 0 && sb) reinterpret_cast<float*>(sb + P.off_knorm)[sl] = zero ? 0.f : n;
       if (corr == TQ_KEY_EDEN || corr == TQ_KEY_RENORM) {
@@ -418,47 +406,221 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
       }
       __syncthreads();
     }
-    if constexpr (KEY) {
-      if (corr == TQ_KEY_QJL && SK != 0) {
-        for (int i = tid; i < TILE * E; i += NT) {
-          const int v = i / E, e = i % E;
-          if (tl.page[v] >= 0)
-            reinterpret_cast<uint32_t*>(C.pool + ((size_t)tl.page[v] * P.hkv + head) * (size_t)P.sub_bytes +
-                                        P.off_ksigns)[tl.slot[v] * E + e] = tl.sw[v][e];
-        }
-      }
-    } else {
-      // value planes: coordinate j, plane p of each 16-token group
-      for (int i = tid; i < MT * D; i += NT) {
-        const int grp = i / D, j = i % D;
-        const int v0 = 16 * grp;
-        for (int p = 0; p < bits; ++p) {
-          if (tl.full[grp]) {
-            uint32_t w16 = 0;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w16 |= ((tl.words[v0 + t][p][j >> 5] >> (j & 31)) & 1u) << t;
-            uint16_t* vc16 = reinterpret_cast<uint16_t*>(C.pool + ((size_t)tl.page[v0] * P.hkv + head) *
-                                                                       (size_t)P.sub_bytes + P.off_vcodes);
-            vc16[p * D + j] = (uint16_t)w16;
-          } else {
-            for (int t = 0; t < 16; ++t) {
-              const int v = v0 + t;
-              if (tl.page[v] < 0) continue;
-              const unsigned bit = (tl.words[v][p][j >> 5] >> (j & 31)) & 1u;
-              uint16_t* vc16 = reinterpret_cast<uint16_t*>(C.pool + ((size_t)tl.page[v] * P.hkv + head) *
-                                                                         (size_t)P.sub_bytes + P.off_vcodes);
-              unsigned int* w32 = reinterpret_cast<unsigned int*>(vc16 + p * D + (j & ~1));
-              const int sh = (j & 1) * 16 + tl.slot[v];
-              atomicAnd(w32, ~(1u << sh));
-              atomicOr(w32, bit << sh);
-            }
-          }
-        }
+    if (corr == TQ_KEY_QJL && SK != 0) {
+      for (int i = tid; i < TILE * E; i += NT) {
+        const int v = i / E, e = i % E;
+        if (tl.page[v] >= 0)
+          reinterpret_cast<uint32_t*>(C.pool + ((size_t)tl.page[v] * P.hkv + head) * (size_t)P.sub_bytes +
+                                      P.off_ksigns)[tl.slot[v] * E + e] = tl.sw[v][e];
       }
     }
     __syncthreads();
   }
   (void)half;
+}
+
+// ------------------------------------------------------------------ values, a page group per warp
+
+// Values at d = 256 (FWHT kind): one warp owns a group of 16 tokens, a page's worth.  Lane l holds
+// coordinates 8 l .. 8 l + 7 (a bf16 row is one 16-byte load a lane), so the Walsh-Hadamard
+// transform takes the three low index levels in registers and the five high ones across lanes,
+// and the group's coordinate-major 16-slot plane words build up in the lane's registers: byte p
+// of accA[e] / accB[e] holds plane p of coordinate 8 l + e for tokens 0..7 / 8..15.  A group that
+// fills one page in slot order leaves as one 16-byte store a lane and plane (and the 16 norms in
+// one store); any other group writes each token's bits with bitwise atomics.  Groups: page pp of
+// sequence b (slot_mapping == NULL: position p of sequence b at input row b seq_tok + p, page
+// block_table[b][p / 16], slot p % 16), or 16 consecutive input tokens (slot_mapping[t]).
+constexpr int VNW = 8;  // warps a CTA
+__global__ void __launch_bounds__(32 * VNW) direct256_values_kernel(const __grid_constant__ KParams P,
+                                                                   const __grid_constant__ KCache C, const void* x,
+                                                                   int dtype, long long n_tok,
+                                                                   const long long* slot_mapping, int seq_tok,
+                                                                   int n_c, int lut_j) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int head = blockIdx.y;
+  const int bits = P.vb;
+  wq::build_code_lut_n<true>(smem_raw, lut_j, P.vt, P.vc, bits, tid, 32 * VNW);
+  const wq::CodeLut lut = wq::code_lut_at(smem_raw, lut_j);
+  float sig[8];
+  {
+    const float4* sp = reinterpret_cast<const float4*>(P.v_rot + (size_t)head * D) + 2 * lane;
+    const float4 a = __ldg(sp), b = __ldg(sp + 1);
+    sig[0] = a.x, sig[1] = a.y, sig[2] = a.z, sig[3] = a.w, sig[4] = b.x, sig[5] = b.y, sig[6] = b.z, sig[7] = b.w;
+  }
+  __syncthreads();
+  const bool vec = dtype == TQ_BF16 && P.dh == D;  // rows of 512 bytes, 16-byte aligned (checked on the host)
+  const uint4* xq = reinterpret_cast<const uint4*>(x);
+  const long long npp = slot_mapping ? 1 : (n_c + kPage - 1) / kPage;  // pages a sequence
+  const long long n_groups = slot_mapping ? (n_tok + 15) / 16 : (n_c > 0 ? n_tok / n_c : 0) * npp;
+
+  // destination and input row of token i = lane (< 16) of group gi
+  struct Dst {
+    long long pg, off;  // page (-1: none), element offset of the input row
+    int sl;
+  };
+  auto dest = [&](long long gi) -> Dst {
+    long long pg = -1, row = 0;
+    int sl = -1;
+    if (lane < 16 && gi < n_groups) {
+      if (slot_mapping) {
+        const long long t = gi * 16 + lane;
+        if (t < n_tok) {
+          row = t;
+          const long long sm = slot_mapping[t];  // negative: skipped
+          if (sm >= 0) {
+            pg = sm / kPage;
+            sl = (int)(sm % kPage);
+            if (pg >= C.n_pages) {
+              atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+              pg = -1;
+            }
+          }
+        }
+      } else {
+        const long long bq = gi / npp;
+        const int pp = (int)(gi - bq * npp), pos = pp * kPage + lane;
+        if (pos < n_c) {
+          row = bq * seq_tok + pos;
+          if (pp < C.max_pages) {
+            const long long pid = C.block_table[(size_t)bq * C.max_pages + pp];
+            if (pid >= 0 && pid < C.n_pages) {
+              pg = pid;
+              sl = lane;
+            } else {
+              atomicOr(&g_quant_err, TQ_DEVERR_SLOT);
+            }
+          } else {
+            atomicOr(&g_quant_err, TQ_DEVERR_SEQ_LEN);
+          }
+        }
+      }
+    }
+    return Dst{pg, (row * P.hkv + head) * (long long)P.dh, sl};
+  };
+  auto load = [&](const Dst& d, int i) -> uint4 {  // row of token i of d's group (zeros if it has none)
+    const long long oi = __shfl_sync(0xffffffffu, d.off, i);
+    const long long pgi = __shfl_sync(0xffffffffu, d.pg, i);
+    return (vec && pgi >= 0) ? __ldg(xq + oi / 8 + lane) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  const long long gstride = (long long)gridDim.x * VNW;
+  long long gi = (long long)blockIdx.x * VNW + warp;
+  Dst cur = dest(gi);
+  // two tokens a pass; the next pass's rows (past the group's end: the next group's first two)
+  // are in flight meanwhile, and the next group's destinations are read at the group's start
+  uint4 r0 = load(cur, 0), r1 = load(cur, 1);
+  for (; gi < n_groups; gi += gstride) {
+    const Dst nxt = dest(gi + gstride);
+    const long long pg = cur.pg, off = cur.off;
+    const int sl = cur.sl;
+    const unsigned vmask = __ballot_sync(0xffffffffu, lane < 16 && pg >= 0);
+    const long long pg0 = __shfl_sync(0xffffffffu, pg, 0);
+    const bool full = vmask == 0xFFFFu && __all_sync(0xffffffffu, lane >= 16 || (pg == pg0 && sl == lane));
+    uint32_t accA[8], accB[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) accA[e] = accB[e] = 0u;
+    float nrm = 0.f;  // lane i < 16: the norm of token i
+    auto token = [&](int i, const uint4 raw) {
+      if (!((vmask >> i) & 1u)) return;  // warp-uniform
+      float xv[8];
+      if (vec) {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xv[2 * k] = __uint_as_float(w[k] << 16);  // bf16 -> fp32, exact
+          xv[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      } else {
+        const long long oi = __shfl_sync(0xffffffffu, off, i);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] = 8 * lane + e < P.dh ? load_elem(x, dtype, oi + 8 * lane + e) : 0.f;
+      }
+      float sq[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sq[e] = xv[e] * xv[e];
+      const float n = sqrtf(warp_sum_f(tree8(sq)));
+      const bool zero = n < kZeroNorm;
+      const float inv = zero ? 0.f : 1.0f / n;
+      // z = sqrt(d) Pi x / n with Pi = H diag(sigma) / sqrt(d): z = H (sigma x) / n; index bits 3..7
+      // (the lane's) across lanes, bits 0..2 (the register's) in registers
+      float z[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) z[e] = xv[e] * sig[e];
+#pragma unroll
+      for (int h = 1; h < 32; h <<= 1) {
+        const float sg = (lane & h) ? -1.f : 1.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = fmaf(sg, z[e], __shfl_xor_sync(0xffffffffu, z[e], h));
+      }
+#pragma unroll
+      for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if ((e & h) == 0) {
+            const float lo = z[e], hi = z[e + h];
+            z[e] = lo + hi;
+            z[e + h] = lo - hi;
+          }
+      uint32_t q[8];  // spread code: plane p at bit 8 p
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = wq::code_spread(z[e] * inv, lut);
+      if (lane == i) nrm = zero ? 0.f : n;
+      if (full) {
+        const int shv = i & 7;
+        if (i < 8) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) accA[e] |= q[e] << shv;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) accB[e] |= q[e] << shv;
+        }
+        return;
+      }
+      // a group that is not one whole page: this token's bits (slot sli of page pgi), coordinate
+      // pairs 8 lane + 2 k, + 1 in one 32-bit word
+      const long long pgi = __shfl_sync(0xffffffffu, pg, i);
+      const int sli = __shfl_sync(0xffffffffu, sl, i);
+      unsigned char* sb = C.pool + ((size_t)pgi * P.hkv + head) * (size_t)P.sub_bytes;
+      unsigned int* w32 = reinterpret_cast<unsigned int*>(sb + P.off_vcodes) + 4 * lane;
+      const unsigned clear = ~((1u << sli) | (1u << (16 + sli)));
+      for (int p = 0; p < bits; ++p) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const unsigned b2 = (((q[2 * k] >> (8 * p)) & 1u) << sli) | (((q[2 * k + 1] >> (8 * p)) & 1u) << (16 + sli));
+          atomicAnd(w32 + p * (D / 2) + k, clear);
+          atomicOr(w32 + p * (D / 2) + k, b2);
+        }
+      }
+      if (lane == 0) reinterpret_cast<float*>(sb + P.off_vnorm)[sli] = zero ? 0.f : n;
+    };
+#pragma unroll 1
+    for (int i = 0; i < 16; i += 2) {
+      const uint4 c0 = r0, c1 = r1;
+      const Dst& d = i + 2 < 16 ? cur : nxt;
+      const int i2 = (i + 2) & 15;
+      r0 = load(d, i2);
+      r1 = load(d, i2 + 1);
+      token(i, c0);
+      token(i + 1, c1);
+    }
+    if (full) {
+      unsigned char* sb = C.pool + ((size_t)pg0 * P.hkv + head) * (size_t)P.sub_bytes;
+      uint4* dst = reinterpret_cast<uint4*>(sb + P.off_vcodes) + lane;  // coordinates 8 lane .. 8 lane + 7
+      for (int p = 0; p < bits; ++p) {
+        const uint32_t sel = (uint32_t)p | ((uint32_t)(p + 4) << 4);  // byte p of each operand
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t xa = __byte_perm(accA[2 * k], accA[2 * k + 1], sel);
+          const uint32_t xb = __byte_perm(accB[2 * k], accB[2 * k + 1], sel);
+          w[k] = __byte_perm(xa, xb, 0x5140);  // word 2k: tokens 0..7 | 8..15 << 8; word 2k + 1 above
+        }
+        dst[p * (D / 8)] = make_uint4(w[0], w[1], w[2], w[3]);  // plane p: D halfwords, 32 uint4
+      }
+      if (lane < 16) reinterpret_cast<float*>(sb + P.off_vnorm)[lane] = nrm;
+    }
+    cur = nxt;
+  }
 }
 
 }  // namespace q256
