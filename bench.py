@@ -804,7 +804,7 @@ def run_gpu(args):
     T = [T0] * args.layers
     used = [0] * args.layers
 
-    def step(i, k=None, v=None, q=None, dec_ev=None):
+    def step(i, k=None, v=None, q=None, dec_ev=None, o=None):
         l = i % args.layers
         j = used[l]
         used[l] += 1
@@ -814,8 +814,8 @@ def run_gpu(args):
         T[l] += 1
         if dec_ev is not None:
             dec_ev[0].record()
-        tq.decode_attention(layers[l].params, caches[l].cache, qs[l] if q is None else q, scale, out, None, None,
-                            work, max_ctx)
+        tq.decode_attention(layers[l].params, caches[l].cache, qs[l] if q is None else q, scale,
+                            out if o is None else o, None, None, work, max_ctx)
         if dec_ev is not None:
             dec_ev[1].record()
         return step_bytes(T[l], W, B, Hkv, Hq, d, w.key_bits, w.value_bits, rec=recs)
@@ -857,26 +857,57 @@ def run_gpu(args):
         raise RuntimeError("device error during the timed steps")
     ms = max_over_ranks(ms)
     # end to end through the public API with host buffers: H2D of the step's K, V, q
-    # from pinned memory and D2H of the output, inside the timed region
+    # from pinned memory and D2H of the output, inside the timed region.  The copies run on a
+    # stream of their own into double buffers, so step i + 1's inputs and step i's output move
+    # while the compute stream runs (events order every buffer's reuse)
     npool = 16  # pinned host copies of step inputs, used cyclically
     hk = [news[i % args.layers][0][i // args.layers].cpu().pin_memory() for i in range(npool)]
     hv = [news[i % args.layers][1][i // args.layers].cpu().pin_memory() for i in range(npool)]
     hq = [qs[i % args.layers].cpu().pin_memory() for i in range(npool)]
-    hout = torch.empty(B, Hq, d).pin_memory()
-    dk, dv, dq = torch.empty_like(news[0][0][0]), torch.empty_like(news[0][1][0]), torch.empty_like(qs[0])
+    houts = [torch.empty(B, Hq, d).pin_memory() for _ in range(2)]
+    dks = [torch.empty_like(news[0][0][0]) for _ in range(2)]
+    dvs = [torch.empty_like(news[0][1][0]) for _ in range(2)]
+    dqs = [torch.empty_like(qs[0]) for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
+    cs, xs = torch.cuda.current_stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b copied
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b done (its inputs free, its output written)
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # output b copied to the host (free again)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-    e0.record()
+    e0.record(cs)
+    xs.wait_event(e0)
+
+    def h2d(i):
+        b = i % 2
+        with torch.cuda.stream(xs):
+            if i >= 2:
+                xs.wait_event(ev_used[b])  # step i - 2 has read buffer b
+            dks[b].copy_(hk[i % npool], non_blocking=True)
+            dvs[b].copy_(hv[i % npool], non_blocking=True)
+            dqs[b].copy_(hq[i % npool], non_blocking=True)
+            ev_in[b].record(xs)
+
     e2e_bytes = 0
+    if args.steps > 0:
+        h2d(0)
     for i in range(args.steps):
-        dk.copy_(hk[i % npool], non_blocking=True)
-        dv.copy_(hv[i % npool], non_blocking=True)
-        dq.copy_(hq[i % npool], non_blocking=True)
-        e2e_bytes += step(args.warmup + args.steps + i, dk, dv, dq)
-        hout.copy_(out, non_blocking=True)
-    e1.record()
+        b = i % 2
+        if i + 1 < args.steps:
+            h2d(i + 1)
+        cs.wait_event(ev_in[b])
+        if i >= 2:
+            cs.wait_event(ev_out[b])  # the host has step i - 2's output: buffer b may be overwritten
+        e2e_bytes += step(args.warmup + args.steps + i, dks[b], dvs[b], dqs[b], o=outs[b])
+        ev_used[b].record(cs)
+        with torch.cuda.stream(xs):
+            xs.wait_event(ev_used[b])
+            houts[b].copy_(outs[b], non_blocking=True)
+            ev_out[b].record(xs)
+    cs.wait_stream(xs)
+    e1.record(cs)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms)
@@ -924,8 +955,9 @@ def run_gpu(args):
         "prefill": pre,
         "quality": qual,
         "e2e": {"value": e2e_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
-                "d2h_bytes_per_step": int(hout.numel() * 4)},
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (dks[0], dvs[0], dqs[0]))),
+                "d2h_bytes_per_step": int(houts[0].numel() * houts[0].element_size()),
+                "copies": "own stream, double-buffered, overlapping the compute stream"},
         "gpu_launches": args.steps * 5,
         "clocks": clk,
     }
