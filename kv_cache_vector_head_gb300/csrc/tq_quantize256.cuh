@@ -60,9 +60,11 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, const uin
 }
 
 // Halfword index of A-fragment element (token row rr of m-tile mt, coordinate k) in a limb array.
+// The fragment of lane tl sits in slot tl ^ 4 on odd k-steps: a warp storing coordinates 32 e + lane
+// (k-steps 2e and 2e + 1, 512 bytes apart) then writes 32 distinct banks.
 __device__ __forceinline__ int a_index(int mt, int rr, int k) {
   const int ks = k >> 4, kk = k & 15;
-  const int tl = (rr & 7) * 4 + ((kk & 7) >> 1), reg = (rr >> 3) + 2 * (kk >> 3);
+  const int tl = ((rr & 7) * 4 + ((kk & 7) >> 1)) ^ ((ks & 1) << 2), reg = (rr >> 3) + 2 * (kk >> 3);
   return ((((mt * KS + ks) * 32 + tl) * 4 + reg) << 1) + (kk & 1);
 }
 
@@ -321,8 +323,8 @@ __global__ void __launch_bounds__(NT, (KEY && SK == 1) ? 1 : 2) direct256_kernel
           for (int q = 0; q < NTW; ++q) b[q] = sB[((NTW * warp + q) * KS + ks) * 32 + lane];
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            const uint4 a = A4[(m * KS + ks) * 32 + lane];
-            const uint4 al = A4l[(m * KS + ks) * 32 + lane];
+            const uint4 a = A4[(m * KS + ks) * 32 + (lane ^ ((ks & 1) << 2))];  // slot swizzle of a_index
+            const uint4 al = A4l[(m * KS + ks) * 32 + (lane ^ ((ks & 1) << 2))];
 #pragma unroll
             for (int q = 0; q < NTW; ++q) {
               mma_f16(acc[m][q], a, b[q]);
