@@ -423,21 +423,26 @@ def test_empty_sequence_and_device_error(tq):
     assert tq.check_device_error() == 0  # cleared
 
 
+@pytest.mark.parametrize("layout", ["scattered", "pages"])
 @pytest.mark.parametrize("name,over", [("llama", {}), ("long", {}), ("long", dict(qjl_structured=1)),
                                        ("qwen", dict(key_qjl=2, head_dim=160))])
-def test_direct_slot_append_with_skips(tq, name, over):
-    """Direct slots scattered over pages 0..7 with one skipped token; the d = 256 cases run the
-    64-token-tile kernel, whose value planes then take the bitwise path (no page filled in order)."""
+def test_direct_slot_append_with_skips(tq, name, over, layout):
+    """Direct slots with one skipped token: scattered over pages 0..7 (at d = 256 every 16-token value
+    group then takes the bitwise path), or in slot order from page 3 on (the first 16 tokens fill
+    page 3 whole, the next group holds the skipped token, the last fills half of page 5)."""
     w = SK.workload(name, batch=1, ctx=40, **over)
     kv = SK.keys_values(w, ctx=40)
     L, O = _layer(tq, w)
     pc = tq.PagedCache(L, 1, 64, pool_pages=8)
     kt = SK.to_torch(kv["K"][0], w.dtype).cuda()
     vt = SK.to_torch(kv["V"][0], w.dtype).cuda()
-    # scattered slots across pages 5, 2, 7; token 3 skipped (-1)
-    rng = np.random.default_rng(0)
-    slots = rng.permutation(8 * 16)[:40].astype(np.int64)
-    slots[3] = -1
+    if layout == "scattered":  # slots across pages 0..7; token 3 skipped (-1)
+        rng = np.random.default_rng(0)
+        slots = rng.permutation(8 * 16)[:40].astype(np.int64)
+        slots[3] = -1
+    else:
+        slots = 48 + np.arange(40, dtype=np.int64)
+        slots[20] = -1
     st = torch.from_numpy(slots).cuda()
     tq.append_page(L.params, pc.cache, kt, vt, 40, st)
     torch.cuda.synchronize()
