@@ -444,11 +444,13 @@ __global__ void __launch_bounds__(32 * VNW) direct256_values_kernel(const __grid
   const int bits = P.vb;
   wq::build_code_lut_n<true>(smem_raw, lut_j, P.vt, P.vc, bits, tid, 32 * VNW);
   const wq::CodeLut lut = wq::code_lut_at(smem_raw, lut_j);
-  float sig[8];
+  uint32_t sgm[8];  // sign bit of sigma_j (+-1) for the lane's coordinates 8 lane + e
   {
-    const float4* sp = reinterpret_cast<const float4*>(P.v_rot + (size_t)head * D) + 2 * lane;
-    const float4 a = __ldg(sp), b = __ldg(sp + 1);
-    sig[0] = a.x, sig[1] = a.y, sig[2] = a.z, sig[3] = a.w, sig[4] = b.x, sig[5] = b.y, sig[6] = b.z, sig[7] = b.w;
+    const uint4* sp = reinterpret_cast<const uint4*>(P.v_rot + (size_t)head * D) + 2 * lane;
+    const uint4 a = __ldg(sp), b = __ldg(sp + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sgm[e] = w[e] & 0x80000000u;
   }
   __syncthreads();
   const bool vec = dtype == TQ_BF16 && P.dh == D;  // rows of 512 bytes, 16-byte aligned (checked on the host)
@@ -508,9 +510,9 @@ __global__ void __launch_bounds__(32 * VNW) direct256_values_kernel(const __grid
   const long long gstride = (long long)gridDim.x * VNW;
   long long gi = (long long)blockIdx.x * VNW + warp;
   Dst cur = dest(gi);
-  // two tokens a pass; the next pass's rows (past the group's end: the next group's first two)
-  // are in flight meanwhile, and the next group's destinations are read at the group's start
-  uint4 r0 = load(cur, 0), r1 = load(cur, 1);
+  // two tokens a pass; the rows of the next two passes (past the group's end: the next group's
+  // first ones) are in flight meanwhile, and the next group's destinations are read at its start
+  uint4 r0 = load(cur, 0), r1 = load(cur, 1), r2 = load(cur, 2), r3 = load(cur, 3);
   for (; gi < n_groups; gi += gstride) {
     const Dst nxt = dest(gi + gstride);
     const long long pg = cur.pg, off = cur.off;
@@ -524,30 +526,32 @@ __global__ void __launch_bounds__(32 * VNW) direct256_values_kernel(const __grid
     float nrm = 0.f;  // lane i < 16: the norm of token i
     auto token = [&](int i, const uint4 raw) {
       if (!((vmask >> i) & 1u)) return;  // warp-uniform
-      float xv[8];
+      // sigma x (sigma = +-1): bf16 rows exactly, the sign flip as an XOR of the sign bit
+      float z[8];
       if (vec) {
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          xv[2 * k] = __uint_as_float(w[k] << 16);  // bf16 -> fp32, exact
-          xv[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          z[2 * k] = __uint_as_float((w[k] << 16) ^ sgm[2 * k]);
+          z[2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ sgm[2 * k + 1]);
         }
       } else {
         const long long oi = __shfl_sync(0xffffffffu, off, i);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xv[e] = 8 * lane + e < P.dh ? load_elem(x, dtype, oi + 8 * lane + e) : 0.f;
+        for (int e = 0; e < 8; ++e)
+          z[e] = __uint_as_float(__float_as_uint(8 * lane + e < P.dh ? load_elem(x, dtype, oi + 8 * lane + e) : 0.f) ^
+                                 sgm[e]);
       }
       float sq[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sq[e] = xv[e] * xv[e];
-      const float n = sqrtf(warp_sum_f(tree8(sq)));
+      for (int e = 0; e < 8; ++e) sq[e] = z[e] * z[e];
+      const float ss = warp_sum_f(tree8(sq));
+      const float n = sqrtf(ss);
       const bool zero = n < kZeroNorm;
-      const float inv = zero ? 0.f : 1.0f / n;
+      // 1 / n within two ulp (the codes compare z to the boundaries; their exemption band is far wider)
+      const float inv = zero ? 0.f : rsqrtf(ss);
       // z = sqrt(d) Pi x / n with Pi = H diag(sigma) / sqrt(d): z = H (sigma x) / n; index bits 3..7
       // (the lane's) across lanes, bits 0..2 (the register's) in registers
-      float z[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) z[e] = xv[e] * sig[e];
 #pragma unroll
       for (int h = 1; h < 32; h <<= 1) {
         const float sg = (lane & h) ? -1.f : 1.f;
@@ -598,10 +602,12 @@ __global__ void __launch_bounds__(32 * VNW) direct256_values_kernel(const __grid
 #pragma unroll 1
     for (int i = 0; i < 16; i += 2) {
       const uint4 c0 = r0, c1 = r1;
-      const Dst& d = i + 2 < 16 ? cur : nxt;
-      const int i2 = (i + 2) & 15;
-      r0 = load(d, i2);
-      r1 = load(d, i2 + 1);
+      r0 = r2;
+      r1 = r3;
+      const Dst& d = i + 4 < 16 ? cur : nxt;
+      const int i4 = (i + 4) & 15;
+      r2 = load(d, i4);
+      r3 = load(d, i4 + 1);
       token(i, c0);
       token(i + 1, c1);
     }
