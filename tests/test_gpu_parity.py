@@ -264,6 +264,9 @@ PAGED = [
     # d = 256 without a window: prefill ends in a partly filled page (64-token tiles, bitwise value planes)
     ("long", dict(batch=3), 37, 12),
     ("long", dict(batch=2, key_qjl=0, key_bits=3, value_bits=1), 70, 9),
+    # d = 256 with float32 and float16 inputs (the prefill kernels' element loads, the one-vector append)
+    ("long", dict(batch=2, dtype="f32"), 37, 6),
+    ("qwen", dict(batch=1, window=20, dtype="f16"), 45, 20),
     # the structured sketch
     ("qwen", dict(batch=2, window=20, qjl_structured=1), 75, 30),
     ("llama", dict(batch=5, kind=SK.FWHT, qjl_structured=1), 29, 21),
