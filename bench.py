@@ -95,6 +95,14 @@ def record_bytes(d, kb, qjl, vb, split=0, norm_u8=False):
     return key, 4 + vb * d // 8
 
 
+def launches_per_step(w) -> int:
+    """Kernels one timed step launches: the append (d = 128 bf16 without a window: the key and value warp-tile
+    kernels, else one step kernel) and the counters, then the decode call (query transform, page kernel and
+    merge; the KIVI arm has no query transform)."""
+    append = 2 if (w.window == 0 and w.d == 128 and w.dtype == "bf16" and not w.kivi) else 1
+    return append + 1 + (2 if w.kivi else 3)
+
+
 def workload_records(w):
     if w.kivi:  # key scale and zero per channel shared by a page's 16 tokens; value scale and zero per token
         return w.d // 4 + w.key_bits * w.d // 8, 4 + w.value_bits * w.d // 8
@@ -958,7 +966,7 @@ def run_gpu(args):
                 "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (dks[0], dvs[0], dqs[0]))),
                 "d2h_bytes_per_step": int(houts[0].numel() * houts[0].element_size()),
                 "copies": "own stream, double-buffered, overlapping the compute stream"},
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clk,
     }
     if ws == 1 and not args.no_cpu_baseline:

@@ -101,3 +101,14 @@ def test_quantize_roofline_bounds():
     assert f["flops_per_token_head"] == 2 * 128 ** 2 + 2 * 2 * 128 * 7
     s = bench.quantize_roofline(1.0, n, 1, peaks, structured=True)
     assert s["flops_per_token_head"] == 3 * 2 * 128 * 7
+
+
+def test_launch_count_follows_the_workload():
+    """Kernels a timed step launches: append kernel(s), counters, then the decode call."""
+    import synthetic_kv as SK
+
+    assert bench.launches_per_step(SK.workload("qwen")) == 5    # step kernel, counters, 3 decode kernels
+    assert bench.launches_per_step(SK.workload("long")) == 5
+    assert bench.launches_per_step(SK.workload("mixed")) == 5
+    assert bench.launches_per_step(SK.workload("llama")) == 6   # key and value warp tiles, counters, 3
+    assert bench.launches_per_step(SK.workload("kivi")) == 4    # step kernel, counters, page kernel, merge
